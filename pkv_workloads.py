@@ -1,0 +1,188 @@
+"""Seeded synthetic workloads for the paged-KV decode step.
+
+This module only draws random numbers and lays out shapes; it holds none of the
+method's arithmetic (no slot or block-table computation, no attention, no
+quantisation). Both the CUDA path's tests and benchmarks and the CPU oracle
+take their inputs from here, and from nowhere else they share.
+
+The workloads stand in for the serving traces the pages measure on (ShareGPT,
+Alpaca), which are not used: lengths, head shapes and sharing structure follow
+the stated recipes, values are N(0, 1).
+
+A workload is described by
+* shapes: ``B`` sequences, ``Hq`` query heads, ``Hkv`` KV heads, ``D`` head dim,
+  ``bs`` block size, ``NB`` pool blocks;
+* ``free_order``: the initial free list (a seeded permutation of the block ids);
+* ``script``: block-manager operations that build the cache state before the
+  measured step (``("add", sid)``, ``("append", sid, n)``, ``("fork", p, c)``);
+* ``step_seqs``: the sequences that append one token in the measured step;
+* value tensors, drawn on demand: the past K/V contents of every pool slot
+  (``past_pools``), and the step's ``q``, ``k_new``, ``v_new``;
+* FP8 scales for the E4M3 variant: ``amax|source| / 448`` per tensor.
+"""
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+E4M3_MAX = 448.0
+_CHUNK_ELEMS = 1 << 26
+
+
+@dataclass
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    bs: int
+    NB: int
+    seed: int
+    scale: float
+    src_dtype: torch.dtype            # dtype of q, k_new, v_new and of the pools' source values
+    kv_dtype: str                     # "f32", "bf16" or "e4m3"
+    free_order: np.ndarray
+    script: list
+    step_seqs: list
+    final_lens: np.ndarray            # length of each sequence after the step (incl. the new token)
+    notes: dict = field(default_factory=dict)
+
+    # ---- value tensors --------------------------------------------------
+    def _randn(self, shape, tag):
+        g = torch.Generator().manual_seed(self.seed * 7919 + tag)
+        numel = math.prod(shape)
+        out = torch.empty(numel, dtype=self.src_dtype)
+        for s in range(0, numel, _CHUNK_ELEMS):
+            e = min(numel, s + _CHUNK_ELEMS)
+            out[s:e] = torch.randn(e - s, generator=g, dtype=torch.float32).to(self.src_dtype)
+        return out.view(*shape)
+
+    def past_pools(self):
+        """Source values of every pool slot, ``[NB, Hkv, bs, D]`` in ``src_dtype``.
+
+        For bf16/f32 caches this is the cache content; for the E4M3 cache it is
+        what gets quantised into it.
+        """
+        shape = (self.NB, self.Hkv, self.bs, self.D)
+        return self._randn(shape, 1), self._randn(shape, 2)
+
+    def step_inputs(self):
+        """``q [B, Hq, D]``, ``k_new [B, Hkv, D]``, ``v_new [B, Hkv, D]`` for the step."""
+        q = self._randn((self.B, self.Hq, self.D), 3)
+        k = self._randn((self.B, self.Hkv, self.D), 4)
+        v = self._randn((self.B, self.Hkv, self.D), 5)
+        return q, k, v
+
+    def fp8_scales(self, k_src, v_src, k_new, v_new):
+        """Per-tensor scales ``amax|x| / 448`` over the pool sources and new tokens."""
+        ks = max(k_src.abs().max().item(), k_new.abs().max().item()) / E4M3_MAX
+        vs = max(v_src.abs().max().item(), v_new.abs().max().item()) / E4M3_MAX
+        return float(ks), float(vs)
+
+    @property
+    def max_blocks_per_seq(self):
+        return int(-(-int(self.final_lens.max()) // self.bs))
+
+
+def _pool_size(total_blocks):
+    return int(math.ceil(1.1 * total_blocks))
+
+
+def _prefill_workload(name, seed, lens, Hq, Hkv, D, bs, src_dtype, kv_dtype, scale, NB=None):
+    """Sequences 0..B-1, each with ``len - 1`` past tokens and one step token."""
+    rng = np.random.default_rng(seed)
+    lens = np.asarray(lens, dtype=np.int64)
+    if NB is None:
+        NB = _pool_size(int(sum(-(-int(L) // bs) for L in lens)))
+    free_order = rng.permutation(NB)
+    script = []
+    for b, L in enumerate(lens):
+        script.append(("add", b))
+        if L > 1:
+            script.append(("append", b, int(L) - 1))
+    return Workload(name=name, B=len(lens), Hq=Hq, Hkv=Hkv, D=D, bs=bs, NB=NB, seed=seed,
+                    scale=scale, src_dtype=src_dtype, kv_dtype=kv_dtype,
+                    free_order=free_order, script=script, step_seqs=list(range(len(lens))),
+                    final_lens=lens)
+
+
+def tiny_fp32():
+    """4 sequences of lengths {1, 17, 40, 100}, 4 heads (MHA), D 64, bs 16, 64 blocks."""
+    return _prefill_workload("tiny_fp32", 0, [1, 17, 40, 100], 4, 4, 64, 16,
+                             torch.float32, "f32", 1.0 / 8.0, NB=64)
+
+
+def llama13b_mha_bf16(B=64):
+    """LLaMA-13B-shaped layer: 40 heads MHA, D 128, bs 16, lengths U[128, 2048]."""
+    rng = np.random.default_rng(1)
+    lens = rng.integers(128, 2048, size=B, endpoint=True)
+    w = _prefill_workload("llama13b_mha_bf16", 1, lens, 40, 40, 128, 16,
+                          torch.bfloat16, "bf16", 1.0 / math.sqrt(128))
+    return w
+
+
+def gqa_chat_bf16(B=256):
+    """GQA 32 query / 8 KV heads, D 128, bs 16, lengths lognormal(median 400, sigma 1)
+    rounded and clipped to [16, 4096]."""
+    rng = np.random.default_rng(2)
+    lens = np.clip(np.round(400.0 * np.exp(rng.standard_normal(B))), 16, 4096).astype(np.int64)
+    return _prefill_workload("gqa_chat_bf16", 2, lens, 32, 8, 128, 16,
+                             torch.bfloat16, "bf16", 1.0 / math.sqrt(128))
+
+
+def shared_prefix_bf16(fork_step=False, groups=64, per_group=4, prompt=520, max_suffix=256):
+    """Parallel sampling: ``groups`` prompts of ``prompt`` tokens, each forked into
+    ``per_group`` sequences (40 heads MHA, D 128, bs 16).
+
+    ``fork_step=True``: every sequence is still at the prompt length, so the step's
+    first append into the shared partial block is the copy-on-write step.
+    Otherwise each sequence first grows by a suffix ~ U[0, max_suffix] (untimed).
+    """
+    seed = 3
+    rng = np.random.default_rng(seed)
+    bs, Hq, D = 16, 40, 128
+    n = groups * per_group
+    suffix = np.zeros(n, dtype=np.int64) if fork_step else rng.integers(0, max_suffix, size=n, endpoint=True)
+    # pool: every prompt's blocks plus, per sequence, enough blocks for its own tail
+    # (the partial prompt block, its suffix and the step token), plus 10%
+    per_prompt = -(-prompt // bs)
+    own = sum(-(-(prompt % bs + int(s) + 1) // bs) for s in suffix)
+    NB = _pool_size(groups * per_prompt + own)
+    free_order = rng.permutation(NB)
+    script = []
+    for g in range(groups):
+        parent = g * per_group
+        script.append(("add", parent))
+        script.append(("append", parent, prompt))
+        for c in range(1, per_group):
+            script.append(("fork", parent, parent + c))
+    if not fork_step:
+        for sid in range(n):
+            if suffix[sid]:
+                script.append(("append", sid, int(suffix[sid])))
+    lens = prompt + suffix + 1
+    name = "shared_prefix_fork_bf16" if fork_step else "shared_prefix_bf16"
+    return Workload(name=name, B=n, Hq=Hq, Hkv=Hq, D=D, bs=bs, NB=NB, seed=seed,
+                    scale=1.0 / math.sqrt(128), src_dtype=torch.bfloat16, kv_dtype="bf16",
+                    free_order=free_order, script=script, step_seqs=list(range(n)),
+                    final_lens=lens, notes={"groups": groups, "per_group": per_group,
+                                            "prompt": prompt})
+
+
+def long_fp8(bs=16, B=16, L=32768):
+    """Long context with an E4M3 cache: B sequences of L tokens, GQA 32/8, D 128."""
+    return _prefill_workload(f"long_fp8_bs{bs}", 4, [L] * B, 32, 8, 128, bs,
+                             torch.bfloat16, "e4m3", 1.0 / math.sqrt(128))
+
+
+CONFIGS = {
+    "tiny_fp32": tiny_fp32,
+    "llama13b_mha_bf16": llama13b_mha_bf16,
+    "gqa_chat_bf16": gqa_chat_bf16,
+    "shared_prefix_bf16": shared_prefix_bf16,
+    "shared_prefix_fork_bf16": lambda: shared_prefix_bf16(fork_step=True),
+    "long_fp8_bs16": lambda: long_fp8(16),
+    "long_fp8_bs32": lambda: long_fp8(32),
+}

@@ -1,0 +1,423 @@
+"""Pins of the CPU oracle to facts outside itself (no GPU needed).
+
+Each test checks the oracle against something it does not compute itself: the
+worked example of the glossary page "PagedAttention" and its printed result,
+a library implementation of attention on contiguous K/V (torch's
+scaled_dot_product_attention in float64), closed forms, brute force over every
+block table of a tiny pool, torch's own float8_e4m3fn conversion, and the
+reference-count / copy-on-write invariants the pages state.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import attention as oatt
+from oracle import cache_ops as oops
+from oracle import fp8_e4m3 as ofp8
+from oracle.block_manager import BlockManager, PoolExhausted
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *rest = line.split()
+            vals[key] = [int(x) for x in rest]
+    return vals
+
+
+# ---------------------------------------------------------------- worked example
+def test_snippet_replay():
+    """The glossary's 40-token example: table [41, 7, 19], keys intact, 8 vs 2,008."""
+    g = read_golden("snippet_40_tokens.txt")
+    bs, d, nb, n = g["block_size"][0], g["head_dim"][0], g["pool_blocks"][0], g["tokens"][0]
+    bm = BlockManager(nb, bs, g["free_blocks"])
+    bm.add_seq(0)
+    slots = [bm.append_slot(0)[0] for _ in range(n)]
+    table = bm.block_table(0)
+    assert table == g["expected_block_table"]
+    assert bm.num_free() == len(g["free_blocks"]) - len(table)
+
+    keys = torch.randn(n, d, generator=torch.Generator().manual_seed(0))
+    pool = torch.zeros(nb, 1, bs, d)
+    vpool = torch.zeros(nb, 1, bs, d)
+    oops.reshape_and_cache(keys[:, None, :], keys[:, None, :], pool, vpool,
+                           torch.tensor(slots), bs)
+    # the example's layout, read off directly: consecutive 16-token chunks of the
+    # request sit in blocks 41, 7 and 19, in order
+    assert torch.equal(pool[41, 0], keys[0:16])
+    assert torch.equal(pool[7, 0], keys[16:32])
+    assert torch.equal(pool[19, 0, :8], keys[32:40])
+    assert torch.count_nonzero(pool[19, 0, 8:]) == 0
+    gathered = oatt.gather(pool, table, n, 0, bs)
+    assert torch.equal(gathered, keys) == bool(g["expected_keys_intact"][0])
+    assert len(table) * bs - n == g["expected_unused_slots"][0]
+    assert g["reservation_tokens"][0] - n == g["expected_unused_reserved"][0]
+
+
+# ---------------------------------------------------------------- helpers
+def scatter_blockwise(Kc, table, pool, bs):
+    """Place contiguous rows ``Kc [L, Hkv, D]`` into ``pool`` chunk by chunk:
+    chunk j (rows j*bs .. j*bs+bs-1) goes to physical block table[j]."""
+    L = Kc.shape[0]
+    for j in range(-(-L // bs)):
+        rows = Kc[j * bs:(j + 1) * bs]
+        pool[table[j], :, :rows.shape[0], :] = rows.transpose(0, 1)
+
+
+def sdpa_reference(q, Kc, Vc, scale):
+    """torch SDPA in float64 on contiguous K/V; query head h uses KV head h // G."""
+    Hq, D = q.shape
+    L, Hkv, _ = Kc.shape
+    G = Hq // Hkv
+    if L == 0:
+        return torch.zeros(Hq, D, dtype=torch.float64)
+    K = Kc.to(torch.float64).transpose(0, 1).repeat_interleave(G, dim=0)  # [Hq, L, D]
+    V = Vc.to(torch.float64).transpose(0, 1).repeat_interleave(G, dim=0)
+    o = F.scaled_dot_product_attention(q.to(torch.float64)[:, None, :], K, V, scale=scale)
+    return o[:, 0, :]
+
+
+def random_case(seed, lens, Hq, Hkv, D, bs, extra_blocks=5, dtype=torch.float32):
+    g = torch.Generator().manual_seed(seed)
+    rng = np.random.default_rng(seed)
+    need = sum(-(-L // bs) for L in lens)
+    NB = need + extra_blocks
+    perm = rng.permutation(NB)
+    MB = max(1, max(-(-L // bs) for L in lens))
+    tables = np.full((len(lens), MB), -1, dtype=np.int64)
+    kpool = torch.randn(NB, Hkv, bs, D, generator=g).to(dtype)
+    vpool = torch.randn(NB, Hkv, bs, D, generator=g).to(dtype)
+    conts = []
+    pos = 0
+    for b, L in enumerate(lens):
+        nb = -(-L // bs)
+        tables[b, :nb] = perm[pos:pos + nb]
+        pos += nb
+        Kc = torch.randn(L, Hkv, D, generator=g).to(dtype)
+        Vc = torch.randn(L, Hkv, D, generator=g).to(dtype)
+        scatter_blockwise(Kc, tables[b], kpool, bs)
+        scatter_blockwise(Vc, tables[b], vpool, bs)
+        conts.append((Kc, Vc))
+    q = torch.randn(len(lens), Hq, D, generator=g).to(dtype)
+    return q, kpool, vpool, tables, np.array(lens), conts
+
+
+# ---------------------------------------------------------------- paged == contiguous
+@pytest.mark.parametrize("Hq,Hkv,D,bs", [(4, 4, 64, 16), (8, 2, 32, 4), (6, 3, 16, 1),
+                                          (8, 1, 64, 32), (4, 4, 128, 2)])
+def test_paged_equals_contiguous_sdpa(Hq, Hkv, D, bs):
+    lens = [1, 2, bs - 1 if bs > 1 else 3, bs, bs + 1, 3 * bs + 5, 0, 57]
+    q, kp, vp, tables, sl, conts = random_case(Hq * 100 + D + bs, lens, Hq, Hkv, D, bs)
+    scale = 1.0 / math.sqrt(D)
+    out = oatt.paged_decode(q, kp, vp, tables, sl, scale, bs)
+    for b, (Kc, Vc) in enumerate(conts):
+        ref = sdpa_reference(q[b], Kc, Vc, scale).numpy()
+        np.testing.assert_allclose(out[b], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_paged_equals_contiguous_bf16_values():
+    q, kp, vp, tables, sl, conts = random_case(7, [40, 100, 17], 8, 2, 128, 16,
+                                               dtype=torch.bfloat16)
+    out = oatt.paged_decode(q, kp, vp, tables, sl, 0.125, 16)
+    for b, (Kc, Vc) in enumerate(conts):
+        np.testing.assert_allclose(out[b], sdpa_reference(q[b], Kc, Vc, 0.125).numpy(),
+                                   rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- closed forms
+def test_single_token_returns_its_value():
+    q, kp, vp, tables, sl, conts = random_case(3, [1, 1], 4, 2, 64, 16)
+    out = oatt.paged_decode(q, kp, vp, tables, sl, 0.3, 16, v_scale=1.0)
+    for b, (Kc, Vc) in enumerate(conts):
+        for h in range(4):
+            assert np.array_equal(out[b, h], Vc[0, h // 2].double().numpy())
+
+
+def test_zero_query_and_equal_keys_give_mean_of_values():
+    q, kp, vp, tables, sl, conts = random_case(4, [37, 16], 2, 2, 32, 8)
+    zero_q = torch.zeros_like(q)
+    out = oatt.paged_decode(zero_q, kp, vp, tables, sl, 1.0, 8)
+    for b, (Kc, Vc) in enumerate(conts):
+        np.testing.assert_allclose(out[b], Vc.double().mean(0).numpy(), rtol=0, atol=1e-14)
+    # all keys equal: scores equal, uniform weights, whatever q is
+    K_eq = torch.randn(1, 2, 32).expand(37, 2, 32).contiguous()
+    table = list(range(5))
+    kpool = torch.zeros(5, 2, 8, 32)
+    scatter_blockwise(K_eq, table, kpool, 8)
+    Vc = conts[0][1]
+    vpool = torch.zeros(5, 2, 8, 32)
+    scatter_blockwise(Vc, table, vpool, 8)
+    out = oatt.paged_decode(q[:1], kpool, vpool, [table], [37], 0.7, 8)
+    np.testing.assert_allclose(out[0], Vc.double().mean(0).numpy(), rtol=0, atol=1e-14)
+
+
+def test_two_tokens_logistic_weight():
+    """Two tokens: out = sigma(s0 - s1) v0 + sigma(s1 - s0) v1."""
+    D = 8
+    k = np.array([[0.5] * D, [-0.25] * D])
+    v = np.array([[1.0] * D, [3.0] * D])
+    qv = np.linspace(-1, 1, D)
+    qv = qv + 0.3
+    s = 0.5 * (k @ qv)
+    w0 = 1.0 / (1.0 + math.exp(s[1] - s[0]))
+    out = oatt.decode_one(qv, k, v, 0.5)
+    np.testing.assert_allclose(out, w0 * v[0] + (1 - w0) * v[1], rtol=1e-15)
+
+
+def test_scales_fold_linearly():
+    """k_scale multiplies the logits, v_scale the output (value = code * scale)."""
+    q, kp, vp, tables, sl, conts = random_case(11, [23], 2, 2, 16, 4)
+    a = oatt.paged_decode(q, kp * 2.0, vp * 4.0, tables, sl, 0.25, 4)
+    b = oatt.paged_decode(q, kp, vp, tables, sl, 0.25, 4, k_scale=2.0, v_scale=4.0)
+    np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- brute force
+def test_every_block_table_of_a_tiny_pool_gives_the_same_result():
+    """Pool of 4 blocks of 2 slots, 3-token sequence: all 12 ordered choices of 2
+    distinct blocks hold the same contiguous K/V and must give identical output,
+    equal to SDPA on the contiguous rows."""
+    g = torch.Generator().manual_seed(5)
+    Kc = torch.randn(3, 1, 4, generator=g)
+    Vc = torch.randn(3, 1, 4, generator=g)
+    q = torch.randn(1, 2, 4, generator=g)
+    ref = sdpa_reference(q[0], Kc, Vc, 0.5).numpy()
+    outs = []
+    for a in range(4):
+        for b in range(4):
+            if a == b:
+                continue
+            kp = torch.randn(4, 1, 2, 4, generator=g)   # junk everywhere else
+            vp = torch.randn(4, 1, 2, 4, generator=g)
+            scatter_blockwise(Kc, [a, b], kp, 2)
+            scatter_blockwise(Vc, [a, b], vp, 2)
+            outs.append(oatt.paged_decode(q, kp, vp, [[a, b]], [3], 0.5, 2))
+    assert len(outs) == 12
+    for o in outs:
+        assert np.array_equal(o, outs[0])
+    np.testing.assert_allclose(outs[0][0], ref, rtol=1e-13, atol=1e-14)
+
+
+def test_relabelling_physical_blocks_changes_nothing():
+    q, kp, vp, tables, sl, conts = random_case(9, [50, 3, 31], 4, 4, 32, 8)
+    NB = kp.shape[0]
+    perm = np.random.default_rng(1).permutation(NB)        # new id of old block i
+    kp2 = torch.empty_like(kp)
+    vp2 = torch.empty_like(vp)
+    kp2[torch.from_numpy(perm)] = kp
+    vp2[torch.from_numpy(perm)] = vp
+    t2 = np.where(tables >= 0, perm[np.maximum(tables, 0)], -1)
+    a = oatt.paged_decode(q, kp, vp, tables, sl, 0.2, 8)
+    b = oatt.paged_decode(q, kp2, vp2, t2, sl, 0.2, 8)
+    assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- FP8 E4M3
+def test_e4m3_decode_all_codes_match_torch_and_spec_anchors():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = ofp8.e4m3_decode(codes)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(lib))
+    ok = ~np.isnan(lib)
+    assert np.array_equal(mine[ok], lib[ok])
+    assert np.isnan(mine[0x7F]) and np.isnan(mine[0xFF]) and np.isnan(mine).sum() == 2
+    assert mine[0x7E] == 448.0 and mine[0xFE] == -448.0
+    assert mine[0x01] == 2.0 ** -9 and mine[0x08] == 2.0 ** -6 and mine[0x07] == 7 * 2.0 ** -9
+    assert mine[0x38] == 1.0 and mine[0x00] == 0.0 and math.copysign(1, mine[0x80]) < 0
+
+
+def test_e4m3_encode_roundtrip_ties_and_saturation():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = ofp8.e4m3_decode(codes).astype(np.float32)
+    assert np.array_equal(ofp8.e4m3_encode(vals), codes)
+    # every midpoint between neighbouring magnitudes rounds to the even code
+    mags = ofp8.e4m3_decode(np.arange(127, dtype=np.uint8))
+    mids = ((mags[:-1] + mags[1:]) / 2).astype(np.float32)
+    assert np.array_equal(mids.astype(np.float64), (mags[:-1] + mags[1:]) / 2)  # exact
+    got = ofp8.e4m3_encode(mids).astype(np.int64)
+    lo = np.arange(126)
+    assert np.array_equal(got, np.where(lo % 2 == 0, lo, lo + 1))
+    # just off the midpoint goes to the nearer one
+    up = np.nextafter(mids, np.float32(np.inf))
+    dn = np.nextafter(mids, np.float32(-np.inf))
+    assert np.array_equal(ofp8.e4m3_encode(up).astype(np.int64), lo + 1)
+    assert np.array_equal(ofp8.e4m3_encode(dn).astype(np.int64), lo)
+    # saturation (satfinite): 448 and beyond stay 448
+    big = np.array([448.0, 449.0, 463.9, 464.0, 1e6, 3e38, -500.0], dtype=np.float32)
+    assert list(ofp8.e4m3_encode(big)) == [0x7E] * 6 + [0xFE]
+    # negative values rounding to zero keep their sign
+    assert list(ofp8.e4m3_encode(np.array([-1e-9, 1e-9, -0.0, 0.0], np.float32))) == \
+        [0x80, 0x00, 0x80, 0x00]
+
+
+def test_e4m3_encode_matches_torch_rne_cast_below_overflow():
+    g = torch.Generator().manual_seed(0)
+    x = torch.cat([torch.randn(200000, generator=g) * s for s in (1e-3, 0.05, 1, 30, 150)])
+    x = x.clamp(-463.0, 463.0)
+    lib = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ofp8.e4m3_encode(x.numpy()), lib)
+
+
+def test_e4m3_quantize_divides_in_float32():
+    x = np.array([1.0, -3.0, 0.1], dtype=np.float32)
+    s = 0.0123
+    q = (x / np.float32(s)).astype(np.float32)
+    assert np.array_equal(ofp8.e4m3_quantize(x, s), ofp8.e4m3_encode(q))
+    lib = torch.from_numpy(q).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ofp8.e4m3_quantize(x, s), lib)
+
+
+def test_fp8_paged_attention_equals_sdpa_on_library_dequantised_values():
+    q, kp, vp, tables, sl, conts = random_case(13, [40, 77], 8, 2, 64, 16)
+    ks, vs = 4.5 / 448, 4.2 / 448
+    kq = torch.from_numpy(ofp8.e4m3_quantize(kp.numpy(), ks))
+    vq = torch.from_numpy(ofp8.e4m3_quantize(vp.numpy(), vs))
+    out = oatt.paged_decode(q, kq, vq, tables, sl, 0.125, 16, k_scale=ks, v_scale=vs)
+    kd = kq.view(torch.float8_e4m3fn).to(torch.float64) * ks
+    vd = vq.view(torch.float8_e4m3fn).to(torch.float64) * vs
+    for b in range(2):
+        L = int(sl[b])
+        nbk = -(-L // 16)
+        Kc = torch.cat([kd[tables[b][j]].transpose(0, 1) for j in range(nbk)])[:L]
+        Vc = torch.cat([vd[tables[b][j]].transpose(0, 1) for j in range(nbk)])[:L]
+        np.testing.assert_allclose(out[b], sdpa_reference(q[b], Kc, Vc, 0.125).numpy(),
+                                   rtol=1e-12, atol=1e-12)
+
+
+def test_reshape_and_cache_fp8_bytes_match_torch_cast():
+    g = torch.Generator().manual_seed(2)
+    k = torch.randn(5, 2, 32, generator=g).to(torch.bfloat16)
+    v = torch.randn(5, 2, 32, generator=g).to(torch.bfloat16)
+    kp = torch.zeros(4, 2, 4, 32, dtype=torch.uint8)
+    vp = torch.zeros(4, 2, 4, 32, dtype=torch.uint8)
+    slots = torch.tensor([3, 9, -1, 14, 0])
+    ks, vs = 0.01, 0.02
+    oops.reshape_and_cache(k, v, kp, vp, slots, 4, ks, vs)
+    for i, s in enumerate(slots.tolist()):
+        if s < 0:
+            continue
+        ref = (k[i].float() / ks).to(torch.float8_e4m3fn).view(torch.uint8)
+        assert torch.equal(kp[s // 4, :, s % 4], ref)
+        ref = (v[i].float() / vs).to(torch.float8_e4m3fn).view(torch.uint8)
+        assert torch.equal(vp[s // 4, :, s % 4], ref)
+    # the padding token (slot -1) wrote nothing: only the 4 real slots are set
+    written = (kp.permute(0, 2, 1, 3).reshape(16, -1) != 0).any(1)
+    assert sorted(torch.nonzero(written).flatten().tolist()) == [0, 3, 9, 14]
+
+
+# ---------------------------------------------------------------- cache ops
+def test_copy_blocks_copies_whole_blocks_only():
+    g = torch.Generator().manual_seed(1)
+    kp = torch.randn(6, 2, 4, 8, generator=g).to(torch.bfloat16)
+    vp = torch.randn(6, 2, 4, 8, generator=g).to(torch.bfloat16)
+    k0, v0 = kp.clone(), vp.clone()
+    oops.copy_blocks(kp, vp, [(1, 4), (2, 5)])
+    assert torch.equal(kp[4], k0[1]) and torch.equal(vp[5], v0[2])
+    for i in (0, 1, 2, 3):
+        assert torch.equal(kp[i], k0[i]) and torch.equal(vp[i], v0[i])
+    with pytest.raises(IndexError):
+        oops.copy_blocks(kp, vp, [(0, 6)])
+
+
+def test_reshape_and_cache_rejects_slot_outside_pool():
+    kp = torch.zeros(2, 1, 4, 8)
+    with pytest.raises(IndexError):
+        oops.reshape_and_cache(torch.ones(1, 1, 8), torch.ones(1, 1, 8), kp, kp.clone(),
+                               torch.tensor([8]), 4)
+
+
+# ---------------------------------------------------------------- block manager
+def check_invariants(bm):
+    used = {b for b in range(bm.num_blocks) if bm.ref[b] > 0}
+    free = set(bm.free)
+    assert len(free) == len(bm.free)                       # no duplicates
+    assert not (used & free)
+    assert all(r >= 0 for r in bm.ref)
+    assert sum(bm.ref) == sum(len(t) for t in bm.tables.values())
+    for sid, t in bm.tables.items():
+        L = bm.lens[sid]
+        assert len(t) == -(-L // bm.block_size)
+        assert len(t) * bm.block_size - L < bm.block_size   # waste below one block
+
+
+def test_block_manager_random_ops_keep_invariants():
+    rng = np.random.default_rng(123)
+    for trial in range(20):
+        nb, bs = int(rng.integers(8, 64)), int(rng.choice([1, 2, 4, 16]))
+        bm = BlockManager(nb, bs, rng.permutation(nb))
+        all_ids = set(range(nb))
+        next_id = 0
+        for _ in range(400):
+            op = rng.integers(0, 10)
+            live = list(bm.tables)
+            try:
+                if op == 0 or not live:
+                    bm.add_seq(next_id)
+                    next_id += 1
+                elif op == 1:
+                    bm.fork(int(rng.choice(live)), next_id)
+                    next_id += 1
+                elif op == 2:
+                    bm.free_seq(int(rng.choice(live)))
+                else:
+                    sid = int(rng.choice(live))
+                    free_before = list(bm.free)
+                    last = bm.tables[sid][-1] if bm.tables[sid] else None
+                    ref_last = bm.ref[last] if last is not None else None
+                    slot, cow = bm.append_slot(sid)
+                    blk = slot // bs
+                    assert blk in bm.tables[sid]
+                    assert bm.ref[blk] == 1          # never write into a shared block
+                    if cow is not None:
+                        src, dst = cow
+                        assert src == last and dst == free_before[0] and src != dst
+                        assert bm.ref[src] == ref_last - 1 and blk == dst
+            except PoolExhausted:
+                assert bm.num_free() == 0
+            check_invariants(bm)
+            used = {b for b in all_ids if bm.ref[b] > 0}
+            assert used | set(bm.free) == all_ids
+
+
+def test_block_manager_fork_then_write_copies_only_the_partial_block():
+    bm = BlockManager(16, 4, range(16))
+    bm.add_seq(0)
+    for _ in range(10):                     # blocks 0, 1, 2 (2 holds 2 tokens)
+        bm.append_slot(0)
+    bm.fork(0, 1)
+    assert [bm.refcount(b) for b in (0, 1, 2)] == [2, 2, 2]
+    slot, cow = bm.append_slot(1)           # child writes into shared block 2
+    assert cow == (2, 3) and slot == 3 * 4 + 2
+    assert bm.block_table(1) == [0, 1, 3] and bm.block_table(0) == [0, 1, 2]
+    assert bm.refcount(2) == 1 and bm.refcount(3) == 1
+    slot, cow = bm.append_slot(0)           # last owner writes in place
+    assert cow is None and slot == 2 * 4 + 2
+    bm.free_seq(0)
+    assert bm.refcount(0) == 1 and bm.refcount(2) == 0 and bm.free[-1] == 2
+
+
+def test_block_manager_exhaustion_is_an_error():
+    bm = BlockManager(2, 2, [1, 0])
+    bm.add_seq(0)
+    for _ in range(4):
+        bm.append_slot(0)
+    with pytest.raises(PoolExhausted):
+        bm.append_slot(0)
+
+
+def test_llama13b_kv_bytes_per_sequence_closed_form():
+    """The glossary's "up to 1.7 GB" for one LLaMA-13B sequence: 40 layers x 40
+    heads x 128 dims x (K, V) x 2 bytes per token, 2,048 tokens."""
+    per_token = 40 * 40 * 128 * 2 * 2
+    assert per_token == 819200
+    assert abs(per_token * 2048 / 1e9 - 1.7) < 0.05
