@@ -1,0 +1,449 @@
+"""Benchmark: one decode step of paged attention (copy_blocks -> reshape_and_cache ->
+paged_attention_decode) on a seeded synthetic workload, timed on the GPU.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+Prints ONE JSON line (rank 0). ``value`` is achieved algorithmic HBM bytes of the
+whole step per second (GB/s), with every input resident in HBM; ``e2e`` is the
+same metric through the public Python API with pinned host inputs copied in and
+the output copied out inside the timed region. ``roofline`` covers the decode
+attention op alone (its kernel plus the split-KV merge), timed with CUDA events
+on its stream. ``cpu_baseline`` times the CPU oracle on a bounded sample of the
+same workload. With ``--impl reference`` the oracle alone is timed (the
+reference arm; a slow CPU program, not a target).
+
+Multi-GPU (torchrun): every rank runs its own copy of the workload (independent
+sequences; decode attention needs no exchange), so scaling is weak; the NCCL
+process group is used only for the barrier and the max-over-ranks time.
+"""
+import os
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")   # the CPU oracle runs single-threaded
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import argparse
+import json
+import math
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import pkv_workloads as wl  # noqa: E402
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of peak) and seq-steps/s"
+DEFAULT_CONFIG = "llama13b_mha_bf16"
+KV_TORCH = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8}
+KV_ELT = {"f32": 4, "bf16": 2, "e4m3": 1}
+L2_BYTES = 129 * 2 ** 20
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- byte accounting
+def step_bytes(w, tables, lens, num_pairs):
+    """Algorithmic HBM bytes of one step, by op.
+
+    decode: K and V of every cached token a sequence attends over (shared blocks
+    counted once: the unique bytes the method must move; ``logical`` counts them
+    per sequence), plus q, out, block tables and lengths. reshape: new K/V read,
+    cache slots written, slot numbers. copy: each CoW block read and written in
+    both pools, plus the pairs.
+    """
+    elt, src = KV_ELT[w.kv_dtype], (4 if w.src_dtype == torch.float32 else 2)
+    per_tok = 2 * w.Hkv * w.D * elt
+    used = {}
+    for b in range(len(lens)):
+        L = int(lens[b])
+        nb = -(-L // w.bs)
+        for j in range(nb):
+            blk = int(tables[b, j])
+            n = min(w.bs, L - j * w.bs)
+            used[blk] = max(used.get(blk, 0), n)
+    unique_tok = sum(used.values())
+    logical_tok = int(np.sum(lens))
+    qo = 2 * w.B * w.Hq * w.D * src + tables.size * 4 + len(lens) * 4
+    decode = unique_tok * per_tok + qo
+    reshape = w.B * w.Hkv * w.D * 2 * (src + elt) + w.B * 8
+    block_bytes = w.Hkv * w.bs * w.D * elt
+    copy = num_pairs * 2 * 2 * block_bytes + num_pairs * 16
+    return {"decode": decode, "decode_logical": logical_tok * per_tok + qo, "reshape": reshape,
+            "copy": copy, "total": decode + reshape + copy, "per_token": per_tok,
+            "unique_tokens": unique_tok, "logical_tokens": logical_tok}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_rate(w, inp_cpu, tables, lens, budget_s, per_tok):
+    """Run the oracle over (sequence, head) units for about budget_s seconds;
+    return (GB/s of algorithmic K/V bytes, units done, seconds, cores)."""
+    from oracle import attention as oatt
+    from oracle import fp8_e4m3 as ofp8
+    q, kp, vp, ks, vs = inp_cpu
+    if w.kv_dtype == "e4m3":
+        wk = lambda r: ofp8.e4m3_decode(ofp8.e4m3_quantize(r.float().numpy(), ks))
+        wv = lambda r: ofp8.e4m3_decode(ofp8.e4m3_quantize(r.float().numpy(), vs))
+    else:
+        wk = wv = oatt.widen
+    prev = torch.get_num_threads()
+    torch.set_num_threads(1)
+    rng = np.random.default_rng(0)
+    done, nbytes = 0, 0
+    t0 = time.perf_counter()
+    try:
+        while time.perf_counter() - t0 < budget_s:
+            b, h = int(rng.integers(w.B)), int(rng.integers(w.Hq))
+            oatt.paged_decode(q, kp, vp, tables, lens, w.scale, w.bs, ks, vs, units=[(b, h)],
+                              widen_k=wk, widen_v=wv)
+            done += 1
+            # per (b, h) unit the oracle reads the sequence's K and V for one query head
+            nbytes += int(lens[b]) * per_tok / w.Hkv
+    finally:
+        torch.set_num_threads(prev)
+    dt = time.perf_counter() - t0
+    return nbytes / dt / 1e9, done, dt, 1
+
+
+# ---------------------------------------------------------------- setup
+def build_state(w, device):
+    import paged_kv_cache_259_gb300 as pkv
+    from paged_kv_cache_259_gb300.engine import PagedKVCache
+    k_src, v_src = w.past_pools()
+    q, k_new, v_new = w.step_inputs()
+    ks = vs = 1.0
+    if w.kv_dtype == "e4m3":
+        ks, vs = w.fp8_scales(k_src, v_src, k_new, v_new)
+    cache = PagedKVCache(w.NB, w.Hq, w.Hkv, w.D, w.bs, KV_TORCH[w.kv_dtype], w.free_order, device)
+    if w.kv_dtype == "e4m3":
+        tok = lambda x: x.to(device).permute(0, 2, 1, 3).reshape(w.NB * w.bs, w.Hkv, w.D).contiguous()
+        slots = torch.arange(w.NB * w.bs, dtype=torch.int64, device=device)
+        pkv.reshape_and_cache(tok(k_src), tok(v_src), cache.k_pool, cache.v_pool, slots, ks, vs)
+    else:
+        cache.k_pool.copy_(k_src.to(device))
+        cache.v_pool.copy_(v_src.to(device))
+    cache.apply_copies(cache.replay(w.script))
+    plan = cache.plan_step(w.step_seqs, max_blocks=w.max_blocks_per_seq)
+    torch.cuda.synchronize()
+    return cache, plan, (q, k_new, v_new, ks, vs), (k_src, v_src)
+
+
+def run_gpu(args, rank, world, device):
+    import paged_kv_cache_259_gb300 as pkv
+    w = wl.CONFIGS[args.config]()
+    cache, plan, (q, k_new, v_new, ks, vs), (k_src, v_src) = build_state(w, device)
+    stream = torch.cuda.current_stream(device)
+    dev = plan.device_tensors(device)
+    qd, kd, vd = q.to(device), k_new.to(device), v_new.to(device)
+    out = torch.empty(w.B, w.Hq, w.D, dtype=w.src_dtype, device=device)
+    ws = cache.workspace(w.B, w.max_blocks_per_seq)
+    nbytes = step_bytes(w, plan.tables, plan.lens, len(plan.pairs))
+    has_copy = len(plan.pairs) > 0
+
+    def step():
+        cache.step(qd, kd, vd, dev, out, w.scale, ks, vs, ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if pkv.get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    # ---- device-resident timing: whole step, plus the decode op alone per step
+    K = args.steps
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start.record(stream)
+    for i in range(K):
+        if has_copy:
+            pkv.copy_blocks(cache.k_pool, cache.v_pool, dev["pairs"], stream=stream)
+        pkv.reshape_and_cache(kd, vd, cache.k_pool, cache.v_pool, dev["slots"], ks, vs, stream=stream)
+        ev_dec[i][0].record(stream)
+        pkv.paged_attention_decode(out, qd, cache.k_pool, cache.v_pool, dev["tables"], dev["lens"],
+                                   w.scale, ks, vs, ws, stream=stream)
+        ev_dec[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    dec_ms = np.array([a.elapsed_time(b) for a, b in ev_dec])
+    if pkv.get_device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    split = ws is not None and pkv.paged_attention_workspace_size(
+        w.B, w.Hq, w.D, w.bs, w.max_blocks_per_seq) > 0
+    launches_per_step = (1 if has_copy else 0) + 1 + 1 + (1 if split else 0)
+
+    # ---- end to end through the public API: pinned host inputs in, output out
+    host = plan.host_tensors(pin=True)
+    hq, hk, hv = q.pin_memory(), k_new.pin_memory(), v_new.pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    dplan = {k: torch.empty_like(v) for k, v in dev.items()}
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, *host.values()))
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        for src_t, dst_t in ((hq, dq), (hk, dk), (hv, dv)):
+            dst_t.copy_(src_t, non_blocking=True)
+        for k in dplan:
+            dplan[k].copy_(host[k], non_blocking=True)
+        cache.step(dq, dk, dv, dplan, out, w.scale, ks, vs, ws)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 4)):
+        e2e_step()
+    torch.cuda.synchronize()
+    K2 = max(3, K // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(K2):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K2
+
+    res = {"w": w, "nbytes": nbytes, "ms_per_step": total_ms / K, "dec_ms": float(dec_ms.mean()),
+           "dec_ms_median": float(np.median(dec_ms)), "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
+           "clocks": clk, "launches": launches_per_step * K, "split": split,
+           "cpu": (q, k_src, v_src, ks, vs, plan)}
+    return res
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_inputs_for_step(w, q, k_src, v_src, plan):
+    """CPU pools after the step's writes, as the oracle sees them (source values;
+    no GPU data). Built with the oracle's own block manager and cache ops."""
+    from oracle import cache_ops as oops
+    from oracle.block_manager import BlockManager as OBM
+    bm = OBM(w.NB, w.bs, w.free_order)
+    pairs = []
+    for op in w.script:
+        if op[0] == "add":
+            bm.add_seq(op[1])
+        elif op[0] == "fork":
+            bm.fork(op[1], op[2])
+        else:
+            for _ in range(op[2]):
+                c = bm.append_slot(op[1])[1]
+                if c is not None:
+                    pairs.append(c)
+    step = [bm.append_slot(s) for s in w.step_seqs]
+    kp, vp = k_src, v_src                   # in place: the bench's copies are not reused
+    oops.copy_blocks(kp, vp, pairs + [c for _, c in step if c is not None])
+    _, k_new, v_new = w.step_inputs()
+    oops.reshape_and_cache(k_new, v_new, kp, vp, torch.tensor([s for s, _ in step]), w.bs)
+    MB = w.max_blocks_per_seq
+    tables = np.full((w.B, MB), -1, dtype=np.int64)
+    for i, s in enumerate(w.step_seqs):
+        t = bm.block_table(s)
+        tables[i, :len(t)] = t
+    lens = np.array([bm.seq_len(s) for s in w.step_seqs])
+    return kp, vp, tables, lens
+
+
+def workload_desc(w):
+    L = np.asarray(w.final_lens)
+    return (f"{w.name}: B={w.B}, Hq={w.Hq}, Hkv={w.Hkv}, D={w.D}, block_size={w.bs}, "
+            f"NB={w.NB}, kv={w.kv_dtype}, L in [{L.min()}, {L.max()}] mean {L.mean():.1f}")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.CONFIGS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args)
+        return
+
+    import paged_kv_cache_259_gb300 as pkv
+    pkv.load_library()                       # fails loudly if the library is not built
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+
+    r = run_gpu(args, rank, world, device)
+    w, nb = r["w"], r["nbytes"]
+    ms = max_over_ranks(r["ms_per_step"], world, device)
+    dec_ms = max_over_ranks(r["dec_ms"], world, device)
+    e2e_ms = max_over_ranks(r["e2e_ms"], world, device)
+    peak, peak_kind = load_peaks()
+    value = world * nb["total"] / (ms * 1e-3) / 1e9
+    dec_gbs = nb["decode"] / (dec_ms * 1e-3) / 1e9
+
+    line = None
+    if rank == 0:
+        q, k_src, v_src, ks, vs, plan = r["cpu"]
+        kp, vp, tables, lens = oracle_inputs_for_step(w, q, k_src, v_src, plan)
+        cpu_gbs, units, secs, cores = oracle_rate(w, (q, kp, vp, ks, vs), tables, lens,
+                                                  args.cpu_budget, nb["per_token"])
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.kv_dtype, "data": "synthetic",
+            "config": {
+                "workload": workload_desc(w),
+                "step": ("copy_blocks (CoW pairs: %d) + reshape_and_cache + "
+                         "paged_attention_decode%s" % (len(plan.pairs),
+                                                       " (split-KV + merge)" if r["split"] else "")),
+                "l2": "inputs larger than L2: %.2f GB of K/V read per step vs %d MB L2"
+                      % (nb["decode"] / 1e9, L2_BYTES >> 20),
+                "bytes_per_step": nb["total"], "decode_bytes_per_step": nb["decode"],
+                "decode_logical_bytes_per_step": nb["decode_logical"],
+                "seq_steps_per_s": round(world * w.B / (ms * 1e-3), 1),
+                "step_frac_of_peak": round(value / world / peak, 4),
+            },
+            "roofline": {
+                "kernel": "paged_attention_decode (decode kernel + split merge)",
+                "bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(dec_gbs / peak, 4), "traffic": None,
+                "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+                "bytes_per_launch": nb["decode"], "ms_per_launch": round(dec_ms, 5),
+                "ms_per_launch_median": round(r["dec_ms_median"], 5),
+            },
+            "cpu_baseline": {
+                "value": round(cpu_gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                "sample": f"{units} (sequence, head) units of this workload in {secs:.1f} s, "
+                          "float64 numpy, one thread",
+            },
+            "e2e": {"value": round(world * nb["total"] / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                    "ms_per_step": round(e2e_ms, 5)},
+            "gpu_launches": r["launches"],
+            "clocks": r["clocks"],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on this workload's config."""
+    w = wl.CONFIGS[args.config]()
+    k_src, v_src = w.past_pools()
+    q, k_new, v_new = w.step_inputs()
+    ks = vs = 1.0
+    if w.kv_dtype == "e4m3":
+        ks, vs = w.fp8_scales(k_src, v_src, k_new, v_new)
+    kp, vp, tables, lens = oracle_inputs_for_step(w, q, k_src, v_src, None)
+    per_tok = 2 * w.Hkv * w.D * KV_ELT[w.kv_dtype]
+    budget = max(0.05, 120.0 / (args.steps + args.warmup))     # whole run within ~2 minutes
+    for _ in range(args.warmup):
+        oracle_rate(w, (q, kp, vp, ks, vs), tables, lens, budget, per_tok)
+    rates, units_done, secs = [], 0, 0.0
+    for _ in range(args.steps):
+        g, u, s, cores = oracle_rate(w, (q, kp, vp, ks, vs), tables, lens, budget, per_tok)
+        rates.append(g)
+        units_done += u
+        secs += s
+    value = float(np.mean(rates))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / max(1, args.steps), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype, "data": "synthetic",
+        "config": {"workload": workload_desc(w)},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{units_done} (sequence, head) units over {args.steps} steps "
+                                   f"of ~{budget:.2f} s each, float64 numpy, one thread"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

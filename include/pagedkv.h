@@ -1,0 +1,221 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv: decode-step attention over a paged KV cache,
+ * the two cache writes of a step, and the host-side block manager.
+ *
+ * Sources, by page title and section:
+ *   "PagedAttention" (Ultralytics glossary)
+ *     - "Cách phân trang hoạt động" (how paging works): the KV cache is cut into
+ *       blocks of a fixed number of tokens (16 by default) that sit anywhere in one
+ *       shared pool; each request owns a block table listing its blocks in order; a
+ *       block is taken only when the last one is full; the attention kernel reads
+ *       keys and values back through that table.
+ *     - "Chia sẻ block giữa các chuỗi" (sharing blocks): sequences may point at
+ *       the same physical block, with a reference count per block; a block still
+ *       used by another sequence is copied before a write (copy-on-write).
+ *     - "Các kỹ thuật liên quan" (related techniques): FlashAttention-style
+ *       tiling, grouped-query attention, FP8 cache quantisation.
+ *   "KV cache paginado e batching contínuo para LLMs" (upskillscore), "Como
+ *     funciona": block tables, waste confined to the last block, reference
+ *     counts, block-level copy-on-write (allocate, copy, decrement the original).
+ *
+ * Conventions for every call
+ *   - Device pointers are plain CUDA device addresses on the current device; the
+ *     caller owns every buffer. The library allocates no device memory.
+ *   - Every device call is asynchronous on `stream` (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream) and does not synchronise.
+ *   - Arguments are checked on the host before any launch; a bad argument
+ *     returns PKV_ERR_INVALID_ARG or PKV_ERR_UNSUPPORTED and launches nothing.
+ *   - Data-dependent errors found on the device (a block id or slot outside the
+ *     pool, a wait that gave up) never trap: the offending access is skipped and
+ *     a sticky device error word is set; read it with pkv_get_device_error().
+ *
+ * KV pool layout (a reading: the glossary's example shows one head as
+ * key_pool[block, slot, dim]): k_pool and v_pool are each
+ *     [num_blocks][num_kv_heads][block_size][head_dim]
+ * contiguous, so one (block, kv head) tile is block_size*head_dim contiguous
+ * elements. Element type: float32, bfloat16, or E4M3 bytes (OCP FP8, value =
+ * code * per-tensor scale).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every call. */
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = -1,    /* null/misaligned pointer, bad size or shape   */
+    PKV_ERR_UNSUPPORTED = -2,    /* valid but not built (head_dim, dtype, group) */
+    PKV_ERR_CUDA = -3,           /* a CUDA runtime call failed                   */
+    PKV_ERR_OUT_OF_RANGE = -4,   /* block id / slot / sequence id outside range  */
+    PKV_ERR_POOL_EXHAUSTED = -5, /* block manager: no free block left            */
+    PKV_ERR_TIMEOUT = -6         /* a device-side wait gave up (see kernels)     */
+} pkv_status;
+
+/* Element types. */
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_E4M3 = 2 } pkv_dtype;
+
+/* Human-readable name of a status code (static string). */
+const char* pkv_status_string(int status);
+
+/* ------------------------------------------------------------------------
+ * paged_attention_decode -- one decode query per sequence, attention over
+ * that sequence's cached tokens gathered through its block table
+ * (glossary "PagedAttention", "Cách phân trang hoạt động"; tiling and online
+ * softmax as in the FlashAttention item of "Các kỹ thuật liên quan").
+ *
+ * For every sequence b < num_seqs and query head h < num_heads, with
+ * G = num_heads / num_kv_heads and L = seq_lens[b]:
+ *     K[t] = k_pool[block_tables[b*max_blocks_per_seq + t/block_size]]
+ *                  [h/G][t % block_size][:]                         t < L
+ *     s_t  = scale * k_scale * <q[b][h], K[t]>
+ *     out[b][h] = v_scale * sum_t softmax(s)_t * V[t]
+ * L counts every cached token including the one the step just wrote; L == 0
+ * gives a zero row. Query head h reads KV head h/G.
+ *
+ *   out           device, [num_seqs][num_heads][head_dim], dtype q_dtype, written
+ *   q             device, [num_seqs][num_heads][head_dim], dtype q_dtype
+ *   k_pool/v_pool device, pool layout above, dtype kv_dtype, 16-byte aligned
+ *   block_tables  device int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                 ceil(L/block_size) are not read
+ *   seq_lens      device int32 [num_seqs], 0 <= L <= max_blocks_per_seq*block_size
+ *   num_blocks    number of blocks in each pool (bounds for table entries)
+ *   scale         softmax scale (e.g. 1/sqrt(head_dim))
+ *   q_dtype/kv_dtype  supported pairs: (F32,F32), (BF16,BF16), (BF16,E4M3)
+ *   k_scale/v_scale   per-tensor FP8 scales; must be 1.0 unless kv_dtype is E4M3
+ *   workspace     device scratch for split-KV partitions (float32), or NULL;
+ *                 with NULL (or workspace_bytes too small for any split) every
+ *                 (sequence, kv head) runs as one partition. Size it with
+ *                 paged_attention_workspace_size(). Contents need no clearing.
+ *   stream        cudaStream_t
+ * Supported: head_dim in {64,128}, block_size in {16,32}, G in {1,2,4,8}.
+ * A table entry outside [0, num_blocks) is skipped (its tokens get zero
+ * weight) and sets the device error word to PKV_ERR_OUT_OF_RANGE.
+ * ---------------------------------------------------------------------- */
+int paged_attention_decode(void* out, const void* q,
+                           const void* k_pool, const void* v_pool,
+                           const int32_t* block_tables, const int32_t* seq_lens,
+                           int num_seqs, int max_blocks_per_seq, int num_blocks,
+                           int num_heads, int num_kv_heads, int head_dim, int block_size,
+                           float scale, int q_dtype, int kv_dtype,
+                           float k_scale, float v_scale,
+                           void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* Bytes of workspace that lets paged_attention_decode use its finest split for
+ * these sizes (an upper bound; any size works, smaller ones split less). */
+size_t paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                      int block_size, int max_blocks_per_seq);
+
+/* ------------------------------------------------------------------------
+ * reshape_and_cache -- write each new token's K and V into its pool slot
+ * (glossary worked example: token pos goes to block table[pos / block_size],
+ * slot pos % block_size; the caller folds both into one slot number).
+ *
+ * For each token i < num_tokens with s = slot_mapping[i]:
+ *     s < 0          : padding, skipped
+ *     s >= num_blocks*block_size : skipped, device error PKV_ERR_OUT_OF_RANGE
+ *     otherwise      : k_pool[s/block_size][h][s%block_size][:] = k[i][h][:]
+ *                      (same for v) for every kv head h.
+ * With cache_dtype E4M3 the stored byte is round-to-nearest-even, saturating
+ * E4M3 of (x / k_scale) (resp. v_scale), the division in IEEE float32.
+ *
+ *   k, v          device [num_tokens][num_kv_heads][head_dim], dtype src_dtype
+ *   k_pool/v_pool device pools, dtype cache_dtype (== src_dtype, or E4M3)
+ *   slot_mapping  device int64 [num_tokens]
+ * Supported: head_dim a multiple of 16; (src, cache) in {(F32,F32),
+ * (BF16,BF16), (F32,E4M3), (BF16,E4M3)}.
+ * ---------------------------------------------------------------------- */
+int reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
+                      const int64_t* slot_mapping, int num_tokens,
+                      int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                      int src_dtype, int cache_dtype, float k_scale, float v_scale,
+                      void* stream);
+
+/* ------------------------------------------------------------------------
+ * copy_blocks -- the copy half of block-level copy-on-write ("Como funciona";
+ * glossary "Chia sẻ block giữa các chuỗi"): for each pair p < num_pairs,
+ * block src = pairs[2p] is copied over block dst = pairs[2p+1], in both pools,
+ * all kv heads (block_bytes bytes per pool).
+ *
+ *   src_dst_pairs device int64 [num_pairs][2]
+ *   block_bytes   bytes of one block of one pool
+ *                 (= num_kv_heads*block_size*head_dim*element size); a
+ *                 multiple of 16
+ * Preconditions (met by the block manager, whose dst is always a block it has
+ * just taken from the free list): dst values are distinct and no dst is also a
+ * src; otherwise the result is unspecified. A pair with an id outside
+ * [0, num_blocks) is skipped and sets PKV_ERR_OUT_OF_RANGE on the device.
+ * ---------------------------------------------------------------------- */
+int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs,
+                int num_pairs, int num_blocks, size_t block_bytes, void* stream);
+
+/* Synchronise `stream`, then return (in *code) and clear the device error word
+ * of the current device: PKV_OK if no kernel recorded an error since the last
+ * read, else PKV_ERR_TIMEOUT if a device wait gave up, else PKV_ERR_OUT_OF_RANGE.
+ * The word is shared by every stream of the device. Once a wait has timed out,
+ * every later wait on the device gives up at once until the word is cleared.
+ * Returns PKV_OK or PKV_ERR_CUDA. */
+int pkv_get_device_error(int* code, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Host block manager ("Como funciona"; glossary "Cách phân trang hoạt động",
+ * "Chia sẻ block giữa các chuỗi"). Host memory only, no CUDA calls; not
+ * thread-safe (one manager per thread, or external locking).
+ *
+ * Rules: blocks are taken from the front of the free list; a sequence takes a
+ * new block at its first token and whenever its length is a multiple of
+ * block_size; appending into a last block whose reference count is above 1
+ * first takes a new block dst, reports (src, dst) for copy_blocks, decrements
+ * src and repoints the table; fork shares every block (counts + 1); freeing a
+ * sequence decrements its blocks in table order and returns each block that
+ * reaches 0 to the tail of the free list.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* free_order: the num_free initially free block ids, front first (distinct,
+ * each in [0, num_blocks)). Returns NULL on a bad argument. */
+pkv_block_manager* bm_create(int num_blocks, int block_size,
+                             const int32_t* free_order, int num_free);
+void bm_destroy(pkv_block_manager* bm);
+
+int bm_add_seq(pkv_block_manager* bm, int64_t seq_id);
+/* Reserve the next token's slot: *slot = block*block_size + offset. If a
+ * copy-on-write is needed *cow_src/*cow_dst get the pair, else both are -1.
+ * PKV_ERR_POOL_EXHAUSTED leaves the manager unchanged. */
+int bm_append_slot(pkv_block_manager* bm, int64_t seq_id, int64_t* slot,
+                   int32_t* cow_src, int32_t* cow_dst);
+/* n appends to one sequence; the CoW pairs they raise are written as
+ * (src, dst) int64 pairs into cow_pairs (capacity cow_cap pairs) and counted in
+ * *num_cow. On exhaustion the appends done so far stay done. */
+int bm_append_n(pkv_block_manager* bm, int64_t seq_id, int n,
+                int64_t* cow_pairs, int cow_cap, int* num_cow);
+/* One append to each of n sequences (a decode step): slots[i] for seq_ids[i];
+ * CoW pairs in order into cow_pairs (capacity n pairs), count in *num_cow. */
+int bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n,
+                    int64_t* slots, int64_t* cow_pairs, int* num_cow);
+int bm_fork(pkv_block_manager* bm, int64_t parent, int64_t child);
+int bm_free_seq(pkv_block_manager* bm, int64_t seq_id);
+/* The sequence's table into out[0..cap), its length in blocks in *n. */
+int bm_block_table(const pkv_block_manager* bm, int64_t seq_id, int32_t* out,
+                   int cap, int* n);
+/* Dense int32 tables [n][max_blocks] (unused entries -1) and lengths [n] for
+ * seq_ids, ready to copy to the device for paged_attention_decode. */
+int bm_build_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
+                    int max_blocks, int32_t* tables, int32_t* seq_lens);
+int bm_seq_len(const pkv_block_manager* bm, int64_t seq_id, int* len);
+int bm_refcount(const pkv_block_manager* bm, int block, int* count);
+int bm_num_free(const pkv_block_manager* bm);
+/* The free list, front first, into out[0..cap); returns its length. */
+int bm_free_list(const pkv_block_manager* bm, int32_t* out, int cap);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

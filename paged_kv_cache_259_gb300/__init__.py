@@ -1,0 +1,336 @@
+"""GB300-native paged KV-cache decode path.
+
+Thin ctypes binding of ``libpagedkv.so`` (C ABI in ``include/pagedkv.h``). The
+functions here only marshal arguments: torch tensors give device pointers,
+shapes and the current CUDA stream; every step of the path runs in the
+library's CUDA kernels. There is no CPU fallback: if the library is missing, or
+a tensor is not on a CUDA device, the call raises.
+
+Entry points (same names as the C ABI):
+
+* ``paged_attention_decode`` -- decode attention through block tables.
+* ``reshape_and_cache``      -- slot-mapped write of new K/V (optionally E4M3).
+* ``copy_blocks``            -- whole-block copies for copy-on-write.
+* ``paged_attention_workspace_size``, ``get_device_error``.
+* ``BlockManager``           -- the host block manager (free list, tables,
+                                reference counts, fork, copy-on-write).
+"""
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+__all__ = [
+    "PagedKVError", "paged_attention_decode", "paged_attention_workspace_size",
+    "reshape_and_cache", "copy_blocks", "get_device_error", "BlockManager",
+    "library_path", "load_library", "PKV_F32", "PKV_BF16", "PKV_E4M3",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+_LIB = None
+
+PKV_F32, PKV_BF16, PKV_E4M3 = 0, 1, 2
+_STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration",
+           -3: "CUDA runtime error", -4: "index out of range", -5: "block pool exhausted",
+           -6: "device wait timed out"}
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: {_STATUS.get(status, 'unknown status')} ({status})")
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libpagedkv.so (built by ``paged_kv_cache_259_gb300.build``); raise if absent."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is not built; run "
+                           "`python -m paged_kv_cache_259_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    c_int, c_float, c_size, vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    ip = ctypes.POINTER(ctypes.c_int)
+    sig = {
+        "pkv_status_string": (ctypes.c_char_p, [c_int]),
+        "paged_attention_decode": (c_int, [vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int,
+                                           c_int, c_int, c_int, c_float, c_int, c_int, c_float,
+                                           c_float, vp, c_size, vp]),
+        "paged_attention_workspace_size": (c_size, [c_int, c_int, c_int, c_int, c_int]),
+        "reshape_and_cache": (c_int, [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
+                                      c_int, c_int, c_float, c_float, vp]),
+        "copy_blocks": (c_int, [vp, vp, vp, c_int, c_int, c_size, vp]),
+        "pkv_get_device_error": (c_int, [ip, vp]),
+        "bm_create": (vp, [c_int, c_int, i32p, c_int]),
+        "bm_destroy": (None, [vp]),
+        "bm_add_seq": (c_int, [vp, ctypes.c_int64]),
+        "bm_append_slot": (c_int, [vp, ctypes.c_int64, i64p, i32p, i32p]),
+        "bm_append_n": (c_int, [vp, ctypes.c_int64, c_int, i64p, c_int, ip]),
+        "bm_append_slots": (c_int, [vp, i64p, c_int, i64p, i64p, ip]),
+        "bm_fork": (c_int, [vp, ctypes.c_int64, ctypes.c_int64]),
+        "bm_free_seq": (c_int, [vp, ctypes.c_int64]),
+        "bm_block_table": (c_int, [vp, ctypes.c_int64, i32p, c_int, ip]),
+        "bm_build_tables": (c_int, [vp, i64p, c_int, c_int, i32p, i32p]),
+        "bm_seq_len": (c_int, [vp, ctypes.c_int64, ip]),
+        "bm_refcount": (c_int, [vp, c_int, ip]),
+        "bm_num_free": (c_int, [vp]),
+        "bm_free_list": (c_int, [vp, i32p, c_int]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _check(status, what):
+    if status != 0:
+        raise PagedKVError(status, what)
+
+
+_DTYPES = {torch.float32: PKV_F32, torch.bfloat16: PKV_BF16, torch.uint8: PKV_E4M3}
+if hasattr(torch, "float8_e4m3fn"):
+    _DTYPES[torch.float8_e4m3fn] = PKV_E4M3
+
+
+def _dt(t, what):
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"{what}: unsupported dtype {t.dtype}") from None
+
+
+def _cuda(t, what, contiguous=True):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{what} must be a CUDA tensor")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return t
+
+
+def _stream_ptr(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class _on_device:
+    """Make ``device`` current for the call (the library works on the current device)."""
+
+    def __init__(self, device):
+        self.idx = device.index if device.index is not None else torch.cuda.current_device()
+        self.prev = None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if cur != self.idx:
+            self.prev = cur
+            torch.cuda.set_device(self.idx)
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+
+
+def paged_attention_workspace_size(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq):
+    """Bytes of split-KV workspace for the finest split of these sizes."""
+    return int(load_library().paged_attention_workspace_size(
+        num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq))
+
+
+def paged_attention_decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale,
+                           k_scale=1.0, v_scale=1.0, workspace=None, stream=None):
+    """out[b, h] = softmax attention of q[b, h] over sequence b's cached tokens.
+
+    q, out: ``[B, Hq, D]`` (float32 or bfloat16, same dtype); pools
+    ``[NB, Hkv, bs, D]`` (float32/bfloat16 like q, or uint8/float8_e4m3fn for the
+    E4M3 cache with per-tensor ``k_scale``/``v_scale``); block_tables int32
+    ``[B, max_blocks]``; seq_lens int32 ``[B]``; workspace: any CUDA tensor used
+    as split-KV scratch (see ``paged_attention_workspace_size``) or None.
+    """
+    lib = load_library()
+    for t, n in ((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
+                 (block_tables, "block_tables"), (seq_lens, "seq_lens")):
+        _cuda(t, n)
+    if q.dim() != 3 or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("q and out must be [B, Hq, D] of the same dtype")
+    if k_pool.dim() != 4 or v_pool.shape != k_pool.shape or v_pool.dtype != k_pool.dtype:
+        raise ValueError("pools must both be [NB, Hkv, bs, D] of one dtype")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    B, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_pool.shape
+    if D2 != D or block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("inconsistent shapes")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _cuda(workspace, "workspace")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    with _on_device(q.device):
+        st = lib.paged_attention_decode(
+            out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+            block_tables.data_ptr(), seq_lens.data_ptr(), B, block_tables.shape[1], NB,
+            Hq, Hkv, D, bs, float(scale), _dt(q, "q"), _dt(k_pool, "k_pool"),
+            float(k_scale), float(v_scale), ws_ptr, ws_bytes, _stream_ptr(stream, q.device))
+    _check(st, "paged_attention_decode")
+    return out
+
+
+def reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, k_scale=1.0, v_scale=1.0, stream=None):
+    """Write k/v ``[T, Hkv, D]`` into the pools at ``slot_mapping`` (int64 ``[T]``)."""
+    lib = load_library()
+    for t, n in ((k, "k"), (v, "v"), (k_pool, "k_pool"), (v_pool, "v_pool"),
+                 (slot_mapping, "slot_mapping")):
+        _cuda(t, n)
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    T, Hkv, D = k.shape
+    NB, Hkv2, bs, D2 = k_pool.shape
+    if v.shape != k.shape or v.dtype != k.dtype or (Hkv2, D2) != (Hkv, D) or \
+            v_pool.shape != k_pool.shape or slot_mapping.shape != (T,):
+        raise ValueError("inconsistent shapes")
+    with _on_device(k.device):
+        st = lib.reshape_and_cache(
+            k.data_ptr(), v.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+            slot_mapping.data_ptr(), T, Hkv, D, bs, NB, _dt(k, "k"), _dt(k_pool, "k_pool"),
+            float(k_scale), float(v_scale), _stream_ptr(stream, k.device))
+    _check(st, "reshape_and_cache")
+
+
+def copy_blocks(k_pool, v_pool, src_dst_pairs, stream=None):
+    """``pool[dst] = pool[src]`` for each row of int64 ``src_dst_pairs [P, 2]``."""
+    lib = load_library()
+    for t, n in ((k_pool, "k_pool"), (v_pool, "v_pool"), (src_dst_pairs, "src_dst_pairs")):
+        _cuda(t, n)
+    if src_dst_pairs.dtype != torch.int64 or src_dst_pairs.dim() != 2 or \
+            src_dst_pairs.shape[1] != 2 or v_pool.shape != k_pool.shape:
+        raise ValueError("src_dst_pairs must be int64 [P, 2]; pools of one shape")
+    block_bytes = k_pool[0].numel() * k_pool.element_size()
+    with _on_device(k_pool.device):
+        st = lib.copy_blocks(k_pool.data_ptr(), v_pool.data_ptr(), src_dst_pairs.data_ptr(),
+                             src_dst_pairs.shape[0], k_pool.shape[0], block_bytes,
+                             _stream_ptr(stream, k_pool.device))
+    _check(st, "copy_blocks")
+
+
+def get_device_error(device=None, stream=None):
+    """Synchronise and return-and-clear the device error word (0 = no error)."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    code = ctypes.c_int(0)
+    with _on_device(dev):
+        _check(lib.pkv_get_device_error(ctypes.byref(code), _stream_ptr(stream, dev)),
+               "pkv_get_device_error")
+    return code.value
+
+
+def _i32p(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _i64p(a):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+
+
+class BlockManager:
+    """Host block manager of the C library (free list front-first, refcounts, CoW)."""
+
+    def __init__(self, num_blocks, block_size, free_order):
+        self._lib = load_library()
+        fo = np.ascontiguousarray(np.asarray(free_order, dtype=np.int32))
+        h = self._lib.bm_create(num_blocks, block_size, _i32p(fo), len(fo))
+        if not h:
+            raise ValueError("bm_create: invalid arguments")
+        self._h = ctypes.c_void_p(h)
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            self._lib.bm_destroy(h)
+            self._h = None
+
+    def add_seq(self, sid):
+        _check(self._lib.bm_add_seq(self._h, sid), "bm_add_seq")
+
+    def append_slot(self, sid):
+        """Returns ``(slot, cow)``; ``cow`` is ``(src, dst)`` or None."""
+        slot = ctypes.c_int64()
+        s, d = ctypes.c_int32(), ctypes.c_int32()
+        _check(self._lib.bm_append_slot(self._h, sid, ctypes.byref(slot), ctypes.byref(s),
+                                        ctypes.byref(d)), "bm_append_slot")
+        return slot.value, ((s.value, d.value) if s.value >= 0 else None)
+
+    def append_n(self, sid, n):
+        """n appends to one sequence; returns the CoW pairs raised, as a list."""
+        cap = max(1, n)
+        buf = np.zeros((cap, 2), dtype=np.int64)
+        cnt = ctypes.c_int(0)
+        _check(self._lib.bm_append_n(self._h, sid, n, _i64p(buf), cap, ctypes.byref(cnt)),
+               "bm_append_n")
+        return [tuple(map(int, r)) for r in buf[:cnt.value]]
+
+    def append_slots(self, seq_ids):
+        """One append per sequence; returns (slots int64 array, pairs int64 [P, 2])."""
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        slots = np.zeros(len(ids), dtype=np.int64)
+        pairs = np.zeros((max(1, len(ids)), 2), dtype=np.int64)
+        cnt = ctypes.c_int(0)
+        _check(self._lib.bm_append_slots(self._h, _i64p(ids), len(ids), _i64p(slots),
+                                         _i64p(pairs), ctypes.byref(cnt)), "bm_append_slots")
+        return slots, pairs[:cnt.value].copy()
+
+    def fork(self, parent, child):
+        _check(self._lib.bm_fork(self._h, parent, child), "bm_fork")
+
+    def free_seq(self, sid):
+        _check(self._lib.bm_free_seq(self._h, sid), "bm_free_seq")
+
+    def block_table(self, sid):
+        n = ctypes.c_int(0)
+        st = self._lib.bm_block_table(self._h, sid, None, 0, ctypes.byref(n))
+        if st not in (0, -1):
+            _check(st, "bm_block_table")
+        out = np.zeros(max(1, n.value), dtype=np.int32)
+        _check(self._lib.bm_block_table(self._h, sid, _i32p(out), len(out), ctypes.byref(n)),
+               "bm_block_table")
+        return [int(x) for x in out[:n.value]]
+
+    def build_tables(self, seq_ids, max_blocks):
+        """int32 tables ``[n, max_blocks]`` (-1 padded) and int32 lengths ``[n]``."""
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        tables = np.zeros((len(ids), max_blocks), dtype=np.int32)
+        lens = np.zeros(len(ids), dtype=np.int32)
+        _check(self._lib.bm_build_tables(self._h, _i64p(ids), len(ids), max_blocks,
+                                         _i32p(tables), _i32p(lens)), "bm_build_tables")
+        return tables, lens
+
+    def seq_len(self, sid):
+        n = ctypes.c_int(0)
+        _check(self._lib.bm_seq_len(self._h, sid, ctypes.byref(n)), "bm_seq_len")
+        return n.value
+
+    def refcount(self, block):
+        n = ctypes.c_int(0)
+        _check(self._lib.bm_refcount(self._h, block, ctypes.byref(n)), "bm_refcount")
+        return n.value
+
+    def num_free(self):
+        return int(self._lib.bm_num_free(self._h))
+
+    def free_list(self):
+        n = self._lib.bm_free_list(self._h, None, 0)
+        out = np.zeros(max(1, n), dtype=np.int32)
+        self._lib.bm_free_list(self._h, _i32p(out), len(out))
+        return [int(x) for x in out[:n]]

@@ -1,0 +1,214 @@
+// The two cache writes of a decode step.
+//
+// reshape_and_cache: slot-mapped write of each new token's K/V into the pools
+//   ("PagedAttention" glossary, "Cách phân trang hoạt động": token pos lives in
+//   block table[pos / block_size] at slot pos % block_size; the caller passes
+//   the folded slot number). Optional FP8 E4M3 quantisation (related-techniques
+//   section, FP8 cache item).
+// copy_blocks: the block copy of copy-on-write ("KV cache paginado...",
+//   "Como funciona"; glossary "Chia sẻ block giữa các chuỗi").
+//
+// Both are plain HBM traffic: 16-byte vector loads and stores, one thread per
+// 16-byte chunk of the destination, grids sized over the SMs.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "pkv_internal.cuh"
+
+namespace pkv {
+namespace {
+
+// Destination-chunk type of the cache: 16 bytes = CV cache elements.
+template <typename ST, typename CT>
+struct ChunkConvert;
+
+// Same type: the 16 bytes are copied unchanged.
+template <typename T>
+struct ChunkConvert<T, T> {
+    static constexpr int CV = 16 / sizeof(T);
+    __device__ __forceinline__ static uint4 run(const T* src, float) {
+        return *reinterpret_cast<const uint4*>(src);
+    }
+};
+
+__device__ __forceinline__ float to_float(float x) { return x; }
+__device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// E4M3 cache: 16 source values -> 16 bytes, each x / scale (IEEE float32 divide)
+// rounded to nearest even E4M3 with saturation to +-448.
+template <typename ST>
+struct ChunkConvert<ST, uint8_t> {
+    static constexpr int CV = 16;
+    __device__ __forceinline__ static uint4 run(const ST* src, float scale) {
+        ST vals[16];
+#pragma unroll
+        for (int i = 0; i < 16 * (int)sizeof(ST) / 16; ++i)
+            reinterpret_cast<uint4*>(vals)[i] = reinterpret_cast<const uint4*>(src)[i];
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float2 f;
+                f.x = __fdiv_rn(to_float(vals[4 * i + 2 * j]), scale);
+                f.y = __fdiv_rn(to_float(vals[4 * i + 2 * j + 1]), scale);
+                const __nv_fp8x2_storage_t pr = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+                word |= static_cast<uint32_t>(pr) << (16 * j);
+            }
+            w[i] = word;
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+template <typename ST, typename CT>
+__global__ void __launch_bounds__(256) reshape_and_cache_kernel(
+    const ST* __restrict__ k, const ST* __restrict__ v, CT* __restrict__ k_pool,
+    CT* __restrict__ v_pool, const int64_t* __restrict__ slots, int num_tokens, int hkv, int d,
+    int bs, int num_blocks, float k_scale, float v_scale, int* err) {
+    using CC = ChunkConvert<ST, CT>;
+    const int chunks_per_row = d / CC::CV;                 // per (token, head)
+    const long long per_pool = (long long)num_tokens * hkv * chunks_per_row;
+    const long long total = 2 * per_pool;
+    const long long slot_limit = (long long)num_blocks * bs;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const bool is_v = idx >= per_pool;
+        long long r = is_v ? idx - per_pool : idx;
+        const int c = (int)(r % chunks_per_row);
+        r /= chunks_per_row;
+        const int h = (int)(r % hkv);
+        const int t = (int)(r / hkv);
+        const long long slot = slots[t];
+        if (slot < 0) continue;                            // padding token
+        if (slot >= slot_limit) {
+            flag_error(err, kErrOutOfRange);
+            continue;
+        }
+        const long long blk = slot / bs, off = slot % bs;
+        const ST* src = (is_v ? v : k) + ((long long)t * hkv + h) * d + (long long)c * CC::CV;
+        CT* dst = (is_v ? v_pool : k_pool) + ((blk * hkv + h) * bs + off) * d +
+                  (long long)c * CC::CV;
+        *reinterpret_cast<uint4*>(dst) = CC::run(src, is_v ? v_scale : k_scale);
+    }
+}
+
+constexpr int kCopyThreads = 256;
+constexpr int kCopyChunkBytes = kCopyThreads * 16 * 4;    // 16 KB per CTA
+
+__global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
+    char* __restrict__ k_pool, char* __restrict__ v_pool, const int64_t* __restrict__ pairs,
+    int num_blocks, size_t block_bytes, int* err) {
+    const int pair = blockIdx.x >> 1;
+    char* pool = (blockIdx.x & 1) ? v_pool : k_pool;
+    const int64_t src = pairs[2 * pair], dst = pairs[2 * pair + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.y == 0 && !(blockIdx.x & 1))
+            flag_error(err, kErrOutOfRange);
+        return;
+    }
+    const uint4* s = reinterpret_cast<const uint4*>(pool + (size_t)src * block_bytes);
+    uint4* o = reinterpret_cast<uint4*>(pool + (size_t)dst * block_bytes);
+    const size_t n16 = block_bytes / 16;
+    const size_t beg = (size_t)blockIdx.y * (kCopyChunkBytes / 16);
+    const size_t end = min(n16, beg + kCopyChunkBytes / 16);
+    uint4 buf[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const size_t i = beg + threadIdx.x + (size_t)u * kCopyThreads;
+        if (i < end) buf[u] = s[i];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const size_t i = beg + threadIdx.x + (size_t)u * kCopyThreads;
+        if (i < end) o[i] = buf[u];
+    }
+}
+
+template <typename ST, typename CT>
+cudaError_t launch_reshape(const void* k, const void* v, void* kp, void* vp, const int64_t* slots,
+                           int num_tokens, int hkv, int d, int bs, int num_blocks, float ks,
+                           float vs, int* err, cudaStream_t stream) {
+    const long long chunks = 2LL * num_tokens * hkv * (d / ChunkConvert<ST, CT>::CV);
+    const int threads = 256;
+    long long blocks = (chunks + threads - 1) / threads;
+    const long long cap = 8LL * num_sms();                 // grid-stride beyond 8 CTAs/SM
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    reshape_and_cache_kernel<ST, CT><<<(unsigned)blocks, threads, 0, stream>>>(
+        static_cast<const ST*>(k), static_cast<const ST*>(v), static_cast<CT*>(kp),
+        static_cast<CT*>(vp), slots, num_tokens, hkv, d, bs, num_blocks, ks, vs, err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+int reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
+                      const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                      int block_size, int num_blocks, int src_dtype, int cache_dtype,
+                      float k_scale, float v_scale, void* stream) {
+    using namespace pkv;
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (head_dim % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !k_pool || !v_pool || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool))
+        return PKV_ERR_INVALID_ARG;
+    const bool fp8 = cache_dtype == PKV_E4M3;
+    if (fp8) {
+        if (!(k_scale > 0.f) || !(v_scale > 0.f) || !isfinite(k_scale) || !isfinite(v_scale))
+            return PKV_ERR_INVALID_ARG;
+    } else if (cache_dtype != src_dtype) {
+        return PKV_ERR_UNSUPPORTED;
+    }
+    int* err = error_word();
+    if (!err) return PKV_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (src_dtype == PKV_F32 && cache_dtype == PKV_F32)
+        e = launch_reshape<float, float>(k, v, k_pool, v_pool, slot_mapping, num_tokens,
+                                         num_kv_heads, head_dim, block_size, num_blocks, 1.f, 1.f,
+                                         err, s);
+    else if (src_dtype == PKV_BF16 && cache_dtype == PKV_BF16)
+        e = launch_reshape<__nv_bfloat16, __nv_bfloat16>(k, v, k_pool, v_pool, slot_mapping,
+                                                         num_tokens, num_kv_heads, head_dim,
+                                                         block_size, num_blocks, 1.f, 1.f, err, s);
+    else if (src_dtype == PKV_F32 && fp8)
+        e = launch_reshape<float, uint8_t>(k, v, k_pool, v_pool, slot_mapping, num_tokens,
+                                           num_kv_heads, head_dim, block_size, num_blocks, k_scale,
+                                           v_scale, err, s);
+    else if (src_dtype == PKV_BF16 && fp8)
+        e = launch_reshape<__nv_bfloat16, uint8_t>(k, v, k_pool, v_pool, slot_mapping, num_tokens,
+                                                   num_kv_heads, head_dim, block_size, num_blocks,
+                                                   k_scale, v_scale, err, s);
+    else
+        return PKV_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs, int num_pairs,
+                int num_blocks, size_t block_bytes, void* stream) {
+    using namespace pkv;
+    if (num_pairs < 0 || num_blocks <= 0 || block_bytes == 0 || block_bytes % 16 != 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_pool || !v_pool || !src_dst_pairs || !aligned16(k_pool) || !aligned16(v_pool))
+        return PKV_ERR_INVALID_ARG;
+    if (num_pairs > (1 << 30) || block_bytes / kCopyChunkBytes >= 65535)
+        return PKV_ERR_UNSUPPORTED;
+    int* err = error_word();
+    if (!err) return PKV_ERR_CUDA;
+    const unsigned chunks = (unsigned)((block_bytes + kCopyChunkBytes - 1) / kCopyChunkBytes);
+    dim3 grid(2u * (unsigned)num_pairs, chunks);
+    copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<char*>(k_pool), static_cast<char*>(v_pool), src_dst_pairs, num_blocks,
+        block_bytes, err);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// C ABI entry points of decode attention: argument checks and dispatch.
+#include <cmath>
+
+#include "pkv_decode_impl.cuh"
+
+namespace pkv {
+namespace decode {
+int dispatch_f32(const Args& a);
+int dispatch_bf16(const Args& a);
+int dispatch_e4m3(const Args& a);
+}  // namespace decode
+}  // namespace pkv
+
+extern "C" {
+
+size_t paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim, int block_size,
+                                      int max_blocks_per_seq) {
+    using namespace pkv::decode;
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        max_blocks_per_seq <= 0)
+        return 0;
+    const int parts = (max_blocks_per_seq + kMinPartBlocks - 1) / kMinPartBlocks;
+    return parts > 1 ? workspace_need(num_seqs, num_heads, head_dim, parts) : 0;
+}
+
+int paged_attention_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                           int max_blocks_per_seq, int num_blocks, int num_heads, int num_kv_heads,
+                           int head_dim, int block_size, float scale, int q_dtype, int kv_dtype,
+                           float k_scale, float v_scale, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    using namespace pkv;
+    if (num_seqs < 0 || num_seqs > 65535 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
+        num_heads <= 0 || num_kv_heads <= 0 || num_kv_heads > 65535 || head_dim <= 0 ||
+        block_size <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale) ||
+        !(k_scale > 0.f) || !(v_scale > 0.f))
+        return PKV_ERR_INVALID_ARG;
+    if (kv_dtype != PKV_E4M3 && (k_scale != 1.f || v_scale != 1.f)) return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(q) || !aligned16(out))
+        return PKV_ERR_INVALID_ARG;
+    if (workspace && !aligned16(workspace)) return PKV_ERR_INVALID_ARG;
+    if ((head_dim != 64 && head_dim != 128) || (block_size != 16 && block_size != 32))
+        return PKV_ERR_UNSUPPORTED;
+
+    decode::Args a;
+    a.out = out;
+    a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.num_seqs = num_seqs;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.scale = scale;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace ? workspace_bytes : 0;
+    a.stream = static_cast<cudaStream_t>(stream);
+    a.err = error_word();
+    if (!a.err) return PKV_ERR_CUDA;
+
+    if (q_dtype == PKV_F32 && kv_dtype == PKV_F32) return decode::dispatch_f32(a);
+    if (q_dtype == PKV_BF16 && kv_dtype == PKV_BF16) return decode::dispatch_bf16(a);
+    if (q_dtype == PKV_BF16 && kv_dtype == PKV_E4M3) return decode::dispatch_e4m3(a);
+    return PKV_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// Internal helpers shared by the libpagedkv translation units (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/pagedkv.h"
+
+// ---------------------------------------------------------------- host side
+namespace pkv {
+
+// Device address of the current device's sticky error word (0 = no error;
+// otherwise the first pkv_status a kernel recorded). Cached per device.
+// Returns nullptr if the runtime cannot resolve it.
+int* error_word();
+
+// Streaming multiprocessor count of the current device (cached per device).
+int num_sms();
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace pkv
+
+// ---------------------------------------------------------------- device side
+namespace pkv {
+
+// Upper bound on any spin-wait in these kernels. A wait that runs past it records
+// kErrTimeout and gives up instead of hanging the GPU; once that bit is set every
+// other wait of the library on the device gives up at once.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
+
+// Bits of the device error word (pkv_get_device_error maps them to a status).
+constexpr int kErrOutOfRange = 1;
+constexpr int kErrTimeout = 2;
+
+__device__ __forceinline__ void flag_error(int* err, int bit) {
+    if (err) atomicOr(err, bit);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of the barrier to complete, for at most kWaitLimitNs
+// (or until another wait has timed out).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, const int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (unsigned it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (global_ns() - t0 > kWaitLimitNs) return false;
+            if (err && (*reinterpret_cast<const volatile int*>(err) & kErrTimeout)) return false;
+        }
+    }
+}
+
+// L2 policy for data read exactly once (K/V tiles): evict first.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 1-D bulk copy global -> shared (TMA engine, no tensor map), completing on `bar`.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+}  // namespace pkv

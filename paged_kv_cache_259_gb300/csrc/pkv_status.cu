@@ -1,0 +1,71 @@
+// Status strings, the device error word and per-device caches.
+#include <atomic>
+
+#include "pkv_internal.cuh"
+
+// Sticky error bits (pkv::kErr*) recorded by any kernel of this library on this device.
+__device__ int g_pkv_error_word;
+
+namespace pkv {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int*> g_err_ptr[kMaxDevices];
+std::atomic<int> g_sms[kMaxDevices];
+}  // namespace
+
+int* error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    int* p = g_err_ptr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_pkv_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev].store(static_cast<int*>(addr), std::memory_order_release);
+    return static_cast<int*>(addr);
+}
+
+int num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    int n = g_sms[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sms[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+const char* pkv_status_string(int status) {
+    switch (status) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PKV_ERR_CUDA: return "CUDA runtime error";
+        case PKV_ERR_OUT_OF_RANGE: return "index out of range";
+        case PKV_ERR_POOL_EXHAUSTED: return "block pool exhausted";
+        case PKV_ERR_TIMEOUT: return "device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int pkv_get_device_error(int* code, void* stream) {
+    if (!code) return PKV_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* p = pkv::error_word();
+    if (!p) return PKV_ERR_CUDA;
+    int host = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaMemcpyAsync(&host, p, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (cudaMemsetAsync(p, 0, sizeof(int), s) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+    *code = (host & pkv::kErrTimeout) ? PKV_ERR_TIMEOUT
+            : (host & pkv::kErrOutOfRange) ? PKV_ERR_OUT_OF_RANGE : PKV_OK;
+    return PKV_OK;
+}
+
+}  // extern "C"

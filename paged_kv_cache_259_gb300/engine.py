@@ -1,0 +1,108 @@
+"""One decode step of paged attention, end to end, over the C ABI.
+
+A ``PagedKVCache`` owns the two device pools (``[NB, Hkv, bs, D]``) and a host
+``BlockManager``. A step is:
+
+1. host: one ``append_slot`` per sequence -> slot numbers and copy-on-write
+   pairs ("KV cache paginado...", "Como funciona": copy a shared block before
+   writing into it); dense block tables and lengths for the batch;
+2. device, in stream order: ``copy_blocks`` (CoW copies first), then
+   ``reshape_and_cache`` (the new token's K/V into its slot), then
+   ``paged_attention_decode`` (glossary "PagedAttention": attention reads the
+   cache back through the block table).
+
+Pools are allocated by torch (device memory is plumbing); all arithmetic runs in
+the library's kernels.
+"""
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import (BlockManager, copy_blocks, paged_attention_decode,
+               paged_attention_workspace_size, reshape_and_cache)
+
+
+@dataclass
+class StepPlan:
+    """Host-side inputs of one decode step."""
+    seq_ids: np.ndarray      # int64 [B]
+    slots: np.ndarray        # int64 [B]
+    pairs: np.ndarray        # int64 [P, 2]
+    tables: np.ndarray       # int32 [B, max_blocks]
+    lens: np.ndarray         # int32 [B]
+
+    def host_tensors(self, pin=True):
+        t = {"slots": torch.from_numpy(self.slots), "pairs": torch.from_numpy(self.pairs),
+             "tables": torch.from_numpy(self.tables), "lens": torch.from_numpy(self.lens)}
+        if pin:
+            t = {k: v.pin_memory() for k, v in t.items()}
+        return t
+
+    def device_tensors(self, device, non_blocking=False):
+        return {k: v.to(device, non_blocking=non_blocking)
+                for k, v in self.host_tensors(pin=non_blocking).items()}
+
+    def nbytes(self):
+        return self.slots.nbytes + self.pairs.nbytes + self.tables.nbytes + self.lens.nbytes
+
+
+class PagedKVCache:
+    def __init__(self, num_blocks, num_heads, num_kv_heads, head_dim, block_size, kv_dtype,
+                 free_order, device="cuda"):
+        self.device = torch.device(device)
+        self.num_blocks = num_blocks
+        self.num_heads = num_heads
+        self.num_kv_heads = num_kv_heads
+        self.head_dim = head_dim
+        self.block_size = block_size
+        shape = (num_blocks, num_kv_heads, block_size, head_dim)
+        self.k_pool = torch.empty(shape, dtype=kv_dtype, device=self.device)
+        self.v_pool = torch.empty(shape, dtype=kv_dtype, device=self.device)
+        self.bm = BlockManager(num_blocks, block_size, free_order)
+
+    def replay(self, script):
+        """Apply block-manager operations; returns the CoW pairs raised (in order)."""
+        pairs = []
+        for op in script:
+            if op[0] == "add":
+                self.bm.add_seq(op[1])
+            elif op[0] == "append":
+                pairs += self.bm.append_n(op[1], op[2])
+            elif op[0] == "fork":
+                self.bm.fork(op[1], op[2])
+            elif op[0] == "free":
+                self.bm.free_seq(op[1])
+            else:
+                raise ValueError(f"unknown op {op[0]}")
+        return pairs
+
+    def apply_copies(self, pairs, stream=None):
+        if len(pairs):
+            t = torch.as_tensor(np.asarray(pairs, dtype=np.int64).reshape(-1, 2), device=self.device)
+            copy_blocks(self.k_pool, self.v_pool, t, stream=stream)
+
+    def plan_step(self, seq_ids, max_blocks=None):
+        ids = np.asarray(seq_ids, dtype=np.int64)
+        slots, pairs = self.bm.append_slots(ids)
+        if max_blocks is None:
+            max_blocks = max(1, max(-(-self.bm.seq_len(int(s)) // self.block_size) for s in ids))
+        tables, lens = self.bm.build_tables(ids, max_blocks)
+        return StepPlan(ids, slots, pairs, tables, lens)
+
+    def workspace(self, batch, max_blocks):
+        n = paged_attention_workspace_size(batch, self.num_heads, self.head_dim, self.block_size,
+                                           max_blocks)
+        return torch.empty(max(n, 16), dtype=torch.uint8, device=self.device)
+
+    def step(self, q, k_new, v_new, dev_plan, out, scale, k_scale=1.0, v_scale=1.0,
+             workspace=None, stream=None):
+        """The device half of a decode step: copies, slot writes, attention."""
+        pairs = dev_plan["pairs"]
+        if pairs.shape[0]:
+            copy_blocks(self.k_pool, self.v_pool, pairs, stream=stream)
+        reshape_and_cache(k_new, v_new, self.k_pool, self.v_pool, dev_plan["slots"],
+                          k_scale, v_scale, stream=stream)
+        paged_attention_decode(out, q, self.k_pool, self.v_pool, dev_plan["tables"],
+                               dev_plan["lens"], scale, k_scale, v_scale, workspace, stream)
+        return out

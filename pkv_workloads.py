@@ -90,7 +90,7 @@ def _pool_size(total_blocks):
     return int(math.ceil(1.1 * total_blocks))
 
 
-def _prefill_workload(name, seed, lens, Hq, Hkv, D, bs, src_dtype, kv_dtype, scale, NB=None):
+def prefill_workload(name, seed, lens, Hq, Hkv, D, bs, src_dtype, kv_dtype, scale, NB=None):
     """Sequences 0..B-1, each with ``len - 1`` past tokens and one step token."""
     rng = np.random.default_rng(seed)
     lens = np.asarray(lens, dtype=np.int64)
@@ -110,7 +110,7 @@ def _prefill_workload(name, seed, lens, Hq, Hkv, D, bs, src_dtype, kv_dtype, sca
 
 def tiny_fp32():
     """4 sequences of lengths {1, 17, 40, 100}, 4 heads (MHA), D 64, bs 16, 64 blocks."""
-    return _prefill_workload("tiny_fp32", 0, [1, 17, 40, 100], 4, 4, 64, 16,
+    return prefill_workload("tiny_fp32", 0, [1, 17, 40, 100], 4, 4, 64, 16,
                              torch.float32, "f32", 1.0 / 8.0, NB=64)
 
 
@@ -118,7 +118,7 @@ def llama13b_mha_bf16(B=64):
     """LLaMA-13B-shaped layer: 40 heads MHA, D 128, bs 16, lengths U[128, 2048]."""
     rng = np.random.default_rng(1)
     lens = rng.integers(128, 2048, size=B, endpoint=True)
-    w = _prefill_workload("llama13b_mha_bf16", 1, lens, 40, 40, 128, 16,
+    w = prefill_workload("llama13b_mha_bf16", 1, lens, 40, 40, 128, 16,
                           torch.bfloat16, "bf16", 1.0 / math.sqrt(128))
     return w
 
@@ -128,7 +128,7 @@ def gqa_chat_bf16(B=256):
     rounded and clipped to [16, 4096]."""
     rng = np.random.default_rng(2)
     lens = np.clip(np.round(400.0 * np.exp(rng.standard_normal(B))), 16, 4096).astype(np.int64)
-    return _prefill_workload("gqa_chat_bf16", 2, lens, 32, 8, 128, 16,
+    return prefill_workload("gqa_chat_bf16", 2, lens, 32, 8, 128, 16,
                              torch.bfloat16, "bf16", 1.0 / math.sqrt(128))
 
 
@@ -173,7 +173,7 @@ def shared_prefix_bf16(fork_step=False, groups=64, per_group=4, prompt=520, max_
 
 def long_fp8(bs=16, B=16, L=32768):
     """Long context with an E4M3 cache: B sequences of L tokens, GQA 32/8, D 128."""
-    return _prefill_workload(f"long_fp8_bs{bs}", 4, [L] * B, 32, 8, 128, bs,
+    return prefill_workload(f"long_fp8_bs{bs}", 4, [L] * B, 32, 8, 128, bs,
                              torch.bfloat16, "e4m3", 1.0 / math.sqrt(128))
 
 

@@ -1,0 +1,109 @@
+"""The library's C++ block manager against the oracle's, operation by operation.
+
+Host logic, bit-exact: slots, copy-on-write pairs, block tables, reference counts
+and the free list must agree after every operation of seeded random scripts and of
+the benchmark workloads' set-up scripts.
+"""
+import numpy as np
+import pytest
+
+from _lib import library, pkv
+import pkv_workloads as wl
+from oracle.block_manager import BlockManager as OracleBM, PoolExhausted
+
+
+def same_state(a, o):
+    assert a.free_list() == o.free
+    for sid in o.tables:
+        assert a.block_table(sid) == o.tables[sid]
+        assert a.seq_len(sid) == o.lens[sid]
+    assert [a.refcount(b) for b in range(o.num_blocks)] == o.ref
+
+
+def test_random_scripts_match_oracle():
+    library()
+    rng = np.random.default_rng(7)
+    for trial in range(25):
+        nb, bs = int(rng.integers(4, 80)), int(rng.choice([1, 2, 4, 16, 32]))
+        free = rng.permutation(nb)
+        a = pkv.BlockManager(nb, bs, free)
+        o = OracleBM(nb, bs, free)
+        nxt = 0
+        for _ in range(300):
+            live = sorted(o.tables)
+            op = int(rng.integers(0, 10))
+            if op == 0 or not live:
+                a.add_seq(nxt)
+                o.add_seq(nxt)
+                nxt += 1
+            elif op == 1:
+                p = int(rng.choice(live))
+                a.fork(p, nxt)
+                o.fork(p, nxt)
+                nxt += 1
+            elif op == 2:
+                s = int(rng.choice(live))
+                a.free_seq(s)
+                o.free_seq(s)
+            else:
+                s = int(rng.choice(live))
+                try:
+                    exp = o.append_slot(s)
+                except PoolExhausted:
+                    with pytest.raises(pkv.PagedKVError) as e:
+                        a.append_slot(s)
+                    assert e.value.status == -5
+                else:
+                    assert a.append_slot(s) == exp
+            same_state(a, o)
+
+
+def test_batch_append_and_tables_match_oracle():
+    library()
+    a = pkv.BlockManager(40, 4, range(40))
+    o = OracleBM(40, 4, range(40))
+    for s in range(3):
+        a.add_seq(s)
+        o.add_seq(s)
+    assert a.append_n(0, 9) == []
+    for _ in range(9):
+        o.append_slot(0)
+    a.fork(0, 3)
+    o.fork(0, 3)
+    slots, pairs = a.append_slots([0, 3, 1, 2])
+    exp = [o.append_slot(s) for s in (0, 3, 1, 2)]
+    assert list(slots) == [e[0] for e in exp]
+    assert [tuple(p) for p in pairs] == [e[1] for e in exp if e[1] is not None]
+    tables, lens = a.build_tables([0, 3, 1, 2], 5)
+    for i, s in enumerate((0, 3, 1, 2)):
+        t = o.tables[s]
+        assert list(tables[i, :len(t)]) == t and all(tables[i, len(t):] == -1)
+        assert lens[i] == o.lens[s]
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "llama13b_mha_bf16", "gqa_chat_bf16",
+                                  "shared_prefix_bf16", "shared_prefix_fork_bf16"])
+def test_workload_setup_and_step_match_oracle(name):
+    library()
+    w = wl.CONFIGS[name]()
+    a = pkv.BlockManager(w.NB, w.bs, w.free_order)
+    o = OracleBM(w.NB, w.bs, w.free_order)
+    for op in w.script:
+        if op[0] == "add":
+            a.add_seq(op[1])
+            o.add_seq(op[1])
+        elif op[0] == "fork":
+            a.fork(op[1], op[2])
+            o.fork(op[1], op[2])
+        elif op[0] == "append":
+            got = a.append_n(op[1], op[2])
+            exp = [c for c in (o.append_slot(op[1])[1] for _ in range(op[2])) if c is not None]
+            assert got == exp
+    slots, pairs = a.append_slots(w.step_seqs)
+    exp = [o.append_slot(s) for s in w.step_seqs]
+    assert list(slots) == [e[0] for e in exp]
+    assert [tuple(p) for p in pairs] == [e[1] for e in exp if e[1] is not None]
+    assert [o.lens[s] for s in w.step_seqs] == list(w.final_lens)
+    same_state(a, o)
+    if name == "shared_prefix_fork_bf16":
+        assert len(pairs) == 64 * 3          # 3 of 4 writers copy; the last writes in place
