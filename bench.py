@@ -188,7 +188,7 @@ def build_state(w, device):
 
 def run_gpu(args, rank, world, device):
     import paged_kv_cache_259_gb300 as pkv
-    w = wl.CONFIGS[args.config]()
+    w = make_workload(args)
     cache, plan, (q, k_new, v_new, ks, vs), (k_src, v_src) = build_state(w, device)
     stream = torch.cuda.current_stream(device)
     dev = plan.device_tensors(device)
@@ -317,6 +317,19 @@ def oracle_inputs_for_step(w, q, k_src, v_src, plan):
     return kp, vp, tables, lens
 
 
+def make_workload(args):
+    if args.batch is None:
+        return wl.CONFIGS[args.config]()
+    scaled = {"llama13b_mha_bf16": lambda B: wl.llama13b_mha_bf16(B=B),
+              "gqa_chat_bf16": lambda B: wl.gqa_chat_bf16(B=B),
+              "long_fp8_bs16": lambda B: wl.long_fp8(16, B=B),
+              "long_fp8_bs32": lambda B: wl.long_fp8(32, B=B),
+              "shared_prefix_bf16": lambda B: wl.shared_prefix_bf16(groups=max(1, B // 4))}
+    if args.config not in scaled:
+        raise SystemExit(f"--batch is not supported for {args.config}")
+    return scaled[args.config](args.batch)
+
+
 def workload_desc(w):
     L = np.asarray(w.final_lens)
     return (f"{w.name}: B={w.B}, Hq={w.Hq}, Hkv={w.Hkv}, D={w.D}, block_size={w.bs}, "
@@ -329,6 +342,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.CONFIGS))
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's sequence count (profiling small cases)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing")
     args = ap.parse_args()
@@ -412,7 +427,7 @@ def main():
 
 def run_reference(args):
     """The reference arm: the CPU oracle, as it stands, on this workload's config."""
-    w = wl.CONFIGS[args.config]()
+    w = make_workload(args)
     k_src, v_src = w.past_pools()
     q, k_new, v_new = w.step_inputs()
     ks = vs = 1.0

@@ -63,6 +63,12 @@ typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_E4M3 = 2 } pkv_dtype;
 /* Human-readable name of a status code (static string). */
 const char* pkv_status_string(int status);
 
+/* Message of the last CUDA runtime failure behind a PKV_ERR_CUDA returned to
+ * this thread (which call, the runtime's error string and code); "" if none.
+ * The string belongs to the library and stays valid until the thread's next
+ * failing call. */
+const char* pkv_last_error_string(void);
+
 /* ------------------------------------------------------------------------
  * paged_attention_decode -- one decode query per sequence, attention over
  * that sequence's cached tokens gathered through its block table

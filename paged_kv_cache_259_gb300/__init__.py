@@ -62,6 +62,7 @@ def load_library():
     ip = ctypes.POINTER(ctypes.c_int)
     sig = {
         "pkv_status_string": (ctypes.c_char_p, [c_int]),
+        "pkv_last_error_string": (ctypes.c_char_p, []),
         "paged_attention_decode": (c_int, [vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int,
                                            c_int, c_int, c_int, c_float, c_int, c_int, c_float,
                                            c_float, vp, c_size, vp]),
@@ -95,6 +96,8 @@ def load_library():
 
 def _check(status, what):
     if status != 0:
+        if status == -3 and _LIB is not None:
+            what = f"{what} [{_LIB.pkv_last_error_string().decode(errors='replace')}]"
         raise PagedKVError(status, what)
 
 

@@ -188,7 +188,7 @@ int reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
                                                    k_scale, v_scale, err, s);
     else
         return PKV_ERR_UNSUPPORTED;
-    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return e == cudaSuccess ? PKV_OK : cuda_fail("reshape_and_cache: kernel launch", e);
 }
 
 int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs, int num_pairs,
@@ -208,7 +208,8 @@ int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs, int nu
     copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<char*>(k_pool), static_cast<char*>(v_pool), src_dst_pairs, num_blocks,
         block_bytes, err);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PKV_OK : cuda_fail("copy_blocks: kernel launch", e);
 }
 
 }  // extern "C"

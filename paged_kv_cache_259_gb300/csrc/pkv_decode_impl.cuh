@@ -147,7 +147,9 @@ struct Shape {
     static constexpr int kSpl = kGbs >= 32 ? kGbs / 32 : 1; // scores per softmax lane
     static constexpr int kActive = kGbs >= 32 ? 32 : kGbs;  // softmax lanes
     static constexpr int kGs = BS / kSpl;                   // softmax lanes per head
-    static constexpr int kStages = (98304 / (NW * 2 * kTile)) < 2 ? 2
+    // about 96 KB of ring per CTA (two CTAs per SM); at least one stage per warp
+    // (a 16 KB tile, float32 D128 with 32-token blocks, gets a single stage)
+    static constexpr int kStages = (98304 / (NW * 2 * kTile)) < 1 ? 1
                                    : (98304 / (NW * 2 * kTile)) > 8 ? 8
                                    : (98304 / (NW * 2 * kTile));
     static constexpr int kRingBytes = NW * kStages * 2 * kTile;
@@ -158,6 +160,7 @@ struct Shape {
     static_assert(32 % kLpr == 0 && kLpr >= 1, "row must map onto whole lanes");
     static_assert(BS % kRpp == 0, "block must hold whole warp passes");
     static_assert(NW * G * (D + 2) * 4 <= kRingBytes, "combine area must fit in the ring");
+    static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
     static_assert(kGbs % kSpl == 0 && BS % kSpl == 0, "softmax lanes");
 };
 
@@ -513,15 +516,15 @@ int launch_variant(const Args& a) {
     auto kern = paged_decode_kernel<QT, KV, D, BS, G, kNumWarps>;
     static int attr_done[kMaxDevices];      // 0 = not yet, else occupancy + 1
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevices) return PKV_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevices)
+        return cuda_fail("decode: current device", cudaErrorInvalidDevice);
     if (!attr_done[dev]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem) !=
-            cudaSuccess)
-            return PKV_ERR_CUDA;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             S::kSmem);
+        if (e != cudaSuccess) return cuda_fail("decode: set max dynamic shared memory", e);
         int occ = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kNumWarps * 32, S::kSmem) !=
-            cudaSuccess)
-            return PKV_ERR_CUDA;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kNumWarps * 32, S::kSmem);
+        if (e != cudaSuccess) return cuda_fail("decode: occupancy query", e);
         attr_done[dev] = occ + 1;
     }
     int parts = 1;
@@ -549,10 +552,12 @@ int launch_variant(const Args& a) {
 
     dim3 grid(parts, a.num_kv_heads, a.num_seqs);
     kern<<<grid, kNumWarps * 32, S::kSmem, a.stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail("decode: kernel launch", e);
     if (parts > 1) {
         split_reduce_kernel<QT><<<dim3(a.num_heads, a.num_seqs), 128, 0, a.stream>>>(p, D, BS);
-        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail("decode: split merge launch", e);
     }
     return PKV_OK;
 }

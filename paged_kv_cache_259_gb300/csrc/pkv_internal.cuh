@@ -19,6 +19,10 @@ int* error_word();
 // Streaming multiprocessor count of the current device (cached per device).
 int num_sms();
 
+// Record a failed CUDA runtime call (message for pkv_last_error_string) and
+// return PKV_ERR_CUDA.
+int cuda_fail(const char* what, cudaError_t e);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace pkv

@@ -1,5 +1,6 @@
 // Status strings, the device error word and per-device caches.
 #include <atomic>
+#include <cstdio>
 
 #include "pkv_internal.cuh"
 
@@ -20,9 +21,23 @@ int* error_word() {
     int* p = g_err_ptr[dev].load(std::memory_order_acquire);
     if (p) return p;
     void* addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_pkv_error_word) != cudaSuccess) return nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&addr, g_pkv_error_word);
+    if (e != cudaSuccess) {
+        cuda_fail("error word address", e);
+        return nullptr;
+    }
     g_err_ptr[dev].store(static_cast<int*>(addr), std::memory_order_release);
     return static_cast<int*>(addr);
+}
+
+namespace {
+thread_local char g_last_error[256] = "";
+}
+
+int cuda_fail(const char* what, cudaError_t e) {
+    (void)cudaGetLastError();   // leave no stale (non-sticky) error for the caller's next check
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+    return PKV_ERR_CUDA;
 }
 
 int num_sms() {
@@ -52,17 +67,19 @@ const char* pkv_status_string(int status) {
     }
 }
 
+const char* pkv_last_error_string(void) { return pkv::g_last_error; }
+
 int pkv_get_device_error(int* code, void* stream) {
     if (!code) return PKV_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int* p = pkv::error_word();
     if (!p) return PKV_ERR_CUDA;
     int host = 0;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
-    if (cudaMemcpyAsync(&host, p, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return PKV_ERR_CUDA;
-    if (cudaMemsetAsync(p, 0, sizeof(int), s) != cudaSuccess) return PKV_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&host, p, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return pkv::cuda_fail("pkv_get_device_error", e);
     *code = (host & pkv::kErrTimeout) ? PKV_ERR_TIMEOUT
             : (host & pkv::kErrOutOfRange) ? PKV_ERR_OUT_OF_RANGE : PKV_OK;
     return PKV_OK;
