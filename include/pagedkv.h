@@ -161,6 +161,37 @@ int reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
 int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs,
                 int num_pairs, int num_blocks, size_t block_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * paged_attention_decode_noalloc -- paged_attention_decode for callers that
+ * cannot allocate device memory where they decode (e.g. a plug-in inside a
+ * runtime that owns all device memory, or a serving loop whose memory plan is
+ * fixed at start-up so nothing allocates -- and possibly synchronises or fails
+ * -- while it serves). The pages have no counterpart: it is a deployment
+ * variant of the same computation.
+ *
+ * Same arguments and result as paged_attention_decode, without workspace: the
+ * split-KV scratch is a fixed array inside the library of
+ * PKV_NOALLOC_WORKSPACE_BYTES per GPU, held by every GPU that loads the
+ * library until the process exits. Nothing is allocated by the call.
+ *   - Limit: num_seqs * num_heads * 2 * (head_dim + 2) * 4 bytes (the smallest
+ *     split) must not exceed PKV_NOALLOC_WORKSPACE_BYTES, else the call returns
+ *     PKV_ERR_INVALID_ARG and launches nothing. Within it the split is chosen
+ *     to fit the array.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (once); make that first call before any stream capture.
+ *   - All calls on a device share the array: calls that overlap on the GPU
+ *     (other streams, other threads) race on it and must be serialised. It
+ *     keeps the last call's contents; nothing in it needs clearing.
+ * ---------------------------------------------------------------------- */
+#define PKV_NOALLOC_WORKSPACE_BYTES (32u * 1024u * 1024u)
+int paged_attention_decode_noalloc(void* out, const void* q,
+                                   const void* k_pool, const void* v_pool,
+                                   const int32_t* block_tables, const int32_t* seq_lens,
+                                   int num_seqs, int max_blocks_per_seq, int num_blocks,
+                                   int num_heads, int num_kv_heads, int head_dim,
+                                   int block_size, float scale, int q_dtype, int kv_dtype,
+                                   float k_scale, float v_scale, void* stream);
+
 /* Synchronise `stream`, then return (in *code) and clear the device error word
  * of the current device: PKV_OK if no kernel recorded an error since the last
  * read, else PKV_ERR_TIMEOUT if a device wait gave up, else PKV_ERR_OUT_OF_RANGE.

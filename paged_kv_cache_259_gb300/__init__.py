@@ -23,6 +23,7 @@ import torch
 
 __all__ = [
     "PagedKVError", "paged_attention_decode", "paged_attention_workspace_size",
+    "paged_attention_decode_noalloc", "NOALLOC_WORKSPACE_BYTES",
     "reshape_and_cache", "copy_blocks", "get_device_error", "BlockManager",
     "library_path", "load_library", "PKV_F32", "PKV_BF16", "PKV_E4M3",
 ]
@@ -67,6 +68,9 @@ def load_library():
                                            c_int, c_int, c_int, c_float, c_int, c_int, c_float,
                                            c_float, vp, c_size, vp]),
         "paged_attention_workspace_size": (c_size, [c_int, c_int, c_int, c_int, c_int]),
+        "paged_attention_decode_noalloc": (c_int, [vp, vp, vp, vp, vp, vp, c_int, c_int, c_int,
+                                                   c_int, c_int, c_int, c_int, c_float, c_int,
+                                                   c_int, c_float, c_float, vp]),
         "reshape_and_cache": (c_int, [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
                                       c_int, c_int, c_float, c_float, vp]),
         "copy_blocks": (c_int, [vp, vp, vp, c_int, c_int, c_size, vp]),
@@ -186,6 +190,40 @@ def paged_attention_decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale
             Hq, Hkv, D, bs, float(scale), _dt(q, "q"), _dt(k_pool, "k_pool"),
             float(k_scale), float(v_scale), ws_ptr, ws_bytes, _stream_ptr(stream, q.device))
     _check(st, "paged_attention_decode")
+    return out
+
+
+# scratch bytes of paged_attention_decode_noalloc (PKV_NOALLOC_WORKSPACE_BYTES)
+NOALLOC_WORKSPACE_BYTES = 32 * 1024 * 1024
+
+
+def paged_attention_decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_lens, scale,
+                                   k_scale=1.0, v_scale=1.0, stream=None):
+    """``paged_attention_decode`` for callers that cannot allocate device memory
+    where they decode (a plug-in inside a runtime that owns all device memory, a
+    serving loop whose memory plan is fixed at start-up): the split-KV scratch is
+    a fixed 32 MiB array inside the library (per GPU), so no workspace is passed
+    and nothing is allocated. Calls on one device share that array and must not
+    overlap on the GPU; the first call on a device should come before any stream
+    capture. Refuses batches with ``B * Hq * 2 * (D + 2) * 4 > NOALLOC_WORKSPACE_BYTES``.
+    """
+    lib = load_library()
+    for t, n in ((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
+                 (block_tables, "block_tables"), (seq_lens, "seq_lens")):
+        _cuda(t, n)
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_pool.shape
+    need = B * Hq * 2 * (D + 2) * 4
+    if need > NOALLOC_WORKSPACE_BYTES:
+        raise PagedKVError(-1, f"paged_attention_decode_noalloc: batch needs {need} bytes of "
+                               f"scratch, the fixed array holds {NOALLOC_WORKSPACE_BYTES}")
+    with _on_device(q.device):
+        st = lib.paged_attention_decode_noalloc(
+            out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+            block_tables.data_ptr(), seq_lens.data_ptr(), B, block_tables.shape[1], NB,
+            Hq, Hkv, D, bs, float(scale), _dt(q, "q"), _dt(k_pool, "k_pool"),
+            float(k_scale), float(v_scale), _stream_ptr(stream, q.device))
+    _check(st, "paged_attention_decode_noalloc")
     return out
 
 

@@ -21,6 +21,7 @@ CUDA_SOURCES = [
     "pkv_decode_f32.cu",
     "pkv_decode_bf16.cu",
     "pkv_decode_e4m3.cu",
+    "pkv_decode_noalloc.cu",
 ]
 CXX_SOURCES = ["block_manager.cpp"]
 
