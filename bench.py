@@ -173,13 +173,7 @@ def build_state(w, device):
     if w.kv_dtype == "e4m3":
         ks, vs = w.fp8_scales(k_src, v_src, k_new, v_new)
     cache = PagedKVCache(w.NB, w.Hq, w.Hkv, w.D, w.bs, KV_TORCH[w.kv_dtype], w.free_order, device)
-    if w.kv_dtype == "e4m3":
-        tok = lambda x: x.to(device).permute(0, 2, 1, 3).reshape(w.NB * w.bs, w.Hkv, w.D).contiguous()
-        slots = torch.arange(w.NB * w.bs, dtype=torch.int64, device=device)
-        pkv.reshape_and_cache(tok(k_src), tok(v_src), cache.k_pool, cache.v_pool, slots, ks, vs)
-    else:
-        cache.k_pool.copy_(k_src.to(device))
-        cache.v_pool.copy_(v_src.to(device))
+    cache.load(k_src, v_src, ks, vs)
     cache.apply_copies(cache.replay(w.script))
     plan = cache.plan_step(w.step_seqs, max_blocks=w.max_blocks_per_seq)
     torch.cuda.synchronize()

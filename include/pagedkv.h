@@ -29,12 +29,19 @@
  *     pool, a wait that gave up) never trap: the offending access is skipped and
  *     a sticky device error word is set; read it with pkv_get_device_error().
  *
- * KV pool layout (a reading: the glossary's example shows one head as
- * key_pool[block, slot, dim]): k_pool and v_pool are each
- *     [num_blocks][num_kv_heads][block_size][head_dim]
- * contiguous, so one (block, kv head) tile is block_size*head_dim contiguous
- * elements. Element type: float32, bfloat16, or E4M3 bytes (OCP FP8, value =
- * code * per-tensor scale).
+ * KV pool layout. The pages show one head as key_pool[block, slot, dim] and
+ * say no more; here each pool is [num_blocks][num_kv_heads][tile], one
+ * contiguous tile of block_size*head_dim elements per (block, kv head), laid
+ * out for the attention kernel:
+ *     K tile: [head_dim/X][block_size][X]   X = 16 bytes of elements
+ *             (4 float32, 8 bfloat16, 16 E4M3): "chunk plane" j holds dims
+ *             jX..jX+X-1 of every token of the block;
+ *     V tile: [head_dim][block_size]        transposed: one row per dim.
+ * So K element (blk, h, t, d) is at ((blk*Hkv + h)*(D/X) + d/X)*bs*X + t*X + d%X
+ * and V element (blk, h, t, d) at ((blk*Hkv + h)*D + d)*bs + t. Element type:
+ * float32, bfloat16, or E4M3 bytes (OCP FP8, value = code * per-tensor scale).
+ * A whole block (every head, K and V) is num_kv_heads*block_size*head_dim
+ * elements per pool, contiguous.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -86,7 +93,7 @@ const char* pkv_last_error_string(void);
  *
  *   out           device, [num_seqs][num_heads][head_dim], dtype q_dtype, written
  *   q             device, [num_seqs][num_heads][head_dim], dtype q_dtype
- *   k_pool/v_pool device, pool layout above, dtype kv_dtype, 16-byte aligned
+ *   k_pool/v_pool device, pool layouts above, dtype kv_dtype, 16-byte aligned
  *   block_tables  device int32 [num_seqs][max_blocks_per_seq]; entries past
  *                 ceil(L/block_size) are not read
  *   seq_lens      device int32 [num_seqs], 0 <= L <= max_blocks_per_seq*block_size
@@ -126,8 +133,9 @@ size_t paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim,
  * For each token i < num_tokens with s = slot_mapping[i]:
  *     s < 0          : padding, skipped
  *     s >= num_blocks*block_size : skipped, device error PKV_ERR_OUT_OF_RANGE
- *     otherwise      : k_pool[s/block_size][h][s%block_size][:] = k[i][h][:]
- *                      (same for v) for every kv head h.
+ *     otherwise      : K and V of token i, every kv head h, are stored as
+ *                      element (s/block_size, h, s%block_size, :) of the
+ *                      pools (layouts above).
  * With cache_dtype E4M3 the stored byte is round-to-nearest-even, saturating
  * E4M3 of (x / k_scale) (resp. v_scale), the division in IEEE float32.
  *

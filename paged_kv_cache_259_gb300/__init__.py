@@ -25,7 +25,7 @@ __all__ = [
     "PagedKVError", "paged_attention_decode", "paged_attention_workspace_size",
     "paged_attention_decode_noalloc", "NOALLOC_WORKSPACE_BYTES",
     "reshape_and_cache", "copy_blocks", "get_device_error", "BlockManager",
-    "library_path", "load_library", "PKV_F32", "PKV_BF16", "PKV_E4M3",
+    "library_path", "load_library", "pool_shapes", "PKV_F32", "PKV_BF16", "PKV_E4M3",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -149,6 +149,33 @@ class _on_device:
             torch.cuda.set_device(self.prev)
 
 
+def pool_shapes(num_blocks, num_kv_heads, block_size, head_dim, dtype):
+    """Tensor shapes of the K and V pools in the library's layout.
+
+    K: ``[NB, Hkv, D // X, bs, X]`` (X = 16 bytes of elements), V:
+    ``[NB, Hkv, D, bs]`` (transposed per block). Each (block, head) tile is
+    contiguous; see ``include/pagedkv.h``.
+    """
+    esize = torch.empty((), dtype=dtype).element_size()
+    x = 16 // esize
+    if head_dim % x:
+        raise ValueError(f"head_dim must be a multiple of {x} for {dtype}")
+    return ((num_blocks, num_kv_heads, head_dim // x, block_size, x),
+            (num_blocks, num_kv_heads, head_dim, block_size))
+
+
+def _pool_dims(k_pool, v_pool):
+    """(NB, Hkv, bs, D) of pools in the library layout; raise on a mismatch."""
+    if k_pool.dim() != 5 or v_pool.dim() != 4 or k_pool.dtype != v_pool.dtype:
+        raise ValueError("pools must be K [NB, Hkv, D/X, bs, X] and V [NB, Hkv, D, bs] "
+                         "of one dtype (see pool_shapes)")
+    NB, Hkv, DX, bs, X = k_pool.shape
+    D = DX * X
+    if X * k_pool.element_size() != 16 or tuple(v_pool.shape) != (NB, Hkv, D, bs):
+        raise ValueError("pool shapes do not match the library layout (see pool_shapes)")
+    return NB, Hkv, bs, D
+
+
 def paged_attention_workspace_size(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq):
     """Bytes of split-KV workspace for the finest split of these sizes."""
     return int(load_library().paged_attention_workspace_size(
@@ -159,9 +186,9 @@ def paged_attention_decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale
                            k_scale=1.0, v_scale=1.0, workspace=None, stream=None):
     """out[b, h] = softmax attention of q[b, h] over sequence b's cached tokens.
 
-    q, out: ``[B, Hq, D]`` (float32 or bfloat16, same dtype); pools
-    ``[NB, Hkv, bs, D]`` (float32/bfloat16 like q, or uint8/float8_e4m3fn for the
-    E4M3 cache with per-tensor ``k_scale``/``v_scale``); block_tables int32
+    q, out: ``[B, Hq, D]`` (float32 or bfloat16, same dtype); pools in the
+    library layout (``pool_shapes``; float32/bfloat16 like q, or uint8/
+    float8_e4m3fn for the E4M3 cache with per-tensor ``k_scale``/``v_scale``); block_tables int32
     ``[B, max_blocks]``; seq_lens int32 ``[B]``; workspace: any CUDA tensor used
     as split-KV scratch (see ``paged_attention_workspace_size``) or None.
     """
@@ -171,12 +198,10 @@ def paged_attention_decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale
         _cuda(t, n)
     if q.dim() != 3 or out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("q and out must be [B, Hq, D] of the same dtype")
-    if k_pool.dim() != 4 or v_pool.shape != k_pool.shape or v_pool.dtype != k_pool.dtype:
-        raise ValueError("pools must both be [NB, Hkv, bs, D] of one dtype")
     if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise TypeError("block_tables and seq_lens must be int32")
     B, Hq, D = q.shape
-    NB, Hkv, bs, D2 = k_pool.shape
+    NB, Hkv, bs, D2 = _pool_dims(k_pool, v_pool)
     if D2 != D or block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.shape != (B,):
         raise ValueError("inconsistent shapes")
     ws_ptr, ws_bytes = None, 0
@@ -212,7 +237,7 @@ def paged_attention_decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_len
                  (block_tables, "block_tables"), (seq_lens, "seq_lens")):
         _cuda(t, n)
     B, Hq, D = q.shape
-    NB, Hkv, bs, _ = k_pool.shape
+    NB, Hkv, bs, _ = _pool_dims(k_pool, v_pool)
     need = B * Hq * 2 * (D + 2) * 4
     if need > NOALLOC_WORKSPACE_BYTES:
         raise PagedKVError(-1, f"paged_attention_decode_noalloc: batch needs {need} bytes of "
@@ -228,7 +253,8 @@ def paged_attention_decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_len
 
 
 def reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, k_scale=1.0, v_scale=1.0, stream=None):
-    """Write k/v ``[T, Hkv, D]`` into the pools at ``slot_mapping`` (int64 ``[T]``)."""
+    """Write k/v ``[T, Hkv, D]`` into the pools (library layout) at ``slot_mapping``
+    (int64 ``[T]``)."""
     lib = load_library()
     for t, n in ((k, "k"), (v, "v"), (k_pool, "k_pool"), (v_pool, "v_pool"),
                  (slot_mapping, "slot_mapping")):
@@ -236,9 +262,9 @@ def reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, k_scale=1.0, v_scale=1
     if slot_mapping.dtype != torch.int64:
         raise TypeError("slot_mapping must be int64")
     T, Hkv, D = k.shape
-    NB, Hkv2, bs, D2 = k_pool.shape
+    NB, Hkv2, bs, D2 = _pool_dims(k_pool, v_pool)
     if v.shape != k.shape or v.dtype != k.dtype or (Hkv2, D2) != (Hkv, D) or \
-            v_pool.shape != k_pool.shape or slot_mapping.shape != (T,):
+            slot_mapping.shape != (T,):
         raise ValueError("inconsistent shapes")
     with _on_device(k.device):
         st = lib.reshape_and_cache(
@@ -254,7 +280,8 @@ def copy_blocks(k_pool, v_pool, src_dst_pairs, stream=None):
     for t, n in ((k_pool, "k_pool"), (v_pool, "v_pool"), (src_dst_pairs, "src_dst_pairs")):
         _cuda(t, n)
     if src_dst_pairs.dtype != torch.int64 or src_dst_pairs.dim() != 2 or \
-            src_dst_pairs.shape[1] != 2 or v_pool.shape != k_pool.shape:
+            src_dst_pairs.shape[1] != 2 or k_pool.shape[0] != v_pool.shape[0] or \
+            k_pool.numel() != v_pool.numel():
         raise ValueError("src_dst_pairs must be int64 [P, 2]; pools of one shape")
     block_bytes = k_pool[0].numel() * k_pool.element_size()
     with _on_device(k_pool.device):

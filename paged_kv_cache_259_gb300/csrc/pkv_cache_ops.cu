@@ -8,8 +8,8 @@
 // copy_blocks: the block copy of copy-on-write ("KV cache paginado...",
 //   "Como funciona"; glossary "Chia sẻ block giữa các chuỗi").
 //
-// Both are plain HBM traffic: 16-byte vector loads and stores, one thread per
-// 16-byte chunk of the destination, grids sized over the SMs.
+// Both are plain HBM traffic: 16-byte vector loads, one thread per 16-byte group
+// of elements, grids sized over the SMs.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -62,22 +62,35 @@ struct ChunkConvert<ST, uint8_t> {
     }
 };
 
+// Cache layout (per block and kv head; see the decode kernels): K as chunk
+// planes [D/X][bs][X] with X = 16 bytes of cache elements, V transposed [D][bs].
+// One thread converts one 16-byte group of X dims of one (token, head): for K it
+// is one 16-byte store into the token's row of plane j, for V X element stores
+// down the token's column of rows jX..jX+X-1.
+template <typename CT>
+__device__ __forceinline__ void store_column(CT* dst, const uint4& v, int stride) {
+    constexpr int CV = 16 / sizeof(CT);
+    const CT* e = reinterpret_cast<const CT*>(&v);
+#pragma unroll
+    for (int i = 0; i < CV; ++i) dst[(size_t)i * stride] = e[i];
+}
+
 template <typename ST, typename CT>
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const ST* __restrict__ k, const ST* __restrict__ v, CT* __restrict__ k_pool,
     CT* __restrict__ v_pool, const int64_t* __restrict__ slots, int num_tokens, int hkv, int d,
     int bs, int num_blocks, float k_scale, float v_scale, int* err) {
     using CC = ChunkConvert<ST, CT>;
-    const int chunks_per_row = d / CC::CV;                 // per (token, head)
-    const long long per_pool = (long long)num_tokens * hkv * chunks_per_row;
+    const int planes = d / CC::CV;                         // 16-byte groups per (token, head)
+    const long long per_pool = (long long)num_tokens * hkv * planes;
     const long long total = 2 * per_pool;
     const long long slot_limit = (long long)num_blocks * bs;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
         const bool is_v = idx >= per_pool;
         long long r = is_v ? idx - per_pool : idx;
-        const int c = (int)(r % chunks_per_row);
-        r /= chunks_per_row;
+        const int j = (int)(r % planes);
+        r /= planes;
         const int h = (int)(r % hkv);
         const int t = (int)(r / hkv);
         const long long slot = slots[t];
@@ -87,10 +100,16 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
             continue;
         }
         const long long blk = slot / bs, off = slot % bs;
-        const ST* src = (is_v ? v : k) + ((long long)t * hkv + h) * d + (long long)c * CC::CV;
-        CT* dst = (is_v ? v_pool : k_pool) + ((blk * hkv + h) * bs + off) * d +
-                  (long long)c * CC::CV;
-        *reinterpret_cast<uint4*>(dst) = CC::run(src, is_v ? v_scale : k_scale);
+        const ST* src = (is_v ? v : k) + ((long long)t * hkv + h) * d + (long long)j * CC::CV;
+        const uint4 val = CC::run(src, is_v ? v_scale : k_scale);
+        const long long tile = (blk * hkv + h) * (long long)d * bs;      // elements
+        if (!is_v) {
+            CT* dst = k_pool + tile + ((long long)j * bs + off) * CC::CV;
+            *reinterpret_cast<uint4*>(dst) = val;
+        } else {
+            CT* dst = v_pool + tile + (long long)j * CC::CV * bs + off;
+            store_column(dst, val, bs);
+        }
     }
 }
 

@@ -1,32 +1,40 @@
-// Decode-step attention over a paged KV cache (CUDA-core variant).
+// Decode-step attention over a paged KV cache.
 //
 // "PagedAttention" (Ultralytics glossary), "Cách phân trang hoạt động": the
 // attention kernel reads a request's keys and values back block by block
 // through its block table, so the cache need not be contiguous. The related-
 // techniques section's FlashAttention item: the score vector is never written to
-// HBM; here it lives in registers/shared memory and softmax is computed online.
+// HBM; here it lives in registers/shared memory and the softmax is computed
+// online (running max m, running sum l, accumulator rescaled by 2^(m_old-m_new);
+// logits pre-multiplied by log2 e so exp2 is used).
 //
-// Work decomposition
+// Cache layout (per pool, per block, per kv head: one contiguous tile of
+// block_size*head_dim elements):
+//   K: [D/X][bs][X]  -- X = 16 bytes of elements; chunk plane j holds dims
+//                       jX..jX+X-1 of every token of the block;
+//   V: [D][bs]       -- transposed: one row per dim, tokens contiguous.
+// Both make the tensor-core operands below load from shared memory with plain,
+// bank-conflict-free 16-byte rows, and keep a tile one 1-D bulk copy.
+//
+// Pipeline (shared by both tile-math variants)
 //   CTA  = (partition p, kv head hk, sequence b). A partition is PB consecutive
-//          logical blocks of the sequence; with one partition per sequence the
-//          CTA writes `out` directly, otherwise it writes a normalised partial
-//          (o_p, m_p, l_p) to the workspace and a second kernel merges them.
-//   warp = an independent streaming engine: warp w takes partition-local blocks
-//          w, w+NW, w+2NW, ... Each has its own STAGES-deep ring of (K tile,
-//          V tile) pairs in shared memory, filled by 1-D bulk copies (TMA engine,
-//          no tensor map) issued by lane 0 and completed on one mbarrier per
-//          stage. A (block, kv head) tile is block_size*head_dim contiguous
-//          elements of the pool, so it is one copy.
-//   lane = a 16-byte column chunk c of a token row and a row group rg; the warp
-//          covers RPP = 32/LPR rows per pass (LPR lanes per row), i.e. one pass
-//          reads 512 contiguous bytes of the tile from shared memory.
+//          logical blocks; with one partition per sequence the CTA writes `out`,
+//          otherwise a normalised partial (o_p, m_p, l_p) to the workspace that
+//          split_reduce_kernel merges.
+//   warp = an independent streaming engine over partition-local blocks
+//          w, w+NW, ...: its own STAGES-deep ring of (K tile, V tile) pairs in
+//          shared memory, filled by 1-D bulk copies (TMA engine, no tensor map)
+//          issued by lane 0 and completed on one mbarrier per stage; block ids
+//          come 32 at a time in registers, double-buffered.
 //
-// Per tile: partial dot products of the lane's chunk with each of the G query
-// heads (GQA: G query heads share the KV head, glossary item "Attention truy vấn
-// theo nhóm"), a butterfly transpose-reduce across the LPR lanes of a row,
-// scores masked beyond the sequence end, an online-softmax update (running
-// max m, running sum l, rescale of the accumulator by 2^(m_old - m_new); logits
-// pre-multiplied by log2 e so exp2 is used), then P.V accumulated per lane.
+// Tile math
+//   SimtMath (MHA, float32 caches): CUDA-core FMAs. Lanes = (token, chunk
+//          plane) for Q.K; lanes own dims for P.V.
+//   MmaMath (GQA G in {2,4,8}, bf16 or E4M3 cache; glossary item "Attention truy
+//          vấn theo nhóm": G query heads share a KV head): the G heads are the
+//          rows of warp-level tensor-core MMAs (m16n8k16, f32 accumulate);
+//          S^T = Q K^T then O += P V per 16-token subtile, P kept in registers.
+//          E4M3 is converted to f16 in registers (exact) and run as f16 MMA.
 //
 // Every spin-wait is bounded (pkv::mbar_wait_bounded); a block-table entry
 // outside the pool is skipped and recorded in the device error word.
@@ -37,6 +45,7 @@
 #include <cuda_fp8.h>
 
 #include <cmath>
+#include <type_traits>
 
 #include "pkv_internal.cuh"
 
@@ -88,95 +97,420 @@ __device__ __forceinline__ void unpack(const uint4& r, float (&f)[8]) {
         f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
 }
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+    uint32_t h;
+    const unsigned short in = (unsigned short)(two_bytes & 0xffffu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(in));
+    return h;
+}
 __device__ __forceinline__ void unpack(const uint4& r, float (&f)[16]) {
     const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const __nv_fp8x2_storage_t pr = (__nv_fp8x2_storage_t)((w[i] >> (16 * j)) & 0xffffu);
-            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
-            const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            const uint32_t h = e4m3x2_to_f16x2(w[i] >> (16 * j));
+            const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&h));
             f[4 * i + 2 * j] = f2.x;
             f[4 * i + 2 * j + 1] = f2.y;
         }
     }
 }
 
-// Sum N per-lane values over aligned groups of W lanes (W a power of two).
-// Afterwards v[0..R) with R = max(1, N/W) holds full sums of value indices
-//   N >= W: j = (lane % W) * R + r
-//   N <  W: j = (lane % W) / (W / N)    (one value, the same in W/N lanes)
-// Each level halves the values a lane carries: the lane keeps one half and
-// receives its partner's sums of that half.
-template <int N, int W>
-struct Butterfly {
-    __device__ __forceinline__ static void run(float* v, int lane) {
-        if constexpr (W > 1) {
-            constexpr int M = W / 2;
-            if constexpr (N > 1) {
-                constexpr int H = N / 2;
-                const bool upper = (lane & M) != 0;
+template <typename KV, int D, int BS>
+struct Layout {
+    static constexpr int kElt = Elt<KV>::kSize;
+    static constexpr int kX = 16 / kElt;          // elements per K chunk (16 bytes)
+    static constexpr int kPlanes = D / kX;        // K chunk planes per tile
+    static constexpr int kTile = BS * D * kElt;   // bytes of one (block, kv head) tile
+    static constexpr int kVRow = BS * kElt;       // bytes of one V row (one dim)
+    static_assert(D % kX == 0, "head_dim must be whole K chunks");
+};
+
+// ============================================================ CUDA-core tile math
+template <typename QT, typename KV, int D, int BS, int G>
+struct SimtMath {
+    using Lay = Layout<KV, D, BS>;
+    static constexpr int X = Lay::kX, NPL = Lay::kPlanes;
+    static constexpr int CPP = 32 / BS;              // chunk planes per warp pass
+    static constexpr int PASSES = NPL / CPP;
+    static constexpr int DPL = D / 32;               // dims per lane for P.V
+    static constexpr int CR = Lay::kVRow / 16;       // 16-byte chunks per V row
+    static constexpr int TPC = X;                    // tokens per V chunk
+    static constexpr bool kQRegs = (G == 1) && (PASSES * X <= 64);
+    static constexpr int kCtaSmemFloats = G * D;     // pre-scaled q rows
+    static constexpr int kWarpSmemFloats = G * BS;   // probabilities of one tile
+    static_assert(NPL % CPP == 0 && D % 32 == 0 && Lay::kVRow % 16 == 0, "shape");
+
+    struct State {
+        float acc[G][DPL];
+        float m[G], l[G];
+        float qr[kQRegs ? PASSES * X : 1];
+    };
+
+    __device__ __forceinline__ static void load_q(float* qs, const Params& p, int b, int hk) {
+        const QT* qb = static_cast<const QT*>(p.q) + ((size_t)b * p.num_heads + (size_t)hk * G) * D;
+        for (int i = threadIdx.x; i < G * D; i += blockDim.x) qs[i] = to_f(qb[i]) * p.qscale;
+    }
+
+    __device__ __forceinline__ static void init(State& st, const float* qs, int lane) {
 #pragma unroll
-                for (int i = 0; i < H; ++i) {
-                    const float send = upper ? v[i] : v[i + H];
-                    const float keep = upper ? v[i + H] : v[i];
-                    v[i] = keep + __shfl_xor_sync(kFull, send, M);
+        for (int g = 0; g < G; ++g) {
+            st.m[g] = -INFINITY;
+            st.l[g] = 0.f;
+#pragma unroll
+            for (int k = 0; k < DPL; ++k) st.acc[g][k] = 0.f;
+        }
+        if constexpr (kQRegs) {
+            const int cp = lane / BS;
+#pragma unroll
+            for (int i = 0; i < PASSES; ++i)
+#pragma unroll
+                for (int x = 0; x < X; ++x) st.qr[i * X + x] = qs[(i * CPP + cp) * X + x];
+        }
+    }
+
+    __device__ __forceinline__ static void tile(State& st, const unsigned char* kt,
+                                                const unsigned char* vt, int ntok, int lane,
+                                                const float* qs, float* pb) {
+        const int t = lane % BS, cp = lane / BS;
+        // ---- scores: lane (t, cp) covers chunk planes cp, cp+CPP, ...
+        float s[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) s[g] = 0.f;
+#pragma unroll
+        for (int i = 0; i < PASSES; ++i) {
+            const int j = i * CPP + cp;
+            float kf[X];
+            unpack(*reinterpret_cast<const uint4*>(kt + (j * BS + t) * 16), kf);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+#pragma unroll
+                for (int x = 0; x < X; ++x) {
+                    const float qv = kQRegs ? st.qr[i * X + x] : qs[g * D + j * X + x];
+                    s[g] = fmaf(qv, kf[x], s[g]);
                 }
-                Butterfly<H, M>::run(v, lane);
-            } else {
-                v[0] += __shfl_xor_sync(kFull, v[0], M);
-                Butterfly<1, M>::run(v, lane);
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            if constexpr (CPP == 2) s[g] += __shfl_xor_sync(kFull, s[g], 16);
+            if (t >= ntok) s[g] = -INFINITY;
+        }
+        // ---- online softmax (every lane keeps every head's m, l)
+        float alpha[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float mx = s[g];
+#pragma unroll
+            for (int msk = BS / 2; msk >= 1; msk >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, msk));
+            const float m_new = fmaxf(st.m[g], mx);        // finite: token 0 is valid
+            alpha[g] = exp2f(st.m[g] - m_new);
+            const float pv = exp2f(s[g] - m_new);
+            st.m[g] = m_new;
+            st.l[g] = st.l[g] * alpha[g] + (cp == 0 ? pv : 0.f);
+            if (cp == 0) pb[g * BS + t] = pv;
+        }
+        __syncwarp();
+        // ---- P.V: lane owns dims lane, lane+32, ...; V row = the dim's tokens
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int k = 0; k < DPL; ++k) st.acc[g][k] *= alpha[g];
+#pragma unroll
+        for (int ch = 0; ch < CR; ++ch) {
+            if (ch * TPC >= ntok) break;
+            const bool partial = (ch + 1) * TPC > ntok;
+#pragma unroll
+            for (int k = 0; k < DPL; ++k) {
+                const int d = lane + 32 * k;
+                float vf[TPC];
+                unpack(*reinterpret_cast<const uint4*>(vt + d * Lay::kVRow + ch * 16), vf);
+                if (partial) {
+#pragma unroll
+                    for (int x = 0; x < TPC; ++x)
+                        if (ch * TPC + x >= ntok) vf[x] = 0.f;      // unwritten slots
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+#pragma unroll
+                    for (int x4 = 0; x4 < TPC / 4; ++x4) {
+                        const float4 pp = *reinterpret_cast<const float4*>(pb + g * BS + ch * TPC + 4 * x4);
+                        st.acc[g][k] = fmaf(pp.x, vf[4 * x4 + 0], st.acc[g][k]);
+                        st.acc[g][k] = fmaf(pp.y, vf[4 * x4 + 1], st.acc[g][k]);
+                        st.acc[g][k] = fmaf(pp.z, vf[4 * x4 + 2], st.acc[g][k]);
+                        st.acc[g][k] = fmaf(pp.w, vf[4 * x4 + 3], st.acc[g][k]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    }
+
+    __device__ __forceinline__ static void finish(State& st, float* cm, float* cl, float* cacc,
+                                                  int w, int lane, bool dead) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float l = st.l[g];
+#pragma unroll
+            for (int msk = 16; msk >= 1; msk >>= 1) l += __shfl_xor_sync(kFull, l, msk);
+            if (lane == 0) {
+                cm[w * G + g] = dead ? -INFINITY : st.m[g];
+                cl[w * G + g] = dead ? 0.f : l;
+            }
+#pragma unroll
+            for (int k = 0; k < DPL; ++k) cacc[(w * G + g) * D + lane + 32 * k] = dead ? 0.f : st.acc[g][k];
+        }
+    }
+};
+
+// ============================================================ tensor-core tile math
+__device__ __forceinline__ void mma16816(bool f16, float& d0, float& d1, uint32_t a0, uint32_t a2,
+                                         uint32_t b0, uint32_t b1, float c0, float c1) {
+    float j0, j1;
+    if (f16)
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%10,%11,%12,%13};"
+            : "=f"(d0), "=f"(d1), "=f"(j0), "=f"(j1)
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(0.f),
+              "f"(0.f));
+    else
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%10,%11,%12,%13};"
+            : "=f"(d0), "=f"(d1), "=f"(j0), "=f"(j1)
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(0.f),
+              "f"(0.f));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Fragment roles (lane = 4r + c): rows of every MMA are query heads (row r < G
+// real, the rest zero); S^T tile u (8 tokens) column 2c+e; O column 2c+e of
+// n-tile nt is dim 8nt+2c+e.
+//   bf16: token of S column (u, 2c+e) = 16h + 8u + 2c + e; K B-operand by
+//         ldmatrix from the chunk planes, V B-operand by ldmatrix from V rows.
+//   E4M3: Q.K dims are permuted inside each 16-dim k-step (lane c's four
+//         k-values {2c,2c+1,2c+8,2c+9} are dims 4c..4c+3, one 32-bit load), and
+//         so are tokens inside each 16-token subtile (S column (u, 2c+e) is token
+//         16h + 4c + 2u + e) so that P's A-fragment needs V bytes 4c..4c+3 of a
+//         V row: again one 32-bit load. Q uses the same dim permutation.
+template <typename KV, int D, int BS, int G>
+struct MmaMath {
+    using Lay = Layout<KV, D, BS>;
+    static constexpr bool F8 = std::is_same<KV, uint8_t>::value;
+    static constexpr int KS = D / 16;                // k-steps of Q.K
+    static constexpr int NT = D / 8;                 // n-tiles of P.V
+    static constexpr int SUB = BS / 16;              // 16-token subtiles per block
+    static constexpr int kCtaSmemFloats = G * D;     // raw q rows
+    static constexpr int kWarpSmemFloats = 0;
+    static_assert(G >= 2 && G <= 8 && BS % 16 == 0 && D % 16 == 0, "mma shape");
+
+    struct State {
+        uint32_t qa[KS][2];                          // A fragments of Q (a0, a2)
+        float o[NT][2];
+        float m, l;
+    };
+
+    __device__ __forceinline__ static void load_q(float* qs, const Params& p, int b, int hk) {
+        const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(p.q) +
+                                  ((size_t)b * p.num_heads + (size_t)hk * G) * D;
+        for (int i = threadIdx.x; i < G * D; i += blockDim.x) qs[i] = __bfloat162float(qb[i]);
+    }
+
+    __device__ __forceinline__ static void init(State& st, const float* qs, int lane) {
+        const int r = lane >> 2, c = lane & 3;
+        const bool live = r < G;
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+            float q0 = 0.f, q1 = 0.f, q2 = 0.f, q3 = 0.f;
+            const int d0 = F8 ? 16 * s + 4 * c : 16 * s + 2 * c;
+            const int d2 = F8 ? 16 * s + 4 * c + 2 : 16 * s + 8 + 2 * c;
+            if (live) {
+                q0 = qs[r * D + d0];
+                q1 = qs[r * D + d0 + 1];
+                q2 = qs[r * D + d2];
+                q3 = qs[r * D + d2 + 1];
+            }
+            st.qa[s][0] = F8 ? pack_f16(q0, q1) : pack_bf16(q0, q1);
+            st.qa[s][1] = F8 ? pack_f16(q2, q3) : pack_bf16(q2, q3);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) st.o[nt][0] = st.o[nt][1] = 0.f;
+        st.m = -INFINITY;
+        st.l = 0.f;
+    }
+
+    __device__ __forceinline__ static void tile(State& st, const unsigned char* kt,
+                                                const unsigned char* vt, int ntok, int lane,
+                                                float qscale, const float*, float*) {
+        const int r = lane >> 2, c = lane & 3;
+        const uint32_t kbase = smem_addr(kt), vbase = smem_addr(vt);
+#pragma unroll
+        for (int h = 0; h < SUB; ++h) {
+            if (16 * h >= ntok) break;                       // warp-uniform
+            // ---- S^T = Q K^T for 16 tokens (two n-tiles of 8)
+            float s[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t b[2][2];
+                if constexpr (F8) {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int tok = 16 * h + 4 * (r >> 1) + 2 * u + (r & 1);
+                        const uint32_t w4 =
+                            *reinterpret_cast<const uint32_t*>(kt + (ks * BS + tok) * 16 + 4 * c);
+                        b[u][0] = e4m3x2_to_f16x2(w4);
+                        b[u][1] = e4m3x2_to_f16x2(w4 >> 16);
+                    }
+                } else {
+                    const int m = lane >> 3, rr = lane & 7;
+                    const int plane = 2 * ks + (m & 1);
+                    const int tok = 16 * h + 8 * (m >> 1) + rr;
+                    ldsm_x4(kbase + (plane * BS + tok) * 16, b[0][0], b[0][1], b[1][0], b[1][1]);
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+                    mma16816(F8, s[u][0], s[u][1], st.qa[ks][0], st.qa[ks][1], b[u][0], b[u][1],
+                             s[u][0], s[u][1]);
+            }
+            // ---- online softmax on this lane's 4 scores of head row r
+            float mx = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tok = F8 ? 16 * h + 4 * c + 2 * u + e : 16 * h + 8 * u + 2 * c + e;
+                    s[u][e] = tok < ntok ? s[u][e] * qscale : -INFINITY;
+                    mx = fmaxf(mx, s[u][e]);
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+            const float m_new = fmaxf(st.m, mx);             // finite: token 16h is valid
+            const float alpha = exp2f(st.m - m_new);
+            float pr[2][2];
+            float psum = 0.f;
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    pr[u][e] = exp2f(s[u][e] - m_new);
+                    psum += pr[u][e];
+                }
+            st.l = st.l * alpha + psum;
+            st.m = m_new;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                st.o[nt][0] *= alpha;
+                st.o[nt][1] *= alpha;
+            }
+            const uint32_t pa0 = F8 ? pack_f16(pr[0][0], pr[0][1]) : pack_bf16(pr[0][0], pr[0][1]);
+            const uint32_t pa2 = F8 ? pack_f16(pr[1][0], pr[1][1]) : pack_bf16(pr[1][0], pr[1][1]);
+            // ---- O += P V (V rows = dims); unwritten slots beyond ntok are zeroed
+            const int tail = ntok - 16 * h;                  // valid tokens in this subtile
+#pragma unroll
+            for (int nt = 0; nt < NT; nt += 2) {
+                uint32_t b[2][2];
+                if constexpr (F8) {
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        const int d = 8 * (nt + x) + r;
+                        uint32_t w4 = *reinterpret_cast<const uint32_t*>(vt + d * Lay::kVRow + 16 * h + 4 * c);
+                        if (tail < 16) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (4 * c + e >= tail) w4 &= ~(0xffu << (8 * e));
+                        }
+                        b[x][0] = e4m3x2_to_f16x2(w4);
+                        b[x][1] = e4m3x2_to_f16x2(w4 >> 16);
+                    }
+                } else {
+                    const int m = lane >> 3, rr = lane & 7;
+                    const int d = 8 * (nt + (m >> 1)) + rr;
+                    const int tok = 16 * h + 8 * (m & 1);
+                    ldsm_x4(vbase + (d * BS + tok) * 2, b[0][0], b[0][1], b[1][0], b[1][1]);
+                    if (tail < 16) {                         // lane holds tokens 2c,2c+1 (+8)
+#pragma unroll
+                        for (int x = 0; x < 2; ++x)
+#pragma unroll
+                            for (int y = 0; y < 2; ++y) {
+                                const int t0 = 8 * y + 2 * c;
+                                if (t0 >= tail) b[x][y] = 0u;
+                                else if (t0 + 1 >= tail) b[x][y] &= 0x0000ffffu;
+                            }
+                    }
+                }
+#pragma unroll
+                for (int x = 0; x < 2; ++x)
+                    mma16816(F8, st.o[nt + x][0], st.o[nt + x][1], pa0, pa2, b[x][0], b[x][1],
+                             st.o[nt + x][0], st.o[nt + x][1]);
+            }
+        }
+    }
+
+    __device__ __forceinline__ static void finish(State& st, float* cm, float* cl, float* cacc,
+                                                  int w, int lane, bool dead) {
+        const int r = lane >> 2, c = lane & 3;
+        float l = st.l;
+        l += __shfl_xor_sync(kFull, l, 1);
+        l += __shfl_xor_sync(kFull, l, 2);
+        if (r < G) {
+            if (c == 0) {
+                cm[w * G + r] = dead ? -INFINITY : st.m;
+                cl[w * G + r] = dead ? 0.f : l;
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                cacc[(w * G + r) * D + 8 * nt + 2 * c] = dead ? 0.f : st.o[nt][0];
+                cacc[(w * G + r) * D + 8 * nt + 2 * c + 1] = dead ? 0.f : st.o[nt][1];
             }
         }
     }
 };
 
-template <typename KV, int D, int BS, int G, int NW>
-struct Shape {
-    static constexpr int kElt = Elt<KV>::kSize;
-    static constexpr int kVec = 16 / kElt;                  // elements per 16-byte chunk
-    static constexpr int kLpr = D / kVec;                   // lanes per token row
-    static constexpr int kRpp = 32 / kLpr;                  // rows per warp pass
-    static constexpr int kTpl = BS / kRpp;                  // tokens per lane per tile
-    static constexpr int kRowBytes = D * kElt;
-    static constexpr int kTile = BS * kRowBytes;            // one (block, kv head) tile
-    static constexpr int kNv = G * kTpl;                    // partial scores per lane
-    static constexpr int kR = kNv >= kLpr ? kNv / kLpr : 1; // reduced scores per lane
-    static constexpr int kGbs = G * BS;                     // scores per tile
-    static constexpr int kSpl = kGbs >= 32 ? kGbs / 32 : 1; // scores per softmax lane
-    static constexpr int kActive = kGbs >= 32 ? 32 : kGbs;  // softmax lanes
-    static constexpr int kGs = BS / kSpl;                   // softmax lanes per head
+// ============================================================ pipeline skeleton
+template <class Math, int D, int BS, int G, int NW>
+struct Pipe {
+    using Lay = typename Math::Lay;
+    static constexpr int kTile = Lay::kTile;
     // about 96 KB of ring per CTA (two CTAs per SM); at least one stage per warp
     // (a 16 KB tile, float32 D128 with 32-token blocks, gets a single stage)
     static constexpr int kStages = (98304 / (NW * 2 * kTile)) < 1 ? 1
                                    : (98304 / (NW * 2 * kTile)) > 8 ? 8
                                    : (98304 / (NW * 2 * kTile));
     static constexpr int kRingBytes = NW * kStages * 2 * kTile;
-    static constexpr int kSmem = kRingBytes + NW * kStages * 8   // mbarriers
-                                 + NW * kStages * 4              // stage block ids
-                                 + NW * kGbs * 4                 // scores / probabilities
-                                 + NW * G * 4;                   // per-head rescale factors
-    static_assert(32 % kLpr == 0 && kLpr >= 1, "row must map onto whole lanes");
-    static_assert(BS % kRpp == 0, "block must hold whole warp passes");
+    static constexpr int kSmem = kRingBytes + NW * kStages * 8     // mbarriers
+                                 + NW * kStages * 4                // stage block ids
+                                 + Math::kCtaSmemFloats * 4
+                                 + NW * Math::kWarpSmemFloats * 4;
     static_assert(NW * G * (D + 2) * 4 <= kRingBytes, "combine area must fit in the ring");
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
-    static_assert(kGbs % kSpl == 0 && BS % kSpl == 0, "softmax lanes");
 };
 
-template <typename QT, typename KV, int D, int BS, int G, int NW>
+template <class Math, typename QT, int D, int BS, int G, int NW>
 __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
-    using S = Shape<KV, D, BS, G, NW>;
-    constexpr int VEC = S::kVec, LPR = S::kLpr, RPP = S::kRpp, TPL = S::kTpl;
-    constexpr int TILE = S::kTile, ST = S::kStages, GBS = S::kGbs;
-    constexpr int SPL = S::kSpl, ACTIVE = S::kActive, GS = S::kGs;
+    using P = Pipe<Math, D, BS, G, NW>;
+    constexpr int TILE = P::kTile, ST = P::kStages;
 
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kRingBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::kRingBytes);
     int32_t* stage_id = reinterpret_cast<int32_t*>(bars + NW * ST);
-    float* sc = reinterpret_cast<float*>(stage_id + NW * ST);
-    float* alph = sc + NW * GBS;
+    float* qs = reinterpret_cast<float*>(stage_id + NW * ST);
+    float* wsm = qs + Math::kCtaSmemFloats;
 
     const int part = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     int L = p.seq_lens[b];
@@ -192,31 +526,18 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
     const int nbp = max(0, min(PB, nblk - blk0));           // blocks in this partition
 
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    const int c = lane % LPR, rg = lane / LPR;
 
     if (lane == 0) {
 #pragma unroll
         for (int s = 0; s < ST; ++s) mbar_init(smem_addr(&bars[w * ST + s]), 1);
         fence_mbar_init();
     }
-    __syncwarp();
+    Math::load_q(qs, p, b, hk);
+    __syncthreads();
 
-    // query rows of the G heads that share kv head hk, pre-scaled
-    float qf[G][VEC];
-    {
-        const QT* qb = static_cast<const QT*>(p.q) + ((size_t)b * p.num_heads + (size_t)hk * G) * D;
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) qf[g][v] = to_f(qb[g * D + c * VEC + v]) * p.qscale;
-    }
-
-    float acc[G][VEC];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) acc[g][v] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
+    typename Math::State st;
+    Math::init(st, qs, lane);
+    float* pb = wsm + w * Math::kWarpSmemFloats;
 
     const int nk = nbp > w ? (nbp - w + NW - 1) / NW : 0;  // this warp's blocks
     const int32_t* bt_row = p.block_tables + (size_t)b * p.max_blocks + blk0 + w;
@@ -278,82 +599,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
         if (id >= 0) {
             const int ntok = min(BS, L - (blk0 + w + k * NW) * BS);
             const unsigned char* kt = ring + (size_t)((w * ST + s) * 2) * TILE;
-            const unsigned char* vt = kt + TILE;
-
-            // ---- scores: partial dots of this lane's chunk, then reduce over the row's lanes
-            float part_s[S::kNv];
-#pragma unroll
-            for (int i = 0; i < TPL; ++i) {
-                const int t = i * RPP + rg;
-                float kf[VEC];
-                unpack(*reinterpret_cast<const uint4*>(kt + t * S::kRowBytes + c * 16), kf);
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float a = 0.f;
-#pragma unroll
-                    for (int v = 0; v < VEC; ++v) a = fmaf(qf[g][v], kf[v], a);
-                    part_s[g * TPL + i] = a;
-                }
-            }
-            Butterfly<S::kNv, LPR>::run(part_s, lane);
-            float* scw = sc + w * GBS;
-#pragma unroll
-            for (int r = 0; r < S::kR; ++r) {
-                const int j = S::kNv >= LPR ? c * S::kR + r : c / (LPR / S::kNv);
-                const bool leader = S::kNv >= LPR || (c % (LPR / S::kNv)) == 0;
-                const int g = j / TPL, t = (j % TPL) * RPP + rg;
-                if (leader) scw[g * BS + t] = t < ntok ? part_s[r] : -INFINITY;
-            }
-            __syncwarp();
-
-            // ---- online softmax over the tile (lane owns SPL scores of one head)
-            float sv[SPL];
-            float tmax = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < SPL; ++i) {
-                sv[i] = lane < ACTIVE ? scw[lane * SPL + i] : -INFINITY;
-                tmax = fmaxf(tmax, sv[i]);
-            }
-#pragma unroll
-            for (int msk = GS / 2; msk >= 1; msk >>= 1)
-                tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, msk));
-            if (lane < ACTIVE) {
-                const float m_new = fmaxf(m_run, tmax);
-                const float alpha = exp2f(m_run - m_new);
-                float psum = 0.f;
-#pragma unroll
-                for (int i = 0; i < SPL; ++i) {
-                    const float pv = exp2f(sv[i] - m_new);
-                    psum += pv;
-                    scw[lane * SPL + i] = pv;
-                }
-                l_run = l_run * alpha + psum;
-                m_run = m_new;
-                if (lane % GS == 0) alph[w * G + (lane * SPL) / BS] = alpha;
-            }
-            __syncwarp();
-
-            // ---- P.V into this lane's chunk of each head's accumulator
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float a = alph[w * G + g];
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) acc[g][v] *= a;
-            }
-#pragma unroll
-            for (int i = 0; i < TPL; ++i) {
-                const int t = i * RPP + rg;
-                if (t < ntok) {
-                    float vf[VEC];
-                    unpack(*reinterpret_cast<const uint4*>(vt + t * S::kRowBytes + c * 16), vf);
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        const float pg = scw[g * BS + t];
-#pragma unroll
-                        for (int v = 0; v < VEC; ++v) acc[g][v] = fmaf(pg, vf[v], acc[g][v]);
-                    }
-                }
-            }
+            if constexpr (Math::kWarpSmemFloats > 0)
+                Math::tile(st, kt, kt + TILE, ntok, lane, qs, pb);
+            else
+                Math::tile(st, kt, kt + TILE, ntok, lane, p.qscale, qs, pb);
         }
         __syncwarp();
         if (k + ST < nk) {
@@ -371,36 +620,13 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
         const int last = min(nk, k + ST);
         for (int kk = k; kk < last; ++kk)
             (void)mbar_wait_bounded(smem_addr(&bars[w * ST + (kk % ST)]), (kk / ST) & 1, p.err);
-        m_run = -INFINITY;
-        l_run = 0.f;
     }
-
-    // ---- warp totals: l over the head's softmax lanes, acc over row groups
-#pragma unroll
-    for (int msk = GS / 2; msk >= 1; msk >>= 1) l_run += __shfl_xor_sync(kFull, l_run, msk);
-#pragma unroll
-    for (int msk = LPR; msk < 32; msk <<= 1)
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) acc[g][v] += __shfl_xor_sync(kFull, acc[g][v], msk);
 
     __syncthreads();                                        // every warp is done with its ring
     float* cm = reinterpret_cast<float*>(ring);             // [NW][G]
     float* cl = cm + NW * G;                                // [NW][G]
     float* cacc = cl + NW * G;                              // [NW][G][D]
-    if (lane < ACTIVE && lane % GS == 0) {
-        const int g = (lane * SPL) / BS;
-        cm[w * G + g] = aborted ? -INFINITY : m_run;
-        cl[w * G + g] = aborted ? 0.f : l_run;
-    }
-    if (rg == 0) {
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int v = 0; v < VEC; ++v)
-                cacc[(w * G + g) * D + c * VEC + v] = aborted ? 0.f : acc[g][v];
-    }
+    Math::finish(st, cm, cl, cacc, w, lane, aborted);
     __syncthreads();
 
     // ---- merge the warps (and write out, or the partition's partial)
@@ -510,25 +736,25 @@ inline int choose_part_blocks(const Args& a, int tile_bytes, int ctas_per_sm, in
     return PB;
 }
 
-template <typename QT, typename KV, int D, int BS, int G>
+template <class Math, typename QT, int D, int BS, int G>
 int launch_variant(const Args& a) {
-    using S = Shape<KV, D, BS, G, kNumWarps>;
-    auto kern = paged_decode_kernel<QT, KV, D, BS, G, kNumWarps>;
+    using P = Pipe<Math, D, BS, G, kNumWarps>;
+    auto kern = paged_decode_kernel<Math, QT, D, BS, G, kNumWarps>;
     static int attr_done[kMaxDevices];      // 0 = not yet, else occupancy + 1
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevices)
         return cuda_fail("decode: current device", cudaErrorInvalidDevice);
     if (!attr_done[dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             S::kSmem);
+                                             P::kSmem);
         if (e != cudaSuccess) return cuda_fail("decode: set max dynamic shared memory", e);
         int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kNumWarps * 32, S::kSmem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kNumWarps * 32, P::kSmem);
         if (e != cudaSuccess) return cuda_fail("decode: occupancy query", e);
         attr_done[dev] = occ + 1;
     }
     int parts = 1;
-    const int PB = choose_part_blocks(a, S::kTile, attr_done[dev] - 1, &parts);
+    const int PB = choose_part_blocks(a, P::kTile, attr_done[dev] - 1, &parts);
 
     Params p;
     p.out = a.out;
@@ -551,7 +777,7 @@ int launch_variant(const Args& a) {
     p.v_scale = a.v_scale;
 
     dim3 grid(parts, a.num_kv_heads, a.num_seqs);
-    kern<<<grid, kNumWarps * 32, S::kSmem, a.stream>>>(p);
+    kern<<<grid, kNumWarps * 32, P::kSmem, a.stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail("decode: kernel launch", e);
     if (parts > 1) {
@@ -562,13 +788,22 @@ int launch_variant(const Args& a) {
     return PKV_OK;
 }
 
+// float32 caches: CUDA cores for every group size. bf16 / E4M3 caches: CUDA
+// cores for MHA (G = 1, one flop per byte), tensor cores for G in {2, 4, 8}.
 template <typename QT, typename KV, int D, int BS>
 int dispatch_group(const Args& a) {
+    constexpr bool simt_only = std::is_same<KV, float>::value;
     switch (a.num_heads / a.num_kv_heads) {
-        case 1: return launch_variant<QT, KV, D, BS, 1>(a);
-        case 2: return launch_variant<QT, KV, D, BS, 2>(a);
-        case 4: return launch_variant<QT, KV, D, BS, 4>(a);
-        case 8: return launch_variant<QT, KV, D, BS, 8>(a);
+        case 1: return launch_variant<SimtMath<QT, KV, D, BS, 1>, QT, D, BS, 1>(a);
+        case 2:
+            if constexpr (simt_only) return launch_variant<SimtMath<QT, KV, D, BS, 2>, QT, D, BS, 2>(a);
+            else return launch_variant<MmaMath<KV, D, BS, 2>, QT, D, BS, 2>(a);
+        case 4:
+            if constexpr (simt_only) return launch_variant<SimtMath<QT, KV, D, BS, 4>, QT, D, BS, 4>(a);
+            else return launch_variant<MmaMath<KV, D, BS, 4>, QT, D, BS, 4>(a);
+        case 8:
+            if constexpr (simt_only) return launch_variant<SimtMath<QT, KV, D, BS, 8>, QT, D, BS, 8>(a);
+            else return launch_variant<MmaMath<KV, D, BS, 8>, QT, D, BS, 8>(a);
         default: return PKV_ERR_UNSUPPORTED;
     }
 }

@@ -20,7 +20,7 @@ import numpy as np
 import torch
 
 from . import (BlockManager, copy_blocks, paged_attention_decode,
-               paged_attention_workspace_size, reshape_and_cache)
+               paged_attention_workspace_size, pool_shapes, reshape_and_cache)
 
 
 @dataclass
@@ -56,10 +56,28 @@ class PagedKVCache:
         self.num_kv_heads = num_kv_heads
         self.head_dim = head_dim
         self.block_size = block_size
-        shape = (num_blocks, num_kv_heads, block_size, head_dim)
-        self.k_pool = torch.empty(shape, dtype=kv_dtype, device=self.device)
-        self.v_pool = torch.empty(shape, dtype=kv_dtype, device=self.device)
+        k_shape, v_shape = pool_shapes(num_blocks, num_kv_heads, block_size, head_dim, kv_dtype)
+        self.k_pool = torch.empty(k_shape, dtype=kv_dtype, device=self.device)
+        self.v_pool = torch.empty(v_shape, dtype=kv_dtype, device=self.device)
         self.bm = BlockManager(num_blocks, block_size, free_order)
+
+    def load(self, k_vals, v_vals, k_scale=1.0, v_scale=1.0):
+        """Fill every slot from values given as ``[NB, Hkv, bs, D]`` (block,
+        head, slot, dim), through the library's slot write (which lays them out
+        and, for an E4M3 cache, quantises them)."""
+        NB, Hkv, bs, D = self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim
+        slots = torch.arange(NB * bs, dtype=torch.int64, device=self.device)
+        tok = lambda x: x.to(self.device).permute(0, 2, 1, 3).reshape(NB * bs, Hkv, D).contiguous()
+        reshape_and_cache(tok(k_vals), tok(v_vals), self.k_pool, self.v_pool, slots, k_scale, v_scale)
+
+    def k_view(self):
+        """K pool as ``[NB, Hkv, bs, D]`` (a copy, for inspection and tests)."""
+        NB, Hkv, bs, D = self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim
+        return self.k_pool.permute(0, 1, 3, 2, 4).reshape(NB, Hkv, bs, D)
+
+    def v_view(self):
+        """V pool as ``[NB, Hkv, bs, D]`` (a copy, for inspection and tests)."""
+        return self.v_pool.transpose(2, 3).contiguous()
 
     def replay(self, script):
         """Apply block-manager operations; returns the CoW pairs raised (in order)."""

@@ -52,15 +52,8 @@ def run_gpu(inp, workspace=True, relabel=None, device="cuda"):
         v_src = torch.empty_like(v_src)
         k_src[perm] = inp.k_src
         v_src[perm] = inp.v_src
-    if w.kv_dtype == "e4m3":
-        # fill the E4M3 pools with the library's own quantising slot write
-        tok = lambda x: x.permute(0, 2, 1, 3).reshape(w.NB * w.bs, w.Hkv, w.D)
-        slots = torch.arange(w.NB * w.bs, dtype=torch.int64, device=device)
-        pkv.reshape_and_cache(tok(k_src.to(device)).contiguous(), tok(v_src.to(device)).contiguous(),
-                              cache.k_pool, cache.v_pool, slots, inp.ks, inp.vs)
-    else:
-        cache.k_pool.copy_(k_src.to(device))
-        cache.v_pool.copy_(v_src.to(device))
+    # fill the pools with the library's own slot write (layout, E4M3 quantising)
+    cache.load(k_src, v_src, inp.ks, inp.vs)
     setup_pairs = cache.replay(w.script)
     cache.apply_copies(setup_pairs)
     plan = cache.plan_step(w.step_seqs, max_blocks=w.max_blocks_per_seq)
@@ -144,12 +137,13 @@ def check_cache_writes(inp, g, o, whole_pool=False):
     (or the whole pools)."""
     w = inp.w
     cache = g["cache"]
+    kview, vview = cache.k_view(), cache.v_view()          # [NB, Hkv, bs, D]
     if whole_pool:
-        for which, gp, op in (("k", cache.k_pool, o["k_pool"]), ("v", cache.v_pool, o["v_pool"])):
+        for which, gp, op in (("k", kview, o["k_pool"]), ("v", vview, o["v_pool"])):
             assert torch.equal(stored_bits(gp.cpu()), stored_bits(oracle_stored(inp, op, which)))
         return
     blocks = sorted({d for _, d in o["setup_pairs"] + o["pairs"]})
-    for which, gp, op in (("k", cache.k_pool, o["k_pool"]), ("v", cache.v_pool, o["v_pool"])):
+    for which, gp, op in (("k", kview, o["k_pool"]), ("v", vview, o["v_pool"])):
         if blocks:
             idx = torch.tensor(blocks)
             assert torch.equal(stored_bits(gp[idx.to(gp.device)].cpu()),

@@ -130,17 +130,32 @@ def test_repeated_step_is_idempotent():
     assert torch.equal(out2.float().cpu(), g["out"])
 
 
+def to_layout(kc, vc):
+    """Canonical ``[NB, Hkv, bs, D]`` K/V -> the library's pool layout (plain copies)."""
+    NB, Hkv, bs, D = kc.shape
+    x = 16 // kc.element_size()
+    kl = kc.reshape(NB, Hkv, bs, D // x, x).permute(0, 1, 3, 2, 4).contiguous()
+    vl = vc.transpose(2, 3).contiguous()
+    return kl, vl
+
+
+def from_layout_k(kl):
+    NB, Hkv, DX, bs, x = kl.shape
+    return kl.permute(0, 1, 3, 2, 4).reshape(NB, Hkv, bs, DX * x)
+
+
 def _decode_args(B, Hq, Hkv, D, bs, NB, MB, dtype=torch.bfloat16, seed=0):
     gen = torch.Generator().manual_seed(seed)
     q = torch.randn(B, Hq, D, generator=gen).to(dtype).cuda()
-    kp = torch.randn(NB, Hkv, bs, D, generator=gen).to(dtype).cuda()
-    vp = torch.randn(NB, Hkv, bs, D, generator=gen).to(dtype).cuda()
+    kc = torch.randn(NB, Hkv, bs, D, generator=gen).to(dtype)
+    vc = torch.randn(NB, Hkv, bs, D, generator=gen).to(dtype)
+    kp, vp = to_layout(kc.cuda(), vc.cuda())
     bt = torch.arange(B * MB, dtype=torch.int32).reshape(B, MB).remainder(NB).cuda()
-    return q, kp, vp, bt
+    return q, kp, vp, bt, kc, vc
 
 
 def test_zero_length_sequences_give_zero_rows():
-    q, kp, vp, bt = _decode_args(4, 4, 4, 128, 16, 32, 8)
+    q, kp, vp, bt, _, _ = _decode_args(4, 4, 4, 128, 16, 32, 8)
     lens = torch.tensor([0, 5, 0, 128], dtype=torch.int32, device="cuda")
     out = torch.full_like(q, 7.0)
     pkv.paged_attention_decode(out, q, kp, vp, bt, lens, 0.1)
@@ -149,8 +164,9 @@ def test_zero_length_sequences_give_zero_rows():
     assert torch.isfinite(out).all() and torch.count_nonzero(out[1]) > 0
 
 
-def test_bad_block_id_sets_error_word_and_skips():
-    q, kp, vp, bt = _decode_args(3, 4, 4, 128, 16, 32, 8)
+@pytest.mark.parametrize("Hq", [4, 16])          # CUDA-core (MHA) and tensor-core (GQA) paths
+def test_bad_block_id_sets_error_word_and_skips(Hq):
+    q, kp, vp, bt, kc, vc = _decode_args(3, Hq, 4, 128, 16, 32, 8)
     bt[1, 2] = 32          # == num_blocks: outside the pool
     bt[2, 0] = -7
     lens = torch.tensor([100, 100, 20], dtype=torch.int32, device="cuda")
@@ -161,24 +177,28 @@ def test_bad_block_id_sets_error_word_and_skips():
     assert pkv.get_device_error() == 0       # read-and-clear
     # sequence 0 is untouched by the bad entries: compare with the oracle
     from oracle import attention as oatt
-    ref = oatt.paged_decode(q.cpu()[:1], kp.cpu(), vp.cpu(), bt.cpu().numpy()[:1], [100], 0.1, 16)
     from _parity import assert_close as ac
+    ref = oatt.paged_decode(q.cpu()[:1], kc, vc, bt.cpu().numpy()[:1], [100], 0.1, 16)
     ac(out[:1].float().cpu().numpy(), ref, "bf16", "seq 0")
 
 
 def test_reshape_and_cache_bad_and_padding_slots():
-    kp = torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16, device="cuda")
-    vp = torch.zeros_like(kp)
+    ks, vs = pkv.pool_shapes(4, 2, 16, 64, torch.bfloat16)
+    kp = torch.zeros(ks, dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros(vs, dtype=torch.bfloat16, device="cuda")
     k = torch.ones(3, 2, 64, dtype=torch.bfloat16, device="cuda")
     slots = torch.tensor([-1, 64, 5], dtype=torch.int64, device="cuda")   # pad, outside, ok
     pkv.reshape_and_cache(k, k, kp, vp, slots)
     assert pkv.get_device_error() == -4
-    assert torch.count_nonzero(kp) == 2 * 64 and torch.all(kp[0, :, 5] == 1)
+    kv = from_layout_k(kp)
+    assert torch.count_nonzero(kp) == 2 * 64 and torch.all(kv[0, :, 5] == 1)
+    assert torch.count_nonzero(vp) == 2 * 64 and torch.all(vp.transpose(2, 3)[0, :, 5] == 1)
 
 
 def test_copy_blocks_bad_pair_sets_error_word():
-    kp = torch.randn(4, 2, 16, 64, device="cuda").to(torch.bfloat16)
-    vp = torch.randn(4, 2, 16, 64, device="cuda").to(torch.bfloat16)
+    ks, vs = pkv.pool_shapes(4, 2, 16, 64, torch.bfloat16)
+    kp = torch.randn(ks, device="cuda").to(torch.bfloat16)
+    vp = torch.randn(vs, device="cuda").to(torch.bfloat16)
     k0 = kp.clone()
     pairs = torch.tensor([[0, 9], [1, 2]], dtype=torch.int64, device="cuda")
     pkv.copy_blocks(kp, vp, pairs)
@@ -187,12 +207,12 @@ def test_copy_blocks_bad_pair_sets_error_word():
 
 
 def test_host_checks_reject_bad_arguments():
-    q, kp, vp, bt = _decode_args(2, 4, 4, 96, 16, 8, 4)       # head_dim 96 not built
+    q, kp, vp, bt, _, _ = _decode_args(2, 4, 4, 96, 16, 8, 4)       # head_dim 96 not built
     lens = torch.tensor([3, 4], dtype=torch.int32, device="cuda")
     with pytest.raises(pkv.PagedKVError) as e:
         pkv.paged_attention_decode(torch.empty_like(q), q, kp, vp, bt, lens, 0.1)
     assert e.value.status == -2
-    q, kp, vp, bt = _decode_args(2, 6, 4, 64, 16, 8, 4)       # 6 heads over 4 kv heads
+    q, kp, vp, bt, _, _ = _decode_args(2, 6, 4, 64, 16, 8, 4)       # 6 heads over 4 kv heads
     with pytest.raises(pkv.PagedKVError) as e:
         pkv.paged_attention_decode(torch.empty_like(q), q, kp, vp, bt, lens, 0.1)
     assert e.value.status == -1
