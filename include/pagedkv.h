@@ -49,6 +49,13 @@
 #include <stddef.h>
 #include <stdint.h>
 
+/* Every entry point is exported; everything else in the library is hidden. */
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -68,13 +75,13 @@ typedef enum {
 typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_E4M3 = 2 } pkv_dtype;
 
 /* Human-readable name of a status code (static string). */
-const char* pkv_status_string(int status);
+PKV_API const char* pkv_status_string(int status);
 
 /* Message of the last CUDA runtime failure behind a PKV_ERR_CUDA returned to
  * this thread (which call, the runtime's error string and code); "" if none.
  * The string belongs to the library and stays valid until the thread's next
  * failing call. */
-const char* pkv_last_error_string(void);
+PKV_API const char* pkv_last_error_string(void);
 
 /* ------------------------------------------------------------------------
  * paged_attention_decode -- one decode query per sequence, attention over
@@ -110,7 +117,7 @@ const char* pkv_last_error_string(void);
  * A table entry outside [0, num_blocks) is skipped (its tokens get zero
  * weight) and sets the device error word to PKV_ERR_OUT_OF_RANGE.
  * ---------------------------------------------------------------------- */
-int paged_attention_decode(void* out, const void* q,
+PKV_API int paged_attention_decode(void* out, const void* q,
                            const void* k_pool, const void* v_pool,
                            const int32_t* block_tables, const int32_t* seq_lens,
                            int num_seqs, int max_blocks_per_seq, int num_blocks,
@@ -122,7 +129,7 @@ int paged_attention_decode(void* out, const void* q,
 
 /* Bytes of workspace that lets paged_attention_decode use its finest split for
  * these sizes (an upper bound; any size works, smaller ones split less). */
-size_t paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim,
+PKV_API size_t paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim,
                                       int block_size, int max_blocks_per_seq);
 
 /* ------------------------------------------------------------------------
@@ -145,7 +152,7 @@ size_t paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim,
  * Supported: head_dim a multiple of 16; (src, cache) in {(F32,F32),
  * (BF16,BF16), (F32,E4M3), (BF16,E4M3)}.
  * ---------------------------------------------------------------------- */
-int reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
+PKV_API int reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
                       const int64_t* slot_mapping, int num_tokens,
                       int num_kv_heads, int head_dim, int block_size, int num_blocks,
                       int src_dtype, int cache_dtype, float k_scale, float v_scale,
@@ -166,7 +173,7 @@ int reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
  * src; otherwise the result is unspecified. A pair with an id outside
  * [0, num_blocks) is skipped and sets PKV_ERR_OUT_OF_RANGE on the device.
  * ---------------------------------------------------------------------- */
-int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs,
+PKV_API int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs,
                 int num_pairs, int num_blocks, size_t block_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
@@ -192,7 +199,7 @@ int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs,
  *     keeps the last call's contents; nothing in it needs clearing.
  * ---------------------------------------------------------------------- */
 #define PKV_NOALLOC_WORKSPACE_BYTES (32u * 1024u * 1024u)
-int paged_attention_decode_noalloc(void* out, const void* q,
+PKV_API int paged_attention_decode_noalloc(void* out, const void* q,
                                    const void* k_pool, const void* v_pool,
                                    const int32_t* block_tables, const int32_t* seq_lens,
                                    int num_seqs, int max_blocks_per_seq, int num_blocks,
@@ -206,7 +213,7 @@ int paged_attention_decode_noalloc(void* out, const void* q,
  * The word is shared by every stream of the device. Once a wait has timed out,
  * every later wait on the device gives up at once until the word is cleared.
  * Returns PKV_OK or PKV_ERR_CUDA. */
-int pkv_get_device_error(int* code, void* stream);
+PKV_API int pkv_get_device_error(int* code, void* stream);
 
 /* ------------------------------------------------------------------------
  * Host block manager ("Como funciona"; glossary "Cách phân trang hoạt động",
@@ -225,39 +232,39 @@ typedef struct pkv_block_manager pkv_block_manager;
 
 /* free_order: the num_free initially free block ids, front first (distinct,
  * each in [0, num_blocks)). Returns NULL on a bad argument. */
-pkv_block_manager* bm_create(int num_blocks, int block_size,
+PKV_API pkv_block_manager* bm_create(int num_blocks, int block_size,
                              const int32_t* free_order, int num_free);
-void bm_destroy(pkv_block_manager* bm);
+PKV_API void bm_destroy(pkv_block_manager* bm);
 
-int bm_add_seq(pkv_block_manager* bm, int64_t seq_id);
+PKV_API int bm_add_seq(pkv_block_manager* bm, int64_t seq_id);
 /* Reserve the next token's slot: *slot = block*block_size + offset. If a
  * copy-on-write is needed *cow_src/*cow_dst get the pair, else both are -1.
  * PKV_ERR_POOL_EXHAUSTED leaves the manager unchanged. */
-int bm_append_slot(pkv_block_manager* bm, int64_t seq_id, int64_t* slot,
+PKV_API int bm_append_slot(pkv_block_manager* bm, int64_t seq_id, int64_t* slot,
                    int32_t* cow_src, int32_t* cow_dst);
 /* n appends to one sequence; the CoW pairs they raise are written as
  * (src, dst) int64 pairs into cow_pairs (capacity cow_cap pairs) and counted in
  * *num_cow. On exhaustion the appends done so far stay done. */
-int bm_append_n(pkv_block_manager* bm, int64_t seq_id, int n,
+PKV_API int bm_append_n(pkv_block_manager* bm, int64_t seq_id, int n,
                 int64_t* cow_pairs, int cow_cap, int* num_cow);
 /* One append to each of n sequences (a decode step): slots[i] for seq_ids[i];
  * CoW pairs in order into cow_pairs (capacity n pairs), count in *num_cow. */
-int bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n,
+PKV_API int bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n,
                     int64_t* slots, int64_t* cow_pairs, int* num_cow);
-int bm_fork(pkv_block_manager* bm, int64_t parent, int64_t child);
-int bm_free_seq(pkv_block_manager* bm, int64_t seq_id);
+PKV_API int bm_fork(pkv_block_manager* bm, int64_t parent, int64_t child);
+PKV_API int bm_free_seq(pkv_block_manager* bm, int64_t seq_id);
 /* The sequence's table into out[0..cap), its length in blocks in *n. */
-int bm_block_table(const pkv_block_manager* bm, int64_t seq_id, int32_t* out,
+PKV_API int bm_block_table(const pkv_block_manager* bm, int64_t seq_id, int32_t* out,
                    int cap, int* n);
 /* Dense int32 tables [n][max_blocks] (unused entries -1) and lengths [n] for
  * seq_ids, ready to copy to the device for paged_attention_decode. */
-int bm_build_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
+PKV_API int bm_build_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
                     int max_blocks, int32_t* tables, int32_t* seq_lens);
-int bm_seq_len(const pkv_block_manager* bm, int64_t seq_id, int* len);
-int bm_refcount(const pkv_block_manager* bm, int block, int* count);
-int bm_num_free(const pkv_block_manager* bm);
+PKV_API int bm_seq_len(const pkv_block_manager* bm, int64_t seq_id, int* len);
+PKV_API int bm_refcount(const pkv_block_manager* bm, int block, int* count);
+PKV_API int bm_num_free(const pkv_block_manager* bm);
 /* The free list, front first, into out[0..cap); returns its length. */
-int bm_free_list(const pkv_block_manager* bm, int32_t* out, int cap);
+PKV_API int bm_free_list(const pkv_block_manager* bm, int32_t* out, int cap);
 
 #ifdef __cplusplus
 }

@@ -26,9 +26,9 @@ CUDA_SOURCES = [
 CXX_SOURCES = ["block_manager.cpp"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
                      "--expt-relaxed-constexpr", "-Xptxas", "-v"]
-CXX_FLAGS = ["-O2", "-fPIC", "-std=c++17", "-Wall"]
+CXX_FLAGS = ["-O2", "-fPIC", "-fvisibility=hidden", "-std=c++17", "-Wall"]
 
 
 def _nvcc():

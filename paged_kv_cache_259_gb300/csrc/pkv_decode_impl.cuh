@@ -52,6 +52,18 @@
 namespace pkv {
 namespace decode {
 
+// Build-time tuning (defaults measured on GB300): shared-memory ring bytes per
+// CTA, warps per CTA, and the K+V bytes a split-KV partition aims at.
+#ifndef PKV_RING_BYTES
+#define PKV_RING_BYTES 65536
+#endif
+#ifndef PKV_DECODE_WARPS
+#define PKV_DECODE_WARPS 4
+#endif
+#ifndef PKV_PART_BYTES
+#define PKV_PART_BYTES (512 * 1024)
+#endif
+
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -213,10 +225,15 @@ struct SimtMath {
         }
         __syncwarp();
         // ---- P.V: lane owns dims lane, lane+32, ...; V row = the dim's tokens
+        bool moved = false;
 #pragma unroll
-        for (int g = 0; g < G; ++g)
+        for (int g = 0; g < G; ++g) moved |= alpha[g] != 1.f;
+        if (__any_sync(kFull, moved)) {                      // running max moved
 #pragma unroll
-            for (int k = 0; k < DPL; ++k) st.acc[g][k] *= alpha[g];
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int k = 0; k < DPL; ++k) st.acc[g][k] *= alpha[g];
+        }
 #pragma unroll
         for (int ch = 0; ch < CR; ++ch) {
             if (ch * TPC >= ntok) break;
@@ -362,17 +379,27 @@ struct MmaMath {
 #pragma unroll
         for (int h = 0; h < SUB; ++h) {
             if (16 * h >= ntok) break;                       // warp-uniform
-            // ---- S^T = Q K^T for 16 tokens (two n-tiles of 8)
+            // ---- S^T = Q K^T for 16 tokens (two n-tiles of 8); even and odd
+            //      k-steps accumulate separately (shorter dependency chains)
             float s[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+            float s2[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+            uint32_t k8[4];                                  // E4M3: 4 bytes per (k-step, n-tile)
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 uint32_t b[2][2];
                 if constexpr (F8) {
+                    // ldmatrix on byte pairs: row = one token's 16 dims of plane ks,
+                    // lane (r, c) receives its bytes 4c..4c+3; matrices: (u, ks),
+                    // (u, ks+1) for u = 0, 1, loaded every other k-step
+                    if ((ks & 1) == 0) {
+                        const int m = lane >> 3, rr = lane & 7;
+                        const int u = m & 1, plane = ks + (m >> 1);
+                        const int tok = 16 * h + 4 * (rr >> 1) + 2 * u + (rr & 1);
+                        ldsm_x4(kbase + (plane * BS + tok) * 16, k8[0], k8[1], k8[2], k8[3]);
+                    }
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const int tok = 16 * h + 4 * (r >> 1) + 2 * u + (r & 1);
-                        const uint32_t w4 =
-                            *reinterpret_cast<const uint32_t*>(kt + (ks * BS + tok) * 16 + 4 * c);
+                        const uint32_t w4 = k8[(ks & 1) * 2 + u];
                         b[u][0] = e4m3x2_to_f16x2(w4);
                         b[u][1] = e4m3x2_to_f16x2(w4 >> 16);
                     }
@@ -383,9 +410,16 @@ struct MmaMath {
                     ldsm_x4(kbase + (plane * BS + tok) * 16, b[0][0], b[0][1], b[1][0], b[1][1]);
                 }
 #pragma unroll
-                for (int u = 0; u < 2; ++u)
-                    mma16816(F8, s[u][0], s[u][1], st.qa[ks][0], st.qa[ks][1], b[u][0], b[u][1],
-                             s[u][0], s[u][1]);
+                for (int u = 0; u < 2; ++u) {
+                    float(&acc)[2][2] = (ks & 1) ? s2 : s;
+                    mma16816(F8, acc[u][0], acc[u][1], st.qa[ks][0], st.qa[ks][1], b[u][0],
+                             b[u][1], acc[u][0], acc[u][1]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                s[u][0] += s2[u][0];
+                s[u][1] += s2[u][1];
             }
             // ---- online softmax on this lane's 4 scores of head row r
             float mx = -INFINITY;
@@ -412,23 +446,33 @@ struct MmaMath {
                 }
             st.l = st.l * alpha + psum;
             st.m = m_new;
+            if (!__all_sync(kFull, alpha == 1.f)) {          // running max moved
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                st.o[nt][0] *= alpha;
-                st.o[nt][1] *= alpha;
+                for (int nt = 0; nt < NT; ++nt) {
+                    st.o[nt][0] *= alpha;
+                    st.o[nt][1] *= alpha;
+                }
             }
             const uint32_t pa0 = F8 ? pack_f16(pr[0][0], pr[0][1]) : pack_bf16(pr[0][0], pr[0][1]);
             const uint32_t pa2 = F8 ? pack_f16(pr[1][0], pr[1][1]) : pack_bf16(pr[1][0], pr[1][1]);
             // ---- O += P V (V rows = dims); unwritten slots beyond ntok are zeroed
             const int tail = ntok - 16 * h;                  // valid tokens in this subtile
+            uint32_t v8[4];                                  // E4M3: 4 bytes per n-tile
 #pragma unroll
             for (int nt = 0; nt < NT; nt += 2) {
                 uint32_t b[2][2];
                 if constexpr (F8) {
+                    // ldmatrix on byte pairs: row = one dim's 16 tokens of this
+                    // subtile, lane (r, c) receives tokens 4c..4c+3 of dim 8nt'+r;
+                    // matrices: n-tiles nt..nt+3, loaded every other pair
+                    if ((nt & 2) == 0) {
+                        const int m = lane >> 3, rr = lane & 7;
+                        const int d = 8 * (nt + m) + rr;
+                        ldsm_x4(vbase + d * Lay::kVRow + 16 * h, v8[0], v8[1], v8[2], v8[3]);
+                    }
 #pragma unroll
                     for (int x = 0; x < 2; ++x) {
-                        const int d = 8 * (nt + x) + r;
-                        uint32_t w4 = *reinterpret_cast<const uint32_t*>(vt + d * Lay::kVRow + 16 * h + 4 * c);
+                        uint32_t w4 = v8[(nt & 2) + x];
                         if (tail < 16) {
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
@@ -486,16 +530,21 @@ template <class Math, int D, int BS, int G, int NW>
 struct Pipe {
     using Lay = typename Math::Lay;
     static constexpr int kTile = Lay::kTile;
-    // about 96 KB of ring per CTA (two CTAs per SM); at least one stage per warp
-    // (a 16 KB tile, float32 D128 with 32-token blocks, gets a single stage)
-    static constexpr int kStages = (98304 / (NW * 2 * kTile)) < 1 ? 1
-                                   : (98304 / (NW * 2 * kTile)) > 8 ? 8
-                                   : (98304 / (NW * 2 * kTile));
+    // about PKV_RING_BYTES of ring per CTA; at least one stage per warp (a 16 KB
+    // tile, float32 D128 with 32-token blocks, gets a single stage)
+    static constexpr int kStages = (PKV_RING_BYTES / (NW * 2 * kTile)) < 1 ? 1
+                                   : (PKV_RING_BYTES / (NW * 2 * kTile)) > 8 ? 8
+                                   : (PKV_RING_BYTES / (NW * 2 * kTile));
     static constexpr int kRingBytes = NW * kStages * 2 * kTile;
-    static constexpr int kSmem = kRingBytes + NW * kStages * 8     // mbarriers
-                                 + NW * kStages * 4                // stage block ids
-                                 + Math::kCtaSmemFloats * 4
-                                 + NW * Math::kWarpSmemFloats * 4;
+    // shared-memory carve-up: ring | mbarriers | stage block ids | q rows | per-warp
+    // scratch; the q rows and the scratch start on 16-byte boundaries (float4 reads)
+    static constexpr int kBarOff = kRingBytes;
+    static constexpr int kIdOff = kBarOff + NW * kStages * 8;
+    static constexpr int kQOff = (kIdOff + NW * kStages * 4 + 15) / 16 * 16;
+    static constexpr int kWarpOff = kQOff + (Math::kCtaSmemFloats * 4 + 15) / 16 * 16;
+    static constexpr int kSmem = kWarpOff + NW * Math::kWarpSmemFloats * 4;
+    static_assert(kRingBytes % 128 == 0 && kQOff % 16 == 0 && kWarpOff % 16 == 0 &&
+                      (Math::kWarpSmemFloats * 4) % 16 == 0, "shared-memory alignment");
     static_assert(NW * G * (D + 2) * 4 <= kRingBytes, "combine area must fit in the ring");
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 };
@@ -507,10 +556,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
 
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::kRingBytes);
-    int32_t* stage_id = reinterpret_cast<int32_t*>(bars + NW * ST);
-    float* qs = reinterpret_cast<float*>(stage_id + NW * ST);
-    float* wsm = qs + Math::kCtaSmemFloats;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::kBarOff);
+    int32_t* stage_id = reinterpret_cast<int32_t*>(smem + P::kIdOff);
+    float* qs = reinterpret_cast<float*>(smem + P::kQOff);
+    float* wsm = reinterpret_cast<float*>(smem + P::kWarpOff);
 
     const int part = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     int L = p.seq_lens[b];
@@ -702,20 +751,18 @@ struct Args {
     int* err;
 };
 
-constexpr int kNumWarps = 4;
+constexpr int kNumWarps = PKV_DECODE_WARPS;
 constexpr int kMinPartBlocks = 2 * kNumWarps;   // finest split: 8 blocks per partition
-constexpr int kMaxDevices = 64;
-
 inline size_t workspace_need(int B, int Hq, int D, int parts) {
     return (size_t)B * Hq * parts * ((size_t)D + 2) * sizeof(float);
 }
 
-// Partition size: about 256 KB of K+V per CTA; smaller when that leaves fewer
+// Partition size: about PKV_PART_BYTES of K+V per CTA; smaller when that leaves fewer
 // than ~2 waves of CTAs; never finer than kMinPartBlocks; one partition when the
 // workspace cannot hold the split.
 inline int choose_part_blocks(const Args& a, int tile_bytes, int ctas_per_sm, int* parts_out) {
     const int MB = a.max_blocks;
-    int target = (256 * 1024) / (2 * tile_bytes);
+    int target = PKV_PART_BYTES / (2 * tile_bytes);
     target = (target + kNumWarps - 1) / kNumWarps * kNumWarps;
     if (target < kMinPartBlocks) target = kMinPartBlocks;
     int PB = MB < target ? MB : target;
@@ -740,21 +787,11 @@ template <class Math, typename QT, int D, int BS, int G>
 int launch_variant(const Args& a) {
     using P = Pipe<Math, D, BS, G, kNumWarps>;
     auto kern = paged_decode_kernel<Math, QT, D, BS, G, kNumWarps>;
-    static int attr_done[kMaxDevices];      // 0 = not yet, else occupancy + 1
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevices)
-        return cuda_fail("decode: current device", cudaErrorInvalidDevice);
-    if (!attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             P::kSmem);
-        if (e != cudaSuccess) return cuda_fail("decode: set max dynamic shared memory", e);
-        int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kNumWarps * 32, P::kSmem);
-        if (e != cudaSuccess) return cuda_fail("decode: occupancy query", e);
-        attr_done[dev] = occ + 1;
-    }
+    int occ = 0;
+    const int st = kernel_setup(reinterpret_cast<const void*>(kern), P::kSmem, kNumWarps * 32, &occ);
+    if (st != PKV_OK) return st;
     int parts = 1;
-    const int PB = choose_part_blocks(a, P::kTile, attr_done[dev] - 1, &parts);
+    const int PB = choose_part_blocks(a, P::kTile, occ, &parts);
 
     Params p;
     p.out = a.out;

@@ -23,6 +23,11 @@ int num_sms();
 // return PKV_ERR_CUDA.
 int cuda_fail(const char* what, cudaError_t e);
 
+// One-time per-(device, kernel) set-up: raise the kernel's dynamic shared
+// memory limit to `smem` bytes and return its resident CTAs per SM for `threads`
+// threads in *occupancy. Cached; thread-safe. Returns PKV_OK or PKV_ERR_CUDA.
+int kernel_setup(const void* kernel, int smem, int threads, int* occupancy);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace pkv

@@ -1,6 +1,9 @@
 // Status strings, the device error word and per-device caches.
 #include <atomic>
 #include <cstdio>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "pkv_internal.cuh"
 
@@ -38,6 +41,28 @@ int cuda_fail(const char* what, cudaError_t e) {
     (void)cudaGetLastError();   // leave no stale (non-sticky) error for the caller's next check
     snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
     return PKV_ERR_CUDA;
+}
+
+int kernel_setup(const void* kernel, int smem, int threads, int* occupancy) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, int> done;   // (device, kernel) -> occupancy
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail("kernel set-up: current device", e);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find({dev, kernel});
+    if (it != done.end()) {
+        *occupancy = it->second;
+        return PKV_OK;
+    }
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_fail("kernel set-up: max dynamic shared memory", e);
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem);
+    if (e != cudaSuccess) return cuda_fail("kernel set-up: occupancy query", e);
+    done[{dev, kernel}] = occ;
+    *occupancy = occ;
+    return PKV_OK;
 }
 
 int num_sms() {
