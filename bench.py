@@ -218,8 +218,7 @@ def run_gpu(args, rank, world, device):
             pkv.copy_blocks(cache.k_pool, cache.v_pool, dev["pairs"], stream=stream)
         pkv.reshape_and_cache(kd, vd, cache.k_pool, cache.v_pool, dev["slots"], ks, vs, stream=stream)
         ev_dec[i][0].record(stream)
-        pkv.paged_attention_decode(out, qd, cache.k_pool, cache.v_pool, dev["tables"], dev["lens"],
-                                   w.scale, ks, vs, ws, stream=stream)
+        cache.decode(qd, dev, out, w.scale, ks, vs, ws, stream=stream)
         ev_dec[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -230,9 +229,7 @@ def run_gpu(args, rank, world, device):
     dec_ms = np.array([a.elapsed_time(b) for a, b in ev_dec])
     if pkv.get_device_error() != 0:
         raise RuntimeError("device error in the timed region")
-    split = ws is not None and pkv.paged_attention_workspace_size(
-        w.B, w.Hq, w.D, w.bs, w.max_blocks_per_seq) > 0
-    launches_per_step = (1 if has_copy else 0) + 1 + 1 + (1 if split else 0)
+    launches_per_step = count_launches(step)
 
     # ---- end to end through the public API: pinned host inputs in, output out
     host = plan.host_tensors(pin=True)
@@ -267,9 +264,27 @@ def run_gpu(args, rank, world, device):
 
     res = {"w": w, "nbytes": nbytes, "ms_per_step": total_ms / K, "dec_ms": float(dec_ms.mean()),
            "dec_ms_median": float(np.median(dec_ms)), "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
-           "clocks": clk, "launches": launches_per_step * K, "split": split,
+           "clocks": clk, "launches": launches_per_step * K, "groups": plan.num_groups,
+           "launches_per_step": launches_per_step,
            "cpu": (q, k_src, v_src, ks, vs, plan)}
     return res
+
+
+OUR_KERNELS = ("paged_decode_kernel", "split_reduce_kernel", "reshape_and_cache_kernel",
+               "copy_blocks_kernel")
+
+
+def count_launches(step, reps=3):
+    """Kernels of this library one step launches, counted by the CUDA profiler."""
+    from torch.profiler import ProfilerActivity, profile
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        for _ in range(reps):
+            step()
+        torch.cuda.synchronize()
+    n = sum(1 for e in prof.events() if any(k in e.name for k in OUR_KERNELS)
+            and e.device_type == torch.autograd.DeviceType.CUDA)
+    return n // reps
 
 
 def max_over_ranks(x, world, device):
@@ -384,9 +399,12 @@ def main():
             "dtype": w.kv_dtype, "data": "synthetic",
             "config": {
                 "workload": workload_desc(w),
-                "step": ("copy_blocks (CoW pairs: %d) + reshape_and_cache + "
-                         "paged_attention_decode%s" % (len(plan.pairs),
-                                                       " (split-KV + merge)" if r["split"] else "")),
+                "step": ("copy_blocks (CoW pairs: %d) + reshape_and_cache + %s; %d kernel "
+                         "launches per step" % (
+                             len(plan.pairs),
+                             "paged_attention_decode_grouped (%d prefix groups)" % r["groups"]
+                             if r["groups"] else "paged_attention_decode",
+                             r["launches_per_step"])),
                 "l2": "inputs larger than L2: %.2f GB of K/V read per step vs %d MB L2"
                       % (nb["decode"] / 1e9, L2_BYTES >> 20),
                 "bytes_per_step": nb["total"], "decode_bytes_per_step": nb["decode"],

@@ -13,6 +13,8 @@
 //
 // Host memory only; no CUDA. The manager never touches KV data: it hands out
 // slot numbers and (src, dst) copy pairs that the device calls consume.
+#include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <deque>
 #include <new>
@@ -214,6 +216,64 @@ int bm_refcount(const pkv_block_manager* bm, int block, int* count) {
 }
 
 int bm_num_free(const pkv_block_manager* bm) { return bm ? (int)bm->free_list.size() : -1; }
+
+// Sequences that point at the same physical blocks (forks of one prompt) can
+// share the attention work on those blocks, not only their memory: group them
+// by their first block, and take as each group's prefix the leading block ids
+// all members have in common, up to the blocks every member has filled.
+int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n, int max_members,
+                     int32_t* group_members, int32_t* group_prefix, int32_t* seq_prefix,
+                     int* num_groups) {
+    if (!bm || n < 0 || max_members < 1 || !num_groups ||
+        (n > 0 && (!seq_ids || !group_members || !group_prefix || !seq_prefix)))
+        return PKV_ERR_INVALID_ARG;
+    *num_groups = 0;
+    std::vector<const pkv_block_manager::Seq*> seqs(n);
+    for (int i = 0; i < n; ++i) {
+        auto it = bm->seqs.find(seq_ids[i]);
+        if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
+        seqs[i] = &it->second;
+        seq_prefix[i] = 0;
+    }
+    std::unordered_map<int32_t, std::vector<int>> buckets;
+    std::vector<int32_t> order;                      // first blocks in batch order
+    for (int i = 0; i < n; ++i) {
+        if (seqs[i]->table.empty()) continue;
+        const int32_t key = seqs[i]->table[0];
+        auto& v = buckets[key];
+        if (v.empty()) order.push_back(key);
+        v.push_back(i);
+    }
+    int ng = 0;
+    for (int32_t key : order) {
+        const std::vector<int>& mem = buckets[key];
+        for (size_t c = 0; c < mem.size(); c += (size_t)max_members) {
+            const size_t e = std::min(mem.size(), c + (size_t)max_members);
+            if (e - c < 2) continue;
+            int64_t full = INT64_MAX;                // blocks every member has filled
+            for (size_t k = c; k < e; ++k)
+                full = std::min<int64_t>(full, seqs[mem[k]]->len / bm->block_size);
+            const auto& t0 = seqs[mem[c]]->table;
+            int64_t prefix = 0;
+            while (prefix < full) {
+                bool same = true;
+                for (size_t k = c + 1; k < e && same; ++k)
+                    same = seqs[mem[k]]->table[prefix] == t0[prefix];
+                if (!same) break;
+                ++prefix;
+            }
+            if (prefix < 1) continue;
+            int32_t* row = group_members + (size_t)ng * max_members;
+            for (int k = 0; k < max_members; ++k)
+                row[k] = c + k < e ? (int32_t)mem[c + k] : -1;
+            group_prefix[ng] = (int32_t)prefix;
+            for (size_t k = c; k < e; ++k) seq_prefix[mem[k]] = (int32_t)prefix;
+            ++ng;
+        }
+    }
+    *num_groups = ng;
+    return PKV_OK;
+}
 
 int bm_free_list(const pkv_block_manager* bm, int32_t* out, int cap) {
     if (!bm) return -1;

@@ -23,12 +23,15 @@ size_t paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim,
     return parts > 1 ? workspace_need(num_seqs, num_heads, head_dim, parts) : 0;
 }
 
-int paged_attention_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
-                           const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
-                           int max_blocks_per_seq, int num_blocks, int num_heads, int num_kv_heads,
-                           int head_dim, int block_size, float scale, int q_dtype, int kv_dtype,
-                           float k_scale, float v_scale, void* workspace, size_t workspace_bytes,
-                           void* stream) {
+namespace {
+
+int decode_common(void* out, const void* q, const void* k_pool, const void* v_pool,
+                  const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                  int max_blocks_per_seq, int num_blocks, int num_heads, int num_kv_heads,
+                  int head_dim, int block_size, float scale, int q_dtype, int kv_dtype,
+                  float k_scale, float v_scale, const int32_t* start_blocks,
+                  const int32_t* group_members, const int32_t* group_prefix, int num_groups,
+                  int max_members, void* workspace, size_t workspace_bytes, void* stream) {
     using namespace pkv;
     if (num_seqs < 0 || num_seqs > 65535 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
         num_heads <= 0 || num_kv_heads <= 0 || num_kv_heads > 65535 || head_dim <= 0 ||
@@ -67,6 +70,11 @@ int paged_attention_decode(void* out, const void* q, const void* k_pool, const v
     a.workspace = workspace;
     a.workspace_bytes = workspace ? workspace_bytes : 0;
     a.stream = static_cast<cudaStream_t>(stream);
+    a.start_blocks = start_blocks;
+    a.group_members = group_members;
+    a.group_prefix = group_prefix;
+    a.num_groups = num_groups;
+    a.max_members = max_members;
     a.err = error_word();
     if (!a.err) return PKV_ERR_CUDA;
 
@@ -74,6 +82,42 @@ int paged_attention_decode(void* out, const void* q, const void* k_pool, const v
     if (q_dtype == PKV_BF16 && kv_dtype == PKV_BF16) return decode::dispatch_bf16(a);
     if (q_dtype == PKV_BF16 && kv_dtype == PKV_E4M3) return decode::dispatch_e4m3(a);
     return PKV_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+int paged_attention_decode(void* out, const void* q, const void* k_pool, const void* v_pool,
+                           const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                           int max_blocks_per_seq, int num_blocks, int num_heads, int num_kv_heads,
+                           int head_dim, int block_size, float scale, int q_dtype, int kv_dtype,
+                           float k_scale, float v_scale, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    return decode_common(out, q, k_pool, v_pool, block_tables, seq_lens, num_seqs,
+                         max_blocks_per_seq, num_blocks, num_heads, num_kv_heads, head_dim,
+                         block_size, scale, q_dtype, kv_dtype, k_scale, v_scale, nullptr, nullptr,
+                         nullptr, 0, 0, workspace, workspace_bytes, stream);
+}
+
+int paged_attention_decode_grouped(void* out, const void* q, const void* k_pool,
+                                   const void* v_pool, const int32_t* block_tables,
+                                   const int32_t* seq_lens, int num_seqs, int max_blocks_per_seq,
+                                   int num_blocks, int num_heads, int num_kv_heads, int head_dim,
+                                   int block_size, float scale, int q_dtype, int kv_dtype,
+                                   float k_scale, float v_scale, const int32_t* seq_prefix_blocks,
+                                   const int32_t* group_members, const int32_t* group_prefix_blocks,
+                                   int num_groups, int max_members, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+    if (num_groups < 0 || (num_groups > 0 && (max_members <= 0 || !seq_prefix_blocks ||
+                                              !group_members || !group_prefix_blocks)))
+        return PKV_ERR_INVALID_ARG;
+    if (num_groups > 65535) return PKV_ERR_UNSUPPORTED;
+    return decode_common(out, q, k_pool, v_pool, block_tables, seq_lens, num_seqs,
+                         max_blocks_per_seq, num_blocks, num_heads, num_kv_heads, head_dim,
+                         block_size, scale, q_dtype, kv_dtype, k_scale, v_scale,
+                         num_groups > 0 ? seq_prefix_blocks : nullptr,
+                         num_groups > 0 ? group_members : nullptr,
+                         num_groups > 0 ? group_prefix_blocks : nullptr, num_groups, max_members,
+                         workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

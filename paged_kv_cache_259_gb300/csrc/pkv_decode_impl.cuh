@@ -81,6 +81,14 @@ struct Params {
     int part_blocks, max_parts;
     float qscale;     // scale * k_scale * log2(e)
     float v_scale;
+    // prefix-grouped decode (null / 0 otherwise)
+    const int32_t* start_blocks;   // [B] first block this launch covers (shared prefix length)
+    const int32_t* group_members;  // [num_groups][max_members] batch indices, -1 padded
+    const int32_t* group_prefix;   // [num_groups] shared full blocks of the group
+    int max_members;
+    int slot_base;                 // workspace slot of partition 0 of this launch
+    int slots;                     // workspace slots per (sequence, head)
+    int prefix_part_blocks;        // partition size of the prefix launch (merge only)
 };
 
 template <typename T> struct Elt;
@@ -143,6 +151,7 @@ struct Layout {
 template <typename QT, typename KV, int D, int BS, int G>
 struct SimtMath {
     using Lay = Layout<KV, D, BS>;
+    using KVT = KV;
     static constexpr int X = Lay::kX, NPL = Lay::kPlanes;
     static constexpr int CPP = 32 / BS;              // chunk planes per warp pass
     static constexpr int PASSES = NPL / CPP;
@@ -160,10 +169,7 @@ struct SimtMath {
         float qr[kQRegs ? PASSES * X : 1];
     };
 
-    __device__ __forceinline__ static void load_q(float* qs, const Params& p, int b, int hk) {
-        const QT* qb = static_cast<const QT*>(p.q) + ((size_t)b * p.num_heads + (size_t)hk * G) * D;
-        for (int i = threadIdx.x; i < G * D; i += blockDim.x) qs[i] = to_f(qb[i]) * p.qscale;
-    }
+    static constexpr bool kPrescaledQ = true;                // q rows carry scale * log2 e
 
     __device__ __forceinline__ static void init(State& st, const float* qs, int lane) {
 #pragma unroll
@@ -328,6 +334,7 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 template <typename KV, int D, int BS, int G>
 struct MmaMath {
     using Lay = Layout<KV, D, BS>;
+    using KVT = KV;
     static constexpr bool F8 = std::is_same<KV, uint8_t>::value;
     static constexpr int KS = D / 16;                // k-steps of Q.K
     static constexpr int NT = D / 8;                 // n-tiles of P.V
@@ -342,11 +349,7 @@ struct MmaMath {
         float m, l;
     };
 
-    __device__ __forceinline__ static void load_q(float* qs, const Params& p, int b, int hk) {
-        const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(p.q) +
-                                  ((size_t)b * p.num_heads + (size_t)hk * G) * D;
-        for (int i = threadIdx.x; i < G * D; i += blockDim.x) qs[i] = __bfloat162float(qb[i]);
-    }
+    static constexpr bool kPrescaledQ = false;               // scale applied to S in fp32
 
     __device__ __forceinline__ static void init(State& st, const float* qs, int lane) {
         const int r = lane >> 2, c = lane & 3;
@@ -549,7 +552,30 @@ struct Pipe {
     static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
 };
 
-template <class Math, typename QT, int D, int BS, int G, int NW>
+// Query row r of the CTA: (sequence, head), or sequence -1 for an unused row.
+// Regular launch: the G heads of kv head hk of sequence b. Prefix launch: row
+// r = m * Gh + g is head hk * Gh + g of the group's m-th member (Gh = the
+// model's query heads per kv head), so every member shares the loaded tiles.
+template <bool PREFIX, int G>
+__device__ __forceinline__ void row_target(const Params& p, int b_or_group, int hk, int r, int* seq,
+                                           int* head) {
+    if constexpr (!PREFIX) {
+        *seq = b_or_group;
+        *head = hk * G + r;
+    } else {
+        const int gh = p.num_heads / p.num_kv_heads;
+        const int m = r / gh;
+        int s = -1;
+        if (m < p.max_members) {
+            s = p.group_members[(size_t)b_or_group * p.max_members + m];
+            if (s >= p.num_seqs) s = -1;
+        }
+        *seq = s;
+        *head = hk * gh + r % gh;
+    }
+}
+
+template <class Math, typename QT, int D, int BS, int G, int NW, bool PREFIX>
 __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
     using P = Pipe<Math, D, BS, G, NW>;
     constexpr int TILE = P::kTile, ST = P::kStages;
@@ -561,18 +587,34 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
     float* qs = reinterpret_cast<float*>(smem + P::kQOff);
     float* wsm = reinterpret_cast<float*>(smem + P::kWarpOff);
 
-    const int part = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
-    int L = p.seq_lens[b];
-    if (L < 0 || L > p.max_blocks * BS) {                   // length the table cannot hold
-        if (part == 0 && hk == 0 && threadIdx.x == 0) flag_error(p.err, kErrOutOfRange);
-        L = L < 0 ? 0 : p.max_blocks * BS;
+    // b: the sequence (regular launch) or the group (prefix launch) whose table
+    // row is read; start: first logical block of this launch's range
+    const int part = blockIdx.x, hk = blockIdx.y;
+    int b = blockIdx.z;
+    int L, start = 0, nblk;
+    if constexpr (PREFIX) {
+        const int lead = p.group_members[(size_t)b * p.max_members];
+        if (lead < 0 || lead >= p.num_seqs) return;
+        const int Ll = min(max(p.seq_lens[lead], 0), p.max_blocks * BS);
+        nblk = min(max(p.group_prefix[b], 0), Ll / BS);     // full shared blocks only
+        L = nblk * BS;
+        b = lead;                                           // its table row holds the prefix
+    } else {
+        L = p.seq_lens[b];
+        if (L < 0 || L > p.max_blocks * BS) {               // length the table cannot hold
+            if (part == 0 && hk == 0 && threadIdx.x == 0) flag_error(p.err, kErrOutOfRange);
+            L = L < 0 ? 0 : p.max_blocks * BS;
+        }
+        nblk = (L + BS - 1) / BS;
+        if (p.start_blocks) start = min(max(p.start_blocks[b], 0), nblk);
     }
-    const int nblk = (L + BS - 1) / BS;
     const int PB = p.part_blocks;
-    const int nparts = (nblk + PB - 1) / PB;
-    if (part >= (nparts > 0 ? nparts : 1)) return;          // beyond this sequence
-    const int blk0 = part * PB;
+    const int nparts = (nblk - start + PB - 1) / PB;
+    if (PREFIX ? part >= nparts : part >= (nparts > 0 ? nparts : 1)) return;
+    const int blk0 = start + part * PB;                     // first block of this partition
     const int nbp = max(0, min(PB, nblk - blk0));           // blocks in this partition
+    // the only contributor to its outputs: write `out` directly
+    const bool single = !PREFIX && start == 0 && nparts <= 1;
 
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
 
@@ -581,7 +623,14 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
         for (int s = 0; s < ST; ++s) mbar_init(smem_addr(&bars[w * ST + s]), 1);
         fence_mbar_init();
     }
-    Math::load_q(qs, p, b, hk);
+    for (int i = tid; i < G * D; i += NW * 32) {            // query rows of this CTA
+        const int r = i / D;
+        int seq, head;
+        row_target<PREFIX, G>(p, blockIdx.z, hk, r, &seq, &head);
+        float qv = 0.f;
+        if (seq >= 0) qv = to_f(static_cast<const QT*>(p.q)[((size_t)seq * p.num_heads + head) * D + i % D]);
+        qs[i] = Math::kPrescaledQ ? qv * p.qscale : qv;
+    }
     __syncthreads();
 
     typename Math::State st;
@@ -679,7 +728,6 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
     __syncthreads();
 
     // ---- merge the warps (and write out, or the partition's partial)
-    const bool single = nparts <= 1;
     for (int idx = tid; idx < G * D; idx += NW * 32) {
         const int g = idx / D, d = idx % D;
         float M = -INFINITY;
@@ -694,12 +742,14 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
                 O += e * cacc[(ww * G + g) * D + d];
             }
         }
-        const int h = hk * G + g;
+        int seq, h;
+        row_target<PREFIX, G>(p, blockIdx.z, hk, g, &seq, &h);
+        if (seq < 0) continue;
         const float o = Ssum > 0.f ? O / Ssum : 0.f;
         if (single) {
-            store_out(static_cast<QT*>(p.out) + ((size_t)b * p.num_heads + h) * D + d, o * p.v_scale);
+            store_out(static_cast<QT*>(p.out) + ((size_t)seq * p.num_heads + h) * D + d, o * p.v_scale);
         } else {
-            const size_t base = ((size_t)b * p.num_heads + h) * p.max_parts + part;
+            const size_t base = ((size_t)seq * p.num_heads + h) * p.slots + p.slot_base + part;
             p.ws_o[base * D + d] = o;
             if (d == 0) {
                 p.ws_ml[2 * base] = M;
@@ -711,23 +761,30 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
 
 // Merge the partitions of every (sequence, query head) that was split:
 //   out = v_scale * sum_p 2^(m_p - M) l_p o_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
+// Slots: [0, prefix parts) from the prefix launch (grouped decode only), then
+// [slot_base, slot_base + parts) for the sequence's own range.
 template <typename QT>
 __global__ void __launch_bounds__(128) split_reduce_kernel(const Params p, int D, int BS) {
     const int h = blockIdx.x, b = blockIdx.y;
     const int L = min(max(p.seq_lens[b], 0), p.max_blocks * BS);   // as the decode kernel clamps
     const int nblk = (L + BS - 1) / BS;
-    const int nparts = (nblk + p.part_blocks - 1) / p.part_blocks;
-    if (nparts <= 1) return;                                // written by the decode kernel
-    const size_t base = ((size_t)b * p.num_heads + h) * p.max_parts;
+    const int start = p.start_blocks ? min(max(p.start_blocks[b], 0), nblk) : 0;
+    const int pre = start > 0 ? (start + p.prefix_part_blocks - 1) / p.prefix_part_blocks : 0;
+    const int own = (nblk - start + p.part_blocks - 1) / p.part_blocks;
+    if (pre == 0 && own <= 1) return;                       // written by the decode kernel
+    const size_t base = ((size_t)b * p.num_heads + h) * p.slots;
+    auto slot = [&](int q) { return base + (q < pre ? q : p.slot_base + (q - pre)); };
+    const int n = pre + own;
     float M = -INFINITY;
-    for (int q = 0; q < nparts; ++q) M = fmaxf(M, p.ws_ml[2 * (base + q)]);
+    for (int q = 0; q < n; ++q) M = fmaxf(M, p.ws_ml[2 * slot(q)]);
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
         float Ssum = 0.f, O = 0.f;
         if (M != -INFINITY) {
-            for (int q = 0; q < nparts; ++q) {
-                const float e = exp2f(p.ws_ml[2 * (base + q)] - M) * p.ws_ml[2 * (base + q) + 1];
+            for (int q = 0; q < n; ++q) {
+                const size_t sq = slot(q);
+                const float e = exp2f(p.ws_ml[2 * sq] - M) * p.ws_ml[2 * sq + 1];
                 Ssum += e;
-                O += e * p.ws_o[(base + q) * D + d];
+                O += e * p.ws_o[sq * D + d];
             }
         }
         store_out(static_cast<QT*>(p.out) + ((size_t)b * p.num_heads + h) * D + d,
@@ -749,18 +806,27 @@ struct Args {
     size_t workspace_bytes;
     cudaStream_t stream;
     int* err;
+    // prefix-grouped decode (all null / 0 for the plain call)
+    const int32_t* start_blocks;
+    const int32_t* group_members;
+    const int32_t* group_prefix;
+    int num_groups, max_members;
 };
 
 constexpr int kNumWarps = PKV_DECODE_WARPS;
 constexpr int kMinPartBlocks = 2 * kNumWarps;   // finest split: 8 blocks per partition
-inline size_t workspace_need(int B, int Hq, int D, int parts) {
-    return (size_t)B * Hq * parts * ((size_t)D + 2) * sizeof(float);
+constexpr int kPrefixRows = 8;                  // query rows of a prefix-group CTA
+
+inline size_t workspace_need(int B, int Hq, int D, int slots) {
+    return (size_t)B * Hq * slots * ((size_t)D + 2) * sizeof(float);
 }
 
-// Partition size: about PKV_PART_BYTES of K+V per CTA; smaller when that leaves fewer
-// than ~2 waves of CTAs; never finer than kMinPartBlocks; one partition when the
-// workspace cannot hold the split.
-inline int choose_part_blocks(const Args& a, int tile_bytes, int ctas_per_sm, int* parts_out) {
+// Partition size: about PKV_PART_BYTES of K+V per CTA; smaller when that leaves
+// fewer than ~2 waves of CTAs; never finer than kMinPartBlocks; coarser until the
+// workspace holds `copies` sets of partials (2 for grouped decode: prefix and
+// own range); one partition when even that does not fit (then *parts_out = 1).
+inline int choose_part_blocks(const Args& a, int tile_bytes, int ctas_per_sm, int copies,
+                              int* parts_out) {
     const int MB = a.max_blocks;
     int target = PKV_PART_BYTES / (2 * tile_bytes);
     target = (target + kNumWarps - 1) / kNumWarps * kNumWarps;
@@ -773,7 +839,8 @@ inline int choose_part_blocks(const Args& a, int tile_bytes, int ctas_per_sm, in
     }
     int parts = (MB + PB - 1) / PB;
     while (parts > 1 && (a.workspace == nullptr ||
-                         workspace_need(a.num_seqs, a.num_heads, a.head_dim, parts) > a.workspace_bytes)) {
+                         workspace_need(a.num_seqs, a.num_heads, a.head_dim, copies * parts) >
+                             a.workspace_bytes)) {
         PB *= 2;
         if (PB >= MB) PB = MB;
         parts = (MB + PB - 1) / PB;
@@ -783,15 +850,36 @@ inline int choose_part_blocks(const Args& a, int tile_bytes, int ctas_per_sm, in
     return PB;
 }
 
-template <class Math, typename QT, int D, int BS, int G>
-int launch_variant(const Args& a) {
+template <class Math, typename QT, int D, int BS, int G, bool PREFIX>
+int launch_kernel(const Params& p, dim3 grid, cudaStream_t stream) {
     using P = Pipe<Math, D, BS, G, kNumWarps>;
-    auto kern = paged_decode_kernel<Math, QT, D, BS, G, kNumWarps>;
+    auto kern = paged_decode_kernel<Math, QT, D, BS, G, kNumWarps, PREFIX>;
     int occ = 0;
     const int st = kernel_setup(reinterpret_cast<const void*>(kern), P::kSmem, kNumWarps * 32, &occ);
     if (st != PKV_OK) return st;
+    kern<<<grid, kNumWarps * 32, P::kSmem, stream>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PKV_OK : cuda_fail("decode: kernel launch", e);
+}
+
+template <class Math, typename QT, int D, int BS, int G>
+int launch_variant(const Args& a) {
+    using P = Pipe<Math, D, BS, G, kNumWarps>;
+    using KV = typename Math::KVT;
+    // grouped decode needs the tensor-core prefix kernel (bf16 / E4M3 caches),
+    // groups whose members fit the CTA's query rows, and room for both partial sets
+    constexpr bool kCanGroup = !std::is_same<KV, float>::value;
+    const int gh = a.num_heads / a.num_kv_heads;
+    bool grouped = kCanGroup && a.group_members && a.group_prefix && a.start_blocks &&
+                   a.num_groups > 0 && a.max_members > 0 && a.max_members * gh <= kPrefixRows;
+    int occ = 0;
+    int st = kernel_setup(reinterpret_cast<const void*>(paged_decode_kernel<Math, QT, D, BS, G, kNumWarps, false>),
+                          P::kSmem, kNumWarps * 32, &occ);
+    if (st != PKV_OK) return st;
     int parts = 1;
-    const int PB = choose_part_blocks(a, P::kTile, occ, &parts);
+    int PB = choose_part_blocks(a, P::kTile, occ, grouped ? 2 : 1, &parts);
+    if (grouped && workspace_need(a.num_seqs, a.num_heads, a.head_dim, 2 * parts) > a.workspace_bytes)
+        grouped = false;                                     // no room for the prefix partials
 
     Params p;
     p.out = a.out;
@@ -800,8 +888,6 @@ int launch_variant(const Args& a) {
     p.v_pool = static_cast<const char*>(a.v_pool);
     p.block_tables = a.block_tables;
     p.seq_lens = a.seq_lens;
-    p.ws_o = parts > 1 ? static_cast<float*>(a.workspace) : nullptr;
-    p.ws_ml = parts > 1 ? p.ws_o + (size_t)a.num_seqs * a.num_heads * parts * D : nullptr;
     p.err = a.err;
     p.num_seqs = a.num_seqs;
     p.max_blocks = a.max_blocks;
@@ -812,14 +898,31 @@ int launch_variant(const Args& a) {
     p.max_parts = parts;
     p.qscale = a.scale * a.k_scale * kLog2e;
     p.v_scale = a.v_scale;
+    p.start_blocks = grouped ? a.start_blocks : nullptr;
+    p.group_members = grouped ? a.group_members : nullptr;
+    p.group_prefix = grouped ? a.group_prefix : nullptr;
+    p.max_members = grouped ? a.max_members : 0;
+    p.slots = grouped ? 2 * parts : parts;
+    p.slot_base = grouped ? parts : 0;
+    p.prefix_part_blocks = PB;
+    const bool split = grouped || parts > 1;
+    p.ws_o = split ? static_cast<float*>(a.workspace) : nullptr;
+    p.ws_ml = split ? p.ws_o + (size_t)a.num_seqs * a.num_heads * p.slots * D : nullptr;
 
-    dim3 grid(parts, a.num_kv_heads, a.num_seqs);
-    kern<<<grid, kNumWarps * 32, P::kSmem, a.stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail("decode: kernel launch", e);
-    if (parts > 1) {
+    if constexpr (kCanGroup) {
+        if (grouped) {                                       // shared prefixes, read once per group
+            Params pp = p;
+            pp.slot_base = 0;
+            st = launch_kernel<MmaMath<KV, D, BS, kPrefixRows>, QT, D, BS, kPrefixRows, true>(
+                pp, dim3(parts, a.num_kv_heads, a.num_groups), a.stream);
+            if (st != PKV_OK) return st;
+        }
+    }
+    st = launch_kernel<Math, QT, D, BS, G, false>(p, dim3(parts, a.num_kv_heads, a.num_seqs), a.stream);
+    if (st != PKV_OK) return st;
+    if (split) {
         split_reduce_kernel<QT><<<dim3(a.num_heads, a.num_seqs), 128, 0, a.stream>>>(p, D, BS);
-        e = cudaGetLastError();
+        const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail("decode: split merge launch", e);
     }
     return PKV_OK;

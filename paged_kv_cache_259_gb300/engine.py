@@ -19,7 +19,7 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from . import (BlockManager, copy_blocks, paged_attention_decode,
+from . import (BlockManager, copy_blocks, paged_attention_decode, paged_attention_decode_grouped,
                paged_attention_workspace_size, pool_shapes, reshape_and_cache)
 
 
@@ -31,10 +31,21 @@ class StepPlan:
     pairs: np.ndarray        # int64 [P, 2]
     tables: np.ndarray       # int32 [B, max_blocks]
     lens: np.ndarray         # int32 [B]
+    seq_prefix: np.ndarray = None     # int32 [B]; shared-prefix groups (may be empty)
+    group_members: np.ndarray = None  # int32 [g, max_members]
+    group_prefix: np.ndarray = None   # int32 [g]
+
+    @property
+    def num_groups(self):
+        return 0 if self.group_members is None else int(self.group_members.shape[0])
 
     def host_tensors(self, pin=True):
         t = {"slots": torch.from_numpy(self.slots), "pairs": torch.from_numpy(self.pairs),
              "tables": torch.from_numpy(self.tables), "lens": torch.from_numpy(self.lens)}
+        if self.num_groups:
+            t.update({"seq_prefix": torch.from_numpy(self.seq_prefix),
+                      "group_members": torch.from_numpy(self.group_members),
+                      "group_prefix": torch.from_numpy(self.group_prefix)})
         if pin:
             t = {k: v.pin_memory() for k, v in t.items()}
         return t
@@ -44,7 +55,10 @@ class StepPlan:
                 for k, v in self.host_tensors(pin=non_blocking).items()}
 
     def nbytes(self):
-        return self.slots.nbytes + self.pairs.nbytes + self.tables.nbytes + self.lens.nbytes
+        n = self.slots.nbytes + self.pairs.nbytes + self.tables.nbytes + self.lens.nbytes
+        if self.num_groups:
+            n += self.seq_prefix.nbytes + self.group_members.nbytes + self.group_prefix.nbytes
+        return n
 
 
 class PagedKVCache:
@@ -100,18 +114,39 @@ class PagedKVCache:
             t = torch.as_tensor(np.asarray(pairs, dtype=np.int64).reshape(-1, 2), device=self.device)
             copy_blocks(self.k_pool, self.v_pool, t, stream=stream)
 
-    def plan_step(self, seq_ids, max_blocks=None):
+    def plan_step(self, seq_ids, max_blocks=None, group_prefixes=True):
+        """Host half of a step: one slot per sequence (CoW pairs included), dense
+        tables and, when sequences share leading full blocks (forks of one prompt),
+        the prefix groups that let the decode read those blocks once per group."""
         ids = np.asarray(seq_ids, dtype=np.int64)
         slots, pairs = self.bm.append_slots(ids)
         if max_blocks is None:
             max_blocks = max(1, max(-(-self.bm.seq_len(int(s)) // self.block_size) for s in ids))
         tables, lens = self.bm.build_tables(ids, max_blocks)
-        return StepPlan(ids, slots, pairs, tables, lens)
+        plan = StepPlan(ids, slots, pairs, tables, lens)
+        if group_prefixes and self.k_pool.dtype != torch.float32:
+            max_members = max(1, 8 // (self.num_heads // self.num_kv_heads))
+            members, prefix, seq_prefix = self.bm.prefix_groups(ids, max_members)
+            if len(members):
+                plan.seq_prefix, plan.group_members, plan.group_prefix = seq_prefix, members, prefix
+        return plan
 
     def workspace(self, batch, max_blocks):
+        """Split-KV scratch, sized for the grouped decode (twice the plain size)."""
         n = paged_attention_workspace_size(batch, self.num_heads, self.head_dim, self.block_size,
                                            max_blocks)
-        return torch.empty(max(n, 16), dtype=torch.uint8, device=self.device)
+        return torch.empty(max(2 * n, 16), dtype=torch.uint8, device=self.device)
+
+    def decode(self, q, dev_plan, out, scale, k_scale=1.0, v_scale=1.0, workspace=None,
+               stream=None):
+        """The attention of a step (grouped when the plan found shared prefixes)."""
+        if "group_members" in dev_plan:
+            return paged_attention_decode_grouped(
+                out, q, self.k_pool, self.v_pool, dev_plan["tables"], dev_plan["lens"], scale,
+                dev_plan["seq_prefix"], dev_plan["group_members"], dev_plan["group_prefix"],
+                k_scale, v_scale, workspace, stream)
+        return paged_attention_decode(out, q, self.k_pool, self.v_pool, dev_plan["tables"],
+                                      dev_plan["lens"], scale, k_scale, v_scale, workspace, stream)
 
     def step(self, q, k_new, v_new, dev_plan, out, scale, k_scale=1.0, v_scale=1.0,
              workspace=None, stream=None):
@@ -121,6 +156,4 @@ class PagedKVCache:
             copy_blocks(self.k_pool, self.v_pool, pairs, stream=stream)
         reshape_and_cache(k_new, v_new, self.k_pool, self.v_pool, dev_plan["slots"],
                           k_scale, v_scale, stream=stream)
-        paged_attention_decode(out, q, self.k_pool, self.v_pool, dev_plan["tables"],
-                               dev_plan["lens"], scale, k_scale, v_scale, workspace, stream)
-        return out
+        return self.decode(q, dev_plan, out, scale, k_scale, v_scale, workspace, stream)

@@ -132,17 +132,16 @@ def gqa_chat_bf16(B=256):
                              torch.bfloat16, "bf16", 1.0 / math.sqrt(128))
 
 
-def shared_prefix_bf16(fork_step=False, groups=64, per_group=4, prompt=520, max_suffix=256):
+def shared_prefix(fork_step=False, groups=64, per_group=4, prompt=520, max_suffix=256, Hq=40,
+                  Hkv=40, D=128, bs=16, kv="bf16", seed=3, name=None):
     """Parallel sampling: ``groups`` prompts of ``prompt`` tokens, each forked into
-    ``per_group`` sequences (40 heads MHA, D 128, bs 16).
+    ``per_group`` sequences that share the prompt's blocks.
 
     ``fork_step=True``: every sequence is still at the prompt length, so the step's
     first append into the shared partial block is the copy-on-write step.
     Otherwise each sequence first grows by a suffix ~ U[0, max_suffix] (untimed).
     """
-    seed = 3
     rng = np.random.default_rng(seed)
-    bs, Hq, D = 16, 40, 128
     n = groups * per_group
     suffix = np.zeros(n, dtype=np.int64) if fork_step else rng.integers(0, max_suffix, size=n, endpoint=True)
     # pool: every prompt's blocks plus, per sequence, enough blocks for its own tail
@@ -163,12 +162,19 @@ def shared_prefix_bf16(fork_step=False, groups=64, per_group=4, prompt=520, max_
             if suffix[sid]:
                 script.append(("append", sid, int(suffix[sid])))
     lens = prompt + suffix + 1
-    name = "shared_prefix_fork_bf16" if fork_step else "shared_prefix_bf16"
-    return Workload(name=name, B=n, Hq=Hq, Hkv=Hq, D=D, bs=bs, NB=NB, seed=seed,
-                    scale=1.0 / math.sqrt(128), src_dtype=torch.bfloat16, kv_dtype="bf16",
+    if name is None:
+        name = "shared_prefix_fork_bf16" if fork_step else "shared_prefix_bf16"
+    src = torch.float32 if kv == "f32" else torch.bfloat16
+    return Workload(name=name, B=n, Hq=Hq, Hkv=Hkv, D=D, bs=bs, NB=NB, seed=seed,
+                    scale=1.0 / math.sqrt(D), src_dtype=src, kv_dtype=kv,
                     free_order=free_order, script=script, step_seqs=list(range(n)),
                     final_lens=lens, notes={"groups": groups, "per_group": per_group,
                                             "prompt": prompt})
+
+
+def shared_prefix_bf16(fork_step=False, groups=64, per_group=4, prompt=520, max_suffix=256):
+    """64 groups x 4 samples of a 520-token prompt, 40 heads MHA, D 128, bs 16."""
+    return shared_prefix(fork_step, groups, per_group, prompt, max_suffix)
 
 
 def long_fp8(bs=16, B=16, L=32768):

@@ -107,3 +107,53 @@ def test_workload_setup_and_step_match_oracle(name):
     same_state(a, o)
     if name == "shared_prefix_fork_bf16":
         assert len(pairs) == 64 * 3          # 3 of 4 writers copy; the last writes in place
+
+
+def test_prefix_groups_share_full_leading_blocks():
+    """bm_prefix_groups against the oracle's tables: members share the group's
+    leading block ids, those blocks are full for every member, the prefix is
+    maximal, no sequence is in two groups, group sizes respect max_members."""
+    library()
+    rng = np.random.default_rng(5)
+    for trial in range(30):
+        bs = int(rng.choice([1, 2, 4, 16]))
+        nb = 400
+        free = rng.permutation(nb)
+        a = pkv.BlockManager(nb, bs, free)
+        o = OracleBM(nb, bs, free)
+        seqs = []
+        for p in range(int(rng.integers(1, 4))):
+            sid = len(seqs)
+            for m in (a, o):
+                m.add_seq(sid)
+            n0 = int(rng.integers(0, 40))
+            a.append_n(sid, n0)
+            for _ in range(n0):
+                o.append_slot(sid)
+            seqs.append(sid)
+            for c in range(int(rng.integers(0, 6))):
+                cid = max(seqs) + 1
+                a.fork(sid, cid)
+                o.fork(sid, cid)
+                k = int(rng.integers(0, 12))
+                a.append_n(cid, k)
+                for _ in range(k):
+                    o.append_slot(cid)
+                seqs.append(cid)
+        ids = list(rng.permutation(seqs))
+        maxm = int(rng.choice([2, 3, 4, 8]))
+        members, prefix, seq_prefix = a.prefix_groups(ids, maxm)
+        seen = set()
+        for row, pre in zip(members, prefix):
+            ms = [int(m) for m in row if m >= 0]
+            assert 2 <= len(ms) <= maxm and pre >= 1
+            tabs = [o.tables[ids[m]] for m in ms]
+            full = min(o.lens[ids[m]] // bs for m in ms)
+            assert pre <= full
+            assert all(t[:pre] == tabs[0][:pre] for t in tabs)
+            if pre < full:                               # maximal
+                assert len({t[pre] for t in tabs}) > 1
+            for m in ms:
+                assert m not in seen and seq_prefix[m] == pre
+                seen.add(m)
+        assert all(seq_prefix[i] == 0 for i in range(len(ids)) if i not in seen)

@@ -216,3 +216,61 @@ def test_host_checks_reject_bad_arguments():
     with pytest.raises(pkv.PagedKVError) as e:
         pkv.paged_attention_decode(torch.empty_like(q), q, kp, vp, bt, lens, 0.1)
     assert e.value.status == -1
+
+
+# ------------------------------------------------------------ prefix-grouped decode
+GROUPED = [  # (kv, Hq, Hkv, D, bs, per_group, prompt, fork_step)
+    ("bf16", 8, 8, 128, 16, 4, 200, False),     # MHA, 4 members
+    ("bf16", 8, 8, 64, 32, 6, 333, False),      # 6 forks: groups of 6 (8 rows allow it)
+    ("bf16", 16, 8, 128, 16, 5, 97, False),     # GQA 2: 5 forks -> groups of 4 and 1
+    ("bf16", 16, 4, 128, 16, 3, 150, True),     # GQA 4: groups of 2 and 1, CoW step
+    ("e4m3", 16, 4, 128, 16, 2, 300, False),    # E4M3 cache
+    ("e4m3", 8, 8, 128, 32, 4, 64, True),       # prompt fills its blocks exactly
+    ("bf16", 64, 8, 128, 16, 3, 150, False),    # GQA 8: one member per group -> plain path
+]
+
+
+@pytest.mark.parametrize("kv,Hq,Hkv,D,bs,per_group,prompt,fork", GROUPED)
+def test_grouped_prefix_decode_matches_oracle(kv, Hq, Hkv, D, bs, per_group, prompt, fork):
+    w = wl.shared_prefix(fork_step=fork, groups=3, per_group=per_group, prompt=prompt,
+                         max_suffix=70, Hq=Hq, Hkv=Hkv, D=D, bs=bs, kv=kv,
+                         seed=per_group * 13 + prompt, name=f"grouped_{kv}_{Hq}_{Hkv}")
+    inp = Inputs(w)
+    g = run_gpu(inp)
+    assert g["err"] == 0
+    plan = g["plan"]
+    G = Hq // Hkv
+    if 8 // G >= 2:
+        assert plan.num_groups > 0
+        # every group: members share the prefix's block ids, full for all of them
+        for members, pre in zip(plan.group_members, plan.group_prefix):
+            ms = [m for m in members if m >= 0]
+            assert 2 <= len(ms) <= 8 // G and pre >= 1
+            for m in ms:
+                assert plan.seq_prefix[m] == pre and plan.lens[m] >= pre * bs
+                assert np.array_equal(plan.tables[m, :pre], plan.tables[ms[0], :pre])
+    else:
+        assert plan.num_groups == 0
+    o = run_oracle(inp)
+    check_indexing(g, o)
+    check_cache_writes(inp, g, o, whole_pool=True)
+    assert_close(g["out"].numpy(), o["out"], kv, w.name)
+    # the plain (ungrouped) decode agrees with the grouped one
+    cache = g["cache"]
+    dev = g["plan"].device_tensors("cuda")
+    for k in ("seq_prefix", "group_members", "group_prefix"):
+        dev.pop(k, None)
+    out2 = torch.empty(w.B, w.Hq, w.D, dtype=w.src_dtype, device="cuda")
+    cache.decode(inp.q.cuda(), dev, out2, w.scale, inp.ks, inp.vs,
+                 cache.workspace(w.B, w.max_blocks_per_seq))
+    assert pkv.get_device_error() == 0
+    assert_close(out2.float().cpu().numpy(), o["out"], kv, w.name + " plain")
+
+
+def test_grouped_decode_without_workspace_falls_back_to_plain():
+    w = wl.shared_prefix(groups=2, per_group=4, prompt=100, max_suffix=40, Hq=8, Hkv=8)
+    inp = Inputs(w)
+    g = run_gpu(inp, workspace=False)
+    assert g["err"] == 0 and g["plan"].num_groups == 2
+    o = run_oracle(inp)
+    assert_close(g["out"].numpy(), o["out"], "bf16", "grouped, no workspace")
