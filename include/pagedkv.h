@@ -135,23 +135,24 @@ PKV_API int paged_attention_decode(void* out, const void* q,
  * "Como funciona": the prompt's KV is stored once); this call also reads it once.
  *
  * A group is up to max_members sequences (batch indices) whose block tables
- * begin with the same group_prefix_blocks[g] physical blocks, every one of them
- * full for every member. The K/V tiles of those blocks are loaded once per
- * (group, kv head) and attended by all members' query heads together (the
- * members' heads are the rows of the tensor-core tiles); each sequence's
- * remaining blocks are attended on their own; split-KV merging combines both.
+ * begin with the same group_prefix_blocks[g] physical blocks, full for every
+ * member. One CTA per (partition, group, kv head) walks the group's block list:
+ * the shared blocks, loaded once and attended by every member's query heads (the
+ * members' heads are the rows of the tensor-core tiles), then each member's own
+ * blocks, attended by that member's rows only. Long lists are split like long
+ * sequences and merged; the sequences in no group are decoded as usual.
  *
- *   seq_prefix_blocks    device int32 [num_seqs]: the prefix length of the
- *                        sequence's group, 0 for a sequence in no group
+ *   seq_group            device int32 [num_seqs]: the sequence's group, -1 if none
  *   group_members        device int32 [num_groups][max_members], -1 padded
  *   group_prefix_blocks  device int32 [num_groups]
  * Preconditions (the block manager's bm_prefix_groups meets them): a sequence
- * is in at most one group; seq_prefix_blocks of every member equals its group's
- * prefix; the prefix blocks are the same ids in every member's table and full.
- * Violations give wrong outputs, never out-of-range accesses.
- * Needs max_members * (num_heads / num_kv_heads) <= 8, a bf16 or E4M3 cache and
- * a workspace of twice paged_attention_workspace_size(); otherwise (or with
- * num_groups == 0) it computes exactly what paged_attention_decode computes.
+ * is in at most one group and seq_group names it; the prefix blocks are the same
+ * ids in every member's table. The prefix is clamped to the blocks every member
+ * has filled; any other violation gives wrong outputs, never out-of-range
+ * accesses.
+ * Needs max_members <= 8 and max_members * (num_heads / num_kv_heads) <= 8 and a
+ * bf16 or E4M3 cache; otherwise (or with num_groups == 0) it computes exactly
+ * what paged_attention_decode computes. Works with or without a workspace.
  * ---------------------------------------------------------------------- */
 PKV_API int paged_attention_decode_grouped(void* out, const void* q,
                                    const void* k_pool, const void* v_pool,
@@ -160,15 +161,15 @@ PKV_API int paged_attention_decode_grouped(void* out, const void* q,
                                    int num_heads, int num_kv_heads, int head_dim,
                                    int block_size, float scale, int q_dtype, int kv_dtype,
                                    float k_scale, float v_scale,
-                                   const int32_t* seq_prefix_blocks,
+                                   const int32_t* seq_group,
                                    const int32_t* group_members,
                                    const int32_t* group_prefix_blocks,
                                    int num_groups, int max_members,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of workspace that lets paged_attention_decode use its finest split for
- * these sizes (an upper bound; any size works, smaller ones split less). The
- * grouped call wants twice this. */
+ * these sizes (an upper bound; any size works, smaller ones split less). A
+ * grouped call splits long group lists too when it has max_members times this. */
 PKV_API size_t paged_attention_workspace_size(int num_seqs, int num_heads, int head_dim,
                                       int block_size, int max_blocks_per_seq);
 
@@ -308,11 +309,12 @@ PKV_API int bm_num_free(const pkv_block_manager* bm);
  * batch order, at most max_members per group); a group's prefix is the number
  * of leading block ids common to all members that are full for every member.
  * Writes group_members [n][max_members] (batch indices, -1 padded; at most n
- * groups), group_prefix [n], seq_prefix [n] (0 outside groups) and *num_groups.
- * Groups with a prefix of 0 blocks or a single member are not emitted. */
+ * groups), group_prefix [n], seq_group [n] (the sequence's group or -1) and
+ * *num_groups. Groups with a prefix of 0 blocks or a single member are not
+ * emitted. */
 PKV_API int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
                      int max_members, int32_t* group_members, int32_t* group_prefix,
-                     int32_t* seq_prefix, int* num_groups);
+                     int32_t* seq_group, int* num_groups);
 /* The free list, front first, into out[0..cap); returns its length. */
 PKV_API int bm_free_list(const pkv_block_manager* bm, int32_t* out, int cap);
 

@@ -224,29 +224,27 @@ def paged_attention_decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale
 
 
 def paged_attention_decode_grouped(out, q, k_pool, v_pool, block_tables, seq_lens, scale,
-                                   seq_prefix_blocks, group_members, group_prefix_blocks,
+                                   seq_group, group_members, group_prefix_blocks,
                                    k_scale=1.0, v_scale=1.0, workspace=None, stream=None):
     """``paged_attention_decode`` reading each shared prefix once per group.
 
-    seq_prefix_blocks int32 ``[B]``; group_members int32 ``[num_groups, max_members]``
-    (batch indices, -1 padded); group_prefix_blocks int32 ``[num_groups]`` -- as
-    ``BlockManager.prefix_groups`` returns them. The workspace should hold twice
-    ``paged_attention_workspace_size``; without room the call computes the plain
-    decode.
+    seq_group int32 ``[B]`` (group or -1); group_members int32 ``[num_groups,
+    max_members]`` (batch indices, -1 padded); group_prefix_blocks int32
+    ``[num_groups]`` -- as ``BlockManager.prefix_groups`` returns them.
     """
     lib = load_library()
     for t, n in ((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
                  (block_tables, "block_tables"), (seq_lens, "seq_lens"),
-                 (seq_prefix_blocks, "seq_prefix_blocks"), (group_members, "group_members"),
+                 (seq_group, "seq_group"), (group_members, "group_members"),
                  (group_prefix_blocks, "group_prefix_blocks")):
         _cuda(t, n)
-    for t in (block_tables, seq_lens, seq_prefix_blocks, group_members, group_prefix_blocks):
+    for t in (block_tables, seq_lens, seq_group, group_members, group_prefix_blocks):
         if t.dtype != torch.int32:
             raise TypeError("tables, lengths and group arrays must be int32")
     B, Hq, D = q.shape
     NB, Hkv, bs, D2 = _pool_dims(k_pool, v_pool)
     if out.shape != q.shape or out.dtype != q.dtype or D2 != D or seq_lens.shape != (B,) or \
-            seq_prefix_blocks.shape != (B,) or group_members.dim() != 2 or \
+            seq_group.shape != (B,) or group_members.dim() != 2 or \
             group_prefix_blocks.shape != (group_members.shape[0],):
         raise ValueError("inconsistent shapes")
     ws_ptr, ws_bytes = None, 0
@@ -258,7 +256,7 @@ def paged_attention_decode_grouped(out, q, k_pool, v_pool, block_tables, seq_len
             out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
             block_tables.data_ptr(), seq_lens.data_ptr(), B, block_tables.shape[1], NB,
             Hq, Hkv, D, bs, float(scale), _dt(q, "q"), _dt(k_pool, "k_pool"), float(k_scale),
-            float(v_scale), seq_prefix_blocks.data_ptr(), group_members.data_ptr(),
+            float(v_scale), seq_group.data_ptr(), group_members.data_ptr(),
             group_prefix_blocks.data_ptr(), group_members.shape[0], group_members.shape[1],
             ws_ptr, ws_bytes, _stream_ptr(stream, q.device))
     _check(st, "paged_attention_decode_grouped")
@@ -433,17 +431,17 @@ class BlockManager:
 
     def prefix_groups(self, seq_ids, max_members):
         """Groups of the batch that share leading full blocks (see bm_prefix_groups):
-        (members int32 [g, max_members], prefix int32 [g], seq_prefix int32 [n])."""
+        (members int32 [g, max_members], prefix int32 [g], seq_group int32 [n])."""
         ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
         n = len(ids)
         members = np.full((max(1, n), max_members), -1, dtype=np.int32)
         prefix = np.zeros(max(1, n), dtype=np.int32)
-        seq_prefix = np.zeros(max(1, n), dtype=np.int32)
+        seq_group = np.full(max(1, n), -1, dtype=np.int32)
         ng = ctypes.c_int(0)
         _check(self._lib.bm_prefix_groups(self._h, _i64p(ids), n, max_members, _i32p(members),
-                                          _i32p(prefix), _i32p(seq_prefix), ctypes.byref(ng)),
+                                          _i32p(prefix), _i32p(seq_group), ctypes.byref(ng)),
                "bm_prefix_groups")
-        return members[:ng.value].copy(), prefix[:ng.value].copy(), seq_prefix[:n].copy()
+        return members[:ng.value].copy(), prefix[:ng.value].copy(), seq_group[:n].copy()
 
     def seq_len(self, sid):
         n = ctypes.c_int(0)

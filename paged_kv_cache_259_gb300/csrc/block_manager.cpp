@@ -222,10 +222,10 @@ int bm_num_free(const pkv_block_manager* bm) { return bm ? (int)bm->free_list.si
 // by their first block, and take as each group's prefix the leading block ids
 // all members have in common, up to the blocks every member has filled.
 int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n, int max_members,
-                     int32_t* group_members, int32_t* group_prefix, int32_t* seq_prefix,
+                     int32_t* group_members, int32_t* group_prefix, int32_t* seq_group,
                      int* num_groups) {
     if (!bm || n < 0 || max_members < 1 || !num_groups ||
-        (n > 0 && (!seq_ids || !group_members || !group_prefix || !seq_prefix)))
+        (n > 0 && (!seq_ids || !group_members || !group_prefix || !seq_group)))
         return PKV_ERR_INVALID_ARG;
     *num_groups = 0;
     std::vector<const pkv_block_manager::Seq*> seqs(n);
@@ -233,7 +233,7 @@ int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
         auto it = bm->seqs.find(seq_ids[i]);
         if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
         seqs[i] = &it->second;
-        seq_prefix[i] = 0;
+        seq_group[i] = -1;
     }
     std::unordered_map<int32_t, std::vector<int>> buckets;
     std::vector<int32_t> order;                      // first blocks in batch order
@@ -267,7 +267,7 @@ int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
             for (int k = 0; k < max_members; ++k)
                 row[k] = c + k < e ? (int32_t)mem[c + k] : -1;
             group_prefix[ng] = (int32_t)prefix;
-            for (size_t k = c; k < e; ++k) seq_prefix[mem[k]] = (int32_t)prefix;
+            for (size_t k = c; k < e; ++k) seq_group[mem[k]] = ng;
             ++ng;
         }
     }

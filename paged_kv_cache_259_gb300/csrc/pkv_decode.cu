@@ -29,7 +29,7 @@ int decode_common(void* out, const void* q, const void* k_pool, const void* v_po
                   const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
                   int max_blocks_per_seq, int num_blocks, int num_heads, int num_kv_heads,
                   int head_dim, int block_size, float scale, int q_dtype, int kv_dtype,
-                  float k_scale, float v_scale, const int32_t* start_blocks,
+                  float k_scale, float v_scale, const int32_t* seq_group,
                   const int32_t* group_members, const int32_t* group_prefix, int num_groups,
                   int max_members, void* workspace, size_t workspace_bytes, void* stream) {
     using namespace pkv;
@@ -70,7 +70,7 @@ int decode_common(void* out, const void* q, const void* k_pool, const void* v_po
     a.workspace = workspace;
     a.workspace_bytes = workspace ? workspace_bytes : 0;
     a.stream = static_cast<cudaStream_t>(stream);
-    a.start_blocks = start_blocks;
+    a.seq_group = seq_group;
     a.group_members = group_members;
     a.group_prefix = group_prefix;
     a.num_groups = num_groups;
@@ -103,18 +103,18 @@ int paged_attention_decode_grouped(void* out, const void* q, const void* k_pool,
                                    const int32_t* seq_lens, int num_seqs, int max_blocks_per_seq,
                                    int num_blocks, int num_heads, int num_kv_heads, int head_dim,
                                    int block_size, float scale, int q_dtype, int kv_dtype,
-                                   float k_scale, float v_scale, const int32_t* seq_prefix_blocks,
+                                   float k_scale, float v_scale, const int32_t* seq_group,
                                    const int32_t* group_members, const int32_t* group_prefix_blocks,
                                    int num_groups, int max_members, void* workspace,
                                    size_t workspace_bytes, void* stream) {
-    if (num_groups < 0 || (num_groups > 0 && (max_members <= 0 || !seq_prefix_blocks ||
+    if (num_groups < 0 || (num_groups > 0 && (max_members <= 0 || !seq_group ||
                                               !group_members || !group_prefix_blocks)))
         return PKV_ERR_INVALID_ARG;
     if (num_groups > 65535) return PKV_ERR_UNSUPPORTED;
     return decode_common(out, q, k_pool, v_pool, block_tables, seq_lens, num_seqs,
                          max_blocks_per_seq, num_blocks, num_heads, num_kv_heads, head_dim,
                          block_size, scale, q_dtype, kv_dtype, k_scale, v_scale,
-                         num_groups > 0 ? seq_prefix_blocks : nullptr,
+                         num_groups > 0 ? seq_group : nullptr,
                          num_groups > 0 ? group_members : nullptr,
                          num_groups > 0 ? group_prefix_blocks : nullptr, num_groups, max_members,
                          workspace, workspace_bytes, stream);

@@ -66,6 +66,7 @@ namespace decode {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxMembers = 8;                 // members of a prefix group (<= query rows)
 
 struct Params {
     void* out;
@@ -82,13 +83,12 @@ struct Params {
     float qscale;     // scale * k_scale * log2(e)
     float v_scale;
     // prefix-grouped decode (null / 0 otherwise)
-    const int32_t* start_blocks;   // [B] first block this launch covers (shared prefix length)
+    const int32_t* seq_group;      // [B] group of the sequence, -1 for none
     const int32_t* group_members;  // [num_groups][max_members] batch indices, -1 padded
     const int32_t* group_prefix;   // [num_groups] shared full blocks of the group
     int max_members;
-    int slot_base;                 // workspace slot of partition 0 of this launch
+    int group_part_blocks;         // partition size of the group launch
     int slots;                     // workspace slots per (sequence, head)
-    int prefix_part_blocks;        // partition size of the prefix launch (merge only)
 };
 
 template <typename T> struct Elt;
@@ -374,10 +374,13 @@ struct MmaMath {
         st.l = 0.f;
     }
 
+    // row_live: bit r set if query row r attends over this tile (all rows, except
+    // in a group CTA's own tiles, which belong to one member's rows)
     __device__ __forceinline__ static void tile(State& st, const unsigned char* kt,
                                                 const unsigned char* vt, int ntok, int lane,
-                                                float qscale, const float*, float*) {
+                                                float qscale, const float*, float*, int row_live) {
         const int r = lane >> 2, c = lane & 3;
+        const bool live = (row_live >> r) & 1;
         const uint32_t kbase = smem_addr(kt), vbase = smem_addr(vt);
 #pragma unroll
         for (int h = 0; h < SUB; ++h) {
@@ -431,20 +434,23 @@ struct MmaMath {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int tok = F8 ? 16 * h + 4 * c + 2 * u + e : 16 * h + 8 * u + 2 * c + e;
-                    s[u][e] = tok < ntok ? s[u][e] * qscale : -INFINITY;
+                    s[u][e] = (live && tok < ntok) ? s[u][e] * qscale : -INFINITY;
                     mx = fmaxf(mx, s[u][e]);
                 }
             mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
-            const float m_new = fmaxf(st.m, mx);             // finite: token 16h is valid
-            const float alpha = exp2f(st.m - m_new);
+            // a row with no live score yet keeps m = -inf; exponents are taken
+            // against 0 then, so nothing becomes NaN and its weights stay 0
+            const float m_new = fmaxf(st.m, mx);
+            const float m_ref = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = exp2f(st.m - m_ref);
             float pr[2][2];
             float psum = 0.f;
 #pragma unroll
             for (int u = 0; u < 2; ++u)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    pr[u][e] = exp2f(s[u][e] - m_new);
+                    pr[u][e] = exp2f(s[u][e] - m_ref);
                     psum += pr[u][e];
                 }
             st.l = st.l * alpha + psum;
@@ -542,8 +548,9 @@ struct Pipe {
     // shared-memory carve-up: ring | mbarriers | stage block ids | q rows | per-warp
     // scratch; the q rows and the scratch start on 16-byte boundaries (float4 reads)
     static constexpr int kBarOff = kRingBytes;
-    static constexpr int kIdOff = kBarOff + NW * kStages * 8;
-    static constexpr int kQOff = (kIdOff + NW * kStages * 4 + 15) / 16 * 16;
+    static constexpr int kIdOff = kBarOff + NW * kStages * 8;          // block id per stage
+    static constexpr int kInfoOff = kIdOff + NW * kStages * 4;         // ntok | live rows << 8
+    static constexpr int kQOff = (kInfoOff + NW * kStages * 4 + 15) / 16 * 16;
     static constexpr int kWarpOff = kQOff + (Math::kCtaSmemFloats * 4 + 15) / 16 * 16;
     static constexpr int kSmem = kWarpOff + NW * Math::kWarpSmemFloats * 4;
     static_assert(kRingBytes % 128 == 0 && kQOff % 16 == 0 && kWarpOff % 16 == 0 &&
@@ -553,7 +560,7 @@ struct Pipe {
 };
 
 // Query row r of the CTA: (sequence, head), or sequence -1 for an unused row.
-// Regular launch: the G heads of kv head hk of sequence b. Prefix launch: row
+// Regular launch: the G heads of kv head hk of sequence b. Group launch: row
 // r = m * Gh + g is head hk * Gh + g of the group's m-th member (Gh = the
 // model's query heads per kv head), so every member shares the loaded tiles.
 template <bool PREFIX, int G>
@@ -587,34 +594,57 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
     float* qs = reinterpret_cast<float*>(smem + P::kQOff);
     float* wsm = reinterpret_cast<float*>(smem + P::kWarpOff);
 
-    // b: the sequence (regular launch) or the group (prefix launch) whose table
-    // row is read; start: first logical block of this launch's range
-    const int part = blockIdx.x, hk = blockIdx.y;
-    int b = blockIdx.z;
-    int L, start = 0, nblk;
+    // Regular launch: CTA (partition, kv head, sequence b) over blocks
+    // [part*PB, ...) of b. Group launch: CTA (partition, kv head, group g) over
+    // g's block list -- the P shared prefix blocks (every member's rows live),
+    // then each member's own blocks P.. (that member's rows live) -- so a group
+    // reads its prompt once and needs no second launch for the members' tails.
+    const int part = blockIdx.x, hk = blockIdx.y, key = blockIdx.z;
+    __shared__ int grp[4 * kMaxMembers + 4];   // b, L, own start, own count per member; P, T
+    int L = 0, nblk = 0;                       // regular launch: the sequence
+    int total;                                 // blocks (or list entries) of this CTA's key
     if constexpr (PREFIX) {
-        const int lead = p.group_members[(size_t)b * p.max_members];
-        if (lead < 0 || lead >= p.num_seqs) return;
-        const int Ll = min(max(p.seq_lens[lead], 0), p.max_blocks * BS);
-        nblk = min(max(p.group_prefix[b], 0), Ll / BS);     // full shared blocks only
-        L = nblk * BS;
-        b = lead;                                           // its table row holds the prefix
+        if (threadIdx.x == 0) {
+            int P = max(p.group_prefix[key], 0), n = 0;
+            for (int m = 0; m < kMaxMembers; ++m) {
+                const int sb = m < p.max_members ? p.group_members[(size_t)key * p.max_members + m] : -1;
+                const bool ok = sb >= 0 && sb < p.num_seqs;
+                const int Lm = ok ? min(max(p.seq_lens[sb], 0), p.max_blocks * BS) : 0;
+                grp[4 * m] = ok ? sb : -1;
+                grp[4 * m + 1] = Lm;
+                if (ok) P = min(P, Lm / BS);                // shared blocks are full for all
+                n += ok;
+            }
+            if (n == 0) P = 0;
+            int T = P;
+            for (int m = 0; m < kMaxMembers; ++m) {
+                const bool ok = m < p.max_members && grp[4 * m] >= 0;
+                const int own = ok ? (grp[4 * m + 1] + BS - 1) / BS - P : 0;
+                grp[4 * m + 2] = T;                          // list index of its first own block
+                grp[4 * m + 3] = own;
+                T += own;
+            }
+            grp[4 * kMaxMembers] = P;
+            grp[4 * kMaxMembers + 1] = T;
+        }
+        __syncthreads();
+        total = grp[4 * kMaxMembers + 1];
     } else {
-        L = p.seq_lens[b];
+        if (p.seq_group && p.seq_group[key] >= 0) return;  // attended by its group's CTAs
+        L = p.seq_lens[key];
         if (L < 0 || L > p.max_blocks * BS) {               // length the table cannot hold
             if (part == 0 && hk == 0 && threadIdx.x == 0) flag_error(p.err, kErrOutOfRange);
             L = L < 0 ? 0 : p.max_blocks * BS;
         }
         nblk = (L + BS - 1) / BS;
-        if (p.start_blocks) start = min(max(p.start_blocks[b], 0), nblk);
+        total = nblk;
     }
     const int PB = p.part_blocks;
-    const int nparts = (nblk - start + PB - 1) / PB;
-    if (PREFIX ? part >= nparts : part >= (nparts > 0 ? nparts : 1)) return;
-    const int blk0 = start + part * PB;                     // first block of this partition
-    const int nbp = max(0, min(PB, nblk - blk0));           // blocks in this partition
-    // the only contributor to its outputs: write `out` directly
-    const bool single = !PREFIX && start == 0 && nparts <= 1;
+    const int nparts = (total + PB - 1) / PB;
+    if (part >= (nparts > 0 ? nparts : 1)) return;          // beyond this key's list
+    const int blk0 = part * PB;                             // first entry of this partition
+    const int nbp = max(0, min(PB, total - blk0));          // entries in this partition
+    const bool single = nparts <= 1;                        // the only contributor: write `out`
 
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
 
@@ -626,7 +656,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
     for (int i = tid; i < G * D; i += NW * 32) {            // query rows of this CTA
         const int r = i / D;
         int seq, head;
-        row_target<PREFIX, G>(p, blockIdx.z, hk, r, &seq, &head);
+        row_target<PREFIX, G>(p, key, hk, r, &seq, &head);
         float qv = 0.f;
         if (seq >= 0) qv = to_f(static_cast<const QT*>(p.q)[((size_t)seq * p.num_heads + head) * D + i % D]);
         qs[i] = Math::kPrescaledQ ? qv * p.qscale : qv;
@@ -638,35 +668,68 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
     float* pb = wsm + w * Math::kWarpSmemFloats;
 
     const int nk = nbp > w ? (nbp - w + NW - 1) / NW : 0;  // this warp's blocks
-    const int32_t* bt_row = p.block_tables + (size_t)b * p.max_blocks + blk0 + w;
     const uint64_t pol = l2_evict_first();
+    const int gh = p.num_heads / p.num_kv_heads;
+    const int all_rows = G >= 32 ? -1 : (1 << G) - 1;
 
-    // block ids, 32 per warp-wide load, double-buffered in registers; invalid -> -1
-    auto load_chunk = [&](int chunk) -> int {
-        const int kk = chunk * 32 + lane;
-        int id = -1;
-        if (kk < nk) {
-            id = bt_row[(size_t)kk * NW];
-            if (id < 0 || id >= p.num_blocks) {
-                flag_error(p.err, kErrOutOfRange);
-                id = -1;
+    // block id and (ntok | live rows << 8) of the warp's kk-th entry
+    auto entry = [&](int kk, int* info) -> int {
+        const int j = blk0 + w + kk * NW;
+        int row, blk, ntok, live;
+        if constexpr (PREFIX) {
+            const int P = grp[4 * kMaxMembers];
+            if (j < P) {
+                row = grp[0];                               // shared: the first member's table
+                for (int m = 0; row < 0 && m + 1 < kMaxMembers; ++m) row = grp[4 * (m + 1)];
+                blk = j;
+                ntok = BS;
+                live = all_rows;
+            } else {
+                int m = 0;
+                while (m + 1 < kMaxMembers && j >= grp[4 * m + 2] + grp[4 * m + 3]) ++m;
+                row = grp[4 * m];
+                blk = P + (j - grp[4 * m + 2]);
+                ntok = min(BS, grp[4 * m + 1] - blk * BS);
+                live = ((1 << gh) - 1) << (m * gh);
             }
+        } else {
+            row = key;
+            blk = j;
+            ntok = min(BS, L - blk * BS);
+            live = all_rows;
+        }
+        *info = ntok | (live << 8);
+        int id = p.block_tables[(size_t)row * p.max_blocks + blk];
+        if (id < 0 || id >= p.num_blocks) {
+            flag_error(p.err, kErrOutOfRange);
+            id = -1;
         }
         return id;
     };
-    int id_cur = load_chunk(0), id_nxt = load_chunk(1), chunk_cur = 0;
-    auto get_id = [&](int kk) -> int {                     // warp-uniform call
+    // 32 entries per warp-wide load, double-buffered in registers; invalid id -> -1
+    int info_cur = 0, info_nxt = 0;
+    auto load_chunk = [&](int chunk, int* info) -> int {
+        const int kk = chunk * 32 + lane;
+        *info = 0;
+        return kk < nk ? entry(kk, info) : -1;
+    };
+    int id_cur = load_chunk(0, &info_cur), id_nxt = load_chunk(1, &info_nxt), chunk_cur = 0;
+    auto get_id = [&](int kk, int* info) -> int {          // warp-uniform call
         while ((kk >> 5) > chunk_cur) {
             id_cur = id_nxt;
+            info_cur = info_nxt;
             ++chunk_cur;
-            id_nxt = load_chunk(chunk_cur + 1);
+            id_nxt = load_chunk(chunk_cur + 1, &info_nxt);
         }
+        *info = __shfl_sync(kFull, info_cur, kk & 31);
         return __shfl_sync(kFull, id_cur, kk & 31);
     };
-    auto issue = [&](int kk, int id) {                      // lane 0 only
+    int32_t* stage_info = reinterpret_cast<int32_t*>(smem + P::kInfoOff);
+    auto issue = [&](int kk, int id, int info) {            // lane 0 only
         const int s = kk % ST;
         const uint32_t bar = smem_addr(&bars[w * ST + s]);
         stage_id[w * ST + s] = id;
+        stage_info[w * ST + s] = info;
         if (id >= 0) {
             const uint32_t dst = smem_addr(ring + (size_t)((w * ST + s) * 2) * TILE);
             const size_t off = ((size_t)id * p.num_kv_heads + hk) * TILE;
@@ -680,8 +743,9 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
 
     const int pro = nk < ST ? nk : ST;
     for (int kk = 0; kk < pro; ++kk) {
-        const int id = get_id(kk);
-        if (lane == 0) issue(kk, id);
+        int info;
+        const int id = get_id(kk, &info);
+        if (lane == 0) issue(kk, id, info);
     }
 
     bool aborted = false;
@@ -695,19 +759,21 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
         }
         const int id = stage_id[w * ST + s];
         if (id >= 0) {
-            const int ntok = min(BS, L - (blk0 + w + k * NW) * BS);
+            const int info = stage_info[w * ST + s];
+            const int ntok = info & 0xff;
             const unsigned char* kt = ring + (size_t)((w * ST + s) * 2) * TILE;
             if constexpr (Math::kWarpSmemFloats > 0)
                 Math::tile(st, kt, kt + TILE, ntok, lane, qs, pb);
             else
-                Math::tile(st, kt, kt + TILE, ntok, lane, p.qscale, qs, pb);
+                Math::tile(st, kt, kt + TILE, ntok, lane, p.qscale, qs, pb, info >> 8);
         }
         __syncwarp();
         if (k + ST < nk) {
-            const int id = get_id(k + ST);
+            int info;
+            const int id = get_id(k + ST, &info);
             if (lane == 0) {
                 fence_proxy_async_smem();
-                issue(k + ST, id);
+                issue(k + ST, id, info);
             }
         }
     }
@@ -743,13 +809,13 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
             }
         }
         int seq, h;
-        row_target<PREFIX, G>(p, blockIdx.z, hk, g, &seq, &h);
+        row_target<PREFIX, G>(p, key, hk, g, &seq, &h);
         if (seq < 0) continue;
         const float o = Ssum > 0.f ? O / Ssum : 0.f;
         if (single) {
             store_out(static_cast<QT*>(p.out) + ((size_t)seq * p.num_heads + h) * D + d, o * p.v_scale);
         } else {
-            const size_t base = ((size_t)seq * p.num_heads + h) * p.slots + p.slot_base + part;
+            const size_t base = ((size_t)seq * p.num_heads + h) * p.slots + part;
             p.ws_o[base * D + d] = o;
             if (d == 0) {
                 p.ws_ml[2 * base] = M;
@@ -761,30 +827,40 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
 
 // Merge the partitions of every (sequence, query head) that was split:
 //   out = v_scale * sum_p 2^(m_p - M) l_p o_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
-// Slots: [0, prefix parts) from the prefix launch (grouped decode only), then
-// [slot_base, slot_base + parts) for the sequence's own range.
+// A sequence of a prefix group has as many partitions as its group's list.
 template <typename QT>
 __global__ void __launch_bounds__(128) split_reduce_kernel(const Params p, int D, int BS) {
     const int h = blockIdx.x, b = blockIdx.y;
-    const int L = min(max(p.seq_lens[b], 0), p.max_blocks * BS);   // as the decode kernel clamps
-    const int nblk = (L + BS - 1) / BS;
-    const int start = p.start_blocks ? min(max(p.start_blocks[b], 0), nblk) : 0;
-    const int pre = start > 0 ? (start + p.prefix_part_blocks - 1) / p.prefix_part_blocks : 0;
-    const int own = (nblk - start + p.part_blocks - 1) / p.part_blocks;
-    if (pre == 0 && own <= 1) return;                       // written by the decode kernel
+    int nparts;
+    const int g = p.seq_group ? p.seq_group[b] : -1;
+    if (g >= 0) {                                          // as the group CTA counts its list
+        int P = max(p.group_prefix[g], 0), n = 0, sum = 0;
+        for (int m = 0; m < p.max_members && m < kMaxMembers; ++m) {
+            const int sb = p.group_members[(size_t)g * p.max_members + m];
+            if (sb < 0 || sb >= p.num_seqs) continue;
+            const int Lm = min(max(p.seq_lens[sb], 0), p.max_blocks * BS);
+            P = min(P, Lm / BS);
+            sum += (Lm + BS - 1) / BS;
+            ++n;
+        }
+        if (n == 0) P = 0;
+        const int T = P + sum - n * P;
+        nparts = (T + p.group_part_blocks - 1) / p.group_part_blocks;
+    } else {
+        const int L = min(max(p.seq_lens[b], 0), p.max_blocks * BS);   // as the decode kernel clamps
+        nparts = ((L + BS - 1) / BS + p.part_blocks - 1) / p.part_blocks;
+    }
+    if (nparts <= 1) return;                               // written by the decode kernel
     const size_t base = ((size_t)b * p.num_heads + h) * p.slots;
-    auto slot = [&](int q) { return base + (q < pre ? q : p.slot_base + (q - pre)); };
-    const int n = pre + own;
     float M = -INFINITY;
-    for (int q = 0; q < n; ++q) M = fmaxf(M, p.ws_ml[2 * slot(q)]);
+    for (int q = 0; q < nparts; ++q) M = fmaxf(M, p.ws_ml[2 * (base + q)]);
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
         float Ssum = 0.f, O = 0.f;
         if (M != -INFINITY) {
-            for (int q = 0; q < n; ++q) {
-                const size_t sq = slot(q);
-                const float e = exp2f(p.ws_ml[2 * sq] - M) * p.ws_ml[2 * sq + 1];
+            for (int q = 0; q < nparts; ++q) {
+                const float e = exp2f(p.ws_ml[2 * (base + q)] - M) * p.ws_ml[2 * (base + q) + 1];
                 Ssum += e;
-                O += e * p.ws_o[sq * D + d];
+                O += e * p.ws_o[(base + q) * D + d];
             }
         }
         store_out(static_cast<QT*>(p.out) + ((size_t)b * p.num_heads + h) * D + d,
@@ -807,7 +883,7 @@ struct Args {
     cudaStream_t stream;
     int* err;
     // prefix-grouped decode (all null / 0 for the plain call)
-    const int32_t* start_blocks;
+    const int32_t* seq_group;
     const int32_t* group_members;
     const int32_t* group_prefix;
     int num_groups, max_members;
@@ -866,20 +942,29 @@ template <class Math, typename QT, int D, int BS, int G>
 int launch_variant(const Args& a) {
     using P = Pipe<Math, D, BS, G, kNumWarps>;
     using KV = typename Math::KVT;
-    // grouped decode needs the tensor-core prefix kernel (bf16 / E4M3 caches),
-    // groups whose members fit the CTA's query rows, and room for both partial sets
+    // grouped decode needs the tensor-core group kernel (bf16 / E4M3 caches) and
+    // groups whose members fit the CTA's query rows
     constexpr bool kCanGroup = !std::is_same<KV, float>::value;
     const int gh = a.num_heads / a.num_kv_heads;
-    bool grouped = kCanGroup && a.group_members && a.group_prefix && a.start_blocks &&
-                   a.num_groups > 0 && a.max_members > 0 && a.max_members * gh <= kPrefixRows;
+    const bool grouped = kCanGroup && a.group_members && a.group_prefix && a.seq_group &&
+                         a.num_groups > 0 && a.max_members > 0 && a.max_members <= kMaxMembers &&
+                         a.max_members * gh <= kPrefixRows;
     int occ = 0;
     int st = kernel_setup(reinterpret_cast<const void*>(paged_decode_kernel<Math, QT, D, BS, G, kNumWarps, false>),
                           P::kSmem, kNumWarps * 32, &occ);
     if (st != PKV_OK) return st;
     int parts = 1;
-    int PB = choose_part_blocks(a, P::kTile, occ, grouped ? 2 : 1, &parts);
-    if (grouped && workspace_need(a.num_seqs, a.num_heads, a.head_dim, 2 * parts) > a.workspace_bytes)
-        grouped = false;                                     // no room for the prefix partials
+    const int PB = choose_part_blocks(a, P::kTile, occ, 1, &parts);
+    // a group's list is at most max_members tables long: split it like a sequence
+    // when the workspace holds its partials, else one partition per group
+    const int group_list = grouped ? a.max_members * a.max_blocks : 0;
+    int gPB = PB, gparts = grouped ? (group_list + PB - 1) / PB : 0;
+    if (grouped && (parts <= 1 || workspace_need(a.num_seqs, a.num_heads, a.head_dim, gparts) >
+                                       a.workspace_bytes)) {
+        gPB = group_list;
+        gparts = 1;
+    }
+    const int slots = gparts > parts ? gparts : parts;
 
     Params p;
     p.out = a.out;
@@ -898,23 +983,22 @@ int launch_variant(const Args& a) {
     p.max_parts = parts;
     p.qscale = a.scale * a.k_scale * kLog2e;
     p.v_scale = a.v_scale;
-    p.start_blocks = grouped ? a.start_blocks : nullptr;
+    p.seq_group = grouped ? a.seq_group : nullptr;
     p.group_members = grouped ? a.group_members : nullptr;
     p.group_prefix = grouped ? a.group_prefix : nullptr;
     p.max_members = grouped ? a.max_members : 0;
-    p.slots = grouped ? 2 * parts : parts;
-    p.slot_base = grouped ? parts : 0;
-    p.prefix_part_blocks = PB;
-    const bool split = grouped || parts > 1;
+    p.group_part_blocks = gPB;
+    p.slots = slots;
+    const bool split = slots > 1;
     p.ws_o = split ? static_cast<float*>(a.workspace) : nullptr;
-    p.ws_ml = split ? p.ws_o + (size_t)a.num_seqs * a.num_heads * p.slots * D : nullptr;
+    p.ws_ml = split ? p.ws_o + (size_t)a.num_seqs * a.num_heads * slots * D : nullptr;
 
     if constexpr (kCanGroup) {
         if (grouped) {                                       // shared prefixes, read once per group
-            Params pp = p;
-            pp.slot_base = 0;
+            Params pg = p;
+            pg.part_blocks = gPB;
             st = launch_kernel<MmaMath<KV, D, BS, kPrefixRows>, QT, D, BS, kPrefixRows, true>(
-                pp, dim3(parts, a.num_kv_heads, a.num_groups), a.stream);
+                pg, dim3(gparts, a.num_kv_heads, a.num_groups), a.stream);
             if (st != PKV_OK) return st;
         }
     }

@@ -31,7 +31,7 @@ class StepPlan:
     pairs: np.ndarray        # int64 [P, 2]
     tables: np.ndarray       # int32 [B, max_blocks]
     lens: np.ndarray         # int32 [B]
-    seq_prefix: np.ndarray = None     # int32 [B]; shared-prefix groups (may be empty)
+    seq_group: np.ndarray = None      # int32 [B]; shared-prefix groups (-1: none)
     group_members: np.ndarray = None  # int32 [g, max_members]
     group_prefix: np.ndarray = None   # int32 [g]
 
@@ -43,7 +43,7 @@ class StepPlan:
         t = {"slots": torch.from_numpy(self.slots), "pairs": torch.from_numpy(self.pairs),
              "tables": torch.from_numpy(self.tables), "lens": torch.from_numpy(self.lens)}
         if self.num_groups:
-            t.update({"seq_prefix": torch.from_numpy(self.seq_prefix),
+            t.update({"seq_group": torch.from_numpy(self.seq_group),
                       "group_members": torch.from_numpy(self.group_members),
                       "group_prefix": torch.from_numpy(self.group_prefix)})
         if pin:
@@ -57,7 +57,7 @@ class StepPlan:
     def nbytes(self):
         n = self.slots.nbytes + self.pairs.nbytes + self.tables.nbytes + self.lens.nbytes
         if self.num_groups:
-            n += self.seq_prefix.nbytes + self.group_members.nbytes + self.group_prefix.nbytes
+            n += self.seq_group.nbytes + self.group_members.nbytes + self.group_prefix.nbytes
         return n
 
 
@@ -126,16 +126,17 @@ class PagedKVCache:
         plan = StepPlan(ids, slots, pairs, tables, lens)
         if group_prefixes and self.k_pool.dtype != torch.float32:
             max_members = max(1, 8 // (self.num_heads // self.num_kv_heads))
-            members, prefix, seq_prefix = self.bm.prefix_groups(ids, max_members)
+            members, prefix, seq_group = self.bm.prefix_groups(ids, max_members)
             if len(members):
-                plan.seq_prefix, plan.group_members, plan.group_prefix = seq_prefix, members, prefix
+                plan.seq_group, plan.group_members, plan.group_prefix = seq_group, members, prefix
         return plan
 
     def workspace(self, batch, max_blocks):
-        """Split-KV scratch, sized for the grouped decode (twice the plain size)."""
+        """Split-KV scratch, room for split group lists included."""
         n = paged_attention_workspace_size(batch, self.num_heads, self.head_dim, self.block_size,
                                            max_blocks)
-        return torch.empty(max(2 * n, 16), dtype=torch.uint8, device=self.device)
+        mult = max(1, 8 // (self.num_heads // self.num_kv_heads))
+        return torch.empty(max(mult * n, 16), dtype=torch.uint8, device=self.device)
 
     def decode(self, q, dev_plan, out, scale, k_scale=1.0, v_scale=1.0, workspace=None,
                stream=None):
@@ -143,7 +144,7 @@ class PagedKVCache:
         if "group_members" in dev_plan:
             return paged_attention_decode_grouped(
                 out, q, self.k_pool, self.v_pool, dev_plan["tables"], dev_plan["lens"], scale,
-                dev_plan["seq_prefix"], dev_plan["group_members"], dev_plan["group_prefix"],
+                dev_plan["seq_group"], dev_plan["group_members"], dev_plan["group_prefix"],
                 k_scale, v_scale, workspace, stream)
         return paged_attention_decode(out, q, self.k_pool, self.v_pool, dev_plan["tables"],
                                       dev_plan["lens"], scale, k_scale, v_scale, workspace, stream)

@@ -142,9 +142,9 @@ def test_prefix_groups_share_full_leading_blocks():
                 seqs.append(cid)
         ids = list(rng.permutation(seqs))
         maxm = int(rng.choice([2, 3, 4, 8]))
-        members, prefix, seq_prefix = a.prefix_groups(ids, maxm)
+        members, prefix, seq_group = a.prefix_groups(ids, maxm)
         seen = set()
-        for row, pre in zip(members, prefix):
+        for gi, (row, pre) in enumerate(zip(members, prefix)):
             ms = [int(m) for m in row if m >= 0]
             assert 2 <= len(ms) <= maxm and pre >= 1
             tabs = [o.tables[ids[m]] for m in ms]
@@ -154,6 +154,6 @@ def test_prefix_groups_share_full_leading_blocks():
             if pre < full:                               # maximal
                 assert len({t[pre] for t in tabs}) > 1
             for m in ms:
-                assert m not in seen and seq_prefix[m] == pre
+                assert m not in seen and seq_group[m] == gi
                 seen.add(m)
-        assert all(seq_prefix[i] == 0 for i in range(len(ids)) if i not in seen)
+        assert all(seq_group[i] == -1 for i in range(len(ids)) if i not in seen)

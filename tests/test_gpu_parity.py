@@ -243,11 +243,11 @@ def test_grouped_prefix_decode_matches_oracle(kv, Hq, Hkv, D, bs, per_group, pro
     if 8 // G >= 2:
         assert plan.num_groups > 0
         # every group: members share the prefix's block ids, full for all of them
-        for members, pre in zip(plan.group_members, plan.group_prefix):
+        for gi, (members, pre) in enumerate(zip(plan.group_members, plan.group_prefix)):
             ms = [m for m in members if m >= 0]
             assert 2 <= len(ms) <= 8 // G and pre >= 1
             for m in ms:
-                assert plan.seq_prefix[m] == pre and plan.lens[m] >= pre * bs
+                assert plan.seq_group[m] == gi and plan.lens[m] >= pre * bs
                 assert np.array_equal(plan.tables[m, :pre], plan.tables[ms[0], :pre])
     else:
         assert plan.num_groups == 0
@@ -258,7 +258,7 @@ def test_grouped_prefix_decode_matches_oracle(kv, Hq, Hkv, D, bs, per_group, pro
     # the plain (ungrouped) decode agrees with the grouped one
     cache = g["cache"]
     dev = g["plan"].device_tensors("cuda")
-    for k in ("seq_prefix", "group_members", "group_prefix"):
+    for k in ("seq_group", "group_members", "group_prefix"):
         dev.pop(k, None)
     out2 = torch.empty(w.B, w.Hq, w.D, dtype=w.src_dtype, device="cuda")
     cache.decode(inp.q.cuda(), dev, out2, w.scale, inp.ks, inp.vs,
@@ -267,10 +267,25 @@ def test_grouped_prefix_decode_matches_oracle(kv, Hq, Hkv, D, bs, per_group, pro
     assert_close(out2.float().cpu().numpy(), o["out"], kv, w.name + " plain")
 
 
-def test_grouped_decode_without_workspace_falls_back_to_plain():
-    w = wl.shared_prefix(groups=2, per_group=4, prompt=100, max_suffix=40, Hq=8, Hkv=8)
+@pytest.mark.parametrize("prompt,suffix", [(100, 40), (1200, 900)])
+def test_grouped_decode_without_workspace(prompt, suffix):
+    """No workspace: every group list and sequence runs as one partition."""
+    w = wl.shared_prefix(groups=2, per_group=4, prompt=prompt, max_suffix=suffix, Hq=8, Hkv=8,
+                         seed=prompt)
     inp = Inputs(w)
     g = run_gpu(inp, workspace=False)
     assert g["err"] == 0 and g["plan"].num_groups == 2
     o = run_oracle(inp)
     assert_close(g["out"].numpy(), o["out"], "bf16", "grouped, no workspace")
+
+
+def test_grouped_decode_long_lists_are_split_and_merged():
+    """Group lists longer than a partition (long prompt, long tails) go through
+    the split merge."""
+    w = wl.shared_prefix(groups=3, per_group=4, prompt=2000, max_suffix=1500, Hq=8, Hkv=8,
+                         seed=77)
+    inp = Inputs(w)
+    g = run_gpu(inp)
+    assert g["err"] == 0 and g["plan"].num_groups == 3
+    o = run_oracle(inp)
+    assert_close(g["out"].numpy(), o["out"], "bf16", "grouped, split lists")
