@@ -43,6 +43,33 @@ KV_ELT = {"f32": 4, "bf16": 2, "e4m3": 1}
 L2_BYTES = 129 * 2 ** 20
 
 
+KERNEL_SOURCES = ["pkv_decode_impl.cuh", "pkv_decode.cu", "pkv_decode_bf16.cu",
+                  "pkv_decode_e4m3.cu", "pkv_decode_f32.cu"]
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_259_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(config):
+    """DRAM bytes per decode launch from profiles/decode_traffic.json (an ncu
+    capture), or None when it was taken on other kernel sources or workloads."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    if t.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    e = t.get("workloads", {}).get(config)
+    return None if e is None else e.get("dram_bytes_per_decode")
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -212,6 +239,7 @@ def run_gpu(args, rank, world, device):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    launches0 = pkv.kernel_launches()
     t_start.record(stream)
     for i in range(K):
         if has_copy:
@@ -222,6 +250,7 @@ def run_gpu(args, rank, world, device):
         ev_dec[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
+    launches_timed = pkv.kernel_launches() - launches0
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
@@ -264,27 +293,20 @@ def run_gpu(args, rank, world, device):
 
     res = {"w": w, "nbytes": nbytes, "ms_per_step": total_ms / K, "dec_ms": float(dec_ms.mean()),
            "dec_ms_median": float(np.median(dec_ms)), "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
-           "clocks": clk, "launches": launches_per_step * K, "groups": plan.num_groups,
+           "clocks": clk, "launches": launches_timed, "groups": plan.num_groups,
            "launches_per_step": launches_per_step,
            "cpu": (q, k_src, v_src, ks, vs, plan)}
     return res
 
 
-OUR_KERNELS = ("paged_decode_kernel", "split_reduce_kernel", "reshape_and_cache_kernel",
-               "copy_blocks_kernel")
-
-
 def count_launches(step, reps=3):
-    """Kernels of this library one step launches, counted by the CUDA profiler."""
-    from torch.profiler import ProfilerActivity, profile
+    """Kernels of this library one step launches (the library counts them)."""
+    import paged_kv_cache_259_gb300 as pkv
+    n0 = pkv.kernel_launches()
+    for _ in range(reps):
+        step()
     torch.cuda.synchronize()
-    with profile(activities=[ProfilerActivity.CUDA]) as prof:
-        for _ in range(reps):
-            step()
-        torch.cuda.synchronize()
-    n = sum(1 for e in prof.events() if any(k in e.name for k in OUR_KERNELS)
-            and e.device_type == torch.autograd.DeviceType.CUDA)
-    return n // reps
+    return (pkv.kernel_launches() - n0) // reps
 
 
 def max_over_ranks(x, world, device):
@@ -415,7 +437,7 @@ def main():
             "roofline": {
                 "kernel": "paged_attention_decode (decode kernel + split merge)",
                 "bound": "hbm", "achieved": round(dec_gbs, 2), "peak": peak, "unit": "GB/s",
-                "frac": round(dec_gbs / peak, 4), "traffic": None,
+                "frac": round(dec_gbs / peak, 4), "traffic": measured_traffic(args.config),
                 "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
                 "bytes_per_launch": nb["decode"], "ms_per_launch": round(dec_ms, 5),
                 "ms_per_launch_median": round(r["dec_ms_median"], 5),

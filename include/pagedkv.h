@@ -248,6 +248,10 @@ PKV_API int paged_attention_decode_noalloc(void* out, const void* q,
                                    int block_size, float scale, int q_dtype, int kv_dtype,
                                    float k_scale, float v_scale, void* stream);
 
+/* Kernels this library has launched in this process so far (all devices and
+ * streams; for tracing and for counting the launches of a step). */
+PKV_API unsigned long long pkv_kernel_launches(void);
+
 /* Synchronise `stream`, then return (in *code) and clear the device error word
  * of the current device: PKV_OK if no kernel recorded an error since the last
  * read, else PKV_ERR_TIMEOUT if a device wait gave up, else PKV_ERR_OUT_OF_RANGE.

@@ -24,7 +24,7 @@ import torch
 __all__ = [
     "PagedKVError", "paged_attention_decode", "paged_attention_workspace_size",
     "paged_attention_decode_noalloc", "NOALLOC_WORKSPACE_BYTES", "paged_attention_decode_grouped",
-    "reshape_and_cache", "copy_blocks", "get_device_error", "BlockManager",
+    "reshape_and_cache", "copy_blocks", "get_device_error", "kernel_launches", "BlockManager",
     "library_path", "load_library", "pool_shapes", "PKV_F32", "PKV_BF16", "PKV_E4M3",
 ]
 
@@ -64,6 +64,7 @@ def load_library():
     sig = {
         "pkv_status_string": (ctypes.c_char_p, [c_int]),
         "pkv_last_error_string": (ctypes.c_char_p, []),
+        "pkv_kernel_launches": (ctypes.c_ulonglong, []),
         "paged_attention_decode": (c_int, [vp, vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int,
                                            c_int, c_int, c_int, c_float, c_int, c_int, c_float,
                                            c_float, vp, c_size, vp]),
@@ -334,6 +335,11 @@ def copy_blocks(k_pool, v_pool, src_dst_pairs, stream=None):
                              src_dst_pairs.shape[0], k_pool.shape[0], block_bytes,
                              _stream_ptr(stream, k_pool.device))
     _check(st, "copy_blocks")
+
+
+def kernel_launches():
+    """Kernels this library has launched in this process so far."""
+    return int(load_library().pkv_kernel_launches())
 
 
 def get_device_error(device=None, stream=None):

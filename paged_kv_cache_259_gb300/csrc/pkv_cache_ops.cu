@@ -155,6 +155,7 @@ cudaError_t launch_reshape(const void* k, const void* v, void* kp, void* vp, con
     const long long cap = 8LL * num_sms();                 // grid-stride beyond 8 CTAs/SM
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
+    note_launch();
     reshape_and_cache_kernel<ST, CT><<<(unsigned)blocks, threads, 0, stream>>>(
         static_cast<const ST*>(k), static_cast<const ST*>(v), static_cast<CT*>(kp),
         static_cast<CT*>(vp), slots, num_tokens, hkv, d, bs, num_blocks, ks, vs, err);
@@ -224,6 +225,7 @@ int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs, int nu
     if (!err) return PKV_ERR_CUDA;
     const unsigned chunks = (unsigned)((block_bytes + kCopyChunkBytes - 1) / kCopyChunkBytes);
     dim3 grid(2u * (unsigned)num_pairs, chunks);
+    note_launch();
     copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<char*>(k_pool), static_cast<char*>(v_pool), src_dst_pairs, num_blocks,
         block_bytes, err);

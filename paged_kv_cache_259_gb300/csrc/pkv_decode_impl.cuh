@@ -933,6 +933,7 @@ int launch_kernel(const Params& p, dim3 grid, cudaStream_t stream) {
     int occ = 0;
     const int st = kernel_setup(reinterpret_cast<const void*>(kern), P::kSmem, kNumWarps * 32, &occ);
     if (st != PKV_OK) return st;
+    note_launch();
     kern<<<grid, kNumWarps * 32, P::kSmem, stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_fail("decode: kernel launch", e);
@@ -1005,6 +1006,7 @@ int launch_variant(const Args& a) {
     st = launch_kernel<Math, QT, D, BS, G, false>(p, dim3(parts, a.num_kv_heads, a.num_seqs), a.stream);
     if (st != PKV_OK) return st;
     if (split) {
+        note_launch();
         split_reduce_kernel<QT><<<dim3(a.num_heads, a.num_seqs), 128, 0, a.stream>>>(p, D, BS);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail("decode: split merge launch", e);

@@ -28,6 +28,9 @@ int cuda_fail(const char* what, cudaError_t e);
 // threads in *occupancy. Cached; thread-safe. Returns PKV_OK or PKV_ERR_CUDA.
 int kernel_setup(const void* kernel, int smem, int threads, int* occupancy);
 
+// Count one kernel launch of this library (see pkv_kernel_launches).
+void note_launch();
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace pkv

@@ -65,6 +65,12 @@ int kernel_setup(const void* kernel, int smem, int threads, int* occupancy) {
     return PKV_OK;
 }
 
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 int num_sms() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
@@ -93,6 +99,10 @@ const char* pkv_status_string(int status) {
 }
 
 const char* pkv_last_error_string(void) { return pkv::g_last_error; }
+
+unsigned long long pkv_kernel_launches(void) {
+    return pkv::g_launches.load(std::memory_order_relaxed);
+}
 
 int pkv_get_device_error(int* code, void* stream) {
     if (!code) return PKV_ERR_INVALID_ARG;
