@@ -145,6 +145,10 @@ PKV_API int paged_attention_decode(void* out, const void* q,
  *   seq_group            device int32 [num_seqs]: the sequence's group, -1 if none
  *   group_members        device int32 [num_groups][max_members], -1 padded
  *   group_prefix_blocks  device int32 [num_groups]
+ *   ungrouped_seqs       device int32 [num_ungrouped]: the batch indices in no
+ *                        group (they get the regular CTAs); num_ungrouped < 0:
+ *                        no list, every sequence is launched and the grouped
+ *                        ones leave at once
  * Preconditions (the block manager's bm_prefix_groups meets them): a sequence
  * is in at most one group and seq_group names it; the prefix blocks are the same
  * ids in every member's table. The prefix is clamped to the blocks every member
@@ -165,6 +169,7 @@ PKV_API int paged_attention_decode_grouped(void* out, const void* q,
                                    const int32_t* group_members,
                                    const int32_t* group_prefix_blocks,
                                    int num_groups, int max_members,
+                                   const int32_t* ungrouped_seqs, int num_ungrouped,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* Bytes of workspace that lets paged_attention_decode use its finest split for

@@ -72,7 +72,7 @@ def load_library():
         "paged_attention_decode_grouped": (c_int, [vp, vp, vp, vp, vp, vp, c_int, c_int, c_int,
                                                    c_int, c_int, c_int, c_int, c_float, c_int,
                                                    c_int, c_float, c_float, vp, vp, vp, c_int,
-                                                   c_int, vp, c_size, vp]),
+                                                   c_int, vp, c_int, vp, c_size, vp]),
         "bm_prefix_groups": (c_int, [vp, i64p, c_int, c_int, i32p, i32p, i32p, ip]),
         "paged_attention_decode_noalloc": (c_int, [vp, vp, vp, vp, vp, vp, c_int, c_int, c_int,
                                                    c_int, c_int, c_int, c_int, c_float, c_int,
@@ -226,12 +226,14 @@ def paged_attention_decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale
 
 def paged_attention_decode_grouped(out, q, k_pool, v_pool, block_tables, seq_lens, scale,
                                    seq_group, group_members, group_prefix_blocks,
-                                   k_scale=1.0, v_scale=1.0, workspace=None, stream=None):
+                                   k_scale=1.0, v_scale=1.0, workspace=None, stream=None,
+                                   ungrouped=None):
     """``paged_attention_decode`` reading each shared prefix once per group.
 
     seq_group int32 ``[B]`` (group or -1); group_members int32 ``[num_groups,
     max_members]`` (batch indices, -1 padded); group_prefix_blocks int32
-    ``[num_groups]`` -- as ``BlockManager.prefix_groups`` returns them.
+    ``[num_groups]`` -- as ``BlockManager.prefix_groups`` returns them; ungrouped:
+    int32 ``[n]`` batch indices in no group (None: every sequence is launched).
     """
     lib = load_library()
     for t, n in ((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
@@ -248,6 +250,10 @@ def paged_attention_decode_grouped(out, q, k_pool, v_pool, block_tables, seq_len
             seq_group.shape != (B,) or group_members.dim() != 2 or \
             group_prefix_blocks.shape != (group_members.shape[0],):
         raise ValueError("inconsistent shapes")
+    if ungrouped is not None:
+        _cuda(ungrouped, "ungrouped")
+        if ungrouped.dtype != torch.int32:
+            raise TypeError("ungrouped must be int32")
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         _cuda(workspace, "workspace")
@@ -259,6 +265,8 @@ def paged_attention_decode_grouped(out, q, k_pool, v_pool, block_tables, seq_len
             Hq, Hkv, D, bs, float(scale), _dt(q, "q"), _dt(k_pool, "k_pool"), float(k_scale),
             float(v_scale), seq_group.data_ptr(), group_members.data_ptr(),
             group_prefix_blocks.data_ptr(), group_members.shape[0], group_members.shape[1],
+            None if ungrouped is None else ungrouped.data_ptr(),
+            -1 if ungrouped is None else ungrouped.numel(),
             ws_ptr, ws_bytes, _stream_ptr(stream, q.device))
     _check(st, "paged_attention_decode_grouped")
     return out

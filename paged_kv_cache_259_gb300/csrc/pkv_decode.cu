@@ -31,7 +31,8 @@ int decode_common(void* out, const void* q, const void* k_pool, const void* v_po
                   int head_dim, int block_size, float scale, int q_dtype, int kv_dtype,
                   float k_scale, float v_scale, const int32_t* seq_group,
                   const int32_t* group_members, const int32_t* group_prefix, int num_groups,
-                  int max_members, void* workspace, size_t workspace_bytes, void* stream) {
+                  int max_members, const int32_t* seq_list, int num_list, void* workspace,
+                  size_t workspace_bytes, void* stream) {
     using namespace pkv;
     if (num_seqs < 0 || num_seqs > 65535 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
         num_heads <= 0 || num_kv_heads <= 0 || num_kv_heads > 65535 || head_dim <= 0 ||
@@ -71,6 +72,8 @@ int decode_common(void* out, const void* q, const void* k_pool, const void* v_po
     a.workspace_bytes = workspace ? workspace_bytes : 0;
     a.stream = static_cast<cudaStream_t>(stream);
     a.seq_group = seq_group;
+    a.seq_list = seq_list;
+    a.num_list = num_list;
     a.group_members = group_members;
     a.group_prefix = group_prefix;
     a.num_groups = num_groups;
@@ -95,7 +98,7 @@ int paged_attention_decode(void* out, const void* q, const void* k_pool, const v
     return decode_common(out, q, k_pool, v_pool, block_tables, seq_lens, num_seqs,
                          max_blocks_per_seq, num_blocks, num_heads, num_kv_heads, head_dim,
                          block_size, scale, q_dtype, kv_dtype, k_scale, v_scale, nullptr, nullptr,
-                         nullptr, 0, 0, workspace, workspace_bytes, stream);
+                         nullptr, 0, 0, nullptr, 0, workspace, workspace_bytes, stream);
 }
 
 int paged_attention_decode_grouped(void* out, const void* q, const void* k_pool,
@@ -105,8 +108,13 @@ int paged_attention_decode_grouped(void* out, const void* q, const void* k_pool,
                                    int block_size, float scale, int q_dtype, int kv_dtype,
                                    float k_scale, float v_scale, const int32_t* seq_group,
                                    const int32_t* group_members, const int32_t* group_prefix_blocks,
-                                   int num_groups, int max_members, void* workspace,
-                                   size_t workspace_bytes, void* stream) {
+                                   int num_groups, int max_members,
+                                   const int32_t* ungrouped_seqs, int num_ungrouped,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+    // num_ungrouped < 0: no list, every sequence gets a regular CTA (grouped ones
+    // leave at once); otherwise the list names the ungrouped batch indices
+    if ((num_ungrouped > 0 && !ungrouped_seqs) || num_ungrouped > num_seqs)
+        return PKV_ERR_INVALID_ARG;
     if (num_groups < 0 || (num_groups > 0 && (max_members <= 0 || !seq_group ||
                                               !group_members || !group_prefix_blocks)))
         return PKV_ERR_INVALID_ARG;
@@ -117,7 +125,7 @@ int paged_attention_decode_grouped(void* out, const void* q, const void* k_pool,
                          num_groups > 0 ? seq_group : nullptr,
                          num_groups > 0 ? group_members : nullptr,
                          num_groups > 0 ? group_prefix_blocks : nullptr, num_groups, max_members,
-                         workspace, workspace_bytes, stream);
+                         ungrouped_seqs, num_ungrouped, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -84,6 +84,7 @@ struct Params {
     float v_scale;
     // prefix-grouped decode (null / 0 otherwise)
     const int32_t* seq_group;      // [B] group of the sequence, -1 for none
+    const int32_t* seq_list;       // regular launch over these batch indices (null: all)
     const int32_t* group_members;  // [num_groups][max_members] batch indices, -1 padded
     const int32_t* group_prefix;   // [num_groups] shared full blocks of the group
     int max_members;
@@ -599,7 +600,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
     // g's block list -- the P shared prefix blocks (every member's rows live),
     // then each member's own blocks P.. (that member's rows live) -- so a group
     // reads its prompt once and needs no second launch for the members' tails.
-    const int part = blockIdx.x, hk = blockIdx.y, key = blockIdx.z;
+    const int part = blockIdx.x, hk = blockIdx.y;
+    const int key = (!PREFIX && p.seq_list) ? p.seq_list[blockIdx.z] : (int)blockIdx.z;
     __shared__ int grp[4 * kMaxMembers + 4];   // b, L, own start, own count per member; P, T
     int L = 0, nblk = 0;                       // regular launch: the sequence
     int total;                                 // blocks (or list entries) of this CTA's key
@@ -630,6 +632,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
         __syncthreads();
         total = grp[4 * kMaxMembers + 1];
     } else {
+        if (key < 0 || key >= p.num_seqs) {                 // a bad ungrouped-list entry
+            if (part == 0 && hk == 0 && threadIdx.x == 0) flag_error(p.err, kErrOutOfRange);
+            return;
+        }
         if (p.seq_group && p.seq_group[key] >= 0) return;  // attended by its group's CTAs
         L = p.seq_lens[key];
         if (L < 0 || L > p.max_blocks * BS) {               // length the table cannot hold
@@ -827,10 +833,15 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
 
 // Merge the partitions of every (sequence, query head) that was split:
 //   out = v_scale * sum_p 2^(m_p - M) l_p o_p / sum_p 2^(m_p - M) l_p,  M = max_p m_p.
+// One warp per (sequence, head): lanes take the partitions' (m, l) 32 at a
+// time, then the weighted rows are summed with each lane owning D/32 dims.
 // A sequence of a prefix group has as many partitions as its group's list.
-template <typename QT>
-__global__ void __launch_bounds__(128) split_reduce_kernel(const Params p, int D, int BS) {
-    const int h = blockIdx.x, b = blockIdx.y;
+template <typename QT, int D>
+__global__ void __launch_bounds__(256) split_reduce_kernel(const Params p, int BS) {
+    constexpr int DPL = D / 32;
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (row >= p.num_seqs * p.num_heads) return;
+    const int b = row / p.num_heads, h = row % p.num_heads;
     int nparts;
     const int g = p.seq_group ? p.seq_group[b] : -1;
     if (g >= 0) {                                          // as the group CTA counts its list
@@ -844,28 +855,52 @@ __global__ void __launch_bounds__(128) split_reduce_kernel(const Params p, int D
             ++n;
         }
         if (n == 0) P = 0;
-        const int T = P + sum - n * P;
-        nparts = (T + p.group_part_blocks - 1) / p.group_part_blocks;
+        nparts = (P + sum - n * P + p.group_part_blocks - 1) / p.group_part_blocks;
     } else {
         const int L = min(max(p.seq_lens[b], 0), p.max_blocks * BS);   // as the decode kernel clamps
         nparts = ((L + BS - 1) / BS + p.part_blocks - 1) / p.part_blocks;
     }
     if (nparts <= 1) return;                               // written by the decode kernel
     const size_t base = ((size_t)b * p.num_heads + h) * p.slots;
+    const float* ml = p.ws_ml + 2 * base;
+    const float* wo = p.ws_o + base * D;
     float M = -INFINITY;
-    for (int q = 0; q < nparts; ++q) M = fmaxf(M, p.ws_ml[2 * (base + q)]);
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float Ssum = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-            for (int q = 0; q < nparts; ++q) {
-                const float e = exp2f(p.ws_ml[2 * (base + q)] - M) * p.ws_ml[2 * (base + q) + 1];
-                Ssum += e;
-                O += e * p.ws_o[(base + q) * D + d];
+    for (int q = lane; q < nparts; q += 32) M = fmaxf(M, ml[2 * q]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    float acc[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+    float S = 0.f;
+    if (M != -INFINITY) {
+        for (int c = 0; c < nparts; c += 32) {
+            const int q = c + lane;
+            const float wq = q < nparts ? exp2f(ml[2 * q] - M) * ml[2 * q + 1] : 0.f;
+            S += wq;
+            const int n = min(32, nparts - c);
+            for (int j = 0; j < n; ++j) {
+                const float wj = __shfl_sync(kFull, wq, j);
+                const float* src = wo + (size_t)(c + j) * D + lane * DPL;
+                if constexpr (DPL == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(src);
+                    acc[0] = fmaf(wj, v.x, acc[0]);
+                    acc[1] = fmaf(wj, v.y, acc[1]);
+                    acc[2] = fmaf(wj, v.z, acc[2]);
+                    acc[3] = fmaf(wj, v.w, acc[3]);
+                } else {
+                    const float2 v = *reinterpret_cast<const float2*>(src);
+                    acc[0] = fmaf(wj, v.x, acc[0]);
+                    acc[1] = fmaf(wj, v.y, acc[1]);
+                }
             }
         }
-        store_out(static_cast<QT*>(p.out) + ((size_t)b * p.num_heads + h) * D + d,
-                  Ssum > 0.f ? O / Ssum * p.v_scale : 0.f);
     }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) S += __shfl_xor_sync(kFull, S, o);
+    const float inv = S > 0.f ? p.v_scale / S : 0.f;
+    QT* dst = static_cast<QT*>(p.out) + ((size_t)b * p.num_heads + h) * D + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) store_out(dst + i, acc[i] * inv);
 }
 
 // ----------------------------------------------------------------- host launch
@@ -884,6 +919,8 @@ struct Args {
     int* err;
     // prefix-grouped decode (all null / 0 for the plain call)
     const int32_t* seq_group;
+    const int32_t* seq_list;
+    int num_list;
     const int32_t* group_members;
     const int32_t* group_prefix;
     int num_groups, max_members;
@@ -985,6 +1022,7 @@ int launch_variant(const Args& a) {
     p.qscale = a.scale * a.k_scale * kLog2e;
     p.v_scale = a.v_scale;
     p.seq_group = grouped ? a.seq_group : nullptr;
+    p.seq_list = nullptr;
     p.group_members = grouped ? a.group_members : nullptr;
     p.group_prefix = grouped ? a.group_prefix : nullptr;
     p.max_members = grouped ? a.max_members : 0;
@@ -1003,11 +1041,18 @@ int launch_variant(const Args& a) {
             if (st != PKV_OK) return st;
         }
     }
-    st = launch_kernel<Math, QT, D, BS, G, false>(p, dim3(parts, a.num_kv_heads, a.num_seqs), a.stream);
-    if (st != PKV_OK) return st;
+    // sequences of no group (all of them, or the caller's list in a grouped call)
+    const bool listed = grouped && a.num_list >= 0;
+    p.seq_list = listed ? a.seq_list : nullptr;
+    const int n_regular = listed ? a.num_list : a.num_seqs;
+    if (n_regular > 0) {
+        st = launch_kernel<Math, QT, D, BS, G, false>(p, dim3(parts, a.num_kv_heads, n_regular), a.stream);
+        if (st != PKV_OK) return st;
+    }
     if (split) {
         note_launch();
-        split_reduce_kernel<QT><<<dim3(a.num_heads, a.num_seqs), 128, 0, a.stream>>>(p, D, BS);
+        const unsigned rows = (unsigned)a.num_seqs * a.num_heads;
+        split_reduce_kernel<QT, D><<<(rows + 7) / 8, 256, 0, a.stream>>>(p, BS);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail("decode: split merge launch", e);
     }

@@ -83,29 +83,31 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// One try: the thread is parked (not spinning) until the phase completes or
+// `suspend_ns` pass, whichever is first.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
         : "memory");
     return ok != 0;
 }
 
 // Wait for phase `parity` of the barrier to complete, for at most kWaitLimitNs
-// (or until another wait has timed out).
+// (or until another wait has timed out). Each try parks the thread for up to
+// 20 us, so waiting warps leave the issue slots to working ones.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, const int* err) {
-    if (mbar_try_wait(bar, parity)) return true;
+    constexpr uint32_t kSuspendNs = 20000;
+    if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
     const unsigned long long t0 = global_ns();
-    for (unsigned it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (global_ns() - t0 > kWaitLimitNs) return false;
-            if (err && (*reinterpret_cast<const volatile int*>(err) & kErrTimeout)) return false;
-        }
+    while (true) {
+        if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (err && (*reinterpret_cast<const volatile int*>(err) & kErrTimeout)) return false;
     }
 }
 

@@ -43,7 +43,9 @@ class StepPlan:
         t = {"slots": torch.from_numpy(self.slots), "pairs": torch.from_numpy(self.pairs),
              "tables": torch.from_numpy(self.tables), "lens": torch.from_numpy(self.lens)}
         if self.num_groups:
-            t.update({"seq_group": torch.from_numpy(self.seq_group),
+            t.update({"ungrouped": torch.from_numpy(
+                          np.nonzero(self.seq_group < 0)[0].astype(np.int32)),
+                      "seq_group": torch.from_numpy(self.seq_group),
                       "group_members": torch.from_numpy(self.group_members),
                       "group_prefix": torch.from_numpy(self.group_prefix)})
         if pin:
@@ -145,7 +147,7 @@ class PagedKVCache:
             return paged_attention_decode_grouped(
                 out, q, self.k_pool, self.v_pool, dev_plan["tables"], dev_plan["lens"], scale,
                 dev_plan["seq_group"], dev_plan["group_members"], dev_plan["group_prefix"],
-                k_scale, v_scale, workspace, stream)
+                k_scale, v_scale, workspace, stream, dev_plan.get("ungrouped"))
         return paged_attention_decode(out, q, self.k_pool, self.v_pool, dev_plan["tables"],
                                       dev_plan["lens"], scale, k_scale, v_scale, workspace, stream)
 

@@ -258,13 +258,24 @@ def test_grouped_prefix_decode_matches_oracle(kv, Hq, Hkv, D, bs, per_group, pro
     # the plain (ungrouped) decode agrees with the grouped one
     cache = g["cache"]
     dev = g["plan"].device_tensors("cuda")
-    for k in ("seq_group", "group_members", "group_prefix"):
+    for k in ("seq_group", "group_members", "group_prefix", "ungrouped"):
         dev.pop(k, None)
     out2 = torch.empty(w.B, w.Hq, w.D, dtype=w.src_dtype, device="cuda")
     cache.decode(inp.q.cuda(), dev, out2, w.scale, inp.ks, inp.vs,
                  cache.workspace(w.B, w.max_blocks_per_seq))
     assert pkv.get_device_error() == 0
     assert_close(out2.float().cpu().numpy(), o["out"], kv, w.name + " plain")
+    if plan.num_groups:
+        # without the ungrouped list every sequence gets a regular CTA; grouped
+        # ones leave at once
+        dev = plan.device_tensors("cuda")
+        out3 = torch.empty_like(out2)
+        pkv.paged_attention_decode_grouped(
+            out3, inp.q.cuda(), cache.k_pool, cache.v_pool, dev["tables"], dev["lens"], w.scale,
+            dev["seq_group"], dev["group_members"], dev["group_prefix"], inp.ks, inp.vs,
+            cache.workspace(w.B, w.max_blocks_per_seq), None, None)
+        assert pkv.get_device_error() == 0
+        assert_close(out3.float().cpu().numpy(), o["out"], kv, w.name + " no list")
 
 
 @pytest.mark.parametrize("prompt,suffix", [(100, 40), (1200, 900)])
