@@ -377,11 +377,13 @@ struct MmaMath {
 
     // row_live: bit r set if query row r attends over this tile (all rows, except
     // in a group CTA's own tiles, which belong to one member's rows)
+    // MASKED (group launches only): rows outside row_live see -inf scores.
+    template <bool MASKED>
     __device__ __forceinline__ static void tile(State& st, const unsigned char* kt,
                                                 const unsigned char* vt, int ntok, int lane,
                                                 float qscale, const float*, float*, int row_live) {
         const int r = lane >> 2, c = lane & 3;
-        const bool live = (row_live >> r) & 1;
+        const bool live = !MASKED || ((row_live >> r) & 1);
         const uint32_t kbase = smem_addr(kt), vbase = smem_addr(vt);
 #pragma unroll
         for (int h = 0; h < SUB; ++h) {
@@ -443,7 +445,7 @@ struct MmaMath {
             // a row with no live score yet keeps m = -inf; exponents are taken
             // against 0 then, so nothing becomes NaN and its weights stay 0
             const float m_new = fmaxf(st.m, mx);
-            const float m_ref = m_new == -INFINITY ? 0.f : m_new;
+            const float m_ref = (MASKED && m_new == -INFINITY) ? 0.f : m_new;
             const float alpha = exp2f(st.m - m_ref);
             float pr[2][2];
             float psum = 0.f;
@@ -583,8 +585,10 @@ __device__ __forceinline__ void row_target(const Params& p, int b_or_group, int 
     }
 }
 
+// Shared memory allows three CTAs per SM (about 66 KB each); the bound lets the
+// compiler spend the registers that leaves.
 template <class Math, typename QT, int D, int BS, int G, int NW, bool PREFIX>
-__global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
+__global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p) {
     using P = Pipe<Math, D, BS, G, NW>;
     constexpr int TILE = P::kTile, ST = P::kStages;
 
@@ -701,7 +705,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
         } else {
             row = key;
             blk = j;
-            ntok = min(BS, L - blk * BS);
+            ntok = 0;                                        // derived by the consumer
             live = all_rows;
         }
         *info = ntok | (live << 8);
@@ -727,7 +731,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
             ++chunk_cur;
             id_nxt = load_chunk(chunk_cur + 1, &info_nxt);
         }
-        *info = __shfl_sync(kFull, info_cur, kk & 31);
+        *info = PREFIX ? __shfl_sync(kFull, info_cur, kk & 31) : 0;
         return __shfl_sync(kFull, id_cur, kk & 31);
     };
     int32_t* stage_info = reinterpret_cast<int32_t*>(smem + P::kInfoOff);
@@ -735,7 +739,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
         const int s = kk % ST;
         const uint32_t bar = smem_addr(&bars[w * ST + s]);
         stage_id[w * ST + s] = id;
-        stage_info[w * ST + s] = info;
+        if constexpr (PREFIX) stage_info[w * ST + s] = info;
         if (id >= 0) {
             const uint32_t dst = smem_addr(ring + (size_t)((w * ST + s) * 2) * TILE);
             const size_t off = ((size_t)id * p.num_kv_heads + hk) * TILE;
@@ -765,13 +769,13 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const Params p) {
         }
         const int id = stage_id[w * ST + s];
         if (id >= 0) {
-            const int info = stage_info[w * ST + s];
-            const int ntok = info & 0xff;
+            const int info = PREFIX ? stage_info[w * ST + s] : 0;
+            const int ntok = PREFIX ? (info & 0xff) : min(BS, L - (blk0 + w + k * NW) * BS);
             const unsigned char* kt = ring + (size_t)((w * ST + s) * 2) * TILE;
             if constexpr (Math::kWarpSmemFloats > 0)
                 Math::tile(st, kt, kt + TILE, ntok, lane, qs, pb);
             else
-                Math::tile(st, kt, kt + TILE, ntok, lane, p.qscale, qs, pb, info >> 8);
+                Math::template tile<PREFIX>(st, kt, kt + TILE, ntok, lane, p.qscale, qs, pb, info >> 8);
         }
         __syncwarp();
         if (k + ST < nk) {
