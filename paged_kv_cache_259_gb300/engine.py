@@ -1,7 +1,8 @@
 """One decode step of paged attention, end to end, over the C ABI.
 
-A ``PagedKVCache`` owns the two device pools (``[NB, Hkv, bs, D]``) and a host
-``BlockManager``. A step is:
+A ``PagedKVCache`` owns the two device pools (K as ``[NB, Hkv, D/X, bs, X]``
+chunk planes, V as ``[NB, Hkv, D, bs]``; ``k_view``/``v_view`` give the plain
+``[NB, Hkv, bs, D]`` view) and a host ``BlockManager``. A step is:
 
 1. host: one ``append_slot`` per sequence -> slot numbers and copy-on-write
    pairs ("KV cache paginado...", "Como funciona": copy a shared block before
