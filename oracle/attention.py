@@ -99,3 +99,63 @@ def paged_decode(q, k_pool, v_pool, block_tables, seq_lens, scale, block_size,
     for (b, h), o in res.items():
         out[b, h] = o
     return out
+
+
+def paged_prefill(q, k_pool, v_pool, block_tables, seq_lens, query_start, scale, block_size,
+                  k_scale=1.0, v_scale=1.0, units=None):
+    """Chunked-prefill attention through block tables: several query tokens per
+    sequence, each attending causally over the paged cache.
+
+    The feature list of "vLLM PagedAttention: uma revolução no throughput..."
+    names chunked prefill: a long prompt's prefill is split into chunks that run
+    as separate steps. The pages' autoregressive model keeps keys and values of
+    every token already seen (upskillscore "KV cache paginado...", opening
+    paragraph; glossary "Vấn đề bộ nhớ"), so a token attends to itself and to the
+    tokens before it. Readings where the pages are silent: sequence ``b`` holds
+    ``seq_lens[b]`` cached tokens after the chunk's own K/V were written; its
+    chunk is the last ``C_b = query_start[b+1] - query_start[b]`` of them, so
+    chunk query ``i`` sits at position ``p = seq_lens[b] - C_b + i`` and attends
+    keys ``0..p``. Each query row is therefore exactly a decode over its own causal
+    prefix:
+
+        out[query_start[b] + i, h] = decode(q[query_start[b] + i, h], K_b[:p+1], V_b[:p+1])
+
+    q: ``[T, Hq, D]`` (T = query_start[B]); pools ``[NB, Hkv, bs, D]``. With
+    ``units=None`` returns float64 ``[T, Hq, D]``; otherwise ``units`` lists
+    ``(token, h)`` pairs and a dict of their rows is returned.
+    """
+    T, Hq, D = q.shape
+    Hkv = k_pool.shape[1]
+    if Hq % Hkv:
+        raise ValueError("num_heads must be a multiple of num_kv_heads")
+    G = Hq // Hkv
+    bt = np.asarray(block_tables)
+    lens = np.asarray(seq_lens)
+    qs = np.asarray(query_start)
+    B = len(lens)
+    seq_of = np.zeros(T, dtype=np.int64)
+    for b in range(B):
+        if qs[b + 1] - qs[b] > lens[b]:
+            raise ValueError("a chunk cannot be longer than its sequence")
+        seq_of[qs[b]:qs[b + 1]] = b
+    todo = units if units is not None else [(t, h) for t in range(T) for h in range(Hq)]
+    res = {}
+    cache = {}
+    for t, h in todo:
+        b = int(seq_of[t])
+        L = int(lens[b])
+        C = int(qs[b + 1] - qs[b])
+        p = L - C + (t - int(qs[b]))
+        hk = h // G
+        if (b, hk) not in cache:
+            cache = {(b, hk): (widen(gather(k_pool, bt[b], L, hk, block_size)).reshape(L, D),
+                               widen(gather(v_pool, bt[b], L, hk, block_size)).reshape(L, D))}
+        K, V = cache[(b, hk)]
+        qv = q[t, h].to(torch.float64).numpy()
+        res[(t, h)] = decode_one(qv, K[:p + 1], V[:p + 1], scale, k_scale, v_scale)
+    if units is not None:
+        return res
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    for (t, h), o in res.items():
+        out[t, h] = o
+    return out

@@ -421,3 +421,90 @@ def test_llama13b_kv_bytes_per_sequence_closed_form():
     per_token = 40 * 40 * 128 * 2 * 2
     assert per_token == 819200
     assert abs(per_token * 2048 / 1e9 - 1.7) < 0.05
+
+
+# ---------------------------------------------------------------- chunked prefill
+def prefill_case(seed, lens, chunks, Hq, Hkv, D, bs, dtype=torch.float32):
+    """random_case plus a query chunk per sequence: q [sum(chunks), Hq, D]."""
+    q1, kp, vp, tables, sl, conts = random_case(seed, lens, Hq, Hkv, D, bs, dtype=dtype)
+    g = torch.Generator().manual_seed(seed + 1)
+    q = torch.randn(int(sum(chunks)), Hq, D, generator=g).to(dtype)
+    qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int64)
+    return q, kp, vp, tables, sl, qs, conts
+
+
+def sdpa_causal_reference(qc, Kc, Vc, scale):
+    """torch SDPA in float64 with an explicit mask: the chunk's C queries are the
+    last C positions of the L keys (query i may see keys 0 .. L - C + i)."""
+    C, Hq, D = qc.shape
+    L, Hkv, _ = Kc.shape
+    G = Hq // Hkv
+    K = Kc.to(torch.float64).transpose(0, 1).repeat_interleave(G, dim=0)   # [Hq, L, D]
+    V = Vc.to(torch.float64).transpose(0, 1).repeat_interleave(G, dim=0)
+    Q = qc.to(torch.float64).transpose(0, 1)                                 # [Hq, C, D]
+    allowed = torch.arange(L)[None, :] <= (L - C + torch.arange(C))[:, None]
+    o = F.scaled_dot_product_attention(Q, K, V, attn_mask=allowed, scale=scale)
+    return o.transpose(0, 1)                                                 # [C, Hq, D]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,bs", [(4, 4, 64, 16), (8, 2, 32, 4), (6, 3, 16, 1),
+                                          (8, 1, 64, 32)])
+def test_prefill_equals_contiguous_causal_sdpa(Hq, Hkv, D, bs):
+    lens = [1, 7, bs + 3, 3 * bs + 5, 57, 40]
+    chunks = [1, 7, 2, 3 * bs + 5, 20, 1]          # whole prompts, partial chunks, single tokens
+    q, kp, vp, tables, sl, qs, conts = prefill_case(Hq * 10 + D + bs, lens, chunks, Hq, Hkv, D, bs)
+    scale = 1.0 / math.sqrt(D)
+    out = oatt.paged_prefill(q, kp, vp, tables, sl, qs, scale, bs)
+    for b, (Kc, Vc) in enumerate(conts):
+        ref = sdpa_causal_reference(q[qs[b]:qs[b + 1]], Kc, Vc, scale).numpy()
+        np.testing.assert_allclose(out[qs[b]:qs[b + 1]], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_of_one_token_per_sequence_is_decode():
+    lens = [1, 17, 40, 100]
+    q, kp, vp, tables, sl, qs, _ = prefill_case(3, lens, [1, 1, 1, 1], 8, 2, 64, 16)
+    np.testing.assert_array_equal(oatt.paged_prefill(q, kp, vp, tables, sl, qs, 0.2, 16),
+                                  oatt.paged_decode(q, kp, vp, tables, sl, 0.2, 16))
+
+
+def test_prefill_equal_keys_give_running_mean_of_values():
+    """All keys equal: query at position p weights keys 0..p equally, so its
+    output is the mean of V over 0..p (an off-by-one in the causal bound fails)."""
+    L, C, bs, D = 37, 29, 4, 8
+    q, kp, vp, tables, sl, qs, conts = prefill_case(11, [L], [C], 2, 2, D, bs,
+                                                    dtype=torch.float64)
+    kp[:] = 0.25
+    out = oatt.paged_prefill(q, kp, vp, tables, sl, qs, 1.0, bs)
+    Vc = conts[0][1].to(torch.float64).numpy()                 # [L, Hkv, D]
+    for i in range(C):
+        p = L - C + i
+        np.testing.assert_allclose(out[i], Vc[:p + 1].mean(axis=0), rtol=1e-13, atol=1e-13)
+
+
+def test_prefill_first_prompt_token_returns_its_value():
+    q, kp, vp, tables, sl, qs, conts = prefill_case(5, [9], [9], 4, 2, 16, 4, dtype=torch.float64)
+    out = oatt.paged_prefill(q, kp, vp, tables, sl, qs, 0.5, 4)
+    Vc = conts[0][1]
+    np.testing.assert_array_equal(out[0], Vc[0].repeat_interleave(2, dim=0).numpy())
+
+
+def test_prefill_in_chunks_equals_prefill_in_one_pass():
+    """Causal attention over a prompt does not depend on how the prompt is cut
+    into chunks: chunks [11, 1, 20] against the same cache, each with the
+    sequence length it would have after its own write, give the rows of one
+    32-token pass."""
+    L, bs = 32, 8
+    q, kp, vp, tables, sl, qs, _ = prefill_case(21, [L], [L], 6, 3, 32, bs)
+    whole = oatt.paged_prefill(q, kp, vp, tables, sl, qs, 0.17, bs)
+    start = 0
+    for c in (11, 1, 20):
+        part = oatt.paged_prefill(q[start:start + c], kp, vp, tables, np.array([start + c]),
+                                  np.array([0, c]), 0.17, bs)
+        np.testing.assert_allclose(part, whole[start:start + c], rtol=1e-13, atol=1e-13)
+        start += c
+
+
+def test_prefill_rejects_chunk_longer_than_sequence():
+    q, kp, vp, tables, sl, qs, _ = prefill_case(2, [5], [5], 2, 2, 8, 4)
+    with pytest.raises(ValueError):
+        oatt.paged_prefill(q, kp, vp, tables, np.array([4]), qs, 1.0, 4)
