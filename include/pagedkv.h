@@ -31,14 +31,21 @@
  *
  * KV pool layout. The pages show one head as key_pool[block, slot, dim] and
  * say no more; here each pool is [num_blocks][num_kv_heads][tile], one
- * contiguous tile of block_size*head_dim elements per (block, kv head), laid
- * out for the attention kernel:
- *     K tile: [head_dim/X][block_size][X]   X = 16 bytes of elements
- *             (4 float32, 8 bfloat16, 16 E4M3): "chunk plane" j holds dims
- *             jX..jX+X-1 of every token of the block;
- *     V tile: [head_dim][block_size]        transposed: one row per dim.
- * So K element (blk, h, t, d) is at ((blk*Hkv + h)*(D/X) + d/X)*bs*X + t*X + d%X
- * and V element (blk, h, t, d) at ((blk*Hkv + h)*D + d)*bs + t. Element type:
+ * contiguous tile of block_size*head_dim elements per (block, kv head), made of
+ * 128-byte "core matrices" (8 rows of 16 bytes; X = 16 bytes of elements: 4
+ * float32, 8 bfloat16, 16 E4M3):
+ *     K tile: [block_size/8][head_dim/X][8][X]  core matrix (g, c) = tokens
+ *             8g..8g+7 (rows) x dims cX..cX+X-1;
+ *     V tile: [block_size/X][head_dim/8][8][X]  core matrix (c, g) = dims
+ *             8g..8g+7 (rows) x tokens cX..cX+X-1 (V is stored transposed).
+ * So K element (blk, h, t, d) is at
+ *     (blk*Hkv + h)*bs*D + ((t/8)*(D/X) + d/X)*8X + (t%8)*X + d%X
+ * and V element (blk, h, t, d) at
+ *     (blk*Hkv + h)*bs*D + ((t/X)*(D/8) + d/8)*8X + (d%8)*X + t%X.
+ * A core matrix is what one ldmatrix or tensor-core operand row group reads,
+ * so every tile lands in shared memory with one 1-D bulk copy already in the
+ * operand layout of the tensor cores. block_size must be a multiple of 16.
+ * Element type:
  * float32, bfloat16, or E4M3 bytes (OCP FP8, value = code * per-tensor scale).
  * A whole block (every head, K and V) is num_kv_heads*block_size*head_dim
  * elements per pool, contiguous.
@@ -221,6 +228,49 @@ PKV_API int reshape_and_cache(const void* k, const void* v, void* k_pool, void* 
  * ---------------------------------------------------------------------- */
 PKV_API int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs,
                 int num_pairs, int num_blocks, size_t block_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * paged_attention_prefill -- chunked prefill: several new query tokens per
+ * sequence, each attending causally over that sequence's cached tokens
+ * gathered through its block table. Chunked prefill (a long prompt's prefill
+ * cut into chunks run as separate steps) is in the feature list of "vLLM
+ * PagedAttention: uma revolução no throughput..."; a token attends to itself
+ * and to every token before it ("KV cache paginado...", opening paragraph:
+ * the autoregressive model keeps K/V of every token already seen); the tiled,
+ * score-matrix-free kernel is the FlashAttention item of the glossary's
+ * "Các kỹ thuật liên quan".
+ *
+ * Sequence b (b < num_seqs) holds L = seq_lens[b] cached tokens, its chunk's
+ * own K/V already written (reshape_and_cache); the chunk is the last
+ * C = query_start[b+1] - query_start[b] of them. For chunk query i < C
+ * (position p = L - C + i) and query head h (KV head h/G, G = num_heads /
+ * num_kv_heads):
+ *     out[query_start[b] + i][h] = sum_{t <= p} softmax_t(scale * <q[.][h], K[t]>) V[t]
+ *
+ *   out           device, [query_start[num_seqs]][num_heads][head_dim] bf16, written
+ *   q             device, [query_start[num_seqs]][num_heads][head_dim] bf16
+ *   k_pool/v_pool device, pool layouts above, bf16, 16-byte aligned
+ *   block_tables  device int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                 ceil(L/block_size) are not read
+ *   seq_lens      device int32 [num_seqs], C <= L <= max_blocks_per_seq*block_size
+ *   query_start   device int32 [num_seqs + 1], non-decreasing, query_start[0] = 0
+ *   max_query_len an upper bound on every C (sizes the grid; queries past it
+ *                 are not computed)
+ *   q_dtype/kv_dtype  BF16 / BF16
+ *   stream        cudaStream_t
+ * Supported: head_dim 128, block_size in {16,32}, G dividing 128. Runs on the
+ * tcgen05 tensor cores (one 128-row query tile per CTA); allocates nothing.
+ * A sequence with C > L or L beyond its table, or a table entry outside
+ * [0, num_blocks), sets PKV_ERR_OUT_OF_RANGE in the device error word (the
+ * sequence's rows are left unwritten, or the block's keys get zero values).
+ * ---------------------------------------------------------------------- */
+PKV_API int paged_attention_prefill(void* out, const void* q,
+                            const void* k_pool, const void* v_pool,
+                            const int32_t* block_tables, const int32_t* seq_lens,
+                            const int32_t* query_start, int num_seqs, int max_query_len,
+                            int max_blocks_per_seq, int num_blocks,
+                            int num_heads, int num_kv_heads, int head_dim, int block_size,
+                            float scale, int q_dtype, int kv_dtype, void* stream);
 
 /* ------------------------------------------------------------------------
  * paged_attention_decode_noalloc -- paged_attention_decode for callers that

@@ -24,8 +24,10 @@ import torch
 __all__ = [
     "PagedKVError", "paged_attention_decode", "paged_attention_workspace_size",
     "paged_attention_decode_noalloc", "NOALLOC_WORKSPACE_BYTES", "paged_attention_decode_grouped",
+    "paged_attention_prefill",
     "reshape_and_cache", "copy_blocks", "get_device_error", "kernel_launches", "BlockManager",
-    "library_path", "load_library", "pool_shapes", "PKV_F32", "PKV_BF16", "PKV_E4M3",
+    "library_path", "load_library", "pool_shapes", "pool_views", "pools_from_views", "PKV_F32",
+    "PKV_BF16", "PKV_E4M3",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -77,6 +79,9 @@ def load_library():
         "paged_attention_decode_noalloc": (c_int, [vp, vp, vp, vp, vp, vp, c_int, c_int, c_int,
                                                    c_int, c_int, c_int, c_int, c_float, c_int,
                                                    c_int, c_float, c_float, vp]),
+        "paged_attention_prefill": (c_int, [vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int,
+                                            c_int, c_int, c_int, c_int, c_int, c_float, c_int,
+                                            c_int, vp]),
         "reshape_and_cache": (c_int, [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
                                       c_int, c_int, c_float, c_float, vp]),
         "copy_blocks": (c_int, [vp, vp, vp, c_int, c_int, c_size, vp]),
@@ -158,26 +163,45 @@ class _on_device:
 def pool_shapes(num_blocks, num_kv_heads, block_size, head_dim, dtype):
     """Tensor shapes of the K and V pools in the library's layout.
 
-    K: ``[NB, Hkv, D // X, bs, X]`` (X = 16 bytes of elements), V:
-    ``[NB, Hkv, D, bs]`` (transposed per block). Each (block, head) tile is
-    contiguous; see ``include/pagedkv.h``.
+    Each (block, head) tile is contiguous and made of 128-byte core matrices
+    (8 rows of 16 bytes; X = 16 bytes of elements): K ``[NB, Hkv, bs/8, D/X, 8,
+    X]`` (8 tokens x X dims per core matrix), V ``[NB, Hkv, bs/X, D/8, 8, X]``
+    (8 dims x X tokens per core matrix). See ``include/pagedkv.h``.
     """
     esize = torch.empty((), dtype=dtype).element_size()
     x = 16 // esize
-    if head_dim % x:
-        raise ValueError(f"head_dim must be a multiple of {x} for {dtype}")
-    return ((num_blocks, num_kv_heads, head_dim // x, block_size, x),
-            (num_blocks, num_kv_heads, head_dim, block_size))
+    if head_dim % x or head_dim % 8 or block_size % 8 or block_size % x:
+        raise ValueError(f"head_dim and block_size must be multiples of {max(x, 8)} for {dtype}")
+    return ((num_blocks, num_kv_heads, block_size // 8, head_dim // x, 8, x),
+            (num_blocks, num_kv_heads, block_size // x, head_dim // 8, 8, x))
+
+
+def pool_views(k_pool, v_pool):
+    """The pools as plain ``[NB, Hkv, bs, D]`` (block, head, slot, dim) copies."""
+    NB, Hkv, bs, D = _pool_dims(k_pool, v_pool)
+    k = k_pool.permute(0, 1, 2, 4, 3, 5).reshape(NB, Hkv, bs, D)
+    v = v_pool.permute(0, 1, 2, 5, 3, 4).reshape(NB, Hkv, bs, D)
+    return k, v
+
+
+def pools_from_views(k, v):
+    """Plain ``[NB, Hkv, bs, D]`` K/V -> pools in the library layout (copies)."""
+    NB, Hkv, bs, D = k.shape
+    x = 16 // k.element_size()
+    kp = k.reshape(NB, Hkv, bs // 8, 8, D // x, x).permute(0, 1, 2, 4, 3, 5).contiguous()
+    vp = v.reshape(NB, Hkv, bs // x, x, D // 8, 8).permute(0, 1, 2, 4, 5, 3).contiguous()
+    return kp, vp
 
 
 def _pool_dims(k_pool, v_pool):
     """(NB, Hkv, bs, D) of pools in the library layout; raise on a mismatch."""
-    if k_pool.dim() != 5 or v_pool.dim() != 4 or k_pool.dtype != v_pool.dtype:
-        raise ValueError("pools must be K [NB, Hkv, D/X, bs, X] and V [NB, Hkv, D, bs] "
-                         "of one dtype (see pool_shapes)")
-    NB, Hkv, DX, bs, X = k_pool.shape
-    D = DX * X
-    if X * k_pool.element_size() != 16 or tuple(v_pool.shape) != (NB, Hkv, D, bs):
+    if k_pool.dim() != 6 or v_pool.dim() != 6 or k_pool.dtype != v_pool.dtype:
+        raise ValueError("pools must be K [NB, Hkv, bs/8, D/X, 8, X] and V [NB, Hkv, bs/X, D/8, "
+                         "8, X] of one dtype (see pool_shapes)")
+    NB, Hkv, G8, P, r8, X = k_pool.shape
+    bs, D = G8 * 8, P * X
+    if X * k_pool.element_size() != 16 or r8 != 8 or bs % X or \
+            tuple(v_pool.shape) != (NB, Hkv, bs // X, D // 8, 8, X):
         raise ValueError("pool shapes do not match the library layout (see pool_shapes)")
     return NB, Hkv, bs, D
 
@@ -303,6 +327,42 @@ def paged_attention_decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_len
             Hq, Hkv, D, bs, float(scale), _dt(q, "q"), _dt(k_pool, "k_pool"),
             float(k_scale), float(v_scale), _stream_ptr(stream, q.device))
     _check(st, "paged_attention_decode_noalloc")
+    return out
+
+
+def paged_attention_prefill(out, q, k_pool, v_pool, block_tables, seq_lens, query_start,
+                            scale, max_query_len, stream=None):
+    """Chunked prefill: for sequence b, the last ``C_b = query_start[b+1] -
+    query_start[b]`` of its ``seq_lens[b]`` cached tokens are the chunk; chunk
+    query i attends causally to keys ``0 .. seq_lens[b] - C_b + i``.
+
+    q, out: bfloat16 ``[T, Hq, D]`` (T = query_start[-1]); pools bfloat16 in the
+    library layout; block_tables int32 ``[B, max_blocks]``; seq_lens int32
+    ``[B]``; query_start int32 ``[B + 1]``; ``max_query_len`` >= every C_b.
+    """
+    lib = load_library()
+    for t, n in ((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
+                 (block_tables, "block_tables"), (seq_lens, "seq_lens"),
+                 (query_start, "query_start")):
+        _cuda(t, n)
+    for t in (block_tables, seq_lens, query_start):
+        if t.dtype != torch.int32:
+            raise TypeError("block_tables, seq_lens and query_start must be int32")
+    if q.dim() != 3 or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("q and out must be [T, Hq, D] of the same dtype")
+    B = seq_lens.shape[0]
+    T, Hq, D = q.shape
+    NB, Hkv, bs, D2 = _pool_dims(k_pool, v_pool)
+    if D2 != D or block_tables.dim() != 2 or block_tables.shape[0] != B or \
+            query_start.shape != (B + 1,):
+        raise ValueError("inconsistent shapes")
+    with _on_device(q.device):
+        st = lib.paged_attention_prefill(
+            out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
+            block_tables.data_ptr(), seq_lens.data_ptr(), query_start.data_ptr(), B,
+            int(max_query_len), block_tables.shape[1], NB, Hq, Hkv, D, bs, float(scale),
+            _dt(q, "q"), _dt(k_pool, "k_pool"), _stream_ptr(stream, q.device))
+    _check(st, "paged_attention_prefill")
     return out
 
 

@@ -22,6 +22,7 @@ CUDA_SOURCES = [
     "pkv_decode_bf16.cu",
     "pkv_decode_e4m3.cu",
     "pkv_decode_noalloc.cu",
+    "pkv_prefill.cu",
 ]
 CXX_SOURCES = ["block_manager.cpp"]
 

@@ -62,17 +62,22 @@ struct ChunkConvert<ST, uint8_t> {
     }
 };
 
-// Cache layout (per block and kv head; see the decode kernels): K as chunk
-// planes [D/X][bs][X] with X = 16 bytes of cache elements, V transposed [D][bs].
-// One thread converts one 16-byte group of X dims of one (token, head): for K it
-// is one 16-byte store into the token's row of plane j, for V X element stores
-// down the token's column of rows jX..jX+X-1.
+// Cache layout (per block and kv head), X = 16 bytes of cache elements: each
+// tile is a sequence of 128-byte core matrices (8 rows of 16 bytes), K as
+// [bs/8][D/X][8][X] (8 tokens x X dims each) and V as [bs/X][D/8][8][X] (8 dims x
+// X tokens each). One thread converts one 16-byte group of X dims of one
+// (token, head): for K it is one 16-byte store, for V X element stores, one into
+// each of the X dims' rows at the token's column.
 template <typename CT>
-__device__ __forceinline__ void store_column(CT* dst, const uint4& v, int stride) {
+__device__ __forceinline__ void store_v_column(CT* tile, const uint4& v, int d0, int d, int off) {
     constexpr int CV = 16 / sizeof(CT);
     const CT* e = reinterpret_cast<const CT*>(&v);
+    const long long col = (long long)(off / CV) * (d / 8) * 8 * CV + off % CV;
 #pragma unroll
-    for (int i = 0; i < CV; ++i) dst[(size_t)i * stride] = e[i];
+    for (int i = 0; i < CV; ++i) {
+        const int dd = d0 + i;
+        tile[col + (long long)(dd >> 3) * 8 * CV + (dd & 7) * CV] = e[i];
+    }
 }
 
 template <typename ST, typename CT>
@@ -104,11 +109,10 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
         const uint4 val = CC::run(src, is_v ? v_scale : k_scale);
         const long long tile = (blk * hkv + h) * (long long)d * bs;      // elements
         if (!is_v) {
-            CT* dst = k_pool + tile + ((long long)j * bs + off) * CC::CV;
+            CT* dst = k_pool + tile + ((off >> 3) * planes + j) * 8 * CC::CV + (off & 7) * CC::CV;
             *reinterpret_cast<uint4*>(dst) = val;
         } else {
-            CT* dst = v_pool + tile + (long long)j * CC::CV * bs + off;
-            store_column(dst, val, bs);
+            store_v_column(v_pool + tile, val, j * CC::CV, d, (int)off);
         }
     }
 }
@@ -174,7 +178,7 @@ int reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
     using namespace pkv;
     if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
         return PKV_ERR_INVALID_ARG;
-    if (head_dim % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    if (head_dim % 16 != 0 || block_size % 16 != 0) return PKV_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PKV_OK;
     if (!k || !v || !k_pool || !v_pool || !slot_mapping) return PKV_ERR_INVALID_ARG;
     if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool))

@@ -141,11 +141,22 @@ __device__ __forceinline__ void unpack(const uint4& r, float (&f)[16]) {
 template <typename KV, int D, int BS>
 struct Layout {
     static constexpr int kElt = Elt<KV>::kSize;
-    static constexpr int kX = 16 / kElt;          // elements per K chunk (16 bytes)
-    static constexpr int kPlanes = D / kX;        // K chunk planes per tile
+    static constexpr int kX = 16 / kElt;          // elements per 16-byte chunk
+    static constexpr int kPlanes = D / kX;        // K chunks per token
     static constexpr int kTile = BS * D * kElt;   // bytes of one (block, kv head) tile
-    static constexpr int kVRow = BS * kElt;       // bytes of one V row (one dim)
-    static_assert(D % kX == 0, "head_dim must be whole K chunks");
+    static constexpr int kVRow = BS * kElt;       // bytes of one dim's tokens in V
+    static_assert(D % kX == 0 && D % 8 == 0 && BS % 8 == 0 && BS % kX == 0,
+                  "head_dim and block_size must be whole chunks");
+    // Both tiles are stored as 128-byte core matrices (8 rows x 16 bytes):
+    // K [BS/8][D/X][8][X] (8 tokens x X dims per core matrix), V [BS/X][D/8][8][X]
+    // (8 dims x X tokens). Byte offset of K chunk `plane` of token `tok`:
+    __host__ __device__ static constexpr int k_off(int plane, int tok) {
+        return ((tok >> 3) * kPlanes + plane) * 128 + (tok & 7) * 16;
+    }
+    // Byte offset of the 16-byte V chunk holding tokens tc*X .. tc*X+X-1 of dim d:
+    __host__ __device__ static constexpr int v_off(int d, int tc) {
+        return (tc * (D / 8) + (d >> 3)) * 128 + (d & 7) * 16;
+    }
 };
 
 // ============================================================ CUDA-core tile math
@@ -201,7 +212,7 @@ struct SimtMath {
         for (int i = 0; i < PASSES; ++i) {
             const int j = i * CPP + cp;
             float kf[X];
-            unpack(*reinterpret_cast<const uint4*>(kt + (j * BS + t) * 16), kf);
+            unpack(*reinterpret_cast<const uint4*>(kt + Lay::k_off(j, t)), kf);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
 #pragma unroll
@@ -249,7 +260,7 @@ struct SimtMath {
             for (int k = 0; k < DPL; ++k) {
                 const int d = lane + 32 * k;
                 float vf[TPC];
-                unpack(*reinterpret_cast<const uint4*>(vt + d * Lay::kVRow + ch * 16), vf);
+                unpack(*reinterpret_cast<const uint4*>(vt + Lay::v_off(d, ch)), vf);
                 if (partial) {
 #pragma unroll
                     for (int x = 0; x < TPC; ++x)
@@ -404,7 +415,7 @@ struct MmaMath {
                         const int m = lane >> 3, rr = lane & 7;
                         const int u = m & 1, plane = ks + (m >> 1);
                         const int tok = 16 * h + 4 * (rr >> 1) + 2 * u + (rr & 1);
-                        ldsm_x4(kbase + (plane * BS + tok) * 16, k8[0], k8[1], k8[2], k8[3]);
+                        ldsm_x4(kbase + Lay::k_off(plane, tok), k8[0], k8[1], k8[2], k8[3]);
                     }
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
@@ -416,7 +427,7 @@ struct MmaMath {
                     const int m = lane >> 3, rr = lane & 7;
                     const int plane = 2 * ks + (m & 1);
                     const int tok = 16 * h + 8 * (m >> 1) + rr;
-                    ldsm_x4(kbase + (plane * BS + tok) * 16, b[0][0], b[0][1], b[1][0], b[1][1]);
+                    ldsm_x4(kbase + Lay::k_off(plane, tok), b[0][0], b[0][1], b[1][0], b[1][1]);
                 }
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
@@ -480,7 +491,7 @@ struct MmaMath {
                     if ((nt & 2) == 0) {
                         const int m = lane >> 3, rr = lane & 7;
                         const int d = 8 * (nt + m) + rr;
-                        ldsm_x4(vbase + d * Lay::kVRow + 16 * h, v8[0], v8[1], v8[2], v8[3]);
+                        ldsm_x4(vbase + Lay::v_off(d, h), v8[0], v8[1], v8[2], v8[3]);
                     }
 #pragma unroll
                     for (int x = 0; x < 2; ++x) {
@@ -497,7 +508,7 @@ struct MmaMath {
                     const int m = lane >> 3, rr = lane & 7;
                     const int d = 8 * (nt + (m >> 1)) + rr;
                     const int tok = 16 * h + 8 * (m & 1);
-                    ldsm_x4(vbase + (d * BS + tok) * 2, b[0][0], b[0][1], b[1][0], b[1][1]);
+                    ldsm_x4(vbase + Lay::v_off(d, tok / 8), b[0][0], b[0][1], b[1][0], b[1][1]);
                     if (tail < 16) {                         // lane holds tokens 2c,2c+1 (+8)
 #pragma unroll
                         for (int x = 0; x < 2; ++x)

@@ -1,0 +1,464 @@
+// Chunked-prefill attention over the paged KV cache on the fifth-generation
+// tensor cores (tcgen05, accumulators in tensor memory).
+//
+// What it computes: the feature list of "vLLM PagedAttention: uma revolução no
+// throughput..." names chunked prefill, a long prompt's prefill split into
+// chunks run as separate steps. Sequence b holds seq_lens[b] cached tokens after
+// its chunk's own K/V were written; the chunk is its last C_b tokens, and chunk
+// query i (position p = L_b - C_b + i) attends keys 0..p, the tokens already
+// seen by the autoregressive model (upskillscore "KV cache paginado...", opening
+// paragraph). The glossary "PagedAttention" ("Các kỹ thuật liên quan") has
+// engines run FlashAttention-style kernels over the paged blocks: the score
+// matrix is tiled and never written to memory.
+//
+// One CTA = one tile of 128 query rows (128/G chunk tokens x the G query heads
+// of one KV head, so each K/V tile feeds every head that shares it) of one
+// sequence. Warp roles:
+// * warps 0-3 (softmax): thread r owns row r = TMEM lane r. Puts its q row in
+//   TMEM, then per KV tile reads its 128 scores, applies the causal mask, keeps
+//   the running max / sum (exp2 domain, scale * log2 e folded in), writes P
+//   (bf16) back into TMEM over the scores, and finally normalises O;
+// * warp 4 (MMA): one thread issues S = Q K^T (A = Q from TMEM, B = the K tile
+//   in shared memory, M = N = 128) and O += P V (A = P from TMEM, B = the V
+//   tile, K = 16 keys per instruction), and owns the TMEM allocation;
+// * warp 5 (loader): one thread copies each KV tile of 128 keys block by block
+//   (through the block table) with 1-D bulk copies: the cache stores every
+//   (block, head) tile as 128-byte core matrices, K [bs/8][D/8][8][8] and V
+//   [bs/8][D/8][8][8] (8 dims x 8 tokens), which is the canonical no-swizzle
+//   K-major operand layout, so a tile lands ready for the tensor cores (S with
+//   N = 128 keys over 8 blocks, P.V with K = 16 keys per instruction). Keys
+//   past the sequence in its last, partly written block get zero V values.
+// S is double-buffered in TMEM so the scores of tile j+1 are computed while the
+// softmax works on tile j; K/V tiles run through a 3-stage shared-memory ring.
+// The running max is only moved (and O rescaled) when a tile's max exceeds it by
+// more than 2^8, so O is rarely touched; the result is the same softmax.
+#include <cmath>
+
+#include <cuda_bf16.h>
+
+#include "pkv_internal.cuh"
+#include "pkv_tcgen05.cuh"
+
+namespace pkv {
+namespace prefill {
+
+constexpr int kD = 128;            // head dim
+constexpr int kRows = 128;         // query rows per CTA (M)
+constexpr int kKeys = 128;         // keys per KV tile (N of S, K of P.V)
+constexpr int kStages = 3;
+constexpr int kTileBytes = kKeys * kD * 2;         // one K (or V) tile, bf16
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kSmem = kStages * kStageBytes;       // 192 KB: one CTA per SM
+constexpr int kMmaWarp = 4;
+constexpr int kLoadWarp = 5;
+constexpr int kThreads = 6 * 32;
+constexpr int kGroupBytes = (kD / 8) * 128;         // K: 8 tokens x 128 dims
+constexpr int kChunkBytes = (kD / 8) * 128;         // V: 128 dims x 8 tokens
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0, kColS = 128, kColQ = 384;   // O | S0 | S1 | Q
+constexpr float kRescaleLog2 = 8.0f;
+constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kRows, 128);      // S and P.V: M = N = 128
+
+static_assert(kSmem <= 227 * 1024, "shared memory ring too large");
+
+struct Params {
+    __nv_bfloat16* out;
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k_pool;
+    const __nv_bfloat16* v_pool;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    const int32_t* query_start;
+    int max_blocks;
+    int num_blocks;
+    int num_heads;
+    int num_kv_heads;
+    int G;
+    float scale_log2;   // softmax scale * log2(e)
+    int* err;
+};
+
+// 1-D bulk copy global -> shared (TMA engine), completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Barriers (in this order in shared memory).
+enum : int { kBarFull = 0, kBarEmpty = kStages, kBarS = 2 * kStages, kBarP = kBarS + 2,
+             kBarO = kBarP + 2, kBarQ = kBarO + 1, kBarDrain = kBarQ + 1, kBarLand = kBarDrain + 1,
+             kNumBars = kBarLand + 1 };
+
+template <int BS>
+__global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params p) {
+    constexpr int kBlocksPerTile = kKeys / BS;
+    constexpr int kBlockBytes = BS * kD * 2;       // one (block, head) tile
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ __align__(8) uint64_t bars[kNumBars];
+    __shared__ uint32_t tmem_slot;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.z, hk = blockIdx.y;
+    const int qtile = gridDim.x - 1 - blockIdx.x;          // longest tiles first
+    const int G = p.G;
+    const int tok_per_tile = kRows / G;
+    const int L = p.seq_lens[b];
+    const int q0 = p.query_start[b];
+    const int C = p.query_start[b + 1] - q0;
+    if (C < 0 || C > L || L > p.max_blocks * BS) {
+        if (tid == 0 && C != 0) flag_error(p.err, kErrOutOfRange);
+        return;
+    }
+    const int i0 = qtile * tok_per_tile;
+    if (i0 >= C) return;                                   // uniform over the CTA
+    const int i_last = min(C, i0 + tok_per_tile) - 1;
+    const int p_min = L - C + i0;                          // first query's position
+    const int p_max = L - C + i_last;                      // last query's position
+    const int n_tiles = p_max / kKeys + 1;                 // tiles of keys 0..p_max
+    const int first_masked = (p_min + 1) / kKeys;          // tiles before it need no mask
+    const int blk_last = p_max / BS;                       // last block any query sees
+
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t bar0 = smem_addr(bars);
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(kBarFull + s), 1);
+            mbar_init(bar(kBarEmpty + s), 1);
+        }
+        mbar_init(bar(kBarLand), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(kBarS + i), 1);
+            mbar_init(bar(kBarP + i), 128);
+        }
+        mbar_init(bar(kBarO), 1);
+        mbar_init(bar(kBarQ), 128);
+        mbar_init(bar(kBarDrain), 1);
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tc::alloc(smem_addr(&tmem_slot), kTmemCols);
+        tc::relinquish_alloc_permit();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == kLoadWarp) {
+        // ------------------------------------------------------------ loader
+        const int32_t* bt = p.block_tables + (size_t)b * p.max_blocks;
+        const int tail = L % BS;                           // tokens in a partly written last block
+        for (int j = 0; j < n_tiles; ++j) {
+            const int s = j % kStages;
+            if (j >= kStages &&
+                !mbar_wait_bounded(bar(kBarEmpty + s), ((j / kStages) - 1) & 1, p.err)) {
+                flag_error(p.err, kErrTimeout);
+                break;
+            }
+            const uint32_t ks = sbase + (uint32_t)(s * kStageBytes);
+            const uint32_t vs = ks + kTileBytes;
+            const int blk0 = j * kBlocksPerTile;
+            const int n_load = min(kBlocksPerTile, blk_last - blk0 + 1);
+            // the block holding the sequence's last token is zero-filled past it
+            const bool fix = tail != 0 && blk_last == (L - 1) / BS && blk_last < blk0 + kBlocksPerTile;
+            const uint32_t land = fix ? bar(kBarLand) : bar(kBarFull + s);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(land, (uint32_t)(2 * n_load * kBlockBytes));
+                for (int jb = 0; jb < n_load; ++jb) {
+                    int id = bt[blk0 + jb];
+                    if (id < 0 || id >= p.num_blocks) {
+                        flag_error(p.err, kErrOutOfRange);
+                        id = 0;                            // in bounds; the sequence is in error
+                    }
+                    const size_t off = ((size_t)id * p.num_kv_heads + hk) * (size_t)(BS * kD);
+                    bulk_load(ks + (uint32_t)(jb * kBlockBytes), p.k_pool + off, kBlockBytes, land);
+                    bulk_load(vs + (uint32_t)(jb * kBlockBytes), p.v_pool + off, kBlockBytes, land);
+                }
+            }
+            if (fix) {
+                if (!mbar_wait_bounded(bar(kBarLand), 0, p.err)) {
+                    flag_error(p.err, kErrTimeout);
+                    break;
+                }
+                // V of the last block: [BS/8 chunks][128 dims] rows of 8 tokens
+                const uint32_t vb = vs + (uint32_t)((blk_last - blk0) * kBlockBytes);
+                for (int row = lane; row < (BS / 8) * kD; row += 32) {
+                    const int valid = tail - (row / kD) * 8;   // tokens of this row's chunk kept
+                    if (valid >= 8) continue;
+                    uint4* v = reinterpret_cast<uint4*>(smem + (vb - sbase) + row * 16);
+                    uint4 x = *v;
+                    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (2 * e >= valid) w[e] = 0u;
+                        else if (2 * e + 1 >= valid) w[e] &= 0x0000ffffu;
+                    }
+                    *v = x;
+                }
+                fence_proxy_async_smem();                  // visible to the tensor cores
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarFull + s));
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = mbar_wait_bounded(bar(kBarQ), 0, p.err);
+            tc::fence_after_sync();
+            auto issue_s = [&](int j) {
+                const int s = j % kStages;
+                ok = ok && mbar_wait_bounded(bar(kBarFull + s), (j / kStages) & 1, p.err);
+                if (!ok) return;
+                tc::fence_after_sync();
+                const uint32_t ks = sbase + (uint32_t)(s * kStageBytes);
+                const uint32_t d = tmem + kColS + (uint32_t)(j & 1) * 128;
+                // B = 128 keys: 8-token core-matrix groups 2 KB apart (SBO), the
+                // two 8-dim chunks of a 16-dim step 128 bytes apart (LBO)
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    tc::mma_ts(d, tmem + kColQ + kk * 8,
+                               tc::smem_desc(ks + (uint32_t)(kk * 256), 128, kGroupBytes), kIdesc,
+                               kk > 0);
+                tc::commit(bar(kBarS + (j & 1)));
+            };
+            issue_s(0);
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                if (j + 1 < n_tiles) issue_s(j + 1);
+                ok = ok && mbar_wait_bounded(bar(kBarP + (j & 1)), (j >> 1) & 1, p.err);
+                if (!ok) break;
+                tc::fence_after_sync();
+                const uint32_t vs = sbase + (uint32_t)((j % kStages) * kStageBytes + kTileBytes);
+                const uint32_t pa = tmem + kColS + (uint32_t)(j & 1) * 128;
+                // 16-key steps that hold a key some query sees (P is 0 past them)
+                const int n16 = min(kKeys / 16, (p_max - j * kKeys) / 16 + 1);
+                // B = V of 16 keys: two 8-token chunks 2 KB apart (LBO), 8-dim
+                // core-matrix rows 128 bytes apart (SBO)
+                for (int jj = 0; jj < n16; ++jj)
+                    tc::mma_ts(tmem + kColO, pa + jj * 8,
+                               tc::smem_desc(vs + (uint32_t)(jj * 2 * kChunkBytes), kChunkBytes, 128),
+                               kIdesc, (j > 0 || jj > 0));
+                tc::commit(bar(kBarEmpty + j % kStages));
+                tc::commit(bar(kBarO));
+            }
+            if (!ok) flag_error(p.err, kErrTimeout);
+            // every MMA issued here is complete before tensor memory is released
+            tc::commit(bar(kBarDrain));
+            mbar_wait_bounded(bar(kBarDrain), 0, nullptr);   // a real wait even after a timeout
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int r = tid;
+        const int il = r / G, g = r % G;
+        const int i = i0 + il;
+        const bool valid = i < C;
+        const int pr = valid ? L - C + i : L - 1;
+        const int h = hk * G + g;
+        const uint32_t row = tmem + ((uint32_t)(warp * 32) << 16);
+        bool ok = true;
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                p.q + ((size_t)(q0 + (valid ? i : 0)) * p.num_heads + h) * kD);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t v[32];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint4 x = valid ? src[half * 8 + u] : make_uint4(0, 0, 0, 0);
+                    v[4 * u] = x.x;
+                    v[4 * u + 1] = x.y;
+                    v[4 * u + 2] = x.z;
+                    v[4 * u + 3] = x.w;
+                }
+                tc::st32(row + kColQ + half * 32, v);
+            }
+            tc::wait_st();
+            tc::fence_before_sync();
+            mbar_arrive(bar(kBarQ));
+        }
+        const float sc = p.scale_log2;
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int j = 0; j < n_tiles; ++j) {
+            const uint32_t sb = kColS + (uint32_t)(j & 1) * 128;
+            ok = ok && mbar_wait_bounded(bar(kBarS + (j & 1)), (j >> 1) & 1, p.err);
+            ok = __all_sync(0xffffffffu, ok);              // the warp's tcgen05 ops stay converged
+            if (!ok) break;
+            tc::fence_after_sync();
+            uint32_t sv[4][32];
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) tc::ld32(row + sb + cb * 32, sv[cb]);
+            tc::wait_ld();
+            float s[kKeys];
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb)
+#pragma unroll
+                for (int c = 0; c < 32; ++c) s[cb * 32 + c] = __uint_as_float(sv[cb][c]);
+            if (j >= first_masked) {
+                const int lim = pr - j * kKeys;            // keys 0..lim of this tile are visible
+#pragma unroll
+                for (int c = 0; c < kKeys; ++c) s[c] = c <= lim ? s[c] : -INFINITY;
+            }
+            float m8[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) m8[c] = s[c];
+#pragma unroll
+            for (int c = 8; c < kKeys; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            const float mt = mx * sc;
+            bool o_seen = false;
+            if (j == 0) {
+                m_run = mt;
+            } else if (__any_sync(0xffffffffu, mt > m_run + kRescaleLog2)) {
+                // move the running max: O must hold P.V of every earlier tile first
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarO), (j - 1) & 1, p.err));
+                o_seen = true;
+                tc::fence_after_sync();
+                const float m_new = fmaxf(m_run, mt);
+                const float alpha = ex2(m_run - m_new);
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t v[32];
+                    tc::ld32(row + kColO + cb * 32, v);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
+                    tc::st32(row + kColO + cb * 32, v);
+                }
+                tc::wait_st();
+                l_run *= alpha;
+                m_run = m_new;
+            }
+            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const float p0 = ex2(fmaf(s[cb * 32 + 2 * c], sc, -m_run));
+                    const float p1 = ex2(fmaf(s[cb * 32 + 2 * c + 1], sc, -m_run));
+                    l4[c & 3] += p0 + p1;
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                    pk[c] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
+                tc::st16(row + sb + cb * 16, pk);
+            }
+            l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+            tc::wait_st();
+            // consume this barrier's phase for tile j-1 so its parity stays unambiguous
+            if (j >= 1 && !o_seen) ok = ok && mbar_wait_bounded(bar(kBarO), (j - 1) & 1, p.err);
+            ok = __all_sync(0xffffffffu, ok);
+            tc::fence_before_sync();
+            mbar_arrive(bar(kBarP + (j & 1)));
+        }
+        if (ok) ok = mbar_wait_bounded(bar(kBarO), (n_tiles - 1) & 1, p.err);
+        ok = __all_sync(0xffffffffu, ok);
+        tc::fence_after_sync();
+        if (!ok) {
+            flag_error(p.err, kErrTimeout);
+        } else {
+            const float inv = 1.f / l_run;
+            uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)(q0 + (valid ? i : 0)) * p.num_heads + h) * kD);
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t v[32];
+                tc::ld32(row + kColO + cb * 32, v);
+                tc::wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                                __uint_as_float(v[8 * u + 2 * e]) * inv,
+                                __uint_as_float(v[8 * u + 2 * e + 1]) * inv);
+                            w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                        }
+                        dst[cb * 4 + u] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc::fence_after_sync();
+        tc::dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int BS>
+int launch(const Params& p, dim3 grid, cudaStream_t stream) {
+    auto kern = paged_prefill_kernel<BS>;
+    int occ = 0;
+    const int st = kernel_setup(reinterpret_cast<const void*>(kern), kSmem, kThreads, &occ);
+    if (st != PKV_OK) return st;
+    note_launch();
+    kern<<<grid, kThreads, kSmem, stream>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PKV_OK : cuda_fail("prefill: kernel launch", e);
+}
+
+}  // namespace prefill
+}  // namespace pkv
+
+extern "C" int paged_attention_prefill(void* out, const void* q, const void* k_pool,
+                                       const void* v_pool, const int32_t* block_tables,
+                                       const int32_t* seq_lens, const int32_t* query_start,
+                                       int num_seqs, int max_query_len, int max_blocks_per_seq,
+                                       int num_blocks, int num_heads, int num_kv_heads,
+                                       int head_dim, int block_size, float scale, int q_dtype,
+                                       int kv_dtype, void* stream) {
+    using namespace pkv;
+    if (num_seqs < 0 || num_seqs > 65535 || max_query_len < 0 || max_blocks_per_seq <= 0 ||
+        num_blocks <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_kv_heads > 65535 ||
+        head_dim <= 0 || block_size <= 0 || !std::isfinite(scale))
+        return PKV_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    const int G = num_heads / num_kv_heads;
+    if (q_dtype != PKV_BF16 || kv_dtype != PKV_BF16 || head_dim != prefill::kD ||
+        (block_size != 16 && block_size != 32) || prefill::kRows % G != 0)
+        return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || max_query_len == 0) return PKV_OK;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens || !query_start)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
+        return PKV_ERR_INVALID_ARG;
+    int* err = error_word();
+    if (!err) return PKV_ERR_CUDA;
+
+    prefill::Params p;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
+    p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.query_start = query_start;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.G = G;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.err = err;
+    const long long rows = (long long)max_query_len * G;
+    const long long tiles = (rows + prefill::kRows - 1) / prefill::kRows;
+    if (tiles > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
+    const dim3 grid((unsigned)tiles, (unsigned)num_kv_heads, (unsigned)num_seqs);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return block_size == 16 ? prefill::launch<16>(p, grid, s) : prefill::launch<32>(p, grid, s);
+}

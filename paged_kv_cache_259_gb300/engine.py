@@ -1,8 +1,8 @@
 """One decode step of paged attention, end to end, over the C ABI.
 
-A ``PagedKVCache`` owns the two device pools (K as ``[NB, Hkv, D/X, bs, X]``
-chunk planes, V as ``[NB, Hkv, D, bs]``; ``k_view``/``v_view`` give the plain
-``[NB, Hkv, bs, D]`` view) and a host ``BlockManager``. A step is:
+A ``PagedKVCache`` owns the two device pools (tiles of 128-byte core matrices,
+see ``pool_shapes``; ``k_view``/``v_view`` give the plain ``[NB, Hkv, bs, D]``
+view) and a host ``BlockManager``. A step is:
 
 1. host: one ``append_slot`` per sequence -> slot numbers and copy-on-write
    pairs ("KV cache paginado...", "Como funciona": copy a shared block before
@@ -21,7 +21,8 @@ import numpy as np
 import torch
 
 from . import (BlockManager, copy_blocks, paged_attention_decode, paged_attention_decode_grouped,
-               paged_attention_workspace_size, pool_shapes, reshape_and_cache)
+               paged_attention_prefill, paged_attention_workspace_size, pool_shapes,
+               pool_views, reshape_and_cache)
 
 
 @dataclass
@@ -64,6 +65,34 @@ class StepPlan:
         return n
 
 
+@dataclass
+class PrefillPlan:
+    """Host-side inputs of one chunked-prefill step."""
+    seq_ids: np.ndarray      # int64 [B]
+    chunks: np.ndarray       # int64 [B] new tokens per sequence
+    slots: np.ndarray        # int64 [T] slot of every chunk token (sequence by sequence)
+    pairs: np.ndarray        # int64 [P, 2]
+    tables: np.ndarray       # int32 [B, max_blocks]
+    lens: np.ndarray         # int32 [B]
+    query_start: np.ndarray  # int32 [B + 1]
+
+    @property
+    def max_query_len(self):
+        return int(self.chunks.max()) if len(self.chunks) else 0
+
+    def host_tensors(self, pin=True):
+        t = {"slots": torch.from_numpy(self.slots), "pairs": torch.from_numpy(self.pairs),
+             "tables": torch.from_numpy(self.tables), "lens": torch.from_numpy(self.lens),
+             "query_start": torch.from_numpy(self.query_start)}
+        if pin:
+            t = {k: v.pin_memory() for k, v in t.items()}
+        return t
+
+    def device_tensors(self, device, non_blocking=False):
+        return {k: v.to(device, non_blocking=non_blocking)
+                for k, v in self.host_tensors(pin=non_blocking).items()}
+
+
 class PagedKVCache:
     def __init__(self, num_blocks, num_heads, num_kv_heads, head_dim, block_size, kv_dtype,
                  free_order, device="cuda"):
@@ -89,12 +118,11 @@ class PagedKVCache:
 
     def k_view(self):
         """K pool as ``[NB, Hkv, bs, D]`` (a copy, for inspection and tests)."""
-        NB, Hkv, bs, D = self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim
-        return self.k_pool.permute(0, 1, 3, 2, 4).reshape(NB, Hkv, bs, D)
+        return pool_views(self.k_pool, self.v_pool)[0]
 
     def v_view(self):
         """V pool as ``[NB, Hkv, bs, D]`` (a copy, for inspection and tests)."""
-        return self.v_pool.transpose(2, 3).contiguous()
+        return pool_views(self.k_pool, self.v_pool)[1]
 
     def replay(self, script):
         """Apply block-manager operations; returns the CoW pairs raised (in order)."""
@@ -133,6 +161,31 @@ class PagedKVCache:
             if len(members):
                 plan.seq_group, plan.group_members, plan.group_prefix = seq_group, members, prefix
         return plan
+
+    def plan_prefill(self, seq_ids, chunks, max_blocks=None):
+        """Host half of a chunked-prefill step: ``chunks[i]`` appends to sequence
+        ``seq_ids[i]`` (slots in token order, CoW pairs), dense tables, lengths and
+        the chunk offsets."""
+        ids = np.asarray(seq_ids, dtype=np.int64)
+        chunks = np.asarray(chunks, dtype=np.int64)
+        slots, pairs = self.bm.append_slots(np.repeat(ids, chunks))
+        if max_blocks is None:
+            max_blocks = max(1, max(-(-self.bm.seq_len(int(s)) // self.block_size) for s in ids))
+        tables, lens = self.bm.build_tables(ids, max_blocks)
+        qs = np.zeros(len(ids) + 1, dtype=np.int32)
+        qs[1:] = np.cumsum(chunks)
+        return PrefillPlan(ids, chunks, slots, pairs, tables, lens, qs)
+
+    def prefill_step(self, q, k_new, v_new, dev_plan, out, scale, max_query_len, stream=None):
+        """Device half of a chunked-prefill step: CoW copies, the chunk's K/V into
+        its slots, then causal attention of every chunk token."""
+        pairs = dev_plan["pairs"]
+        if pairs.shape[0]:
+            copy_blocks(self.k_pool, self.v_pool, pairs, stream=stream)
+        reshape_and_cache(k_new, v_new, self.k_pool, self.v_pool, dev_plan["slots"], stream=stream)
+        return paged_attention_prefill(out, q, self.k_pool, self.v_pool, dev_plan["tables"],
+                                       dev_plan["lens"], dev_plan["query_start"], scale,
+                                       max_query_len, stream)
 
     def workspace(self, batch, max_blocks):
         """Split-KV scratch, room for split group lists included."""

@@ -183,6 +183,77 @@ def long_fp8(bs=16, B=16, L=32768):
                              torch.bfloat16, "e4m3", 1.0 / math.sqrt(128))
 
 
+@dataclass
+class ChunkWorkload(Workload):
+    """A chunked-prefill step: sequence b appends ``chunks[b]`` tokens at once
+    (its chunk) on top of the context the script built, and every chunk token
+    is a query."""
+    chunks: np.ndarray = None
+
+    @property
+    def T(self):
+        return int(np.sum(self.chunks))
+
+    @property
+    def max_query_len(self):
+        return int(np.max(self.chunks)) if len(self.chunks) else 0
+
+    @property
+    def query_start(self):
+        """Offsets of each sequence's chunk rows in q / out (int32 [B + 1])."""
+        return np.concatenate([[0], np.cumsum(self.chunks)]).astype(np.int32)
+
+    def step_inputs(self):
+        """``q [T, Hq, D]``, ``k_new [T, Hkv, D]``, ``v_new [T, Hkv, D]``: the chunk
+        tokens of sequence 0, then of sequence 1, ..."""
+        q = self._randn((self.T, self.Hq, self.D), 3)
+        k = self._randn((self.T, self.Hkv, self.D), 4)
+        v = self._randn((self.T, self.Hkv, self.D), 5)
+        return q, k, v
+
+
+def chunked_prefill(name, seed, context, chunks, Hq, Hkv, D, bs, NB=None):
+    """Sequences 0..B-1 with ``context[b]`` cached tokens, then a chunk of
+    ``chunks[b]`` new tokens each (bf16, N(0, 1) values, scale 1/sqrt(D))."""
+    rng = np.random.default_rng(seed)
+    context = np.asarray(context, dtype=np.int64)
+    chunks = np.asarray(chunks, dtype=np.int64)
+    lens = context + chunks
+    if NB is None:
+        NB = _pool_size(int(sum(-(-int(L) // bs) for L in lens)))
+    free_order = rng.permutation(NB)
+    script = []
+    for b, c in enumerate(context):
+        script.append(("add", b))
+        if c > 0:
+            script.append(("append", b, int(c)))
+    return ChunkWorkload(name=name, B=len(lens), Hq=Hq, Hkv=Hkv, D=D, bs=bs, NB=NB, seed=seed,
+                         scale=1.0 / math.sqrt(D), src_dtype=torch.bfloat16, kv_dtype="bf16",
+                         free_order=free_order, script=script, step_seqs=list(range(len(lens))),
+                         final_lens=lens, chunks=chunks)
+
+
+def prefill_llama13b_bf16(B=16, chunk=512):
+    """LLaMA-13B-shaped chunked prefill: 40 heads MHA, D 128, bs 16; B sequences
+    with a context of U[0, 1536] cached tokens each take a chunk of 512 tokens."""
+    rng = np.random.default_rng(5)
+    ctx = rng.integers(0, 1536, size=B, endpoint=True)
+    return chunked_prefill("prefill_llama13b_bf16", 5, ctx, [chunk] * B, 40, 40, 128, 16)
+
+
+def prefill_gqa_bf16(B=16, chunk=512):
+    """GQA 32 query / 8 KV heads, D 128, bs 16; contexts U[0, 3584], chunks of 512."""
+    rng = np.random.default_rng(6)
+    ctx = rng.integers(0, 3584, size=B, endpoint=True)
+    return chunked_prefill("prefill_gqa_bf16", 6, ctx, [chunk] * B, 32, 8, 128, 16)
+
+
+PREFILL_CONFIGS = {
+    "prefill_llama13b_bf16": prefill_llama13b_bf16,
+    "prefill_gqa_bf16": prefill_gqa_bf16,
+}
+
+
 CONFIGS = {
     "tiny_fp32": tiny_fp32,
     "llama13b_mha_bf16": llama13b_mha_bf16,

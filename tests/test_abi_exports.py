@@ -3,6 +3,11 @@ import ctypes
 import os
 import re
 
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_259_gb300 as pkv
 from _lib import ROOT, library
 
 HEADER = os.path.join(ROOT, "include", "pagedkv.h")
@@ -58,3 +63,32 @@ def test_status_strings_and_host_side_argument_checks():
     assert lib.copy_blocks(None, None, None, 1, 8, 4100, None) == -1                  # bytes % 16
     assert lib.paged_attention_workspace_size(64, 40, 128, 16, 128) == 64 * 40 * 16 * 130 * 4
     assert lib.paged_attention_workspace_size(4, 4, 64, 16, 8) == 0                  # never split
+
+
+@pytest.mark.parametrize("dtype,bs,D", [(torch.bfloat16, 16, 128), (torch.bfloat16, 32, 64),
+                                         (torch.float32, 16, 64), (torch.uint8, 32, 128)])
+def test_pool_layout_helpers_follow_the_header_formula(dtype, bs, D):
+    """pools_from_views / pool_views against the element offsets the header states:
+    K (blk, h, t, d) at (blk*Hkv + h)*bs*D + ((t/8)*(D/X) + d/X)*8X + (t%8)*X + d%X,
+    V (blk, h, t, d) at (blk*Hkv + h)*bs*D + ((t/X)*(D/8) + d/8)*8X + (d%8)*X + t%X."""
+    NB, Hkv = 3, 2
+    X = 16 // torch.empty((), dtype=dtype).element_size()
+    n = NB * Hkv * bs * D
+    ids = torch.arange(n, dtype=torch.int64)
+    k = (ids % 251).to(dtype).reshape(NB, Hkv, bs, D) if dtype == torch.uint8 else \
+        ids.to(torch.float32).to(dtype).reshape(NB, Hkv, bs, D)
+    v = (k.to(torch.float32) + 1).to(dtype) if dtype != torch.uint8 else (k + 1)
+    kp, vp = pkv.pools_from_views(k, v)
+    ks, vs = pkv.pool_shapes(NB, Hkv, bs, D, dtype)
+    assert tuple(kp.shape) == ks and tuple(vp.shape) == vs
+    kf, vf = kp.reshape(-1), vp.reshape(-1)
+    rng = np.random.default_rng(0)
+    for _ in range(300):
+        blk, h, t, d = (int(rng.integers(NB)), int(rng.integers(Hkv)), int(rng.integers(bs)),
+                        int(rng.integers(D)))
+        base = (blk * Hkv + h) * bs * D
+        ko = base + ((t // 8) * (D // X) + d // X) * 8 * X + (t % 8) * X + d % X
+        vo = base + ((t // X) * (D // 8) + d // 8) * 8 * X + (d % 8) * X + t % X
+        assert kf[ko] == k[blk, h, t, d] and vf[vo] == v[blk, h, t, d]
+    k2, v2 = pkv.pool_views(kp, vp)
+    assert torch.equal(k2, k) and torch.equal(v2, v)

@@ -132,16 +132,7 @@ def test_repeated_step_is_idempotent():
 
 def to_layout(kc, vc):
     """Canonical ``[NB, Hkv, bs, D]`` K/V -> the library's pool layout (plain copies)."""
-    NB, Hkv, bs, D = kc.shape
-    x = 16 // kc.element_size()
-    kl = kc.reshape(NB, Hkv, bs, D // x, x).permute(0, 1, 3, 2, 4).contiguous()
-    vl = vc.transpose(2, 3).contiguous()
-    return kl, vl
-
-
-def from_layout_k(kl):
-    NB, Hkv, DX, bs, x = kl.shape
-    return kl.permute(0, 1, 3, 2, 4).reshape(NB, Hkv, bs, DX * x)
+    return pkv.pools_from_views(kc, vc)
 
 
 def _decode_args(B, Hq, Hkv, D, bs, NB, MB, dtype=torch.bfloat16, seed=0):
@@ -190,9 +181,9 @@ def test_reshape_and_cache_bad_and_padding_slots():
     slots = torch.tensor([-1, 64, 5], dtype=torch.int64, device="cuda")   # pad, outside, ok
     pkv.reshape_and_cache(k, k, kp, vp, slots)
     assert pkv.get_device_error() == -4
-    kv = from_layout_k(kp)
+    kv, vv = pkv.pool_views(kp, vp)
     assert torch.count_nonzero(kp) == 2 * 64 and torch.all(kv[0, :, 5] == 1)
-    assert torch.count_nonzero(vp) == 2 * 64 and torch.all(vp.transpose(2, 3)[0, :, 5] == 1)
+    assert torch.count_nonzero(vp) == 2 * 64 and torch.all(vv[0, :, 5] == 1)
 
 
 def test_copy_blocks_bad_pair_sets_error_word():

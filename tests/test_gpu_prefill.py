@@ -1,0 +1,213 @@
+"""GPU parity of chunked-prefill attention (tcgen05 kernel, through the C ABI)
+against the CPU oracle.
+
+A step appends each sequence's chunk (slots and copy-on-write pairs from the
+block manager), writes the chunk's K/V with reshape_and_cache, and runs
+paged_attention_prefill. Indexing and cache writes are compared bit-exactly;
+attention outputs elementwise within |gpu - oracle| <= 2e-2 + 2e-2 |oracle|
+(bf16 cache, f32 accumulation). Small ragged cases compare every row; the
+full-size workloads compare sampled (token, head) rows in the benchmark's
+launch configuration.
+"""
+import numpy as np
+import pytest
+import torch
+
+import pkv_workloads as wl
+from _lib import library, pkv
+from _parity import assert_close, stored_bits
+from paged_kv_cache_259_gb300.engine import PagedKVCache
+
+from oracle import attention as oatt
+from oracle import cache_ops as oops
+from oracle.block_manager import BlockManager as OracleBM
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_and_library():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test selected but no CUDA device is visible")
+    library()
+    torch.cuda.set_device(0)
+
+
+class Case:
+    def __init__(self, w):
+        self.w = w
+        self.k_src, self.v_src = w.past_pools()
+        self.q, self.k_new, self.v_new = w.step_inputs()
+
+
+def run_gpu(c, max_query_len=None, bad=None, device="cuda"):
+    w = c.w
+    cache = PagedKVCache(w.NB, w.Hq, w.Hkv, w.D, w.bs, torch.bfloat16, w.free_order, device)
+    cache.load(c.k_src, c.v_src)
+    setup_pairs = cache.replay(w.script)
+    cache.apply_copies(setup_pairs)
+    plan = cache.plan_prefill(w.step_seqs, w.chunks, max_blocks=w.max_blocks_per_seq)
+    dev = plan.device_tensors(device)
+    if bad is not None:
+        bad(dev)
+    out = torch.full((w.T, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device=device)
+    mql = plan.max_query_len if max_query_len is None else max_query_len
+    cache.prefill_step(c.q.to(device), c.k_new.to(device), c.v_new.to(device), dev, out, w.scale,
+                       mql)
+    err = pkv.get_device_error()
+    return {"out": out.float().cpu(), "cache": cache, "plan": plan, "setup_pairs": setup_pairs,
+            "err": err}
+
+
+def run_oracle(c, units=None):
+    w = c.w
+    bm = OracleBM(w.NB, w.bs, w.free_order)
+    setup_pairs = []
+    for op in w.script:
+        if op[0] == "add":
+            bm.add_seq(op[1])
+        elif op[0] == "fork":
+            bm.fork(op[1], op[2])
+        else:
+            for _ in range(op[2]):
+                cow = bm.append_slot(op[1])[1]
+                if cow is not None:
+                    setup_pairs.append(cow)
+    kp, vp = c.k_src.clone(), c.v_src.clone()
+    oops.copy_blocks(kp, vp, setup_pairs)
+    slots, pairs = [], []
+    for s, n in zip(w.step_seqs, w.chunks):
+        for _ in range(int(n)):
+            slot, cow = bm.append_slot(s)
+            slots.append(slot)
+            if cow is not None:
+                pairs.append(cow)
+    oops.copy_blocks(kp, vp, pairs)
+    oops.reshape_and_cache(c.k_new, c.v_new, kp, vp, torch.tensor(slots, dtype=torch.int64), w.bs)
+    MB = w.max_blocks_per_seq
+    tables = np.full((w.B, MB), -1, dtype=np.int64)
+    for i, s in enumerate(w.step_seqs):
+        t = bm.block_table(s)
+        tables[i, :len(t)] = t
+    lens = np.array([bm.seq_len(s) for s in w.step_seqs])
+    qs = [0]
+    for n in w.chunks:
+        qs.append(qs[-1] + int(n))
+    out = oatt.paged_prefill(c.q, kp, vp, tables, lens, np.array(qs), w.scale, w.bs,
+                             units=units)
+    return {"out": out, "slots": slots, "pairs": pairs, "setup_pairs": setup_pairs,
+            "tables": tables, "lens": lens, "k_pool": kp, "v_pool": vp}
+
+
+def check_indexing_and_writes(g, o):
+    plan = g["plan"]
+    assert list(plan.slots) == o["slots"]
+    assert [tuple(p) for p in plan.pairs] == o["pairs"]
+    assert g["setup_pairs"] == o["setup_pairs"]
+    assert np.array_equal(plan.tables.astype(np.int64), o["tables"])
+    assert np.array_equal(plan.lens, o["lens"])
+    cache = g["cache"]
+    assert torch.equal(stored_bits(cache.k_view().cpu()), stored_bits(o["k_pool"]))
+    assert torch.equal(stored_bits(cache.v_view().cpu()), stored_bits(o["v_pool"]))
+
+
+CTX = [0, 5, 16, 200, 0, 1000, 37, 3]
+CHUNK = [1, 7, 128, 129, 300, 17, 64, 0]
+
+SMALL = [
+    ("mha_bs16", 8, 8, 16),
+    ("gqa4_bs16", 16, 4, 16),
+    ("gqa8_bs32", 16, 2, 32),
+    ("gqa2_bs32", 8, 4, 32),
+    ("gqa16_bs16", 16, 1, 16),
+]
+
+
+@pytest.mark.parametrize("name,Hq,Hkv,bs", SMALL, ids=[s[0] for s in SMALL])
+def test_prefill_small_ragged_every_row(name, Hq, Hkv, bs):
+    w = wl.chunked_prefill(f"prefill_{name}", 40 + Hq + bs, CTX, CHUNK, Hq, Hkv, 128, bs)
+    c = Case(w)
+    g = run_gpu(c)
+    o = run_oracle(c)
+    assert g["err"] == 0
+    check_indexing_and_writes(g, o)
+    assert_close(g["out"].numpy(), o["out"], "bf16", name)
+
+
+def test_prefill_after_fork_copies_the_shared_partial_block():
+    """Two samples share a 40-token prompt (last block partial); the second one's
+    chunk first copies that block (copy-on-write), then attends over it."""
+    w = wl.chunked_prefill("prefill_fork", 77, [0, 0], [1, 1], 8, 2, 128, 16, NB=40)
+    w.script = [("add", 0), ("append", 0, 40), ("fork", 0, 1)]
+    w.chunks = np.array([20, 150])
+    w.final_lens = np.array([60, 190])
+    c = Case(w)
+    g = run_gpu(c)
+    o = run_oracle(c)
+    assert g["err"] == 0
+    assert len(o["pairs"]) == 1 and not o["setup_pairs"]
+    check_indexing_and_writes(g, o)
+    assert_close(g["out"].numpy(), o["out"], "bf16", "fork")
+
+
+def test_prefill_larger_max_query_len_changes_nothing():
+    w = wl.chunked_prefill("prefill_mql", 9, [30, 0], [33, 100], 8, 8, 128, 16)
+    c = Case(w)
+    a = run_gpu(c)
+    b = run_gpu(c, max_query_len=1000)
+    assert a["err"] == 0 and b["err"] == 0
+    assert torch.equal(a["out"], b["out"])
+    assert_close(a["out"].numpy(), run_oracle(c)["out"], "bf16", "mql")
+
+
+def test_prefill_bad_block_id_is_flagged_not_followed():
+    w = wl.chunked_prefill("prefill_bad", 13, [100, 20], [40, 10], 8, 8, 128, 16)
+    c = Case(w)
+
+    def corrupt(dev):
+        dev["tables"][0, 2] = w.NB + 1000
+    g = run_gpu(c, bad=corrupt)
+    assert g["err"] == -4
+    # the other sequence is unaffected
+    o = run_oracle(c)
+    assert_close(g["out"][40:].numpy(), o["out"][40:], "bf16", "unaffected sequence")
+
+
+def test_prefill_chunk_longer_than_sequence_is_flagged():
+    w = wl.chunked_prefill("prefill_bad_len", 14, [10, 20], [5, 10], 8, 8, 128, 16)
+    c = Case(w)
+
+    def corrupt(dev):
+        dev["lens"][0] = 3          # shorter than its 5-token chunk
+    g = run_gpu(c, bad=corrupt)
+    assert g["err"] == -4
+    assert torch.isnan(g["out"][:5]).all()              # its rows are not written
+    o = run_oracle(c)
+    assert_close(g["out"][5:].numpy(), o["out"][5:], "bf16", "unaffected sequence")
+
+
+def sample_rows(w, n, seed=0):
+    rng = np.random.default_rng(seed)
+    qs = w.query_start
+    units = set()
+    for b in (0, w.B - 1):
+        units.add((int(qs[b]), 0))                           # first chunk token
+        units.add((int(qs[b + 1]) - 1, w.Hq - 1))            # last chunk token
+    while len(units) < n:
+        units.add((int(rng.integers(w.T)), int(rng.integers(w.Hq))))
+    return sorted(units)
+
+
+@pytest.mark.parametrize("config", sorted(wl.PREFILL_CONFIGS))
+def test_prefill_full_size_sampled(config):
+    w = wl.PREFILL_CONFIGS[config]()
+    c = Case(w)
+    g = run_gpu(c)
+    assert g["err"] == 0
+    assert torch.isfinite(g["out"]).all()
+    units = sample_rows(w, 48)
+    o = run_oracle(c, units=units)
+    got = np.stack([g["out"][t, h].numpy() for t, h in units])
+    ref = np.stack([o["out"][u] for u in units])
+    assert_close(got, ref, "bf16", config)
+    assert list(g["plan"].slots) == o["slots"]
