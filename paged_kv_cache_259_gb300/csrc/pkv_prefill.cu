@@ -17,19 +17,25 @@
 // * warps 0-3 (softmax): thread r owns row r = TMEM lane r. Puts its q row in
 //   TMEM, then per KV tile reads its 128 scores, applies the causal mask, keeps
 //   the running max / sum (exp2 domain, scale * log2 e folded in), writes P
-//   (bf16) back into TMEM over the scores, and finally normalises O;
-// * warp 4 (MMA): one thread issues S = Q K^T (A = Q from TMEM, B = the K tile
-//   in shared memory, M = N = 128) and O += P V (A = P from TMEM, B = the V
-//   tile, K = 16 keys per instruction), and owns the TMEM allocation;
-// * warp 5 (loader): one thread copies each KV tile of 128 keys block by block
-//   (through the block table) with 1-D bulk copies: the cache stores every
+//   (bf16) into its own TMEM columns, and finally normalises O;
+// * warp 4 (S issuer): one thread issues S = Q K^T (A = Q from TMEM, B = the K
+//   tile in shared memory, M = N = 128) as soon as an S buffer is free, and owns
+//   the TMEM allocation; warp 7 (P.V issuer): one thread issues O += P V (A = P
+//   from TMEM, B = the V tile, K = 16 keys per instruction) as soon as P is
+//   ready. The two streams touch disjoint operands (Q, K -> S; P, V -> O), so
+//   neither waits behind the other's issue;
+// * warps 5 and 6 (loaders, K and V): copy each tile of 128 keys block by block
+//   (through the block table) with 1-D bulk copies, lane i copying block i of
+//   the tile; K and V run through separate rings, so K of a tile is refilled as
+//   soon as its scores are computed and V once P.V has used it. The cache stores every
 //   (block, head) tile as 128-byte core matrices, K [bs/8][D/8][8][8] and V
 //   [bs/8][D/8][8][8] (8 dims x 8 tokens), which is the canonical no-swizzle
 //   K-major operand layout, so a tile lands ready for the tensor cores (S with
 //   N = 128 keys over 8 blocks, P.V with K = 16 keys per instruction). Keys
 //   past the sequence in its last, partly written block get zero V values.
-// S is double-buffered in TMEM so the scores of tile j+1 are computed while the
-// softmax works on tile j; K/V tiles run through a 3-stage shared-memory ring.
+// S is double-buffered in TMEM and a buffer is handed back as soon as the
+// softmax has read it, so the scores of tile j+2 are computed while the softmax
+// works on tile j+1, ahead of P.V of tile j; K/V tiles run through 3-stage rings.
 // The running max is only moved (and O rescaled) when a tile's max exceeds it by
 // more than 2^8, so O is rarely touched; the result is the same softmax.
 #include <cmath>
@@ -49,15 +55,18 @@ constexpr int kStages = 3;
 constexpr int kTileBytes = kKeys * kD * 2;         // one K (or V) tile, bf16
 constexpr int kStageBytes = 2 * kTileBytes;
 constexpr int kSmem = kStages * kStageBytes;       // 192 KB: one CTA per SM
-constexpr int kMmaWarp = 4;
-constexpr int kLoadWarp = 5;
-constexpr int kThreads = 6 * 32;
+constexpr int kMmaWarp = 4;                       // S issuer, TMEM owner
+constexpr int kKLoadWarp = 5, kVLoadWarp = 6;
+constexpr int kPvWarp = 7;                        // P.V issuer
+constexpr int kThreads = 8 * 32;
 constexpr int kGroupBytes = (kD / 8) * 128;         // K: 8 tokens x 128 dims
 constexpr int kChunkBytes = (kD / 8) * 128;         // V: 128 dims x 8 tokens
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 128, kColQ = 384;   // O | S0 | S1 | Q
+constexpr uint32_t kColO = 0, kColS = 128, kColQ = 384, kColP = 448;   // O | S0 | S1 | Q | P
 constexpr float kRescaleLog2 = 8.0f;
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kRows, 128);      // S and P.V: M = N = 128
+constexpr uint32_t kKDescHi = tc::desc_hi(kGroupBytes);           // K: SBO = 8-token group
+constexpr uint32_t kVDescHi = tc::desc_hi(128);                   // V: SBO = 8-dim group
 
 static_assert(kSmem <= 227 * 1024, "shared memory ring too large");
 
@@ -94,9 +103,11 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // Barriers (in this order in shared memory).
-enum : int { kBarFull = 0, kBarEmpty = kStages, kBarS = 2 * kStages, kBarP = kBarS + 2,
-             kBarO = kBarP + 2, kBarQ = kBarO + 1, kBarDrain = kBarQ + 1, kBarLand = kBarDrain + 1,
-             kNumBars = kBarLand + 1 };
+enum : int { kBarKFull = 0, kBarKEmpty = kStages, kBarVFull = 2 * kStages,
+             kBarVEmpty = 3 * kStages, kBarS = 4 * kStages, kBarSFree = kBarS + 2,
+             kBarP = kBarSFree + 2, kBarO = kBarP + 1,
+             kBarQ = kBarO + 1, kBarDrain = kBarQ + 1, kBarLand = kBarDrain + 1,
+             kBarDrainPv = kBarLand + 1, kNumBars = kBarDrainPv + 1 };
 
 template <int BS>
 __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params p) {
@@ -132,17 +143,21 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(kBarFull + s), 1);
-            mbar_init(bar(kBarEmpty + s), 1);
+            mbar_init(bar(kBarKFull + s), 1);
+            mbar_init(bar(kBarKEmpty + s), 1);
+            mbar_init(bar(kBarVFull + s), 1);
+            mbar_init(bar(kBarVEmpty + s), 1);
         }
         mbar_init(bar(kBarLand), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(kBarS + i), 1);
-            mbar_init(bar(kBarP + i), 128);
+            mbar_init(bar(kBarSFree + i), 128);
         }
+        mbar_init(bar(kBarP), 128);
         mbar_init(bar(kBarO), 1);
         mbar_init(bar(kBarQ), 128);
         mbar_init(bar(kBarDrain), 1);
+        mbar_init(bar(kBarDrainPv), 1);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -154,36 +169,54 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
     tc::fence_after_sync();
     const uint32_t tmem = tmem_slot;
 
-    if (warp == kLoadWarp) {
-        // ------------------------------------------------------------ loader
+    if (warp == kKLoadWarp || warp == kVLoadWarp) {
+        // ------------------------------------------------------------ loaders
+        const bool is_v = warp == kVLoadWarp;
+        const int bar_full = is_v ? kBarVFull : kBarKFull;
+        const int bar_empty = is_v ? kBarVEmpty : kBarKEmpty;
+        const __nv_bfloat16* pool = is_v ? p.v_pool : p.k_pool;
         const int32_t* bt = p.block_tables + (size_t)b * p.max_blocks;
         const int tail = L % BS;                           // tokens in a partly written last block
+        // block ids in a window of 32 blocks, one per lane, with the next window
+        // fetched a window ahead, so table reads never wait on the copies
+        auto fetch_id = [&](int blk) {
+            if (blk > blk_last) return 0;
+            const int id = bt[blk];
+            if (id < 0 || id >= p.num_blocks) {
+                flag_error(p.err, kErrOutOfRange);
+                return 0;                                  // in bounds; the sequence is in error
+            }
+            return id;
+        };
+        int win = 0;
+        int win_ids = fetch_id(lane), next_ids = fetch_id(32 + lane);
         for (int j = 0; j < n_tiles; ++j) {
+            if ((j * kBlocksPerTile) / 32 != win) {
+                ++win;
+                win_ids = next_ids;
+                next_ids = fetch_id((win + 1) * 32 + lane);
+            }
+            const int my_id = __shfl_sync(0xffffffffu, win_ids, (j * kBlocksPerTile) % 32 +
+                                                                    (lane % kBlocksPerTile));
             const int s = j % kStages;
             if (j >= kStages &&
-                !mbar_wait_bounded(bar(kBarEmpty + s), ((j / kStages) - 1) & 1, p.err)) {
+                !mbar_wait_bounded(bar(bar_empty + s), ((j / kStages) - 1) & 1, p.err)) {
                 flag_error(p.err, kErrTimeout);
                 break;
             }
-            const uint32_t ks = sbase + (uint32_t)(s * kStageBytes);
-            const uint32_t vs = ks + kTileBytes;
+            const uint32_t dst = sbase + (uint32_t)(s * kStageBytes + (is_v ? kTileBytes : 0));
             const int blk0 = j * kBlocksPerTile;
             const int n_load = min(kBlocksPerTile, blk_last - blk0 + 1);
-            // the block holding the sequence's last token is zero-filled past it
-            const bool fix = tail != 0 && blk_last == (L - 1) / BS && blk_last < blk0 + kBlocksPerTile;
-            const uint32_t land = fix ? bar(kBarLand) : bar(kBarFull + s);
-            if (lane == 0) {
-                mbar_arrive_expect_tx(land, (uint32_t)(2 * n_load * kBlockBytes));
-                for (int jb = 0; jb < n_load; ++jb) {
-                    int id = bt[blk0 + jb];
-                    if (id < 0 || id >= p.num_blocks) {
-                        flag_error(p.err, kErrOutOfRange);
-                        id = 0;                            // in bounds; the sequence is in error
-                    }
-                    const size_t off = ((size_t)id * p.num_kv_heads + hk) * (size_t)(BS * kD);
-                    bulk_load(ks + (uint32_t)(jb * kBlockBytes), p.k_pool + off, kBlockBytes, land);
-                    bulk_load(vs + (uint32_t)(jb * kBlockBytes), p.v_pool + off, kBlockBytes, land);
-                }
+            // V of the block holding the sequence's last token is zero-filled
+            // past it (K there only meets masked scores)
+            const bool fix = is_v && tail != 0 && blk_last == (L - 1) / BS &&
+                             blk_last < blk0 + kBlocksPerTile;
+            const uint32_t land = fix ? bar(kBarLand) : bar(bar_full + s);
+            if (lane == 0) mbar_arrive_expect_tx(land, (uint32_t)(n_load * kBlockBytes));
+            __syncwarp();
+            if (lane < n_load) {                           // lane jb copies block jb of the tile
+                const size_t off = ((size_t)my_id * p.num_kv_heads + hk) * (size_t)(BS * kD);
+                bulk_load(dst + (uint32_t)(lane * kBlockBytes), pool + off, kBlockBytes, land);
             }
             if (fix) {
                 if (!mbar_wait_bounded(bar(kBarLand), 0, p.err)) {
@@ -191,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
                     break;
                 }
                 // V of the last block: [BS/8 chunks][128 dims] rows of 8 tokens
-                const uint32_t vb = vs + (uint32_t)((blk_last - blk0) * kBlockBytes);
+                const uint32_t vb = dst + (uint32_t)((blk_last - blk0) * kBlockBytes);
                 for (int row = lane; row < (BS / 8) * kD; row += 32) {
                     const int valid = tail - (row / kD) * 8;   // tokens of this row's chunk kept
                     if (valid >= 8) continue;
@@ -207,53 +240,69 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
                 }
                 fence_proxy_async_smem();                  // visible to the tensor cores
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarFull + s));
+                if (lane == 0) mbar_arrive(bar(bar_full + s));
             }
         }
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ S issuer
         if (lane == 0) {
             bool ok = mbar_wait_bounded(bar(kBarQ), 0, p.err);
             tc::fence_after_sync();
             auto issue_s = [&](int j) {
                 const int s = j % kStages;
-                ok = ok && mbar_wait_bounded(bar(kBarFull + s), (j / kStages) & 1, p.err);
+                ok = ok && mbar_wait_bounded(bar(kBarKFull + s), (j / kStages) & 1, p.err);
                 if (!ok) return;
                 tc::fence_after_sync();
-                const uint32_t ks = sbase + (uint32_t)(s * kStageBytes);
                 const uint32_t d = tmem + kColS + (uint32_t)(j & 1) * 128;
                 // B = 128 keys: 8-token core-matrix groups 2 KB apart (SBO), the
-                // two 8-dim chunks of a 16-dim step 128 bytes apart (LBO)
+                // two 8-dim chunks of a 16-dim step 128 bytes apart (LBO); each
+                // 16-dim step starts 256 bytes on
+                const uint32_t lo = tc::desc_lo(sbase + (uint32_t)(s * kStageBytes), 128);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
-                    tc::mma_ts(d, tmem + kColQ + kk * 8,
-                               tc::smem_desc(ks + (uint32_t)(kk * 256), 128, kGroupBytes), kIdesc,
-                               kk > 0);
+                    tc::mma_ts2(d, tmem + kColQ + kk * 8, lo + kk * (256 / 16), kKDescHi, kIdesc,
+                                kk > 0);
                 tc::commit(bar(kBarS + (j & 1)));
             };
-            issue_s(0);
             for (int j = 0; j < n_tiles && ok; ++j) {
-                if (j + 1 < n_tiles) issue_s(j + 1);
-                ok = ok && mbar_wait_bounded(bar(kBarP + (j & 1)), (j >> 1) & 1, p.err);
-                if (!ok) break;
-                tc::fence_after_sync();
-                const uint32_t vs = sbase + (uint32_t)((j % kStages) * kStageBytes + kTileBytes);
-                const uint32_t pa = tmem + kColS + (uint32_t)(j & 1) * 128;
-                // 16-key steps that hold a key some query sees (P is 0 past them)
-                const int n16 = min(kKeys / 16, (p_max - j * kKeys) / 16 + 1);
-                // B = V of 16 keys: two 8-token chunks 2 KB apart (LBO), 8-dim
-                // core-matrix rows 128 bytes apart (SBO)
-                for (int jj = 0; jj < n16; ++jj)
-                    tc::mma_ts(tmem + kColO, pa + jj * 8,
-                               tc::smem_desc(vs + (uint32_t)(jj * 2 * kChunkBytes), kChunkBytes, 128),
-                               kIdesc, (j > 0 || jj > 0));
-                tc::commit(bar(kBarEmpty + j % kStages));
-                tc::commit(bar(kBarO));
+                if (j >= 2) {                              // S buffer of tile j-2 read: refill it
+                    ok = ok && mbar_wait_bounded(bar(kBarSFree + (j & 1)), ((j - 2) >> 1) & 1, p.err);
+                    tc::fence_after_sync();
+                }
+                issue_s(j);
             }
             if (!ok) flag_error(p.err, kErrTimeout);
             // every MMA issued here is complete before tensor memory is released
             tc::commit(bar(kBarDrain));
             mbar_wait_bounded(bar(kBarDrain), 0, nullptr);   // a real wait even after a timeout
+        }
+        __syncwarp();
+    } else if (warp == kPvWarp) {
+        // ------------------------------------------------------------ P.V issuer
+        if (lane == 0) {
+            bool ok = true;
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                ok = ok && mbar_wait_bounded(bar(kBarP), j & 1, p.err);
+                ok = ok && mbar_wait_bounded(bar(kBarVFull + j % kStages), (j / kStages) & 1, p.err);
+                if (!ok) break;
+                tc::fence_after_sync();
+                const uint32_t lo = tc::desc_lo(
+                    sbase + (uint32_t)((j % kStages) * kStageBytes + kTileBytes), kChunkBytes);
+                // 16-key steps that hold a key some query sees (P is 0 past them)
+                const int n16 = min(kKeys / 16, (p_max - j * kKeys) / 16 + 1);
+                // B = V of 16 keys: two 8-token chunks 2 KB apart (LBO), 8-dim
+                // core-matrix rows 128 bytes apart (SBO); each step 4 KB on
+#pragma unroll
+                for (int jj = 0; jj < kKeys / 16; ++jj)
+                    if (jj < n16)
+                        tc::mma_ts2(tmem + kColO, tmem + kColP + jj * 8,
+                                    lo + jj * (2 * kChunkBytes / 16), kVDescHi, kIdesc,
+                                    (j > 0 || jj > 0));
+                tc::commit(bar(kBarO));
+            }
+            if (!ok) flag_error(p.err, kErrTimeout);
+            tc::commit(bar(kBarDrainPv));
+            mbar_wait_bounded(bar(kBarDrainPv), 0, nullptr);
         }
         __syncwarp();
     } else {
@@ -293,11 +342,14 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
             ok = ok && mbar_wait_bounded(bar(kBarS + (j & 1)), (j >> 1) & 1, p.err);
             ok = __all_sync(0xffffffffu, ok);              // the warp's tcgen05 ops stay converged
             if (!ok) break;
+            if (tid == 0) mbar_arrive(bar(kBarKEmpty + j % kStages));   // S done: K tile free
             tc::fence_after_sync();
             uint32_t sv[4][32];
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) tc::ld32(row + sb + cb * 32, sv[cb]);
             tc::wait_ld();
+            tc::fence_before_sync();
+            mbar_arrive(bar(kBarSFree + (j & 1)));         // the MMA warp may refill this S
             float s[kKeys];
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb)
@@ -323,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
                 // move the running max: O must hold P.V of every earlier tile first
                 ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarO), (j - 1) & 1, p.err));
                 o_seen = true;
+                if (tid == 0) mbar_arrive(bar(kBarVEmpty + (j - 1) % kStages));   // V tile free
                 tc::fence_after_sync();
                 const float m_new = fmaxf(m_run, mt);
                 const float alpha = ex2(m_run - m_new);
@@ -340,26 +393,32 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
                 m_run = m_new;
             }
             float l4[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[4][16];
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
-                uint32_t pk[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     const float p0 = ex2(fmaf(s[cb * 32 + 2 * c], sc, -m_run));
                     const float p1 = ex2(fmaf(s[cb * 32 + 2 * c + 1], sc, -m_run));
                     l4[c & 3] += p0 + p1;
                     const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                    pk[c] = *reinterpret_cast<const uint32_t*>(&h2);
+                    pk[cb][c] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
-                tc::st16(row + sb + cb * 16, pk);
             }
             l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
-            tc::wait_st();
-            // consume this barrier's phase for tile j-1 so its parity stays unambiguous
-            if (j >= 1 && !o_seen) ok = ok && mbar_wait_bounded(bar(kBarO), (j - 1) & 1, p.err);
+            // P.V of tile j-1 must be done with the P columns (and this consumes
+            // the O barrier's phase for tile j-1, keeping its parity unambiguous)
+            if (j >= 1 && !o_seen) {
+                ok = ok && mbar_wait_bounded(bar(kBarO), (j - 1) & 1, p.err);
+                if (tid == 0) mbar_arrive(bar(kBarVEmpty + (j - 1) % kStages));
+            }
             ok = __all_sync(0xffffffffu, ok);
+            tc::fence_after_sync();
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) tc::st16(row + kColP + cb * 16, pk[cb]);
+            tc::wait_st();
             tc::fence_before_sync();
-            mbar_arrive(bar(kBarP + (j & 1)));
+            mbar_arrive(bar(kBarP));
         }
         if (ok) ok = mbar_wait_bounded(bar(kBarO), (n_tiles - 1) & 1, p.err);
         ok = __all_sync(0xffffffffu, ok);
