@@ -102,6 +102,33 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Two-wide float32 arithmetic (one instruction for a pair of values) and a
+// three-input max: the softmax is bound by instruction issue, one warp per
+// scheduler, so each element should cost as few instructions as possible.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Barriers (in this order in shared memory).
 enum : int { kBarKFull = 0, kBarKEmpty = kStages, kBarVFull = 2 * kStages,
              kBarVEmpty = 3 * kStages, kBarS = 4 * kStages, kBarSFree = kBarS + 2,
@@ -362,11 +389,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
             }
             float m8[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) m8[c] = s[c];
+            for (int c = 0; c < 8; ++c) m8[c] = fmaxf(s[2 * c], s[2 * c + 1]);
 #pragma unroll
-            for (int c = 8; c < kKeys; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            for (int c = 8; c < kKeys / 2; ++c) m8[c & 7] = max3(m8[c & 7], s[2 * c], s[2 * c + 1]);
+            const float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]),
+                                  fmaxf(m8[6], m8[7]));
             const float mt = mx * sc;
             bool o_seen = false;
             if (j == 0) {
@@ -392,20 +419,29 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
                 l_run *= alpha;
                 m_run = m_new;
             }
-            float l4[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t sc2 = f2(sc, sc), nm2 = f2(-m_run, -m_run);
+            uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};       // pairs of partial row sums
             uint32_t pk[4][16];
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                    const float p0 = ex2(fmaf(s[cb * 32 + 2 * c], sc, -m_run));
-                    const float p1 = ex2(fmaf(s[cb * 32 + 2 * c + 1], sc, -m_run));
-                    l4[c & 3] += p0 + p1;
+                    float x0, x1;
+                    f2_split(fma2(f2(s[cb * 32 + 2 * c], s[cb * 32 + 2 * c + 1]), sc2, nm2), x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    l2[c & 3] = add2(l2[c & 3], f2(p0, p1));
                     const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
                     pk[cb][c] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
             }
-            l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+            {
+                float a0, a1, b0, b1, c0, c1, d0, d1;
+                f2_split(l2[0], a0, a1);
+                f2_split(l2[1], b0, b1);
+                f2_split(l2[2], c0, c1);
+                f2_split(l2[3], d0, d1);
+                l_run += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
+            }
             // P.V of tile j-1 must be done with the P columns (and this consumes
             // the O barrier's phase for tile j-1, keeping its parity unambiguous)
             if (j >= 1 && !o_seen) {
