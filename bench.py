@@ -70,6 +70,16 @@ def measured_traffic(config):
     return None if e is None else e.get("dram_bytes_per_decode")
 
 
+def load_tensor_peak():
+    """Dense bf16 tensor peak in TFLOP/s: the measured burst figure (a kernel
+    timed alone), else the recipe's fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -176,6 +186,18 @@ def _oracle_loop(p, inp, tables, lens, run_s, seed):
     rng = np.random.default_rng(seed)
     fin, nbytes = [], []
     t0 = time.perf_counter()
+    if p.get("mode") == "prefill":
+        # units are (chunk token, head); the amount is the token's attention FLOPs
+        qs = np.asarray(p["query_start"])
+        seq_of = np.searchsorted(qs, np.arange(int(qs[-1])), side="right") - 1
+        while time.perf_counter() - t0 < run_s:
+            t, h = int(rng.integers(int(qs[-1]))), int(rng.integers(p["Hq"]))
+            oatt.paged_prefill(q, kp, vp, tables, lens, qs, p["scale"], p["bs"], units=[(t, h)])
+            fin.append(time.perf_counter() - t0)
+            b = int(seq_of[t])
+            pos = int(lens[b]) - int(qs[b + 1] - qs[b]) + (t - int(qs[b]))
+            nbytes.append(4.0 * p["D"] * (pos + 1))
+        return np.array(fin), np.array(nbytes)
     while time.perf_counter() - t0 < run_s:
         b, h = int(rng.integers(p["B"])), int(rng.integers(p["Hq"]))
         oatt.paged_decode(q, kp, vp, tables, lens, p["scale"], p["bs"], ks, vs, units=[(b, h)],
@@ -204,7 +226,7 @@ def _oracle_worker(idx, spec, barrier, results):
         results.put((-1, repr(e)))
 
 
-def oracle_timing(w, inp, tables, lens, per_tok, slice_s, slices, cores=None):
+def oracle_timing(w, inp, tables, lens, per_tok, slice_s, slices, cores=None, extra=None):
     """Times the unmodified oracle on the host cores: one spawned single-threaded
     process per core, all started together and run for ``slices * slice_s``
     seconds over random (sequence, head) units of the workload. Each unit counts
@@ -215,7 +237,7 @@ def oracle_timing(w, inp, tables, lens, per_tok, slice_s, slices, cores=None):
     import shutil
     import tempfile
     p = {"kv": w.kv_dtype, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "bs": w.bs, "scale": w.scale,
-         "per_tok": per_tok}
+         "per_tok": per_tok, "D": w.D, **(extra or {})}
     run_s = slice_s * slices
     cores = cores or len(os.sched_getaffinity(0))
     note, runs = "", None
@@ -426,6 +448,247 @@ def oracle_inputs_for_step(w, q, k_src, v_src, plan):
     return kp, vp, tables, lens
 
 
+# ---------------------------------------------------------------- chunked prefill
+PREFILL_METRIC = ("paged chunked-prefill attention: achieved TFLOP/s (% of bf16 tensor peak) "
+                  "and chunk tokens/s")
+
+
+def prefill_flops(w):
+    """Algorithmic FLOPs of the step's attention: chunk token i of sequence b sees
+    p + 1 keys (p = L_b - C_b + i), and per (token, head, key) Q.K and P.V are
+    2 * D multiply-adds each."""
+    L = np.asarray(w.final_lens, dtype=np.float64)
+    C = np.asarray(w.chunks, dtype=np.float64)
+    keys = C * (L - C) + C * (C + 1) / 2
+    return float(keys.sum()) * w.Hq * 4 * w.D
+
+
+def prefill_oracle_inputs(w, k_src, v_src, k_new, v_new):
+    """CPU pools after the step's writes (the oracle's own block manager and
+    cache ops; no GPU data), block tables and lengths."""
+    from oracle import cache_ops as oops
+    from oracle.block_manager import BlockManager as OBM
+    bm = OBM(w.NB, w.bs, w.free_order)
+    pairs = []
+    for op in w.script:
+        if op[0] == "add":
+            bm.add_seq(op[1])
+        elif op[0] == "fork":
+            bm.fork(op[1], op[2])
+        else:
+            for _ in range(op[2]):
+                c = bm.append_slot(op[1])[1]
+                if c is not None:
+                    pairs.append(c)
+    slots = []
+    for sid, n in zip(w.step_seqs, w.chunks):
+        for _ in range(int(n)):
+            slot, c = bm.append_slot(sid)
+            slots.append(slot)
+            if c is not None:
+                pairs.append(c)
+    kp, vp = k_src, v_src
+    oops.copy_blocks(kp, vp, pairs)
+    oops.reshape_and_cache(k_new, v_new, kp, vp, torch.tensor(slots, dtype=torch.int64), w.bs)
+    tables = np.full((w.B, w.max_blocks_per_seq), -1, dtype=np.int64)
+    for i, sid in enumerate(w.step_seqs):
+        t = bm.block_table(sid)
+        tables[i, :len(t)] = t
+    lens = np.array([bm.seq_len(sid) for sid in w.step_seqs])
+    return kp, vp, tables, lens
+
+
+def run_prefill(args, rank, world, device):
+    """One chunked-prefill step (CoW copies, the chunk's K/V into the cache,
+    causal attention of every chunk token), timed like the decode step."""
+    import paged_kv_cache_259_gb300 as pkv
+    from paged_kv_cache_259_gb300.engine import PagedKVCache
+    w = wl.PREFILL_CONFIGS[args.config]()
+    k_src, v_src = w.past_pools()
+    q, k_new, v_new = w.step_inputs()
+    cache = PagedKVCache(w.NB, w.Hq, w.Hkv, w.D, w.bs, torch.bfloat16, w.free_order, device)
+    cache.load(k_src, v_src)
+    cache.apply_copies(cache.replay(w.script))
+    plan = cache.plan_prefill(w.step_seqs, w.chunks, max_blocks=w.max_blocks_per_seq)
+    mql = plan.max_query_len
+    stream = torch.cuda.current_stream(device)
+    dev = plan.device_tensors(device)
+    qd, kd, vd = q.to(device), k_new.to(device), v_new.to(device)
+    out = torch.empty(w.T, w.Hq, w.D, dtype=torch.bfloat16, device=device)
+    torch.cuda.synchronize()
+
+    def step():
+        cache.prefill_step(qd, kd, vd, dev, out, w.scale, mql, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if pkv.get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = pkv.kernel_launches()
+    t0.record(stream)
+    for i in range(K):
+        if dev["pairs"].shape[0]:
+            pkv.copy_blocks(cache.k_pool, cache.v_pool, dev["pairs"], stream=stream)
+        pkv.reshape_and_cache(kd, vd, cache.k_pool, cache.v_pool, dev["slots"], stream=stream)
+        ev[i][0].record(stream)
+        pkv.paged_attention_prefill(out, qd, cache.k_pool, cache.v_pool, dev["tables"],
+                                    dev["lens"], dev["query_start"], w.scale, mql, stream)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    launches = pkv.kernel_launches() - launches0
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    if pkv.get_device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    att_ms = np.array([a.elapsed_time(b) for a, b in ev])
+    launches_per_step = count_launches(step)
+
+    host = plan.host_tensors(pin=True)
+    hq, hk, hv = q.pin_memory(), k_new.pin_memory(), v_new.pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    dplan = {k: torch.empty_like(v) for k, v in dev.items()}
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, *host.values()))
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        for src_t, dst_t in ((hq, dq), (hk, dk), (hv, dv)):
+            dst_t.copy_(src_t, non_blocking=True)
+        for k in dplan:
+            dplan[k].copy_(host[k], non_blocking=True)
+        cache.prefill_step(dq, dk, dv, dplan, out, w.scale, mql, stream=stream)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    K2 = max(3, K // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(K2):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return {"w": w, "ms_per_step": t0.elapsed_time(t1) / K, "att_ms": float(att_ms.mean()),
+            "att_ms_median": float(np.median(att_ms)), "e2e_ms": e0.elapsed_time(e1) / K2,
+            "h2d": h2d, "d2h": d2h, "clocks": clk, "launches": launches,
+            "launches_per_step": launches_per_step, "pairs": int(plan.pairs.shape[0]),
+            "cpu": (q, k_src, v_src, k_new, v_new)}
+
+
+def prefill_workload_desc(w):
+    ctx = np.asarray(w.final_lens) - np.asarray(w.chunks)
+    return (f"{w.name}: B={w.B}, chunk={int(w.chunks[0])} tokens per sequence (T={w.T}), "
+            f"context {int(ctx.min())}..{int(ctx.max())} cached tokens, Hq={w.Hq}, Hkv={w.Hkv}, "
+            f"D={w.D}, block_size={w.bs}, NB={w.NB}, bf16")
+
+
+def prefill_cpu_inputs(w, cpu):
+    q, k_src, v_src, k_new, v_new = cpu
+    kp, vp, tables, lens = prefill_oracle_inputs(w, k_src, v_src, k_new, v_new)
+    return (q, kp, vp, 1.0, 1.0), tables, lens
+
+
+def prefill_main(args, rank, world, device):
+    r = run_prefill(args, rank, world, device)
+    w = r["w"]
+    ms = max_over_ranks(r["ms_per_step"], world, device)
+    att_ms = max_over_ranks(r["att_ms"], world, device)
+    e2e_ms = max_over_ranks(r["e2e_ms"], world, device)
+    fl = prefill_flops(w)
+    peak, kind = load_tensor_peak()
+    if rank != 0:
+        return
+    inp, tables, lens = prefill_cpu_inputs(w, r["cpu"])
+    extra = {"mode": "prefill", "query_start": w.query_start}
+    gf, units, cores, note = oracle_timing(w, inp, tables, lens, 0, args.cpu_budget, 1,
+                                           extra=extra)
+    att_tf = fl / (att_ms * 1e-3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC, "value": round(world * fl / (ms * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": prefill_workload_desc(w),
+            "step": ("copy_blocks (CoW pairs: %d) + reshape_and_cache of %d chunk tokens + "
+                     "paged_attention_prefill; %d kernel launches per step"
+                     % (r["pairs"], w.T, r["launches_per_step"])),
+            "l2": "K/V of the step's sequences %.2f GB vs %d MB L2; the chunk's K/V "
+                  "(%.0f MB) is rewritten every step" % (
+                      float(np.sum(w.final_lens)) * 2 * w.Hkv * w.D * 2 / 1e9, L2_BYTES >> 20,
+                      w.T * 2 * w.Hkv * w.D * 2 / 1e6),
+            "flops_per_step": fl,
+            "chunk_tokens_per_s": round(world * w.T / (ms * 1e-3), 1),
+            "step_frac_of_peak": round(fl / (ms * 1e-3) / 1e12 / peak, 4),
+        },
+        "roofline": {
+            "kernel": "paged_attention_prefill (tcgen05)", "bound": "tensor",
+            "achieved": round(att_tf, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(att_tf / peak, 4), "traffic": None,
+            "peak_source": f"{kind} bf16_tflops (dense bf16 GEMM burst, MEASURED_PEAKS.json)",
+            "flops_per_launch": fl, "ms_per_launch": round(att_ms, 5),
+            "ms_per_launch_median": round(r["att_ms_median"], 5),
+        },
+        "cpu_baseline": {
+            "value": round(float(gf[0]) / 1e3, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{int(units[0])} random (chunk token, head) rows of this workload in "
+                      f"{args.cpu_budget:.1f} s on {cores} host cores (one single-threaded "
+                      f"float64 oracle process per core){note}",
+        },
+        "e2e": {"value": round(world * fl / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_prefill(args):
+    """Reference arm for a chunked-prefill workload: the oracle on the host cores."""
+    w = wl.PREFILL_CONFIGS[args.config]()
+    k_src, v_src = w.past_pools()
+    q, k_new, v_new = w.step_inputs()
+    inp, tables, lens = prefill_cpu_inputs(w, (q, k_src, v_src, k_new, v_new))
+    slice_s = 120.0 / (args.steps + args.warmup)
+    gf, units, cores, note = oracle_timing(w, inp, tables, lens, 0, slice_s,
+                                           args.warmup + args.steps,
+                                           extra={"mode": "prefill", "query_start": w.query_start})
+    value = float(gf[args.warmup:].mean()) / 1e3
+    line = {
+        "impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6),
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * slice_s, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": prefill_workload_desc(w)},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{int(units[args.warmup:].sum())} random (chunk token, head) "
+                                   f"rows finished in {args.steps} time slices of {slice_s:.3f} s "
+                                   f"on {cores} host cores{note}"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def make_workload(args):
     if args.batch is None:
         return wl.CONFIGS[args.config]()
@@ -462,7 +725,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.CONFIGS))
+    ap.add_argument("--config", default=DEFAULT_CONFIG,
+                    choices=sorted(wl.CONFIGS) + sorted(wl.PREFILL_CONFIGS))
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's sequence count (profiling small cases)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -477,7 +741,10 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        run_reference(args)
+        if args.config in wl.PREFILL_CONFIGS:
+            run_reference_prefill(args)
+        else:
+            run_reference(args)
         return
 
     import paged_kv_cache_259_gb300 as pkv
@@ -488,6 +755,13 @@ def main():
     torch.cuda.set_device(device)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
+
+    if args.config in wl.PREFILL_CONFIGS:
+        prefill_main(args, rank, world, device)
+        if world > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return
 
     r = run_gpu(args, rank, world, device)
     w, nb = r["w"], r["nbytes"]

@@ -117,6 +117,74 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     }
 }
 
+// bf16 caches, written by aligned 8-slot windows. Token i (slot s) looks at the
+// window of slots s - s%8 .. s - s%8 + 7: if tokens i - s%8 .. i - s%8 + 7 fill
+// exactly that window (a prefill chunk away from its two ends), their V values
+// for 8 dims are one whole V core matrix (8 dims x 8 tokens) and their K chunks
+// the 8 rows of one K core matrix, so the window's first token transposes V in
+// registers and writes both as 8 rows of 16 bytes each (the token-by-token path
+// writes V as 64 scattered 2-byte values); the other 7 tokens of the window do
+// nothing. Every token not in such a window (decode steps, ragged chunk ends,
+// padding) is written on its own as above. One thread per (token, kv head,
+// 8-dim chunk).
+__global__ void __launch_bounds__(256) reshape_and_cache_bf16_windows(
+    const uint4* __restrict__ k, const uint4* __restrict__ v, uint4* __restrict__ k_pool,
+    uint4* __restrict__ v_pool, const int64_t* __restrict__ slots, int num_tokens, int hkv, int d,
+    int bs, int num_blocks, int* err) {
+    const int planes = d / 8;                              // 16-byte chunks per (token, head)
+    const long long total = (long long)num_tokens * hkv * planes;
+    const long long slot_limit = (long long)num_blocks * bs;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int j = (int)(idx % planes);
+        const long long r = idx / planes;
+        const int h = (int)(r % hkv);
+        const int t = (int)(r / hkv);
+        const long long slot = slots[t];
+        if (slot < 0) continue;                            // padding token
+        if (slot >= slot_limit) {
+            flag_error(err, kErrOutOfRange);
+            continue;
+        }
+        const int lead = t - (int)(slot & 7);              // first token of the window
+        bool run = lead >= 0 && lead + 8 <= num_tokens && (slot | 7) < slot_limit;
+        if (run) {                                         // tokens lead..lead+7 exist
+#pragma unroll
+            for (int i = 0; i < 8; ++i) run = run && slots[lead + i] == (slot & ~7LL) + i;
+        }
+        const long long blk = slot / bs, off = slot % bs;
+        const long long tile = (blk * hkv + h) * (long long)(d * bs / 8);   // 16-byte units
+        if (!run) {
+            const long long src = ((long long)t * hkv + h) * planes + j;
+            k_pool[tile + ((off >> 3) * planes + j) * 8 + (off & 7)] = k[src];
+            store_v_column(reinterpret_cast<__nv_bfloat16*>(v_pool + tile), v[src], j * 8, d,
+                           (int)off);
+            continue;
+        }
+        if (t != lead) continue;                           // written by the window's first token
+        const long long cm = tile + ((off >> 3) * planes + j) * 8;   // core matrix (off/8, j)
+        uint4 vv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const long long src = ((long long)(lead + i) * hkv + h) * planes + j;
+            k_pool[cm + i] = k[src];
+            vv[i] = v[src];
+        }
+#pragma unroll
+        for (int dd = 0; dd < 8; ++dd) {
+            const uint32_t sel = (dd & 1) ? 0x7632u : 0x5410u;   // high or low halves
+            uint32_t w[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t* a = reinterpret_cast<const uint32_t*>(&vv[2 * m]);
+                const uint32_t* b = reinterpret_cast<const uint32_t*>(&vv[2 * m + 1]);
+                w[m] = __byte_perm(a[dd >> 1], b[dd >> 1], sel);   // tokens 2m, 2m+1 of dim dd
+            }
+            v_pool[cm + dd] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
 constexpr int kCopyThreads = 256;
 constexpr int kCopyChunkBytes = kCopyThreads * 16 * 4;    // 16 KB per CTA
 
@@ -166,6 +234,26 @@ cudaError_t launch_reshape(const void* k, const void* v, void* kp, void* vp, con
     return cudaGetLastError();
 }
 
+// Batches this large (a prefill chunk) go through the window kernel; smaller
+// ones (a decode step: one token per sequence, no runs) skip its window checks.
+constexpr int kGroupTokens = 512;
+
+cudaError_t launch_reshape_groups(const void* k, const void* v, void* kp, void* vp,
+                                  const int64_t* slots, int num_tokens, int hkv, int d, int bs,
+                                  int num_blocks, int* err, cudaStream_t stream) {
+    const long long items = (long long)num_tokens * hkv * (d / 8);
+    const int threads = 256;
+    long long blocks = (items + threads - 1) / threads;
+    const long long cap = 8LL * num_sms();
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    note_launch();
+    reshape_and_cache_bf16_windows<<<(unsigned)blocks, threads, 0, stream>>>(
+        static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(kp),
+        static_cast<uint4*>(vp), slots, num_tokens, hkv, d, bs, num_blocks, err);
+    return cudaGetLastError();
+}
+
 }  // namespace
 }  // namespace pkv
 
@@ -198,6 +286,9 @@ int reshape_and_cache(const void* k, const void* v, void* k_pool, void* v_pool,
         e = launch_reshape<float, float>(k, v, k_pool, v_pool, slot_mapping, num_tokens,
                                          num_kv_heads, head_dim, block_size, num_blocks, 1.f, 1.f,
                                          err, s);
+    else if (src_dtype == PKV_BF16 && cache_dtype == PKV_BF16 && num_tokens >= kGroupTokens)
+        e = launch_reshape_groups(k, v, k_pool, v_pool, slot_mapping, num_tokens, num_kv_heads,
+                                  head_dim, block_size, num_blocks, err, s);
     else if (src_dtype == PKV_BF16 && cache_dtype == PKV_BF16)
         e = launch_reshape<__nv_bfloat16, __nv_bfloat16>(k, v, k_pool, v_pool, slot_mapping,
                                                          num_tokens, num_kv_heads, head_dim,

@@ -291,3 +291,38 @@ def test_grouped_decode_long_lists_are_split_and_merged():
     assert g["err"] == 0 and g["plan"].num_groups == 3
     o = run_oracle(inp)
     assert_close(g["out"].numpy(), o["out"], "bf16", "grouped, split lists")
+
+
+def test_reshape_and_cache_large_batch_runs_and_ragged_slots():
+    """A batch large enough for the grouped slot write (>= 512 tokens): aligned
+    runs of 8 consecutive slots (written as whole core matrices), runs that start
+    off a multiple of 8, scattered slots, padding and one slot outside the pool;
+    the pools must equal the oracle's slot writes bit for bit."""
+    from oracle import cache_ops as oops
+    NB, Hkv, bs, D = 96, 3, 16, 128
+    rng = np.random.default_rng(5)
+    slots = list(range(0, 256))                      # aligned runs
+    slots += list(range(261, 261 + 203))             # a run off the 8-slot grid
+    slots += [-1] * 5                                 # padding
+    slots += [int(x) for x in rng.choice(np.arange(600, NB * bs), 100, replace=False)]
+    slots += [NB * bs + 3]                            # outside the pool
+    slots += list(range(520, 560))                    # another aligned run
+    T = len(slots)
+    assert T >= 512
+    g = torch.Generator().manual_seed(9)
+    k = torch.randn(T, Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(T, Hkv, D, generator=g).to(torch.bfloat16)
+    k0 = torch.randn(NB, Hkv, bs, D, generator=g).to(torch.bfloat16)
+    v0 = torch.randn(NB, Hkv, bs, D, generator=g).to(torch.bfloat16)
+    kp, vp = pkv.pools_from_views(k0.cuda(), v0.cuda())
+    st = torch.tensor(slots, dtype=torch.int64)
+    assert pkv.get_device_error() == 0
+    pkv.reshape_and_cache(k.cuda(), v.cuda(), kp, vp, st.cuda())
+    assert pkv.get_device_error() == -4               # the slot outside the pool
+    ok_slots = st.clone()
+    ok_slots[st >= NB * bs] = -1
+    kr, vr = k0.clone(), v0.clone()
+    oops.reshape_and_cache(k, v, kr, vr, ok_slots, bs)
+    kv, vv = pkv.pool_views(kp, vp)
+    assert torch.equal(kv.cpu().view(torch.int16), kr.view(torch.int16))
+    assert torch.equal(vv.cpu().view(torch.int16), vr.view(torch.int16))
