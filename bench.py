@@ -498,12 +498,43 @@ def prefill_oracle_inputs(w, k_src, v_src, k_new, v_new):
     return kp, vp, tables, lens
 
 
+PREFILL_SOURCES = ["pkv_prefill.cu", "pkv_tcgen05.cuh"]
+
+
+def prefill_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in PREFILL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_259_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def prefill_traffic(config):
+    """DRAM bytes per prefill launch from profiles/prefill_traffic.json (one ncu
+    capture at full size), or None for other kernel sources or workloads."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "prefill_traffic.json")) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    if t.get("kernel_source_sha") != prefill_source_hash():
+        return None
+    e = t.get("workloads", {}).get(config)
+    return None if e is None else e.get("dram_bytes_per_launch")
+
+
+def prefill_workload(args):
+    make = wl.PREFILL_CONFIGS[args.config]
+    return make() if args.batch is None else make(B=args.batch)
+
+
 def run_prefill(args, rank, world, device):
     """One chunked-prefill step (CoW copies, the chunk's K/V into the cache,
     causal attention of every chunk token), timed like the decode step."""
     import paged_kv_cache_259_gb300 as pkv
     from paged_kv_cache_259_gb300.engine import PagedKVCache
-    w = wl.PREFILL_CONFIGS[args.config]()
+    w = prefill_workload(args)
     k_src, v_src = w.past_pools()
     q, k_new, v_new = w.step_inputs()
     cache = PagedKVCache(w.NB, w.Hq, w.Hkv, w.D, w.bs, torch.bfloat16, w.free_order, device)
@@ -640,7 +671,8 @@ def prefill_main(args, rank, world, device):
         "roofline": {
             "kernel": "paged_attention_prefill (tcgen05)", "bound": "tensor",
             "achieved": round(att_tf, 2), "peak": peak, "unit": "TFLOP/s",
-            "frac": round(att_tf / peak, 4), "traffic": None,
+            "frac": round(att_tf / peak, 4),
+            "traffic": prefill_traffic(args.config) if args.batch is None else None,
             "peak_source": f"{kind} bf16_tflops (dense bf16 GEMM burst, MEASURED_PEAKS.json)",
             "flops_per_launch": fl, "ms_per_launch": round(att_ms, 5),
             "ms_per_launch_median": round(r["att_ms_median"], 5),
@@ -663,7 +695,7 @@ def prefill_main(args, rank, world, device):
 
 def run_reference_prefill(args):
     """Reference arm for a chunked-prefill workload: the oracle on the host cores."""
-    w = wl.PREFILL_CONFIGS[args.config]()
+    w = prefill_workload(args)
     k_src, v_src = w.past_pools()
     q, k_new, v_new = w.step_inputs()
     inp, tables, lens = prefill_cpu_inputs(w, (q, k_src, v_src, k_new, v_new))
