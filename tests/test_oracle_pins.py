@@ -508,3 +508,172 @@ def test_prefill_rejects_chunk_longer_than_sequence():
     q, kp, vp, tables, sl, qs, _ = prefill_case(2, [5], [5], 2, 2, 8, 4)
     with pytest.raises(ValueError):
         oatt.paged_prefill(q, kp, vp, tables, np.array([4]), qs, 1.0, 4)
+
+
+# ---------------------------------------------------------------- prefix caching
+from oracle.prefix_cache import PrefixCachingBlockManager  # noqa: E402
+
+
+class Shadow:
+    """What every slot of the pool holds (the token whose K/V was written
+    there), updated by the slot writes and block copies a manager asks for."""
+
+    def __init__(self, num_blocks, bs):
+        self.bs = bs
+        self.slot = [None] * (num_blocks * bs)
+
+    def write(self, slot, token):
+        self.slot[slot] = token
+
+    def copy(self, src, dst):
+        bs = self.bs
+        self.slot[dst * bs:(dst + 1) * bs] = self.slot[src * bs:(src + 1) * bs]
+
+    def gather(self, table, n):
+        bs = self.bs
+        return [self.slot[table[t // bs] * bs + t % bs] for t in range(n)]
+
+
+def pc_append(bm, sh, sid, token):
+    slot, cow = bm.append_token(sid, token)
+    if cow is not None:
+        sh.copy(*cow)
+    sh.write(slot, token)
+
+
+def pc_check(bm, sh, live):
+    """Every live sequence reads back exactly its own tokens through its table;
+    counts equal table references; free, evictable and used blocks partition
+    the pool; every registered block holds the last block of its prefix."""
+    refs = [0] * bm.num_blocks
+    for sid in live:
+        t = bm.block_table(sid)
+        for b in t:
+            refs[b] += 1
+        assert sh.gather(t, bm.seq_len(sid)) == bm.tokens[sid]
+    assert refs == bm.ref
+    used = {b for b in range(bm.num_blocks) if bm.ref[b] > 0}
+    free, ev = set(bm.free), set(bm.evictable)
+    assert not (free & ev) and not (free & used) and not (ev & used)
+    assert len(bm.free) == len(free) and len(bm.evictable) == len(ev)
+    assert all(bm.ref[b] == 0 and b in bm.key_of for b in ev)
+    for key, b in bm.block_of.items():
+        assert bm.key_of[b] == key
+        assert sh.slot[b * sh.bs:(b + 1) * sh.bs] == list(key[-sh.bs:])
+
+
+def test_prefix_cache_reuses_common_system_prompt_blocks():
+    bs = 16
+    bm = PrefixCachingBlockManager(64, bs, range(64))
+    sh = Shadow(64, bs)
+    system = list(range(1000, 1100))                   # 100-token system prompt
+    p1 = system + [1, 2, 3]
+    assert bm.add_seq_prompt("a", p1) == 0             # nothing cached yet
+    for t in p1:
+        pc_append(bm, sh, "a", t)
+    assert bm.num_cached() == 6                        # its 6 full blocks registered
+    p2 = system + list(range(50, 80))
+    n = bm.add_seq_prompt("b", p2)
+    assert n == 96 and bm.hit_blocks == 6              # 6 full blocks of the common 100
+    for t in p2[n:]:
+        pc_append(bm, sh, "b", t)
+    assert bm.block_table("b")[:6] == bm.block_table("a")[:6]
+    assert bm.block_table("b")[6] != bm.block_table("a")[6]
+    pc_check(bm, sh, ["a", "b"])
+
+
+def test_prefix_cache_leaves_one_prompt_token_to_compute():
+    bs = 16
+    bm = PrefixCachingBlockManager(32, bs, range(32))
+    sh = Shadow(32, bs)
+    p = list(range(64))                                # exactly 4 blocks
+    bm.add_seq_prompt(0, p)
+    for t in p:
+        pc_append(bm, sh, 0, t)
+    assert bm.add_seq_prompt(1, p) == 48               # 3 blocks reused, 16 tokens left
+    for t in p[48:]:
+        pc_append(bm, sh, 1, t)
+    pc_check(bm, sh, [0, 1])
+
+
+def test_prefix_cache_never_shares_blocks_of_different_prefixes():
+    """Block 1 of both prompts holds the same 16 ids, but their first tokens
+    differ: the second request must not reuse either block."""
+    bs = 16
+    bm = PrefixCachingBlockManager(32, bs, range(32))
+    sh = Shadow(32, bs)
+    a = [7] + list(range(1, 40))
+    b = [8] + list(range(1, 40))
+    bm.add_seq_prompt("a", a)
+    for t in a:
+        pc_append(bm, sh, "a", t)
+    assert bm.add_seq_prompt("b", b) == 0
+    for t in b:
+        pc_append(bm, sh, "b", t)
+    assert not set(bm.block_table("a")) & set(bm.block_table("b"))
+    pc_check(bm, sh, ["a", "b"])
+
+
+def test_prefix_cache_revives_freed_blocks_and_evicts_oldest_first():
+    bs = 4
+    bm = PrefixCachingBlockManager(8, bs, range(8))
+    sh = Shadow(8, bs)
+    p = list(range(12))                                # 3 full blocks
+    bm.add_seq_prompt(0, p)
+    for t in p:
+        pc_append(bm, sh, 0, t)
+    t0 = bm.block_table(0)
+    bm.free_seq(0)
+    assert bm.evictable == t0[::-1] and bm.num_free() == 5   # cached, kept, end first
+    assert bm.add_seq_prompt(1, p + [99]) == 12        # revived: all 3 blocks reused
+    assert bm.block_table(1) == t0 and bm.num_evictable() == 0
+    pc_append(bm, sh, 1, 99)
+    bm.free_seq(1)                                     # 4th block holds 1 token: uncached
+    assert bm.evictable == t0[::-1]
+    # fill the 5 free blocks with an unrelated 20-token prompt, then one more block
+    q = list(range(500, 520))
+    bm.add_seq_prompt(2, q)
+    for t in q:
+        pc_append(bm, sh, 2, t)
+    assert bm.num_free() == 0
+    pc_append(bm, sh, 2, 520)                          # needs a block: evicts the oldest
+    assert bm.block_table(2)[-1] == t0[2]              # the end of the old prefix went first
+    assert tuple(p) not in bm.block_of and tuple(p[:8]) in bm.block_of
+    assert bm.add_seq_prompt(3, p + [1]) == 8          # only 2 blocks still cached
+    pc_check(bm, sh, [2, 3])
+
+
+def test_prefix_cache_random_scripts_keep_content_and_count_invariants():
+    bs = 4
+    rng = np.random.default_rng(11)
+    for trial in range(30):
+        nb = 40
+        bm = PrefixCachingBlockManager(nb, bs, list(rng.permutation(nb)))
+        sh = Shadow(nb, bs)
+        prompts = [list(rng.integers(0, 3, size=rng.integers(1, 20))) for _ in range(4)]
+        live, nxt = [], 0
+        for step in range(60):
+            op = rng.integers(0, 4)
+            try:
+                if op == 0 or not live:
+                    base = prompts[rng.integers(len(prompts))]
+                    p = base + list(rng.integers(0, 3, size=rng.integers(0, 6)))
+                    n = bm.add_seq_prompt(nxt, p)
+                    live.append(nxt)
+                    for t in p[n:]:
+                        pc_append(bm, sh, nxt, int(t))
+                    nxt += 1
+                elif op == 1:
+                    sid = live[rng.integers(len(live))]
+                    pc_append(bm, sh, sid, int(rng.integers(0, 3)))
+                elif op == 2:
+                    sid = live[rng.integers(len(live))]
+                    bm.fork(sid, nxt)
+                    live.append(nxt)
+                    nxt += 1
+                else:
+                    sid = live.pop(rng.integers(len(live)))
+                    bm.free_seq(sid)
+            except PoolExhausted:
+                break
+            pc_check(bm, sh, live)
