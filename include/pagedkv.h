@@ -374,6 +374,41 @@ PKV_API int bm_num_free(const pkv_block_manager* bm);
 PKV_API int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
                      int max_members, int32_t* group_members, int32_t* group_prefix,
                      int32_t* seq_group, int* num_groups);
+/* Prefix caching (glossary "Chia sẻ block giữa các chuỗi": requests that begin
+ * with the same system prompt reuse one copy of the common prefix, with a count
+ * per block; "vLLM PagedAttention: uma revolução...": prefix caching).
+ * A block filled by tokens whose ids are known is registered under its prefix
+ * (every token id from the start of the sequence through the block). A new
+ * request reuses, from the front, the registered blocks of its prompt, leaving
+ * at least one prompt token to compute. A registered block whose count reaches 0
+ * stays cached as "evictable" (a later hit revives it); when a block is needed
+ * and the free list is empty, the oldest evictable block is evicted. One release
+ * sends uncached blocks to the free list in table order and cached ones to the
+ * evictable list in reverse table order. Lookups use a 64-bit hash of the whole
+ * prefix and compare the block's own token ids and the hash of the prefix
+ * before it (a false hit needs a 64-bit hash collision).
+ *
+ * bm_enable_prefix_caching: switch it on; only before any sequence is added
+ *   (else PKV_ERR_INVALID_ARG). Appends through bm_append_slot / _n / _slots
+ *   carry no token ids: their blocks are never registered.
+ * bm_add_seq_prompt: create seq_id and reuse the cached blocks of prompt[0..n);
+ *   *num_cached = prompt tokens already cached (a multiple of block_size). The
+ *   caller appends prompt[*num_cached..n) with bm_append_tokens.
+ * bm_append_tokens: n appends with token ids; slots[i] for tokens[i]; CoW pairs
+ *   as bm_append_n. On exhaustion the appends done so far stay done.
+ * bm_cache_stats: blocks looked up / found by bm_add_seq_prompt so far, blocks
+ *   registered, evictable blocks.
+ * bm_evictable_list: evictable block ids, oldest first, into out[0..cap);
+ *   returns their number. */
+PKV_API int bm_enable_prefix_caching(pkv_block_manager* bm);
+PKV_API int bm_add_seq_prompt(pkv_block_manager* bm, int64_t seq_id, const int32_t* prompt,
+                              int n, int* num_cached);
+PKV_API int bm_append_tokens(pkv_block_manager* bm, int64_t seq_id, const int32_t* tokens, int n,
+                             int64_t* slots, int64_t* cow_pairs, int cow_cap, int* num_cow);
+PKV_API int bm_cache_stats(const pkv_block_manager* bm, int64_t* hit_blocks,
+                           int64_t* lookup_blocks, int* num_cached, int* num_evictable);
+PKV_API int bm_evictable_list(const pkv_block_manager* bm, int32_t* out, int cap);
+
 /* The free list, front first, into out[0..cap); returns its length. */
 PKV_API int bm_free_list(const pkv_block_manager* bm, int32_t* out, int cap);
 

@@ -100,6 +100,11 @@ def load_library():
         "bm_refcount": (c_int, [vp, c_int, ip]),
         "bm_num_free": (c_int, [vp]),
         "bm_free_list": (c_int, [vp, i32p, c_int]),
+        "bm_enable_prefix_caching": (c_int, [vp]),
+        "bm_add_seq_prompt": (c_int, [vp, ctypes.c_int64, i32p, c_int, ip]),
+        "bm_append_tokens": (c_int, [vp, ctypes.c_int64, i32p, c_int, i64p, i64p, c_int, ip]),
+        "bm_cache_stats": (c_int, [vp, i64p, i64p, ip, ip]),
+        "bm_evictable_list": (c_int, [vp, i32p, c_int]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -432,7 +437,7 @@ def _i64p(a):
 class BlockManager:
     """Host block manager of the C library (free list front-first, refcounts, CoW)."""
 
-    def __init__(self, num_blocks, block_size, free_order):
+    def __init__(self, num_blocks, block_size, free_order, prefix_caching=False):
         self._lib = load_library()
         fo = np.ascontiguousarray(np.asarray(free_order, dtype=np.int32))
         h = self._lib.bm_create(num_blocks, block_size, _i32p(fo), len(fo))
@@ -441,6 +446,9 @@ class BlockManager:
         self._h = ctypes.c_void_p(h)
         self.num_blocks = num_blocks
         self.block_size = block_size
+        self.prefix_caching = bool(prefix_caching)
+        if prefix_caching:
+            _check(self._lib.bm_enable_prefix_caching(self._h), "bm_enable_prefix_caching")
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -534,4 +542,40 @@ class BlockManager:
         n = self._lib.bm_free_list(self._h, None, 0)
         out = np.zeros(max(1, n), dtype=np.int32)
         self._lib.bm_free_list(self._h, _i32p(out), len(out))
+        return [int(x) for x in out[:n]]
+
+    # ---- prefix caching (BlockManager(..., prefix_caching=True))
+    def add_seq_prompt(self, sid, prompt):
+        """New sequence reusing the cached full blocks of ``prompt``; returns the
+        number of prompt tokens already cached (append the rest with
+        ``append_tokens``)."""
+        p = np.ascontiguousarray(np.asarray(prompt, dtype=np.int32))
+        n = ctypes.c_int(0)
+        _check(self._lib.bm_add_seq_prompt(self._h, sid, _i32p(p), len(p), ctypes.byref(n)),
+               "bm_add_seq_prompt")
+        return n.value
+
+    def append_tokens(self, sid, tokens):
+        """Appends with token ids; returns (slots int64 array, CoW pairs int64 [P, 2])."""
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        slots = np.zeros(max(1, len(t)), dtype=np.int64)
+        pairs = np.zeros((max(1, len(t)), 2), dtype=np.int64)
+        cnt = ctypes.c_int(0)
+        _check(self._lib.bm_append_tokens(self._h, sid, _i32p(t), len(t), _i64p(slots),
+                                          _i64p(pairs), len(t), ctypes.byref(cnt)),
+               "bm_append_tokens")
+        return slots[:len(t)].copy(), pairs[:cnt.value].copy()
+
+    def cache_stats(self):
+        """(hit blocks, looked-up blocks, registered blocks, evictable blocks)."""
+        h, l = ctypes.c_int64(), ctypes.c_int64()
+        c, e = ctypes.c_int(), ctypes.c_int()
+        _check(self._lib.bm_cache_stats(self._h, ctypes.byref(h), ctypes.byref(l), ctypes.byref(c),
+                                        ctypes.byref(e)), "bm_cache_stats")
+        return h.value, l.value, c.value, e.value
+
+    def evictable_list(self):
+        n = self._lib.bm_evictable_list(self._h, None, 0)
+        out = np.zeros(max(1, n), dtype=np.int32)
+        self._lib.bm_evictable_list(self._h, _i32p(out), len(out))
         return [int(x) for x in out[:n]]

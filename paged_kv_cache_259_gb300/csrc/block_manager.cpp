@@ -13,15 +13,53 @@
 //
 // Host memory only; no CUDA. The manager never touches KV data: it hands out
 // slot numbers and (src, dst) copy pairs that the device calls consume.
+//
+// Prefix caching (optional; glossary "Chia sẻ block giữa các chuỗi": requests
+// that begin with the same system prompt reuse one copy of the common prefix;
+// the vLLM feature list names prefix caching): a block filled by tokens whose
+// ids are known is registered under its prefix -- every token id from the start
+// of the sequence to the end of the block. A new request reuses, from the front,
+// the registered blocks of its prompt (leaving at least one prompt token to
+// compute); a registered block whose count reaches 0 stays cached as evictable
+// (revived by a later hit) until a new block is needed and the free list is
+// empty, when the oldest evictable block is evicted. Within one release,
+// uncached blocks go to the free list in table order and cached ones to the
+// evictable list in reverse table order. The index is a 64-bit hash of the whole
+// prefix (chained block by block); a hit also compares the block's own token
+// ids and the hash of the prefix before it.
 #include <algorithm>
 #include <climits>
 #include <cstdint>
 #include <deque>
+#include <list>
 #include <new>
 #include <unordered_map>
 #include <vector>
 
 #include "../../include/pagedkv.h"
+
+namespace {
+
+constexpr int64_t kUnknownToken = INT64_MIN;
+constexpr uint64_t kPrefixSeed = 0x243f6a8885a308d3ULL;
+
+// splitmix64's output function (Steele, Lea, Flood: "Fast splittable
+// pseudorandom number generators"), used to chain token ids into a prefix hash.
+uint64_t mix64(uint64_t x) {
+    x ^= x >> 30;
+    x *= 0xbf58476d1ce4e5b9ULL;
+    x ^= x >> 27;
+    x *= 0x94d049bb133111ebULL;
+    x ^= x >> 31;
+    return x;
+}
+
+uint64_t chain(uint64_t h, const int64_t* tok, int n) {
+    for (int i = 0; i < n; ++i) h = mix64(h ^ (mix64((uint64_t)tok[i]) + 0x9e3779b97f4a7c15ULL));
+    return h;
+}
+
+}  // namespace
 
 struct pkv_block_manager {
     int num_blocks = 0;
@@ -31,28 +69,97 @@ struct pkv_block_manager {
     struct Seq {
         std::vector<int32_t> table;      // logical block i -> physical block id
         int64_t len = 0;                 // tokens cached
+        std::vector<int64_t> tokens;     // token ids (prefix caching only)
+        std::vector<uint64_t> hashes;    // prefix hash after each full block
     };
     std::unordered_map<int64_t, Seq> seqs;
 
+    // ---- prefix caching
+    bool caching = false;
+    std::vector<char> registered;                    // block holds a registered prefix
+    std::vector<uint64_t> key_hash, parent_hash;     // hash through / before the block
+    std::vector<int64_t> block_tokens;               // num_blocks x block_size ids
+    std::unordered_multimap<uint64_t, int32_t> index;
+    std::list<int32_t> evictable;                    // registered, count 0; oldest first
+    std::vector<std::list<int32_t>::iterator> ev_pos;
+    std::vector<char> in_ev;
+    int64_t hit_blocks = 0, lookup_blocks = 0;
+
+    bool can_take() const { return !free_list.empty() || (caching && !evictable.empty()); }
+
+    void deregister(int32_t b) {
+        auto range = index.equal_range(key_hash[b]);
+        for (auto it = range.first; it != range.second; ++it)
+            if (it->second == b) {
+                index.erase(it);
+                break;
+            }
+        registered[b] = 0;
+    }
+
     int32_t take() {
-        int32_t b = free_list.front();
-        free_list.pop_front();
+        int32_t b;
+        if (!free_list.empty()) {
+            b = free_list.front();
+            free_list.pop_front();
+        } else {                                     // caller checked can_take()
+            b = evictable.front();
+            evictable.pop_front();
+            in_ev[b] = 0;
+            deregister(b);
+        }
         ref[b] = 1;
         return b;
     }
 
+    // Registered block holding the block after prefix hash `parent` with these
+    // token ids, or -1.
+    int32_t find(uint64_t parent, uint64_t key, const int64_t* tok) const {
+        auto range = index.equal_range(key);
+        for (auto it = range.first; it != range.second; ++it) {
+            const int32_t b = it->second;
+            if (parent_hash[b] != parent) continue;
+            bool same = true;
+            for (int i = 0; i < block_size && same; ++i)
+                same = block_tokens[(size_t)b * block_size + i] == tok[i];
+            if (same) return b;
+        }
+        return -1;
+    }
+
+    // The sequence's last block has just been filled: register it under its
+    // prefix unless a token id is unknown or the prefix is registered already.
+    void maybe_register(Seq& s) {
+        const int64_t nb = s.len / block_size;
+        // the chain stops at the first block with an unknown token id
+        if (s.hashes.size() != (size_t)(nb - 1)) return;
+        const int64_t* tok = s.tokens.data() + (nb - 1) * block_size;
+        for (int i = 0; i < block_size; ++i)
+            if (tok[i] == kUnknownToken) return;
+        const uint64_t parent = nb > 1 ? s.hashes[nb - 2] : kPrefixSeed;
+        const uint64_t key = chain(parent, tok, block_size);
+        s.hashes.push_back(key);
+        const int32_t b = s.table.back();
+        if (registered[b] || find(parent, key, tok) >= 0) return;
+        registered[b] = 1;
+        key_hash[b] = key;
+        parent_hash[b] = parent;
+        for (int i = 0; i < block_size; ++i) block_tokens[(size_t)b * block_size + i] = tok[i];
+        index.emplace(key, b);
+    }
+
     // One append; on exhaustion nothing changes.
-    int append(Seq& s, int64_t* slot, int32_t* cow_src, int32_t* cow_dst) {
+    int append(Seq& s, int64_t token, int64_t* slot, int32_t* cow_src, int32_t* cow_dst) {
         *cow_src = -1;
         *cow_dst = -1;
         const int64_t n = s.len;
         if (n % block_size == 0) {
-            if (free_list.empty()) return PKV_ERR_POOL_EXHAUSTED;
+            if (!can_take()) return PKV_ERR_POOL_EXHAUSTED;
             s.table.push_back(take());
         } else {
             const int32_t last = s.table.back();
             if (ref[last] > 1) {                       // shared: copy before writing
-                if (free_list.empty()) return PKV_ERR_POOL_EXHAUSTED;
+                if (!can_take()) return PKV_ERR_POOL_EXHAUSTED;
                 const int32_t dst = take();
                 ref[last] -= 1;
                 s.table.back() = dst;
@@ -63,7 +170,15 @@ struct pkv_block_manager {
         const int32_t block = s.table[n / block_size];
         *slot = (int64_t)block * block_size + n % block_size;
         s.len = n + 1;
+        if (caching) {
+            s.tokens.push_back(token);
+            if (s.len % block_size == 0) maybe_register(s);
+        }
         return PKV_OK;
+    }
+
+    int append(Seq& s, int64_t* slot, int32_t* cow_src, int32_t* cow_dst) {
+        return append(s, kUnknownToken, slot, cow_src, cow_dst);
     }
 };
 
@@ -165,9 +280,19 @@ int bm_free_seq(pkv_block_manager* bm, int64_t seq_id) {
     if (!bm) return PKV_ERR_INVALID_ARG;
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
+    std::vector<int32_t> cached;
     for (int32_t b : it->second.table) {
         bm->ref[b] -= 1;
-        if (bm->ref[b] == 0) bm->free_list.push_back(b);
+        if (bm->ref[b] == 0) {
+            if (bm->caching && bm->registered[b])
+                cached.push_back(b);
+            else
+                bm->free_list.push_back(b);
+        }
+    }
+    for (auto r = cached.rbegin(); r != cached.rend(); ++r) {
+        bm->ev_pos[*r] = bm->evictable.insert(bm->evictable.end(), *r);
+        bm->in_ev[*r] = 1;
     }
     bm->seqs.erase(it);
     return PKV_OK;
@@ -273,6 +398,93 @@ int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
     }
     *num_groups = ng;
     return PKV_OK;
+}
+
+int bm_enable_prefix_caching(pkv_block_manager* bm) {
+    if (!bm || !bm->seqs.empty()) return PKV_ERR_INVALID_ARG;
+    if (bm->caching) return PKV_OK;
+    bm->caching = true;
+    bm->registered.assign(bm->num_blocks, 0);
+    bm->key_hash.assign(bm->num_blocks, 0);
+    bm->parent_hash.assign(bm->num_blocks, 0);
+    bm->block_tokens.assign((size_t)bm->num_blocks * bm->block_size, kUnknownToken);
+    bm->ev_pos.resize(bm->num_blocks);
+    bm->in_ev.assign(bm->num_blocks, 0);
+    return PKV_OK;
+}
+
+int bm_add_seq_prompt(pkv_block_manager* bm, int64_t seq_id, const int32_t* prompt, int n,
+                      int* num_cached) {
+    if (!bm || !bm->caching || n < 0 || (n > 0 && !prompt) || !num_cached)
+        return PKV_ERR_INVALID_ARG;
+    if (bm->seqs.count(seq_id)) return PKV_ERR_INVALID_ARG;
+    pkv_block_manager::Seq s;
+    const int bs = bm->block_size;
+    const int reusable = n > 0 ? (n - 1) / bs : 0;
+    std::vector<int64_t> tok(prompt, prompt + n);
+    uint64_t h = kPrefixSeed;
+    for (int i = 0; i < reusable; ++i) {
+        const uint64_t key = chain(h, tok.data() + (size_t)i * bs, bs);
+        bm->lookup_blocks += 1;
+        const int32_t b = bm->find(h, key, tok.data() + (size_t)i * bs);
+        if (b < 0) break;
+        bm->hit_blocks += 1;
+        if (bm->ref[b] == 0 && bm->in_ev[b]) {      // revive
+            bm->evictable.erase(bm->ev_pos[b]);
+            bm->in_ev[b] = 0;
+        }
+        bm->ref[b] += 1;
+        s.table.push_back(b);
+        s.hashes.push_back(key);
+        h = key;
+    }
+    s.len = (int64_t)s.table.size() * bs;
+    s.tokens.assign(tok.begin(), tok.begin() + s.len);
+    *num_cached = (int)s.len;
+    bm->seqs.emplace(seq_id, std::move(s));
+    return PKV_OK;
+}
+
+int bm_append_tokens(pkv_block_manager* bm, int64_t seq_id, const int32_t* tokens, int n,
+                     int64_t* slots, int64_t* cow_pairs, int cow_cap, int* num_cow) {
+    if (!bm || n < 0 || (n > 0 && (!tokens || !slots)) || !num_cow || (cow_cap > 0 && !cow_pairs))
+        return PKV_ERR_INVALID_ARG;
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
+    *num_cow = 0;
+    for (int i = 0; i < n; ++i) {
+        int32_t src, dst;
+        const int st = bm->append(it->second, (int64_t)tokens[i], &slots[i], &src, &dst);
+        if (st != PKV_OK) return st;
+        if (src >= 0) {
+            if (*num_cow >= cow_cap) return PKV_ERR_INVALID_ARG;
+            cow_pairs[2 * *num_cow] = src;
+            cow_pairs[2 * *num_cow + 1] = dst;
+            *num_cow += 1;
+        }
+    }
+    return PKV_OK;
+}
+
+int bm_cache_stats(const pkv_block_manager* bm, int64_t* hit_blocks, int64_t* lookup_blocks,
+                   int* num_cached, int* num_evictable) {
+    if (!bm || !hit_blocks || !lookup_blocks || !num_cached || !num_evictable)
+        return PKV_ERR_INVALID_ARG;
+    *hit_blocks = bm->hit_blocks;
+    *lookup_blocks = bm->lookup_blocks;
+    *num_cached = (int)bm->index.size();
+    *num_evictable = (int)bm->evictable.size();
+    return PKV_OK;
+}
+
+int bm_evictable_list(const pkv_block_manager* bm, int32_t* out, int cap) {
+    if (!bm) return -1;
+    int i = 0;
+    for (int32_t b : bm->evictable) {
+        if (i < cap && out) out[i] = b;
+        ++i;
+    }
+    return i;
 }
 
 int bm_free_list(const pkv_block_manager* bm, int32_t* out, int cap) {

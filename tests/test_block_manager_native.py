@@ -157,3 +157,80 @@ def test_prefix_groups_share_full_leading_blocks():
                 assert m not in seen and seq_group[m] == gi
                 seen.add(m)
         assert all(seq_group[i] == -1 for i in range(len(ids)) if i not in seen)
+
+
+# ---------------------------------------------------------------- prefix caching
+from oracle.prefix_cache import PrefixCachingBlockManager  # noqa: E402
+
+BlockManager = pkv.BlockManager
+
+
+def _same_state(nat, ora, live):
+    for sid in live:
+        assert nat.block_table(sid) == ora.block_table(sid)
+        assert nat.seq_len(sid) == ora.seq_len(sid)
+    assert nat.free_list() == ora.free
+    assert nat.evictable_list() == ora.evictable
+    assert [nat.refcount(b) for b in range(ora.num_blocks)] == ora.ref
+    h, l, c, e = nat.cache_stats()
+    assert (h, l, c, e) == (ora.hit_blocks, ora.lookup_blocks, ora.num_cached(), ora.num_evictable())
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_prefix_caching_matches_oracle_operation_by_operation(seed):
+    rng = np.random.default_rng(100 + seed)
+    bs = int(rng.choice([2, 4, 16]))
+    nb = int(rng.integers(20, 60))
+    order = list(rng.permutation(nb))
+    nat = BlockManager(nb, bs, order, prefix_caching=True)
+    ora = PrefixCachingBlockManager(nb, bs, order)
+    prompts = [list(rng.integers(0, 4, size=rng.integers(1, 6 * bs))) for _ in range(4)]
+    live, nxt = [], 0
+    for step in range(120):
+        op = int(rng.integers(0, 5))
+        try:
+            if op == 0 or not live:
+                p = prompts[rng.integers(len(prompts))] + list(rng.integers(0, 4, size=rng.integers(0, 2 * bs)))
+                n_o = ora.add_seq_prompt(nxt, p)
+                n_n = nat.add_seq_prompt(nxt, p)
+                assert n_n == n_o
+                live.append(nxt)
+                rest = [int(t) for t in p[n_o:]]
+                slots, pairs = nat.append_tokens(nxt, rest)
+                exp = [ora.append_token(nxt, t) for t in rest]
+                assert list(slots) == [s for s, _ in exp]
+                assert [tuple(x) for x in pairs] == [c for _, c in exp if c is not None]
+                nxt += 1
+            elif op == 1:
+                sid = live[rng.integers(len(live))]
+                toks = [int(t) for t in rng.integers(0, 4, size=rng.integers(1, 2 * bs))]
+                slots, pairs = nat.append_tokens(sid, toks)
+                exp = [ora.append_token(sid, t) for t in toks]
+                assert list(slots) == [s for s, _ in exp]
+                assert [tuple(x) for x in pairs] == [c for _, c in exp if c is not None]
+            elif op == 2:
+                sid = live[rng.integers(len(live))]
+                nat.fork(sid, nxt)
+                ora.fork(sid, nxt)
+                live.append(nxt)
+                nxt += 1
+            elif op == 3:
+                sid = live[rng.integers(len(live))]
+                assert nat.append_slot(sid) == ora.append_slot(sid)     # token id unknown
+            else:
+                sid = live.pop(rng.integers(len(live)))
+                nat.free_seq(sid)
+                ora.free_seq(sid)
+        except (pkv.PagedKVError, PoolExhausted) as e:
+            # both must run out at the same point
+            assert isinstance(e, PoolExhausted) or e.status == -5
+            break
+        _same_state(nat, ora, live)
+
+
+def test_prefix_caching_must_be_enabled_before_sequences_exist():
+    bm = BlockManager(8, 4, range(8))
+    bm.add_seq(0)
+    assert bm._lib.bm_enable_prefix_caching(bm._h) == -1
+    with pytest.raises(pkv.PagedKVError):
+        bm.add_seq_prompt(1, [1, 2, 3])              # caching is off
