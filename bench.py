@@ -453,12 +453,12 @@ PREFILL_METRIC = ("paged chunked-prefill attention: achieved TFLOP/s (% of bf16 
                   "and chunk tokens/s")
 
 
-def prefill_flops(w):
+def prefill_flops(w, lens=None, chunks=None):
     """Algorithmic FLOPs of the step's attention: chunk token i of sequence b sees
     p + 1 keys (p = L_b - C_b + i), and per (token, head, key) Q.K and P.V are
     2 * D multiply-adds each."""
-    L = np.asarray(w.final_lens, dtype=np.float64)
-    C = np.asarray(w.chunks, dtype=np.float64)
+    L = np.asarray(w.final_lens if lens is None else lens, dtype=np.float64)
+    C = np.asarray(w.chunks if chunks is None else chunks, dtype=np.float64)
     keys = C * (L - C) + C * (C + 1) / 2
     return float(keys.sum()) * w.Hq * 4 * w.D
 
@@ -525,7 +525,7 @@ def prefill_traffic(config):
 
 
 def prefill_workload(args):
-    make = wl.PREFILL_CONFIGS[args.config]
+    make = {**wl.PREFILL_CONFIGS, **wl.PROMPT_CONFIGS}[args.config]
     return make() if args.batch is None else make(B=args.batch)
 
 
@@ -536,16 +536,34 @@ def run_prefill(args, rank, world, device):
     from paged_kv_cache_259_gb300.engine import PagedKVCache
     w = prefill_workload(args)
     k_src, v_src = w.past_pools()
-    q, k_new, v_new = w.step_inputs()
-    cache = PagedKVCache(w.NB, w.Hq, w.Hkv, w.D, w.bs, torch.bfloat16, w.free_order, device)
+    prompts = isinstance(w, wl.PromptWorkload)
+    cache = PagedKVCache(w.NB, w.Hq, w.Hkv, w.D, w.bs, torch.bfloat16, w.free_order, device,
+                         prefix_caching=prompts)
     cache.load(k_src, v_src)
-    cache.apply_copies(cache.replay(w.script))
-    plan = cache.plan_prefill(w.step_seqs, w.chunks, max_blocks=w.max_blocks_per_seq)
+    plan_s = 0.0
+    if prompts:
+        # serve the system prompt first (its blocks are then cached), then plan
+        # the batch: each request reuses them and computes only the rest
+        warm = cache.plan_prompts([10 ** 9], w.warm, max_blocks=w.max_blocks_per_seq)
+        wq, wk, wv = (t.to(device) for t in w.rows("warm", 0, 0, len(w.warm[0])))
+        wout = torch.empty(wq.shape, dtype=torch.bfloat16, device=device)
+        cache.prefill_step(wq, wk, wv, warm.device_tensors(device), wout, w.scale,
+                           warm.max_query_len)
+        cache.bm.free_seq(10 ** 9)
+        t_plan = time.perf_counter()
+        plan = cache.plan_prompts(list(range(w.B)), w.prompts, max_blocks=w.max_blocks_per_seq)
+        plan_s = time.perf_counter() - t_plan
+        rows = [w.rows("step", b, int(n), len(p)) for b, (p, n) in enumerate(zip(w.prompts, plan.cached))]
+        q, k_new, v_new = (torch.cat([r[i] for r in rows]) for i in range(3))
+    else:
+        q, k_new, v_new = w.step_inputs()
+        cache.apply_copies(cache.replay(w.script))
+        plan = cache.plan_prefill(w.step_seqs, w.chunks, max_blocks=w.max_blocks_per_seq)
     mql = plan.max_query_len
     stream = torch.cuda.current_stream(device)
     dev = plan.device_tensors(device)
     qd, kd, vd = q.to(device), k_new.to(device), v_new.to(device)
-    out = torch.empty(w.T, w.Hq, w.D, dtype=torch.bfloat16, device=device)
+    out = torch.empty(int(plan.chunks.sum()), w.Hq, w.D, dtype=torch.bfloat16, device=device)
     torch.cuda.synchronize()
 
     def step():
@@ -619,34 +637,87 @@ def run_prefill(args, rank, world, device):
             "att_ms_median": float(np.median(att_ms)), "e2e_ms": e0.elapsed_time(e1) / K2,
             "h2d": h2d, "d2h": d2h, "clocks": clk, "launches": launches,
             "launches_per_step": launches_per_step, "pairs": int(plan.pairs.shape[0]),
+            "plan": plan, "plan_s": plan_s, "T": int(plan.chunks.sum()),
             "cpu": (q, k_src, v_src, k_new, v_new)}
 
 
+def prompt_stats(w, plan, r, ms, world):
+    """Prefix-cache figures of a prompt workload's step."""
+    served = int(np.sum(plan.lens))
+    cached = int(np.sum(plan.cached))
+    return {"prompt_tokens_per_s": round(world * served / (ms * 1e-3), 1),
+            "cached_fraction": round(cached / served, 4),
+            "host_plan_us_per_request": round(1e6 * r["plan_s"] / w.B, 2)}
+
+
 def prefill_workload_desc(w):
+    if isinstance(w, wl.PromptWorkload):
+        L = np.asarray(w.final_lens)
+        return (f"{w.name}: B={w.B} requests of {int(L.min())}..{int(L.max())} prompt tokens that "
+                f"all begin with one {len(w.warm[0])}-token system prompt, served first (prefix "
+                f"caching: its full blocks are reused), Hq={w.Hq}, Hkv={w.Hkv}, D={w.D}, "
+                f"block_size={w.bs}, NB={w.NB}, bf16")
     ctx = np.asarray(w.final_lens) - np.asarray(w.chunks)
     return (f"{w.name}: B={w.B}, chunk={int(w.chunks[0])} tokens per sequence (T={w.T}), "
             f"context {int(ctx.min())}..{int(ctx.max())} cached tokens, Hq={w.Hq}, Hkv={w.Hkv}, "
             f"D={w.D}, block_size={w.bs}, NB={w.NB}, bf16")
 
 
+def prompt_oracle_inputs(w, k_src, v_src):
+    """Oracle pools, tables, lengths and chunk offsets of a prompt workload's step:
+    the oracle's prefix-caching manager serves the warm prompt, releases it, then
+    plans the batch (no GPU data)."""
+    from oracle import cache_ops as oops
+    from oracle.prefix_cache import PrefixCachingBlockManager as OPC
+    bm = OPC(w.NB, w.bs, w.free_order)
+    kp, vp = k_src, v_src
+    for phase, ids, prompts in (("warm", [10 ** 9], w.warm), ("step", list(range(w.B)), w.prompts)):
+        cached, slots, pairs = [], [], []
+        for sid, p in zip(ids, prompts):
+            n = bm.add_seq_prompt(sid, p)
+            cached.append(n)
+            for t in p[n:]:
+                s_, c = bm.append_token(sid, int(t))
+                slots.append(s_)
+                if c is not None:
+                    pairs.append(c)
+        rows = [w.rows(phase, b, int(n), len(p)) for b, (p, n) in enumerate(zip(prompts, cached))]
+        oops.copy_blocks(kp, vp, pairs)
+        oops.reshape_and_cache(torch.cat([r[1] for r in rows]), torch.cat([r[2] for r in rows]),
+                               kp, vp, torch.tensor(slots, dtype=torch.int64), w.bs)
+        if phase == "warm":
+            for sid in ids:
+                bm.free_seq(sid)
+    tables = np.full((w.B, w.max_blocks_per_seq), -1, dtype=np.int64)
+    for i in range(w.B):
+        t = bm.block_table(i)
+        tables[i, :len(t)] = t
+    lens = np.array([bm.seq_len(i) for i in range(w.B)])
+    chunks = [len(p) - n for p, n in zip(w.prompts, cached)]
+    return kp, vp, tables, lens, np.concatenate([[0], np.cumsum(chunks)])
+
+
 def prefill_cpu_inputs(w, cpu):
     q, k_src, v_src, k_new, v_new = cpu
+    if isinstance(w, wl.PromptWorkload):
+        kp, vp, tables, lens, qs = prompt_oracle_inputs(w, k_src, v_src)
+        return (q, kp, vp, 1.0, 1.0), tables, lens, qs
     kp, vp, tables, lens = prefill_oracle_inputs(w, k_src, v_src, k_new, v_new)
-    return (q, kp, vp, 1.0, 1.0), tables, lens
+    return (q, kp, vp, 1.0, 1.0), tables, lens, w.query_start
 
 
 def prefill_main(args, rank, world, device):
     r = run_prefill(args, rank, world, device)
-    w = r["w"]
+    w, plan = r["w"], r["plan"]
     ms = max_over_ranks(r["ms_per_step"], world, device)
     att_ms = max_over_ranks(r["att_ms"], world, device)
     e2e_ms = max_over_ranks(r["e2e_ms"], world, device)
-    fl = prefill_flops(w)
+    fl = prefill_flops(w, plan.lens, plan.chunks)
     peak, kind = load_tensor_peak()
     if rank != 0:
         return
-    inp, tables, lens = prefill_cpu_inputs(w, r["cpu"])
-    extra = {"mode": "prefill", "query_start": w.query_start}
+    inp, tables, lens, qs = prefill_cpu_inputs(w, r["cpu"])
+    extra = {"mode": "prefill", "query_start": qs}
     gf, units, cores, note = oracle_timing(w, inp, tables, lens, 0, args.cpu_budget, 1,
                                            extra=extra)
     att_tf = fl / (att_ms * 1e-3) / 1e12
@@ -659,13 +730,14 @@ def prefill_main(args, rank, world, device):
             "workload": prefill_workload_desc(w),
             "step": ("copy_blocks (CoW pairs: %d) + reshape_and_cache of %d chunk tokens + "
                      "paged_attention_prefill; %d kernel launches per step"
-                     % (r["pairs"], w.T, r["launches_per_step"])),
+                     % (r["pairs"], r["T"], r["launches_per_step"])),
             "l2": "K/V of the step's sequences %.2f GB vs %d MB L2; the chunk's K/V "
                   "(%.0f MB) is rewritten every step" % (
                       float(np.sum(w.final_lens)) * 2 * w.Hkv * w.D * 2 / 1e9, L2_BYTES >> 20,
-                      w.T * 2 * w.Hkv * w.D * 2 / 1e6),
+                      r["T"] * 2 * w.Hkv * w.D * 2 / 1e6),
             "flops_per_step": fl,
-            "chunk_tokens_per_s": round(world * w.T / (ms * 1e-3), 1),
+            "chunk_tokens_per_s": round(world * r["T"] / (ms * 1e-3), 1),
+            **(prompt_stats(w, plan, r, ms, world) if isinstance(w, wl.PromptWorkload) else {}),
             "step_frac_of_peak": round(fl / (ms * 1e-3) / 1e12 / peak, 4),
         },
         "roofline": {
@@ -697,12 +769,18 @@ def run_reference_prefill(args):
     """Reference arm for a chunked-prefill workload: the oracle on the host cores."""
     w = prefill_workload(args)
     k_src, v_src = w.past_pools()
-    q, k_new, v_new = w.step_inputs()
-    inp, tables, lens = prefill_cpu_inputs(w, (q, k_src, v_src, k_new, v_new))
+    if isinstance(w, wl.PromptWorkload):
+        kp, vp, tables, lens, qs = prompt_oracle_inputs(w, k_src, v_src)
+        cached = np.asarray(lens) - np.diff(qs)
+        rows = [w.rows("step", b, int(n), len(p)) for b, (p, n) in enumerate(zip(w.prompts, cached))]
+        inp = (torch.cat([r[0] for r in rows]), kp, vp, 1.0, 1.0)
+    else:
+        q, k_new, v_new = w.step_inputs()
+        inp, tables, lens, qs = prefill_cpu_inputs(w, (q, k_src, v_src, k_new, v_new))
     slice_s = 120.0 / (args.steps + args.warmup)
     gf, units, cores, note = oracle_timing(w, inp, tables, lens, 0, slice_s,
                                            args.warmup + args.steps,
-                                           extra={"mode": "prefill", "query_start": w.query_start})
+                                           extra={"mode": "prefill", "query_start": qs})
     value = float(gf[args.warmup:].mean()) / 1e3
     line = {
         "impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6),
@@ -758,7 +836,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default=DEFAULT_CONFIG,
-                    choices=sorted(wl.CONFIGS) + sorted(wl.PREFILL_CONFIGS))
+                    choices=sorted(wl.CONFIGS) + sorted(wl.PREFILL_CONFIGS) +
+                    sorted(wl.PROMPT_CONFIGS))
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's sequence count (profiling small cases)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -773,7 +852,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        if args.config in wl.PREFILL_CONFIGS:
+        if args.config in wl.PREFILL_CONFIGS or args.config in wl.PROMPT_CONFIGS:
             run_reference_prefill(args)
         else:
             run_reference(args)
@@ -788,7 +867,7 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
 
-    if args.config in wl.PREFILL_CONFIGS:
+    if args.config in wl.PREFILL_CONFIGS or args.config in wl.PROMPT_CONFIGS:
         prefill_main(args, rank, world, device)
         if world > 1:
             torch.distributed.barrier()

@@ -95,7 +95,7 @@ class PrefillPlan:
 
 class PagedKVCache:
     def __init__(self, num_blocks, num_heads, num_kv_heads, head_dim, block_size, kv_dtype,
-                 free_order, device="cuda"):
+                 free_order, device="cuda", prefix_caching=False):
         self.device = torch.device(device)
         self.num_blocks = num_blocks
         self.num_heads = num_heads
@@ -105,7 +105,7 @@ class PagedKVCache:
         k_shape, v_shape = pool_shapes(num_blocks, num_kv_heads, block_size, head_dim, kv_dtype)
         self.k_pool = torch.empty(k_shape, dtype=kv_dtype, device=self.device)
         self.v_pool = torch.empty(v_shape, dtype=kv_dtype, device=self.device)
-        self.bm = BlockManager(num_blocks, block_size, free_order)
+        self.bm = BlockManager(num_blocks, block_size, free_order, prefix_caching=prefix_caching)
 
     def load(self, k_vals, v_vals, k_scale=1.0, v_scale=1.0):
         """Fill every slot from values given as ``[NB, Hkv, bs, D]`` (block,
@@ -175,6 +175,31 @@ class PagedKVCache:
         qs = np.zeros(len(ids) + 1, dtype=np.int32)
         qs[1:] = np.cumsum(chunks)
         return PrefillPlan(ids, chunks, slots, pairs, tables, lens, qs)
+
+    def plan_prompts(self, seq_ids, prompts, max_blocks=None):
+        """Host half of a prefill step with prefix caching (the manager must have
+        it on): each new sequence reuses the cached full blocks of its prompt and
+        the rest of the prompt is its chunk. ``plan.cached[i]`` = prompt tokens of
+        sequence i found in the cache."""
+        ids = np.asarray(seq_ids, dtype=np.int64)
+        cached, slots, pairs = [], [], []
+        for sid, p in zip(ids, prompts):
+            n = self.bm.add_seq_prompt(int(sid), p)
+            s, pr = self.bm.append_tokens(int(sid), np.asarray(p)[n:])
+            cached.append(n)
+            slots.append(s)
+            pairs.append(pr)
+        chunks = np.array([len(p) - n for p, n in zip(prompts, cached)], dtype=np.int64)
+        if max_blocks is None:
+            max_blocks = max(1, max(-(-self.bm.seq_len(int(s)) // self.block_size) for s in ids))
+        tables, lens = self.bm.build_tables(ids, max_blocks)
+        qs = np.zeros(len(ids) + 1, dtype=np.int32)
+        qs[1:] = np.cumsum(chunks)
+        plan = PrefillPlan(ids, chunks, np.concatenate(slots) if slots else np.zeros(0, np.int64),
+                           np.concatenate(pairs).reshape(-1, 2) if pairs else np.zeros((0, 2), np.int64),
+                           tables, lens, qs)
+        plan.cached = np.asarray(cached, dtype=np.int64)
+        return plan
 
     def prefill_step(self, q, k_new, v_new, dev_plan, out, scale, max_query_len, stream=None):
         """Device half of a chunked-prefill step: CoW copies, the chunk's K/V into

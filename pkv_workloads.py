@@ -248,9 +248,82 @@ def prefill_gqa_bf16(B=16, chunk=512):
     return chunked_prefill("prefill_gqa_bf16", 6, ctx, [chunk] * B, 32, 8, 128, 16)
 
 
+@dataclass
+class PromptWorkload:
+    """Requests given as token ids, for prefix caching: the ``warm`` prompts are
+    served first (and released), then every request of ``prompts`` arrives in
+    one batch. q/k/v values are N(0, 1), drawn per (phase, request) for a range
+    of positions; the pool's earlier content is drawn like the other workloads'.
+    """
+    name: str
+    Hq: int
+    Hkv: int
+    D: int
+    bs: int
+    NB: int
+    seed: int
+    scale: float
+    free_order: np.ndarray
+    prompts: list
+    warm: list
+    src_dtype: torch.dtype = torch.bfloat16
+    kv_dtype: str = "bf16"
+
+    @property
+    def B(self):
+        return len(self.prompts)
+
+    @property
+    def final_lens(self):
+        return np.array([len(p) for p in self.prompts], dtype=np.int64)
+
+    @property
+    def max_blocks_per_seq(self):
+        return int(-(-int(self.final_lens.max()) // self.bs))
+
+    def _randn(self, shape, tag):
+        g = torch.Generator().manual_seed(self.seed * 7919 + tag)
+        return torch.randn(*shape, generator=g, dtype=torch.float32).to(self.src_dtype)
+
+    def past_pools(self):
+        shape = (self.NB, self.Hkv, self.bs, self.D)
+        return self._randn(shape, 1), self._randn(shape, 2)
+
+    def rows(self, phase, b, start, stop):
+        """q ``[n, Hq, D]``, k and v ``[n, Hkv, D]`` for positions start..stop-1
+        of request b of ``phase`` ("warm" or "step")."""
+        n = stop - start
+        tag = 1000 + 3 * (b + (0 if phase == "warm" else 100000))
+        q = self._randn((n, self.Hq, self.D), tag)
+        k = self._randn((n, self.Hkv, self.D), tag + 1)
+        v = self._randn((n, self.Hkv, self.D), tag + 2)
+        return q, k, v
+
+
+def system_prompt(B=64, system=1024, suffix=256, Hq=40, Hkv=40, D=128, bs=16, seed=7,
+                  vocab=32000, name="prefill_system_prompt_bf16", suffix_lens=None):
+    """B requests that all begin with one ``system``-token prompt followed by their
+    own ``suffix`` tokens (or ``suffix_lens[b]``); the system prompt alone is
+    served first. Token ids uniform in [0, vocab)."""
+    rng = np.random.default_rng(seed)
+    sys_ids = rng.integers(0, vocab, size=system)
+    sl = [suffix] * B if suffix_lens is None else list(suffix_lens)
+    prompts = [np.concatenate([sys_ids, rng.integers(0, vocab, size=int(n))]) for n in sl]
+    total = -(-system // bs) + sum(-(-(system + int(n)) // bs) for n in sl)
+    NB = _pool_size(total)
+    return PromptWorkload(name=name, Hq=Hq, Hkv=Hkv, D=D, bs=bs, NB=NB, seed=seed,
+                          scale=1.0 / math.sqrt(D), free_order=rng.permutation(NB),
+                          prompts=prompts, warm=[sys_ids.copy()])
+
+
 PREFILL_CONFIGS = {
     "prefill_llama13b_bf16": prefill_llama13b_bf16,
     "prefill_gqa_bf16": prefill_gqa_bf16,
+}
+
+# prefix caching: 64 requests sharing a 1024-token system prompt (LLaMA-13B shape)
+PROMPT_CONFIGS = {
+    "prefill_system_prompt_bf16": system_prompt,
 }
 
 
