@@ -27,6 +27,17 @@ Readings where the pages are silent:
   a sequence's blocks are released in table order;
 * running out of free blocks is an error (``PoolExhausted``), never a silent
   overwrite.
+
+Swapping ("KV cache paginado...", "Como funciona": when physical blocks run out
+the newest requests are preempted, all or nothing, and their blocks recovered by
+swapping them to the CPU or by recomputation). Readings: a second pool of
+``num_cpu_blocks`` host blocks with its own free list (front first, freed blocks
+to the tail); ``swap_out`` moves one sequence whole -- each block of its table,
+in table order, gets a fresh host block and a (device, host) copy pair, and the
+device blocks are released as on ``free_seq``; ``swap_in`` is the reverse with
+(host, device) pairs and fresh device blocks. If either pool cannot take the
+whole sequence nothing changes (``PoolExhausted``). A swapped-out sequence can
+only be swapped in or freed (its host blocks return to the host free list).
 """
 
 
@@ -35,9 +46,10 @@ class PoolExhausted(RuntimeError):
 
 
 class BlockManager:
-    def __init__(self, num_blocks, block_size, free_order):
+    def __init__(self, num_blocks, block_size, free_order, num_cpu_blocks=0):
         """``free_order``: the initially free block ids, front first (blocks not
-        listed belong to someone else and are never handed out)."""
+        listed belong to someone else and are never handed out); host blocks
+        0..num_cpu_blocks-1 start free in that order."""
         free_order = [int(b) for b in free_order]
         if len(set(free_order)) != len(free_order) or any(
                 not 0 <= b < num_blocks for b in free_order):
@@ -48,6 +60,9 @@ class BlockManager:
         self.ref = [0] * num_blocks
         self.tables = {}
         self.lens = {}
+        self.num_cpu_blocks = num_cpu_blocks
+        self.cpu_free = list(range(num_cpu_blocks))
+        self.swapped = set()
 
     def _take(self):
         if not self.free:
@@ -63,12 +78,14 @@ class BlockManager:
         self.lens[sid] = 0
 
     def append_slot(self, sid):
-        """Reserve the slot for the sequence's next token.
+        """Reserve the slot for the sequence's next token (not while swapped out).
 
         Returns ``(slot, cow)`` with ``slot = block * block_size + offset`` and
         ``cow`` either ``None`` or the pair ``(src, dst)`` of a block copy that
         must happen before the token is written.
         """
+        if sid in self.swapped:
+            raise ValueError("sequence is swapped out")
         table = self.tables[sid]
         n = self.lens[sid]
         cow = None
@@ -90,17 +107,60 @@ class BlockManager:
         """Child shares every block of the parent; counts go up by one."""
         if child in self.tables:
             raise ValueError("sequence exists")
+        if parent in self.swapped:
+            raise ValueError("sequence is swapped out")
         self.tables[child] = list(self.tables[parent])
         self.lens[child] = self.lens[parent]
         for b in self.tables[child]:
             self.ref[b] += 1
 
-    def free_seq(self, sid):
-        for b in self.tables.pop(sid):
+    def _release(self, table):
+        """Drop one reference to each device block of ``table``, in order."""
+        for b in table:
             self.ref[b] -= 1
             if self.ref[b] == 0:
                 self.free.append(b)
+
+    def _device_blocks_available(self):
+        return len(self.free)
+
+    def free_seq(self, sid):
+        table = self.tables.pop(sid)
+        if sid in self.swapped:
+            self.swapped.discard(sid)
+            self.cpu_free.extend(table)
+        else:
+            self._release(table)
         del self.lens[sid]
+
+    def swap_out(self, sid):
+        """Move the sequence's blocks to the host pool; returns the (device,
+        host) copy pairs, in table order."""
+        if sid in self.swapped:
+            raise ValueError("sequence is swapped out")
+        table = self.tables[sid]
+        if len(table) > len(self.cpu_free):
+            raise PoolExhausted("host pool cannot take the sequence")
+        host = [self.cpu_free.pop(0) for _ in table]
+        pairs = list(zip(table, host))
+        self._release(table)
+        self.tables[sid] = host
+        self.swapped.add(sid)
+        return pairs
+
+    def swap_in(self, sid):
+        """Move a swapped-out sequence back to fresh device blocks; returns the
+        (host, device) copy pairs, in table order."""
+        if sid not in self.swapped:
+            raise ValueError("sequence is not swapped out")
+        host = self.tables[sid]
+        if len(host) > self._device_blocks_available():
+            raise PoolExhausted("device pool cannot take the sequence")
+        dev = [self._take() for _ in host]
+        self.tables[sid] = dev
+        self.swapped.discard(sid)
+        self.cpu_free.extend(host)
+        return list(zip(host, dev))
 
     def block_table(self, sid):
         return list(self.tables[sid])

@@ -34,8 +34,8 @@ from .block_manager import BlockManager, PoolExhausted
 
 
 class PrefixCachingBlockManager(BlockManager):
-    def __init__(self, num_blocks, block_size, free_order):
-        super().__init__(num_blocks, block_size, free_order)
+    def __init__(self, num_blocks, block_size, free_order, num_cpu_blocks=0):
+        super().__init__(num_blocks, block_size, free_order, num_cpu_blocks)
         self.tokens = {}          # sid -> token ids (None where unknown)
         self.key_of = {}          # registered block -> its prefix (tuple of ids)
         self.block_of = {}        # prefix -> registered block
@@ -106,8 +106,7 @@ class PrefixCachingBlockManager(BlockManager):
         super().fork(parent, child)
         self.tokens[child] = list(self.tokens[parent])
 
-    def free_seq(self, sid):
-        table = self.tables.pop(sid)
+    def _release(self, table):
         cached = []
         for b in table:
             self.ref[b] -= 1
@@ -117,7 +116,12 @@ class PrefixCachingBlockManager(BlockManager):
                 else:
                     self.free.append(b)
         self.evictable.extend(reversed(cached))
-        del self.lens[sid]
+
+    def _device_blocks_available(self):
+        return len(self.free) + len(self.evictable)
+
+    def free_seq(self, sid):
+        super().free_seq(sid)
         del self.tokens[sid]
 
     def num_evictable(self):

@@ -677,3 +677,139 @@ def test_prefix_cache_random_scripts_keep_content_and_count_invariants():
             except PoolExhausted:
                 break
             pc_check(bm, sh, live)
+
+
+# ---------------------------------------------------------------- swapping to host memory
+class Shadow2:
+    """Slot contents of the device pool and of the host pool."""
+
+    def __init__(self, nb, ncpu, bs):
+        self.dev, self.host = Shadow(nb, bs), Shadow(ncpu, bs)
+
+    def swap(self, pairs, to_host):
+        bs = self.dev.bs
+        src, dst = (self.dev, self.host) if to_host else (self.host, self.dev)
+        for a, b in pairs:
+            dst.slot[b * bs:(b + 1) * bs] = src.slot[a * bs:(a + 1) * bs]
+
+
+def swap_check(bm, sh, live):
+    for sid in live:
+        pool = sh.host if sid in bm.swapped else sh.dev
+        assert pool.gather(bm.tables[sid], bm.lens[sid]) == bm.tokens[sid]
+    host_used = [b for sid in bm.swapped for b in bm.tables[sid]]
+    assert len(host_used) == len(set(host_used))
+    assert sorted(host_used + bm.cpu_free) == list(range(bm.num_cpu_blocks))
+    refs = [0] * bm.num_blocks
+    for sid in live:
+        if sid not in bm.swapped:
+            for b in bm.tables[sid]:
+                refs[b] += 1
+    assert refs == bm.ref
+
+
+def test_swap_round_trip_preserves_content_while_device_blocks_are_reused():
+    bs = 4
+    bm = PrefixCachingBlockManager(6, bs, range(6), num_cpu_blocks=4)
+    sh = Shadow2(6, 4, bs)
+    bm.add_seq("a")
+    for t in range(10):                                # 3 blocks
+        slot, _ = bm.append_token("a", t)
+        sh.dev.write(slot, t)
+    dev_table = bm.block_table("a")
+    pairs = bm.swap_out("a")
+    assert pairs == list(zip(dev_table, [0, 1, 2])) and bm.block_table("a") == [0, 1, 2]
+    sh.swap(pairs, to_host=True)
+    bm.add_seq("b")                                    # b takes the freed device blocks
+    for t in range(100, 124):
+        slot, _ = bm.append_token("b", t)
+        sh.dev.write(slot, t)
+    swap_check(bm, sh, ["a", "b"])
+    with pytest.raises(PoolExhausted):                 # all or nothing: device pool is full
+        bm.swap_in("a")
+    swap_check(bm, sh, ["a", "b"])
+    bm.free_seq("b")
+    pairs = bm.swap_in("a")
+    sh.swap(pairs, to_host=False)
+    assert [h for h, _ in pairs] == [0, 1, 2] and bm.cpu_free == [3, 0, 1, 2]
+    swap_check(bm, sh, ["a"])
+    for t in range(10, 14):                            # and it keeps growing
+        slot, _ = bm.append_token("a", t)
+        sh.dev.write(slot, t)
+    swap_check(bm, sh, ["a"])
+
+
+def test_swap_out_is_all_or_nothing_and_a_swapped_sequence_is_frozen():
+    bm = BlockManager(8, 2, range(8), num_cpu_blocks=2)
+    bm.add_seq(0)
+    for _ in range(5):                                 # 3 blocks
+        bm.append_slot(0)
+    before = (list(bm.free), list(bm.cpu_free), bm.block_table(0))
+    with pytest.raises(PoolExhausted):
+        bm.swap_out(0)
+    assert (list(bm.free), list(bm.cpu_free), bm.block_table(0)) == before
+    bm2 = BlockManager(8, 2, range(8), num_cpu_blocks=4)
+    bm2.add_seq(0)
+    bm2.append_slot(0)
+    bm2.swap_out(0)
+    with pytest.raises(ValueError):
+        bm2.append_slot(0)
+    with pytest.raises(ValueError):
+        bm2.fork(0, 1)
+    bm2.free_seq(0)
+    assert sorted(bm2.cpu_free) == [0, 1, 2, 3] and bm2.num_free() == 8
+
+
+@pytest.mark.parametrize("caching", [False, True])
+def test_swap_random_scripts_keep_content_and_partitions(caching):
+    bs = 4
+    rng = np.random.default_rng(21 + caching)
+    for trial in range(25):
+        nb, ncpu = 30, 20
+        bm = PrefixCachingBlockManager(nb, bs, list(rng.permutation(nb)), ncpu)
+        sh = Shadow2(nb, ncpu, bs)
+        live, nxt = [], 0
+        for step in range(80):
+            op = int(rng.integers(0, 6))
+            try:
+                resident = [s for s in live if s not in bm.swapped]
+                if op == 0 or not live:
+                    p = list(rng.integers(0, 3, size=rng.integers(1, 14)))
+                    if not caching:                    # ids of one sequence only: no hits
+                        p = [t + 10 * (nxt + 1) for t in p]
+                    sid = nxt
+                    nxt += 1
+                    n = bm.add_seq_prompt(sid, p)
+                    live.append(sid)
+                    for t in p[n:]:
+                        slot, cow = bm.append_token(sid, int(t))
+                        if cow:
+                            sh.dev.copy(*cow)
+                        sh.dev.write(slot, int(t))
+                elif op == 1 and resident:
+                    sid = resident[rng.integers(len(resident))]
+                    t = int(rng.integers(0, 3)) + (0 if caching else 10 * (sid + 1))
+                    slot, cow = bm.append_token(sid, t)
+                    if cow:
+                        sh.dev.copy(*cow)
+                    sh.dev.write(slot, t)
+                elif op == 2 and resident:
+                    sid = resident[rng.integers(len(resident))]
+                    bm.fork(sid, nxt)
+                    live.append(nxt)
+                    nxt += 1
+                elif op == 3 and resident:
+                    sid = resident[rng.integers(len(resident))]
+                    sh.swap(bm.swap_out(sid), to_host=True)
+                elif op == 4 and bm.swapped:
+                    sid = sorted(bm.swapped)[rng.integers(len(bm.swapped))]
+                    sh.swap(bm.swap_in(sid), to_host=False)
+                elif op == 5:
+                    sid = live.pop(rng.integers(len(live)))
+                    bm.free_seq(sid)
+            except PoolExhausted:
+                pass                                   # all or nothing: state unchanged
+            swap_check(bm, sh, live)
+
+            if not caching:
+                assert bm.hit_blocks == 0
