@@ -273,6 +273,30 @@ PKV_API int paged_attention_prefill(void* out, const void* q,
                             float scale, int q_dtype, int kv_dtype, void* stream);
 
 /* ------------------------------------------------------------------------
+ * swap_blocks -- copy whole blocks between two pools, e.g. a device pool and a
+ * pinned host pool of the same layout, for preemption by swapping
+ * ("KV cache paginado e batching contínuo para LLMs", "Como funciona": when
+ * physical blocks run out the newest requests are preempted and their blocks
+ * swapped to the CPU). For every pair i:
+ *     dst_pool[src_dst_pairs[2i+1]] = src_pool[src_dst_pairs[2i]]   (K and V)
+ *   dst_k_pool/dst_v_pool, src_k_pool/src_v_pool: device memory or pinned host
+ *                 memory (cudaHostAlloc / cudaHostRegister; the device reaches
+ *                 it through its mapped address); anything else is
+ *                 PKV_ERR_INVALID_ARG. 16-byte aligned.
+ *   src_dst_pairs int64 [num_pairs][2], device or pinned host memory; the
+ *                 destinations must be distinct and not also sources
+ *   src_num_blocks/dst_num_blocks  bounds of the two pools
+ *   block_bytes   bytes of one block in one pool (num_kv_heads*block_size*
+ *                 head_dim*elt), a multiple of 16
+ * A pair outside either pool is skipped and sets PKV_ERR_OUT_OF_RANGE in the
+ * device error word. Asynchronous on `stream`.
+ * ---------------------------------------------------------------------- */
+PKV_API int swap_blocks(void* dst_k_pool, void* dst_v_pool, const void* src_k_pool,
+                        const void* src_v_pool, const int64_t* src_dst_pairs, int num_pairs,
+                        int src_num_blocks, int dst_num_blocks, size_t block_bytes,
+                        void* stream);
+
+/* ------------------------------------------------------------------------
  * paged_attention_decode_noalloc -- paged_attention_decode for callers that
  * cannot allocate device memory where they decode (e.g. a plug-in inside a
  * runtime that owns all device memory, or a serving loop whose memory plan is
@@ -338,7 +362,7 @@ PKV_API void bm_destroy(pkv_block_manager* bm);
 
 PKV_API int bm_add_seq(pkv_block_manager* bm, int64_t seq_id);
 /* Reserve the next token's slot: *slot = block*block_size + offset. If a
- * copy-on-write is needed *cow_src/*cow_dst get the pair, else both are -1.
+ * copy-on-write is needed *cow_src and *cow_dst get the pair, else both are -1.
  * PKV_ERR_POOL_EXHAUSTED leaves the manager unchanged. */
 PKV_API int bm_append_slot(pkv_block_manager* bm, int64_t seq_id, int64_t* slot,
                    int32_t* cow_src, int32_t* cow_dst);
@@ -408,6 +432,27 @@ PKV_API int bm_append_tokens(pkv_block_manager* bm, int64_t seq_id, const int32_
 PKV_API int bm_cache_stats(const pkv_block_manager* bm, int64_t* hit_blocks,
                            int64_t* lookup_blocks, int* num_cached, int* num_evictable);
 PKV_API int bm_evictable_list(const pkv_block_manager* bm, int32_t* out, int cap);
+
+/* Swapping to a host block pool ("KV cache paginado...", "Como funciona":
+ * preempted requests, all or nothing, swapped to the CPU).
+ * bm_set_host_blocks: give the manager host blocks 0..n-1 (only before any
+ *   sequence exists).
+ * bm_swap_out: move seq_id to host blocks: pairs[i] = (device block, host block)
+ *   for each table entry in order (*num_pairs of them; cap must hold them);
+ *   its device blocks are released as by bm_free_seq. PKV_ERR_POOL_EXHAUSTED
+ *   (nothing changed) if the host pool cannot take the whole sequence.
+ * bm_swap_in: the reverse onto fresh device blocks, pairs = (host, device);
+ *   PKV_ERR_POOL_EXHAUSTED if the device pool (free plus evictable blocks)
+ *   cannot take it. A swapped-out sequence cannot be appended to, forked or put
+ *   in a batch (PKV_ERR_INVALID_ARG); bm_free_seq returns its host blocks.
+ * bm_is_swapped, bm_host_free_list: state queries. */
+PKV_API int bm_set_host_blocks(pkv_block_manager* bm, int num_host_blocks);
+PKV_API int bm_swap_out(pkv_block_manager* bm, int64_t seq_id, int64_t* pairs, int cap,
+                        int* num_pairs);
+PKV_API int bm_swap_in(pkv_block_manager* bm, int64_t seq_id, int64_t* pairs, int cap,
+                       int* num_pairs);
+PKV_API int bm_is_swapped(const pkv_block_manager* bm, int64_t seq_id, int* swapped);
+PKV_API int bm_host_free_list(const pkv_block_manager* bm, int32_t* out, int cap);
 
 /* The free list, front first, into out[0..cap); returns its length. */
 PKV_API int bm_free_list(const pkv_block_manager* bm, int32_t* out, int cap);

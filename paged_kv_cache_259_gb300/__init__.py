@@ -24,7 +24,7 @@ import torch
 __all__ = [
     "PagedKVError", "paged_attention_decode", "paged_attention_workspace_size",
     "paged_attention_decode_noalloc", "NOALLOC_WORKSPACE_BYTES", "paged_attention_decode_grouped",
-    "paged_attention_prefill",
+    "paged_attention_prefill", "swap_blocks",
     "reshape_and_cache", "copy_blocks", "get_device_error", "kernel_launches", "BlockManager",
     "library_path", "load_library", "pool_shapes", "pool_views", "pools_from_views", "PKV_F32",
     "PKV_BF16", "PKV_E4M3",
@@ -101,6 +101,12 @@ def load_library():
         "bm_num_free": (c_int, [vp]),
         "bm_free_list": (c_int, [vp, i32p, c_int]),
         "bm_enable_prefix_caching": (c_int, [vp]),
+        "bm_set_host_blocks": (c_int, [vp, c_int]),
+        "bm_swap_out": (c_int, [vp, ctypes.c_int64, i64p, c_int, ip]),
+        "bm_swap_in": (c_int, [vp, ctypes.c_int64, i64p, c_int, ip]),
+        "bm_is_swapped": (c_int, [vp, ctypes.c_int64, ip]),
+        "bm_host_free_list": (c_int, [vp, i32p, c_int]),
+        "swap_blocks": (c_int, [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_size, vp]),
         "bm_add_seq_prompt": (c_int, [vp, ctypes.c_int64, i32p, c_int, ip]),
         "bm_append_tokens": (c_int, [vp, ctypes.c_int64, i32p, c_int, i64p, i64p, c_int, ip]),
         "bm_cache_stats": (c_int, [vp, i64p, i64p, ip, ip]),
@@ -410,6 +416,31 @@ def copy_blocks(k_pool, v_pool, src_dst_pairs, stream=None):
     _check(st, "copy_blocks")
 
 
+def swap_blocks(dst_k_pool, dst_v_pool, src_k_pool, src_v_pool, src_dst_pairs, stream=None):
+    """``dst_pool[d] = src_pool[s]`` for every (s, d) pair, K and V; each pool is a
+    CUDA tensor or a pinned CPU tensor (``pin_memory()``) in the library layout."""
+    lib = load_library()
+    for t, n in ((dst_k_pool, "dst_k_pool"), (dst_v_pool, "dst_v_pool"),
+                 (src_k_pool, "src_k_pool"), (src_v_pool, "src_v_pool")):
+        if not t.is_contiguous() or (not t.is_cuda and not t.is_pinned()):
+            raise ValueError(f"{n} must be a contiguous CUDA or pinned CPU tensor")
+    if src_dst_pairs.dtype != torch.int64 or not src_dst_pairs.is_contiguous() or \
+            (not src_dst_pairs.is_cuda and not src_dst_pairs.is_pinned()):
+        raise TypeError("src_dst_pairs must be contiguous int64, on the GPU or pinned")
+    NBd, Hkv, bs, D = _pool_dims(dst_k_pool, dst_v_pool)
+    NBs, Hkv2, bs2, D2 = _pool_dims(src_k_pool, src_v_pool)
+    if (Hkv, bs, D) != (Hkv2, bs2, D2) or dst_k_pool.dtype != src_k_pool.dtype:
+        raise ValueError("pools of different layouts")
+    block_bytes = Hkv * bs * D * dst_k_pool.element_size()
+    dev = dst_k_pool.device if dst_k_pool.is_cuda else src_k_pool.device
+    with _on_device(dev):
+        st = lib.swap_blocks(dst_k_pool.data_ptr(), dst_v_pool.data_ptr(), src_k_pool.data_ptr(),
+                             src_v_pool.data_ptr(), src_dst_pairs.data_ptr(),
+                             src_dst_pairs.shape[0], NBs, NBd, block_bytes,
+                             _stream_ptr(stream, dev))
+    _check(st, "swap_blocks")
+
+
 def kernel_launches():
     """Kernels this library has launched in this process so far."""
     return int(load_library().pkv_kernel_launches())
@@ -437,7 +468,8 @@ def _i64p(a):
 class BlockManager:
     """Host block manager of the C library (free list front-first, refcounts, CoW)."""
 
-    def __init__(self, num_blocks, block_size, free_order, prefix_caching=False):
+    def __init__(self, num_blocks, block_size, free_order, prefix_caching=False,
+                 num_host_blocks=0):
         self._lib = load_library()
         fo = np.ascontiguousarray(np.asarray(free_order, dtype=np.int32))
         h = self._lib.bm_create(num_blocks, block_size, _i32p(fo), len(fo))
@@ -449,6 +481,9 @@ class BlockManager:
         self.prefix_caching = bool(prefix_caching)
         if prefix_caching:
             _check(self._lib.bm_enable_prefix_caching(self._h), "bm_enable_prefix_caching")
+        self.num_host_blocks = int(num_host_blocks)
+        if num_host_blocks:
+            _check(self._lib.bm_set_host_blocks(self._h, int(num_host_blocks)), "bm_set_host_blocks")
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -573,6 +608,37 @@ class BlockManager:
         _check(self._lib.bm_cache_stats(self._h, ctypes.byref(h), ctypes.byref(l), ctypes.byref(c),
                                         ctypes.byref(e)), "bm_cache_stats")
         return h.value, l.value, c.value, e.value
+
+    # ---- swapping to host blocks (BlockManager(..., num_host_blocks=n))
+    def _swap(self, fn, sid, what):
+        n = ctypes.c_int(0)
+        st = fn(self._h, sid, None, 0, ctypes.byref(n))
+        if st == 0:                                      # a sequence without blocks
+            return np.zeros((0, 2), dtype=np.int64)
+        if st != -1 or n.value == 0:
+            _check(st, what)
+        pairs = np.zeros((max(1, n.value), 2), dtype=np.int64)
+        _check(fn(self._h, sid, _i64p(pairs), n.value, ctypes.byref(n)), what)
+        return pairs[:n.value].copy()
+
+    def swap_out(self, sid):
+        """Move the sequence to host blocks; returns (device, host) pairs [n, 2]."""
+        return self._swap(self._lib.bm_swap_out, sid, "bm_swap_out")
+
+    def swap_in(self, sid):
+        """Move a swapped-out sequence back; returns (host, device) pairs [n, 2]."""
+        return self._swap(self._lib.bm_swap_in, sid, "bm_swap_in")
+
+    def is_swapped(self, sid):
+        f = ctypes.c_int(0)
+        _check(self._lib.bm_is_swapped(self._h, sid, ctypes.byref(f)), "bm_is_swapped")
+        return bool(f.value)
+
+    def host_free_list(self):
+        n = self._lib.bm_host_free_list(self._h, None, 0)
+        out = np.zeros(max(1, n), dtype=np.int32)
+        self._lib.bm_host_free_list(self._h, _i32p(out), len(out))
+        return [int(x) for x in out[:n]]
 
     def evictable_list(self):
         n = self._lib.bm_evictable_list(self._h, None, 0)

@@ -27,6 +27,15 @@
 // evictable list in reverse table order. The index is a 64-bit hash of the whole
 // prefix (chained block by block); a hit also compares the block's own token
 // ids and the hash of the prefix before it.
+//
+// Swapping ("KV cache paginado...", "Como funciona": when physical blocks run
+// out the newest requests are preempted, all or nothing, and their blocks
+// recovered by swapping to the CPU or by recomputation): a host pool of blocks
+// with its own free list; swapping a sequence out gives each block of its table,
+// in order, a fresh host block and a (device, host) copy pair and releases the
+// device blocks as a free does; swapping in is the reverse onto fresh device
+// blocks. Either is refused, changing nothing, if the receiving pool cannot take
+// the whole sequence. A swapped-out sequence can only be swapped in or freed.
 #include <algorithm>
 #include <climits>
 #include <cstdint>
@@ -71,6 +80,7 @@ struct pkv_block_manager {
         int64_t len = 0;                 // tokens cached
         std::vector<int64_t> tokens;     // token ids (prefix caching only)
         std::vector<uint64_t> hashes;    // prefix hash after each full block
+        bool swapped = false;            // table holds host blocks
     };
     std::unordered_map<int64_t, Seq> seqs;
 
@@ -84,6 +94,34 @@ struct pkv_block_manager {
     std::vector<std::list<int32_t>::iterator> ev_pos;
     std::vector<char> in_ev;
     int64_t hit_blocks = 0, lookup_blocks = 0;
+
+    // ---- host pool (swapping)
+    int num_host_blocks = 0;
+    std::deque<int32_t> host_free;                   // front = next host block
+
+    size_t device_available() const {
+        return free_list.size() + (caching ? evictable.size() : 0);
+    }
+
+    // Drop one reference to each device block of `table`: uncached blocks that
+    // reach 0 go to the free list in table order, cached ones to the evictable
+    // list in reverse table order.
+    void release(const std::vector<int32_t>& table) {
+        std::vector<int32_t> cached;
+        for (int32_t b : table) {
+            ref[b] -= 1;
+            if (ref[b] == 0) {
+                if (caching && registered[b])
+                    cached.push_back(b);
+                else
+                    free_list.push_back(b);
+            }
+        }
+        for (auto r = cached.rbegin(); r != cached.rend(); ++r) {
+            ev_pos[*r] = evictable.insert(evictable.end(), *r);
+            in_ev[*r] = 1;
+        }
+    }
 
     bool can_take() const { return !free_list.empty() || (caching && !evictable.empty()); }
 
@@ -152,6 +190,7 @@ struct pkv_block_manager {
     int append(Seq& s, int64_t token, int64_t* slot, int32_t* cow_src, int32_t* cow_dst) {
         *cow_src = -1;
         *cow_dst = -1;
+        if (s.swapped) return PKV_ERR_INVALID_ARG;
         const int64_t n = s.len;
         if (n % block_size == 0) {
             if (!can_take()) return PKV_ERR_POOL_EXHAUSTED;
@@ -269,7 +308,7 @@ int bm_fork(pkv_block_manager* bm, int64_t parent, int64_t child) {
     if (!bm) return PKV_ERR_INVALID_ARG;
     auto it = bm->seqs.find(parent);
     if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
-    if (bm->seqs.count(child)) return PKV_ERR_INVALID_ARG;
+    if (bm->seqs.count(child) || it->second.swapped) return PKV_ERR_INVALID_ARG;
     pkv_block_manager::Seq c = it->second;    // copy of the parent's table
     for (int32_t b : c.table) bm->ref[b] += 1;
     bm->seqs.emplace(child, std::move(c));
@@ -280,19 +319,10 @@ int bm_free_seq(pkv_block_manager* bm, int64_t seq_id) {
     if (!bm) return PKV_ERR_INVALID_ARG;
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
-    std::vector<int32_t> cached;
-    for (int32_t b : it->second.table) {
-        bm->ref[b] -= 1;
-        if (bm->ref[b] == 0) {
-            if (bm->caching && bm->registered[b])
-                cached.push_back(b);
-            else
-                bm->free_list.push_back(b);
-        }
-    }
-    for (auto r = cached.rbegin(); r != cached.rend(); ++r) {
-        bm->ev_pos[*r] = bm->evictable.insert(bm->evictable.end(), *r);
-        bm->in_ev[*r] = 1;
+    if (it->second.swapped) {
+        for (int32_t b : it->second.table) bm->host_free.push_back(b);
+    } else {
+        bm->release(it->second.table);
     }
     bm->seqs.erase(it);
     return PKV_OK;
@@ -317,7 +347,8 @@ int bm_build_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int n, 
         auto it = bm->seqs.find(seq_ids[i]);
         if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
         const auto& s = it->second;
-        if ((int64_t)s.table.size() > max_blocks || s.len > INT32_MAX) return PKV_ERR_INVALID_ARG;
+        if ((int64_t)s.table.size() > max_blocks || s.len > INT32_MAX || s.swapped)
+            return PKV_ERR_INVALID_ARG;
         int32_t* row = tables + (size_t)i * max_blocks;
         for (int j = 0; j < max_blocks; ++j) row[j] = j < (int)s.table.size() ? s.table[j] : -1;
         seq_lens[i] = (int32_t)s.len;
@@ -357,6 +388,7 @@ int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
     for (int i = 0; i < n; ++i) {
         auto it = bm->seqs.find(seq_ids[i]);
         if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
+        if (it->second.swapped) return PKV_ERR_INVALID_ARG;
         seqs[i] = &it->second;
         seq_group[i] = -1;
     }
@@ -481,6 +513,73 @@ int bm_evictable_list(const pkv_block_manager* bm, int32_t* out, int cap) {
     if (!bm) return -1;
     int i = 0;
     for (int32_t b : bm->evictable) {
+        if (i < cap && out) out[i] = b;
+        ++i;
+    }
+    return i;
+}
+
+int bm_set_host_blocks(pkv_block_manager* bm, int num_host_blocks) {
+    if (!bm || num_host_blocks < 0 || !bm->seqs.empty()) return PKV_ERR_INVALID_ARG;
+    bm->num_host_blocks = num_host_blocks;
+    bm->host_free.clear();
+    for (int i = 0; i < num_host_blocks; ++i) bm->host_free.push_back(i);
+    return PKV_OK;
+}
+
+int bm_swap_out(pkv_block_manager* bm, int64_t seq_id, int64_t* pairs, int cap, int* num_pairs) {
+    if (!bm || !num_pairs || (cap > 0 && !pairs)) return PKV_ERR_INVALID_ARG;
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
+    auto& s = it->second;
+    *num_pairs = (int)s.table.size();
+    if (s.swapped || cap < (int)s.table.size()) return PKV_ERR_INVALID_ARG;
+    if (s.table.size() > bm->host_free.size()) return PKV_ERR_POOL_EXHAUSTED;
+    std::vector<int32_t> host(s.table.size());
+    for (size_t i = 0; i < host.size(); ++i) {
+        host[i] = bm->host_free.front();
+        bm->host_free.pop_front();
+        pairs[2 * i] = s.table[i];
+        pairs[2 * i + 1] = host[i];
+    }
+    bm->release(s.table);
+    s.table = std::move(host);
+    s.swapped = true;
+    return PKV_OK;
+}
+
+int bm_swap_in(pkv_block_manager* bm, int64_t seq_id, int64_t* pairs, int cap, int* num_pairs) {
+    if (!bm || !num_pairs || (cap > 0 && !pairs)) return PKV_ERR_INVALID_ARG;
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
+    auto& s = it->second;
+    *num_pairs = (int)s.table.size();
+    if (!s.swapped || cap < (int)s.table.size()) return PKV_ERR_INVALID_ARG;
+    if (s.table.size() > bm->device_available()) return PKV_ERR_POOL_EXHAUSTED;
+    for (size_t i = 0; i < s.table.size(); ++i) {
+        const int32_t h = s.table[i];
+        const int32_t d = bm->take();
+        pairs[2 * i] = h;
+        pairs[2 * i + 1] = d;
+        s.table[i] = d;
+        bm->host_free.push_back(h);
+    }
+    s.swapped = false;
+    return PKV_OK;
+}
+
+int bm_is_swapped(const pkv_block_manager* bm, int64_t seq_id, int* swapped) {
+    if (!bm || !swapped) return PKV_ERR_INVALID_ARG;
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
+    *swapped = it->second.swapped ? 1 : 0;
+    return PKV_OK;
+}
+
+int bm_host_free_list(const pkv_block_manager* bm, int32_t* out, int cap) {
+    if (!bm) return -1;
+    int i = 0;
+    for (int32_t b : bm->host_free) {
         if (i < cap && out) out[i] = b;
         ++i;
     }

@@ -234,6 +234,52 @@ cudaError_t launch_reshape(const void* k, const void* v, void* kp, void* vp, con
     return cudaGetLastError();
 }
 
+// Block copies between two pools (device or pinned host memory, both reached by
+// the kernel through the device's own addresses: host memory over the CPU-GPU
+// link). One CTA per (pair, pool, 16 KB chunk), 16-byte vector copies. A pair
+// outside either pool is skipped and flagged.
+__global__ void __launch_bounds__(kCopyThreads) swap_blocks_kernel(
+    char* __restrict__ dst_k, char* __restrict__ dst_v, const char* __restrict__ src_k,
+    const char* __restrict__ src_v, const int64_t* __restrict__ pairs, int src_blocks,
+    int dst_blocks, size_t block_bytes, int* err) {
+    const int pair = blockIdx.x >> 1;
+    const bool is_v = blockIdx.x & 1;
+    const int64_t src = pairs[2 * pair], dst = pairs[2 * pair + 1];
+    if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+        if (threadIdx.x == 0 && blockIdx.y == 0 && !is_v) flag_error(err, kErrOutOfRange);
+        return;
+    }
+    const uint4* s = reinterpret_cast<const uint4*>((is_v ? src_v : src_k) + (size_t)src * block_bytes);
+    uint4* o = reinterpret_cast<uint4*>((is_v ? dst_v : dst_k) + (size_t)dst * block_bytes);
+    const size_t n16 = block_bytes / 16;
+    const size_t beg = (size_t)blockIdx.y * (kCopyChunkBytes / 16);
+    const size_t end = min(n16, beg + kCopyChunkBytes / 16);
+    uint4 buf[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const size_t i = beg + threadIdx.x + (size_t)u * kCopyThreads;
+        if (i < end) buf[u] = s[i];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const size_t i = beg + threadIdx.x + (size_t)u * kCopyThreads;
+        if (i < end) o[i] = buf[u];
+    }
+}
+
+// The address the device uses for a pool: itself for device memory, the mapped
+// address for pinned host memory; nullptr for memory the device cannot reach.
+void* device_address(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return const_cast<void*>(p);
+    if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+    return nullptr;
+}
+
 // Batches this large (a prefill chunk) go through the window kernel; smaller
 // ones (a decode step: one token per sequence, no runs) skip its window checks.
 constexpr int kGroupTokens = 512;
@@ -326,6 +372,39 @@ int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs, int nu
         block_bytes, err);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_fail("copy_blocks: kernel launch", e);
+}
+
+int swap_blocks(void* dst_k_pool, void* dst_v_pool, const void* src_k_pool,
+                const void* src_v_pool, const int64_t* src_dst_pairs, int num_pairs,
+                int src_num_blocks, int dst_num_blocks, size_t block_bytes, void* stream) {
+    using namespace pkv;
+    if (num_pairs < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0 || block_bytes == 0 ||
+        block_bytes % 16 != 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PKV_OK;
+    if (!dst_k_pool || !dst_v_pool || !src_k_pool || !src_v_pool || !src_dst_pairs)
+        return PKV_ERR_INVALID_ARG;
+    if (num_pairs > (1 << 30) || block_bytes / kCopyChunkBytes >= 65535)
+        return PKV_ERR_UNSUPPORTED;
+    void* dk = device_address(dst_k_pool);
+    void* dv = device_address(dst_v_pool);
+    const void* sk = device_address(src_k_pool);
+    const void* sv = device_address(src_v_pool);
+    const void* pp = device_address(src_dst_pairs);
+    if (!dk || !dv || !sk || !sv || !pp) return PKV_ERR_INVALID_ARG;   // unreachable memory
+    if (!aligned16(dk) || !aligned16(dv) || !aligned16(sk) || !aligned16(sv))
+        return PKV_ERR_INVALID_ARG;
+    int* err = error_word();
+    if (!err) return PKV_ERR_CUDA;
+    const unsigned chunks = (unsigned)((block_bytes + kCopyChunkBytes - 1) / kCopyChunkBytes);
+    dim3 grid(2u * (unsigned)num_pairs, chunks);
+    note_launch();
+    swap_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<char*>(dk), static_cast<char*>(dv), static_cast<const char*>(sk),
+        static_cast<const char*>(sv), static_cast<const int64_t*>(pp), src_num_blocks,
+        dst_num_blocks, block_bytes, err);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PKV_OK : cuda_fail("swap_blocks: kernel launch", e);
 }
 
 }  // extern "C"

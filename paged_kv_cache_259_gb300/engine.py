@@ -22,7 +22,7 @@ import torch
 
 from . import (BlockManager, copy_blocks, paged_attention_decode, paged_attention_decode_grouped,
                paged_attention_prefill, paged_attention_workspace_size, pool_shapes,
-               pool_views, reshape_and_cache)
+               pool_views, reshape_and_cache, swap_blocks)
 
 
 @dataclass
@@ -95,7 +95,7 @@ class PrefillPlan:
 
 class PagedKVCache:
     def __init__(self, num_blocks, num_heads, num_kv_heads, head_dim, block_size, kv_dtype,
-                 free_order, device="cuda", prefix_caching=False):
+                 free_order, device="cuda", prefix_caching=False, num_host_blocks=0):
         self.device = torch.device(device)
         self.num_blocks = num_blocks
         self.num_heads = num_heads
@@ -105,7 +105,13 @@ class PagedKVCache:
         k_shape, v_shape = pool_shapes(num_blocks, num_kv_heads, block_size, head_dim, kv_dtype)
         self.k_pool = torch.empty(k_shape, dtype=kv_dtype, device=self.device)
         self.v_pool = torch.empty(v_shape, dtype=kv_dtype, device=self.device)
-        self.bm = BlockManager(num_blocks, block_size, free_order, prefix_caching=prefix_caching)
+        self.bm = BlockManager(num_blocks, block_size, free_order, prefix_caching=prefix_caching,
+                               num_host_blocks=num_host_blocks)
+        self.num_host_blocks = num_host_blocks
+        if num_host_blocks:
+            hk, hv = pool_shapes(num_host_blocks, num_kv_heads, block_size, head_dim, kv_dtype)
+            self.host_k = torch.empty(hk, dtype=kv_dtype).pin_memory()
+            self.host_v = torch.empty(hv, dtype=kv_dtype).pin_memory()
 
     def load(self, k_vals, v_vals, k_scale=1.0, v_scale=1.0):
         """Fill every slot from values given as ``[NB, Hkv, bs, D]`` (block,
@@ -175,6 +181,26 @@ class PagedKVCache:
         qs = np.zeros(len(ids) + 1, dtype=np.int32)
         qs[1:] = np.cumsum(chunks)
         return PrefillPlan(ids, chunks, slots, pairs, tables, lens, qs)
+
+    def swap_out(self, seq_ids, stream=None):
+        """Preempt sequences by swapping: each moves, all or nothing, to host blocks
+        and its K/V is copied there; returns the (device, host) pairs."""
+        pairs = [self.bm.swap_out(int(s)) for s in seq_ids]
+        pairs = np.concatenate(pairs) if pairs else np.zeros((0, 2), np.int64)
+        if len(pairs):
+            swap_blocks(self.host_k, self.host_v, self.k_pool, self.v_pool,
+                        torch.as_tensor(pairs, device=self.device), stream)
+        return pairs
+
+    def swap_in(self, seq_ids, stream=None):
+        """Bring swapped-out sequences back onto fresh device blocks; returns the
+        (host, device) pairs."""
+        pairs = [self.bm.swap_in(int(s)) for s in seq_ids]
+        pairs = np.concatenate(pairs) if pairs else np.zeros((0, 2), np.int64)
+        if len(pairs):
+            swap_blocks(self.k_pool, self.v_pool, self.host_k, self.host_v,
+                        torch.as_tensor(pairs, device=self.device), stream)
+        return pairs
 
     def plan_prompts(self, seq_ids, prompts, max_blocks=None):
         """Host half of a prefill step with prefix caching (the manager must have

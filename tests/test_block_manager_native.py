@@ -234,3 +234,81 @@ def test_prefix_caching_must_be_enabled_before_sequences_exist():
     assert bm._lib.bm_enable_prefix_caching(bm._h) == -1
     with pytest.raises(pkv.PagedKVError):
         bm.add_seq_prompt(1, [1, 2, 3])              # caching is off
+
+
+@pytest.mark.parametrize("seed,caching", [(s, c) for s in range(6) for c in (False, True)])
+def test_swapping_matches_oracle_operation_by_operation(seed, caching):
+    rng = np.random.default_rng(300 + seed)
+    bs = int(rng.choice([2, 4, 16]))
+    nb, ncpu = int(rng.integers(20, 50)), int(rng.integers(5, 40))
+    order = list(rng.permutation(nb))
+    nat = BlockManager(nb, bs, order, prefix_caching=caching, num_host_blocks=ncpu)
+    ora = PrefixCachingBlockManager(nb, bs, order, ncpu)
+    live, nxt = [], 0
+    for step in range(150):
+        op = int(rng.integers(0, 6))
+        resident = [s for s in live if s not in ora.swapped]
+        try:
+            if op == 0 or not live:
+                p = [int(t) for t in rng.integers(0, 3, size=rng.integers(1, 5 * bs))]
+                if not caching:
+                    n_o = 0
+                    ora.add_seq(nxt)
+                    nat.add_seq(nxt)
+                    toks = [t + 10 * (nxt + 1) for t in p]
+                else:
+                    n_o = ora.add_seq_prompt(nxt, p)
+                    assert nat.add_seq_prompt(nxt, p) == n_o
+                    toks = p[n_o:]
+                sid = nxt
+                nxt += 1
+                live.append(sid)
+                slots, pairs = nat.append_tokens(sid, toks) if caching else (
+                    np.array([nat.append_slot(sid)[0] for _ in toks]), None)
+                exp = [ora.append_token(sid, t) if caching else ora.append_slot(sid) for t in toks]
+                assert list(slots) == [s for s, _ in exp]
+            elif op == 1 and resident:
+                sid = resident[rng.integers(len(resident))]
+                assert nat.append_slot(sid) == ora.append_slot(sid)
+            elif op == 2 and resident:
+                sid = resident[rng.integers(len(resident))]
+                nat.fork(sid, nxt)
+                ora.fork(sid, nxt)
+                live.append(nxt)
+                nxt += 1
+            elif op == 3 and resident:
+                sid = resident[rng.integers(len(resident))]
+                try:
+                    exp = ora.swap_out(sid)
+                except PoolExhausted:
+                    with pytest.raises(pkv.PagedKVError) as e:
+                        nat.swap_out(sid)
+                    assert e.value.status == -5
+                    continue
+                assert [tuple(x) for x in nat.swap_out(sid)] == exp
+                assert nat.is_swapped(sid)
+            elif op == 4 and ora.swapped:
+                sid = sorted(ora.swapped)[rng.integers(len(ora.swapped))]
+                try:
+                    exp = ora.swap_in(sid)
+                except PoolExhausted:
+                    with pytest.raises(pkv.PagedKVError) as e:
+                        nat.swap_in(sid)
+                    assert e.value.status == -5
+                    continue
+                assert [tuple(x) for x in nat.swap_in(sid)] == exp
+            elif op == 5:
+                sid = live.pop(rng.integers(len(live)))
+                nat.free_seq(sid)
+                ora.free_seq(sid)
+        except (PoolExhausted, pkv.PagedKVError) as e:
+            assert isinstance(e, PoolExhausted) or e.status == -5
+            break                                      # the device pool ran out
+        for sid in live:
+            assert nat.block_table(sid) == ora.block_table(sid)
+            assert nat.is_swapped(sid) == (sid in ora.swapped)
+        assert nat.free_list() == ora.free
+        assert nat.host_free_list() == ora.cpu_free
+        assert [nat.refcount(b) for b in range(nb)] == ora.ref
+        if caching:
+            assert nat.evictable_list() == ora.evictable
