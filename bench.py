@@ -799,6 +799,242 @@ def run_reference_prefill(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- swapping
+SWAP_METRIC = ("swap of preempted sequences' KV blocks between HBM and pinned host memory: "
+               "achieved GB/s of block bytes moved (% of the measured copy-engine rate)")
+
+
+def swap_plans(bm, victims, n):
+    """Host half of n swap steps: every victim swapped out, then every victim
+    swapped back in; returns [(out pairs, in pairs)] as int64 [P, 2] arrays."""
+    plans = []
+    for _ in range(n):
+        o = np.concatenate([bm.swap_out(int(s)) for s in victims])
+        i = np.concatenate([bm.swap_in(int(s)) for s in victims])
+        plans.append((np.asarray(o, dtype=np.int64).reshape(-1, 2),
+                      np.asarray(i, dtype=np.int64).reshape(-1, 2)))
+    return plans
+
+
+def copy_engine_rate(nbytes, device, reps=5):
+    """GB/s of one contiguous device->pinned-host copy plus one pinned-host->device
+    copy of ``nbytes`` each (cudaMemcpyAsync on the copy engines), best of reps."""
+    d = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d.fill_(1)
+    stream = torch.cuda.current_stream(device)
+    best = {}
+    for name, dst, src in (("d2h", h, d), ("h2d", d, h)):
+        ts = []
+        for _ in range(reps + 1):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dst.copy_(src, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        best[name] = min(ts[1:])
+    return 2 * nbytes / ((best["d2h"] + best["h2d"]) * 1e-3) / 1e9, best
+
+
+def swap_oracle_state(sw, k_src, v_src):
+    """The oracle's block manager after the workload's script, with its pools."""
+    from oracle.block_manager import BlockManager as OracleBM
+    w = sw.base
+    bm = OracleBM(w.NB, w.bs, list(w.free_order), num_cpu_blocks=sw.num_host_blocks)
+    for op in w.script:
+        if op[0] == "add":
+            bm.add_seq(op[1])
+        else:
+            for _ in range(op[2]):
+                bm.append_slot(op[1])
+    hk = torch.zeros((sw.num_host_blocks,) + tuple(k_src.shape[1:]), dtype=k_src.dtype)
+    return bm, k_src, v_src, hk, torch.zeros_like(hk)
+
+
+def swap_oracle_timing(sw, k_src, v_src, slice_s, slices):
+    """The oracle (block manager swap + whole-block copies on host tensors), one
+    thread, for ``slices`` windows of ``slice_s`` s; a step (all victims out,
+    then in) counts in the window it finishes in. Returns GB/s per window and
+    steps per window."""
+    from oracle import cache_ops as oops
+    bm, kp, vp, hk, hv = swap_oracle_state(sw, k_src, v_src)
+    step_bytes = 2 * sw.victim_blocks * 2 * kp[0].numel() * kp.element_size()
+    prev = torch.get_num_threads()
+    torch.set_num_threads(1)
+    fin = []
+    try:
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < slice_s * slices:
+            for s in sw.victims:
+                oops.swap_blocks(hk, hv, kp, vp, bm.swap_out(s))
+            for s in sw.victims:
+                oops.swap_blocks(kp, vp, hk, hv, bm.swap_in(s))
+            fin.append(time.perf_counter() - t0)
+    finally:
+        torch.set_num_threads(prev)
+    fin = np.array(fin)
+    width = max(slice_s * slices, float(fin.max()) if fin.size else 0.0) / slices
+    idx = np.minimum((fin / width).astype(np.int64), slices - 1)
+    steps = np.bincount(idx, minlength=slices)
+    return steps * step_bytes / width / 1e9, steps
+
+
+def swap_workload_desc(sw):
+    w = sw.base
+    L = np.asarray(w.final_lens) - 1
+    Lv = L[sw.victims]
+    return (f"{sw.name}: B={w.B} sequences holding L in [{L.min()}, {L.max()}] tokens "
+            f"(LLaMA-13B layer: Hkv={w.Hkv}, D={w.D}, block_size={w.bs}, bf16, NB={w.NB}); "
+            f"the newest {len(sw.victims)} (L mean {Lv.mean():.1f}, {sw.victim_blocks} blocks) "
+            f"swapped out to a pinned host pool of {sw.num_host_blocks} blocks and back in "
+            f"each step")
+
+
+def swap_main(args, rank, world, device):
+    import paged_kv_cache_259_gb300 as pkv
+    from paged_kv_cache_259_gb300.engine import PagedKVCache
+    sw = wl.SWAP_CONFIGS[args.config]()
+    w = sw.base
+    cache = PagedKVCache(w.NB, w.Hq, w.Hkv, w.D, w.bs, torch.bfloat16, w.free_order, device,
+                         num_host_blocks=sw.num_host_blocks)
+    k_src, v_src = w.past_pools()
+    cache.load(k_src, v_src)
+    cache.replay(w.script)
+    stream = torch.cuda.current_stream(device)
+    block_bytes = w.Hkv * w.bs * w.D * 2
+    P = sw.victim_blocks
+    dir_bytes = P * 2 * block_bytes                         # K and V blocks, one direction
+    step_bytes = 2 * dir_bytes
+    K, W = args.steps, args.warmup
+    plans = [(torch.as_tensor(o, device=device), torch.as_tensor(i, device=device))
+             for o, i in swap_plans(cache.bm, sw.victims, W + K)]
+
+    def step(o, i):
+        pkv.swap_blocks(cache.host_k, cache.host_v, cache.k_pool, cache.v_pool, o, stream)
+        pkv.swap_blocks(cache.k_pool, cache.v_pool, cache.host_k, cache.host_v, i, stream)
+
+    for o, i in plans[:W]:
+        step(o, i)
+    torch.cuda.synchronize()
+    if pkv.get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = pkv.kernel_launches()
+    t_start.record(stream)
+    for k in range(K):
+        o, i = plans[W + k]
+        ev[k][0].record(stream)
+        pkv.swap_blocks(cache.host_k, cache.host_v, cache.k_pool, cache.v_pool, o, stream)
+        ev[k][1].record(stream)
+        pkv.swap_blocks(cache.k_pool, cache.v_pool, cache.host_k, cache.host_v, i, stream)
+        ev[k][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = pkv.kernel_launches() - launches0
+    clk = clocks.stop()
+    if pkv.get_device_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    ms = max_over_ranks(t_start.elapsed_time(t_end) / K, world, device)
+    out_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in ev]))
+    in_ms = float(np.mean([b.elapsed_time(c) for _, b, c in ev]))
+
+    # end to end through the engine: block-manager swaps on the host, pair
+    # upload, both copies; wall clock around whole steps
+    for _ in range(3):
+        cache.swap_out(sw.victims, stream)
+        cache.swap_in(sw.victims, stream)
+    torch.cuda.synchronize()
+    K2 = max(3, K // 2)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(K2):
+        cache.swap_out(sw.victims, stream)
+        cache.swap_in(sw.victims, stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / K2, world, device)
+    if pkv.get_device_error() != 0:
+        raise RuntimeError("device error in the end-to-end steps")
+    peak, ce = copy_engine_rate(dir_bytes, device)
+    if rank != 0:
+        return
+    gbs, steps = swap_oracle_timing(sw, k_src, v_src, args.cpu_budget, 1)
+    achieved = step_bytes / ((out_ms + in_ms) * 1e-3) / 1e9
+    line = {
+        "metric": SWAP_METRIC, "value": round(world * step_bytes / (ms * 1e-3) / 1e9, 2),
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": swap_workload_desc(sw),
+            "step": ("swap_blocks device->host (%d block pairs, K and V) + swap_blocks "
+                     "host->device (%d pairs); pairs planned by the block manager beforehand "
+                     "and resident on the device" % (P, P)),
+            "l2": "inputs larger than L2: %.0f MB of device blocks read per step vs %d MB L2"
+                  % (dir_bytes / 1e6, L2_BYTES >> 20),
+            "bytes_per_step": step_bytes,
+            "swap_out_gbs": round(dir_bytes / (out_ms * 1e-3) / 1e9, 2),
+            "swap_in_gbs": round(dir_bytes / (in_ms * 1e-3) / 1e9, 2),
+            "copy_engine_ms": {k: round(v, 5) for k, v in ce.items()},
+            "sequences_swapped_per_s": round(world * 2 * len(sw.victims) / (ms * 1e-3), 1),
+        },
+        "roofline": {
+            "kernel": "swap_blocks (out + in)", "bound": "host-link",
+            "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": None,
+            "peak_source": ("measured in this run: one contiguous cudaMemcpyAsync of the same "
+                            "bytes device->pinned host plus one back (copy engines)"),
+            "bytes_per_launch": dir_bytes,
+            "ms_per_launch": round((out_ms + in_ms) / 2, 5),
+        },
+        "cpu_baseline": {
+            "value": round(float(gbs[0]), 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{int(steps[0])} whole swap steps (block-manager swaps plus whole-block "
+                      f"copies of host tensors) of this workload in {args.cpu_budget:.1f} s on "
+                      f"one host thread",
+        },
+        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": dir_bytes + 2 * P * 16, "d2h_bytes_per_step": dir_bytes,
+                "ms_per_step": round(e2e_ms, 5),
+                "note": "wall clock around engine swap_out + swap_in (host block manager, "
+                        "pair upload, both copies)"},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_swap(args):
+    """Reference arm for the swap workload: the oracle on one host thread."""
+    sw = wl.SWAP_CONFIGS[args.config]()
+    k_src, v_src = sw.base.past_pools()
+    slice_s = 120.0 / (args.steps + args.warmup)
+    gbs, steps = swap_oracle_timing(sw, k_src, v_src, slice_s, args.warmup + args.steps)
+    value = float(gbs[args.warmup:].mean())
+    line = {
+        "impl": "reference", "metric": SWAP_METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * slice_s, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": swap_workload_desc(sw)},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{int(steps[args.warmup:].sum())} whole swap steps finished "
+                                   f"in {args.steps} time slices of {slice_s:.3f} s on one host "
+                                   f"thread"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def make_workload(args):
     if args.batch is None:
         return wl.CONFIGS[args.config]()
@@ -837,7 +1073,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default=DEFAULT_CONFIG,
                     choices=sorted(wl.CONFIGS) + sorted(wl.PREFILL_CONFIGS) +
-                    sorted(wl.PROMPT_CONFIGS))
+                    sorted(wl.PROMPT_CONFIGS) + sorted(wl.SWAP_CONFIGS))
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's sequence count (profiling small cases)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -854,6 +1090,8 @@ def main():
             return
         if args.config in wl.PREFILL_CONFIGS or args.config in wl.PROMPT_CONFIGS:
             run_reference_prefill(args)
+        elif args.config in wl.SWAP_CONFIGS:
+            run_reference_swap(args)
         else:
             run_reference(args)
         return
@@ -867,8 +1105,11 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
 
-    if args.config in wl.PREFILL_CONFIGS or args.config in wl.PROMPT_CONFIGS:
-        prefill_main(args, rank, world, device)
+    modes = {**{c: prefill_main for c in wl.PREFILL_CONFIGS},
+             **{c: prefill_main for c in wl.PROMPT_CONFIGS},
+             **{c: swap_main for c in wl.SWAP_CONFIGS}}
+    if args.config in modes:
+        modes[args.config](args, rank, world, device)
         if world > 1:
             torch.distributed.barrier()
             torch.distributed.destroy_process_group()

@@ -16,6 +16,10 @@ Pool layout (a reading; the glossary's example shows one head as
   paginado...", "Como funciona"; glossary, "Chia sẻ block giữa các chuỗi"):
   for each ``(src, dst)`` the whole block, every head, K and V, becomes a copy of
   ``src``.
+* ``swap_blocks`` is the copy of swapping ("KV cache paginado...", "Como
+  funciona": preempted requests' blocks go to CPU memory and come back): the
+  same whole-block copy, but from one pool into another (device pool to host
+  pool on swap-out, host to device on swap-in).
 
 All functions take torch CPU tensors and write in place, copying stored bits
 exactly (no arithmetic except the FP8 quantiser).
@@ -61,3 +65,13 @@ def copy_blocks(k_pool, v_pool, pairs):
             raise IndexError("block id outside the pool")
         k_pool[dst] = k_pool[src]
         v_pool[dst] = v_pool[src]
+
+
+def swap_blocks(dst_k_pool, dst_v_pool, src_k_pool, src_v_pool, pairs):
+    """``dst_pool[d] = src_pool[s]`` for every ``(s, d)`` pair, K and V, all heads."""
+    ns, nd = src_k_pool.shape[0], dst_k_pool.shape[0]
+    for src, dst in pairs:
+        if not (0 <= src < ns and 0 <= dst < nd):
+            raise IndexError("block id outside its pool")
+        dst_k_pool[dst] = src_k_pool[src]
+        dst_v_pool[dst] = src_v_pool[src]

@@ -316,6 +316,37 @@ def system_prompt(B=64, system=1024, suffix=256, Hq=40, Hkv=40, D=128, bs=16, se
                           prompts=prompts, warm=[sys_ids.copy()])
 
 
+@dataclass
+class SwapWorkload:
+    """Preemption by swapping: of the decode batch ``base`` (each sequence holding
+    its past tokens), the ``victims`` -- the newest arrivals -- are swapped out to
+    a host pool of ``num_host_blocks`` blocks and swapped back in, step after step."""
+    name: str
+    base: Workload
+    victims: list
+    num_host_blocks: int
+
+    @property
+    def victim_blocks(self):
+        return int(sum(-(-(int(self.base.final_lens[s]) - 1) // self.base.bs)
+                       for s in self.victims))
+
+
+def swap_llama13b_bf16(B=64, victims=16):
+    """The LLaMA-13B-shaped bf16 decode batch (B sequences, lengths U[128, 2048]);
+    its last ``victims`` sequences are preempted by swapping."""
+    base = llama13b_mha_bf16(B)
+    v = list(range(B - min(victims, B), B))
+    sw = SwapWorkload("swap_llama13b_bf16", base, v, 0)
+    sw.num_host_blocks = _pool_size(sw.victim_blocks)
+    return sw
+
+
+SWAP_CONFIGS = {
+    "swap_llama13b_bf16": swap_llama13b_bf16,
+}
+
+
 PREFILL_CONFIGS = {
     "prefill_llama13b_bf16": prefill_llama13b_bf16,
     "prefill_gqa_bf16": prefill_gqa_bf16,

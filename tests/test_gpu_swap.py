@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import pkv_workloads as wl
 from _lib import library, pkv
 from _parity import assert_close, stored_bits
 from paged_kv_cache_259_gb300.engine import PagedKVCache
@@ -122,3 +123,48 @@ def test_swap_blocks_rejects_pageable_host_memory_and_flags_bad_pairs():
     assert pkv.get_device_error() == -4                  # (0, 9): outside the host pool
     assert torch.all(ph[2] == 1) and torch.all(pv[2] == 2)
     assert torch.count_nonzero(ph[0]) == 0 and torch.count_nonzero(pv[[0, 1, 3]]) == 0
+
+
+def test_full_size_swap_workload_two_round_trips_bit_exact():
+    """The benchmarked workload (the newest 16 of 64 LLaMA-13B-shaped sequences,
+    1105 blocks) swapped out and in twice, block ids changing every time; pairs
+    equal the oracle's, and sampled blocks of both pools equal the oracle's pools."""
+    sw = wl.swap_llama13b_bf16()
+    w = sw.base
+    cache = PagedKVCache(w.NB, w.Hq, w.Hkv, w.D, w.bs, torch.bfloat16, w.free_order, "cuda",
+                         num_host_blocks=sw.num_host_blocks)
+    kp, vp = w.past_pools()                                # also the oracle's device pools
+    cache.load(kp, vp)
+    cache.replay(w.script)
+    obm = OracleBM(w.NB, w.bs, list(w.free_order), num_cpu_blocks=sw.num_host_blocks)
+    for op in w.script:
+        if op[0] == "add":
+            obm.add_seq(op[1])
+        else:
+            for _ in range(op[2]):
+                obm.append_slot(op[1])
+    hk = torch.zeros((sw.num_host_blocks,) + tuple(kp.shape[1:]), dtype=kp.dtype)
+    hv = torch.zeros_like(hk)
+    for _ in range(2):
+        g = cache.swap_out(sw.victims)
+        o = [p for s in sw.victims for p in obm.swap_out(s)]
+        assert [tuple(x) for x in g] == o and len(o) == sw.victim_blocks
+        oops.swap_blocks(hk, hv, kp, vp, o)
+        g = cache.swap_in(sw.victims)
+        o = [p for s in sw.victims for p in obm.swap_in(s)]
+        assert [tuple(x) for x in g] == o
+        oops.swap_blocks(kp, vp, hk, hv, o)
+    assert pkv.get_device_error() == 0
+    rng = np.random.default_rng(0)
+    victim_blocks = [b for s in sw.victims for b in obm.block_table(s)]
+    other = [b for s in range(w.B) if s not in sw.victims for b in obm.block_table(s)]
+    idx = torch.tensor(sorted(set(rng.choice(victim_blocks, 64).tolist() +
+                                  rng.choice(other, 32).tolist())))
+    kv, vv = cache.k_view(), cache.v_view()
+    assert torch.equal(stored_bits(kv[idx.cuda()].cpu()), stored_bits(kp[idx]))
+    assert torch.equal(stored_bits(vv[idx.cuda()].cpu()), stored_bits(vp[idx]))
+    del kv, vv
+    hidx = torch.tensor(sorted(set(rng.choice(sw.num_host_blocks, 64).tolist())))
+    hkv, hvv = pkv.pool_views(cache.host_k, cache.host_v)
+    assert torch.equal(stored_bits(hkv[hidx]), stored_bits(hk[hidx]))
+    assert torch.equal(stored_bits(hvv[hidx]), stored_bits(hv[hidx]))

@@ -813,3 +813,43 @@ def test_swap_random_scripts_keep_content_and_partitions(caching):
 
             if not caching:
                 assert bm.hit_blocks == 0
+
+def test_oracle_swap_blocks_round_trip_restores_every_sequence_through_its_table():
+    """Pool values tagged by token id: after swapping a sequence out, letting
+    another overwrite its freed device blocks and swapping it back, gathering
+    through its new table gives back exactly the rows written for its tokens."""
+    bs, Hkv, D, nb, ncpu = 4, 2, 3, 8, 6
+    bm = BlockManager(nb, bs, [5, 2, 7, 0, 3, 6, 1, 4], num_cpu_blocks=ncpu)
+    kp = torch.full((nb, Hkv, bs, D), -1.0, dtype=torch.float64)
+    vp = kp.clone()
+    hk = torch.full((ncpu, Hkv, bs, D), -1.0, dtype=torch.float64)
+    hv = hk.clone()
+
+    def write(sid, tok):
+        s, _ = bm.append_slot(sid)
+        row = torch.full((Hkv, D), float(tok), dtype=torch.float64)
+        oops.reshape_and_cache(row[None], -row[None], kp, vp, torch.tensor([s]), bs)
+
+    def rows(sid, kpool, vpool):
+        t = bm.block_table(sid)
+        k = torch.cat([kpool[b] for b in t], dim=1)[:, :bm.seq_len(sid)]
+        v = torch.cat([vpool[b] for b in t], dim=1)[:, :bm.seq_len(sid)]
+        return k[0, :, 0].tolist(), v[1, :, 2].tolist()
+
+    for s, n in ((0, 10), (1, 5)):
+        bm.add_seq(s)
+        for i in range(n):
+            write(s, 100 * s + i)
+    want0 = [float(i) for i in range(10)]
+    oops.swap_blocks(hk, hv, kp, vp, bm.swap_out(0))
+    assert rows(0, hk, hv) == (want0, [-x for x in want0])
+    bm.add_seq(2)
+    for i in range(12):                                # 3 blocks: reuses 0's freed blocks
+        write(2, 200 + i)
+    oops.swap_blocks(hk, hv, kp, vp, bm.swap_out(2))   # 2 out as well, then 0 back in
+    oops.swap_blocks(kp, vp, hk, hv, bm.swap_in(0))
+    assert rows(0, kp, vp) == (want0, [-x for x in want0])
+    assert rows(1, kp, vp)[0] == [100.0 + i for i in range(5)]
+    assert rows(2, hk, hv)[0] == [200.0 + i for i in range(12)]
+    with pytest.raises(IndexError):
+        oops.swap_blocks(kp, vp, hk, hv, [(ncpu, 0)])
