@@ -38,6 +38,14 @@ device blocks are released as on ``free_seq``; ``swap_in`` is the reverse with
 (host, device) pairs and fresh device blocks. If either pool cannot take the
 whole sequence nothing changes (``PoolExhausted``). A swapped-out sequence can
 only be swapped in or freed (its host blocks return to the host free list).
+
+Beam search (glossary, "Chia sẻ block giữa các chuỗi": beams share blocks
+through their tables with a count per block, and a beam about to write into a
+shared block copies it first). One step's reshuffle of the beams, a reading:
+new beam ``i`` continues old beam ``parents[i]`` -- forked from it, in order of
+``i`` -- and then every old beam is freed, in order, so an old beam nobody
+continues returns the blocks only it held and a continued one hands its blocks
+on. The new beams' next appends then copy any shared partial last block.
 """
 
 
@@ -173,3 +181,50 @@ class BlockManager:
 
     def num_free(self):
         return len(self.free)
+
+    def beam_step(self, old_ids, parents, new_ids):
+        """New beam ``new_ids[i]`` continues ``old_ids[parents[i]]``; then the old
+        beams are freed. Nothing changes if an argument is invalid."""
+        old_ids, new_ids = list(old_ids), list(new_ids)
+        if len(parents) != len(new_ids) or len(set(old_ids)) != len(old_ids) or \
+                len(set(new_ids)) != len(new_ids):
+            raise ValueError("parents must match new_ids; ids must be distinct")
+        if any(s not in self.tables or s in self.swapped for s in old_ids):
+            raise ValueError("old beam unknown or swapped out")
+        if any(s in self.tables for s in new_ids):
+            raise ValueError("new beam id in use")
+        if any(not 0 <= int(p) < len(old_ids) for p in parents):
+            raise ValueError("parent index out of range")
+        for p, sid in zip(parents, new_ids):
+            self.fork(old_ids[int(p)], sid)
+        for sid in old_ids:
+            self.free_seq(sid)
+
+    def blocks_in_use(self):
+        """Physical device blocks with a nonzero count."""
+        return sum(1 for c in self.ref if c > 0)
+
+
+def replay(bm, script):
+    """Apply a workload script's operations to ``bm``; returns the CoW pairs the
+    appends raised, in order. Ops: ``("add", sid)``, ``("append", sid, n)``,
+    ``("fork", parent, child)``, ``("free", sid)``, ``("beam", old_ids, parents,
+    new_ids)``."""
+    pairs = []
+    for op in script:
+        if op[0] == "add":
+            bm.add_seq(op[1])
+        elif op[0] == "append":
+            for _ in range(op[2]):
+                cow = bm.append_slot(op[1])[1]
+                if cow is not None:
+                    pairs.append(cow)
+        elif op[0] == "fork":
+            bm.fork(op[1], op[2])
+        elif op[0] == "free":
+            bm.free_seq(op[1])
+        elif op[0] == "beam":
+            bm.beam_step(op[1], op[2], op[3])
+        else:
+            raise ValueError(f"unknown op {op[0]}")
+    return pairs

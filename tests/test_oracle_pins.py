@@ -853,3 +853,108 @@ def test_oracle_swap_blocks_round_trip_restores_every_sequence_through_its_table
     assert rows(2, hk, hv)[0] == [200.0 + i for i in range(12)]
     with pytest.raises(IndexError):
         oops.swap_blocks(kp, vp, hk, hv, [(ncpu, 0)])
+
+
+# ---------------------------------------------------------------- beam search
+class Beams:
+    """Beam search on the oracle's manager with a slot-content shadow and each
+    beam's token history kept apart from the manager (its lineage)."""
+
+    def __init__(self, P, bs, nb=600):
+        self.bm = BlockManager(nb, bs, list(range(nb)))
+        self.sh = Shadow(nb, bs)
+        self.hist = {"p": []}
+        self.bm.add_seq("p")
+        for t in range(P):
+            self.append("p", t)
+        self.beams = ["p"]
+
+    def append(self, sid, token):
+        slot, cow = self.bm.append_slot(sid)
+        if cow is not None:
+            self.sh.copy(*cow)
+        self.sh.write(slot, token)
+        self.hist[sid].append(token)
+
+    def step(self, g, parents):
+        new = [(g, i) for i in range(len(parents))]
+        self.bm.beam_step(self.beams, parents, new)
+        hist = {n: self.hist[self.beams[p]] + [] for n, p in zip(new, parents)}
+        self.hist = hist
+        self.beams = new
+        for i, sid in enumerate(new):
+            self.append(sid, 10000 * (g + 1) + i)      # each beam's own new token
+
+    def check(self):
+        bm = self.bm
+        refs = [0] * bm.num_blocks
+        for sid in self.beams:
+            t = bm.block_table(sid)
+            assert self.sh.gather(t, bm.seq_len(sid)) == self.hist[sid]
+            for b in t:
+                refs[b] += 1
+        assert refs == bm.ref
+        assert sorted(bm.free + [b for b in range(bm.num_blocks) if bm.ref[b]]) == \
+            list(range(bm.num_blocks))
+
+
+@pytest.mark.parametrize("P,W,bs", [(40, 4, 16), (48, 4, 16), (47, 3, 16), (5, 2, 4), (1, 8, 16)])
+def test_beams_collapsing_onto_one_parent_share_all_but_their_last_blocks(P, W, bs):
+    """Every step, all W new beams continue old beam 0. After the step's appends
+    the beams share every block except the one holding their last token, so the
+    pool holds ceil(L/bs) - 1 + W blocks (W * ceil(L/bs) without sharing)."""
+    b = Beams(P, bs)
+    for g in range(40):
+        b.step(g, [0] * W)
+        L = P + g + 1
+        assert b.bm.blocks_in_use() == -(-L // bs) - 1 + W
+        b.check()
+
+
+@pytest.mark.parametrize("P,W,bs", [(40, 4, 16), (48, 4, 16), (5, 3, 4)])
+def test_beams_that_never_merge_share_only_the_prompts_full_blocks(P, W, bs):
+    """The first step forks W beams off the prompt; after that beam i always
+    continues beam i. Only the prompt's full blocks stay shared: the pool holds
+    floor(P/bs) + W * (ceil(L/bs) - floor(P/bs)) blocks."""
+    b = Beams(P, bs)
+    b.step(0, [0] * W)
+    for g in range(1, 40):
+        b.step(g, list(range(W)))
+        L = P + g + 1
+        assert b.bm.blocks_in_use() == P // bs + W * (-(-L // bs) - P // bs)
+        b.check()
+
+
+def test_beam_step_copies_a_shared_partial_block_for_all_but_its_last_writer():
+    b = Beams(20, 16)                                  # block 1 partial (4 tokens)
+    b.bm.beam_step(["p"], [0, 0, 0], ["a", "b", "c"])
+    pairs = [b.bm.append_slot(s)[1] for s in ("a", "b", "c")]
+    shared = b.bm.block_table("c")[1]                  # c, the last writer, keeps it
+    assert pairs[2] is None and pairs[0][0] == pairs[1][0] == shared
+    assert len({pairs[0][1], pairs[1][1], shared}) == 3
+    assert [b.bm.refcount(x) for x in (shared, pairs[0][1], pairs[1][1])] == [1, 1, 1]
+
+
+@pytest.mark.parametrize("W,seed", [(2, 0), (4, 1), (4, 2), (8, 3)])
+def test_random_beam_steps_keep_each_beams_history_and_the_counts(W, seed):
+    rng = np.random.default_rng(seed)
+    b = Beams(int(rng.integers(1, 60)), 4)
+    b.step(0, [0] * W)
+    for g in range(1, 60):
+        b.step(g, sorted(rng.integers(0, W, size=W).tolist()))
+        b.check()
+    used = b.bm.blocks_in_use()
+    assert used <= sum(-(-b.bm.seq_len(s) // 4) for s in b.beams)
+
+
+def test_beam_step_rejects_bad_arguments_and_changes_nothing():
+    b = Beams(10, 4)
+    b.step(0, [0, 0])
+    before = (dict(b.bm.tables), list(b.bm.ref), list(b.bm.free))
+    for old, parents, new in ((b.beams, [0, 2], ["x", "y"]),        # parent out of range
+                              (b.beams, [0, 1], ["x", "x"]),        # duplicate new id
+                              (b.beams, [0, 1], [b.beams[0], "y"]),  # new id in use
+                              (b.beams + ["zz"], [0, 1], ["x", "y"])):  # unknown old beam
+        with pytest.raises(ValueError):
+            b.bm.beam_step(old, parents, new)
+        assert (dict(b.bm.tables), list(b.bm.ref), list(b.bm.free)) == before
