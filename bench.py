@@ -421,19 +421,9 @@ def oracle_inputs_for_step(w, q, k_src, v_src, plan):
     """CPU pools after the step's writes, as the oracle sees them (source values;
     no GPU data). Built with the oracle's own block manager and cache ops."""
     from oracle import cache_ops as oops
-    from oracle.block_manager import BlockManager as OBM
+    from oracle.block_manager import BlockManager as OBM, replay
     bm = OBM(w.NB, w.bs, w.free_order)
-    pairs = []
-    for op in w.script:
-        if op[0] == "add":
-            bm.add_seq(op[1])
-        elif op[0] == "fork":
-            bm.fork(op[1], op[2])
-        else:
-            for _ in range(op[2]):
-                c = bm.append_slot(op[1])[1]
-                if c is not None:
-                    pairs.append(c)
+    pairs = replay(bm, w.script)
     step = [bm.append_slot(s) for s in w.step_seqs]
     kp, vp = k_src, v_src                   # in place: the bench's copies are not reused
     oops.copy_blocks(kp, vp, pairs + [c for _, c in step if c is not None])
@@ -1042,10 +1032,55 @@ def make_workload(args):
               "gqa_chat_bf16": lambda B: wl.gqa_chat_bf16(B=B),
               "long_fp8_bs16": lambda B: wl.long_fp8(16, B=B),
               "long_fp8_bs32": lambda B: wl.long_fp8(32, B=B),
-              "shared_prefix_bf16": lambda B: wl.shared_prefix_bf16(groups=max(1, B // 4))}
+              "shared_prefix_bf16": lambda B: wl.shared_prefix_bf16(groups=max(1, B // 4)),
+              "beam_search_bf16": lambda B: wl.beam_search_bf16(requests=max(1, B // 4))}
     if args.config not in scaled:
         raise SystemExit(f"--batch is not supported for {args.config}")
     return scaled[args.config](args.batch)
+
+
+def beam_stats(w, steps=50, seed=0):
+    """Beam workloads: blocks held with sharing vs one copy per beam after the
+    measured step, and the host half of further real beam steps on the library's
+    block manager (every request's beams reshuffled by seeded random parents,
+    one append per beam, dense tables, prefix groups), in us per step."""
+    import paged_kv_cache_259_gb300 as pkv
+    bm = pkv.BlockManager(w.NB, w.bs, w.free_order)
+    for op in w.script:
+        if op[0] == "add":
+            bm.add_seq(op[1])
+        elif op[0] == "append":
+            bm.append_n(op[1], op[2])
+        elif op[0] == "beam":
+            bm.beam_step(op[1], op[2], op[3])
+        else:
+            raise ValueError(f"unexpected op {op[0]}")
+    bm.append_slots(w.step_seqs)
+    held = w.NB - bm.num_free()
+    unshared = int(sum(-(-int(L) // w.bs) for L in w.final_lens))
+    W = w.notes["width"]
+    beams = [list(w.step_seqs[i:i + W]) for i in range(0, w.B, W)]
+    nxt = max(w.step_seqs) + 1
+    rng = np.random.default_rng(seed)
+    parents = rng.integers(0, W, size=(steps, len(beams), W))
+    MB = w.max_blocks_per_seq + -(-steps // w.bs) + 1
+    max_members = max(1, 8 // (w.Hq // w.Hkv))
+    t0 = time.perf_counter()
+    for k in range(steps):
+        old = [s for b in beams for s in b]
+        par = (parents[k] + W * np.arange(len(beams))[:, None]).reshape(-1)
+        ids = list(range(nxt, nxt + len(old)))
+        nxt += len(old)
+        bm.beam_step(old, par, ids)
+        beams = [ids[i:i + W] for i in range(0, len(ids), W)]
+        bm.append_slots(ids)
+        bm.build_tables(ids, MB)
+        bm.prefix_groups(ids, max_members)
+    us = (time.perf_counter() - t0) * 1e6 / steps
+    return {"requests": w.notes["requests"], "width": W, "generated": w.notes["generated"],
+            "blocks_held": held, "blocks_unshared": unshared,
+            "memory_saving": round(1 - held / unshared, 4),
+            "host_beam_step_us": round(us, 1)}
 
 
 def kv_utilisation(w, plan):
@@ -1150,6 +1185,7 @@ def main():
                 "decode_logical_bytes_per_step": nb["decode_logical"],
                 "seq_steps_per_s": round(world * w.B / (ms * 1e-3), 1),
                 "kv_utilisation": kv_utilisation(w, plan),
+                **({"beam": beam_stats(w)} if "width" in w.notes else {}),
                 "step_frac_of_peak": round(value / world / peak, 4),
             },
             "roofline": {

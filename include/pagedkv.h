@@ -377,6 +377,20 @@ PKV_API int bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n
                     int64_t* slots, int64_t* cow_pairs, int* num_cow);
 PKV_API int bm_fork(pkv_block_manager* bm, int64_t parent, int64_t child);
 PKV_API int bm_free_seq(pkv_block_manager* bm, int64_t seq_id);
+/* One beam-search step's reshuffle ("PagedAttention" glossary, "Chia sẻ block
+ * giữa các chuỗi": beams share blocks through their tables, counted per block).
+ * New beam new_ids[i] continues old beam old_ids[parents[i]]: it is forked from
+ * it, in order of i; then every old beam is freed, in order (a beam nobody
+ * continues returns the blocks only it held). The new beams' next appends copy
+ * any shared partial last block (CoW pairs as usual).
+ *   old_ids  host int64 [num_old], distinct, existing, not swapped out
+ *   parents  host int32 [num_new], each in [0, num_old)
+ *   new_ids  host int64 [num_new], distinct, not in use (so not among old_ids)
+ * Returns PKV_ERR_OUT_OF_RANGE for an unknown old beam or a parent index out of
+ * range, PKV_ERR_INVALID_ARG for a repeated or used id or a swapped-out beam;
+ * on any error nothing changes. */
+PKV_API int bm_beam_step(pkv_block_manager* bm, const int64_t* old_ids, int num_old,
+                 const int32_t* parents, const int64_t* new_ids, int num_new);
 /* The sequence's table into out[0..cap), its length in blocks in *n. */
 PKV_API int bm_block_table(const pkv_block_manager* bm, int64_t seq_id, int32_t* out,
                    int cap, int* n);

@@ -94,6 +94,7 @@ def load_library():
         "bm_append_slots": (c_int, [vp, i64p, c_int, i64p, i64p, ip]),
         "bm_fork": (c_int, [vp, ctypes.c_int64, ctypes.c_int64]),
         "bm_free_seq": (c_int, [vp, ctypes.c_int64]),
+        "bm_beam_step": (c_int, [vp, i64p, c_int, i32p, i64p, c_int]),
         "bm_block_table": (c_int, [vp, ctypes.c_int64, i32p, c_int, ip]),
         "bm_build_tables": (c_int, [vp, i64p, c_int, c_int, i32p, i32p]),
         "bm_seq_len": (c_int, [vp, ctypes.c_int64, ip]),
@@ -526,6 +527,17 @@ class BlockManager:
 
     def free_seq(self, sid):
         _check(self._lib.bm_free_seq(self._h, sid), "bm_free_seq")
+
+    def beam_step(self, old_ids, parents, new_ids):
+        """New beam ``new_ids[i]`` continues ``old_ids[parents[i]]`` (forked, in
+        order), then the old beams are freed; nothing changes on an error."""
+        old = np.ascontiguousarray(np.asarray(old_ids, dtype=np.int64))
+        par = np.ascontiguousarray(np.asarray(parents, dtype=np.int32))
+        new = np.ascontiguousarray(np.asarray(new_ids, dtype=np.int64))
+        if len(par) != len(new):
+            raise ValueError("parents and new_ids differ in length")
+        _check(self._lib.bm_beam_step(self._h, _i64p(old), len(old), _i32p(par), _i64p(new),
+                                      len(new)), "bm_beam_step")
 
     def block_table(self, sid):
         n = ctypes.c_int(0)

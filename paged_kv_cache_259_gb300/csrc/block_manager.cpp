@@ -28,6 +28,11 @@
 // prefix (chained block by block); a hit also compares the block's own token
 // ids and the hash of the prefix before it.
 //
+// Beam search (glossary, "Chia sẻ block giữa các chuỗi": beams share blocks with
+// a count per block and copy a shared block before writing into it): one step's
+// reshuffle forks every new beam from its parent, in order, then frees the old
+// beams in order; the new beams' appends then copy shared partial blocks.
+//
 // Swapping ("KV cache paginado...", "Como funciona": when physical blocks run
 // out the newest requests are preempted, all or nothing, and their blocks
 // recovered by swapping to the CPU or by recomputation): a host pool of blocks
@@ -325,6 +330,34 @@ int bm_free_seq(pkv_block_manager* bm, int64_t seq_id) {
         bm->release(it->second.table);
     }
     bm->seqs.erase(it);
+    return PKV_OK;
+}
+
+int bm_beam_step(pkv_block_manager* bm, const int64_t* old_ids, int num_old,
+                 const int32_t* parents, const int64_t* new_ids, int num_new) {
+    if (!bm || num_old < 0 || num_new < 0 || (num_old > 0 && !old_ids) ||
+        (num_new > 0 && (!parents || !new_ids)))
+        return PKV_ERR_INVALID_ARG;
+    std::unordered_map<int64_t, int> seen;
+    seen.reserve((size_t)(num_old + num_new));
+    for (int i = 0; i < num_old; ++i) {
+        auto it = bm->seqs.find(old_ids[i]);
+        if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
+        if (it->second.swapped || !seen.emplace(old_ids[i], i).second) return PKV_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i < num_new; ++i) {
+        if (parents[i] < 0 || parents[i] >= num_old) return PKV_ERR_OUT_OF_RANGE;
+        if (bm->seqs.count(new_ids[i]) || !seen.emplace(new_ids[i], i).second)
+            return PKV_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i < num_new; ++i) {
+        const int st = bm_fork(bm, old_ids[parents[i]], new_ids[i]);
+        if (st != PKV_OK) return st;                   // cannot happen after the checks
+    }
+    for (int i = 0; i < num_old; ++i) {
+        const int st = bm_free_seq(bm, old_ids[i]);
+        if (st != PKV_OK) return st;
+    }
     return PKV_OK;
 }
 

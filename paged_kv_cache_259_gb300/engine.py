@@ -142,6 +142,8 @@ class PagedKVCache:
                 self.bm.fork(op[1], op[2])
             elif op[0] == "free":
                 self.bm.free_seq(op[1])
+            elif op[0] == "beam":
+                self.bm.beam_step(op[1], op[2], op[3])
             else:
                 raise ValueError(f"unknown op {op[0]}")
         return pairs

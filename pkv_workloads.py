@@ -316,6 +316,52 @@ def system_prompt(B=64, system=1024, suffix=256, Hq=40, Hkv=40, D=128, bs=16, se
                           prompts=prompts, warm=[sys_ids.copy()])
 
 
+def beam_search(name, requests, width, prompt, generated, Hq, Hkv, D, bs, seed,
+                src_dtype=torch.bfloat16, kv_dtype="bf16"):
+    """Beam search: ``requests`` prompts (lengths U[prompt[0], prompt[1]]) with
+    ``width`` beams each, after ``generated`` beam steps. Every step each new
+    beam's parent is drawn uniformly from its request's old beams (the scores
+    that pick them in a real search come from the model), then every beam
+    appends its token. The script ends with the measured step's reshuffle; the
+    measured step appends one token to each of its beams."""
+    rng = np.random.default_rng(seed)
+    P = rng.integers(prompt[0], prompt[1], size=requests, endpoint=True)
+    script, beams, sid = [], [], 0
+    for r in range(requests):
+        script += [("add", sid), ("append", sid, int(P[r]))]
+        beams.append((sid,))
+        sid += 1
+    for g in range(generated + 1):
+        # one reshuffle of every request's beams: parents index the old beams of
+        # all requests, listed request after request
+        old, parents, new = [], [], []
+        for r in range(requests):
+            parents += [len(old) + int(x) for x in rng.integers(0, len(beams[r]), size=width)]
+            old += beams[r]
+            beams[r] = tuple(range(sid, sid + width))
+            new += beams[r]
+            sid += width
+        script.append(("beam", tuple(old), tuple(parents), tuple(new)))
+        if g < generated:
+            script += [("append", s, 1) for b in beams for s in b]
+    lens = np.repeat(P + generated + 1, width).astype(np.int64)
+    NB = _pool_size(int(sum(-(-int(L) // bs) for L in lens)))
+    return Workload(name=name, B=requests * width, Hq=Hq, Hkv=Hkv, D=D, bs=bs, NB=NB, seed=seed,
+                    scale=1.0 / math.sqrt(D), src_dtype=src_dtype, kv_dtype=kv_dtype,
+                    free_order=rng.permutation(NB), script=script,
+                    step_seqs=[s for b in beams for s in b], final_lens=lens,
+                    notes={"requests": requests, "width": width, "generated": generated,
+                           "prompt_lens": P})
+
+
+def beam_search_bf16(requests=16, width=4, generated=128):
+    """LLaMA-13B-shaped beam search: 16 requests x 4 beams (64 sequences), prompts
+    U[128, 2048] (the decode batch's length distribution), 128 generated tokens,
+    40/40 heads, D 128, bs 16, seed 8."""
+    return beam_search("beam_search_bf16", requests, width, (128, 2048), generated, 40, 40, 128,
+                       16, 8)
+
+
 @dataclass
 class SwapWorkload:
     """Preemption by swapping: of the decode batch ``base`` (each sequence holding
@@ -366,4 +412,5 @@ CONFIGS = {
     "shared_prefix_fork_bf16": lambda: shared_prefix_bf16(fork_step=True),
     "long_fp8_bs16": lambda: long_fp8(16),
     "long_fp8_bs32": lambda: long_fp8(32),
+    "beam_search_bf16": beam_search_bf16,
 }

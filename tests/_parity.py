@@ -19,7 +19,7 @@ from paged_kv_cache_259_gb300.engine import PagedKVCache
 from oracle import attention as oatt
 from oracle import cache_ops as oops
 from oracle import fp8_e4m3 as ofp8
-from oracle.block_manager import BlockManager as OracleBM
+from oracle.block_manager import BlockManager as OracleBM, replay as oracle_replay
 
 KV_TORCH = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8}
 # |gpu - oracle| <= ATOL + RTOL * |oracle|, elementwise (the stated max-abs 2e-2 /
@@ -70,17 +70,7 @@ def run_gpu(inp, workspace=True, relabel=None, device="cuda"):
 def run_oracle(inp, units=None):
     w = inp.w
     bm = OracleBM(w.NB, w.bs, w.free_order)
-    setup_pairs = []
-    for op in w.script:
-        if op[0] == "add":
-            bm.add_seq(op[1])
-        elif op[0] == "fork":
-            bm.fork(op[1], op[2])
-        elif op[0] == "append":
-            for _ in range(op[2]):
-                cow = bm.append_slot(op[1])[1]
-                if cow is not None:
-                    setup_pairs.append(cow)
+    setup_pairs = oracle_replay(bm, w.script)
     kp, vp = inp.k_src.clone(), inp.v_src.clone()
     oops.copy_blocks(kp, vp, setup_pairs)
     step = [bm.append_slot(s) for s in w.step_seqs]

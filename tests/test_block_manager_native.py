@@ -82,7 +82,8 @@ def test_batch_append_and_tables_match_oracle():
 
 
 @pytest.mark.parametrize("name", ["tiny_fp32", "llama13b_mha_bf16", "gqa_chat_bf16",
-                                  "shared_prefix_bf16", "shared_prefix_fork_bf16"])
+                                  "shared_prefix_bf16", "shared_prefix_fork_bf16",
+                                  "beam_search_bf16"])
 def test_workload_setup_and_step_match_oracle(name):
     library()
     w = wl.CONFIGS[name]()
@@ -99,6 +100,11 @@ def test_workload_setup_and_step_match_oracle(name):
             got = a.append_n(op[1], op[2])
             exp = [c for c in (o.append_slot(op[1])[1] for _ in range(op[2])) if c is not None]
             assert got == exp
+        elif op[0] == "beam":
+            a.beam_step(*op[1:])
+            o.beam_step(*op[1:])
+        else:
+            raise AssertionError(f"unexpected op {op[0]}")
     slots, pairs = a.append_slots(w.step_seqs)
     exp = [o.append_slot(s) for s in w.step_seqs]
     assert list(slots) == [e[0] for e in exp]
@@ -312,3 +318,65 @@ def test_swapping_matches_oracle_operation_by_operation(seed, caching):
         assert [nat.refcount(b) for b in range(nb)] == ora.ref
         if caching:
             assert nat.evictable_list() == ora.evictable
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_beam_steps_match_oracle(seed):
+    """Requests of W beams reshuffled by seeded random parents every step, one
+    append per beam, interleaved with whole-request frees and new requests."""
+    library()
+    rng = np.random.default_rng(100 + seed)
+    nb, bs, W = 1200, int(rng.choice([2, 4, 16])), int(rng.choice([2, 3, 4, 8]))
+    free = rng.permutation(nb)
+    a, o = pkv.BlockManager(nb, bs, free), OracleBM(nb, bs, free)
+    nxt, reqs = 0, []
+    for step in range(120):
+        if len(reqs) < 3 or rng.random() < 0.05:
+            P = int(rng.integers(1, 40))
+            a.add_seq(nxt)
+            o.add_seq(nxt)
+            assert a.append_n(nxt, P) == []
+            for _ in range(P):
+                o.append_slot(nxt)
+            reqs.append([nxt])
+            nxt += 1
+        if rng.random() < 0.03 and len(reqs) > 1:
+            for s in reqs.pop(int(rng.integers(len(reqs)))):
+                a.free_seq(s)
+                o.free_seq(s)
+        for r, beams in enumerate(reqs):
+            parents = rng.integers(0, len(beams), size=W).tolist()
+            new = list(range(nxt, nxt + W))
+            nxt += W
+            a.beam_step(beams, parents, new)
+            o.beam_step(beams, parents, new)
+            reqs[r] = new
+            try:
+                exp = [o.append_slot(s) for s in new]
+            except PoolExhausted:
+                assert step > 30                        # the script ran long enough
+                return                                  # pool full: the script ends here
+            slots, pairs = a.append_slots(new)
+            assert list(slots) == [s for s, _ in exp]
+            assert [tuple(p) for p in pairs] == [c for _, c in exp if c is not None]
+        same_state(a, o)
+
+
+def test_beam_step_refusals_change_nothing():
+    library()
+    a = pkv.BlockManager(16, 4, range(16))
+    a.add_seq(0)
+    a.append_n(0, 6)
+    a.beam_step([0], [0, 0], [1, 2])
+    before = (a.free_list(), a.block_table(1), a.block_table(2))
+    for old, par, new, st in (([1, 2], [0, 2], [3, 4], -4),      # parent out of range
+                              ([1, 9], [0, 1], [3, 4], -4),      # unknown old beam
+                              ([1, 2], [0, 1], [3, 3], -1),      # repeated new id
+                              ([1, 2], [0, 1], [2, 4], -1),      # new id in use
+                              ([1, 1], [0, 1], [3, 4], -1)):     # repeated old beam
+        with pytest.raises(pkv.PagedKVError) as e:
+            a.beam_step(old, par, new)
+        assert e.value.status == st
+        assert (a.free_list(), a.block_table(1), a.block_table(2)) == before
+    with pytest.raises(ValueError):
+        a.beam_step([1, 2], [0], [3, 4])

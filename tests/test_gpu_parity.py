@@ -78,7 +78,7 @@ def test_tiny_fp32_config_all_outputs():
 
 
 FULL = ["llama13b_mha_bf16", "gqa_chat_bf16", "shared_prefix_bf16", "shared_prefix_fork_bf16",
-        "long_fp8_bs16", "long_fp8_bs32"]
+        "long_fp8_bs16", "long_fp8_bs32", "beam_search_bf16"]
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -267,6 +267,35 @@ def test_grouped_prefix_decode_matches_oracle(kv, Hq, Hkv, D, bs, per_group, pro
             cache.workspace(w.B, w.max_blocks_per_seq), None, None)
         assert pkv.get_device_error() == 0
         assert_close(out3.float().cpu().numpy(), o["out"], kv, w.name + " no list")
+
+
+BEAMS = [  # (kv, Hq, Hkv, D, bs, requests, width, prompt range, generated)
+    ("bf16", 8, 8, 128, 16, 3, 4, (1, 60), 40),      # MHA: beams grouped (up to 8 rows)
+    ("bf16", 16, 4, 128, 16, 3, 2, (20, 300), 70),   # GQA 4: groups of 2
+    ("bf16", 8, 8, 64, 32, 2, 8, (1, 33), 50),       # 8 beams, block size 32
+    ("e4m3", 8, 8, 128, 16, 2, 4, (100, 200), 33),   # E4M3 cache
+    ("f32", 4, 4, 64, 16, 2, 3, (5, 40), 20),        # float32 cache: no grouping
+]
+
+
+@pytest.mark.parametrize("kv,Hq,Hkv,D,bs,requests,width,prompt,gen", BEAMS)
+def test_beam_search_step_matches_oracle(kv, Hq, Hkv, D, bs, requests, width, prompt, gen):
+    """A beam-search state (beams reshuffled every step: forks of the chosen
+    parents, frees of the old beams, CoW of shared partial blocks) and the next
+    step (CoW, slot write, grouped decode): pairs, tables, the whole pools and
+    every output against the oracle."""
+    src = torch.float32 if kv == "f32" else torch.bfloat16
+    w = wl.beam_search(f"beam_{kv}_{Hq}_{width}", requests, width, prompt, gen, Hq, Hkv, D, bs,
+                       seed=gen + width, src_dtype=src, kv_dtype=kv)
+    inp = Inputs(w)
+    g = run_gpu(inp)
+    assert g["err"] == 0
+    o = run_oracle(inp)
+    check_indexing(g, o)
+    check_cache_writes(inp, g, o, whole_pool=True)
+    assert_close(g["out"].numpy(), o["out"], kv, w.name)
+    if kv != "f32" and 8 // (Hq // Hkv) >= 2:
+        assert g["plan"].num_groups > 0                # beams of a request share their prefix
 
 
 @pytest.mark.parametrize("prompt,suffix", [(100, 40), (1200, 900)])
