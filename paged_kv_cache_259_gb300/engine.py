@@ -93,6 +93,25 @@ class PrefillPlan:
                 for k, v in self.host_tensors(pin=non_blocking).items()}
 
 
+def copy_waves(pairs):
+    """Cut a list of (src, dst) block copies, meant to run in order, into
+    consecutive [start, stop) waves that ``copy_blocks`` may run concurrently:
+    within a wave no block is written twice and no block written is also read.
+    A copy that reads or writes a block an earlier copy of the current wave
+    wrote, or writes one it read, starts a new wave. The pairs of one step
+    (fresh destinations) always form a single wave."""
+    waves, start, written, read = [], 0, set(), set()
+    for i, (src, dst) in enumerate(np.asarray(pairs, dtype=np.int64).reshape(-1, 2).tolist()):
+        if src in written or dst in written or dst in read:
+            waves.append((start, i))
+            start, written, read = i, set(), set()
+        written.add(dst)
+        read.add(src)
+    if len(pairs) > start:
+        waves.append((start, len(pairs)))
+    return waves
+
+
 class PagedKVCache:
     def __init__(self, num_blocks, num_heads, num_kv_heads, head_dim, block_size, kv_dtype,
                  free_order, device="cuda", prefix_caching=False, num_host_blocks=0):
@@ -149,8 +168,12 @@ class PagedKVCache:
         return pairs
 
     def apply_copies(self, pairs, stream=None):
-        if len(pairs):
-            t = torch.as_tensor(np.asarray(pairs, dtype=np.int64).reshape(-1, 2), device=self.device)
+        """Apply (src, dst) block copies in list order, e.g. the CoW pairs of a
+        replayed script spanning many steps: one ``copy_blocks`` launch per wave
+        of ``copy_waves``."""
+        pairs = np.asarray(pairs, dtype=np.int64).reshape(-1, 2)
+        for a, b in copy_waves(pairs):
+            t = torch.as_tensor(pairs[a:b], device=self.device)
             copy_blocks(self.k_pool, self.v_pool, t, stream=stream)
 
     def plan_step(self, seq_ids, max_blocks=None, group_prefixes=True):

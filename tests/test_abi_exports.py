@@ -92,3 +92,32 @@ def test_pool_layout_helpers_follow_the_header_formula(dtype, bs, D):
         assert kf[ko] == k[blk, h, t, d] and vf[vo] == v[blk, h, t, d]
     k2, v2 = pkv.pool_views(kp, vp)
     assert torch.equal(k2, k) and torch.equal(v2, v)
+
+
+def test_copy_waves_run_concurrently_give_the_in_order_result():
+    """Host logic of PagedKVCache.apply_copies: pairs cut into waves, each wave
+    applied at once (every destination gets its source as the wave began), must
+    give what applying the pairs one by one gives."""
+    import numpy as np
+    from paged_kv_cache_259_gb300.engine import copy_waves
+    rng = np.random.default_rng(0)
+    for trial in range(200):
+        nb = int(rng.integers(2, 12))
+        pairs = [tuple(rng.choice(nb, 2, replace=False).tolist())
+                 for _ in range(int(rng.integers(0, 20)))]
+        seq = list(range(nb))
+        for s, d in pairs:
+            seq[d] = seq[s]
+        par = list(range(nb))
+        waves = copy_waves(pairs)
+        assert [i for a, b in waves for i in range(a, b)] == list(range(len(pairs)))
+        for a, b in waves:
+            w = pairs[a:b]
+            dsts = [d for _, d in w]
+            assert len(set(dsts)) == len(dsts) and not set(dsts) & {s for s, _ in w}
+            snap = list(par)
+            for s, d in w:
+                par[d] = snap[s]
+        assert par == seq
+    assert copy_waves([(0, 5), (1, 6), (2, 7)]) == [(0, 3)]
+    assert copy_waves([(0, 5), (5, 6)]) == [(0, 1), (1, 2)]
