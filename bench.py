@@ -365,14 +365,14 @@ def run_gpu(args, rank, world, device):
     hq, hk, hv = q.pin_memory(), k_new.pin_memory(), v_new.pin_memory()
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    dplan = {k: torch.empty_like(v) for k, v in dev.items()}
+    dplan = {k: (torch.empty_like(v) if torch.is_tensor(v) else v) for k, v in dev.items()}
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, *host.values()))
     d2h = hout.numel() * hout.element_size()
 
     def e2e_step():
         for src_t, dst_t in ((hq, dq), (hk, dk), (hv, dv)):
             dst_t.copy_(src_t, non_blocking=True)
-        for k in dplan:
+        for k in host:
             dplan[k].copy_(host[k], non_blocking=True)
         cache.step(dq, dk, dv, dplan, out, w.scale, ks, vs, ws)
         hout.copy_(out, non_blocking=True)
@@ -599,14 +599,14 @@ def run_prefill(args, rank, world, device):
     hq, hk, hv = q.pin_memory(), k_new.pin_memory(), v_new.pin_memory()
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    dplan = {k: torch.empty_like(v) for k, v in dev.items()}
+    dplan = {k: (torch.empty_like(v) if torch.is_tensor(v) else v) for k, v in dev.items()}
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, *host.values()))
     d2h = hout.numel() * hout.element_size()
 
     def e2e_step():
         for src_t, dst_t in ((hq, dq), (hk, dk), (hv, dv)):
             dst_t.copy_(src_t, non_blocking=True)
-        for k in dplan:
+        for k in host:
             dplan[k].copy_(host[k], non_blocking=True)
         cache.prefill_step(dq, dk, dv, dplan, out, w.scale, mql, stream=stream)
         hout.copy_(out, non_blocking=True)

@@ -152,6 +152,13 @@ PKV_API int paged_attention_decode(void* out, const void* q,
  *   seq_group            device int32 [num_seqs]: the sequence's group, -1 if none
  *   group_members        device int32 [num_groups][max_members], -1 padded
  *   group_prefix_blocks  device int32 [num_groups]
+ *   max_group_blocks     host int: the longest group's block list (its prefix
+ *                        once plus each member's blocks after it, as
+ *                        bm_prefix_groups reports it); sizes the group CTAs'
+ *                        partitions. <= 0: unknown, max_members *
+ *                        max_blocks_per_seq is assumed. A list longer than
+ *                        this is cut short and sets PKV_ERR_OUT_OF_RANGE in the
+ *                        device error word (wrong outputs, no bad access).
  *   ungrouped_seqs       device int32 [num_ungrouped]: the batch indices in no
  *                        group (they get the regular CTAs); num_ungrouped < 0:
  *                        no list, every sequence is launched and the grouped
@@ -175,7 +182,7 @@ PKV_API int paged_attention_decode_grouped(void* out, const void* q,
                                    const int32_t* seq_group,
                                    const int32_t* group_members,
                                    const int32_t* group_prefix_blocks,
-                                   int num_groups, int max_members,
+                                   int num_groups, int max_members, int max_group_blocks,
                                    const int32_t* ungrouped_seqs, int num_ungrouped,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
@@ -406,12 +413,14 @@ PKV_API int bm_num_free(const pkv_block_manager* bm);
  * batch order, at most max_members per group); a group's prefix is the number
  * of leading block ids common to all members that are full for every member.
  * Writes group_members [n][max_members] (batch indices, -1 padded; at most n
- * groups), group_prefix [n], seq_group [n] (the sequence's group or -1) and
- * *num_groups. Groups with a prefix of 0 blocks or a single member are not
- * emitted. */
+ * groups), group_prefix [n], seq_group [n] (the sequence's group or -1),
+ * group_blocks [n] (may be null: the group's block list for the grouped decode,
+ * its prefix once plus each member's blocks after it; the largest is that
+ * call's max_group_blocks) and *num_groups. Groups with a prefix of 0 blocks or
+ * a single member are not emitted. */
 PKV_API int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
                      int max_members, int32_t* group_members, int32_t* group_prefix,
-                     int32_t* seq_group, int* num_groups);
+                     int32_t* seq_group, int32_t* group_blocks, int* num_groups);
 /* Prefix caching (glossary "Chia sẻ block giữa các chuỗi": requests that begin
  * with the same system prompt reuse one copy of the common prefix, with a count
  * per block; "vLLM PagedAttention: uma revolução...": prefix caching).

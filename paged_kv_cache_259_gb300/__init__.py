@@ -74,8 +74,8 @@ def load_library():
         "paged_attention_decode_grouped": (c_int, [vp, vp, vp, vp, vp, vp, c_int, c_int, c_int,
                                                    c_int, c_int, c_int, c_int, c_float, c_int,
                                                    c_int, c_float, c_float, vp, vp, vp, c_int,
-                                                   c_int, vp, c_int, vp, c_size, vp]),
-        "bm_prefix_groups": (c_int, [vp, i64p, c_int, c_int, i32p, i32p, i32p, ip]),
+                                                   c_int, c_int, vp, c_int, vp, c_size, vp]),
+        "bm_prefix_groups": (c_int, [vp, i64p, c_int, c_int, i32p, i32p, i32p, i32p, ip]),
         "paged_attention_decode_noalloc": (c_int, [vp, vp, vp, vp, vp, vp, c_int, c_int, c_int,
                                                    c_int, c_int, c_int, c_int, c_float, c_int,
                                                    c_int, c_float, c_float, vp]),
@@ -263,13 +263,14 @@ def paged_attention_decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale
 def paged_attention_decode_grouped(out, q, k_pool, v_pool, block_tables, seq_lens, scale,
                                    seq_group, group_members, group_prefix_blocks,
                                    k_scale=1.0, v_scale=1.0, workspace=None, stream=None,
-                                   ungrouped=None):
+                                   ungrouped=None, max_group_blocks=0):
     """``paged_attention_decode`` reading each shared prefix once per group.
 
     seq_group int32 ``[B]`` (group or -1); group_members int32 ``[num_groups,
     max_members]`` (batch indices, -1 padded); group_prefix_blocks int32
     ``[num_groups]`` -- as ``BlockManager.prefix_groups`` returns them; ungrouped:
-    int32 ``[n]`` batch indices in no group (None: every sequence is launched).
+    int32 ``[n]`` batch indices in no group (None: every sequence is launched);
+    max_group_blocks: the largest of ``prefix_groups``' list blocks (0: unknown).
     """
     lib = load_library()
     for t, n in ((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
@@ -301,7 +302,7 @@ def paged_attention_decode_grouped(out, q, k_pool, v_pool, block_tables, seq_len
             Hq, Hkv, D, bs, float(scale), _dt(q, "q"), _dt(k_pool, "k_pool"), float(k_scale),
             float(v_scale), seq_group.data_ptr(), group_members.data_ptr(),
             group_prefix_blocks.data_ptr(), group_members.shape[0], group_members.shape[1],
-            None if ungrouped is None else ungrouped.data_ptr(),
+            int(max_group_blocks), None if ungrouped is None else ungrouped.data_ptr(),
             -1 if ungrouped is None else ungrouped.numel(),
             ws_ptr, ws_bytes, _stream_ptr(stream, q.device))
     _check(st, "paged_attention_decode_grouped")
@@ -560,17 +561,20 @@ class BlockManager:
 
     def prefix_groups(self, seq_ids, max_members):
         """Groups of the batch that share leading full blocks (see bm_prefix_groups):
-        (members int32 [g, max_members], prefix int32 [g], seq_group int32 [n])."""
+        (members int32 [g, max_members], prefix int32 [g], seq_group int32 [n],
+        list blocks int32 [g])."""
         ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
         n = len(ids)
         members = np.full((max(1, n), max_members), -1, dtype=np.int32)
         prefix = np.zeros(max(1, n), dtype=np.int32)
         seq_group = np.full(max(1, n), -1, dtype=np.int32)
+        blocks = np.zeros(max(1, n), dtype=np.int32)
         ng = ctypes.c_int(0)
         _check(self._lib.bm_prefix_groups(self._h, _i64p(ids), n, max_members, _i32p(members),
-                                          _i32p(prefix), _i32p(seq_group), ctypes.byref(ng)),
-               "bm_prefix_groups")
-        return members[:ng.value].copy(), prefix[:ng.value].copy(), seq_group[:n].copy()
+                                          _i32p(prefix), _i32p(seq_group), _i32p(blocks),
+                                          ctypes.byref(ng)), "bm_prefix_groups")
+        g = ng.value
+        return members[:g].copy(), prefix[:g].copy(), seq_group[:n].copy(), blocks[:g].copy()
 
     def seq_len(self, sid):
         n = ctypes.c_int(0)

@@ -412,7 +412,7 @@ int bm_num_free(const pkv_block_manager* bm) { return bm ? (int)bm->free_list.si
 // all members have in common, up to the blocks every member has filled.
 int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n, int max_members,
                      int32_t* group_members, int32_t* group_prefix, int32_t* seq_group,
-                     int* num_groups) {
+                     int32_t* group_blocks, int* num_groups) {
     if (!bm || n < 0 || max_members < 1 || !num_groups ||
         (n > 0 && (!seq_ids || !group_members || !group_prefix || !seq_group)))
         return PKV_ERR_INVALID_ARG;
@@ -457,6 +457,12 @@ int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
             for (int k = 0; k < max_members; ++k)
                 row[k] = c + k < e ? (int32_t)mem[c + k] : -1;
             group_prefix[ng] = (int32_t)prefix;
+            if (group_blocks) {                      // the shared blocks once, then each own tail
+                int64_t list = prefix;
+                for (size_t k = c; k < e; ++k)
+                    list += (seqs[mem[k]]->len + bm->block_size - 1) / bm->block_size - prefix;
+                group_blocks[ng] = (int32_t)std::min<int64_t>(list, INT32_MAX);
+            }
             for (size_t k = c; k < e; ++k) seq_group[mem[k]] = ng;
             ++ng;
         }

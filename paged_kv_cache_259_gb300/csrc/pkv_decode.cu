@@ -31,7 +31,8 @@ int decode_common(void* out, const void* q, const void* k_pool, const void* v_po
                   int head_dim, int block_size, float scale, int q_dtype, int kv_dtype,
                   float k_scale, float v_scale, const int32_t* seq_group,
                   const int32_t* group_members, const int32_t* group_prefix, int num_groups,
-                  int max_members, const int32_t* seq_list, int num_list, void* workspace,
+                  int max_members, int max_group_blocks, const int32_t* seq_list, int num_list,
+                  void* workspace,
                   size_t workspace_bytes, void* stream) {
     using namespace pkv;
     if (num_seqs < 0 || num_seqs > 65535 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
@@ -78,6 +79,7 @@ int decode_common(void* out, const void* q, const void* k_pool, const void* v_po
     a.group_prefix = group_prefix;
     a.num_groups = num_groups;
     a.max_members = max_members;
+    a.max_group_blocks = max_group_blocks;
     a.err = error_word();
     if (!a.err) return PKV_ERR_CUDA;
 
@@ -98,7 +100,7 @@ int paged_attention_decode(void* out, const void* q, const void* k_pool, const v
     return decode_common(out, q, k_pool, v_pool, block_tables, seq_lens, num_seqs,
                          max_blocks_per_seq, num_blocks, num_heads, num_kv_heads, head_dim,
                          block_size, scale, q_dtype, kv_dtype, k_scale, v_scale, nullptr, nullptr,
-                         nullptr, 0, 0, nullptr, 0, workspace, workspace_bytes, stream);
+                         nullptr, 0, 0, 0, nullptr, 0, workspace, workspace_bytes, stream);
 }
 
 int paged_attention_decode_grouped(void* out, const void* q, const void* k_pool,
@@ -108,7 +110,7 @@ int paged_attention_decode_grouped(void* out, const void* q, const void* k_pool,
                                    int block_size, float scale, int q_dtype, int kv_dtype,
                                    float k_scale, float v_scale, const int32_t* seq_group,
                                    const int32_t* group_members, const int32_t* group_prefix_blocks,
-                                   int num_groups, int max_members,
+                                   int num_groups, int max_members, int max_group_blocks,
                                    const int32_t* ungrouped_seqs, int num_ungrouped,
                                    void* workspace, size_t workspace_bytes, void* stream) {
     // num_ungrouped < 0: no list, every sequence gets a regular CTA (grouped ones
@@ -125,7 +127,7 @@ int paged_attention_decode_grouped(void* out, const void* q, const void* k_pool,
                          num_groups > 0 ? seq_group : nullptr,
                          num_groups > 0 ? group_members : nullptr,
                          num_groups > 0 ? group_prefix_blocks : nullptr, num_groups, max_members,
-                         ungrouped_seqs, num_ungrouped, workspace, workspace_bytes, stream);
+                         max_group_blocks, ungrouped_seqs, num_ungrouped, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

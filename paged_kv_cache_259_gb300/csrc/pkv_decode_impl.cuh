@@ -63,6 +63,19 @@ namespace decode {
 #ifndef PKV_PART_BYTES
 #define PKV_PART_BYTES (512 * 1024)
 #endif
+// Group launches: K+V bytes a group-list partition aims at (coarser than a
+// sequence's: a group CTA loads up to 8 query rows and its partials are merged
+// per member row); whole lists while the group CTAs fill PKV_GROUP_WHOLE_WAVES
+// waves; finer partitions while they fill fewer than PKV_GROUP_MIN_WAVES.
+#ifndef PKV_GROUP_PART_BYTES
+#define PKV_GROUP_PART_BYTES (768 * 1024)
+#endif
+#ifndef PKV_GROUP_WHOLE_WAVES
+#define PKV_GROUP_WHOLE_WAVES 4
+#endif
+#ifndef PKV_GROUP_MIN_WAVES
+#define PKV_GROUP_MIN_WAVES 2
+#endif
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -89,6 +102,7 @@ struct Params {
     const int32_t* group_prefix;   // [num_groups] shared full blocks of the group
     int max_members;
     int group_part_blocks;         // partition size of the group launch
+    int group_parts;               // partitions the group launch has (its grid x)
     int slots;                     // workspace slots per (sequence, head)
 };
 
@@ -661,7 +675,11 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
         total = nblk;
     }
     const int PB = p.part_blocks;
-    const int nparts = (total + PB - 1) / PB;
+    int nparts = (total + PB - 1) / PB;
+    if (PREFIX && nparts > (int)gridDim.x) {                // list longer than the caller said
+        if (part == 0 && hk == 0 && threadIdx.x == 0) flag_error(p.err, kErrOutOfRange);
+        nparts = gridDim.x;                                 // wrong result, flagged; in bounds
+    }
     if (part >= (nparts > 0 ? nparts : 1)) return;          // beyond this key's list
     const int blk0 = part * PB;                             // first entry of this partition
     const int nbp = max(0, min(PB, total - blk0));          // entries in this partition
@@ -871,6 +889,7 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const Params p, int B
         }
         if (n == 0) P = 0;
         nparts = (P + sum - n * P + p.group_part_blocks - 1) / p.group_part_blocks;
+        nparts = min(nparts, p.group_parts);               // as the group CTAs clamp it
     } else {
         const int L = min(max(p.seq_lens[b], 0), p.max_blocks * BS);   // as the decode kernel clamps
         nparts = ((L + BS - 1) / BS + p.part_blocks - 1) / p.part_blocks;
@@ -939,6 +958,7 @@ struct Args {
     const int32_t* group_members;
     const int32_t* group_prefix;
     int num_groups, max_members;
+    int max_group_blocks;          // longest group list (prefix + own blocks), <= 0: unknown
 };
 
 constexpr int kNumWarps = PKV_DECODE_WARPS;
@@ -1008,14 +1028,37 @@ int launch_variant(const Args& a) {
     if (st != PKV_OK) return st;
     int parts = 1;
     const int PB = choose_part_blocks(a, P::kTile, occ, 1, &parts);
-    // a group's list is at most max_members tables long: split it like a sequence
-    // when the workspace holds its partials, else one partition per group
-    const int group_list = grouped ? a.max_members * a.max_blocks : 0;
-    int gPB = PB, gparts = grouped ? (group_list + PB - 1) / PB : 0;
-    if (grouped && (parts <= 1 || workspace_need(a.num_seqs, a.num_heads, a.head_dim, gparts) >
-                                       a.workspace_bytes)) {
-        gPB = group_list;
-        gparts = 1;
+    // A group's list is at most max_members tables long, or as long as the
+    // caller's max_group_blocks says. Whole lists, one CTA each, while the group
+    // CTAs fill ~4 waves and no list is longer than twice a sequence partition
+    // (a split costs a merge). Otherwise cut the longest list into equal pieces
+    // of about the sequence partition (finer while the group CTAs make fewer than
+    // ~2 waves) when the workspace holds their partials.
+    int group_list = 0, gPB = 0, gparts = 0;
+    if (grouped) {
+        group_list = a.max_members * a.max_blocks;
+        if (a.max_group_blocks > 0 && a.max_group_blocks < group_list) group_list = a.max_group_blocks;
+        const long long gunits = (long long)a.num_groups * a.num_kv_heads;
+        const long long wave = (long long)num_sms() * (occ > 0 ? occ : 1);
+        int target = PKV_GROUP_PART_BYTES / (2 * P::kTile);
+        target = target < kMinPartBlocks ? kMinPartBlocks : target / kNumWarps * kNumWarps;
+        if (gunits >= PKV_GROUP_WHOLE_WAVES * wave && group_list <= 2 * target) {
+            gparts = 1;
+        } else {
+            gPB = target;
+            while (gPB > kMinPartBlocks &&
+                   gunits * ((group_list + gPB - 1) / gPB) < PKV_GROUP_MIN_WAVES * wave)
+                gPB = gPB / 2 < kMinPartBlocks ? kMinPartBlocks : gPB / 2;
+            gparts = (group_list + gPB - 1) / gPB;
+        }
+        gPB = ((group_list + gparts - 1) / gparts + kNumWarps - 1) / kNumWarps * kNumWarps;
+        gparts = (group_list + gPB - 1) / gPB;
+        if (gparts > 1 && (a.workspace == nullptr ||
+                           workspace_need(a.num_seqs, a.num_heads, a.head_dim, gparts) >
+                               a.workspace_bytes)) {
+            gPB = group_list;
+            gparts = 1;
+        }
     }
     const int slots = gparts > parts ? gparts : parts;
 
@@ -1042,6 +1085,7 @@ int launch_variant(const Args& a) {
     p.group_prefix = grouped ? a.group_prefix : nullptr;
     p.max_members = grouped ? a.max_members : 0;
     p.group_part_blocks = gPB;
+    p.group_parts = gparts;
     p.slots = slots;
     const bool split = slots > 1;
     p.ws_o = split ? static_cast<float*>(a.workspace) : nullptr;

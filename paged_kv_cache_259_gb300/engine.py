@@ -36,6 +36,7 @@ class StepPlan:
     seq_group: np.ndarray = None      # int32 [B]; shared-prefix groups (-1: none)
     group_members: np.ndarray = None  # int32 [g, max_members]
     group_prefix: np.ndarray = None   # int32 [g]
+    group_blocks: np.ndarray = None   # int32 [g]; each group's block list (prefix once)
 
     @property
     def num_groups(self):
@@ -55,8 +56,17 @@ class StepPlan:
         return t
 
     def device_tensors(self, device, non_blocking=False):
-        return {k: v.to(device, non_blocking=non_blocking)
-                for k, v in self.host_tensors(pin=non_blocking).items()}
+        """The host tensors on the device, plus (grouped plans) the host int
+        ``max_group_blocks`` that sizes the group launch."""
+        d = {k: v.to(device, non_blocking=non_blocking)
+             for k, v in self.host_tensors(pin=non_blocking).items()}
+        if self.num_groups:
+            d["max_group_blocks"] = self.max_group_blocks
+        return d
+
+    @property
+    def max_group_blocks(self):
+        return int(self.group_blocks.max()) if self.num_groups else 0
 
     def nbytes(self):
         n = self.slots.nbytes + self.pairs.nbytes + self.tables.nbytes + self.lens.nbytes
@@ -188,9 +198,10 @@ class PagedKVCache:
         plan = StepPlan(ids, slots, pairs, tables, lens)
         if group_prefixes and self.k_pool.dtype != torch.float32:
             max_members = max(1, 8 // (self.num_heads // self.num_kv_heads))
-            members, prefix, seq_group = self.bm.prefix_groups(ids, max_members)
+            members, prefix, seq_group, blocks = self.bm.prefix_groups(ids, max_members)
             if len(members):
                 plan.seq_group, plan.group_members, plan.group_prefix = seq_group, members, prefix
+                plan.group_blocks = blocks
         return plan
 
     def plan_prefill(self, seq_ids, chunks, max_blocks=None):
@@ -277,7 +288,8 @@ class PagedKVCache:
             return paged_attention_decode_grouped(
                 out, q, self.k_pool, self.v_pool, dev_plan["tables"], dev_plan["lens"], scale,
                 dev_plan["seq_group"], dev_plan["group_members"], dev_plan["group_prefix"],
-                k_scale, v_scale, workspace, stream, dev_plan.get("ungrouped"))
+                k_scale, v_scale, workspace, stream, dev_plan.get("ungrouped"),
+                dev_plan.get("max_group_blocks", 0))
         return paged_attention_decode(out, q, self.k_pool, self.v_pool, dev_plan["tables"],
                                       dev_plan["lens"], scale, k_scale, v_scale, workspace, stream)
 

@@ -148,12 +148,14 @@ def test_prefix_groups_share_full_leading_blocks():
                 seqs.append(cid)
         ids = list(rng.permutation(seqs))
         maxm = int(rng.choice([2, 3, 4, 8]))
-        members, prefix, seq_group = a.prefix_groups(ids, maxm)
+        members, prefix, seq_group, blocks = a.prefix_groups(ids, maxm)
         seen = set()
-        for gi, (row, pre) in enumerate(zip(members, prefix)):
+        for gi, (row, pre, nlist) in enumerate(zip(members, prefix, blocks)):
             ms = [int(m) for m in row if m >= 0]
             assert 2 <= len(ms) <= maxm and pre >= 1
             tabs = [o.tables[ids[m]] for m in ms]
+            # the group's list: the shared blocks once, then every member's others
+            assert nlist == pre + sum(len(t) - pre for t in tabs)
             full = min(o.lens[ids[m]] // bs for m in ms)
             assert pre <= full
             assert all(t[:pre] == tabs[0][:pre] for t in tabs)

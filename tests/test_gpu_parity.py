@@ -298,6 +298,36 @@ def test_beam_search_step_matches_oracle(kv, Hq, Hkv, D, bs, requests, width, pr
         assert g["plan"].num_groups > 0                # beams of a request share their prefix
 
 
+def test_group_list_hint_sizes_the_launch_and_a_short_hint_is_flagged():
+    """The engine passes the longest group list (bm_prefix_groups' count); the
+    grouped decode without it (bound max_members x max_blocks) gives the same
+    outputs; a hint shorter than a list cuts it, and the device error says so."""
+    w = wl.beam_search("beam_hint", 3, 4, (300, 900), 40, 8, 8, 128, 16, seed=5)
+    inp = Inputs(w)
+    g = run_gpu(inp)
+    assert g["err"] == 0
+    plan, cache = g["plan"], g["cache"]
+    assert plan.num_groups == 3
+    assert plan.max_group_blocks < plan.group_members.shape[1] * plan.tables.shape[1]
+    o = run_oracle(inp)
+    assert_close(g["out"].numpy(), o["out"], "bf16", "engine (hint)")
+    dev = plan.device_tensors("cuda")
+    ws = cache.workspace(w.B, w.max_blocks_per_seq)
+    q = inp.q.cuda()
+    for hint in (0, plan.max_group_blocks, 1):
+        out = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        pkv.paged_attention_decode_grouped(
+            out, q, cache.k_pool, cache.v_pool, dev["tables"], dev["lens"], w.scale,
+            dev["seq_group"], dev["group_members"], dev["group_prefix"], 1.0, 1.0, ws, None,
+            dev["ungrouped"], hint)
+        err = pkv.get_device_error()
+        if hint == 1:
+            assert err == -4                           # lists longer than the hint
+        else:
+            assert err == 0
+            assert_close(out.float().cpu().numpy(), o["out"], "bf16", f"hint {hint}")
+
+
 @pytest.mark.parametrize("prompt,suffix", [(100, 40), (1200, 900)])
 def test_grouped_decode_without_workspace(prompt, suffix):
     """No workspace: every group list and sequence runs as one partition."""
