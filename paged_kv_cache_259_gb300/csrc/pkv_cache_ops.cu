@@ -117,70 +117,87 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     }
 }
 
-// bf16 caches, written by aligned 8-slot windows. Token i (slot s) looks at the
-// window of slots s - s%8 .. s - s%8 + 7: if tokens i - s%8 .. i - s%8 + 7 fill
-// exactly that window (a prefill chunk away from its two ends), their V values
-// for 8 dims are one whole V core matrix (8 dims x 8 tokens) and their K chunks
-// the 8 rows of one K core matrix, so the window's first token transposes V in
-// registers and writes both as 8 rows of 16 bytes each (the token-by-token path
-// writes V as 64 scattered 2-byte values); the other 7 tokens of the window do
-// nothing. Every token not in such a window (decode steps, ragged chunk ends,
-// padding) is written on its own as above. One thread per (token, kv head,
-// 8-dim chunk).
+// bf16 caches, written by aligned 8-slot windows. One warp per (group of 8
+// consecutive tokens, kv head), walking its 8 tokens. Token i (slot s) looks at
+// the window of slots s - s%8 .. s - s%8 + 7 (8 lanes check 8 slots at once): if
+// tokens i - s%8 .. i - s%8 + 7 fill exactly that window (a prefill chunk away
+// from its two ends), the window is one 8-token chunk of the block, whose K rows
+// (plane j, token) and V rows (dim, 8 tokens) are each 2 KB of contiguous core
+// matrices, and the window's first token writes both with coalesced 16-byte
+// stores: K row j*8+t is token t's 16-byte chunk j, V row dim is that dim of the
+// 8 tokens (gathered as 2-byte loads, lane by lane, already transposed); the
+// window's other tokens are skipped (the walk jumps past them). So nearly every
+// warp moves about one window.
+// Every token not in such a window (decode steps, ragged chunk ends) is written
+// on its own: lane j stores K chunk j and V dims 8j..8j+7 down their column.
+// DT: the head dim when known at compile time (its row loops unroll), else 0.
+template <int DT>
 __global__ void __launch_bounds__(256) reshape_and_cache_bf16_windows(
     const uint4* __restrict__ k, const uint4* __restrict__ v, uint4* __restrict__ k_pool,
-    uint4* __restrict__ v_pool, const int64_t* __restrict__ slots, int num_tokens, int hkv, int d,
-    int bs, int num_blocks, int* err) {
+    uint4* __restrict__ v_pool, const int64_t* __restrict__ slots, int num_tokens, int hkv,
+    int d_rt, int bs, int num_blocks, int* err) {
+    const int d = DT ? DT : d_rt;
     const int planes = d / 8;                              // 16-byte chunks per (token, head)
-    const long long total = (long long)num_tokens * hkv * planes;
+    const int lane = threadIdx.x & 31;
+    const long long units = (long long)((num_tokens + 7) / 8) * hkv;
     const long long slot_limit = (long long)num_blocks * bs;
-    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
-         idx += (long long)gridDim.x * blockDim.x) {
-        const int j = (int)(idx % planes);
-        const long long r = idx / planes;
-        const int h = (int)(r % hkv);
-        const int t = (int)(r / hkv);
-        const long long slot = slots[t];
-        if (slot < 0) continue;                            // padding token
-        if (slot >= slot_limit) {
-            flag_error(err, kErrOutOfRange);
-            continue;
-        }
-        const int lead = t - (int)(slot & 7);              // first token of the window
-        bool run = lead >= 0 && lead + 8 <= num_tokens && (slot | 7) < slot_limit;
-        if (run) {                                         // tokens lead..lead+7 exist
-#pragma unroll
-            for (int i = 0; i < 8; ++i) run = run && slots[lead + i] == (slot & ~7LL) + i;
-        }
-        const long long blk = slot / bs, off = slot % bs;
-        const long long tile = (blk * hkv + h) * (long long)(d * bs / 8);   // 16-byte units
-        if (!run) {
-            const long long src = ((long long)t * hkv + h) * planes + j;
-            k_pool[tile + ((off >> 3) * planes + j) * 8 + (off & 7)] = k[src];
-            store_v_column(reinterpret_cast<__nv_bfloat16*>(v_pool + tile), v[src], j * 8, d,
-                           (int)off);
-            continue;
-        }
-        if (t != lead) continue;                           // written by the window's first token
-        const long long cm = tile + ((off >> 3) * planes + j) * 8;   // core matrix (off/8, j)
-        uint4 vv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const long long src = ((long long)(lead + i) * hkv + h) * planes + j;
-            k_pool[cm + i] = k[src];
-            vv[i] = v[src];
-        }
-#pragma unroll
-        for (int dd = 0; dd < 8; ++dd) {
-            const uint32_t sel = (dd & 1) ? 0x7632u : 0x5410u;   // high or low halves
-            uint32_t w[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const uint32_t* a = reinterpret_cast<const uint32_t*>(&vv[2 * m]);
-                const uint32_t* b = reinterpret_cast<const uint32_t*>(&vv[2 * m + 1]);
-                w[m] = __byte_perm(a[dd >> 1], b[dd >> 1], sel);   // tokens 2m, 2m+1 of dim dd
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    const unsigned short* vh = reinterpret_cast<const unsigned short*>(v);
+    for (long long u = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5); u < units;
+         u += warps) {
+        const int grp = (int)(u / hkv), h = (int)(u - (long long)grp * hkv);
+        // after a token that is in a window, jump past the window's end
+        for (int q = 0, step = 1; q < 8; q += step) {
+            step = 1;
+            const int t = grp * 8 + q;
+            if (t >= num_tokens) break;
+            const long long slot = slots[t];
+            if (slot < 0) continue;                        // padding token
+            if (slot >= slot_limit) {
+                if (lane == 0) flag_error(err, kErrOutOfRange);
+                continue;
             }
-            v_pool[cm + dd] = make_uint4(w[0], w[1], w[2], w[3]);
+            const int lead = t - (int)(slot & 7);          // first token of the window
+            bool ok = true;
+            if (lane < 8) {
+                ok = lead >= 0 && lead + 8 <= num_tokens && (slot | 7) < slot_limit &&
+                     slots[lead >= 0 && lead + lane < num_tokens ? lead + lane : t] ==
+                         (slot & ~7LL) + lane;
+            }
+            const bool run = __all_sync(0xffffffffu, ok);
+            if (run) step = lead + 8 - t;                  // the window's tokens are done here
+            if (run && t != lead) continue;                // written by the window's first token
+            const long long blk = slot / bs, off = slot - blk * bs;
+            const long long tile = (blk * hkv + h) * (long long)(d * bs / 8);   // 16-byte units
+            if (run) {
+                const long long base = tile + (off >> 3) * planes * 8;   // the window's core matrices
+                constexpr int kIters = DT ? DT / 32 : 1;
+#pragma unroll
+                for (int it = 0; it < kIters; ++it) {
+                    for (int o = lane + it * 32; o < planes * 8; o += kIters * 32) {
+                        // K row o: token o % 8, chunk o / 8
+                        const uint4 kk =
+                            k[((long long)(lead + (o & 7)) * hkv + h) * planes + (o >> 3)];
+                        // V row o: dim o of the 8 tokens
+                        uint32_t w[4];
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const uint32_t lo = vh[((long long)(lead + 2 * m) * hkv + h) * d + o];
+                            const uint32_t hi = vh[((long long)(lead + 2 * m + 1) * hkv + h) * d + o];
+                            w[m] = lo | (hi << 16);
+                        }
+                        k_pool[base + o] = kk;
+                        v_pool[base + o] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+                continue;
+            }
+            if (lane < planes) {                           // this token alone
+                const long long src = ((long long)t * hkv + h) * planes + lane;
+                k_pool[tile + ((off >> 3) * planes + lane) * 8 + (off & 7)] = k[src];
+                store_v_column(reinterpret_cast<__nv_bfloat16*>(v_pool + tile), v[src], lane * 8,
+                               d, (int)off);
+            }
         }
     }
 }
@@ -287,14 +304,17 @@ constexpr int kGroupTokens = 512;
 cudaError_t launch_reshape_groups(const void* k, const void* v, void* kp, void* vp,
                                   const int64_t* slots, int num_tokens, int hkv, int d, int bs,
                                   int num_blocks, int* err, cudaStream_t stream) {
-    const long long items = (long long)num_tokens * hkv * (d / 8);
+    const long long items = (long long)((num_tokens + 7) / 8) * hkv;   // one warp each
     const int threads = 256;
-    long long blocks = (items + threads - 1) / threads;
+    long long blocks = (items + threads / 32 - 1) / (threads / 32);
     const long long cap = 8LL * num_sms();
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     note_launch();
-    reshape_and_cache_bf16_windows<<<(unsigned)blocks, threads, 0, stream>>>(
+    auto kern = d == 128 ? reshape_and_cache_bf16_windows<128>
+                         : d == 64 ? reshape_and_cache_bf16_windows<64>
+                                   : reshape_and_cache_bf16_windows<0>;
+    kern<<<(unsigned)blocks, threads, 0, stream>>>(
         static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(kp),
         static_cast<uint4*>(vp), slots, num_tokens, hkv, d, bs, num_blocks, err);
     return cudaGetLastError();
