@@ -146,24 +146,27 @@ __global__ void __launch_bounds__(256) reshape_and_cache_bf16_windows(
     for (long long u = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5); u < units;
          u += warps) {
         const int grp = (int)(u / hkv), h = (int)(u - (long long)grp * hkv);
+        // the slots of tokens grp*8-8 .. grp*8+15 (every window a token of this
+        // group can be in), one per lane, read once; -1 outside the batch
+        const int t_lo = grp * 8 - 8;
+        const long long near =
+            lane < 24 && t_lo + lane >= 0 && t_lo + lane < num_tokens ? slots[t_lo + lane] : -1LL;
         // after a token that is in a window, jump past the window's end
         for (int q = 0, step = 1; q < 8; q += step) {
             step = 1;
             const int t = grp * 8 + q;
             if (t >= num_tokens) break;
-            const long long slot = slots[t];
+            const long long slot = __shfl_sync(0xffffffffu, near, 8 + q);
             if (slot < 0) continue;                        // padding token
             if (slot >= slot_limit) {
                 if (lane == 0) flag_error(err, kErrOutOfRange);
                 continue;
             }
             const int lead = t - (int)(slot & 7);          // first token of the window
-            bool ok = true;
-            if (lane < 8) {
-                ok = lead >= 0 && lead + 8 <= num_tokens && (slot | 7) < slot_limit &&
-                     slots[lead >= 0 && lead + lane < num_tokens ? lead + lane : t] ==
-                         (slot & ~7LL) + lane;
-            }
+            // lane i < 8 compares token lead + i's slot (lane lead - t_lo + i of `near`)
+            const long long other = __shfl_sync(0xffffffffu, near, (lead - t_lo + (lane & 7)) & 31);
+            const bool ok = lane >= 8 || (lead >= 0 && lead + 8 <= num_tokens &&
+                                          (slot | 7) < slot_limit && other == (slot & ~7LL) + lane);
             const bool run = __all_sync(0xffffffffu, ok);
             if (run) step = lead + 8 - t;                  // the window's tokens are done here
             if (run && t != lead) continue;                // written by the window's first token
