@@ -302,3 +302,94 @@ class PagedKVCache:
         reshape_and_cache(k_new, v_new, self.k_pool, self.v_pool, dev_plan["slots"],
                           k_scale, v_scale, stream=stream)
         return self.decode(q, dev_plan, out, scale, k_scale, v_scale, workspace, stream)
+
+
+class StepPipeline:
+    """Decode steps fed from host memory, with the copies overlapped.
+
+    The inputs of a step (q, k_new, v_new and the plan's tensors) live in one
+    pinned host slab per buffer set (``host_inputs(i)`` gives step i's views to
+    fill in); ``submit`` uploads the slab with one copy on an upload stream, runs
+    the step on the compute stream once it has landed, and reads the output back
+    into the given pinned buffer on a download stream as soon as the step is
+    done. Two buffer sets alternate, so step i+1's upload runs while step i
+    computes and step i's download while step i+1 computes; steps run in
+    submission order on the compute stream (the cache writes stay ordered).
+
+    ``templates``: tensors shaped like q, k_new, v_new and every plan tensor (a
+    first step's ``StepPlan.host_tensors`` plus q and the new K/V), and any host
+    values the plan carries (``max_group_blocks``); ``out_template`` is shaped
+    like the output. Step i's host views may be rewritten once step i-2's
+    ``uploaded`` event has completed (``host_inputs`` waits for it), and its
+    output read once its ``downloaded`` event has.
+    """
+
+    _ALIGN = 256
+
+    def __init__(self, cache, templates, out_template, stream=None):
+        self.cache = cache
+        self.device = cache.device
+        self.compute = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self.up = torch.cuda.Stream(self.device)
+        self.down = torch.cuda.Stream(self.device)
+        self.extra = {k: v for k, v in templates.items() if not torch.is_tensor(v)}
+        self.layout, off = {}, 0
+        for k, t in templates.items():
+            if torch.is_tensor(t):
+                nbytes = t.numel() * t.element_size()
+                self.layout[k] = (off, t.dtype, tuple(t.shape))
+                off += -(-nbytes // self._ALIGN) * self._ALIGN
+        self.slab_bytes = max(off, self._ALIGN)
+        self.host_slabs = [torch.empty(self.slab_bytes, dtype=torch.uint8).pin_memory()
+                           for _ in range(2)]
+        self.dev_slabs = [torch.empty(self.slab_bytes, dtype=torch.uint8, device=self.device)
+                          for _ in range(2)]
+        self.outs = [torch.empty_like(out_template, device=self.device) for _ in range(2)]
+        self.steps = []                                   # per slab: (q, k_new, v_new, plan)
+        for slab in self.dev_slabs:
+            dev = self._views(slab)
+            plan = {k: v for k, v in dev.items() if k not in ("q", "k_new", "v_new")}
+            plan.update(self.extra)
+            self.steps.append((dev["q"], dev["k_new"], dev["v_new"], plan))
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]
+        self.uploaded, self.computed, self.downloaded = ev(), ev(), ev()
+        self.n = 0
+
+    def _views(self, slab):
+        out = {}
+        for k, (off, dtype, shape) in self.layout.items():
+            n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            out[k] = slab[off:off + n].view(dtype).view(shape)
+        return out
+
+    def host_inputs(self, i=None):
+        """Pinned views to fill with step i's inputs (default: the next step)."""
+        i = self.n if i is None else i
+        if i >= 2:
+            self.uploaded[i % 2].synchronize()            # step i-2's slab has been read
+        return self._views(self.host_slabs[i % 2])
+
+    def submit(self, host_out, scale, k_scale=1.0, v_scale=1.0, workspace=None):
+        """Run the next step from its filled host views; ``host_out`` = pinned
+        buffer the output is read back into. Returns the step's (uploaded,
+        downloaded) events."""
+        b = self.n % 2
+        out = self.outs[b]
+        if self.n >= 2:
+            self.up.wait_event(self.computed[b])          # step n-2 is done with this slab
+        with torch.cuda.stream(self.up):
+            self.dev_slabs[b].copy_(self.host_slabs[b], non_blocking=True)
+        self.uploaded[b].record(self.up)
+        self.compute.wait_event(self.uploaded[b])
+        if self.n >= 2:
+            self.compute.wait_event(self.downloaded[b])   # step n-2's output was read
+        q, k_new, v_new, plan = self.steps[b]
+        self.cache.step(q, k_new, v_new, plan, out, scale, k_scale, v_scale, workspace,
+                        self.compute)
+        self.computed[b].record(self.compute)
+        self.down.wait_event(self.computed[b])
+        with torch.cuda.stream(self.down):
+            host_out.copy_(out, non_blocking=True)
+        self.downloaded[b].record(self.down)
+        self.n += 1
+        return self.uploaded[b], self.downloaded[b]

@@ -385,3 +385,51 @@ def test_reshape_and_cache_large_batch_runs_and_ragged_slots():
     kv, vv = pkv.pool_views(kp, vp)
     assert torch.equal(kv.cpu().view(torch.int16), kr.view(torch.int16))
     assert torch.equal(vv.cpu().view(torch.int16), vr.view(torch.int16))
+
+
+def test_step_pipeline_matches_serial_steps():
+    """engine.StepPipeline (uploads and downloads overlapped with the compute of
+    neighbouring steps, two device buffer sets) gives, step by step, exactly the
+    outputs of the same steps run one after another with device inputs."""
+    from paged_kv_cache_259_gb300.engine import StepPipeline
+    w = wl.shared_prefix(fork_step=True, groups=3, per_group=4, prompt=150, max_suffix=40,
+                         Hq=8, Hkv=8, seed=9)
+    n = 4
+    gen = torch.Generator().manual_seed(4)
+    qs = [torch.randn(w.B, w.Hq, w.D, generator=gen).to(torch.bfloat16) for _ in range(n)]
+    ks = [torch.randn(w.B, w.Hkv, w.D, generator=gen).to(torch.bfloat16) for _ in range(n)]
+    vs = [torch.randn(w.B, w.Hkv, w.D, generator=gen).to(torch.bfloat16) for _ in range(n)]
+    outs = {}
+    for mode in ("serial", "pipelined"):
+        inp = Inputs(w)
+        g = run_gpu(inp)                                   # same set-up and first step
+        cache, plan = g["cache"], g["plan"]
+        assert plan.num_groups > 0
+        ws = cache.workspace(w.B, w.max_blocks_per_seq)
+        res = []
+        if mode == "serial":
+            dev = plan.device_tensors("cuda")
+            for i in range(n):
+                o = torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16, device="cuda")
+                cache.step(qs[i].cuda(), ks[i].cuda(), vs[i].cuda(), dev, o, w.scale, workspace=ws)
+                res.append(o.cpu())
+        else:
+            host = plan.host_tensors(pin=False)
+            tmpl = dict(host, q=qs[0], k_new=ks[0], v_new=vs[0],
+                        max_group_blocks=plan.max_group_blocks)
+            pipe = StepPipeline(cache, tmpl, torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16,
+                                                         device="cuda"))
+            houts = [torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16).pin_memory()
+                     for _ in range(n)]
+            for i in range(n):
+                views = pipe.host_inputs()
+                for k, t in dict(host, q=qs[i], k_new=ks[i], v_new=vs[i]).items():
+                    views[k].copy_(t)
+                pipe.submit(houts[i], w.scale, workspace=ws)
+            torch.cuda.synchronize()
+            res = houts
+        assert pkv.get_device_error() == 0
+        outs[mode] = res
+    for a, b in zip(outs["serial"], outs["pipelined"]):
+        assert torch.equal(a, b)
+    assert not torch.equal(outs["serial"][0], outs["serial"][1])
