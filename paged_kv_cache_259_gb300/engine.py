@@ -321,13 +321,18 @@ class StepPipeline:
     values the plan carries (``max_group_blocks``); ``out_template`` is shaped
     like the output. Step i's host views may be rewritten once step i-2's
     ``uploaded`` event has completed (``host_inputs`` waits for it), and its
-    output read once its ``downloaded`` event has.
+    output read once its ``downloaded`` event has. ``run(q, k_new, v_new, plan,
+    out, stream)`` is the device half of a step; by default a decode step
+    (``PagedKVCache.step``; ``submit`` passes its scales and workspace), for a
+    chunked-prefill step e.g. ``lambda q, k, v, plan, out, s:
+    cache.prefill_step(q, k, v, plan, out, scale, max_query_len, stream=s)``.
     """
 
     _ALIGN = 256
 
-    def __init__(self, cache, templates, out_template, stream=None):
+    def __init__(self, cache, templates, out_template, stream=None, run=None):
         self.cache = cache
+        self.run = run
         self.device = cache.device
         self.compute = stream if stream is not None else torch.cuda.current_stream(self.device)
         self.up = torch.cuda.Stream(self.device)
@@ -369,7 +374,7 @@ class StepPipeline:
             self.uploaded[i % 2].synchronize()            # step i-2's slab has been read
         return self._views(self.host_slabs[i % 2])
 
-    def submit(self, host_out, scale, k_scale=1.0, v_scale=1.0, workspace=None):
+    def submit(self, host_out, scale=None, k_scale=1.0, v_scale=1.0, workspace=None):
         """Run the next step from its filled host views; ``host_out`` = pinned
         buffer the output is read back into. Returns the step's (uploaded,
         downloaded) events."""
@@ -384,8 +389,11 @@ class StepPipeline:
         if self.n >= 2:
             self.compute.wait_event(self.downloaded[b])   # step n-2's output was read
         q, k_new, v_new, plan = self.steps[b]
-        self.cache.step(q, k_new, v_new, plan, out, scale, k_scale, v_scale, workspace,
-                        self.compute)
+        if self.run is None:
+            self.cache.step(q, k_new, v_new, plan, out, scale, k_scale, v_scale, workspace,
+                            self.compute)
+        else:
+            self.run(q, k_new, v_new, plan, out, self.compute)
         self.computed[b].record(self.compute)
         self.down.wait_event(self.computed[b])
         with torch.cuda.stream(self.down):
