@@ -191,6 +191,24 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
         tc::alloc(smem_addr(&tmem_slot), kTmemCols);
         tc::relinquish_alloc_permit();
     }
+    // The first DRAM reads go out before the set-up barrier: each softmax
+    // thread's q row, and the loaders' first two windows of block ids (a row's
+    // first 64 entries are inside the table whatever the length; they are
+    // checked where they are used)
+    uint4 q_early[kD / 8];
+    int bt_early0 = 0, bt_early1 = 0;
+    if (warp < 4) {
+        const int il = tid / G;
+        const bool v_ok = i0 + il < C;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + ((size_t)(q0 + (v_ok ? i0 + il : 0)) * p.num_heads + hk * G + tid % G) * kD);
+#pragma unroll
+        for (int c = 0; c < kD / 8; ++c) q_early[c] = v_ok ? src[c] : make_uint4(0, 0, 0, 0);
+    } else if (warp == kKLoadWarp || warp == kVLoadWarp) {
+        const int32_t* bt = p.block_tables + (size_t)b * p.max_blocks;
+        if (lane < p.max_blocks) bt_early0 = bt[lane];
+        if (32 + lane < p.max_blocks) bt_early1 = bt[32 + lane];
+    }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -206,6 +224,14 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
         const int tail = L % BS;                           // tokens in a partly written last block
         // block ids in a window of 32 blocks, one per lane, with the next window
         // fetched a window ahead, so table reads never wait on the copies
+        auto check_id = [&](int blk, int id) {
+            if (blk > blk_last) return 0;
+            if (id < 0 || id >= p.num_blocks) {
+                flag_error(p.err, kErrOutOfRange);
+                return 0;                                  // in bounds; the sequence is in error
+            }
+            return id;
+        };
         auto fetch_id = [&](int blk) {
             if (blk > blk_last) return 0;
             const int id = bt[blk];
@@ -216,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
             return id;
         };
         int win = 0;
-        int win_ids = fetch_id(lane), next_ids = fetch_id(32 + lane);
+        int win_ids = check_id(lane, bt_early0), next_ids = check_id(32 + lane, bt_early1);
         for (int j = 0; j < n_tiles; ++j) {
             if ((j * kBlocksPerTile) / 32 != win) {
                 ++win;
@@ -343,14 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
         const uint32_t row = tmem + ((uint32_t)(warp * 32) << 16);
         bool ok = true;
         {
-            const uint4* src = reinterpret_cast<const uint4*>(
-                p.q + ((size_t)(q0 + (valid ? i : 0)) * p.num_heads + h) * kD);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t v[32];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const uint4 x = valid ? src[half * 8 + u] : make_uint4(0, 0, 0, 0);
+                    const uint4 x = q_early[half * 8 + u];
                     v[4 * u] = x.x;
                     v[4 * u + 1] = x.y;
                     v[4 * u + 2] = x.z;
@@ -464,25 +488,25 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
         } else {
             const float inv = 1.f / l_run;
             uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)(q0 + (valid ? i : 0)) * p.num_heads + h) * kD);
+            uint32_t ov[4][32];
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t v[32];
-                tc::ld32(row + kColO + cb * 32, v);
-                tc::wait_ld();
-                if (valid) {
+            for (int cb = 0; cb < 4; ++cb) tc::ld32(row + kColO + cb * 32, ov[cb]);
+            tc::wait_ld();
+            if (valid) {
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb)
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         uint32_t w[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const __nv_bfloat162 h2 = __floats2bfloat162_rn(
-                                __uint_as_float(v[8 * u + 2 * e]) * inv,
-                                __uint_as_float(v[8 * u + 2 * e + 1]) * inv);
+                                __uint_as_float(ov[cb][8 * u + 2 * e]) * inv,
+                                __uint_as_float(ov[cb][8 * u + 2 * e + 1]) * inv);
                             w[e] = *reinterpret_cast<const uint32_t*>(&h2);
                         }
                         dst[cb * 4 + u] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
-                }
             }
         }
     }
