@@ -304,6 +304,27 @@ class PagedKVCache:
         return self.decode(q, dev_plan, out, scale, k_scale, v_scale, workspace, stream)
 
 
+def slab_layout(templates, align=256):
+    """Byte offsets of the tensors of ``templates`` packed one after another into
+    one buffer, each start a multiple of ``align``: ({name: (offset, dtype,
+    shape)}, total bytes). Non-tensor entries are left out."""
+    layout, off = {}, 0
+    for k, t in templates.items():
+        if torch.is_tensor(t):
+            layout[k] = (off, t.dtype, tuple(t.shape))
+            off += -(-(t.numel() * t.element_size()) // align) * align
+    return layout, max(off, align)
+
+
+def slab_views(slab, layout):
+    """Typed views of a uint8 buffer laid out by ``slab_layout``."""
+    out = {}
+    for k, (off, dtype, shape) in layout.items():
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        out[k] = slab[off:off + n].view(dtype).view(shape)
+    return out
+
+
 class StepPipeline:
     """Decode steps fed from host memory, with the copies overlapped.
 
@@ -338,13 +359,7 @@ class StepPipeline:
         self.up = torch.cuda.Stream(self.device)
         self.down = torch.cuda.Stream(self.device)
         self.extra = {k: v for k, v in templates.items() if not torch.is_tensor(v)}
-        self.layout, off = {}, 0
-        for k, t in templates.items():
-            if torch.is_tensor(t):
-                nbytes = t.numel() * t.element_size()
-                self.layout[k] = (off, t.dtype, tuple(t.shape))
-                off += -(-nbytes // self._ALIGN) * self._ALIGN
-        self.slab_bytes = max(off, self._ALIGN)
+        self.layout, self.slab_bytes = slab_layout(templates, self._ALIGN)
         self.host_slabs = [torch.empty(self.slab_bytes, dtype=torch.uint8).pin_memory()
                            for _ in range(2)]
         self.dev_slabs = [torch.empty(self.slab_bytes, dtype=torch.uint8, device=self.device)
@@ -361,11 +376,7 @@ class StepPipeline:
         self.n = 0
 
     def _views(self, slab):
-        out = {}
-        for k, (off, dtype, shape) in self.layout.items():
-            n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
-            out[k] = slab[off:off + n].view(dtype).view(shape)
-        return out
+        return slab_views(slab, self.layout)
 
     def host_inputs(self, i=None):
         """Pinned views to fill with step i's inputs (default: the next step)."""

@@ -121,3 +121,30 @@ def test_copy_waves_run_concurrently_give_the_in_order_result():
         assert par == seq
     assert copy_waves([(0, 5), (1, 6), (2, 7)]) == [(0, 3)]
     assert copy_waves([(0, 5), (5, 6)]) == [(0, 1), (1, 2)]
+
+
+def test_step_pipeline_slab_layout_packs_every_input_once_aligned():
+    """Host logic of engine.StepPipeline: a step's inputs share one slab; each
+    view starts on a 256-byte boundary, keeps its dtype and shape, and no two
+    views overlap (empty tensors included); values round-trip."""
+    import torch
+    from paged_kv_cache_259_gb300.engine import slab_layout, slab_views
+    t = {"q": torch.randn(3, 5, 8).to(torch.bfloat16), "slots": torch.arange(3, dtype=torch.int64),
+         "pairs": torch.zeros((0, 2), dtype=torch.int64),
+         "tables": torch.arange(21, dtype=torch.int32).view(3, 7), "lens": torch.ones(3, dtype=torch.int32),
+         "max_group_blocks": 9}
+    layout, nbytes = slab_layout(t)
+    assert set(layout) == {"q", "slots", "pairs", "tables", "lens"}
+    spans = []
+    for k, (off, dtype, shape) in layout.items():
+        assert off % 256 == 0 and dtype == t[k].dtype and shape == tuple(t[k].shape)
+        spans.append((off, off + t[k].numel() * t[k].element_size()))
+    spans.sort()
+    assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:])) and spans[-1][1] <= nbytes
+    slab = torch.zeros(nbytes, dtype=torch.uint8)
+    views = slab_views(slab, layout)
+    for k, v in views.items():
+        v.copy_(t[k])
+    again = slab_views(slab, layout)
+    for k in layout:
+        assert torch.equal(again[k], t[k])
