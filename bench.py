@@ -987,6 +987,8 @@ def swap_main(args, rank, world, device):
             "frac": round(achieved / peak, 4), "traffic": None,
             "peak_source": ("measured in this run: one contiguous cudaMemcpyAsync of the same "
                             "bytes device->pinned host plus one back (copy engines)"),
+            "traffic_note": "null: the bound is the host link; the device side reads and "
+                            "writes the same block bytes once",
             "bytes_per_launch": dir_bytes,
             "ms_per_launch": round((out_ms + in_ms) / 2, 5),
         },
