@@ -832,6 +832,109 @@ def copy_engine_rate(nbytes, device, reps=5):
     return 2 * nbytes / ((best["d2h"] + best["h2d"]) * 1e-3) / 1e9, best
 
 
+def swap_copy_engine_path(cache, sw, stream, n):
+    """The same swap steps with the host link crossed by the copy engines: a
+    gather launch (HBM to HBM) into a contiguous staging buffer, one
+    cudaMemcpyAsync per run of consecutive host blocks each way, a scatter
+    launch. Pairs and runs planned beforehand; returns GB/s over n steps and a
+    callable that issues the next planned step on a stream."""
+    import paged_kv_cache_259_gb300 as pkv
+    from paged_kv_cache_259_gb300.engine import host_runs
+    dev = cache.device
+    P = sw.victim_blocks
+    sk, sv = cache._staging(P)
+    idx = np.arange(P)
+    plans = []
+    for o, i in swap_plans(cache.bm, sw.victims, n + 3 + 64):
+        plans.append((torch.as_tensor(np.stack([o[:, 0], idx], 1), device=dev), host_runs(o[:, 1]),
+                      torch.as_tensor(np.stack([idx, i[:, 1]], 1), device=dev), host_runs(i[:, 0])))
+    state = {"next": 0}
+
+    def step(st):
+        go, ro, si, ri = plans[state["next"]]
+        state["next"] += 1
+        pkv.swap_blocks(sk, sv, cache.k_pool, cache.v_pool, go, st)
+        with torch.cuda.stream(st):
+            for a, b, h in ro:
+                cache.host_k[h:h + b - a].copy_(sk[a:b], non_blocking=True)
+                cache.host_v[h:h + b - a].copy_(sv[a:b], non_blocking=True)
+            for a, b, h in ri:
+                sk[a:b].copy_(cache.host_k[h:h + b - a], non_blocking=True)
+                sv[a:b].copy_(cache.host_v[h:h + b - a], non_blocking=True)
+        pkv.swap_blocks(cache.k_pool, cache.v_pool, sk, sv, si, st)
+
+    for _ in range(3):
+        step(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if pkv.get_device_error() != 0:
+        raise RuntimeError("device error in the copy-engine swap steps")
+    ms = e0.elapsed_time(e1) / n
+    runs = np.mean([len(p_[1]) + len(p_[3]) for p_ in plans[:n]])
+    return {"gbs": round(2 * P * 2 * cache.k_pool[0].numel() * cache.k_pool.element_size() /
+                         (ms * 1e-3) / 1e9, 2),
+            "ms_per_step": round(ms, 5), "host_runs_per_step": float(runs), "step": step}
+
+
+def swap_overlap(cache, sw, w, device, ce_path, others, plan):
+    """Decode steps of the sequences that stay on the device (``others``, their
+    step ``plan``), on one stream, while one swap step (all victims out, then
+    in) runs on another: the time of the two together against each alone, for
+    the SM-kernel swap and for the copy-engine one."""
+    import paged_kv_cache_259_gb300 as pkv
+    dev = plan.device_tensors(device)
+    q, k_new, v_new = (t[others].to(device) for t in w.step_inputs())
+    out = torch.empty(len(others), w.Hq, w.D, dtype=torch.bfloat16, device=device)
+    ws = cache.workspace(len(others), w.max_blocks_per_seq)
+    sa, sb = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    P = sw.victim_blocks
+    kplans = [(torch.as_tensor(o, device=device), torch.as_tensor(i, device=device))
+              for o, i in swap_plans(cache.bm, sw.victims, 8)]
+    kstate = {"next": 0}
+
+    def kernel_swap(st):
+        o, i = kplans[kstate["next"]]
+        kstate["next"] += 1
+        pkv.swap_blocks(cache.host_k, cache.host_v, cache.k_pool, cache.v_pool, o, st)
+        pkv.swap_blocks(cache.k_pool, cache.v_pool, cache.host_k, cache.host_v, i, st)
+
+    def decode(st, m):
+        for _ in range(m):
+            cache.step(q, k_new, v_new, dev, out, w.scale, workspace=ws, stream=st)
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(sa)
+        sb.wait_event(e0)
+        fn()
+        done = torch.cuda.Event()
+        done.record(sb)
+        sa.wait_event(done)
+        e1.record(sa)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    decode(sa, 5)
+    t1 = timed(lambda: decode(sa, 20)) / 20
+    ts_k = timed(lambda: kernel_swap(sb))
+    ts_c = timed(lambda: ce_path["step"](sb))
+    m = max(1, int(round(ts_c / t1)))
+    alone = timed(lambda: decode(sa, m))
+    both_k = timed(lambda: (kernel_swap(sb), decode(sa, m)))
+    both_c = timed(lambda: (ce_path["step"](sb), decode(sa, m)))
+    if pkv.get_device_error() != 0:
+        raise RuntimeError("device error in the overlap steps")
+    return {"decode_batch": len(others), "decode_steps": m, "decode_ms": round(alone, 4),
+            "swap_ms_kernel": round(ts_k, 4), "swap_ms_copy_engines": round(ts_c, 4),
+            "together_ms_kernel": round(both_k, 4), "together_ms_copy_engines": round(both_c, 4)}
+
+
 def swap_oracle_state(sw, k_src, v_src):
     """The oracle's block manager after the workload's script, with its pools."""
     from oracle.block_manager import BlockManager as OracleBM
@@ -959,6 +1062,12 @@ def swap_main(args, rank, world, device):
     if pkv.get_device_error() != 0:
         raise RuntimeError("device error in the end-to-end steps")
     peak, ce = copy_engine_rate(dir_bytes, device)
+    # the staying sequences' decode plan first: their blocks are then never a
+    # destination of the swaps planned after it
+    others = [s_ for s_ in range(w.B) if s_ not in sw.victims]
+    dplan = cache.plan_step(others, max_blocks=w.max_blocks_per_seq)
+    ce_path = swap_copy_engine_path(cache, sw, stream, max(3, K // 2))
+    overlap = swap_overlap(cache, sw, w, device, ce_path, others, dplan)
     if rank != 0:
         return
     gbs, steps = swap_oracle_timing(sw, k_src, v_src, args.cpu_budget, 1)
@@ -980,6 +1089,8 @@ def swap_main(args, rank, world, device):
             "swap_in_gbs": round(dir_bytes / (in_ms * 1e-3) / 1e9, 2),
             "copy_engine_ms": {k: round(v, 5) for k, v in ce.items()},
             "sequences_swapped_per_s": round(world * 2 * len(sw.victims) / (ms * 1e-3), 1),
+            "copy_engine_path": {k: v for k, v in ce_path.items() if k != "step"},
+            "overlap_with_decode": overlap,
         },
         "roofline": {
             "kernel": "swap_blocks (out + in)", "bound": "host-link",

@@ -103,6 +103,19 @@ class PrefillPlan:
                 for k, v in self.host_tensors(pin=non_blocking).items()}
 
 
+def host_runs(host_ids):
+    """Runs of consecutive host block ids in a list: (start, stop, first id)
+    triples, so block ``host_ids[i]`` for ``start <= i < stop`` is ``first id +
+    i - start``."""
+    ids = np.asarray(host_ids, dtype=np.int64).reshape(-1)
+    runs, a = [], 0
+    for i in range(1, len(ids) + 1):
+        if i == len(ids) or ids[i] != ids[i - 1] + 1:
+            runs.append((a, i, int(ids[a])))
+            a = i
+    return runs
+
+
 def copy_waves(pairs):
     """Cut a list of (src, dst) block copies, meant to run in order, into
     consecutive [start, stop) waves that ``copy_blocks`` may run concurrently:
@@ -218,25 +231,60 @@ class PagedKVCache:
         qs[1:] = np.cumsum(chunks)
         return PrefillPlan(ids, chunks, slots, pairs, tables, lens, qs)
 
-    def swap_out(self, seq_ids, stream=None):
+    def swap_out(self, seq_ids, stream=None, copy_engines=False):
         """Preempt sequences by swapping: each moves, all or nothing, to host blocks
-        and its K/V is copied there; returns the (device, host) pairs."""
+        and its K/V is copied there; returns the (device, host) pairs.
+
+        ``copy_engines``: the blocks are first gathered into a contiguous device
+        staging buffer (one ``swap_blocks`` launch, HBM to HBM), then cross to the
+        host on the copy engines, one copy per run of consecutive host blocks, so
+        the SMs stay free for concurrent work; otherwise one ``swap_blocks``
+        launch copies every block over the host link from the SMs."""
         pairs = [self.bm.swap_out(int(s)) for s in seq_ids]
         pairs = np.concatenate(pairs) if pairs else np.zeros((0, 2), np.int64)
-        if len(pairs):
+        if len(pairs) and not copy_engines:
             swap_blocks(self.host_k, self.host_v, self.k_pool, self.v_pool,
                         torch.as_tensor(pairs, device=self.device), stream)
+        elif len(pairs):
+            sk, sv = self._staging(len(pairs))
+            gather = np.stack([pairs[:, 0], np.arange(len(pairs))], 1)
+            swap_blocks(sk, sv, self.k_pool, self.v_pool,
+                        torch.as_tensor(gather, device=self.device), stream)
+            with torch.cuda.stream(stream or torch.cuda.current_stream(self.device)):
+                for a, b, h in host_runs(pairs[:, 1]):
+                    self.host_k[h:h + b - a].copy_(sk[a:b], non_blocking=True)
+                    self.host_v[h:h + b - a].copy_(sv[a:b], non_blocking=True)
         return pairs
 
-    def swap_in(self, seq_ids, stream=None):
+    def swap_in(self, seq_ids, stream=None, copy_engines=False):
         """Bring swapped-out sequences back onto fresh device blocks; returns the
-        (host, device) pairs."""
+        (host, device) pairs. ``copy_engines`` as for ``swap_out``, in reverse: the
+        host runs land in the staging buffer, one launch scatters them."""
         pairs = [self.bm.swap_in(int(s)) for s in seq_ids]
         pairs = np.concatenate(pairs) if pairs else np.zeros((0, 2), np.int64)
-        if len(pairs):
+        if len(pairs) and not copy_engines:
             swap_blocks(self.k_pool, self.v_pool, self.host_k, self.host_v,
                         torch.as_tensor(pairs, device=self.device), stream)
+        elif len(pairs):
+            sk, sv = self._staging(len(pairs))
+            with torch.cuda.stream(stream or torch.cuda.current_stream(self.device)):
+                for a, b, h in host_runs(pairs[:, 0]):
+                    sk[a:b].copy_(self.host_k[h:h + b - a], non_blocking=True)
+                    sv[a:b].copy_(self.host_v[h:h + b - a], non_blocking=True)
+            scatter = np.stack([np.arange(len(pairs)), pairs[:, 1]], 1)
+            swap_blocks(self.k_pool, self.v_pool, sk, sv,
+                        torch.as_tensor(scatter, device=self.device), stream)
         return pairs
+
+    def _staging(self, n):
+        """Device staging pools of at least n blocks (grown on demand)."""
+        have = getattr(self, "_stage", None)
+        if have is None or have[0].shape[0] < n:
+            ks, vs = pool_shapes(n, self.num_kv_heads, self.block_size, self.head_dim,
+                                 self.k_pool.dtype)
+            self._stage = (torch.empty(ks, dtype=self.k_pool.dtype, device=self.device),
+                           torch.empty(vs, dtype=self.k_pool.dtype, device=self.device))
+        return self._stage[0][:n], self._stage[1][:n]
 
     def plan_prompts(self, seq_ids, prompts, max_blocks=None):
         """Host half of a prefill step with prefix caching (the manager must have

@@ -148,3 +148,16 @@ def test_step_pipeline_slab_layout_packs_every_input_once_aligned():
     again = slab_views(slab, layout)
     for k in layout:
         assert torch.equal(again[k], t[k])
+
+
+def test_host_runs_cover_the_ids_in_order():
+    import numpy as np
+    from paged_kv_cache_259_gb300.engine import host_runs
+    assert host_runs([]) == []
+    assert host_runs([5]) == [(0, 1, 5)]
+    assert host_runs([3, 4, 5, 9, 10, 2]) == [(0, 3, 3), (3, 5, 9), (5, 6, 2)]
+    rng = np.random.default_rng(1)
+    for _ in range(50):
+        ids = rng.permutation(40)[:int(rng.integers(0, 40))]
+        rebuilt = [h + i for a, b, h in host_runs(ids) for i in range(b - a)]
+        assert rebuilt == list(ids)

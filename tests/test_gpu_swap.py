@@ -37,8 +37,9 @@ def randn(shape, seed):
     return torch.randn(*shape, generator=g).to(torch.bfloat16)
 
 
+@pytest.mark.parametrize("copy_engines", [False, True])
 @pytest.mark.parametrize("Hq,Hkv,bs", [(8, 8, 16), (16, 4, 32)])
-def test_swap_out_reuse_swap_in_then_decode(Hq, Hkv, bs):
+def test_swap_out_reuse_swap_in_then_decode(Hq, Hkv, bs, copy_engines):
     NB, NH, D = 24, 16, 128
     lens = {0: 3 * bs + 5, 1: bs + 1, 2: 2 * bs}
     order = list(np.random.default_rng(bs).permutation(NB))
@@ -58,7 +59,7 @@ def test_swap_out_reuse_swap_in_then_decode(Hq, Hkv, bs):
         for _ in range(L):
             obm.append_slot(sid)
     # preempt 0 and 2 by swapping
-    pairs = cache.swap_out([0, 2])
+    pairs = cache.swap_out([0, 2], copy_engines=copy_engines)
     exp = obm.swap_out(0) + obm.swap_out(2)
     assert [tuple(x) for x in pairs] == exp
     for d, h in exp:
@@ -75,7 +76,7 @@ def test_swap_out_reuse_swap_in_then_decode(Hq, Hkv, bs):
                           torch.as_tensor(slots, device="cuda"))
     oops.reshape_and_cache(k9, v9, kp, vp, torch.tensor(exp_slots), bs)
     # bring 0 and 2 back onto fresh device blocks
-    pairs = cache.swap_in([0, 2])
+    pairs = cache.swap_in([0, 2], copy_engines=copy_engines)
     exp = obm.swap_in(0) + obm.swap_in(2)
     assert [tuple(x) for x in pairs] == exp
     for h, d in exp:
@@ -125,7 +126,8 @@ def test_swap_blocks_rejects_pageable_host_memory_and_flags_bad_pairs():
     assert torch.count_nonzero(ph[0]) == 0 and torch.count_nonzero(pv[[0, 1, 3]]) == 0
 
 
-def test_full_size_swap_workload_two_round_trips_bit_exact():
+@pytest.mark.parametrize("copy_engines", [False, True])
+def test_full_size_swap_workload_two_round_trips_bit_exact(copy_engines):
     """The benchmarked workload (the newest 16 of 64 LLaMA-13B-shaped sequences,
     1105 blocks) swapped out and in twice, block ids changing every time; pairs
     equal the oracle's, and sampled blocks of both pools equal the oracle's pools."""
@@ -146,11 +148,11 @@ def test_full_size_swap_workload_two_round_trips_bit_exact():
     hk = torch.zeros((sw.num_host_blocks,) + tuple(kp.shape[1:]), dtype=kp.dtype)
     hv = torch.zeros_like(hk)
     for _ in range(2):
-        g = cache.swap_out(sw.victims)
+        g = cache.swap_out(sw.victims, copy_engines=copy_engines)
         o = [p for s in sw.victims for p in obm.swap_out(s)]
         assert [tuple(x) for x in g] == o and len(o) == sw.victim_blocks
         oops.swap_blocks(hk, hv, kp, vp, o)
-        g = cache.swap_in(sw.victims)
+        g = cache.swap_in(sw.victims, copy_engines=copy_engines)
         o = [p for s in sw.victims for p in obm.swap_in(s)]
         assert [tuple(x) for x in g] == o
         oops.swap_blocks(kp, vp, hk, hv, o)
