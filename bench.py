@@ -842,7 +842,7 @@ def swap_copy_engine_path(cache, sw, stream, n):
     from paged_kv_cache_259_gb300.engine import host_runs
     dev = cache.device
     P = sw.victim_blocks
-    sk, sv = cache._staging(P)
+    sk, sv = cache.staging_pools(P)
     idx = np.arange(P)
     plans = []
     for o, i in swap_plans(cache.bm, sw.victims, n + 3 + 64):

@@ -246,7 +246,7 @@ class PagedKVCache:
             swap_blocks(self.host_k, self.host_v, self.k_pool, self.v_pool,
                         torch.as_tensor(pairs, device=self.device), stream)
         elif len(pairs):
-            sk, sv = self._staging(len(pairs))
+            sk, sv = self.staging_pools(len(pairs))
             gather = np.stack([pairs[:, 0], np.arange(len(pairs))], 1)
             swap_blocks(sk, sv, self.k_pool, self.v_pool,
                         torch.as_tensor(gather, device=self.device), stream)
@@ -266,7 +266,7 @@ class PagedKVCache:
             swap_blocks(self.k_pool, self.v_pool, self.host_k, self.host_v,
                         torch.as_tensor(pairs, device=self.device), stream)
         elif len(pairs):
-            sk, sv = self._staging(len(pairs))
+            sk, sv = self.staging_pools(len(pairs))
             with torch.cuda.stream(stream or torch.cuda.current_stream(self.device)):
                 for a, b, h in host_runs(pairs[:, 0]):
                     sk[a:b].copy_(self.host_k[h:h + b - a], non_blocking=True)
@@ -276,7 +276,7 @@ class PagedKVCache:
                         torch.as_tensor(scatter, device=self.device), stream)
         return pairs
 
-    def _staging(self, n):
+    def staging_pools(self, n):
         """Device staging pools of at least n blocks (grown on demand)."""
         have = getattr(self, "_stage", None)
         if have is None or have[0].shape[0] < n:
