@@ -276,6 +276,25 @@ class PagedKVCache:
                         torch.as_tensor(scatter, device=self.device), stream)
         return pairs
 
+    def preempt_by_recompute(self, seq_ids):
+        """Preempt sequences by recomputation ("KV cache paginado...", "Como
+        funciona": a preempted request's blocks are recovered by swapping or by
+        recomputing them later): their blocks are freed now. Returns each one's
+        token count, for ``plan_resume``."""
+        lens = {int(s): self.bm.seq_len(int(s)) for s in seq_ids}
+        for s in seq_ids:
+            self.bm.free_seq(int(s))
+        return lens
+
+    def plan_resume(self, seq_ids, lens, max_blocks=None):
+        """Host half of resuming sequences preempted by recomputation: each is
+        added again and all of its ``lens[s]`` tokens form one chunk, so one
+        chunked-prefill step (``prefill_step`` with their recomputed q, K, V)
+        writes their K/V into fresh blocks and attends over them."""
+        for s in seq_ids:
+            self.bm.add_seq(int(s))
+        return self.plan_prefill(seq_ids, [lens[int(s)] for s in seq_ids], max_blocks)
+
     def staging_pools(self, n):
         """Device staging pools of at least n blocks (grown on demand)."""
         have = getattr(self, "_stage", None)

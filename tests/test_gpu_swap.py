@@ -170,3 +170,69 @@ def test_full_size_swap_workload_two_round_trips_bit_exact(copy_engines):
     hkv, hvv = pkv.pool_views(cache.host_k, cache.host_v)
     assert torch.equal(stored_bits(hkv[hidx]), stored_bits(hk[hidx]))
     assert torch.equal(stored_bits(hvv[hidx]), stored_bits(hv[hidx]))
+
+
+def test_preempt_by_recompute_then_resume_decodes_as_before():
+    """Two sequences are preempted by recomputation (blocks freed), another
+    sequence takes every free block, overwrites it and finishes, then they
+    resume: one
+    chunked-prefill step over all their tokens rewrites their K/V (the values
+    the model would recompute: here the original ones) into fresh blocks. The
+    next decode step gives bit for bit the outputs it gave before, and the
+    resumed tables read back the original K/V."""
+    Hq, Hkv, bs, D, NB = 8, 2, 16, 128, 40
+    lens = {0: 3 * bs + 5, 1: bs + 1, 2: 2 * bs}
+    order = list(np.random.default_rng(3).permutation(NB))
+    cache = PagedKVCache(NB, Hq, Hkv, D, bs, torch.bfloat16, order, "cuda")
+    k0, v0 = randn((NB, Hkv, bs, D), 11), randn((NB, Hkv, bs, D), 12)
+    cache.load(k0, v0)
+    for sid, L in lens.items():
+        cache.bm.add_seq(sid)
+        assert cache.bm.append_n(sid, L) == []
+    ids = [0, 1, 2]
+    MB = max(-(-L // bs) for L in lens.values()) + 1
+    q = randn((len(ids), Hq, D), 13)
+
+    def decode():
+        tables, slens = cache.bm.build_tables(ids, MB)
+        out = torch.empty(len(ids), Hq, D, dtype=torch.bfloat16, device="cuda")
+        pkv.paged_attention_decode(out, q.cuda(), cache.k_pool, cache.v_pool,
+                                   torch.as_tensor(tables, device="cuda"),
+                                   torch.as_tensor(slens, device="cuda"), 1 / math.sqrt(D))
+        return out.cpu()
+
+    def rows(sid):                                        # [L, Hkv, D] through the table
+        kv, vv = cache.k_view().cpu(), cache.v_view().cpu()
+        t = cache.bm.block_table(sid)
+        k = torch.cat([kv[b].transpose(0, 1) for b in t])[:cache.bm.seq_len(sid)]
+        v = torch.cat([vv[b].transpose(0, 1) for b in t])[:cache.bm.seq_len(sid)]
+        return k, v
+
+    before = decode()
+    saved = {s: rows(s) for s in (0, 2)}
+    old_tables = {s: cache.bm.block_table(s) for s in (0, 2)}
+    n = cache.preempt_by_recompute([0, 2])
+    assert n == {0: lens[0], 2: lens[2]}
+    # another sequence takes every free block (theirs included), overwrites them
+    # all and finishes: whatever blocks the resumed sequences get hold garbage
+    cache.bm.add_seq(9)
+    n9 = cache.bm.num_free() * bs
+    slots = np.concatenate([cache.bm.append_slots([9])[0] for _ in range(n9)])
+    assert cache.bm.num_free() == 0 and set(old_tables[0] + old_tables[2]) <= set(
+        cache.bm.block_table(9))
+    pkv.reshape_and_cache(randn((n9, Hkv, D), 14).cuda(), randn((n9, Hkv, D), 15).cuda(),
+                          cache.k_pool, cache.v_pool, torch.as_tensor(slots, device="cuda"))
+    cache.bm.free_seq(9)
+    plan = cache.plan_resume([0, 2], n)
+    k = torch.cat([saved[0][0], saved[2][0]])
+    v = torch.cat([saved[0][1], saved[2][1]])
+    qp = randn((k.shape[0], Hq, D), 16)
+    out = torch.empty(k.shape[0], Hq, D, dtype=torch.bfloat16, device="cuda")
+    cache.prefill_step(qp.cuda(), k.cuda(), v.cuda(), plan.device_tensors("cuda"), out,
+                       1 / math.sqrt(D), plan.max_query_len)
+    assert pkv.get_device_error() == 0
+    for s in (0, 2):
+        kk, vv = rows(s)
+        assert torch.equal(stored_bits(kk), stored_bits(saved[s][0]))
+        assert torch.equal(stored_bits(vv), stored_bits(saved[s][1]))
+    assert torch.equal(decode(), before)
