@@ -1,6 +1,8 @@
 /*
- * pagedkv.h -- C ABI of libpagedkv: decode-step attention over a paged KV cache,
- * the two cache writes of a step, and the host-side block manager.
+ * pagedkv.h -- C ABI of libpagedkv: decode-step and chunked-prefill attention
+ * over a paged KV cache, the cache writes of a step (slot write, copy-on-write
+ * copy, swap copy to and from host memory), and the host-side block manager
+ * (with prefix caching, beam-search reshuffles and swapping).
  *
  * Sources, by page title and section:
  *   "PagedAttention" (Ultralytics glossary)
@@ -16,11 +18,16 @@
  *       tiling, grouped-query attention, FP8 cache quantisation.
  *   "KV cache paginado e batching contínuo para LLMs" (upskillscore), "Como
  *     funciona": block tables, waste confined to the last block, reference
- *     counts, block-level copy-on-write (allocate, copy, decrement the original).
+ *     counts, block-level copy-on-write (allocate, copy, decrement the original),
+ *     preemption of whole requests by swapping their blocks to CPU memory or by
+ *     recomputation.
+ *   "vLLM PagedAttention: uma revolução no throughput..." (news.hada.io), the
+ *     feature list: chunked prefill, prefix caching.
  *
  * Conventions for every call
  *   - Device pointers are plain CUDA device addresses on the current device; the
  *     caller owns every buffer. The library allocates no device memory.
+ *     swap_blocks alone also takes pinned host memory (see there).
  *   - Every device call is asynchronous on `stream` (a cudaStream_t passed as
  *     void*; NULL is the legacy default stream) and does not synchronise.
  *   - Arguments are checked on the host before any launch; a bad argument
