@@ -382,3 +382,58 @@ def test_beam_step_refusals_change_nothing():
         assert (a.free_list(), a.block_table(1), a.block_table(2)) == before
     with pytest.raises(ValueError):
         a.beam_step([1, 2], [0], [3, 4])
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_beam_steps_with_prefix_caching_match_oracle(seed):
+    """Beam search on a caching manager: requests that share a prompt prefix
+    (cached full blocks reused), beams reshuffled every step (forks carry their
+    token history, freed beams' registered blocks become evictable), one token
+    id appended per beam, requests finishing and new ones reviving cached
+    blocks. The library's manager and the oracle's agree after every operation."""
+    rng = np.random.default_rng(300 + seed)
+    bs = int(rng.choice([2, 4, 16]))
+    nb = int(rng.integers(60, 160))
+    W = int(rng.choice([2, 3, 4]))
+    order = list(rng.permutation(nb))
+    nat = BlockManager(nb, bs, order, prefix_caching=True)
+    ora = PrefixCachingBlockManager(nb, bs, order)
+    system = [int(t) for t in rng.integers(0, 5, size=int(rng.integers(1, 4 * bs)))]
+    reqs, nxt = [], 0
+    try:
+        for step in range(60):
+            if len(reqs) < 2 or rng.random() < 0.1:
+                p = system + [int(t) for t in rng.integers(0, 5, size=int(rng.integers(1, 2 * bs)))]
+                n_o = ora.add_seq_prompt(nxt, p)
+                assert nat.add_seq_prompt(nxt, p) == n_o
+                rest = p[n_o:]
+                slots, pairs = nat.append_tokens(nxt, rest)
+                exp = [ora.append_token(nxt, t) for t in rest]
+                assert list(slots) == [s for s, _ in exp]
+                assert [tuple(x) for x in pairs] == [c for _, c in exp if c is not None]
+                reqs.append([nxt])
+                nxt += 1
+            if rng.random() < 0.08 and len(reqs) > 1:
+                for s in reqs.pop(int(rng.integers(len(reqs)))):
+                    nat.free_seq(s)
+                    ora.free_seq(s)
+            old = [s for b in reqs for s in b]
+            parents, new, base = [], [], 0
+            for b in reqs:
+                parents += [base + int(x) for x in rng.integers(0, len(b), size=W)]
+                base += len(b)
+            new = list(range(nxt, nxt + len(parents)))
+            nxt += len(parents)
+            nat.beam_step(old, parents, new)
+            ora.beam_step(old, parents, new)
+            reqs = [new[i:i + W] for i in range(0, len(new), W)]
+            for s in new:
+                t = int(rng.integers(0, 5))
+                slots, pairs = nat.append_tokens(s, [t])
+                slot, cow = ora.append_token(s, t)
+                assert list(slots) == [slot]
+                assert [tuple(x) for x in pairs] == ([cow] if cow is not None else [])
+            _same_state(nat, ora, new)
+    except (pkv.PagedKVError, PoolExhausted) as e:
+        assert isinstance(e, PoolExhausted) or e.status == -5
+        assert step > 10                                 # the script ran long enough
