@@ -5,12 +5,20 @@ paged_attention_decode) on a seeded synthetic workload, timed on the GPU.
 
 Prints ONE JSON line (rank 0). ``value`` is achieved algorithmic HBM bytes of the
 whole step per second (GB/s), with every input resident in HBM; ``e2e`` is the
-same metric through the public Python API with pinned host inputs copied in and
-the output copied out inside the timed region. ``roofline`` covers the decode
+same metric through the engine (``StepPipeline``), every step's inputs uploaded
+from pinned host memory and its output read back inside the timed region,
+overlapped with the neighbouring steps. ``roofline`` covers the decode
 attention op alone (its kernel plus the split-KV merge), timed with CUDA events
 on its stream. ``cpu_baseline`` times the CPU oracle on a bounded sample of the
 same workload. With ``--impl reference`` the oracle alone is timed (the
 reference arm; a slow CPU program, not a target).
+
+Other workloads (``--config``): ``prefill_*`` time a chunked-prefill step
+(TFLOP/s of the causal attention, tensor-bound roofline), the prompt workload a
+prefill step with prefix caching, ``swap_*`` a swap step of preempted sequences
+to and from pinned host memory (GB/s of block bytes against the copy engines'
+rate measured in the same run, plus the copy-engine path and its overlap with
+decode), ``beam_search_bf16`` a beam-search decode step.
 
 Multi-GPU (torchrun): every rank runs its own copy of the workload (independent
 sequences; decode attention needs no exchange), so scaling is weak; the NCCL
