@@ -1,4 +1,5 @@
-"""Oracle for the paged KV-cache decode path: plain, slow, obviously correct CPU code.
+"""Oracle for the paged KV-cache path (decode, chunked prefill, block manager with
+prefix caching, beam steps and swapping): plain, slow, obviously correct CPU code.
 
 TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import, call or
@@ -26,13 +27,20 @@ Sources, by page title and section:
 * "KV cache paginado e batching contínuo para LLMs" (upskillscore), section
   "Como funciona": block tables, waste confined to the last block, reference
   counts, block-level copy-on-write (allocate another block, copy, decrement the
-  original's count).
+  original's count); preemption by swapping blocks to CPU memory.
+* "vLLM PagedAttention: uma revolução no throughput..." (news.hada.io), the
+  feature list: chunked prefill, prefix caching.
 
 Modules:
 
-* ``attention``    -- decode attention as the plain softmax definition, over K/V
-                      gathered through the block table.
-* ``cache_ops``    -- slot-mapped write of new K/V, block copy for copy-on-write.
+* ``attention``    -- decode and chunked-prefill attention as the plain softmax
+                      definition, over K/V gathered through the block table.
+* ``cache_ops``    -- slot-mapped write of new K/V, block copy for copy-on-write,
+                      block copy between the device and host pools (swapping).
 * ``fp8_e4m3``     -- E4M3 decode/encode written from the OCP FP8 definition.
-* ``block_manager``-- free list, block tables, reference counts, fork, CoW, free.
+* ``block_manager``-- free list, block tables, reference counts, fork, CoW, free,
+                      beam-search reshuffles, swapping to a host pool, and the
+                      script replayer.
+* ``prefix_cache`` -- the block manager with full blocks shared across requests
+                      by their exact prefix (evictable when unused).
 """
