@@ -1,0 +1,63 @@
+/* A plain C client of libpagedkv: the host block manager driven through the C
+ * ABI alone (no Python, no torch), printing what it hands out so a test can
+ * compare it with the CPU oracle. Build: cc -I include this.c -L<dir> -lpagedkv */
+#include <stdint.h>
+#include <stdio.h>
+
+#include "pagedkv.h"
+
+static int check(int st, const char* what) {
+    if (st != PKV_OK) printf("error %s %d %s\n", what, st, pkv_status_string(st));
+    return st;
+}
+
+static void table(pkv_block_manager* bm, int64_t sid) {
+    int32_t t[16];
+    int n = 0;
+    check(bm_block_table(bm, sid, t, 16, &n), "bm_block_table");
+    printf("table %lld", (long long)sid);
+    for (int i = 0; i < n; ++i) printf(" %d", t[i]);
+    printf("\n");
+}
+
+int main(void) {
+    const int32_t order[12] = {5, 2, 7, 0, 3, 6, 1, 4, 11, 9, 10, 8};
+    pkv_block_manager* bm = bm_create(12, 4, order, 12);
+    if (!bm) {
+        printf("error bm_create\n");
+        return 1;
+    }
+    /* sequence 0: 6 tokens (two blocks, the second half full) */
+    check(bm_add_seq(bm, 0), "bm_add_seq");
+    for (int i = 0; i < 6; ++i) {
+        int64_t slot;
+        int32_t s, d;
+        check(bm_append_slot(bm, 0, &slot, &s, &d), "bm_append_slot");
+        printf("slot 0 %lld cow %d %d\n", (long long)slot, s, d);
+    }
+    /* fork: 1 shares both blocks; its next token copies the partial one */
+    check(bm_fork(bm, 0, 1), "bm_fork");
+    for (int64_t sid = 1; sid >= 0; --sid) {
+        int64_t slot;
+        int32_t s, d;
+        check(bm_append_slot(bm, sid, &slot, &s, &d), "bm_append_slot");
+        printf("slot %lld %lld cow %d %d\n", (long long)sid, (long long)slot, s, d);
+    }
+    table(bm, 0);
+    table(bm, 1);
+    /* a beam step: two new beams both continue sequence 1, then 0 and 1 go */
+    const int64_t old_ids[2] = {0, 1}, new_ids[2] = {2, 3};
+    const int32_t parents[2] = {1, 1};
+    check(bm_beam_step(bm, old_ids, 2, parents, new_ids, 2), "bm_beam_step");
+    table(bm, 2);
+    table(bm, 3);
+    int32_t freel[12];
+    const int nf = bm_free_list(bm, freel, 12);
+    printf("free");
+    for (int i = 0; i < nf; ++i) printf(" %d", freel[i]);
+    printf("\n");
+    /* an unknown sequence is an error, and the manager is unchanged */
+    printf("unknown %d\n", bm_free_seq(bm, 99));
+    bm_destroy(bm);
+    return 0;
+}
