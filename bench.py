@@ -55,13 +55,23 @@ KERNEL_SOURCES = ["pkv_decode_impl.cuh", "pkv_decode.cu", "pkv_decode_bf16.cu",
                   "pkv_decode_e4m3.cu", "pkv_decode_f32.cu"]
 
 
-def kernel_source_hash():
+def code_hash(files):
+    """Hash of kernel sources with their comments and blank lines removed, so
+    that documentation edits do not orphan counters captured on the same code."""
     import hashlib
+    import re
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "paged_kv_cache_259_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    for f in files:
+        with open(os.path.join(ROOT, "paged_kv_cache_259_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("\n".join(line.rstrip() for line in src.splitlines() if line.strip()).encode())
     return h.hexdigest()[:16]
+
+
+def kernel_source_hash():
+    return code_hash(KERNEL_SOURCES)
 
 
 def measured_traffic(config):
@@ -501,12 +511,7 @@ PREFILL_SOURCES = ["pkv_prefill.cu", "pkv_tcgen05.cuh"]
 
 
 def prefill_source_hash():
-    import hashlib
-    h = hashlib.sha256()
-    for f in PREFILL_SOURCES:
-        with open(os.path.join(ROOT, "paged_kv_cache_259_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    return h.hexdigest()[:16]
+    return code_hash(PREFILL_SOURCES)
 
 
 def prefill_traffic(config):

@@ -9,12 +9,14 @@
 // logits pre-multiplied by log2 e so exp2 is used).
 //
 // Cache layout (per pool, per block, per kv head: one contiguous tile of
-// block_size*head_dim elements):
-//   K: [D/X][bs][X]  -- X = 16 bytes of elements; chunk plane j holds dims
-//                       jX..jX+X-1 of every token of the block;
-//   V: [D][bs]       -- transposed: one row per dim, tokens contiguous.
-// Both make the tensor-core operands below load from shared memory with plain,
-// bank-conflict-free 16-byte rows, and keep a tile one 1-D bulk copy.
+// block_size*head_dim elements, made of 128-byte core matrices of 8 rows x 16
+// bytes; X = 16 bytes of elements):
+//   K: [bs/8][D/X][8][X]  -- core matrix (g, c) = tokens 8g..8g+7 (rows) x
+//                            dims cX..cX+X-1 (Layout::k_off);
+//   V: [bs/X][D/8][8][X]  -- transposed: core matrix (c, g) = dims 8g..8g+7
+//                            (rows) x tokens cX..cX+X-1 (Layout::v_off).
+// Every ldmatrix / 16-byte operand read below is then one core-matrix row
+// (bank-conflict-free), and a tile stays one 1-D bulk copy.
 //
 // Pipeline (shared by both tile-math variants)
 //   CTA  = (partition p, kv head hk, sequence b). A partition is PB consecutive

@@ -52,3 +52,16 @@ def test_prefill_flops_count_every_visible_key():
             p = int(L) - int(C) + i                      # the token's position
             plain += (p + 1) * 4 * w.D * w.Hq             # Q.K and P.V: 2*D multiply-adds each
     assert math.isclose(bench.prefill_flops(w), plain, rel_tol=0, abs_tol=0.5)
+
+
+def test_kernel_source_hash_ignores_comments_only(tmp_path, monkeypatch):
+    """bench.code_hash: comments and blank lines do not change it, code does."""
+    csrc = tmp_path / "paged_kv_cache_259_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (csrc / "k.cu").write_text("// a kernel\nint f(int x) {\n  return x + 1;  // one\n}\n")
+    h0 = bench.code_hash(["k.cu"])
+    (csrc / "k.cu").write_text("/* the same kernel,\n   described */\n\nint f(int x) {\n  return x + 1;\n}\n")
+    assert bench.code_hash(["k.cu"]) == h0
+    (csrc / "k.cu").write_text("int f(int x) {\n  return x + 2;\n}\n")
+    assert bench.code_hash(["k.cu"]) != h0
