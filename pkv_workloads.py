@@ -1,4 +1,6 @@
-"""Seeded synthetic workloads for the paged-KV decode step.
+"""Seeded synthetic workloads for the paged-KV path: decode steps (plain, GQA,
+shared prefixes, FP8, beam search), chunked-prefill steps, prompts that share a
+system prompt (prefix caching) and swap steps.
 
 This module only draws random numbers and lays out shapes; it holds none of the
 method's arithmetic (no slot or block-table computation, no attention, no
@@ -14,7 +16,9 @@ A workload is described by
   ``bs`` block size, ``NB`` pool blocks;
 * ``free_order``: the initial free list (a seeded permutation of the block ids);
 * ``script``: block-manager operations that build the cache state before the
-  measured step (``("add", sid)``, ``("append", sid, n)``, ``("fork", p, c)``);
+  measured step (``("add", sid)``, ``("append", sid, n)``, ``("fork", p, c)``,
+  ``("beam", old_ids, parents, new_ids)``; the random parent draws of a beam
+  search are inputs here, each side reshuffles its own manager with them);
 * ``step_seqs``: the sequences that append one token in the measured step;
 * value tensors, drawn on demand: the past K/V contents of every pool slot
   (``past_pools``), and the step's ``q``, ``k_new``, ``v_new``;
