@@ -31,7 +31,6 @@ os.environ.setdefault("MKL_NUM_THREADS", "1")
 
 import argparse
 import json
-import math
 import subprocess
 import sys
 import time

@@ -19,7 +19,7 @@ import torch
 
 import pkv_workloads as wl
 from _lib import library, pkv
-from _parity import (Inputs, KV_TORCH, assert_close, check_cache_writes, check_indexing,
+from _parity import (Inputs, assert_close, check_cache_writes, check_indexing,
                      run_gpu, run_oracle, sample_units)
 
 pytestmark = pytest.mark.gpu
