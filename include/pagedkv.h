@@ -381,12 +381,21 @@ PKV_API int bm_add_seq(pkv_block_manager* bm, int64_t seq_id);
 PKV_API int bm_append_slot(pkv_block_manager* bm, int64_t seq_id, int64_t* slot,
                    int32_t* cow_src, int32_t* cow_dst);
 /* n appends to one sequence; the CoW pairs they raise are written as
- * (src, dst) int64 pairs into cow_pairs (capacity cow_cap pairs) and counted in
- * *num_cow. On exhaustion the appends done so far stay done. */
+ * (src, dst) int64 pairs into cow_pairs (capacity cow_cap pairs; n appends raise
+ * at most one) and counted in *num_cow.
+ *
+ * Every batch append (this call, bm_append_slots, bm_append_tokens) is all or
+ * nothing. The blocks and CoW pairs the whole batch needs are counted first,
+ * without changing anything. PKV_ERR_POOL_EXHAUSTED if the free (plus, with
+ * prefix caching, evictable) blocks cannot cover them. PKV_ERR_INVALID_ARG if
+ * the pairs exceed cow_cap or a sequence is swapped out. PKV_ERR_OUT_OF_RANGE
+ * for an unknown sequence. On any error nothing changes and *num_cow is 0. */
 PKV_API int bm_append_n(pkv_block_manager* bm, int64_t seq_id, int n,
                 int64_t* cow_pairs, int cow_cap, int* num_cow);
 /* One append to each of n sequences (a decode step): slots[i] for seq_ids[i];
- * CoW pairs in order into cow_pairs (capacity n pairs), count in *num_cow. */
+ * CoW pairs in order into cow_pairs (capacity n pairs), count in *num_cow. An
+ * id may repeat: a chunked-prefill step lists a sequence once per token of its
+ * chunk, and its appends then run in list order. All or nothing, as above. */
 PKV_API int bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n,
                     int64_t* slots, int64_t* cow_pairs, int* num_cow);
 PKV_API int bm_fork(pkv_block_manager* bm, int64_t parent, int64_t child);
@@ -449,7 +458,7 @@ PKV_API int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids
  *   *num_cached = prompt tokens already cached (a multiple of block_size). The
  *   caller appends prompt[*num_cached..n) with bm_append_tokens.
  * bm_append_tokens: n appends with token ids; slots[i] for tokens[i]; CoW pairs
- *   as bm_append_n. On exhaustion the appends done so far stay done.
+ *   and errors as bm_append_n (all or nothing).
  * bm_cache_stats: blocks looked up / found by bm_add_seq_prompt so far, blocks
  *   registered, evictable blocks.
  * bm_evictable_list: evictable block ids, oldest first, into out[0..cap);

@@ -224,6 +224,40 @@ struct pkv_block_manager {
     int append(Seq& s, int64_t* slot, int32_t* cow_src, int32_t* cow_dst) {
         return append(s, kUnknownToken, slot, cow_src, cow_dst);
     }
+
+    // What a batch of appends would take, found without changing anything, so
+    // that a batch either fits whole or is refused whole. Feed it the batch in
+    // order as (sequence, count) runs; a sequence may come back in later runs.
+    struct Demand {
+        const pkv_block_manager& bm;
+        std::unordered_map<const Seq*, int64_t> len;    // sequences appended to so far
+        std::unordered_map<int32_t, int64_t> dropped;   // references given up by CoW
+        int64_t blocks = 0, cows = 0;
+
+        explicit Demand(const pkv_block_manager& m) : bm(m) {}
+
+        void add(const Seq& s, int64_t k) {
+            if (k <= 0) return;
+            const int64_t bs = bm.block_size;
+            auto it = len.find(&s);
+            const bool touched = it != len.end();
+            const int64_t L = touched ? it->second : s.len;
+            // A sequence's first append into a partial last block copies it
+            // when another table still holds it; later ones write in place.
+            if (!touched && L % bs != 0) {
+                const int32_t last = s.table.back();
+                if (bm.ref[last] - dropped[last] > 1) {
+                    blocks += 1;
+                    cows += 1;
+                    dropped[last] += 1;
+                }
+            }
+            blocks += (L + k + bs - 1) / bs - (L + bs - 1) / bs;   // block starts in [L, L+k)
+            len[&s] = L + k;
+        }
+
+        bool fits() const { return blocks <= (int64_t)bm.device_available(); }
+    };
 };
 
 extern "C" {
@@ -271,16 +305,20 @@ int bm_append_slot(pkv_block_manager* bm, int64_t seq_id, int64_t* slot, int32_t
 int bm_append_n(pkv_block_manager* bm, int64_t seq_id, int n, int64_t* cow_pairs, int cow_cap,
                 int* num_cow) {
     if (!bm || n < 0 || !num_cow || (cow_cap > 0 && !cow_pairs)) return PKV_ERR_INVALID_ARG;
+    *num_cow = 0;
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
-    *num_cow = 0;
+    if (it->second.swapped) return PKV_ERR_INVALID_ARG;
+    pkv_block_manager::Demand need(*bm);
+    need.add(it->second, n);
+    if (need.cows > cow_cap) return PKV_ERR_INVALID_ARG;
+    if (!need.fits()) return PKV_ERR_POOL_EXHAUSTED;
     for (int i = 0; i < n; ++i) {
         int64_t slot;
         int32_t src, dst;
         const int st = bm->append(it->second, &slot, &src, &dst);
-        if (st != PKV_OK) return st;
+        if (st != PKV_OK) return st;                   // cannot happen after the checks
         if (src >= 0) {
-            if (*num_cow >= cow_cap) return PKV_ERR_INVALID_ARG;
             cow_pairs[2 * *num_cow] = src;
             cow_pairs[2 * *num_cow + 1] = dst;
             *num_cow += 1;
@@ -294,12 +332,20 @@ int bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int n, int64_
     if (!bm || n < 0 || (n > 0 && (!seq_ids || !slots || !cow_pairs)) || !num_cow)
         return PKV_ERR_INVALID_ARG;
     *num_cow = 0;
+    std::vector<pkv_block_manager::Seq*> seqs(n);
+    pkv_block_manager::Demand need(*bm);
     for (int i = 0; i < n; ++i) {
         auto it = bm->seqs.find(seq_ids[i]);
         if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
+        if (it->second.swapped) return PKV_ERR_INVALID_ARG;
+        seqs[i] = &it->second;
+        need.add(it->second, 1);
+    }
+    if (!need.fits()) return PKV_ERR_POOL_EXHAUSTED;
+    for (int i = 0; i < n; ++i) {
         int32_t src, dst;
-        const int st = bm->append(it->second, &slots[i], &src, &dst);
-        if (st != PKV_OK) return st;
+        const int st = bm->append(*seqs[i], &slots[i], &src, &dst);
+        if (st != PKV_OK) return st;                   // cannot happen after the checks
         if (src >= 0) {
             cow_pairs[2 * *num_cow] = src;
             cow_pairs[2 * *num_cow + 1] = dst;
@@ -520,15 +566,19 @@ int bm_append_tokens(pkv_block_manager* bm, int64_t seq_id, const int32_t* token
                      int64_t* slots, int64_t* cow_pairs, int cow_cap, int* num_cow) {
     if (!bm || n < 0 || (n > 0 && (!tokens || !slots)) || !num_cow || (cow_cap > 0 && !cow_pairs))
         return PKV_ERR_INVALID_ARG;
+    *num_cow = 0;
     auto it = bm->seqs.find(seq_id);
     if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
-    *num_cow = 0;
+    if (it->second.swapped) return PKV_ERR_INVALID_ARG;
+    pkv_block_manager::Demand need(*bm);
+    need.add(it->second, n);
+    if (need.cows > cow_cap) return PKV_ERR_INVALID_ARG;
+    if (!need.fits()) return PKV_ERR_POOL_EXHAUSTED;
     for (int i = 0; i < n; ++i) {
         int32_t src, dst;
         const int st = bm->append(it->second, (int64_t)tokens[i], &slots[i], &src, &dst);
-        if (st != PKV_OK) return st;
+        if (st != PKV_OK) return st;                   // cannot happen after the checks
         if (src >= 0) {
-            if (*num_cow >= cow_cap) return PKV_ERR_INVALID_ARG;
             cow_pairs[2 * *num_cow] = src;
             cow_pairs[2 * *num_cow + 1] = dst;
             *num_cow += 1;

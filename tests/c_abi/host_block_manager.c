@@ -56,6 +56,24 @@ int main(void) {
     printf("free");
     for (int i = 0; i < nf; ++i) printf(" %d", freel[i]);
     printf("\n");
+    /* a decode step over both beams: 2 copies the shared partial block, which
+     * leaves 3 its only owner, so 3 writes in place */
+    const int64_t step_ids[2] = {2, 3};
+    int64_t slots[2], pairs[4];
+    int ncow = 0;
+    check(bm_append_slots(bm, step_ids, 2, slots, pairs, &ncow), "bm_append_slots");
+    printf("step %lld %lld", (long long)slots[0], (long long)slots[1]);
+    for (int i = 0; i < ncow; ++i)
+        printf(" cow %lld %lld", (long long)pairs[2 * i], (long long)pairs[2 * i + 1]);
+    printf("\n");
+    /* a chunk the pool cannot hold is refused whole: nothing changes */
+    const int free_before = bm_num_free(bm);
+    int len_before = 0, len_after = 0;
+    check(bm_seq_len(bm, 2, &len_before), "bm_seq_len");
+    const int st = bm_append_n(bm, 2, 4 * (free_before + 1), pairs, 2, &ncow);
+    check(bm_seq_len(bm, 2, &len_after), "bm_seq_len");
+    printf("refused %d cow %d len %d %d free %d %d\n", st, ncow, len_before, len_after,
+           free_before, bm_num_free(bm));
     /* an unknown sequence is an error, and the manager is unchanged */
     printf("unknown %d\n", bm_free_seq(bm, 99));
     bm_destroy(bm);

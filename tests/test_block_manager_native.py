@@ -4,6 +4,9 @@ Host logic, bit-exact: slots, copy-on-write pairs, block tables, reference count
 and the free list must agree after every operation of seeded random scripts and of
 the benchmark workloads' set-up scripts.
 """
+import copy
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -437,3 +440,140 @@ def test_beam_steps_with_prefix_caching_match_oracle(seed):
     except (pkv.PagedKVError, PoolExhausted) as e:
         assert isinstance(e, PoolExhausted) or e.status == -5
         assert step > 10                                 # the script ran long enough
+
+
+# ---------------------------------------------------------------- batch appends: all or nothing
+def _snapshot(nat, ids):
+    return (nat.free_list(), [nat.refcount(b) for b in range(nat.num_blocks)],
+            {s: (nat.block_table(s), nat.seq_len(s)) for s in ids})
+
+
+def test_batch_append_counts_a_shared_block_copied_once():
+    """Two tables share a partial last block and one block is free: the first
+    append copies it, which leaves the second table its only owner, so the batch
+    needs one block and fits. A batch that needs one more block is refused whole."""
+    library()
+    nat = BlockManager(2, 4, [0, 1])
+    ora = OracleBM(2, 4, [0, 1])
+    for bm in (nat, ora):
+        bm.add_seq(0)
+    assert nat.append_n(0, 2) == []
+    ora.append_slot(0), ora.append_slot(0)
+    nat.fork(0, 1)
+    ora.fork(0, 1)
+    slots, pairs = nat.append_slots([0, 1])
+    exp = [ora.append_slot(0), ora.append_slot(1)]
+    assert list(slots) == [s for s, _ in exp] and [tuple(p) for p in pairs] == [(0, 1)]
+    same_state(nat, ora)
+    assert nat.free_list() == []
+    nat.append_slots([0])
+    ora.append_slot(0)
+    before = _snapshot(nat, [0, 1])
+    with pytest.raises(pkv.PagedKVError) as e:    # seq 1: one slot in place, then a new block
+        nat.append_slots([1, 1])
+    assert e.value.status == -5
+    assert _snapshot(nat, [0, 1]) == before
+    with pytest.raises(pkv.PagedKVError) as e:
+        nat.append_n(1, 2)
+    assert e.value.status == -5
+    assert _snapshot(nat, [0, 1]) == before
+    assert nat.append_n(1, 1) == []                  # the in-place slot alone fits
+    ora.append_slot(1)
+    same_state(nat, ora)
+
+
+def test_append_with_too_small_cow_capacity_changes_nothing():
+    lib = library()
+    nat = BlockManager(4, 4, range(4))
+    nat.add_seq(0)
+    nat.append_n(0, 1)
+    nat.fork(0, 1)
+    before = _snapshot(nat, [0, 1])
+    buf = np.zeros((2, 2), dtype=np.int64)
+    cnt = ctypes.c_int(7)
+    st = lib.bm_append_n(nat._h, 1, 3, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), 0,
+                         ctypes.byref(cnt))
+    assert st == -1 and cnt.value == 0             # PKV_ERR_INVALID_ARG
+    assert _snapshot(nat, [0, 1]) == before
+    st = lib.bm_append_n(nat._h, 1, 3, buf.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), 1,
+                         ctypes.byref(cnt))
+    assert st == 0 and cnt.value == 1 and tuple(buf[0]) == (0, 1)
+
+
+@pytest.mark.parametrize("caching", [False, True])
+@pytest.mark.parametrize("seed", range(8))
+def test_batch_appends_are_all_or_nothing_against_oracle(seed, caching):
+    """Seeded scripts of forks, frees and batch appends (ids repeated in runs, as
+    a chunked-prefill step lists them) on small pools. The oracle applies each
+    batch one append at a time; where it runs out part-way, the library must
+    refuse the whole batch and keep its state; otherwise slots, pairs and state
+    must match."""
+    rng = np.random.default_rng(900 + seed)
+    bs = int(rng.choice([1, 2, 4, 16]))
+    nb = int(rng.integers(6, 40))
+    order = list(rng.permutation(nb))
+    nat = BlockManager(nb, bs, order, prefix_caching=caching)
+    ora = (PrefixCachingBlockManager if caching else OracleBM)(nb, bs, order)
+    live, nxt = [], 0
+    refused = done = cows = 0
+    for _ in range(250):
+        op = int(rng.integers(0, 6))
+        if op == 0 or not live:
+            nat.add_seq(nxt)
+            ora.add_seq(nxt)
+            live.append(nxt)
+            nxt += 1
+            continue
+        if op == 1:
+            sid = live[rng.integers(len(live))]
+            nat.fork(sid, nxt)
+            ora.fork(sid, nxt)
+            live.append(nxt)
+            nxt += 1
+            continue
+        if op == 2 and len(live) > 1:
+            sid = live.pop(rng.integers(len(live)))
+            nat.free_seq(sid)
+            ora.free_seq(sid)
+            continue
+        snap = copy.deepcopy(ora)
+        if op == 3:                                    # one sequence, k tokens with ids
+            sid = live[rng.integers(len(live))]
+            toks = [int(t) for t in rng.integers(0, 3, size=int(rng.integers(1, 3 * bs + 2)))]
+            if caching:
+                call = lambda: nat.append_tokens(sid, toks)
+                step = [(lambda t=t: ora.append_token(sid, t)) for t in toks]
+            else:
+                call = lambda: (None, nat.append_n(sid, len(toks)))
+                step = [(lambda: ora.append_slot(sid)) for _ in toks]
+        else:                                          # a batch with runs of repeated ids
+            k = int(rng.integers(1, len(live) + 1))
+            pick = rng.choice(live, size=k, replace=False)
+            ids = np.repeat(pick, rng.integers(1, bs + 2, size=k)).astype(np.int64)
+            call = lambda: nat.append_slots(ids)
+            step = [(lambda s=int(s): ora.append_slot(s)) for s in ids]
+        try:
+            exp = [f() for f in step]
+        except PoolExhausted:
+            ora = snap
+            before = _snapshot(nat, live)
+            with pytest.raises(pkv.PagedKVError) as e:
+                call()
+            assert e.value.status == -5
+            assert _snapshot(nat, live) == before
+            refused += 1
+        else:
+            slots, pairs = call()
+            if slots is not None:
+                assert list(slots) == [s for s, _ in exp]
+            assert [tuple(map(int, p)) for p in pairs] == [c for _, c in exp if c is not None]
+            done += 1
+            cows += len(pairs)
+        assert nat.free_list() == ora.free
+        assert [nat.refcount(b) for b in range(nb)] == ora.ref
+        for sid in live:
+            assert nat.block_table(sid) == ora.block_table(sid)
+            assert nat.seq_len(sid) == ora.seq_len(sid)
+        if caching:
+            assert nat.evictable_list() == ora.evictable
+    assert refused > 0 and done > 0 and cows > 0

@@ -1,8 +1,8 @@
 """The C ABI from plain C: tests/c_abi/host_block_manager.c, compiled with the
 system C compiler against include/pagedkv.h and linked to the built library,
-drives the host block manager (appends, fork, copy-on-write, a beam step,
-frees) with no Python or torch in between. Its output must equal the oracle's
-manager on the same operations."""
+drives the host block manager (appends, fork, copy-on-write, a beam step, a
+batch step, a refused chunk, frees) with no Python or torch in between. Its
+output must equal the oracle's manager on the same operations."""
 import os
 import shutil
 import subprocess
@@ -34,6 +34,16 @@ def expected():
     for sid in (2, 3):
         out.append(" ".join(["table", str(sid)] + [str(b) for b in bm.block_table(sid)]))
     out.append(" ".join(["free"] + [str(b) for b in bm.free]))
+    line = ["step"]
+    cows = []
+    for sid in (2, 3):
+        slot, cow = bm.append_slot(sid)
+        line.append(str(slot))
+        if cow:
+            cows += ["cow", str(cow[0]), str(cow[1])]
+    out.append(" ".join(line + cows))
+    nf, n2 = len(bm.free), bm.seq_len(2)
+    out.append(f"refused -5 cow 0 len {n2} {n2} free {nf} {nf}")
     out.append("unknown -4")
     return out
 
