@@ -27,7 +27,7 @@ __all__ = [
     "paged_attention_prefill", "swap_blocks",
     "reshape_and_cache", "copy_blocks", "get_device_error", "kernel_launches", "BlockManager",
     "library_path", "load_library", "pool_shapes", "pool_views", "pools_from_views", "PKV_F32",
-    "PKV_BF16", "PKV_E4M3",
+    "PKV_BF16", "PKV_E4M3", "PKV_ERR_POOL_EXHAUSTED",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -35,6 +35,7 @@ _LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
 _LIB = None
 
 PKV_F32, PKV_BF16, PKV_E4M3 = 0, 1, 2
+PKV_ERR_POOL_EXHAUSTED = -5
 _STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported configuration",
            -3: "CUDA runtime error", -4: "index out of range", -5: "block pool exhausted",
            -6: "device wait timed out"}

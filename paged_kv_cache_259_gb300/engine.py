@@ -20,9 +20,10 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from . import (BlockManager, copy_blocks, paged_attention_decode, paged_attention_decode_grouped,
-               paged_attention_prefill, paged_attention_workspace_size, pool_shapes,
-               pool_views, reshape_and_cache, swap_blocks)
+from . import (PKV_ERR_POOL_EXHAUSTED, BlockManager, PagedKVError, copy_blocks,
+               paged_attention_decode, paged_attention_decode_grouped, paged_attention_prefill,
+               paged_attention_workspace_size, pool_shapes, pool_views, reshape_and_cache,
+               swap_blocks)
 
 
 @dataclass
@@ -216,6 +217,32 @@ class PagedKVCache:
                 plan.seq_group, plan.group_members, plan.group_prefix = seq_group, members, prefix
                 plan.group_blocks = blocks
         return plan
+
+    def plan_step_preempting(self, requests, preempt, max_blocks=None, group_prefixes=True):
+        """``plan_step`` under the rule for running out of blocks ("KV cache
+        paginado...", "Como funciona": the newest requests are preempted, all or
+        nothing, and their blocks recovered by swapping or recomputation).
+
+        ``requests``: the running requests, oldest first; each is a sequence id
+        or a list of the ids of one request's sequences (its samples or beams).
+        The step appends to every sequence of every request. While the manager
+        refuses the whole step (it changes nothing then), the newest remaining
+        request goes whole to ``preempt(ids)``, which must release its device
+        blocks (``preempt_by_recompute``, or ``swap_out``), and the step is planned
+        again without it. Returns ``(plan, preempted)``: ``preempted`` lists what
+        each ``preempt`` call returned, newest request first; ``plan`` is None
+        when no request was left."""
+        reqs = [[int(r)] if np.isscalar(r) else [int(s) for s in r] for r in requests]
+        preempted = []
+        while reqs:
+            ids = [s for r in reqs for s in r]
+            try:
+                return self.plan_step(ids, max_blocks, group_prefixes), preempted
+            except PagedKVError as e:
+                if e.status != PKV_ERR_POOL_EXHAUSTED:
+                    raise
+            preempted.append(preempt(reqs.pop()))
+        return None, preempted
 
     def plan_prefill(self, seq_ids, chunks, max_blocks=None):
         """Host half of a chunked-prefill step: ``chunks[i]`` appends to sequence
