@@ -554,8 +554,8 @@ class BlockManager:
     def build_tables(self, seq_ids, max_blocks):
         """int32 tables ``[n, max_blocks]`` (-1 padded) and int32 lengths ``[n]``."""
         ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
-        tables = np.zeros((len(ids), max_blocks), dtype=np.int32)
-        lens = np.zeros(len(ids), dtype=np.int32)
+        tables = np.empty((len(ids), max_blocks), dtype=np.int32)   # every entry written
+        lens = np.empty(len(ids), dtype=np.int32)
         _check(self._lib.bm_build_tables(self._h, _i64p(ids), len(ids), max_blocks,
                                          _i32p(tables), _i32p(lens)), "bm_build_tables")
         return tables, lens

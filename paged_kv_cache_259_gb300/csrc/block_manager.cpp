@@ -86,6 +86,8 @@ struct pkv_block_manager {
         std::vector<int64_t> tokens;     // token ids (prefix caching only)
         std::vector<uint64_t> hashes;    // prefix hash after each full block
         bool swapped = false;            // table holds host blocks
+        uint64_t demand_epoch = 0;       // Demand scratch: length within a batch count
+        int64_t demand_len = 0;
     };
     std::unordered_map<int64_t, Seq> seqs;
 
@@ -99,6 +101,12 @@ struct pkv_block_manager {
     std::vector<std::list<int32_t>::iterator> ev_pos;
     std::vector<char> in_ev;
     int64_t hit_blocks = 0, lookup_blocks = 0;
+
+    // ---- Demand scratch: references given up by CoW within one batch count,
+    // valid where drop_epoch matches the count's epoch (no clearing per batch)
+    uint64_t epoch = 0;
+    std::vector<uint64_t> drop_epoch;
+    std::vector<int32_t> drop_count;
 
     // ---- host pool (swapping)
     int num_host_blocks = 0;
@@ -228,32 +236,37 @@ struct pkv_block_manager {
     // What a batch of appends would take, found without changing anything, so
     // that a batch either fits whole or is refused whole. Feed it the batch in
     // order as (sequence, count) runs; a sequence may come back in later runs.
+    // Allocation-free: per-sequence and per-block scratch stamped with a fresh
+    // epoch, so one count never sees another's.
     struct Demand {
-        const pkv_block_manager& bm;
-        std::unordered_map<const Seq*, int64_t> len;    // sequences appended to so far
-        std::unordered_map<int32_t, int64_t> dropped;   // references given up by CoW
+        pkv_block_manager& bm;
+        const uint64_t epoch;
         int64_t blocks = 0, cows = 0;
 
-        explicit Demand(const pkv_block_manager& m) : bm(m) {}
+        explicit Demand(pkv_block_manager& m) : bm(m), epoch(++m.epoch) {}
 
-        void add(const Seq& s, int64_t k) {
+        void add(Seq& s, int64_t k) {
             if (k <= 0) return;
             const int64_t bs = bm.block_size;
-            auto it = len.find(&s);
-            const bool touched = it != len.end();
-            const int64_t L = touched ? it->second : s.len;
+            const bool touched = s.demand_epoch == epoch;
+            const int64_t L = touched ? s.demand_len : s.len;
             // A sequence's first append into a partial last block copies it
             // when another table still holds it; later ones write in place.
             if (!touched && L % bs != 0) {
                 const int32_t last = s.table.back();
-                if (bm.ref[last] - dropped[last] > 1) {
+                if (bm.drop_epoch[last] != epoch) {
+                    bm.drop_epoch[last] = epoch;
+                    bm.drop_count[last] = 0;
+                }
+                if (bm.ref[last] - bm.drop_count[last] > 1) {
                     blocks += 1;
                     cows += 1;
-                    dropped[last] += 1;
+                    bm.drop_count[last] += 1;
                 }
             }
             blocks += (L + k + bs - 1) / bs - (L + bs - 1) / bs;   // block starts in [L, L+k)
-            len[&s] = L + k;
+            s.demand_epoch = epoch;
+            s.demand_len = L + k;
         }
 
         bool fits() const { return blocks <= (int64_t)bm.device_available(); }
@@ -272,6 +285,8 @@ pkv_block_manager* bm_create(int num_blocks, int block_size, const int32_t* free
     bm->num_blocks = num_blocks;
     bm->block_size = block_size;
     bm->ref.assign(num_blocks, 0);
+    bm->drop_epoch.assign(num_blocks, 0);
+    bm->drop_count.assign(num_blocks, 0);
     std::vector<char> seen(num_blocks, 0);
     for (int i = 0; i < num_free; ++i) {
         const int32_t b = free_order[i];
@@ -429,7 +444,7 @@ int bm_build_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int n, 
         if ((int64_t)s.table.size() > max_blocks || s.len > INT32_MAX || s.swapped)
             return PKV_ERR_INVALID_ARG;
         int32_t* row = tables + (size_t)i * max_blocks;
-        for (int j = 0; j < max_blocks; ++j) row[j] = j < (int)s.table.size() ? s.table[j] : -1;
+        std::fill(std::copy(s.table.begin(), s.table.end(), row), row + max_blocks, -1);
         seq_lens[i] = (int32_t)s.len;
     }
     return PKV_OK;
@@ -471,18 +486,26 @@ int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
         seqs[i] = &it->second;
         seq_group[i] = -1;
     }
-    std::unordered_map<int32_t, std::vector<int>> buckets;
-    std::vector<int32_t> order;                      // first blocks in batch order
-    for (int i = 0; i < n; ++i) {
-        if (seqs[i]->table.empty()) continue;
-        const int32_t key = seqs[i]->table[0];
-        auto& v = buckets[key];
-        if (v.empty()) order.push_back(key);
-        v.push_back(i);
+    // Buckets of batch indices by first block, each in batch order, the buckets
+    // in order of their first member: (block, index) pairs sorted, then the
+    // runs of equal blocks sorted by their first index.
+    std::vector<std::pair<int32_t, int>> by_block;
+    by_block.reserve((size_t)n);
+    for (int i = 0; i < n; ++i)
+        if (!seqs[i]->table.empty()) by_block.emplace_back(seqs[i]->table[0], i);
+    std::sort(by_block.begin(), by_block.end());
+    struct Run { int first; size_t a, b; };
+    std::vector<Run> runs;
+    for (size_t a = 0, b; a < by_block.size(); a = b) {
+        for (b = a + 1; b < by_block.size() && by_block[b].first == by_block[a].first; ++b) {}
+        runs.push_back({by_block[a].second, a, b});
     }
+    std::sort(runs.begin(), runs.end(), [](const Run& x, const Run& y) { return x.first < y.first; });
+    std::vector<int> mem;
     int ng = 0;
-    for (int32_t key : order) {
-        const std::vector<int>& mem = buckets[key];
+    for (const Run& r : runs) {
+        mem.clear();
+        for (size_t j = r.a; j < r.b; ++j) mem.push_back(by_block[j].second);
         for (size_t c = 0; c < mem.size(); c += (size_t)max_members) {
             const size_t e = std::min(mem.size(), c + (size_t)max_members);
             if (e - c < 2) continue;
