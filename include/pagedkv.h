@@ -425,15 +425,17 @@ PKV_API int bm_seq_len(const pkv_block_manager* bm, int64_t seq_id, int* len);
 PKV_API int bm_refcount(const pkv_block_manager* bm, int block, int* count);
 PKV_API int bm_num_free(const pkv_block_manager* bm);
 /* Prefix groups for paged_attention_decode_grouped over the batch seq_ids[0..n):
- * sequences whose tables start with the same physical block are grouped (in
- * batch order, at most max_members per group); a group's prefix is the number
- * of leading block ids common to all members that are full for every member.
+ * sequences whose tables start with the same physical block form a bucket; the
+ * buckets are taken in the order of their first member in the batch, and each
+ * is cut, in batch order, into consecutive runs of max_members (the last may be
+ * shorter). A run's prefix is the number of leading block ids common to all of
+ * its members that are full for every member; a run with two or more members
+ * and a prefix of at least one block is the next group.
  * Writes group_members [n][max_members] (batch indices, -1 padded; at most n
  * groups), group_prefix [n], seq_group [n] (the sequence's group or -1),
  * group_blocks [n] (may be null: the group's block list for the grouped decode,
  * its prefix once plus each member's blocks after it; the largest is that
- * call's max_group_blocks) and *num_groups. Groups with a prefix of 0 blocks or
- * a single member are not emitted. */
+ * call's max_group_blocks) and *num_groups. */
 PKV_API int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
                      int max_members, int32_t* group_members, int32_t* group_prefix,
                      int32_t* seq_group, int32_t* group_blocks, int* num_groups);
