@@ -317,10 +317,18 @@ class PagedKVCache:
         """Host half of resuming sequences preempted by recomputation: each is
         added again and all of its ``lens[s]`` tokens form one chunk, so one
         chunked-prefill step (``prefill_step`` with their recomputed q, K, V)
-        writes their K/V into fresh blocks and attends over them."""
-        for s in seq_ids:
-            self.bm.add_seq(int(s))
-        return self.plan_prefill(seq_ids, [lens[int(s)] for s in seq_ids], max_blocks)
+        writes their K/V into fresh blocks and attends over them. If the pool
+        cannot take them all, none is added and the error is raised."""
+        added = []
+        try:
+            for s in seq_ids:
+                self.bm.add_seq(int(s))
+                added.append(int(s))
+            return self.plan_prefill(seq_ids, [lens[int(s)] for s in seq_ids], max_blocks)
+        except PagedKVError:
+            for s in reversed(added):                # still preempted, nothing held
+                self.bm.free_seq(s)
+            raise
 
     def staging_pools(self, n):
         """Device staging pools of at least n blocks (grown on demand)."""
@@ -336,15 +344,26 @@ class PagedKVCache:
         """Host half of a prefill step with prefix caching (the manager must have
         it on): each new sequence reuses the cached full blocks of its prompt and
         the rest of the prompt is its chunk. ``plan.cached[i]`` = prompt tokens of
-        sequence i found in the cache."""
+        sequence i found in the cache.
+
+        If the pool cannot take every prompt, the sequences this call added are
+        freed again, newest first, and the error is raised: their blocks return
+        as if they had finished (full prompt blocks stay cached)."""
         ids = np.asarray(seq_ids, dtype=np.int64)
         cached, slots, pairs = [], [], []
-        for sid, p in zip(ids, prompts):
-            n = self.bm.add_seq_prompt(int(sid), p)
-            s, pr = self.bm.append_tokens(int(sid), np.asarray(p)[n:])
-            cached.append(n)
-            slots.append(s)
-            pairs.append(pr)
+        added = []
+        try:
+            for sid, p in zip(ids, prompts):
+                n = self.bm.add_seq_prompt(int(sid), p)
+                added.append(int(sid))
+                s, pr = self.bm.append_tokens(int(sid), np.asarray(p)[n:])
+                cached.append(n)
+                slots.append(s)
+                pairs.append(pr)
+        except PagedKVError:
+            for s in reversed(added):
+                self.bm.free_seq(s)
+            raise
         chunks = np.array([len(p) - n for p, n in zip(prompts, cached)], dtype=np.int64)
         if max_blocks is None:
             max_blocks = max(1, max(-(-self.bm.seq_len(int(s)) // self.block_size) for s in ids))

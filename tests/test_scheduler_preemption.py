@@ -19,9 +19,10 @@ from oracle.block_manager import BlockManager as OracleBM, PoolExhausted
 from paged_kv_cache_259_gb300.engine import PagedKVCache
 
 
-def host_cache(nb, bs, order):
+def host_cache(nb, bs, order, prefix_caching=False):
     library()
-    return PagedKVCache(nb, 4, 4, 16, bs, torch.bfloat16, order, device="cpu")
+    return PagedKVCache(nb, 4, 4, 16, bs, torch.bfloat16, order, device="cpu",
+                        prefix_caching=prefix_caching)
 
 
 def oracle_step(ora, requests):
@@ -152,3 +153,47 @@ def test_random_steps_match_the_oracle(seed):
                 cache.bm.free_seq(s)
                 ora.free_seq(s)
     assert preemptions > 0
+
+
+def test_resume_that_does_not_fit_adds_nothing():
+    cache = host_cache(4, 8, range(4))
+    bm = cache.bm
+    bm.add_seq(0)
+    bm.append_n(0, 20)                               # 3 blocks
+    lens = cache.preempt_by_recompute([0])
+    bm.add_seq(1)
+    bm.append_n(1, 9)                                # 2 blocks: 2 left, 0 needs 3
+    free = bm.free_list()
+    with pytest.raises(pkv.PagedKVError) as e:
+        cache.plan_resume([0], lens)
+    assert e.value.status == -5
+    with pytest.raises(pkv.PagedKVError) as e:
+        bm.seq_len(0)
+    assert e.value.status == -4                      # still preempted
+    assert bm.free_list() == free
+    bm.free_seq(1)
+    plan = cache.plan_resume([0], lens)
+    assert list(plan.chunks) == [20] and bm.seq_len(0) == 20
+
+
+def test_prompts_that_do_not_fit_are_freed_again():
+    bs = 8
+    cache = host_cache(6, bs, range(6), prefix_caching=True)
+    bm = cache.bm
+    system = list(range(100, 100 + 2 * bs))          # two full blocks
+    cache.plan_prompts([0], [system + [1]])
+    bm.free_seq(0)                                   # its full blocks stay cached
+    assert bm.cache_stats()[2:] == (2, 2)
+    before = (bm.free_list(), bm.evictable_list())
+    with pytest.raises(pkv.PagedKVError) as e:       # 1 reuses both; 2 needs 5 of 4 left
+        cache.plan_prompts([1, 2], [system + [2], list(range(200, 200 + 5 * bs))])
+    assert e.value.status == -5
+    for sid in (1, 2):
+        with pytest.raises(pkv.PagedKVError):
+            bm.seq_len(sid)
+    assert [bm.refcount(b) for b in range(6)] == [0] * 6
+    free, evictable = bm.free_list(), bm.evictable_list()
+    assert sorted(free + evictable) == sorted(before[0] + before[1])
+    assert sorted(evictable) == sorted(before[1])    # the system prompt is still cached
+    plan = cache.plan_prompts([3], [system + [3]])
+    assert list(plan.cached) == [2 * bs]
