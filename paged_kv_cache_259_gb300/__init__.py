@@ -149,6 +149,51 @@ def _cuda(t, what, contiguous=True):
     return t
 
 
+def _on_gpu(named):
+    """Every (tensor, name) a contiguous CUDA tensor, all on one device; returns
+    that device. Called after the shape checks, so those run without a GPU."""
+    dev = None
+    for t, n in named:
+        _cuda(t, n)
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{n} is on {t.device}, the other tensors on {dev}")
+    return dev
+
+
+def _tensors(named):
+    for t, n in named:
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{n} must be a tensor")
+
+
+def _decode_shapes(out, q, k_pool, v_pool, block_tables, seq_lens):
+    """(B, Hq, D, NB, Hkv, bs) of a decode call; raise on a mismatch."""
+    _tensors(((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
+              (block_tables, "block_tables"), (seq_lens, "seq_lens")))
+    if q.dim() != 3 or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("q and out must be [B, Hq, D] of the same dtype")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    B, Hq, D = q.shape
+    NB, Hkv, bs, D2 = _pool_dims(k_pool, v_pool)
+    if D2 != D or block_tables.dim() != 2 or block_tables.shape[0] != B or \
+            tuple(seq_lens.shape) != (B,):
+        raise ValueError("inconsistent shapes: block_tables must be [B, max_blocks], "
+                         "seq_lens [B], pools of q's head_dim")
+    return B, Hq, D, NB, Hkv, bs
+
+
+def _workspace(workspace, device):
+    if workspace is None:
+        return None, 0
+    _on_gpu(((workspace, "workspace"),))
+    if workspace.device != device:
+        raise ValueError(f"workspace is on {workspace.device}, the other tensors on {device}")
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
 def _stream_ptr(stream, device):
     if stream is None:
         stream = torch.cuda.current_stream(device)
@@ -236,27 +281,16 @@ def paged_attention_decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale
     as split-KV scratch (see ``paged_attention_workspace_size``) or None.
     """
     lib = load_library()
-    for t, n in ((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
-                 (block_tables, "block_tables"), (seq_lens, "seq_lens")):
-        _cuda(t, n)
-    if q.dim() != 3 or out.shape != q.shape or out.dtype != q.dtype:
-        raise ValueError("q and out must be [B, Hq, D] of the same dtype")
-    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
-        raise TypeError("block_tables and seq_lens must be int32")
-    B, Hq, D = q.shape
-    NB, Hkv, bs, D2 = _pool_dims(k_pool, v_pool)
-    if D2 != D or block_tables.dim() != 2 or block_tables.shape[0] != B or seq_lens.shape != (B,):
-        raise ValueError("inconsistent shapes")
-    ws_ptr, ws_bytes = None, 0
-    if workspace is not None:
-        _cuda(workspace, "workspace")
-        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    with _on_device(q.device):
+    B, Hq, D, NB, Hkv, bs = _decode_shapes(out, q, k_pool, v_pool, block_tables, seq_lens)
+    dev = _on_gpu(((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
+                   (block_tables, "block_tables"), (seq_lens, "seq_lens")))
+    ws_ptr, ws_bytes = _workspace(workspace, dev)
+    with _on_device(dev):
         st = lib.paged_attention_decode(
             out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
             block_tables.data_ptr(), seq_lens.data_ptr(), B, block_tables.shape[1], NB,
             Hq, Hkv, D, bs, float(scale), _dt(q, "q"), _dt(k_pool, "k_pool"),
-            float(k_scale), float(v_scale), ws_ptr, ws_bytes, _stream_ptr(stream, q.device))
+            float(k_scale), float(v_scale), ws_ptr, ws_bytes, _stream_ptr(stream, dev))
     _check(st, "paged_attention_decode")
     return out
 
@@ -274,29 +308,24 @@ def paged_attention_decode_grouped(out, q, k_pool, v_pool, block_tables, seq_len
     max_group_blocks: the largest of ``prefix_groups``' list blocks (0: unknown).
     """
     lib = load_library()
-    for t, n in ((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
-                 (block_tables, "block_tables"), (seq_lens, "seq_lens"),
-                 (seq_group, "seq_group"), (group_members, "group_members"),
-                 (group_prefix_blocks, "group_prefix_blocks")):
-        _cuda(t, n)
-    for t in (block_tables, seq_lens, seq_group, group_members, group_prefix_blocks):
-        if t.dtype != torch.int32:
-            raise TypeError("tables, lengths and group arrays must be int32")
-    B, Hq, D = q.shape
-    NB, Hkv, bs, D2 = _pool_dims(k_pool, v_pool)
-    if out.shape != q.shape or out.dtype != q.dtype or D2 != D or seq_lens.shape != (B,) or \
-            seq_group.shape != (B,) or group_members.dim() != 2 or \
-            group_prefix_blocks.shape != (group_members.shape[0],):
-        raise ValueError("inconsistent shapes")
+    B, Hq, D, NB, Hkv, bs = _decode_shapes(out, q, k_pool, v_pool, block_tables, seq_lens)
+    groups = [(seq_group, "seq_group"), (group_members, "group_members"),
+              (group_prefix_blocks, "group_prefix_blocks")]
     if ungrouped is not None:
-        _cuda(ungrouped, "ungrouped")
-        if ungrouped.dtype != torch.int32:
-            raise TypeError("ungrouped must be int32")
-    ws_ptr, ws_bytes = None, 0
-    if workspace is not None:
-        _cuda(workspace, "workspace")
-        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    with _on_device(q.device):
+        groups.append((ungrouped, "ungrouped"))
+    _tensors(groups)
+    for t, n in groups:
+        if t.dtype != torch.int32:
+            raise TypeError(f"{n} must be int32")
+    if tuple(seq_group.shape) != (B,) or group_members.dim() != 2 or \
+            tuple(group_prefix_blocks.shape) != (group_members.shape[0],) or \
+            (ungrouped is not None and ungrouped.dim() != 1):
+        raise ValueError("inconsistent shapes: seq_group [B], group_members [G, max_members], "
+                         "group_prefix_blocks [G], ungrouped [n]")
+    dev = _on_gpu([(out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
+                   (block_tables, "block_tables"), (seq_lens, "seq_lens")] + groups)
+    ws_ptr, ws_bytes = _workspace(workspace, dev)
+    with _on_device(dev):
         st = lib.paged_attention_decode_grouped(
             out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
             block_tables.data_ptr(), seq_lens.data_ptr(), B, block_tables.shape[1], NB,
@@ -305,7 +334,7 @@ def paged_attention_decode_grouped(out, q, k_pool, v_pool, block_tables, seq_len
             group_prefix_blocks.data_ptr(), group_members.shape[0], group_members.shape[1],
             int(max_group_blocks), None if ungrouped is None else ungrouped.data_ptr(),
             -1 if ungrouped is None else ungrouped.numel(),
-            ws_ptr, ws_bytes, _stream_ptr(stream, q.device))
+            ws_ptr, ws_bytes, _stream_ptr(stream, dev))
     _check(st, "paged_attention_decode_grouped")
     return out
 
@@ -325,21 +354,19 @@ def paged_attention_decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_len
     capture. Refuses batches with ``B * Hq * 2 * (D + 2) * 4 > NOALLOC_WORKSPACE_BYTES``.
     """
     lib = load_library()
-    for t, n in ((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
-                 (block_tables, "block_tables"), (seq_lens, "seq_lens")):
-        _cuda(t, n)
-    B, Hq, D = q.shape
-    NB, Hkv, bs, _ = _pool_dims(k_pool, v_pool)
+    B, Hq, D, NB, Hkv, bs = _decode_shapes(out, q, k_pool, v_pool, block_tables, seq_lens)
     need = B * Hq * 2 * (D + 2) * 4
     if need > NOALLOC_WORKSPACE_BYTES:
         raise PagedKVError(-1, f"paged_attention_decode_noalloc: batch needs {need} bytes of "
                                f"scratch, the fixed array holds {NOALLOC_WORKSPACE_BYTES}")
-    with _on_device(q.device):
+    dev = _on_gpu(((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
+                   (block_tables, "block_tables"), (seq_lens, "seq_lens")))
+    with _on_device(dev):
         st = lib.paged_attention_decode_noalloc(
             out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
             block_tables.data_ptr(), seq_lens.data_ptr(), B, block_tables.shape[1], NB,
             Hq, Hkv, D, bs, float(scale), _dt(q, "q"), _dt(k_pool, "k_pool"),
-            float(k_scale), float(v_scale), _stream_ptr(stream, q.device))
+            float(k_scale), float(v_scale), _stream_ptr(stream, dev))
     _check(st, "paged_attention_decode_noalloc")
     return out
 
@@ -355,27 +382,30 @@ def paged_attention_prefill(out, q, k_pool, v_pool, block_tables, seq_lens, quer
     ``[B]``; query_start int32 ``[B + 1]``; ``max_query_len`` >= every C_b.
     """
     lib = load_library()
-    for t, n in ((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
-                 (block_tables, "block_tables"), (seq_lens, "seq_lens"),
-                 (query_start, "query_start")):
-        _cuda(t, n)
+    named = ((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
+             (block_tables, "block_tables"), (seq_lens, "seq_lens"), (query_start, "query_start"))
+    _tensors(named)
     for t in (block_tables, seq_lens, query_start):
         if t.dtype != torch.int32:
             raise TypeError("block_tables, seq_lens and query_start must be int32")
     if q.dim() != 3 or out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("q and out must be [T, Hq, D] of the same dtype")
+    if seq_lens.dim() != 1:
+        raise ValueError("seq_lens must be [B]")
     B = seq_lens.shape[0]
     T, Hq, D = q.shape
     NB, Hkv, bs, D2 = _pool_dims(k_pool, v_pool)
     if D2 != D or block_tables.dim() != 2 or block_tables.shape[0] != B or \
-            query_start.shape != (B + 1,):
-        raise ValueError("inconsistent shapes")
-    with _on_device(q.device):
+            tuple(query_start.shape) != (B + 1,):
+        raise ValueError("inconsistent shapes: block_tables [B, max_blocks], query_start "
+                         "[B + 1], pools of q's head_dim")
+    dev = _on_gpu(named)
+    with _on_device(dev):
         st = lib.paged_attention_prefill(
             out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
             block_tables.data_ptr(), seq_lens.data_ptr(), query_start.data_ptr(), B,
             int(max_query_len), block_tables.shape[1], NB, Hq, Hkv, D, bs, float(scale),
-            _dt(q, "q"), _dt(k_pool, "k_pool"), _stream_ptr(stream, q.device))
+            _dt(q, "q"), _dt(k_pool, "k_pool"), _stream_ptr(stream, dev))
     _check(st, "paged_attention_prefill")
     return out
 
@@ -384,38 +414,44 @@ def reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, k_scale=1.0, v_scale=1
     """Write k/v ``[T, Hkv, D]`` into the pools (library layout) at ``slot_mapping``
     (int64 ``[T]``)."""
     lib = load_library()
-    for t, n in ((k, "k"), (v, "v"), (k_pool, "k_pool"), (v_pool, "v_pool"),
-                 (slot_mapping, "slot_mapping")):
-        _cuda(t, n)
+    named = ((k, "k"), (v, "v"), (k_pool, "k_pool"), (v_pool, "v_pool"),
+             (slot_mapping, "slot_mapping"))
+    _tensors(named)
     if slot_mapping.dtype != torch.int64:
         raise TypeError("slot_mapping must be int64")
+    if k.dim() != 3:
+        raise ValueError("k and v must be [T, Hkv, D]")
     T, Hkv, D = k.shape
     NB, Hkv2, bs, D2 = _pool_dims(k_pool, v_pool)
     if v.shape != k.shape or v.dtype != k.dtype or (Hkv2, D2) != (Hkv, D) or \
-            slot_mapping.shape != (T,):
-        raise ValueError("inconsistent shapes")
-    with _on_device(k.device):
+            tuple(slot_mapping.shape) != (T,):
+        raise ValueError("inconsistent shapes: k and v [T, Hkv, D] like the pools, "
+                         "slot_mapping [T]")
+    dev = _on_gpu(named)
+    with _on_device(dev):
         st = lib.reshape_and_cache(
             k.data_ptr(), v.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
             slot_mapping.data_ptr(), T, Hkv, D, bs, NB, _dt(k, "k"), _dt(k_pool, "k_pool"),
-            float(k_scale), float(v_scale), _stream_ptr(stream, k.device))
+            float(k_scale), float(v_scale), _stream_ptr(stream, dev))
     _check(st, "reshape_and_cache")
 
 
 def copy_blocks(k_pool, v_pool, src_dst_pairs, stream=None):
     """``pool[dst] = pool[src]`` for each row of int64 ``src_dst_pairs [P, 2]``."""
     lib = load_library()
-    for t, n in ((k_pool, "k_pool"), (v_pool, "v_pool"), (src_dst_pairs, "src_dst_pairs")):
-        _cuda(t, n)
+    named = ((k_pool, "k_pool"), (v_pool, "v_pool"), (src_dst_pairs, "src_dst_pairs"))
+    _tensors(named)
     if src_dst_pairs.dtype != torch.int64 or src_dst_pairs.dim() != 2 or \
-            src_dst_pairs.shape[1] != 2 or k_pool.shape[0] != v_pool.shape[0] or \
-            k_pool.numel() != v_pool.numel():
-        raise ValueError("src_dst_pairs must be int64 [P, 2]; pools of one shape")
+            src_dst_pairs.shape[1] != 2 or k_pool.dim() < 1 or v_pool.dim() < 1 or \
+            k_pool.shape[0] != v_pool.shape[0] or k_pool.numel() != v_pool.numel() or \
+            k_pool.dtype != v_pool.dtype:
+        raise ValueError("src_dst_pairs must be int64 [P, 2]; pools of one shape and dtype")
+    dev = _on_gpu(named)
     block_bytes = k_pool[0].numel() * k_pool.element_size()
-    with _on_device(k_pool.device):
+    with _on_device(dev):
         st = lib.copy_blocks(k_pool.data_ptr(), v_pool.data_ptr(), src_dst_pairs.data_ptr(),
                              src_dst_pairs.shape[0], k_pool.shape[0], block_bytes,
-                             _stream_ptr(stream, k_pool.device))
+                             _stream_ptr(stream, dev))
     _check(st, "copy_blocks")
 
 
