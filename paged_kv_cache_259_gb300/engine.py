@@ -207,7 +207,8 @@ class PagedKVCache:
         ids = np.asarray(seq_ids, dtype=np.int64)
         slots, pairs = self.bm.append_slots(ids)
         if max_blocks is None:
-            max_blocks = max(1, max(-(-self.bm.seq_len(int(s)) // self.block_size) for s in ids))
+            max_blocks = max(1, max((-(-self.bm.seq_len(int(s)) // self.block_size) for s in ids),
+                                    default=0))
         tables, lens = self.bm.build_tables(ids, max_blocks)
         plan = StepPlan(ids, slots, pairs, tables, lens)
         if group_prefixes and self.k_pool.dtype != torch.float32:
@@ -252,7 +253,8 @@ class PagedKVCache:
         chunks = np.asarray(chunks, dtype=np.int64)
         slots, pairs = self.bm.append_slots(np.repeat(ids, chunks))
         if max_blocks is None:
-            max_blocks = max(1, max(-(-self.bm.seq_len(int(s)) // self.block_size) for s in ids))
+            max_blocks = max(1, max((-(-self.bm.seq_len(int(s)) // self.block_size) for s in ids),
+                                    default=0))
         tables, lens = self.bm.build_tables(ids, max_blocks)
         qs = np.zeros(len(ids) + 1, dtype=np.int32)
         qs[1:] = np.cumsum(chunks)
@@ -366,7 +368,8 @@ class PagedKVCache:
             raise
         chunks = np.array([len(p) - n for p, n in zip(prompts, cached)], dtype=np.int64)
         if max_blocks is None:
-            max_blocks = max(1, max(-(-self.bm.seq_len(int(s)) // self.block_size) for s in ids))
+            max_blocks = max(1, max((-(-self.bm.seq_len(int(s)) // self.block_size) for s in ids),
+                                    default=0))
         tables, lens = self.bm.build_tables(ids, max_blocks)
         qs = np.zeros(len(ids) + 1, dtype=np.int32)
         qs[1:] = np.cumsum(chunks)

@@ -155,6 +155,23 @@ def test_zero_length_sequences_give_zero_rows():
     assert torch.isfinite(out).all() and torch.count_nonzero(out[1]) > 0
 
 
+def test_an_empty_step_launches_nothing():
+    """No sequences: the engine plans empty arrays and every call returns at once."""
+    from paged_kv_cache_259_gb300.engine import PagedKVCache
+    cache = PagedKVCache(8, 8, 2, 128, 16, torch.bfloat16, range(8), "cuda")
+    n0 = pkv.kernel_launches()
+    plan = cache.plan_step([])
+    out = torch.empty(0, 8, 128, dtype=torch.bfloat16, device="cuda")
+    q = torch.empty(0, 8, 128, dtype=torch.bfloat16, device="cuda")
+    kv = torch.empty(0, 2, 128, dtype=torch.bfloat16, device="cuda")
+    cache.step(q, kv, kv, plan.device_tensors("cuda"), out, 0.1,
+               workspace=cache.workspace(1, plan.tables.shape[1]))
+    pre = cache.plan_prefill([], [])
+    cache.prefill_step(q, kv, kv, pre.device_tensors("cuda"), out, 0.1, pre.max_query_len)
+    torch.cuda.synchronize()
+    assert pkv.kernel_launches() == n0 and pkv.get_device_error() == 0
+
+
 @pytest.mark.parametrize("Hq", [4, 16])          # CUDA-core (MHA) and tensor-core (GQA) paths
 def test_bad_block_id_sets_error_word_and_skips(Hq):
     q, kp, vp, bt, kc, vc = _decode_args(3, Hq, 4, 128, 16, 32, 8)

@@ -197,3 +197,19 @@ def test_prompts_that_do_not_fit_are_freed_again():
     assert sorted(evictable) == sorted(before[1])    # the system prompt is still cached
     plan = cache.plan_prompts([3], [system + [3]])
     assert list(plan.cached) == [2 * bs]
+
+
+def test_empty_batches_plan_to_empty_steps():
+    """An empty step plans to empty arrays (the library returns at once for zero
+    sequences, tokens or pairs)."""
+    cache = host_cache(4, 8, range(4), prefix_caching=True)
+    plan = cache.plan_step([])
+    assert plan.slots.shape == (0,) and plan.pairs.shape == (0, 2)
+    assert plan.tables.shape == (0, 1) and plan.lens.shape == (0,) and plan.num_groups == 0
+    pre = cache.plan_prefill([], [])
+    assert pre.slots.shape == (0,) and list(pre.query_start) == [0] and pre.max_query_len == 0
+    prompts = cache.plan_prompts([], [])
+    assert prompts.slots.shape == (0,) and list(prompts.query_start) == [0]
+    plan, gone = cache.plan_step_preempting([], lambda ids: pytest.fail("preempted"))
+    assert plan is None and gone == []
+    assert cache.bm.free_list() == [0, 1, 2, 3]
