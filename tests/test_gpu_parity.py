@@ -155,6 +155,33 @@ def test_zero_length_sequences_give_zero_rows():
     assert torch.isfinite(out).all() and torch.count_nonzero(out[1]) > 0
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2)])   # CUDA-core (MHA) and tensor-core (GQA)
+def test_largest_batch_of_65535_sequences(Hq, Hkv):
+    """The largest batch the decode takes (the sequence index is a grid
+    dimension): 65,535 short sequences over a small shared pool, zero lengths
+    included; sampled rows against the oracle, the first and last sequences among
+    them."""
+    from oracle import attention as oatt
+    B, D, bs, NB, MB = 65535, 128, 16, 256, 4
+    q, kp, vp, _, kc, vc = _decode_args(B, Hq, Hkv, D, bs, NB, MB, seed=Hq)
+    rng = np.random.default_rng(Hq)
+    tables = rng.integers(0, NB, size=(B, MB)).astype(np.int32)
+    lens = rng.integers(0, MB * bs + 1, size=B).astype(np.int32)
+    lens[0], lens[-1] = MB * bs, 1
+    out = torch.full_like(q, float("nan"))
+    pkv.paged_attention_decode(out, q, kp, vp, torch.from_numpy(tables).cuda(),
+                               torch.from_numpy(lens).cuda(), 1 / math.sqrt(D))
+    assert pkv.get_device_error() == 0
+    got = out.float().cpu()
+    assert torch.isfinite(got).all()
+    assert torch.count_nonzero(got[torch.from_numpy(lens == 0)]) == 0
+    picks = zip(rng.integers(0, B, 400), rng.integers(0, Hq, 400))
+    units = sorted({(0, 0), (B - 1, Hq - 1)} | {(int(b), int(h)) for b, h in picks})
+    ref = oatt.paged_decode(q.cpu(), kc, vc, tables, lens, 1 / math.sqrt(D), bs, units=units)
+    for (b, h), row in ref.items():
+        assert_close(got[b, h].numpy(), row, "bf16", f"sequence {b} head {h}")
+
+
 def test_an_empty_step_launches_nothing():
     """No sequences: the engine plans empty arrays and every call returns at once."""
     from paged_kv_cache_259_gb300.engine import PagedKVCache
