@@ -542,7 +542,9 @@ class BlockManager:
         return slot.value, ((s.value, d.value) if s.value >= 0 else None)
 
     def append_n(self, sid, n):
-        """n appends to one sequence; returns the CoW pairs raised, as a list."""
+        """n appends to one sequence; returns the CoW pairs raised, as a list. All
+        or nothing: if the pool cannot take them all, ``PagedKVError`` (status
+        ``PKV_ERR_POOL_EXHAUSTED``) and nothing changes."""
         cap = max(1, n)
         buf = np.zeros((cap, 2), dtype=np.int64)
         cnt = ctypes.c_int(0)
@@ -551,7 +553,9 @@ class BlockManager:
         return [tuple(map(int, r)) for r in buf[:cnt.value]]
 
     def append_slots(self, seq_ids):
-        """One append per sequence; returns (slots int64 array, pairs int64 [P, 2])."""
+        """One append per listed sequence, in list order (an id may repeat);
+        returns (slots int64 array, pairs int64 [P, 2]). All or nothing, as
+        ``append_n``."""
         ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
         slots = np.zeros(len(ids), dtype=np.int64)
         pairs = np.zeros((max(1, len(ids)), 2), dtype=np.int64)
@@ -644,7 +648,8 @@ class BlockManager:
         return n.value
 
     def append_tokens(self, sid, tokens):
-        """Appends with token ids; returns (slots int64 array, CoW pairs int64 [P, 2])."""
+        """Appends with token ids; returns (slots int64 array, CoW pairs int64
+        [P, 2]). All or nothing, as ``append_n``."""
         t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
         slots = np.zeros(max(1, len(t)), dtype=np.int64)
         pairs = np.zeros((max(1, len(t)), 2), dtype=np.int64)
