@@ -353,6 +353,15 @@ PKV_API unsigned long long pkv_kernel_launches(void);
  * Returns PKV_OK or PKV_ERR_CUDA. */
 PKV_API int pkv_get_device_error(int* code, void* stream);
 
+/* A check of the timeout path on the current device: launches on `stream` one
+ * kernel whose bounded wait cannot complete (a barrier nothing arrives at). The
+ * wait gives up after its limit (about one second) and sets the device error
+ * word, so the next pkv_get_device_error reports PKV_ERR_TIMEOUT; the context
+ * stays usable. Until the word is read, every other wait of the library on the
+ * device gives up at once, so run it while no other work of the library is in
+ * flight on the device. Returns PKV_OK or PKV_ERR_CUDA (launch failed). */
+PKV_API int pkv_check_wait_timeout(void* stream);
+
 /* ------------------------------------------------------------------------
  * Host block manager ("Como funciona"; glossary "Cách phân trang hoạt động",
  * "Chia sẻ block giữa các chuỗi"). Host memory only, no CUDA calls; not

@@ -25,7 +25,8 @@ __all__ = [
     "PagedKVError", "paged_attention_decode", "paged_attention_workspace_size",
     "paged_attention_decode_noalloc", "NOALLOC_WORKSPACE_BYTES", "paged_attention_decode_grouped",
     "paged_attention_prefill", "swap_blocks",
-    "reshape_and_cache", "copy_blocks", "get_device_error", "kernel_launches", "BlockManager",
+    "reshape_and_cache", "copy_blocks", "get_device_error", "check_wait_timeout",
+    "kernel_launches", "BlockManager",
     "library_path", "load_library", "pool_shapes", "pool_views", "pools_from_views", "PKV_F32",
     "PKV_BF16", "PKV_E4M3", "PKV_ERR_POOL_EXHAUSTED",
 ]
@@ -87,6 +88,7 @@ def load_library():
                                       c_int, c_int, c_float, c_float, vp]),
         "copy_blocks": (c_int, [vp, vp, vp, c_int, c_int, c_size, vp]),
         "pkv_get_device_error": (c_int, [ip, vp]),
+        "pkv_check_wait_timeout": (c_int, [vp]),
         "bm_create": (vp, [c_int, c_int, i32p, c_int]),
         "bm_destroy": (None, [vp]),
         "bm_add_seq": (c_int, [vp, ctypes.c_int64]),
@@ -494,6 +496,17 @@ def get_device_error(device=None, stream=None):
         _check(lib.pkv_get_device_error(ctypes.byref(code), _stream_ptr(stream, dev)),
                "pkv_get_device_error")
     return code.value
+
+
+def check_wait_timeout(device=None, stream=None):
+    """Launch the library's timeout check: a bounded wait that nothing completes
+    gives up after about a second, so the next ``get_device_error`` returns
+    ``PKV_ERR_TIMEOUT`` (-6). Run it with no other work of the library in flight
+    on the device."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    with _on_device(dev):
+        _check(lib.pkv_check_wait_timeout(_stream_ptr(stream, dev)), "pkv_check_wait_timeout")
 
 
 def _i32p(a):

@@ -81,9 +81,28 @@ int num_sms() {
     return n;
 }
 
+// One thread waits, bounded, on a barrier that nothing arrives at: the wait
+// gives up after kWaitLimitNs and records kErrTimeout, as a stuck wait in any
+// kernel of the library would.
+__global__ void wait_timeout_kernel(int* err) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t a = smem_addr(&bar);
+    mbar_init(a, 1);
+    if (!mbar_wait_bounded(a, 0, err)) flag_error(err, kErrTimeout);
+}
+
 }  // namespace pkv
 
 extern "C" {
+
+int pkv_check_wait_timeout(void* stream) {
+    int* err = pkv::error_word();
+    if (!err) return PKV_ERR_CUDA;
+    pkv::wait_timeout_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(err);
+    pkv::note_launch();
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PKV_OK : pkv::cuda_fail("pkv_check_wait_timeout: kernel launch", e);
+}
 
 const char* pkv_status_string(int status) {
     switch (status) {

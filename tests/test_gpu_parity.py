@@ -217,6 +217,27 @@ def test_bad_block_id_sets_error_word_and_skips(Hq):
     ac(out[:1].float().cpu().numpy(), ref, "bf16", "seq 0")
 
 
+def test_a_wait_nothing_completes_times_out_and_the_context_stays_usable():
+    """The library's timeout check: one bounded wait on a barrier nothing arrives
+    at gives up after its one-second limit and reports PKV_ERR_TIMEOUT (then the
+    word is clear); a decode right after it still matches the oracle."""
+    import time
+    from oracle import attention as oatt
+    assert pkv.get_device_error() == 0
+    t0 = time.perf_counter()
+    pkv.check_wait_timeout()
+    assert pkv.get_device_error() == -6
+    assert 0.9 < time.perf_counter() - t0 < 60
+    assert pkv.get_device_error() == 0
+    q, kp, vp, bt, kc, vc = _decode_args(2, 8, 2, 128, 16, 16, 4, seed=6)
+    lens = torch.tensor([50, 64], dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    pkv.paged_attention_decode(out, q, kp, vp, bt, lens, 0.1)
+    assert pkv.get_device_error() == 0
+    ref = oatt.paged_decode(q.cpu(), kc, vc, bt.cpu().numpy(), [50, 64], 0.1, 16)
+    assert_close(out.float().cpu().numpy(), ref, "bf16", "decode after the timeout check")
+
+
 def test_reshape_and_cache_bad_and_padding_slots():
     ks, vs = pkv.pool_shapes(4, 2, 16, 64, torch.bfloat16)
     kp = torch.zeros(ks, dtype=torch.bfloat16, device="cuda")
