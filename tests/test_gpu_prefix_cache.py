@@ -58,7 +58,9 @@ def run_gpu(w, warm_ids, step_ids):
     return outs, plans, cache, pkv.get_device_error()
 
 
-def run_oracle(w, warm_ids, step_ids):
+def run_oracle(w, warm_ids, step_ids, units=None):
+    """``units``: None (every output row) or {phase: [(row, head), ...]}; then each
+    phase's output is a dict of the sampled rows."""
     bm = PrefixCachingBlockManager(w.NB, w.bs, w.free_order)
     kp, vp = w.past_pools()
     outs, info = [], []
@@ -82,7 +84,8 @@ def run_oracle(w, warm_ids, step_ids):
         lens = np.array([bm.seq_len(sid) for sid in ids])
         chunks = [len(p) - n for p, n in zip(prompts, cached)]
         qs = np.concatenate([[0], np.cumsum(chunks)])
-        outs.append(oatt.paged_prefill(q, kp, vp, tables, lens, qs, w.scale, w.bs))
+        outs.append(oatt.paged_prefill(q, kp, vp, tables, lens, qs, w.scale, w.bs,
+                                       units=None if units is None else units[phase]))
         info.append({"cached": cached, "slots": slots, "pairs": pairs, "tables": tables,
                      "lens": lens})
         if phase == "warm":
@@ -117,3 +120,43 @@ def test_system_prompt_prefix_cache_parity(system, bs, Hq, Hkv):
     assert torch.equal(stored_bits(cache.v_view().cpu()), stored_bits(vp))
     for g, o, what in zip(g_out, o_out, ("warm", "step")):
         assert_close(g.numpy(), o, "bf16", what)
+
+
+def test_full_size_system_prompt_workload_sampled():
+    """The benchmark's prompt workload at full size (a 1024-token system prompt
+    served first, then 64 requests of it plus 256 tokens each), in the
+    benchmark's launch configuration: cached counts, slots, pairs, tables and
+    lengths bit for bit, every written slot bit for bit, sampled output rows
+    of both phases against the oracle."""
+    w = wl.PROMPT_CONFIGS["prefill_system_prompt_bf16"]()
+    warm_ids, step_ids = [10_000], list(range(w.B))
+    rng = np.random.default_rng(17)
+    g_out, g_plans, cache, err = run_gpu(w, warm_ids, step_ids)
+    assert err == 0
+    T = [int(gp.chunks.sum()) for gp in g_plans]
+    units = {}
+    for phase, n in zip(("warm", "step"), T):
+        u = {(0, 0), (n - 1, w.Hq - 1)}
+        while len(u) < 24:
+            u.add((int(rng.integers(n)), int(rng.integers(w.Hq))))
+        units[phase] = sorted(u)
+    o_out, o_info, kp, vp, obm = run_oracle(w, warm_ids, step_ids, units=units)
+    for gp, oi in zip(g_plans, o_info):
+        assert list(gp.cached) == oi["cached"]
+        assert list(gp.slots) == oi["slots"]
+        assert [tuple(x) for x in gp.pairs] == oi["pairs"]
+        assert np.array_equal(gp.tables.astype(np.int64), oi["tables"])
+        assert np.array_equal(gp.lens, oi["lens"])
+    assert o_info[1]["cached"] == [1024] * w.B          # the whole system prompt was reused
+    kview, vview = cache.k_view(), cache.v_view()
+    for gv, ov in ((kview, kp), (vview, vp)):
+        for oi in o_info:
+            sl = torch.tensor(oi["slots"], dtype=torch.int64)
+            b, off = sl // w.bs, sl % w.bs
+            got = gv[b.cuda(), :, off.cuda()].cpu()
+            assert torch.equal(stored_bits(got), stored_bits(ov[b, :, off]))
+    for g, o, phase in zip(g_out, o_out, ("warm", "step")):
+        got = np.stack([g[t, h].numpy() for t, h in units[phase]])
+        ref = np.stack([o[u] for u in units[phase]])
+        assert_close(got, ref, "bf16", f"full size, {phase}")
+        assert torch.isfinite(g).all()
