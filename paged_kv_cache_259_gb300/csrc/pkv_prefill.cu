@@ -243,6 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
         };
         int win = 0;
         int win_ids = check_id(lane, bt_early0), next_ids = check_id(32 + lane, bt_early1);
+        int issued = 0;                                    // tiles whose copies went out
+        bool land_pending = false;                         // the zero-fill tile's copies
         for (int j = 0; j < n_tiles; ++j) {
             if ((j * kBlocksPerTile) / 32 != win) {
                 ++win;
@@ -271,11 +273,14 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
                 const size_t off = ((size_t)my_id * p.num_kv_heads + hk) * (size_t)(BS * kD);
                 bulk_load(dst + (uint32_t)(lane * kBlockBytes), pool + off, kBlockBytes, land);
             }
+            issued = j + 1;
+            land_pending = fix;
             if (fix) {
                 if (!mbar_wait_bounded(bar(kBarLand), 0, p.err)) {
                     flag_error(p.err, kErrTimeout);
                     break;
                 }
+                land_pending = false;
                 // V of the last block: [BS/8 chunks][128 dims] rows of 8 tokens
                 const uint32_t vb = dst + (uint32_t)((blk_last - blk0) * kBlockBytes);
                 for (int row = lane; row < (BS / 8) * kD; row += 32) {
@@ -296,6 +301,15 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
                 if (lane == 0) mbar_arrive(bar(bar_full + s));
             }
         }
+        // Every copy this warp issued lands before the CTA may exit, also after a
+        // timeout here or in a consumer: wait, with a bound of its own, on the
+        // last tile issued on each stage (a stage takes a tile only after the
+        // previous one there landed, so that phase is unambiguous).
+        for (int jj = max(0, issued - kStages); jj < issued; ++jj) {
+            if (land_pending && jj == issued - 1) continue;   // it lands on kBarLand
+            (void)mbar_wait_bounded(bar(bar_full + jj % kStages), (jj / kStages) & 1, nullptr);
+        }
+        if (land_pending) (void)mbar_wait_bounded(bar(kBarLand), 0, nullptr);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ S issuer
         if (lane == 0) {
