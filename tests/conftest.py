@@ -1,18 +1,12 @@
 import os
 import sys
 
-import pytest
-
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+# A selected GPU test never passes without a GPU: each GPU module's fixture
+# fails when no CUDA device is visible.
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
-
-
-def pytest_collection_modifyitems(config, items):
-    # a GPU test must never run silently without a GPU: if one is selected on a
-    # machine without CUDA it fails loudly inside the test (see tests/_gpu.py)
-    pass
