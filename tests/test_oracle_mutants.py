@@ -3,10 +3,12 @@
 Each case plants one mistake in a copy of the oracle and runs
 tests/test_oracle_pins.py against that copy. Nothing is written to the
 repository's own oracle: the copy and the pins live in a temporary directory.
-Each run must fail the pins: the mistakes are a wrong head mapping, a dropped
-scale, an off-by-one mask or slot, the E4M3 rounding, bias or scale, a copy in
-the wrong direction, the free-list order, the copy-on-write count, beam
-parents, swap pairs and prefix-cache keys. A control run of the unchanged copy
+Each run must fail the pins. The mistakes cover head mapping, scales,
+softmax normalisation, causal positions, block and slot indexing, E4M3
+rounding, sign, NaN, bias, subnormals and scaling, and copy and swap
+direction. They also cover copy-on-write, fork counts, free-list order, beam
+parents, swap pairs and capacity, and prefix-cache keys, registration,
+revival and eviction order. A control run of the unchanged copy
 must pass, so a broken set-up cannot pass for a caught mistake.
 """
 import concurrent.futures
@@ -71,6 +73,28 @@ MUTANTS = [
      "            key = tuple(prompt[bs * i:bs * (i + 1)])"),
     ("evictable blocks in table order", "oracle/prefix_cache.py",
      "        self.evictable.extend(reversed(cached))", "        self.evictable.extend(cached)"),
+    ("prefill position counted from the chunk start", "oracle/attention.py",
+     "        p = L - C + (t - int(qs[b]))", "        p = (t - int(qs[b]))"),
+    ("softmax normalised by its largest term", "oracle/attention.py",
+     "    p = p / p.sum()", "    p = p / p.max()"),
+    ("E4M3 sign lost", "oracle/fp8_e4m3.py",
+     "    sign = np.signbit(x32).astype(np.int64) << 7",
+     "    sign = np.zeros_like(x32, dtype=np.int64)"),
+    ("E4M3 NaN for the whole top exponent", "oracle/fp8_e4m3.py",
+     "np.where((e == 15) & (m == 7), np.nan, out)", "np.where((e == 15), np.nan, out)"),
+    ("fork leaves the counts alone", "oracle/block_manager.py",
+     "        for b in self.tables[child]:\n            self.ref[b] += 1\n", ""),
+    ("swap-out accepts one block too many", "oracle/block_manager.py",
+     "        if len(table) > len(self.cpu_free):", "        if len(table) > len(self.cpu_free) + 1:"),
+    ("new block one token late", "oracle/block_manager.py",
+     "        if n % self.block_size == 0:", "        if n % self.block_size == 1 or n == 0:"),
+    ("revived block stays evictable", "oracle/prefix_cache.py",
+     "                self.evictable.remove(b)", "                pass"),
+    ("blocks of unknown tokens registered", "oracle/prefix_cache.py",
+     "            if None not in key and key not in self.block_of:",
+     "            if key not in self.block_of:"),
+    ("a later registration wins", "oracle/prefix_cache.py",
+     "            if None not in key and key not in self.block_of:", "            if None not in key:"),
 ]
 
 

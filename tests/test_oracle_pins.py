@@ -614,6 +614,24 @@ def test_prefix_cache_never_shares_blocks_of_different_prefixes():
     pc_check(bm, sh, ["a", "b"])
 
 
+def test_prefix_cache_never_registers_blocks_of_unknown_tokens():
+    """A block's K/V depends on its token ids. Where they are not known
+    (appends without ids) no later prompt can be shown to match, so the block
+    is never registered. Freed, it goes back to the free list, not the
+    evictable one, and a known block after it starts no chain."""
+    bs = 4
+    bm = PrefixCachingBlockManager(8, bs, range(8))
+    bm.add_seq(0)
+    for _ in range(2 * bs):
+        bm.append_slot(0)                                # two full blocks, ids unknown
+    for t in range(bs):
+        bm.append_token(0, t)                            # a third, ids known
+    assert bm.num_cached() == 0
+    bm.free_seq(0)
+    assert bm.num_evictable() == 0 and sorted(bm.free) == list(range(8))
+    assert bm.add_seq_prompt(1, list(range(3 * bs + 1))) == 0
+
+
 def test_prefix_cache_revives_freed_blocks_and_evicts_oldest_first():
     bs = 4
     bm = PrefixCachingBlockManager(8, bs, range(8))
