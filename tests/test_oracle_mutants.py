@@ -7,8 +7,9 @@ Each run must fail the pins. The mistakes cover head mapping, scales,
 softmax normalisation, causal positions, block and slot indexing, E4M3
 rounding, sign, NaN, bias, subnormals and scaling, and copy and swap
 direction. They also cover copy-on-write, fork counts, free-list order, beam
-parents, swap pairs and capacity, and prefix-cache keys, registration,
-revival and eviction order. A control run of the unchanged copy
+parents and their order against the frees, swap pairs and capacity, and
+prefix-cache keys, registration, revival, counters and eviction order. A
+control run of the unchanged copy
 must pass, so a broken set-up cannot pass for a caught mistake.
 """
 import concurrent.futures
@@ -95,6 +96,30 @@ MUTANTS = [
      "            if key not in self.block_of:"),
     ("a later registration wins", "oracle/prefix_cache.py",
      "            if None not in key and key not in self.block_of:", "            if None not in key:"),
+    ("decode length one short", "oracle/attention.py",
+     "        L = int(lens[b])\n        hk = h // G\n        K = widen_k",
+     "        L = int(lens[b]) - 1\n        hk = h // G\n        K = widen_k"),
+    ("chunk rows mapped to the next sequence", "oracle/attention.py",
+     "        seq_of[qs[b]:qs[b + 1]] = b", "        seq_of[qs[b]:qs[b + 1]] = min(b + 1, B - 1)"),
+    ("quantisation divides by the unrounded scale", "oracle/fp8_e4m3.py",
+     "    q = np.asarray(x, dtype=np.float32) / np.float32(scale)",
+     "    q = (np.asarray(x, dtype=np.float64) / float(scale)).astype(np.float32)"),
+    ("swap-in pairs reversed", "oracle/block_manager.py",
+     "        return list(zip(host, dev))", "        return list(zip(dev, host))"),
+    ("old beams freed before the forks", "oracle/block_manager.py",
+     "        for p, sid in zip(parents, new_ids):\n            self.fork(old_ids[int(p)], sid)\n"
+     "        for sid in old_ids:\n            self.free_seq(sid)",
+     "        keep = {s: (list(self.tables[s]), self.lens[s]) for s in old_ids}\n"
+     "        for sid in old_ids:\n            self.free_seq(sid)\n"
+     "        for p, sid in zip(parents, new_ids):\n"
+     "            t, n = keep[old_ids[int(p)]]\n"
+     "            self.tables[sid] = list(t)\n            self.lens[sid] = n\n"
+     "            for b in t:\n                self.ref[b] += 1"),
+    ("prefix lookups not counted", "oracle/prefix_cache.py", "            self.lookup_blocks += 1\n", ""),
+    ("prefix hits not counted", "oracle/prefix_cache.py", "            self.hit_blocks += 1\n", ""),
+    ("caching manager frees to the front", "oracle/prefix_cache.py",
+     "                else:\n                    self.free.append(b)",
+     "                else:\n                    self.free.insert(0, b)"),
 ]
 
 

@@ -277,6 +277,30 @@ def test_e4m3_quantize_divides_in_float32():
     assert np.array_equal(ofp8.e4m3_quantize(x, s), lib)
 
 
+def test_e4m3_quantize_rounds_the_scale_to_float32_like_torch():
+    """The kernel receives a float32 scale and divides in float32. Inputs a few
+    float32 steps from tie points, with a scale float32 cannot hold exactly
+    (0.1), tell that apart from dividing by the exact scale. Every code must
+    equal torch's float32 divide followed by its float8_e4m3fn cast."""
+    s = 0.1
+    s32 = torch.tensor(s, dtype=torch.float32)
+    mags = ofp8.e4m3_decode(np.arange(127, dtype=np.uint8))
+    ties = (mags[:-1] + mags[1:]) / 2
+    base = torch.from_numpy(ties[1:]).float() * s32                 # rounded to float32
+    xs = [base]
+    for _ in range(3):                                            # 3 steps either way
+        xs.append(torch.nextafter(xs[-1], torch.full_like(base, float("inf"))))
+    lo = base
+    for _ in range(3):
+        lo = torch.nextafter(lo, torch.full_like(base, float("-inf")))
+        xs.append(lo)
+    x = torch.cat(xs)
+    lib = (x / s32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ofp8.e4m3_quantize(x.numpy(), s), lib)
+    exact = ofp8.e4m3_encode((x.double().numpy() / s).astype(np.float32))
+    assert (exact != lib).sum() > 0          # the cases do tell the two apart
+
+
 def test_fp8_paged_attention_equals_sdpa_on_library_dequantised_values():
     q, kp, vp, tables, sl, conts = random_case(13, [40, 77], 8, 2, 64, 16)
     ks, vs = 4.5 / 448, 4.2 / 448
@@ -569,12 +593,14 @@ def test_prefix_cache_reuses_common_system_prompt_blocks():
     system = list(range(1000, 1100))                   # 100-token system prompt
     p1 = system + [1, 2, 3]
     assert bm.add_seq_prompt("a", p1) == 0             # nothing cached yet
+    assert (bm.hit_blocks, bm.lookup_blocks) == (0, 1)  # the first lookup misses: stop
     for t in p1:
         pc_append(bm, sh, "a", t)
     assert bm.num_cached() == 6                        # its 6 full blocks registered
     p2 = system + list(range(50, 80))
     n = bm.add_seq_prompt("b", p2)
     assert n == 96 and bm.hit_blocks == 6              # 6 full blocks of the common 100
+    assert bm.lookup_blocks == 1 + 7                   # 6 hits, then the miss that stops it
     for t in p2[n:]:
         pc_append(bm, sh, "b", t)
     assert bm.block_table("b")[:6] == bm.block_table("a")[:6]
@@ -626,9 +652,9 @@ def test_prefix_cache_never_registers_blocks_of_unknown_tokens():
         bm.append_slot(0)                                # two full blocks, ids unknown
     for t in range(bs):
         bm.append_token(0, t)                            # a third, ids known
-    assert bm.num_cached() == 0
-    bm.free_seq(0)
-    assert bm.num_evictable() == 0 and sorted(bm.free) == list(range(8))
+    assert bm.num_cached() == 0 and bm.block_table(0) == [0, 1, 2]
+    bm.free_seq(0)                                       # to the tail, in table order
+    assert bm.num_evictable() == 0 and bm.free == [3, 4, 5, 6, 7, 0, 1, 2]
     assert bm.add_seq_prompt(1, list(range(3 * bs + 1))) == 0
 
 
