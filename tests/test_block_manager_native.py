@@ -613,3 +613,33 @@ def test_batch_appends_are_all_or_nothing_against_oracle(seed, caching):
         if caching:
             assert nat.evictable_list() == ora.evictable
     assert refused > 0 and done > 0 and cows > 0
+
+
+def test_swap_in_takes_evictable_blocks_when_the_free_list_is_short():
+    """With prefix caching, cached blocks nobody holds count as available: a
+    swap-in with an empty free list evicts them (oldest first), as the oracle
+    does."""
+    library()
+    nat = BlockManager(6, 4, range(6), prefix_caching=True, num_host_blocks=4)
+    ora = PrefixCachingBlockManager(6, 4, list(range(6)), num_cpu_blocks=4)
+    prompt = list(range(12))                           # three full blocks, ids known
+    for m in (nat, ora):
+        assert m.add_seq_prompt(0, prompt) == 0
+    nat.append_tokens(0, prompt)
+    for t in prompt:
+        ora.append_token(0, t)
+    for m in (nat, ora):
+        m.add_seq(1)
+    nat.append_n(1, 8)
+    for _ in range(8):
+        ora.append_slot(1)
+    assert [tuple(p) for p in nat.swap_out(1)] == [tuple(p) for p in ora.swap_out(1)]
+    for m in (nat, ora):
+        m.free_seq(0)                                  # its three blocks become evictable
+        m.add_seq(2)
+    nat.append_n(2, 12)
+    for _ in range(12):
+        ora.append_slot(2)
+    assert nat.free_list() == ora.free == [] and len(ora.evictable) == 3
+    assert [tuple(p) for p in nat.swap_in(1)] == [tuple(p) for p in ora.swap_in(1)]
+    _same_state(nat, ora, [1, 2])
