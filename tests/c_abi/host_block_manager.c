@@ -77,5 +77,44 @@ int main(void) {
     /* an unknown sequence is an error, and the manager is unchanged */
     printf("unknown %d\n", bm_free_seq(bm, 99));
     bm_destroy(bm);
+
+    /* prefix caching and swapping on a second manager: a 9-token prompt is
+     * served, a second request reuses its two full blocks, then the first
+     * request is swapped out and back in */
+    const int32_t order2[8] = {0, 1, 2, 3, 4, 5, 6, 7};
+    pkv_block_manager* pc = bm_create(8, 4, order2, 8);
+    if (!pc) {
+        printf("error bm_create\n");
+        return 1;
+    }
+    check(bm_enable_prefix_caching(pc), "bm_enable_prefix_caching");
+    check(bm_set_host_blocks(pc, 4), "bm_set_host_blocks");
+    const int32_t prompt[9] = {5, 6, 7, 8, 9, 10, 11, 12, 13};
+    int cached = -1;
+    check(bm_add_seq_prompt(pc, 0, prompt, 9, &cached), "bm_add_seq_prompt");
+    int64_t pslots[9], ppairs[4];
+    int pcow = 0;
+    check(bm_append_tokens(pc, 0, prompt + cached, 9 - cached, pslots, ppairs, 2, &pcow),
+          "bm_append_tokens");
+    printf("prompt 0 cached %d", cached);
+    for (int i = 0; i < 9 - cached; ++i) printf(" %lld", (long long)pslots[i]);
+    printf("\n");
+    check(bm_add_seq_prompt(pc, 1, prompt, 9, &cached), "bm_add_seq_prompt");
+    printf("prompt 1 cached %d\n", cached);
+    int64_t hits = 0, looks = 0;
+    int ncached = 0, nev = 0;
+    check(bm_cache_stats(pc, &hits, &looks, &ncached, &nev), "bm_cache_stats");
+    printf("stats %lld %lld %d %d\n", (long long)hits, (long long)looks, ncached, nev);
+    int64_t sp[8];
+    int nsp = 0;
+    check(bm_swap_out(pc, 0, sp, 4, &nsp), "bm_swap_out");
+    printf("out");
+    for (int i = 0; i < nsp; ++i) printf(" %lld %lld", (long long)sp[2 * i], (long long)sp[2 * i + 1]);
+    printf("\n");
+    check(bm_swap_in(pc, 0, sp, 4, &nsp), "bm_swap_in");
+    printf("in");
+    for (int i = 0; i < nsp; ++i) printf(" %lld %lld", (long long)sp[2 * i], (long long)sp[2 * i + 1]);
+    printf("\n");
+    bm_destroy(pc);
     return 0;
 }

@@ -1,8 +1,10 @@
 """The C ABI from plain C: tests/c_abi/host_block_manager.c, compiled with the
 system C compiler against include/pagedkv.h and linked to the built library,
 drives the host block manager (appends, fork, copy-on-write, a beam step, a
-batch step, a refused chunk, frees) with no Python or torch in between. Its
-output must equal the oracle's manager on the same operations."""
+batch step, a refused chunk, frees), then a second manager with prefix caching
+and a host pool (a served prompt, a request reusing its blocks, cache
+statistics, a swap out and back in), with no Python or torch in between. Its
+output must equal the oracle's managers on the same operations."""
 import os
 import shutil
 import subprocess
@@ -11,6 +13,7 @@ import pytest
 
 from _lib import library
 from oracle.block_manager import BlockManager as OracleBM
+from oracle.prefix_cache import PrefixCachingBlockManager
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -45,6 +48,15 @@ def expected():
     nf, n2 = len(bm.free), bm.seq_len(2)
     out.append(f"refused -5 cow 0 len {n2} {n2} free {nf} {nf}")
     out.append("unknown -4")
+    pc = PrefixCachingBlockManager(8, 4, list(range(8)), num_cpu_blocks=4)
+    prompt = [5, 6, 7, 8, 9, 10, 11, 12, 13]
+    n = pc.add_seq_prompt(0, prompt)
+    slots = [pc.append_token(0, t)[0] for t in prompt[n:]]
+    out.append(" ".join(["prompt", "0", "cached", str(n)] + [str(x) for x in slots]))
+    out.append(f"prompt 1 cached {pc.add_seq_prompt(1, prompt)}")
+    out.append(f"stats {pc.hit_blocks} {pc.lookup_blocks} {pc.num_cached()} {pc.num_evictable()}")
+    out.append(" ".join(["out"] + [str(x) for p in pc.swap_out(0) for x in p]))
+    out.append(" ".join(["in"] + [str(x) for p in pc.swap_in(0) for x in p]))
     return out
 
 
