@@ -35,6 +35,7 @@
  *   - Data-dependent errors found on the device (a block id or slot outside the
  *     pool, a wait that gave up) never trap: the offending access is skipped and
  *     a sticky device error word is set; read it with pkv_get_device_error().
+ *     pkv_check_wait_timeout() exercises the timeout path without a fault.
  *
  * KV pool layout. The pages show one head as key_pool[block, slot, dim] and
  * say no more; here each pool is [num_blocks][num_kv_heads][tile], one
