@@ -1,8 +1,9 @@
 """The library's block manager against the oracle's under stateful random
 testing: hypothesis interleaves every operation (sequences added plain or from
 a prompt, single and batch appends, forks, frees, beam steps, swaps out and
-in), compares the whole state after each one, and shrinks a failing script to
-a short one. Prefix caching and the host pool are drawn per run.
+in), compares the whole state after each one, checks the prefix groups of
+random batches exactly, and shrinks a failing script to a short one. Prefix
+caching and the host pool are drawn per run.
 """
 import copy
 
@@ -14,6 +15,7 @@ from hypothesis import HealthCheck, settings, strategies as st  # noqa: E402
 from hypothesis.stateful import (RuleBasedStateMachine, initialize, invariant,  # noqa: E402
                                  precondition, rule)
 
+from _groups import assert_groups_exact  # noqa: E402
 from _lib import library, pkv  # noqa: E402
 from oracle.block_manager import BlockManager as OracleBM, PoolExhausted  # noqa: E402
 from oracle.prefix_cache import PrefixCachingBlockManager  # noqa: E402
@@ -147,6 +149,14 @@ class Managers(RuleBasedStateMachine):
             assert e.value.status == -5
             return
         assert [tuple(map(int, p)) for p in self.nat.swap_in(sid)] == [tuple(p) for p in exp]
+
+    @precondition(lambda self: self.resident())
+    @rule(data=st.data())
+    def prefix_groups(self, data):
+        ids = data.draw(st.lists(st.sampled_from(self.resident()), min_size=1, max_size=10,
+                                 unique=True))
+        maxm = data.draw(st.integers(1, 8))
+        assert_groups_exact(self.ora, ids, maxm, self.nat.prefix_groups(ids, maxm))
 
     # ---------------------------------------------------------------- state
     @invariant()
