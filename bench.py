@@ -187,10 +187,11 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle timing
-def _oracle_loop(p, inp, tables, lens, run_s, seed):
+def _oracle_loop(p, inp, tables, lens, run_s, seed, check=()):
     """The oracle over random (sequence, head) units for about run_s seconds, one
     thread; returns the finish time (s from the start) and algorithmic K/V bytes
-    of every unit."""
+    of every unit, and the output rows of the ``check`` units, which it computes
+    first (they count as timed units like the others)."""
     from oracle import attention as oatt
     from oracle import fp8_e4m3 as ofp8
     q, kp, vp, ks, vs = inp
@@ -201,28 +202,35 @@ def _oracle_loop(p, inp, tables, lens, run_s, seed):
     else:
         wk = wv = oatt.widen
     rng = np.random.default_rng(seed)
-    fin, nbytes = [], []
+    fin, nbytes, outs = [], [], {}
+    todo = [tuple(int(x) for x in u) for u in check]
     t0 = time.perf_counter()
     if p.get("mode") == "prefill":
         # units are (chunk token, head); the amount is the token's attention FLOPs
         qs = np.asarray(p["query_start"])
         seq_of = np.searchsorted(qs, np.arange(int(qs[-1])), side="right") - 1
-        while time.perf_counter() - t0 < run_s:
-            t, h = int(rng.integers(int(qs[-1]))), int(rng.integers(p["Hq"]))
-            oatt.paged_prefill(q, kp, vp, tables, lens, qs, p["scale"], p["bs"], units=[(t, h)])
+        while todo or time.perf_counter() - t0 < run_s:
+            t, h = todo.pop(0) if todo else (int(rng.integers(int(qs[-1]))),
+                                             int(rng.integers(p["Hq"])))
+            r = oatt.paged_prefill(q, kp, vp, tables, lens, qs, p["scale"], p["bs"],
+                                   units=[(t, h)])
             fin.append(time.perf_counter() - t0)
+            if len(outs) < len(check):
+                outs[(t, h)] = r[(t, h)]
             b = int(seq_of[t])
             pos = int(lens[b]) - int(qs[b + 1] - qs[b]) + (t - int(qs[b]))
             nbytes.append(4.0 * p["D"] * (pos + 1))
-        return np.array(fin), np.array(nbytes)
-    while time.perf_counter() - t0 < run_s:
-        b, h = int(rng.integers(p["B"])), int(rng.integers(p["Hq"]))
-        oatt.paged_decode(q, kp, vp, tables, lens, p["scale"], p["bs"], ks, vs, units=[(b, h)],
-                          widen_k=wk, widen_v=wv)
+        return np.array(fin), np.array(nbytes), outs
+    while todo or time.perf_counter() - t0 < run_s:
+        b, h = todo.pop(0) if todo else (int(rng.integers(p["B"])), int(rng.integers(p["Hq"])))
+        r = oatt.paged_decode(q, kp, vp, tables, lens, p["scale"], p["bs"], ks, vs,
+                              units=[(b, h)], widen_k=wk, widen_v=wv)
         fin.append(time.perf_counter() - t0)
+        if len(outs) < len(check):
+            outs[(b, h)] = r[(b, h)]
         # per (b, h) unit the oracle reads the sequence's K and V for one query head
         nbytes.append(int(lens[b]) * p["per_tok"] / p["Hkv"])
-    return np.array(fin), np.array(nbytes)
+    return np.array(fin), np.array(nbytes), outs
 
 
 def _oracle_worker(idx, spec, barrier, results):
@@ -238,18 +246,22 @@ def _oracle_worker(idx, spec, barrier, results):
         inp = (load("q"), load("k"), load("v"), spec["ks"], spec["vs"])
         barrier.wait(timeout=600)
         results.put((idx,) + _oracle_loop(spec["p"], inp, spec["tables"], spec["lens"],
-                                          spec["run_s"], 1000 + idx))
+                                          spec["run_s"], 1000 + idx, spec["check"][idx]))
     except Exception as e:           # reported to the parent, which then times in-process
         results.put((-1, repr(e)))
 
 
-def oracle_timing(w, inp, tables, lens, per_tok, slice_s, slices, cores=None, extra=None):
+def oracle_timing(w, inp, tables, lens, per_tok, slice_s, slices, cores=None, extra=None,
+                  check_units=()):
     """Times the unmodified oracle on the host cores: one spawned single-threaded
     process per core, all started together and run for ``slices * slice_s``
     seconds over random (sequence, head) units of the workload. Each unit counts
-    in the time slice it finishes in. Returns (GB/s of each slice, units of each
-    slice, cores used, note). Falls back to one in-process thread when the
-    processes cannot be set up (cores 1, the note says why)."""
+    in the time slice it finishes in. The ``check_units`` are computed first
+    (spread over the cores) and their output rows kept, so that the timed GPU
+    run can be compared with them. Returns (GB/s of each slice, units of each
+    slice, cores used, note, {check unit: oracle row}). Falls back to one
+    in-process thread when the processes cannot be set up (cores 1, the note
+    says why)."""
     import multiprocessing as mp
     import shutil
     import tempfile
@@ -263,7 +275,8 @@ def oracle_timing(w, inp, tables, lens, per_tok, slice_s, slices, cores=None, ex
         try:
             tmp = tempfile.mkdtemp(prefix=".oracle_timing_", dir=ROOT)
             spec = {"p": p, "tables": np.asarray(tables), "lens": np.asarray(lens),
-                    "ks": inp[3], "vs": inp[4], "run_s": run_s}
+                    "ks": inp[3], "vs": inp[4], "run_s": run_s,
+                    "check": [list(check_units)[i::cores] for i in range(cores)]}
             for name, t in (("q", inp[0]), ("k", inp[1]), ("v", inp[2])):
                 path = os.path.join(tmp, name)
                 t.contiguous().view(torch.uint8).reshape(-1).numpy().tofile(path)
@@ -294,17 +307,70 @@ def oracle_timing(w, inp, tables, lens, per_tok, slice_s, slices, cores=None, ex
         prev = torch.get_num_threads()
         torch.set_num_threads(1)
         try:
-            runs = [_oracle_loop(p, inp, tables, lens, run_s, 7)]
+            runs = [_oracle_loop(p, inp, tables, lens, run_s, 7, list(check_units))]
         finally:
             torch.set_num_threads(prev)
     fin = np.concatenate([r[0] for r in runs])
     nb = np.concatenate([r[1] for r in runs])
+    outs = {u: row for r in runs for u, row in r[2].items()}
     # the window ends when the last unit does (units started before run_s finish)
     width = max(run_s, float(fin.max()) if fin.size else run_s) / slices
     idx = np.minimum((fin / width).astype(np.int64), slices - 1)
     gbs = np.bincount(idx, weights=nb, minlength=slices) / width / 1e9
     units = np.bincount(idx, minlength=slices)
-    return gbs, units, cores, note
+    return gbs, units, cores, note, outs
+
+
+# Elementwise bound |gpu - oracle| <= atol + rtol |oracle| of the parity tests:
+# the stated max-abs 2e-2 / max-rel 2e-2 read per element (6e-2 with the E4M3
+# cache; float32 caches are held to 1e-5).
+CHECK_TOL = {"bf16": (2e-2, 2e-2), "e4m3": (6e-2, 6e-2), "f32": (1e-5, 1e-5)}
+
+
+def check_units_decode(w, n, seed=0):
+    """(sequence, query head) units for the run's self-check: the longest and
+    the shortest sequence, then seeded random ones."""
+    rng = np.random.default_rng(seed)
+    L = np.asarray(w.final_lens)
+    units = [(int(np.argmax(L)), 0), (int(np.argmin(L)), w.Hq - 1)]
+    while len(units) < min(n, w.B * w.Hq):
+        u = (int(rng.integers(w.B)), int(rng.integers(w.Hq)))
+        if u not in units:
+            units.append(u)
+    return units
+
+
+def check_units_prefill(T, Hq, query_start, n, seed=0):
+    """(chunk token, head) units: each sequence's first and last chunk token of
+    the first and last sequence, then seeded random ones."""
+    rng = np.random.default_rng(seed)
+    qs = np.asarray(query_start)
+    units = []
+    for b in (0, len(qs) - 2):
+        for u in ((int(qs[b]), 0), (int(qs[b + 1]) - 1, Hq - 1)):
+            if qs[b + 1] > qs[b] and u not in units:
+                units.append(u)
+    while len(units) < min(n, T * Hq):
+        u = (int(rng.integers(T)), int(rng.integers(Hq)))
+        if u not in units:
+            units.append(u)
+    return units
+
+
+def self_check(got, ref_rows, kv):
+    """The GPU rows of the timed run against the oracle rows the CPU baseline
+    computed: max abs error, max relative error over |oracle| > 1e-3, and whether
+    every element is inside the parity tests' bound."""
+    atol, rtol = CHECK_TOL[kv]
+    units = sorted(ref_rows)
+    g = np.stack([np.asarray(got[u[0], u[1]], dtype=np.float64) for u in units])
+    r = np.stack([ref_rows[u] for u in units])
+    err = np.abs(g - r)
+    big = np.abs(r) > 1e-3
+    return {"units": len(units), "max_abs_err": float(err.max()),
+            "max_rel_err": float((err[big] / np.abs(r[big])).max()) if big.any() else 0.0,
+            "atol": atol, "rtol": rtol,
+            "pass": bool(np.all(np.isfinite(g)) and np.all(err <= atol + rtol * np.abs(r)))}
 
 
 # ---------------------------------------------------------------- setup
@@ -322,6 +388,144 @@ def build_state(w, device):
     plan = cache.plan_step(w.step_seqs, max_blocks=w.max_blocks_per_seq)
     torch.cuda.synchronize()
     return cache, plan, (q, k_new, v_new, ks, vs), (k_src, v_src)
+
+
+def time_steps(cache, dev, qd, kd, vd, out, w, ks, vs, ws, K, stream, has_copy):
+    """K device-resident steps (copy_blocks when the step has CoW pairs,
+    reshape_and_cache, decode), back to back on ``stream``. Returns the whole
+    time (ms), each step's decode-op time (ms, CUDA events on the stream) and the
+    library's launches."""
+    import paged_kv_cache_259_gb300 as pkv
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = pkv.kernel_launches()
+    t_start.record(stream)
+    for i in range(K):
+        if has_copy:
+            pkv.copy_blocks(cache.k_pool, cache.v_pool, dev["pairs"], stream=stream)
+        pkv.reshape_and_cache(kd, vd, cache.k_pool, cache.v_pool, dev["slots"], ks, vs, stream=stream)
+        ev_dec[i][0].record(stream)
+        cache.decode(qd, dev, out, w.scale, ks, vs, ws, stream=stream)
+        ev_dec[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = pkv.kernel_launches() - launches0
+    return (t_start.elapsed_time(t_end), np.array([a.elapsed_time(b) for a, b in ev_dec]),
+            launches)
+
+
+def rewind(cache, w, max_blocks):
+    """A fresh block manager in the state after the measured step's appends: the
+    workload's script replayed, then that step planned (its K/V already sit in
+    the pools; the script's copies were applied when the cache was built)."""
+    import paged_kv_cache_259_gb300 as pkv
+    cache.bm = pkv.BlockManager(w.NB, w.bs, w.free_order)
+    cache.replay(w.script)
+    return cache.plan_step(w.step_seqs, max_blocks=max_blocks)
+
+
+def e2e_live_planning(cache, w, q, k_new, v_new, out, ks, vs, ws, stream, steps, warmup, world,
+                      nb):
+    """End to end through the public API, host planning included: every step the
+    native block manager appends one token to every sequence (``plan_step``:
+    ``append_slots``, ``build_tables``, ``prefix_groups``), the plan is written
+    into the pinned slab of ``engine.StepPipeline``, the slab (plan, q, k_new,
+    v_new) is uploaded, the step runs and its output is read back -- each step's
+    planning and copies overlapped with the neighbouring steps' device work.
+    Sequences grow by one token per step; when the pool's free blocks could run
+    out, the manager is rewound to the measured step's state between passes
+    (outside the timed passes). Returns ms per step, bytes per step (the
+    step's algorithmic bytes at its lengths), h2d/d2h bytes per step and the
+    median host planning time per step (us)."""
+    from paged_kv_cache_259_gb300.engine import StepPipeline
+    free = w.NB - int(sum(-(-int(L) // w.bs) for L in w.final_lens))
+    per_pass = max(1, min(steps, w.bs * (free // w.B)))
+    mb = w.max_blocks_per_seq + -(-per_pass // w.bs) + 1
+    plan0 = rewind(cache, w, mb)
+    host = plan0.host_tensors(pin=True)
+    if set(host) != {"slots", "pairs", "tables", "lens"} or host["pairs"].shape[0]:
+        raise RuntimeError("e2e with live planning needs steps without copies or groups")
+    host.update(q=q.pin_memory(), k_new=k_new.pin_memory(), v_new=v_new.pin_memory())
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    pipe = StepPipeline(cache, dict(host), out, stream=stream)
+    for i in range(2):
+        for k, view in pipe.host_inputs(i).items():
+            view.copy_(host[k])
+    ids = np.asarray(w.step_seqs, dtype=np.int64)
+    keys = ("slots", "pairs", "tables", "lens")
+
+    def one_step(plan_us):
+        t0 = time.perf_counter()
+        plan = cache.plan_step(ids, max_blocks=mb)
+        t1 = time.perf_counter()
+        views = pipe.host_inputs()
+        t2 = time.perf_counter()
+        ht = plan.host_tensors(pin=False)
+        if set(ht) != set(keys) or ht["pairs"].shape[0]:
+            raise RuntimeError("a live step raised copies or groups")
+        for k in keys:
+            views[k].copy_(ht[k])
+        plan_us.append(1e6 * ((t1 - t0) + (time.perf_counter() - t2)))
+        pipe.submit(hout, w.scale, ks, vs, ws)
+        return int(plan.lens.astype(np.int64).sum())
+
+    warm_us = []
+    for _ in range(min(warmup, per_pass)):
+        one_step(warm_us)
+    torch.cuda.synchronize()
+    base_tokens = int(plan0.lens.astype(np.int64).sum())
+    total_ms, total_bytes, done, plan_us = 0.0, 0.0, 0, []
+    while done < steps:
+        rewind(cache, w, mb)
+        n = min(per_pass, steps - done)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0.record(pipe.up)
+        for _ in range(n):
+            tokens = one_step(plan_us)
+            total_bytes += nb["total"] + (tokens - base_tokens) * nb["per_token"]
+        e1.record(pipe.down)
+        torch.cuda.synchronize()
+        total_ms += e0.elapsed_time(e1)
+        done += n
+    return {"ms": total_ms / steps, "bytes": total_bytes / steps, "h2d": pipe.slab_bytes,
+            "d2h": hout.numel() * hout.element_size(),
+            "host_plan_us": float(np.median(plan_us)), "steps": steps, "per_pass": per_pass}
+
+
+def e2e_replay(cache, plan, dev, q, k_new, v_new, out, w, ks, vs, ws, stream, steps, warmup,
+               world, nb):
+    """End to end for steps that copy blocks or decode by prefix groups: the
+    measured step's plan, written once into both pinned slabs of
+    ``engine.StepPipeline``, replayed every step (uploaded with q, k_new and
+    v_new, run, output read back, overlapped with the neighbouring steps)."""
+    from paged_kv_cache_259_gb300.engine import StepPipeline
+    host = plan.host_tensors(pin=True)
+    host.update(q=q.pin_memory(), k_new=k_new.pin_memory(), v_new=v_new.pin_memory())
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    templates = dict(host)
+    templates.update({k: v for k, v in dev.items() if not torch.is_tensor(v)})
+    pipe = StepPipeline(cache, templates, out, stream=stream)
+    for i in range(2):
+        for k, view in pipe.host_inputs(i).items():
+            view.copy_(host[k])
+    for _ in range(warmup):
+        pipe.submit(hout, w.scale, ks, vs, ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(pipe.up)
+    for _ in range(steps):
+        pipe.submit(hout, w.scale, ks, vs, ws)
+    e1.record(pipe.down)
+    torch.cuda.synchronize()
+    return {"ms": e0.elapsed_time(e1) / steps, "bytes": nb["total"], "h2d": pipe.slab_bytes,
+            "d2h": hout.numel() * hout.element_size(), "host_plan_us": None, "steps": steps,
+            "per_pass": None}
 
 
 def run_gpu(args, rank, world, device):
@@ -347,74 +551,87 @@ def run_gpu(args, rank, world, device):
 
     # ---- device-resident timing: whole step, plus the decode op alone per step
     K = args.steps
-    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(K)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(device.index if device.index is not None else 0)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    launches0 = pkv.kernel_launches()
-    t_start.record(stream)
-    for i in range(K):
-        if has_copy:
-            pkv.copy_blocks(cache.k_pool, cache.v_pool, dev["pairs"], stream=stream)
-        pkv.reshape_and_cache(kd, vd, cache.k_pool, cache.v_pool, dev["slots"], ks, vs, stream=stream)
-        ev_dec[i][0].record(stream)
-        cache.decode(qd, dev, out, w.scale, ks, vs, ws, stream=stream)
-        ev_dec[i][1].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    launches_timed = pkv.kernel_launches() - launches0
+    total_ms, dec_ms, launches_timed = time_steps(cache, dev, qd, kd, vd, out, w, ks, vs, ws, K,
+                                                  stream, has_copy)
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = t_start.elapsed_time(t_end)
-    dec_ms = np.array([a.elapsed_time(b) for a, b in ev_dec])
     if pkv.get_device_error() != 0:
         raise RuntimeError("device error in the timed region")
+    out_timed = out.float().cpu()                        # the timed steps' result (self-check)
     launches_per_step = count_launches(step)
 
-    # ---- end to end through the public API: every step's inputs copied in from
-    # pinned host memory and its output read back, through engine.StepPipeline
-    # (uploads on one stream, downloads on another, overlapped with the compute
-    # of the neighbouring steps)
-    from paged_kv_cache_259_gb300.engine import StepPipeline
-    host = plan.host_tensors(pin=True)
-    host.update(q=q.pin_memory(), k_new=k_new.pin_memory(), v_new=v_new.pin_memory())
-    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    templates = dict(host)
-    templates.update({k: v for k, v in dev.items() if not torch.is_tensor(v)})
-    pipe = StepPipeline(cache, templates, out, stream=stream)
-    for i in range(2):                                   # both slabs hold this step's inputs
-        for k, view in pipe.host_inputs(i).items():
-            view.copy_(host[k])
-    h2d = pipe.slab_bytes
-    d2h = hout.numel() * hout.element_size()
-    for _ in range(max(4, args.warmup // 4)):
-        pipe.submit(hout, w.scale, ks, vs, ws)
-    torch.cuda.synchronize()
-    K2 = max(4, K // 4)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    e0.record(pipe.up)
-    for _ in range(K2):
-        pipe.submit(hout, w.scale, ks, vs, ws)
-    e1.record(pipe.down)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / K2
+    # ---- end to end through the public API, host planning included
+    if not has_copy and plan.num_groups == 0:
+        e2e = e2e_live_planning(cache, w, q, k_new, v_new, out, ks, vs, ws, stream,
+                                max(50, K // 4), max(4, args.warmup // 4), world, nbytes)
+    else:
+        e2e = e2e_replay(cache, plan, dev, q, k_new, v_new, out, w, ks, vs, ws, stream,
+                         max(50, K // 4), max(4, args.warmup // 4), world, nbytes)
     if pkv.get_device_error() != 0:
         raise RuntimeError("device error in the end-to-end steps")
 
     res = {"w": w, "nbytes": nbytes, "ms_per_step": total_ms / K, "dec_ms": float(dec_ms.mean()),
-           "dec_ms_median": float(np.median(dec_ms)), "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
+           "dec_ms_median": float(np.median(dec_ms)), "e2e": e2e,
            "clocks": clk, "launches": launches_timed, "groups": plan.num_groups,
-           "launches_per_step": launches_per_step,
+           "launches_per_step": launches_per_step, "out": out_timed,
            "cpu": (q, k_src, v_src, ks, vs, plan)}
     return res
+
+
+OTHER_DECODE = ["gqa_chat_bf16", "shared_prefix_bf16", "shared_prefix_fork_bf16",
+                "long_fp8_bs16", "long_fp8_bs32", "beam_search_bf16"]
+
+
+def run_other(name, steps, warmup, device, peak):
+    """Another decode workload, timed like the headline's device-resident steps
+    (fewer of them), with its self-check: the GPU rows of the timed steps
+    against oracle rows computed on one host core (the check units of a
+    one-core oracle timing run with no time budget beyond them)."""
+    import paged_kv_cache_259_gb300 as pkv
+    w = wl.CONFIGS[name]()
+    cache, plan, (q, k_new, v_new, ks, vs), (k_src, v_src) = build_state(w, device)
+    stream = torch.cuda.current_stream(device)
+    dev = plan.device_tensors(device)
+    qd, kd, vd = q.to(device), k_new.to(device), v_new.to(device)
+    out = torch.empty(w.B, w.Hq, w.D, dtype=w.src_dtype, device=device)
+    ws = cache.workspace(w.B, w.max_blocks_per_seq)
+    nb = step_bytes(w, plan.tables, plan.lens, len(plan.pairs))
+    has_copy = len(plan.pairs) > 0
+    for _ in range(warmup):
+        cache.step(qd, kd, vd, dev, out, w.scale, ks, vs, ws)
+    torch.cuda.synchronize()
+    if pkv.get_device_error() != 0:
+        raise RuntimeError(f"{name}: device error during warm-up")
+    total_ms, dec_ms, _ = time_steps(cache, dev, qd, kd, vd, out, w, ks, vs, ws, steps, stream,
+                                     has_copy)
+    if pkv.get_device_error() != 0:
+        raise RuntimeError(f"{name}: device error in the timed region")
+    got = out.float().cpu()
+    groups = plan.num_groups
+    del cache, dev, qd, kd, vd, out, ws
+    torch.cuda.empty_cache()
+    kp, vp, tables, lens = oracle_inputs_for_step(w, q, k_src, v_src, plan)
+    n_check = 8 if w.kv_dtype == "e4m3" else 24
+    _, _, _, _, ref_rows = oracle_timing(w, (q, kp, vp, ks, vs), tables, lens, nb["per_token"],
+                                         0.0, 1, cores=1,
+                                         check_units=check_units_decode(w, n_check))
+    ms = total_ms / steps
+    dgbs = nb["decode"] / (float(dec_ms.mean()) * 1e-3) / 1e9
+    return {"workload": workload_desc(w), "kv": w.kv_dtype, "steps": steps,
+            "decode_gbs": round(dgbs, 2), "frac": round(dgbs / peak, 4),
+            "decode_ms": round(float(dec_ms.mean()), 5),
+            "decode_bytes": nb["decode"], "decode_logical_bytes": nb["decode_logical"],
+            "step_gbs": round(nb["total"] / (ms * 1e-3) / 1e9, 2), "ms_per_step": round(ms, 5),
+            "seq_steps_per_s": round(w.B / (ms * 1e-3), 1), "cow_pairs": int(len(plan.pairs)),
+            "prefix_groups": groups, "traffic": measured_traffic(name),
+            "check": self_check(got, ref_rows, w.kv_dtype)}
 
 
 def count_launches(step, reps=3):
@@ -606,6 +823,7 @@ def run_prefill(args, rank, world, device):
     if pkv.get_device_error() != 0:
         raise RuntimeError("device error in the timed region")
     att_ms = np.array([a.elapsed_time(b) for a, b in ev])
+    out_timed = out.float().cpu()                        # the timed steps' result (self-check)
     launches_per_step = count_launches(step)
 
     host = plan.host_tensors(pin=True)
@@ -641,7 +859,7 @@ def run_prefill(args, rank, world, device):
             "att_ms_median": float(np.median(att_ms)), "e2e_ms": e0.elapsed_time(e1) / K2,
             "h2d": h2d, "d2h": d2h, "clocks": clk, "launches": launches,
             "launches_per_step": launches_per_step, "pairs": int(plan.pairs.shape[0]),
-            "plan": plan, "plan_s": plan_s, "T": int(plan.chunks.sum()),
+            "plan": plan, "plan_s": plan_s, "T": int(plan.chunks.sum()), "out": out_timed,
             "cpu": (q, k_src, v_src, k_new, v_new)}
 
 
@@ -720,10 +938,22 @@ def prefill_main(args, rank, world, device):
     peak, kind = load_tensor_peak()
     if rank != 0:
         return
-    inp, tables, lens, qs = prefill_cpu_inputs(w, r["cpu"])
-    extra = {"mode": "prefill", "query_start": qs}
-    gf, units, cores, note = oracle_timing(w, inp, tables, lens, 0, args.cpu_budget, 1,
-                                           extra=extra)
+    cpu_line, check = None, None
+    if args.cpu_budget > 0:                           # <= 0: profiling runs skip the CPU leg
+        inp, tables, lens, qs = prefill_cpu_inputs(w, r["cpu"])
+        extra = {"mode": "prefill", "query_start": qs}
+        gf, units, cores, note, ref_rows = oracle_timing(
+            w, inp, tables, lens, 0, args.cpu_budget, 1, extra=extra,
+            check_units=check_units_prefill(r["T"], w.Hq, qs, 48))
+        cpu_line = {
+            "value": round(float(gf[0]) / 1e3, 6), "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{int(units[0])} random (chunk token, head) rows of this workload in "
+                      f"{args.cpu_budget:.1f} s on {cores} host cores (one single-threaded "
+                      f"float64 oracle process per core){note}"}
+        check = {**self_check(r["out"], ref_rows, "bf16"),
+                 "of": "the timed steps' output rows against the oracle rows of the "
+                       "cpu_baseline run (its first units)"}
     att_tf = fl / (att_ms * 1e-3) / 1e12
     line = {
         "metric": PREFILL_METRIC, "value": round(world * fl / (ms * 1e-3) / 1e12, 2),
@@ -753,19 +983,14 @@ def prefill_main(args, rank, world, device):
             "flops_per_launch": fl, "ms_per_launch": round(att_ms, 5),
             "ms_per_launch_median": round(r["att_ms_median"], 5),
         },
-        "cpu_baseline": {
-            "value": round(float(gf[0]) / 1e3, 6), "unit": "TFLOP/s", "cores": cores,
-            "kind": "oracle",
-            "sample": f"{int(units[0])} random (chunk token, head) rows of this workload in "
-                      f"{args.cpu_budget:.1f} s on {cores} host cores (one single-threaded "
-                      f"float64 oracle process per core){note}",
-        },
+        "cpu_baseline": cpu_line,
         "e2e": {"value": round(world * fl / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "ms_per_step": round(e2e_ms, 5),
                 "note": "engine.StepPipeline: each step's q/k/v and plan uploaded from one "
                         "pinned slab and its output read back inside the timed region, "
                         "overlapped with the neighbouring steps (bound by the host link)"},
+        "check": check,
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
@@ -785,9 +1010,9 @@ def run_reference_prefill(args):
         q, k_new, v_new = w.step_inputs()
         inp, tables, lens, qs = prefill_cpu_inputs(w, (q, k_src, v_src, k_new, v_new))
     slice_s = 120.0 / (args.steps + args.warmup)
-    gf, units, cores, note = oracle_timing(w, inp, tables, lens, 0, slice_s,
-                                           args.warmup + args.steps,
-                                           extra={"mode": "prefill", "query_start": qs})
+    gf, units, cores, note, _ = oracle_timing(w, inp, tables, lens, 0, slice_s,
+                                              args.warmup + args.steps,
+                                              extra={"mode": "prefill", "query_start": qs})
     value = float(gf[args.warmup:].mean()) / 1e3
     line = {
         "impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6),
@@ -1243,6 +1468,8 @@ def main():
                     help="override the workload's sequence count (profiling small cases)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle timing")
+    ap.add_argument("--no-others", dest="others", action="store_false",
+                    help="default workload only: skip timing the other decode workloads")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -1284,18 +1511,36 @@ def main():
     w, nb = r["w"], r["nbytes"]
     ms = max_over_ranks(r["ms_per_step"], world, device)
     dec_ms = max_over_ranks(r["dec_ms"], world, device)
-    e2e_ms = max_over_ranks(r["e2e_ms"], world, device)
+    e2e = r["e2e"]
+    e2e_ms = max_over_ranks(e2e["ms"], world, device)
     peak, peak_kind = load_peaks()
     value = world * nb["total"] / (ms * 1e-3) / 1e9
     dec_gbs = nb["decode"] / (dec_ms * 1e-3) / 1e9
+    others = {}
+    if world == 1 and args.others and args.config == DEFAULT_CONFIG and args.batch is None:
+        n_other = max(20, min(args.steps, 200))
+        for name in OTHER_DECODE:
+            others[name] = run_other(name, n_other, args.warmup, device, peak)
 
     line = None
     if rank == 0:
-        q, k_src, v_src, ks, vs, plan = r["cpu"]
-        kp, vp, tables, lens = oracle_inputs_for_step(w, q, k_src, v_src, plan)
-        gbs, units, cores, note = oracle_timing(w, (q, kp, vp, ks, vs), tables, lens,
-                                                nb["per_token"], args.cpu_budget, 1)
-        cpu_gbs, units, secs = float(gbs[0]), int(units[0]), args.cpu_budget
+        cpu_line, check = None, None
+        if args.cpu_budget > 0:                       # <= 0: profiling runs skip the CPU leg
+            q, k_src, v_src, ks, vs, plan = r["cpu"]
+            kp, vp, tables, lens = oracle_inputs_for_step(w, q, k_src, v_src, plan)
+            gbs, units, cores, note, ref_rows = oracle_timing(
+                w, (q, kp, vp, ks, vs), tables, lens, nb["per_token"], args.cpu_budget, 1,
+                check_units=check_units_decode(w, 48))
+            cpu_line = {
+                "value": round(float(gbs[0]), 4), "unit": "GB/s", "cores": cores,
+                "kind": "oracle",
+                "sample": f"{int(units[0])} random (sequence, head) units of this workload in "
+                          f"{args.cpu_budget:.1f} s on {cores} host cores (one single-threaded "
+                          f"float64 oracle process per core){note}"}
+            check = {**self_check(r["out"], ref_rows, w.kv_dtype),
+                     "of": "the timed steps' output rows against the oracle rows of the "
+                           "cpu_baseline run (its first units)"}
+        plan = r["cpu"][5]
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -1326,18 +1571,27 @@ def main():
                 "bytes_per_launch": nb["decode"], "ms_per_launch": round(dec_ms, 5),
                 "ms_per_launch_median": round(r["dec_ms_median"], 5),
             },
-            "cpu_baseline": {
-                "value": round(cpu_gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                "sample": f"{units} random (sequence, head) units of this workload in "
-                          f"{secs:.1f} s on {cores} host cores (one single-threaded float64 "
-                          f"oracle process per core){note}",
-            },
-            "e2e": {"value": round(world * nb["total"] / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                    "ms_per_step": round(e2e_ms, 5),
-                    "note": "engine.StepPipeline: each step's pinned inputs uploaded and output "
-                            "read back inside the timed region, overlapped with the "
-                            "neighbouring steps' compute (two device buffer sets)"},
+            "cpu_baseline": cpu_line,
+            "e2e": {
+                "value": round(world * e2e["bytes"] / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": round(e2e_ms, 5), "steps": e2e["steps"],
+                "host_plan_us_per_step": (None if e2e["host_plan_us"] is None
+                                          else round(e2e["host_plan_us"], 1)),
+                "note": ("public API with host planning: every step the native block manager "
+                         "appends a token to every sequence (append_slots, build_tables, "
+                         "prefix_groups), the plan goes into a pinned slab of "
+                         "engine.StepPipeline, the slab (plan, q, k, v) is uploaded, the step "
+                         "runs and its output is read back, overlapped with the neighbouring "
+                         "steps; sequences grow by one token per step (bytes counted at each "
+                         "step's lengths), the manager rewound every %d steps outside the "
+                         "timed passes" % e2e["per_pass"]) if e2e["per_pass"] else
+                        ("engine.StepPipeline replaying the measured step's plan (it copies "
+                         "blocks or decodes by prefix groups): each step's pinned inputs "
+                         "uploaded and output read back inside the timed region, overlapped "
+                         "with the neighbouring steps' compute")},
+            "check": check,
+            **({"others": others} if others else {}),
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
         }
@@ -1358,8 +1612,8 @@ def run_reference(args):
     kp, vp, tables, lens = oracle_inputs_for_step(w, q, k_src, v_src, None)
     per_tok = 2 * w.Hkv * w.D * KV_ELT[w.kv_dtype]
     slice_s = 120.0 / (args.steps + args.warmup)       # whole run within ~2 minutes
-    gbs, units, cores, note = oracle_timing(w, (q, kp, vp, ks, vs), tables, lens, per_tok,
-                                            slice_s, args.warmup + args.steps)
+    gbs, units, cores, note, _ = oracle_timing(w, (q, kp, vp, ks, vs), tables, lens, per_tok,
+                                               slice_s, args.warmup + args.steps)
     value = float(gbs[args.warmup:].mean())
     units_done = int(units[args.warmup:].sum())
     line = {

@@ -36,6 +36,10 @@
  *     pool, a wait that gave up) never trap: the offending access is skipped and
  *     a sticky device error word is set; read it with pkv_get_device_error().
  *     pkv_check_wait_timeout() exercises the timeout path without a fault.
+ *   - Per-device state (the error word's address, each kernel's shared-memory
+ *     set-up, the address of paged_attention_decode_noalloc's scratch) is
+ *     looked up once per device and kept for the process: do not use the
+ *     library across a cudaDeviceReset of a device it has run on.
  *
  * KV pool layout. The pages show one head as key_pool[block, slot, dim] and
  * say no more; here each pool is [num_blocks][num_kv_heads][tile], one
@@ -238,7 +242,11 @@ PKV_API int reshape_and_cache(const void* k, const void* v, void* k_pool, void* 
  *                 multiple of 16
  * Preconditions (met by the block manager, whose dst is always a block it has
  * just taken from the free list): dst values are distinct and no dst is also a
- * src; otherwise the result is unspecified. A pair with an id outside
+ * src (of any pair, its own included); otherwise which bytes land is
+ * unspecified. A launch of at most 4096 pairs checks this on the device (one
+ * read of every pair per pair, while the copies' loads are in flight) and sets
+ * PKV_ERR_INVALID_ARG in the device error word on a violation; the copies still
+ * run, in bounds. Larger launches are not checked. A pair with an id outside
  * [0, num_blocks) is skipped and sets PKV_ERR_OUT_OF_RANGE on the device.
  * ---------------------------------------------------------------------- */
 PKV_API int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs,
@@ -323,10 +331,13 @@ PKV_API int swap_blocks(void* dst_k_pool, void* dst_v_pool, const void* src_k_po
  * split-KV scratch is a fixed array inside the library of
  * PKV_NOALLOC_WORKSPACE_BYTES per GPU, held by every GPU that loads the
  * library until the process exits. Nothing is allocated by the call.
- *   - Limit: num_seqs * num_heads * 2 * (head_dim + 2) * 4 bytes (the smallest
- *     split) must not exceed PKV_NOALLOC_WORKSPACE_BYTES, else the call returns
- *     PKV_ERR_INVALID_ARG and launches nothing. Within it the split is chosen
- *     to fit the array.
+ *   - Limit: when the batch can be split at all (that is, when
+ *     paged_attention_workspace_size(num_seqs, num_heads, head_dim, block_size,
+ *     max_blocks_per_seq) > 0), num_seqs * num_heads * 2 * (head_dim + 2) * 4
+ *     bytes (the smallest split) must not exceed PKV_NOALLOC_WORKSPACE_BYTES,
+ *     else the call returns PKV_ERR_INVALID_ARG and launches nothing. A batch
+ *     that can never be split uses no scratch and has no limit here. Within
+ *     the limit the split is chosen to fit the array.
  *   - The first call on a device looks up the array's device address on that
  *     device (once); make that first call before any stream capture.
  *   - All calls on a device share the array: calls that overlap on the GPU
@@ -348,7 +359,9 @@ PKV_API unsigned long long pkv_kernel_launches(void);
 
 /* Synchronise `stream`, then return (in *code) and clear the device error word
  * of the current device: PKV_OK if no kernel recorded an error since the last
- * read, else PKV_ERR_TIMEOUT if a device wait gave up, else PKV_ERR_OUT_OF_RANGE.
+ * read, else PKV_ERR_TIMEOUT if a device wait gave up, else PKV_ERR_OUT_OF_RANGE
+ * if an id, slot or length was out of range, else PKV_ERR_INVALID_ARG
+ * (copy_blocks pairs that break its preconditions).
  * The word is shared by every stream of the device. Once a wait has timed out,
  * every later wait on the device gives up at once until the word is cleared.
  * Returns PKV_OK or PKV_ERR_CUDA. */

@@ -353,12 +353,14 @@ def paged_attention_decode_noalloc(out, q, k_pool, v_pool, block_tables, seq_len
     a fixed 32 MiB array inside the library (per GPU), so no workspace is passed
     and nothing is allocated. Calls on one device share that array and must not
     overlap on the GPU; the first call on a device should come before any stream
-    capture. Refuses batches with ``B * Hq * 2 * (D + 2) * 4 > NOALLOC_WORKSPACE_BYTES``.
+    capture. A batch that can be split (``paged_attention_workspace_size`` > 0)
+    is refused when ``B * Hq * 2 * (D + 2) * 4 > NOALLOC_WORKSPACE_BYTES``.
     """
     lib = load_library()
     B, Hq, D, NB, Hkv, bs = _decode_shapes(out, q, k_pool, v_pool, block_tables, seq_lens)
     need = B * Hq * 2 * (D + 2) * 4
-    if need > NOALLOC_WORKSPACE_BYTES:
+    splittable = lib.paged_attention_workspace_size(B, Hq, D, bs, block_tables.shape[1]) > 0
+    if splittable and need > NOALLOC_WORKSPACE_BYTES:
         raise PagedKVError(-1, f"paged_attention_decode_noalloc: batch needs {need} bytes of "
                                f"scratch, the fixed array holds {NOALLOC_WORKSPACE_BYTES}")
     dev = _on_gpu(((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
@@ -439,7 +441,11 @@ def reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, k_scale=1.0, v_scale=1
 
 
 def copy_blocks(k_pool, v_pool, src_dst_pairs, stream=None):
-    """``pool[dst] = pool[src]`` for each row of int64 ``src_dst_pairs [P, 2]``."""
+    """``pool[dst] = pool[src]`` for each row of int64 ``src_dst_pairs [P, 2]``.
+
+    Destinations must be distinct and none may also be a source; a launch of at
+    most 4096 pairs checks this on the device and reports a violation as
+    ``PKV_ERR_INVALID_ARG`` through ``get_device_error``."""
     lib = load_library()
     named = ((k_pool, "k_pool"), (v_pool, "v_pool"), (src_dst_pairs, "src_dst_pairs"))
     _tensors(named)

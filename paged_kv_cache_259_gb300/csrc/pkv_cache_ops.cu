@@ -207,10 +207,19 @@ __global__ void __launch_bounds__(256) reshape_and_cache_bf16_windows(
 
 constexpr int kCopyThreads = 256;
 constexpr int kCopyChunkBytes = kCopyThreads * 16 * 4;    // 16 KB per CTA
+// Launches of at most this many pairs check copy_blocks' preconditions on the
+// device (each pair's first CTA scans every pair once: P^2 pair reads in L2).
+constexpr int kCopyCheckPairs = 4096;
 
+// One CTA per (pair, pool, 16 KB chunk), 16-byte vector copies. The first CTA
+// of each pair (K pool, first chunk) also checks the launch's preconditions for
+// that pair while its loads are in flight: its destination is no other pair's
+// destination and no pair's source (its own included). A violation sets
+// kErrBadPairs; the copies still run (in bounds; which bytes land is then
+// unspecified).
 __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
     char* __restrict__ k_pool, char* __restrict__ v_pool, const int64_t* __restrict__ pairs,
-    int num_blocks, size_t block_bytes, int* err) {
+    int num_pairs, int num_blocks, size_t block_bytes, int* err) {
     const int pair = blockIdx.x >> 1;
     char* pool = (blockIdx.x & 1) ? v_pool : k_pool;
     const int64_t src = pairs[2 * pair], dst = pairs[2 * pair + 1];
@@ -229,6 +238,14 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
     for (int u = 0; u < 4; ++u) {
         const size_t i = beg + threadIdx.x + (size_t)u * kCopyThreads;
         if (i < end) buf[u] = s[i];
+    }
+    if (blockIdx.y == 0 && !(blockIdx.x & 1) && num_pairs <= kCopyCheckPairs) {
+        bool bad = false;
+        for (int j = threadIdx.x; j < num_pairs; j += kCopyThreads) {
+            const int64_t sj = pairs[2 * j], dj = pairs[2 * j + 1];
+            bad |= sj == dst || (j != pair && dj == dst);
+        }
+        if (__syncthreads_or(bad) && threadIdx.x == 0) flag_error(err, kErrBadPairs);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -391,8 +408,8 @@ int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs, int nu
     dim3 grid(2u * (unsigned)num_pairs, chunks);
     note_launch();
     copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<char*>(k_pool), static_cast<char*>(v_pool), src_dst_pairs, num_blocks,
-        block_bytes, err);
+        static_cast<char*>(k_pool), static_cast<char*>(v_pool), src_dst_pairs, num_pairs,
+        num_blocks, block_bytes, err);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_fail("copy_blocks: kernel launch", e);
 }

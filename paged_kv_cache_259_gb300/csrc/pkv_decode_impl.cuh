@@ -820,11 +820,13 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
     }
     if (aborted) {
         // give up: record it, and let the copies already issued land before the
-        // shared memory is reused or released
+        // shared memory is reused or released. These waits have a bound of their
+        // own and ignore the error word: the timeout bit set above (or by another
+        // CTA) must not cut them short while a copy may still be landing.
         if (lane == 0) flag_error(p.err, kErrTimeout);
         const int last = min(nk, k + ST);
         for (int kk = k; kk < last; ++kk)
-            (void)mbar_wait_bounded(smem_addr(&bars[w * ST + (kk % ST)]), (kk / ST) & 1, p.err);
+            (void)mbar_wait_bounded(smem_addr(&bars[w * ST + (kk % ST)]), (kk / ST) & 1, nullptr);
     }
 
     __syncthreads();                                        // every warp is done with its ring

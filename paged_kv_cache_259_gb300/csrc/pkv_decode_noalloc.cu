@@ -14,7 +14,10 @@
 // Every GPU that loads the library holds it until the process exits. In host
 // code its name is only a host-side stand-in, so its device address is looked up
 // once per device (cudaGetSymbolAddress with that device current) by the first
-// call made on that device; make that first call before any stream capture. All
+// call made on that device; make that first call before any stream capture.
+// The address is kept for the life of the process, so the library must not be
+// used across a cudaDeviceReset of that device (its error word and per-kernel
+// set-up are cached the same way). All
 // calls on a device share the one array, so calls that overlap on the GPU (on
 // different streams, or from different threads) race on it: serialise them. The
 // array keeps the last call's contents; nothing in it needs to start at zero,
@@ -54,9 +57,13 @@ extern "C" int paged_attention_decode_noalloc(
     const int32_t* block_tables, const int32_t* seq_lens, int num_seqs, int max_blocks_per_seq,
     int num_blocks, int num_heads, int num_kv_heads, int head_dim, int block_size, float scale,
     int q_dtype, int kv_dtype, float k_scale, float v_scale, void* stream) {
-    // The smallest split (two partitions per sequence and head) must fit, or the
-    // call is refused: such a batch is beyond what the fixed scratch serves.
-    if (num_seqs > 0 && num_heads > 0 && head_dim > 0) {
+    // A batch that can be split (some sequence may span more than one minimal
+    // partition) needs the smallest split -- two partitions per sequence and
+    // head -- to fit, or the call is refused: such a batch is beyond what the
+    // fixed scratch serves. A batch that can never be split uses no scratch.
+    if (num_seqs > 0 && num_heads > 0 && head_dim > 0 &&
+        paged_attention_workspace_size(num_seqs, num_heads, head_dim, block_size,
+                                       max_blocks_per_seq) > 0) {
         const size_t need =
             (size_t)num_seqs * num_heads * 2 * ((size_t)head_dim + 2) * sizeof(float);
         if (need > (size_t)PKV_NOALLOC_WORKSPACE_BYTES) return PKV_ERR_INVALID_ARG;

@@ -46,6 +46,7 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
 // Bits of the device error word (pkv_get_device_error maps them to a status).
 constexpr int kErrOutOfRange = 1;
 constexpr int kErrTimeout = 2;
+constexpr int kErrBadPairs = 4;      // copy_blocks: a destination repeated or also a source
 
 __device__ __forceinline__ void flag_error(int* err, int bit) {
     if (err) atomicOr(err, bit);

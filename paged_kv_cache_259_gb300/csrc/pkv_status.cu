@@ -135,7 +135,8 @@ int pkv_get_device_error(int* code, void* stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return pkv::cuda_fail("pkv_get_device_error", e);
     *code = (host & pkv::kErrTimeout) ? PKV_ERR_TIMEOUT
-            : (host & pkv::kErrOutOfRange) ? PKV_ERR_OUT_OF_RANGE : PKV_OK;
+            : (host & pkv::kErrOutOfRange) ? PKV_ERR_OUT_OF_RANGE
+            : (host & pkv::kErrBadPairs) ? PKV_ERR_INVALID_ARG : PKV_OK;
     return PKV_OK;
 }
 

@@ -161,3 +161,16 @@ def test_host_runs_cover_the_ids_in_order():
         ids = rng.permutation(40)[:int(rng.integers(0, 40))]
         rebuilt = [h + i for a, b, h in host_runs(ids) for i in range(b - a)]
         assert rebuilt == list(ids)
+
+
+def test_noalloc_refuses_a_splittable_batch_beyond_its_scratch():
+    """65535 sequences x 64 heads x 2 partitions x 130 floats is far above the
+    fixed 32 MiB scratch: with 9 blocks per sequence (the batch may be split)
+    the call is refused on the host before any pointer is used or anything is
+    launched; the GPU is never touched."""
+    lib = library()
+    st = lib.paged_attention_decode_noalloc(None, None, None, None, None, None, 65535, 9, 64, 64,
+                                            8, 128, 16, 0.1, 1, 1, 1.0, 1.0, None)
+    assert st == -1
+    assert lib.paged_attention_workspace_size(65535, 64, 128, 16, 9) > 0
+

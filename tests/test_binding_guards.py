@@ -149,3 +149,34 @@ def test_copy_blocks_refuses_malformed_arguments(over, exc):
     a.update(over)
     with pytest.raises(exc):
         pkv.copy_blocks(**a)
+
+
+def _noalloc_batch(max_blocks):
+    """1024 sequences x 32 heads, D 128: the smallest split (2 partitions of
+    130 floats per sequence and head) needs 34 MB, more than the fixed scratch."""
+    b, hq, hkv, d, bs = 1024, 32, 8, 128, 16
+    ks, vs = pkv.pool_shapes(4, hkv, bs, d, torch.bfloat16)
+    return dict(out=torch.empty(b, hq, d, dtype=torch.bfloat16),
+                q=torch.empty(b, hq, d, dtype=torch.bfloat16),
+                k_pool=torch.empty(ks, dtype=torch.bfloat16),
+                v_pool=torch.empty(vs, dtype=torch.bfloat16),
+                block_tables=torch.zeros(b, max_blocks, dtype=torch.int32),
+                seq_lens=torch.zeros(b, dtype=torch.int32), scale=0.125)
+
+
+def test_noalloc_wrapper_refuses_a_splittable_batch_beyond_its_scratch():
+    a = _noalloc_batch(max_blocks=9)                # may span two 8-block partitions
+    assert 1024 * 32 * 2 * 130 * 4 > pkv.NOALLOC_WORKSPACE_BYTES
+    assert pkv.paged_attention_workspace_size(1024, 32, 128, 16, 9) > 0
+    with pytest.raises(pkv.PagedKVError) as e:
+        pkv.paged_attention_decode_noalloc(**a)
+    assert e.value.status == -1 and "scratch" in str(e.value)
+
+
+def test_noalloc_wrapper_lets_an_unsplittable_batch_through_the_size_check():
+    """With at most 8 blocks per sequence the batch is never split and needs no
+    scratch: the size check passes and the next check (CPU tensors) refuses."""
+    a = _noalloc_batch(max_blocks=8)
+    assert pkv.paged_attention_workspace_size(1024, 32, 128, 16, 8) == 0
+    with pytest.raises(TypeError, match="CUDA tensor"):
+        pkv.paged_attention_decode_noalloc(**a)

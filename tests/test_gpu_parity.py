@@ -262,6 +262,27 @@ def test_copy_blocks_bad_pair_sets_error_word():
     assert torch.equal(kp[2], k0[1]) and torch.equal(kp[0], k0[0])
 
 
+@pytest.mark.parametrize("pairs", [[[0, 2], [1, 2]],          # a destination written twice
+                                   [[0, 2], [2, 3]],          # a destination also read
+                                   [[1, 1]]],                 # a block copied onto itself
+                         ids=["dst_twice", "dst_is_src", "self_copy"])
+def test_copy_blocks_conflicting_pairs_set_error_word(pairs):
+    """copy_blocks' preconditions (distinct destinations, none also a source) are
+    checked on the device: a launch that breaks them reports PKV_ERR_INVALID_ARG
+    through the device error word. Every id is inside the pool, so the copies
+    stay in bounds; only which bytes land is unspecified."""
+    ks, vs = pkv.pool_shapes(4, 2, 16, 64, torch.bfloat16)
+    kp = torch.randn(ks, device="cuda").to(torch.bfloat16)
+    vp = torch.randn(vs, device="cuda").to(torch.bfloat16)
+    assert pkv.get_device_error() == 0
+    pkv.copy_blocks(kp, vp, torch.tensor(pairs, dtype=torch.int64, device="cuda"))
+    assert pkv.get_device_error() == -1
+    # a valid launch right after leaves the word clear
+    pkv.copy_blocks(kp, vp, torch.tensor([[0, 2], [0, 3]], dtype=torch.int64, device="cuda"))
+    assert pkv.get_device_error() == 0
+    assert torch.equal(kp[2], kp[0]) and torch.equal(vp[3], vp[0])
+
+
 def test_host_checks_reject_bad_arguments():
     q, kp, vp, bt, _, _ = _decode_args(2, 4, 4, 96, 16, 8, 4)       # head_dim 96 not built
     lens = torch.tensor([3, 4], dtype=torch.int32, device="cuda")

@@ -255,3 +255,137 @@ def test_prefill_through_step_pipeline_matches_serial_steps():
         outs[mode] = res
     for a, b in zip(outs["serial"], outs["pipelined"]):
         assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------ running-max moves
+# The kernel keeps a running row max m and moves it (rescaling O in tensor
+# memory and the row sum by 2^(m_old - m_new)) only when a 128-key tile's max of
+# the scaled log2 scores exceeds m by more than 8; otherwise it exponentiates
+# against the old max. With N(0, 1) inputs a later tile almost never beats the
+# first by 8, so these cases build keys whose size grows tile by tile along the
+# query's direction: K[pos] = a(tile of pos) * u + noise, q = +/-u + noise with u
+# a +/-1 vector per KV head. Query heads with +u see their scores rise from tile
+# to tile (the move is taken, often on consecutive tiles and on diagonal tiles
+# where the row sees a single key), heads with -u see them fall (never taken),
+# so most warps mix rows that move with rows that do not.
+RISE_LEVEL_STEPS = (0.75, 0.2, 0.75, 0.75, -0.3)   # a(tile) walks by these, in turn
+KEY_TILE = 128
+MOVE_LOG2 = 8.0
+
+
+def _positions_to_slots(w):
+    """(sequence, position) -> pool slot of every token cached before the step,
+    from the oracle's block manager replaying the workload's script."""
+    bm = OracleBM(w.NB, w.bs, w.free_order)
+    for op in w.script:
+        if op[0] == "add":
+            bm.add_seq(op[1])
+        else:
+            for _ in range(op[2]):
+                bm.append_slot(op[1])
+    return {b: [bm.block_table(b)[t // w.bs] * w.bs + t % w.bs for t in range(bm.seq_len(b))]
+            for b in w.step_seqs}
+
+
+def rising_case(name, seed, context, chunks, Hq, Hkv, bs):
+    w = wl.chunked_prefill(name, seed, context, chunks, Hq, Hkv, 128, bs)
+    c = Case(w)
+    rng = np.random.default_rng(seed)
+    G = Hq // Hkv
+    u = torch.from_numpy(rng.choice([-1.0, 1.0], size=(Hkv, w.D)))
+    sign = torch.from_numpy(np.where(np.arange(Hq) % 3 == 2, -1.0, 1.0))   # 1 head in 3 falls
+    n_tiles = int(max(w.final_lens)) // KEY_TILE + 1
+    steps = [RISE_LEVEL_STEPS[j % len(RISE_LEVEL_STEPS)] for j in range(n_tiles - 1)]
+    level = np.concatenate([[0.0], np.cumsum(steps)])
+    level = torch.from_numpy(level)
+
+    def keys(noise, pos):                     # noise [n, Hkv, D], pos [n]
+        a = level[torch.as_tensor(pos) // KEY_TILE].view(-1, 1, 1)
+        return (a * u.unsqueeze(0) + 0.25 * noise.double()).to(torch.bfloat16)
+
+    # cached context tokens, in the pool at the slots the script gives them
+    slots = _positions_to_slots(w)
+    for b in w.step_seqs:
+        sl = torch.tensor(slots[b], dtype=torch.int64)
+        if len(sl) == 0:
+            continue
+        blk, off = sl // w.bs, sl % w.bs
+        c.k_src[blk, :, off] = keys(c.k_src[blk, :, off], np.arange(len(sl)))
+    # the chunk tokens (written by the step), then the queries
+    pos = np.concatenate([np.arange(cx, cx + n) for cx, n in zip(context, chunks)])
+    c.k_new = keys(c.k_new, pos)
+    qdir = (sign.view(1, Hq, 1) * u[torch.arange(Hq) // G].unsqueeze(0))
+    c.q = (qdir + 0.25 * c.q.double()).to(torch.bfloat16)
+    return c
+
+
+def running_max_moves(c, o):
+    """Per query row (token, head): how many tiles move the running max, and how
+    many of those moves happen on a tile where the row sees at most 2 keys --
+    the kernel's rule replayed in float64 on the stored bf16 values (a move is
+    counted only with a margin of 0.05 over the threshold, so float32 rounding in
+    the kernel cannot undo it)."""
+    w = c.w
+    G = w.Hq // w.Hkv
+    sc = w.scale * np.log2(np.e)
+    qs = w.query_start
+    moves = np.zeros((w.T, w.Hq), dtype=np.int64)
+    sparse_moves = 0
+    for b in range(w.B):
+        L, C = int(o["lens"][b]), int(qs[b + 1] - qs[b])
+        for hk in range(w.Hkv):
+            K = oatt.widen(oatt.gather(o["k_pool"], o["tables"][b], L, hk, w.bs)).reshape(L, w.D)
+            for h in range(hk * G, (hk + 1) * G):
+                Q = c.q[qs[b]:qs[b + 1], h].to(torch.float64).numpy()
+                S = (Q @ K.T) * sc                                   # [C, L]
+                for i in range(C):
+                    p = L - C + i
+                    m = None
+                    for j in range(p // KEY_TILE + 1):
+                        seen = S[i, j * KEY_TILE:min(p + 1, (j + 1) * KEY_TILE)]
+                        mt = seen.max()
+                        if m is None:
+                            m = mt
+                        elif mt > m + MOVE_LOG2 + 0.05:
+                            moves[qs[b] + i, h] += 1
+                            sparse_moves += len(seen) <= 2
+                            m = mt
+    return moves, sparse_moves
+
+
+RISING = [  # (name, Hq, Hkv, bs, context, chunks)
+    ("small_mha_bs16", 8, 8, 16, [0, 300], [420, 90]),
+    ("mid_mha_bs32", 8, 8, 32, [0, 700, 333], [520, 300, 250]),
+    ("mid_gqa4_bs16", 16, 4, 16, [0, 450, 1000], [400, 333, 129]),
+    ("mid_gqa8_bs32", 16, 2, 32, [5, 640], [260, 384]),
+]
+
+
+@pytest.mark.parametrize("name,Hq,Hkv,bs,context,chunks", RISING, ids=[r[0] for r in RISING])
+def test_prefill_running_max_moves_every_row(name, Hq, Hkv, bs, context, chunks):
+    """Inputs whose tile maxima rise by more than 8 log2 units (shown on the CPU
+    from the stored values) take the kernel's O-rescale branch on most rows;
+    every output row still equals the oracle's."""
+    c = rising_case(f"rising_{name}", 91 + Hq + bs, context, chunks, Hq, Hkv, bs)
+    w = c.w
+    g = run_gpu(c)
+    assert g["err"] == 0
+    G = Hq // Hkv
+    seq_of = np.repeat(np.arange(w.B), w.chunks)
+    units = sorted(((t, h) for t in range(w.T) for h in range(w.Hq)),
+                   key=lambda th: (seq_of[th[0]], th[1] // G, th[0], th[1]))
+    o = run_oracle(c, units=units)
+    check_indexing_and_writes(g, o)
+    # the input forces moves of the running max
+    moves, sparse = running_max_moves(c, o)
+    rising = np.arange(w.Hq) % 3 != 2
+    long_rows = np.array([[L - C + i >= KEY_TILE for h in range(w.Hq)]
+                          for b, (L, C) in enumerate(zip(o["lens"], w.chunks))
+                          for i in range(int(C))])
+    assert (moves[:, rising][long_rows[:, rising]] >= 1).mean() > 0.9
+    assert (moves >= 2).any()                          # moves on more than one tile
+    assert not moves[:, ~rising].any()
+    assert sparse > 0
+    got = g["out"].numpy()
+    ref = np.stack([o["out"][(t, h)] for t in range(w.T) for h in range(w.Hq)]).reshape(got.shape)
+    assert_close(got, ref, "bf16", name)
