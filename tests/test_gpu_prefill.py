@@ -205,7 +205,7 @@ def test_prefill_full_size_sampled(config):
     g = run_gpu(c)
     assert g["err"] == 0
     assert torch.isfinite(g["out"]).all()
-    units = sample_rows(w, 48)
+    units = sample_rows(w, 512)
     o = run_oracle(c, units=units)
     got = np.stack([g["out"][t, h].numpy() for t, h in units])
     ref = np.stack([o["out"][u] for u in units])
