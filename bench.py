@@ -427,54 +427,52 @@ def rewind(cache, w, max_blocks):
 
 def e2e_live_planning(cache, w, q, k_new, v_new, out, ks, vs, ws, stream, steps, warmup, world,
                       nb):
-    """End to end through the public API, host planning included: every step the
-    native block manager appends one token to every sequence (``plan_step``:
-    ``append_slots``, ``build_tables``, ``prefix_groups``), the plan is written
-    into the pinned slab of ``engine.StepPipeline``, the slab (plan, q, k_new,
-    v_new) is uploaded, the step runs and its output is read back -- each step's
-    planning and copies overlapped with the neighbouring steps' device work.
-    Sequences grow by one token per step; when the pool's free blocks could run
-    out, the manager is rewound to the measured step's state between passes
-    (outside the timed passes). Returns ms per step, bytes per step (the
-    step's algorithmic bytes at its lengths), h2d/d2h bytes per step and the
-    median host planning time per step (us)."""
-    from paged_kv_cache_259_gb300.engine import StepPipeline
+    """End to end through the public API, host planning included
+    (``engine.LiveDecodePipeline``): every step the native block manager
+    appends one token to every sequence (slots and copy-on-write pairs), builds
+    the tables and finds the prefix groups straight into a pinned slab; the slab
+    (plan, q, k_new, v_new) is uploaded, the step runs with that step's counts
+    and its output is read back -- each step's planning and copies overlapped
+    with the neighbouring steps' device work. Sequences grow by one token per
+    step; the manager is rewound to the measured step's state between passes
+    (outside the timed passes), and a pass ends early when the pool has no room
+    for a further step. Returns ms per step, bytes per step (each step's
+    algorithmic bytes at its lengths), h2d/d2h bytes per step, the median host
+    planning time per step (us) and the pass length."""
+    from paged_kv_cache_259_gb300 import PKV_ERR_POOL_EXHAUSTED, PagedKVError
+    from paged_kv_cache_259_gb300.engine import LiveDecodePipeline
     free = w.NB - int(sum(-(-int(L) // w.bs) for L in w.final_lens))
-    per_pass = max(1, min(steps, w.bs * (free // w.B)))
+    per_pass = max(1, min(steps, w.bs * max(1, free // w.B)))
     mb = w.max_blocks_per_seq + -(-per_pass // w.bs) + 1
     plan0 = rewind(cache, w, mb)
-    host = plan0.host_tensors(pin=True)
-    if set(host) != {"slots", "pairs", "tables", "lens"} or host["pairs"].shape[0]:
-        raise RuntimeError("e2e with live planning needs steps without copies or groups")
-    host.update(q=q.pin_memory(), k_new=k_new.pin_memory(), v_new=v_new.pin_memory())
+    hq, hk, hv = q.pin_memory(), k_new.pin_memory(), v_new.pin_memory()
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    pipe = StepPipeline(cache, dict(host), out, stream=stream)
+    pipe = LiveDecodePipeline(cache, w.step_seqs, hq, hk, hv, out, mb, stream=stream)
     for i in range(2):
-        for k, view in pipe.host_inputs(i).items():
-            view.copy_(host[k])
-    ids = np.asarray(w.step_seqs, dtype=np.int64)
-    keys = ("slots", "pairs", "tables", "lens")
+        v = pipe.host_inputs(i)
+        v["q"].copy_(hq)
+        v["k_new"].copy_(hk)
+        v["v_new"].copy_(hv)
+    base_tokens = int(plan0.lens.astype(np.int64).sum())
 
     def one_step(plan_us):
-        t0 = time.perf_counter()
-        plan = cache.plan_step(ids, max_blocks=mb)
+        pipe.host_inputs()                 # wait for the slab outside the planning time
         t1 = time.perf_counter()
-        views = pipe.host_inputs()
-        t2 = time.perf_counter()
-        ht = plan.host_tensors(pin=False)
-        if set(ht) != set(keys) or ht["pairs"].shape[0]:
-            raise RuntimeError("a live step raised copies or groups")
-        for k in keys:
-            views[k].copy_(ht[k])
-        plan_us.append(1e6 * ((t1 - t0) + (time.perf_counter() - t2)))
+        try:
+            pipe.plan()
+        except PagedKVError as e:
+            if e.status != PKV_ERR_POOL_EXHAUSTED:
+                raise
+            return None                    # no room for another step in this pass
+        plan_us.append(1e6 * (time.perf_counter() - t1))
         pipe.submit(hout, w.scale, ks, vs, ws)
-        return int(plan.lens.astype(np.int64).sum())
+        return pipe.last_lens_sum
 
     warm_us = []
     for _ in range(min(warmup, per_pass)):
-        one_step(warm_us)
+        if one_step(warm_us) is None:
+            break
     torch.cuda.synchronize()
-    base_tokens = int(plan0.lens.astype(np.int64).sum())
     total_ms, total_bytes, done, plan_us = 0.0, 0.0, 0, []
     while done < steps:
         rewind(cache, w, mb)
@@ -484,48 +482,22 @@ def e2e_live_planning(cache, w, q, k_new, v_new, out, ks, vs, ws, stream, steps,
             torch.distributed.barrier()
         torch.cuda.synchronize()
         e0.record(pipe.up)
+        k = 0
         for _ in range(n):
             tokens = one_step(plan_us)
+            if tokens is None:
+                break
             total_bytes += nb["total"] + (tokens - base_tokens) * nb["per_token"]
+            k += 1
         e1.record(pipe.down)
         torch.cuda.synchronize()
+        if k == 0:
+            raise RuntimeError("e2e: the pool has no room for a single further step")
         total_ms += e0.elapsed_time(e1)
-        done += n
-    return {"ms": total_ms / steps, "bytes": total_bytes / steps, "h2d": pipe.slab_bytes,
+        done += k
+    return {"ms": total_ms / done, "bytes": total_bytes / done, "h2d": pipe.slab_bytes,
             "d2h": hout.numel() * hout.element_size(),
-            "host_plan_us": float(np.median(plan_us)), "steps": steps, "per_pass": per_pass}
-
-
-def e2e_replay(cache, plan, dev, q, k_new, v_new, out, w, ks, vs, ws, stream, steps, warmup,
-               world, nb):
-    """End to end for steps that copy blocks or decode by prefix groups: the
-    measured step's plan, written once into both pinned slabs of
-    ``engine.StepPipeline``, replayed every step (uploaded with q, k_new and
-    v_new, run, output read back, overlapped with the neighbouring steps)."""
-    from paged_kv_cache_259_gb300.engine import StepPipeline
-    host = plan.host_tensors(pin=True)
-    host.update(q=q.pin_memory(), k_new=k_new.pin_memory(), v_new=v_new.pin_memory())
-    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    templates = dict(host)
-    templates.update({k: v for k, v in dev.items() if not torch.is_tensor(v)})
-    pipe = StepPipeline(cache, templates, out, stream=stream)
-    for i in range(2):
-        for k, view in pipe.host_inputs(i).items():
-            view.copy_(host[k])
-    for _ in range(warmup):
-        pipe.submit(hout, w.scale, ks, vs, ws)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    e0.record(pipe.up)
-    for _ in range(steps):
-        pipe.submit(hout, w.scale, ks, vs, ws)
-    e1.record(pipe.down)
-    torch.cuda.synchronize()
-    return {"ms": e0.elapsed_time(e1) / steps, "bytes": nb["total"], "h2d": pipe.slab_bytes,
-            "d2h": hout.numel() * hout.element_size(), "host_plan_us": None, "steps": steps,
-            "per_pass": None}
+            "host_plan_us": float(np.median(plan_us)), "steps": done, "per_pass": per_pass}
 
 
 def run_gpu(args, rank, world, device):
@@ -568,12 +540,8 @@ def run_gpu(args, rank, world, device):
     launches_per_step = count_launches(step)
 
     # ---- end to end through the public API, host planning included
-    if not has_copy and plan.num_groups == 0:
-        e2e = e2e_live_planning(cache, w, q, k_new, v_new, out, ks, vs, ws, stream,
-                                max(50, K // 4), max(4, args.warmup // 4), world, nbytes)
-    else:
-        e2e = e2e_replay(cache, plan, dev, q, k_new, v_new, out, w, ks, vs, ws, stream,
-                         max(50, K // 4), max(4, args.warmup // 4), world, nbytes)
+    e2e = e2e_live_planning(cache, w, q, k_new, v_new, out, ks, vs, ws, stream,
+                            max(50, K // 4), max(4, args.warmup // 4), world, nbytes)
     if pkv.get_device_error() != 0:
         raise RuntimeError("device error in the end-to-end steps")
 
@@ -1576,20 +1544,15 @@ def main():
                 "value": round(world * e2e["bytes"] / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e_ms, 5), "steps": e2e["steps"],
-                "host_plan_us_per_step": (None if e2e["host_plan_us"] is None
-                                          else round(e2e["host_plan_us"], 1)),
-                "note": ("public API with host planning: every step the native block manager "
-                         "appends a token to every sequence (append_slots, build_tables, "
-                         "prefix_groups), the plan goes into a pinned slab of "
-                         "engine.StepPipeline, the slab (plan, q, k, v) is uploaded, the step "
-                         "runs and its output is read back, overlapped with the neighbouring "
+                "host_plan_us_per_step": round(e2e["host_plan_us"], 1),
+                "note": ("public API with host planning (engine.LiveDecodePipeline): every "
+                         "step the native block manager appends a token to every sequence, "
+                         "builds the tables and finds the prefix groups straight into a "
+                         "pinned slab; the slab (plan, q, k, v) is uploaded, the step runs "
+                         "and its output is read back, overlapped with the neighbouring "
                          "steps; sequences grow by one token per step (bytes counted at each "
                          "step's lengths), the manager rewound every %d steps outside the "
-                         "timed passes" % e2e["per_pass"]) if e2e["per_pass"] else
-                        ("engine.StepPipeline replaying the measured step's plan (it copies "
-                         "blocks or decodes by prefix groups): each step's pinned inputs "
-                         "uploaded and output read back inside the timed region, overlapped "
-                         "with the neighbouring steps' compute")},
+                         "timed passes" % e2e["per_pass"])},
             "check": check,
             **({"others": others} if others else {}),
             "gpu_launches": r["launches"],

@@ -26,6 +26,8 @@ __all__ = [
     "paged_attention_decode_noalloc", "NOALLOC_WORKSPACE_BYTES", "paged_attention_decode_grouped",
     "paged_attention_prefill", "swap_blocks",
     "reshape_and_cache", "copy_blocks", "get_device_error", "check_wait_timeout",
+    "BoundCall", "bind_paged_attention_decode", "bind_paged_attention_decode_grouped",
+    "bind_reshape_and_cache", "bind_copy_blocks",
     "kernel_launches", "BlockManager",
     "library_path", "load_library", "pool_shapes", "pool_views", "pools_from_views", "PKV_F32",
     "PKV_BF16", "PKV_E4M3", "PKV_ERR_POOL_EXHAUSTED",
@@ -282,19 +284,25 @@ def paged_attention_decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale
     ``[B, max_blocks]``; seq_lens int32 ``[B]``; workspace: any CUDA tensor used
     as split-KV scratch (see ``paged_attention_workspace_size``) or None.
     """
+    bind_paged_attention_decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale, k_scale,
+                                v_scale, workspace)(stream)
+    return out
+
+
+def bind_paged_attention_decode(out, q, k_pool, v_pool, block_tables, seq_lens, scale,
+                                k_scale=1.0, v_scale=1.0, workspace=None):
+    """``paged_attention_decode`` checked once and bound to these tensors
+    (``BoundCall``): calling the result launches it on a stream."""
     lib = load_library()
     B, Hq, D, NB, Hkv, bs = _decode_shapes(out, q, k_pool, v_pool, block_tables, seq_lens)
     dev = _on_gpu(((out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
                    (block_tables, "block_tables"), (seq_lens, "seq_lens")))
     ws_ptr, ws_bytes = _workspace(workspace, dev)
-    with _on_device(dev):
-        st = lib.paged_attention_decode(
-            out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
-            block_tables.data_ptr(), seq_lens.data_ptr(), B, block_tables.shape[1], NB,
-            Hq, Hkv, D, bs, float(scale), _dt(q, "q"), _dt(k_pool, "k_pool"),
-            float(k_scale), float(v_scale), ws_ptr, ws_bytes, _stream_ptr(stream, dev))
-    _check(st, "paged_attention_decode")
-    return out
+    args = [_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens)]
+    args += _c_args([B, block_tables.shape[1], NB, Hq, Hkv, D, bs, float(scale), _dt(q, "q"),
+                     _dt(k_pool, "k_pool"), float(k_scale), float(v_scale)])
+    args += [ctypes.c_void_p(ws_ptr), ctypes.c_size_t(ws_bytes)]
+    return BoundCall(lib.paged_attention_decode, args, "paged_attention_decode", dev)
 
 
 def paged_attention_decode_grouped(out, q, k_pool, v_pool, block_tables, seq_lens, scale,
@@ -309,6 +317,21 @@ def paged_attention_decode_grouped(out, q, k_pool, v_pool, block_tables, seq_len
     int32 ``[n]`` batch indices in no group (None: every sequence is launched);
     max_group_blocks: the largest of ``prefix_groups``' list blocks (0: unknown).
     """
+    bind_paged_attention_decode_grouped(
+        out, q, k_pool, v_pool, block_tables, seq_lens, scale, seq_group, group_members,
+        group_prefix_blocks, k_scale, v_scale, workspace, ungrouped, max_group_blocks)(stream)
+    return out
+
+
+def bind_paged_attention_decode_grouped(out, q, k_pool, v_pool, block_tables, seq_lens, scale,
+                                        seq_group, group_members, group_prefix_blocks,
+                                        k_scale=1.0, v_scale=1.0, workspace=None,
+                                        ungrouped=None, max_group_blocks=0):
+    """``paged_attention_decode_grouped`` checked once and bound to these
+    tensors (``BoundCall``). ``group_members``, ``group_prefix_blocks`` and
+    ``ungrouped`` may be sized for the most groups and ungrouped sequences a
+    step can have: each call may then pass ``num_groups``, ``num_ungrouped`` and
+    ``max_group_blocks`` for the rows actually filled."""
     lib = load_library()
     B, Hq, D, NB, Hkv, bs = _decode_shapes(out, q, k_pool, v_pool, block_tables, seq_lens)
     groups = [(seq_group, "seq_group"), (group_members, "group_members"),
@@ -327,18 +350,18 @@ def paged_attention_decode_grouped(out, q, k_pool, v_pool, block_tables, seq_len
     dev = _on_gpu([(out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
                    (block_tables, "block_tables"), (seq_lens, "seq_lens")] + groups)
     ws_ptr, ws_bytes = _workspace(workspace, dev)
-    with _on_device(dev):
-        st = lib.paged_attention_decode_grouped(
-            out.data_ptr(), q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
-            block_tables.data_ptr(), seq_lens.data_ptr(), B, block_tables.shape[1], NB,
-            Hq, Hkv, D, bs, float(scale), _dt(q, "q"), _dt(k_pool, "k_pool"), float(k_scale),
-            float(v_scale), seq_group.data_ptr(), group_members.data_ptr(),
-            group_prefix_blocks.data_ptr(), group_members.shape[0], group_members.shape[1],
-            int(max_group_blocks), None if ungrouped is None else ungrouped.data_ptr(),
-            -1 if ungrouped is None else ungrouped.numel(),
-            ws_ptr, ws_bytes, _stream_ptr(stream, dev))
-    _check(st, "paged_attention_decode_grouped")
-    return out
+    G, n_un = group_members.shape[0], -1 if ungrouped is None else ungrouped.numel()
+    args = [_ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens)]
+    args += _c_args([B, block_tables.shape[1], NB, Hq, Hkv, D, bs, float(scale), _dt(q, "q"),
+                     _dt(k_pool, "k_pool"), float(k_scale), float(v_scale)])
+    args += [_ptr(seq_group), _ptr(group_members), _ptr(group_prefix_blocks)]
+    args += _c_args([G, group_members.shape[1], int(max_group_blocks)])
+    args += [_ptr(ungrouped), ctypes.c_int(n_un), ctypes.c_void_p(ws_ptr), ctypes.c_size_t(ws_bytes)]
+    counts = {"num_groups": (21, G), "max_group_blocks": (23, 2 ** 31 - 1)}
+    if ungrouped is not None:
+        counts["num_ungrouped"] = (25, n_un)
+    return BoundCall(lib.paged_attention_decode_grouped, args, "paged_attention_decode_grouped",
+                     dev, counts)
 
 
 # scratch bytes of paged_attention_decode_noalloc (PKV_NOALLOC_WORKSPACE_BYTES)
@@ -417,6 +440,11 @@ def paged_attention_prefill(out, q, k_pool, v_pool, block_tables, seq_lens, quer
 def reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, k_scale=1.0, v_scale=1.0, stream=None):
     """Write k/v ``[T, Hkv, D]`` into the pools (library layout) at ``slot_mapping``
     (int64 ``[T]``)."""
+    bind_reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, k_scale, v_scale)(stream)
+
+
+def bind_reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, k_scale=1.0, v_scale=1.0):
+    """``reshape_and_cache`` checked once and bound to these tensors (``BoundCall``)."""
     lib = load_library()
     named = ((k, "k"), (v, "v"), (k_pool, "k_pool"), (v_pool, "v_pool"),
              (slot_mapping, "slot_mapping"))
@@ -432,12 +460,74 @@ def reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, k_scale=1.0, v_scale=1
         raise ValueError("inconsistent shapes: k and v [T, Hkv, D] like the pools, "
                          "slot_mapping [T]")
     dev = _on_gpu(named)
-    with _on_device(dev):
-        st = lib.reshape_and_cache(
-            k.data_ptr(), v.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr(),
-            slot_mapping.data_ptr(), T, Hkv, D, bs, NB, _dt(k, "k"), _dt(k_pool, "k_pool"),
-            float(k_scale), float(v_scale), _stream_ptr(stream, dev))
-    _check(st, "reshape_and_cache")
+    args = [_ptr(k), _ptr(v), _ptr(k_pool), _ptr(v_pool), _ptr(slot_mapping)]
+    args += _c_args([T, Hkv, D, bs, NB, _dt(k, "k"), _dt(k_pool, "k_pool"), float(k_scale),
+                     float(v_scale)])
+    return BoundCall(lib.reshape_and_cache, args, "reshape_and_cache", dev)
+
+
+class BoundCall:
+    """One library call whose tensors, shapes and sizes were checked once, as the
+    plain call checks them, with its arguments kept as C values: calling it
+    launches on the given stream (default: the current stream of its device).
+    Count arguments named at binding time (``counts``: name -> (argument index,
+    largest allowed value)) may be given anew per call, e.g. the number of
+    copy-on-write pairs held in a buffer sized for the most a step can raise.
+    The tensors must stay alive and in place while the bound call is used."""
+
+    __slots__ = ("_fn", "_args", "_what", "_idx", "_stream", "_sptr", "_counts")
+
+    def __init__(self, fn, args, what, device, counts=None):
+        self._fn = fn
+        self._args = list(args)
+        self._what = what
+        self._idx = device.index if device.index is not None else torch.cuda.current_device()
+        self._stream = None
+        self._sptr = None
+        self._counts = counts or {}
+
+    def __call__(self, stream=None, **counts):
+        if stream is None:
+            stream = torch.cuda.current_stream(self._idx)
+        if stream is not self._stream:
+            self._stream, self._sptr = stream, ctypes.c_void_p(stream.cuda_stream)
+        args = self._args
+        if counts:
+            args = list(args)
+            for name, v in counts.items():
+                i, top = self._counts[name]
+                if not 0 <= int(v) <= top:
+                    raise ValueError(f"{self._what}: {name}={v} outside [0, {top}]")
+                args[i] = type(args[i])(int(v))
+        if torch.cuda.current_device() != self._idx:
+            with _on_device(torch.device("cuda", self._idx)):
+                st = self._fn(*args, self._sptr)
+        else:
+            st = self._fn(*args, self._sptr)
+        _check(st, self._what)
+
+
+def _c_args(values):
+    """C values of a call's arguments: pointers (ints from data_ptr or None)
+    as void*, ints as int, floats as float; ``size_t`` values wrapped by the
+    caller."""
+    out = []
+    for v in values:
+        if isinstance(v, (ctypes.c_size_t, ctypes.c_void_p)):
+            out.append(v)
+        elif isinstance(v, bool):
+            out.append(ctypes.c_int(int(v)))
+        elif isinstance(v, int):
+            out.append(ctypes.c_int(v))
+        elif isinstance(v, float):
+            out.append(ctypes.c_float(v))
+        else:
+            raise TypeError(f"unexpected argument {v!r}")
+    return out
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(None)
 
 
 def copy_blocks(k_pool, v_pool, src_dst_pairs, stream=None):
@@ -446,6 +536,13 @@ def copy_blocks(k_pool, v_pool, src_dst_pairs, stream=None):
     Destinations must be distinct and none may also be a source; a launch of at
     most 4096 pairs checks this on the device and reports a violation as
     ``PKV_ERR_INVALID_ARG`` through ``get_device_error``."""
+    bind_copy_blocks(k_pool, v_pool, src_dst_pairs)(stream)
+
+
+def bind_copy_blocks(k_pool, v_pool, src_dst_pairs):
+    """``copy_blocks`` checked once and bound to these tensors (``BoundCall``);
+    ``src_dst_pairs`` may be sized for the most pairs a step can raise, each call
+    passing ``num_pairs`` for the rows filled."""
     lib = load_library()
     named = ((k_pool, "k_pool"), (v_pool, "v_pool"), (src_dst_pairs, "src_dst_pairs"))
     _tensors(named)
@@ -456,11 +553,10 @@ def copy_blocks(k_pool, v_pool, src_dst_pairs, stream=None):
         raise ValueError("src_dst_pairs must be int64 [P, 2]; pools of one shape and dtype")
     dev = _on_gpu(named)
     block_bytes = k_pool[0].numel() * k_pool.element_size()
-    with _on_device(dev):
-        st = lib.copy_blocks(k_pool.data_ptr(), v_pool.data_ptr(), src_dst_pairs.data_ptr(),
-                             src_dst_pairs.shape[0], k_pool.shape[0], block_bytes,
-                             _stream_ptr(stream, dev))
-    _check(st, "copy_blocks")
+    P = src_dst_pairs.shape[0]
+    args = [_ptr(k_pool), _ptr(v_pool), _ptr(src_dst_pairs), ctypes.c_int(P),
+            ctypes.c_int(k_pool.shape[0]), ctypes.c_size_t(block_bytes)]
+    return BoundCall(lib.copy_blocks, args, "copy_blocks", dev, {"num_pairs": (3, P)})
 
 
 def swap_blocks(dst_k_pool, dst_v_pool, src_k_pool, src_v_pool, src_dst_pairs, stream=None):
@@ -582,6 +678,30 @@ class BlockManager:
         _check(self._lib.bm_append_slots(self._h, _i64p(ids), len(ids), _i64p(slots),
                                          _i64p(pairs), ctypes.byref(cnt)), "bm_append_slots")
         return slots, pairs[:cnt.value].copy()
+
+    def plan_decode_into(self, ids_p, n, max_blocks, slots_p, pairs_p, tables_p, lens_p,
+                         groups=None):
+        """The host half of a decode step written straight into caller buffers
+        given as ctypes pointers (e.g. views of a pinned upload slab), with no
+        array allocated: one append per listed sequence (``slots_p`` int64 [n],
+        ``pairs_p`` int64 [n, 2]: the copy-on-write pairs), dense ``tables_p``
+        int32 [n, max_blocks] and ``lens_p`` int32 [n], and, with ``groups =
+        (max_members, members_p, prefix_p, seq_group_p, blocks_p)`` (int32 [n,
+        max_members], [n], [n], [n]), the prefix groups. Returns (number of
+        pairs, number of groups). The appends are all or nothing, as in
+        ``append_slots``: PKV_ERR_POOL_EXHAUSTED leaves the manager unchanged."""
+        cnt = ctypes.c_int(0)
+        _check(self._lib.bm_append_slots(self._h, ids_p, n, slots_p, pairs_p, ctypes.byref(cnt)),
+               "bm_append_slots")
+        _check(self._lib.bm_build_tables(self._h, ids_p, n, max_blocks, tables_p, lens_p),
+               "bm_build_tables")
+        ng = ctypes.c_int(0)
+        if groups is not None:
+            mm, members_p, prefix_p, seq_group_p, blocks_p = groups
+            _check(self._lib.bm_prefix_groups(self._h, ids_p, n, mm, members_p, prefix_p,
+                                              seq_group_p, blocks_p, ctypes.byref(ng)),
+                   "bm_prefix_groups")
+        return cnt.value, ng.value
 
     def fork(self, parent, child):
         _check(self._lib.bm_fork(self._h, parent, child), "bm_fork")

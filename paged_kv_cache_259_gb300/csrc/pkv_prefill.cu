@@ -13,31 +13,35 @@
 //
 // One CTA = one tile of 128 query rows (128/G chunk tokens x the G query heads
 // of one KV head, so each K/V tile feeds every head that shares it) of one
-// sequence. Warp roles:
-// * warps 0-3 (softmax): thread r owns row r = TMEM lane r. Puts its q row in
-//   TMEM, then per KV tile reads its 128 scores, applies the causal mask, keeps
-//   the running max / sum (exp2 domain, scale * log2 e folded in), writes P
-//   (bf16) into its own TMEM columns, and finally normalises O;
-// * warp 4 (S issuer): one thread issues S = Q K^T (A = Q from TMEM, B = the K
-//   tile in shared memory, M = N = 128) as soon as an S buffer is free, and owns
-//   the TMEM allocation; warp 7 (P.V issuer): one thread issues O += P V (A = P
-//   from TMEM, B = the V tile, K = 16 keys per instruction) as soon as P is
-//   ready. The two streams touch disjoint operands (Q, K -> S; P, V -> O), so
-//   neither waits behind the other's issue;
+// sequence; two CTAs share an SM (half its tensor memory, registers and shared
+// memory each), so one CTA's set-up and epilogue overlap the other's tiles and
+// the tensor cores alternate between two independent score pipelines. Warp
+// roles:
+// * warps 0-3 (softmax, one warpgroup with most of the registers): thread r
+//   owns row r = TMEM lane r. Puts its q row into shared memory, then per KV
+//   tile reads its 128 scores, applies the causal mask, keeps the running max /
+//   sum (exp2 domain, scale * log2 e folded in), writes P (bf16) over the
+//   scores it has just read, and finally normalises O;
+// * warp 4 (S issuer): one thread issues S = Q K^T (A = Q, B = the K tile, both
+//   in shared memory, M = N = 128) once the K tile has landed and the previous
+//   tile's P.V has consumed P, and owns the TMEM allocation; warp 7 (P.V
+//   issuer): one thread issues O += P V (A = P from TMEM, B = the V tile, K = 16
+//   keys per instruction) once P is written;
 // * warps 5 and 6 (loaders, K and V): copy each tile of 128 keys block by block
 //   (through the block table) with 1-D bulk copies, lane i copying block i of
-//   the tile; K and V run through separate rings, so K of a tile is refilled as
-//   soon as its scores are computed and V once P.V has used it. The cache stores every
+//   the tile, into one K and one V buffer: K of the next tile as soon as S is
+//   computed, V of the next tile as soon as P.V is done. The cache stores every
 //   (block, head) tile as 128-byte core matrices, K [bs/8][D/8][8][8] and V
 //   [bs/8][D/8][8][8] (8 dims x 8 tokens), which is the canonical no-swizzle
 //   K-major operand layout, so a tile lands ready for the tensor cores (S with
-//   N = 128 keys over 8 blocks, P.V with K = 16 keys per instruction). Keys
-//   past the sequence in its last, partly written block get zero V values.
-// S is double-buffered in TMEM and a buffer is handed back as soon as the
-// softmax has read it, so the scores of tile j+2 are computed while the softmax
-// works on tile j+1, ahead of P.V of tile j; K/V tiles run through 3-stage rings.
-// The running max is only moved (and O rescaled) when a tile's max exceeds it by
-// more than 2^8, so O is rarely touched; the result is the same softmax.
+//   N = 128 keys over 8 blocks, P.V with K = 16 keys per instruction); the q
+//   rows are written in the same layout. Keys past the sequence in its last,
+//   partly written block get zero V values.
+// Tensor memory per CTA: O in columns 0-127, S in 128-255 with P over its first
+// 64 (P aliases S, so S of the next tile is issued once P.V has read P; by then
+// O holds every earlier tile, so the softmax may rescale it without a wait).
+// The running max is only moved (and O rescaled) when a tile's max exceeds it
+// by more than 2^8, so O is rarely touched; the result is the same softmax.
 #include <cmath>
 
 #include <cuda_bf16.h>
@@ -51,24 +55,31 @@ namespace prefill {
 constexpr int kD = 128;            // head dim
 constexpr int kRows = 128;         // query rows per CTA (M)
 constexpr int kKeys = 128;         // keys per KV tile (N of S, K of P.V)
-constexpr int kStages = 3;
-constexpr int kTileBytes = kKeys * kD * 2;         // one K (or V) tile, bf16
-constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kSmem = kStages * kStageBytes;       // 192 KB: one CTA per SM
+constexpr int kTileBytes = kKeys * kD * 2;         // one K (or V, or Q) tile, bf16
+constexpr int kQOff = 0, kKOff = kTileBytes, kVOff = 2 * kTileBytes;
+constexpr int kSmem = 3 * kTileBytes;              // 96 KB: two CTAs per SM
+constexpr int kCtasPerSm = 2;
 constexpr int kMmaWarp = 4;                       // S issuer, TMEM owner
 constexpr int kKLoadWarp = 5, kVLoadWarp = 6;
 constexpr int kPvWarp = 7;                        // P.V issuer
 constexpr int kThreads = 8 * 32;
-constexpr int kGroupBytes = (kD / 8) * 128;         // K: 8 tokens x 128 dims
+constexpr int kGroupBytes = (kD / 8) * 128;         // Q, K: 8 rows x 128 dims
 constexpr int kChunkBytes = (kD / 8) * 128;         // V: 128 dims x 8 tokens
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0, kColS = 128, kColQ = 384, kColP = 448;   // O | S0 | S1 | Q | P
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColO = 0, kColS = 128;        // O | S (P over S's first 64 columns)
 constexpr float kRescaleLog2 = 8.0f;
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kRows, 128);      // S and P.V: M = N = 128
-constexpr uint32_t kKDescHi = tc::desc_hi(kGroupBytes);           // K: SBO = 8-token group
+constexpr uint32_t kKDescHi = tc::desc_hi(kGroupBytes);           // Q, K: SBO = 8-row group
 constexpr uint32_t kVDescHi = tc::desc_hi(128);                   // V: SBO = 8-dim group
+// Registers: the launch gives every thread kLaunchRegs; the softmax warpgroup
+// takes what the other warpgroup (issuers and loaders) gives back.
+constexpr int kLaunchRegs = 65536 / (kThreads * kCtasPerSm);      // 128
+constexpr uint32_t kSoftmaxRegs = 208, kOtherRegs = 48;
 
-static_assert(kSmem <= 227 * 1024, "shared memory ring too large");
+static_assert(kCtasPerSm * (kSmem + 1024) <= 228 * 1024, "two CTAs' shared memory per SM");
+static_assert(kCtasPerSm * kTmemCols <= 512, "two CTAs' tensor memory per SM");
+static_assert(128 * kSoftmaxRegs + 128 * kOtherRegs == (uint32_t)(kThreads * kLaunchRegs),
+              "the register split must add up to the launch's registers");
 
 struct Params {
     __nv_bfloat16* out;
@@ -103,8 +114,8 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // Two-wide float32 arithmetic (one instruction for a pair of values) and a
-// three-input max: the softmax is bound by instruction issue, one warp per
-// scheduler, so each element should cost as few instructions as possible.
+// three-input max: the softmax is bound by instruction issue, so each element
+// should cost as few instructions as possible.
 __device__ __forceinline__ uint64_t f2(float a, float b) {
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
@@ -129,15 +140,13 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return r;
 }
 
-// Barriers (in this order in shared memory).
-enum : int { kBarKFull = 0, kBarKEmpty = kStages, kBarVFull = 2 * kStages,
-             kBarVEmpty = 3 * kStages, kBarS = 4 * kStages, kBarSFree = kBarS + 2,
-             kBarP = kBarSFree + 2, kBarO = kBarP + 1,
-             kBarQ = kBarO + 1, kBarDrain = kBarQ + 1, kBarLand = kBarDrain + 1,
-             kBarDrainPv = kBarLand + 1, kNumBars = kBarDrainPv + 1 };
+// Barriers (in this order in shared memory). One buffer each for K and V, and
+// one phase per KV tile on every barrier.
+enum : int { kBarKFull = 0, kBarVFull, kBarS, kBarP, kBarPV, kBarLand, kBarDrain,
+             kBarDrainPv, kNumBars };
 
 template <int BS>
-__global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(const Params p) {
     constexpr int kBlocksPerTile = kKeys / BS;
     constexpr int kBlockBytes = BS * kD * 2;       // one (block, head) tile
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -169,20 +178,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
     const uint32_t bar0 = smem_addr(bars);
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar(kBarKFull + s), 1);
-            mbar_init(bar(kBarKEmpty + s), 1);
-            mbar_init(bar(kBarVFull + s), 1);
-            mbar_init(bar(kBarVEmpty + s), 1);
-        }
-        mbar_init(bar(kBarLand), 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(kBarS + i), 1);
-            mbar_init(bar(kBarSFree + i), 128);
-        }
+        mbar_init(bar(kBarKFull), 1);
+        mbar_init(bar(kBarVFull), 1);
+        mbar_init(bar(kBarS), 1);
         mbar_init(bar(kBarP), 128);
-        mbar_init(bar(kBarO), 1);
-        mbar_init(bar(kBarQ), 128);
+        mbar_init(bar(kBarPV), 1);
+        mbar_init(bar(kBarLand), 1);
         mbar_init(bar(kBarDrain), 1);
         mbar_init(bar(kBarDrainPv), 1);
         fence_mbar_init();
@@ -192,18 +193,24 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
         tc::relinquish_alloc_permit();
     }
     // The first DRAM reads go out before the set-up barrier: each softmax
-    // thread's q row, and the loaders' first two windows of block ids (a row's
-    // first 64 entries are inside the table whatever the length; they are
-    // checked where they are used)
-    uint4 q_early[kD / 8];
+    // thread's q row goes straight to shared memory (row r in the K-major core
+    // matrix layout: 8-row groups 2 KB apart, 8-dim chunks 128 bytes apart), and
+    // the loaders fetch their first two windows of block ids (a row's first 64
+    // entries are inside the table whatever the length; they are checked where
+    // they are used)
     int bt_early0 = 0, bt_early1 = 0;
     if (warp < 4) {
         const int il = tid / G;
         const bool v_ok = i0 + il < C;
         const uint4* src = reinterpret_cast<const uint4*>(
             p.q + ((size_t)(q0 + (v_ok ? i0 + il : 0)) * p.num_heads + hk * G + tid % G) * kD);
+        uint4 qv[kD / 8];
 #pragma unroll
-        for (int c = 0; c < kD / 8; ++c) q_early[c] = v_ok ? src[c] : make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < kD / 8; ++c) qv[c] = v_ok ? src[c] : make_uint4(0, 0, 0, 0);
+        unsigned char* qrow = smem + kQOff + (tid >> 3) * kGroupBytes + (tid & 7) * 16;
+#pragma unroll
+        for (int c = 0; c < kD / 8; ++c) *reinterpret_cast<uint4*>(qrow + c * 128) = qv[c];
+        fence_proxy_async_smem();   // visible to the tensor cores after the barrier below
     } else if (warp == kKLoadWarp || warp == kVLoadWarp) {
         const int32_t* bt = p.block_tables + (size_t)b * p.max_blocks;
         if (lane < p.max_blocks) bt_early0 = bt[lane];
@@ -214,14 +221,18 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
     tc::fence_after_sync();
     const uint32_t tmem = tmem_slot;
 
+    // warpgroup 1 (issuers, loaders) hands registers to warpgroup 0 (softmax)
+    if (warp >= 4) {
+    tc::regs_dec<kOtherRegs>();
     if (warp == kKLoadWarp || warp == kVLoadWarp) {
         // ------------------------------------------------------------ loaders
         const bool is_v = warp == kVLoadWarp;
         const int bar_full = is_v ? kBarVFull : kBarKFull;
-        const int bar_empty = is_v ? kBarVEmpty : kBarKEmpty;
+        const int bar_free = is_v ? kBarPV : kBarS;         // the buffer's last reader is done
         const __nv_bfloat16* pool = is_v ? p.v_pool : p.k_pool;
         const int32_t* bt = p.block_tables + (size_t)b * p.max_blocks;
         const int tail = L % BS;                           // tokens in a partly written last block
+        const uint32_t buf = sbase + (uint32_t)(is_v ? kVOff : kKOff);
         // block ids in a window of 32 blocks, one per lane, with the next window
         // fetched a window ahead, so table reads never wait on the copies
         auto check_id = [&](int blk, int id) {
@@ -253,25 +264,23 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
             }
             const int my_id = __shfl_sync(0xffffffffu, win_ids, (j * kBlocksPerTile) % 32 +
                                                                     (lane % kBlocksPerTile));
-            const int s = j % kStages;
-            if (j >= kStages &&
-                !mbar_wait_bounded(bar(bar_empty + s), ((j / kStages) - 1) & 1, p.err)) {
+            // the buffer is free once the previous tile's reader has completed
+            if (j >= 1 && !mbar_wait_bounded(bar(bar_free), (j - 1) & 1, p.err)) {
                 flag_error(p.err, kErrTimeout);
                 break;
             }
-            const uint32_t dst = sbase + (uint32_t)(s * kStageBytes + (is_v ? kTileBytes : 0));
             const int blk0 = j * kBlocksPerTile;
             const int n_load = min(kBlocksPerTile, blk_last - blk0 + 1);
             // V of the block holding the sequence's last token is zero-filled
             // past it (K there only meets masked scores)
             const bool fix = is_v && tail != 0 && blk_last == (L - 1) / BS &&
                              blk_last < blk0 + kBlocksPerTile;
-            const uint32_t land = fix ? bar(kBarLand) : bar(bar_full + s);
+            const uint32_t land = fix ? bar(kBarLand) : bar(bar_full);
             if (lane == 0) mbar_arrive_expect_tx(land, (uint32_t)(n_load * kBlockBytes));
             __syncwarp();
             if (lane < n_load) {                           // lane jb copies block jb of the tile
                 const size_t off = ((size_t)my_id * p.num_kv_heads + hk) * (size_t)(BS * kD);
-                bulk_load(dst + (uint32_t)(lane * kBlockBytes), pool + off, kBlockBytes, land);
+                bulk_load(buf + (uint32_t)(lane * kBlockBytes), pool + off, kBlockBytes, land);
             }
             issued = j + 1;
             land_pending = fix;
@@ -282,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
                 }
                 land_pending = false;
                 // V of the last block: [BS/8 chunks][128 dims] rows of 8 tokens
-                const uint32_t vb = dst + (uint32_t)((blk_last - blk0) * kBlockBytes);
+                const uint32_t vb = buf + (uint32_t)((blk_last - blk0) * kBlockBytes);
                 for (int row = lane; row < (BS / 8) * kD; row += 32) {
                     const int valid = tail - (row / kD) * 8;   // tokens of this row's chunk kept
                     if (valid >= 8) continue;
@@ -298,45 +307,37 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
                 }
                 fence_proxy_async_smem();                  // visible to the tensor cores
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(bar_full + s));
+                if (lane == 0) mbar_arrive(bar(bar_full));
             }
         }
         // Every copy this warp issued lands before the CTA may exit, also after a
         // timeout here or in a consumer: wait, with a bound of its own, on the
-        // last tile issued on each stage (a stage takes a tile only after the
-        // previous one there landed, so that phase is unambiguous).
-        for (int jj = max(0, issued - kStages); jj < issued; ++jj) {
-            if (land_pending && jj == issued - 1) continue;   // it lands on kBarLand
-            (void)mbar_wait_bounded(bar(bar_full + jj % kStages), (jj / kStages) & 1, nullptr);
+        // last tile issued (a tile is issued only after the previous one landed
+        // and was read, so that phase is unambiguous).
+        if (issued > 0) {
+            if (land_pending) (void)mbar_wait_bounded(bar(kBarLand), 0, nullptr);
+            else (void)mbar_wait_bounded(bar(bar_full), (issued - 1) & 1, nullptr);
         }
-        if (land_pending) (void)mbar_wait_bounded(bar(kBarLand), 0, nullptr);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ S issuer
         if (lane == 0) {
-            bool ok = mbar_wait_bounded(bar(kBarQ), 0, p.err);
-            tc::fence_after_sync();
-            auto issue_s = [&](int j) {
-                const int s = j % kStages;
-                ok = ok && mbar_wait_bounded(bar(kBarKFull + s), (j / kStages) & 1, p.err);
-                if (!ok) return;
+            bool ok = true;
+            // A = 128 q rows (8-row groups 2 KB apart, SBO; 8-dim chunks 128 bytes
+            // apart, LBO); B = 128 keys, the same layout; each 16-dim step starts
+            // 256 bytes on for both
+            const uint32_t a_lo = tc::desc_lo(sbase + kQOff, 128);
+            const uint32_t b_lo = tc::desc_lo(sbase + kKOff, 128);
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                ok = ok && mbar_wait_bounded(bar(kBarKFull), j & 1, p.err);
+                // S's columns hold P of the previous tile until P.V has read it
+                if (j >= 1) ok = ok && mbar_wait_bounded(bar(kBarPV), (j - 1) & 1, p.err);
+                if (!ok) break;
                 tc::fence_after_sync();
-                const uint32_t d = tmem + kColS + (uint32_t)(j & 1) * 128;
-                // B = 128 keys: 8-token core-matrix groups 2 KB apart (SBO), the
-                // two 8-dim chunks of a 16-dim step 128 bytes apart (LBO); each
-                // 16-dim step starts 256 bytes on
-                const uint32_t lo = tc::desc_lo(sbase + (uint32_t)(s * kStageBytes), 128);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
-                    tc::mma_ts2(d, tmem + kColQ + kk * 8, lo + kk * (256 / 16), kKDescHi, kIdesc,
-                                kk > 0);
-                tc::commit(bar(kBarS + (j & 1)));
-            };
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                if (j >= 2) {                              // S buffer of tile j-2 read: refill it
-                    ok = ok && mbar_wait_bounded(bar(kBarSFree + (j & 1)), ((j - 2) >> 1) & 1, p.err);
-                    tc::fence_after_sync();
-                }
-                issue_s(j);
+                    tc::mma_ss2(tmem + kColS, a_lo + kk * (256 / 16), kKDescHi,
+                                b_lo + kk * (256 / 16), kKDescHi, kIdesc, kk > 0);
+                tc::commit(bar(kBarS));
             }
             if (!ok) flag_error(p.err, kErrTimeout);
             // every MMA issued here is complete before tensor memory is released
@@ -348,13 +349,12 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
         // ------------------------------------------------------------ P.V issuer
         if (lane == 0) {
             bool ok = true;
+            const uint32_t lo = tc::desc_lo(sbase + kVOff, kChunkBytes);
             for (int j = 0; j < n_tiles && ok; ++j) {
                 ok = ok && mbar_wait_bounded(bar(kBarP), j & 1, p.err);
-                ok = ok && mbar_wait_bounded(bar(kBarVFull + j % kStages), (j / kStages) & 1, p.err);
+                ok = ok && mbar_wait_bounded(bar(kBarVFull), j & 1, p.err);
                 if (!ok) break;
                 tc::fence_after_sync();
-                const uint32_t lo = tc::desc_lo(
-                    sbase + (uint32_t)((j % kStages) * kStageBytes + kTileBytes), kChunkBytes);
                 // 16-key steps that hold a key some query sees (P is 0 past them)
                 const int n16 = min(kKeys / 16, (p_max - j * kKeys) / 16 + 1);
                 // B = V of 16 keys: two 8-token chunks 2 KB apart (LBO), 8-dim
@@ -362,18 +362,20 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
 #pragma unroll
                 for (int jj = 0; jj < kKeys / 16; ++jj)
                     if (jj < n16)
-                        tc::mma_ts2(tmem + kColO, tmem + kColP + jj * 8,
+                        tc::mma_ts2(tmem + kColO, tmem + kColS + jj * 8,
                                     lo + jj * (2 * kChunkBytes / 16), kVDescHi, kIdesc,
                                     (j > 0 || jj > 0));
-                tc::commit(bar(kBarO));
+                tc::commit(bar(kBarPV));
             }
             if (!ok) flag_error(p.err, kErrTimeout);
             tc::commit(bar(kBarDrainPv));
             mbar_wait_bounded(bar(kBarDrainPv), 0, nullptr);
         }
         __syncwarp();
+    }
     } else {
         // ------------------------------------------------------------ softmax
+        tc::regs_inc<kSoftmaxRegs>();
         const int r = tid;
         const int il = r / G, g = r % G;
         const int i = i0 + il;
@@ -382,39 +384,17 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
         const int h = hk * G + g;
         const uint32_t row = tmem + ((uint32_t)(warp * 32) << 16);
         bool ok = true;
-        {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t v[32];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const uint4 x = q_early[half * 8 + u];
-                    v[4 * u] = x.x;
-                    v[4 * u + 1] = x.y;
-                    v[4 * u + 2] = x.z;
-                    v[4 * u + 3] = x.w;
-                }
-                tc::st32(row + kColQ + half * 32, v);
-            }
-            tc::wait_st();
-            tc::fence_before_sync();
-            mbar_arrive(bar(kBarQ));
-        }
         const float sc = p.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         for (int j = 0; j < n_tiles; ++j) {
-            const uint32_t sb = kColS + (uint32_t)(j & 1) * 128;
-            ok = ok && mbar_wait_bounded(bar(kBarS + (j & 1)), (j >> 1) & 1, p.err);
+            ok = ok && mbar_wait_bounded(bar(kBarS), j & 1, p.err);
             ok = __all_sync(0xffffffffu, ok);              // the warp's tcgen05 ops stay converged
             if (!ok) break;
-            if (tid == 0) mbar_arrive(bar(kBarKEmpty + j % kStages));   // S done: K tile free
             tc::fence_after_sync();
             uint32_t sv[4][32];
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) tc::ld32(row + sb + cb * 32, sv[cb]);
+            for (int cb = 0; cb < 4; ++cb) tc::ld32(row + kColS + cb * 32, sv[cb]);
             tc::wait_ld();
-            tc::fence_before_sync();
-            mbar_arrive(bar(kBarSFree + (j & 1)));         // the MMA warp may refill this S
             float s[kKeys];
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb)
@@ -433,15 +413,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
             const float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]),
                                   fmaxf(m8[6], m8[7]));
             const float mt = mx * sc;
-            bool o_seen = false;
             if (j == 0) {
                 m_run = mt;
             } else if (__any_sync(0xffffffffu, mt > m_run + kRescaleLog2)) {
-                // move the running max: O must hold P.V of every earlier tile first
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarO), (j - 1) & 1, p.err));
-                o_seen = true;
-                if (tid == 0) mbar_arrive(bar(kBarVEmpty + (j - 1) % kStages));   // V tile free
-                tc::fence_after_sync();
+                // move the running max: O holds P.V of every earlier tile (S of
+                // this tile was issued after the previous P.V completed)
                 const float m_new = fmaxf(m_run, mt);
                 const float alpha = ex2(m_run - m_new);
 #pragma unroll
@@ -453,15 +429,15 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
                     for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
                     tc::st32(row + kColO + cb * 32, v);
                 }
-                tc::wait_st();
                 l_run *= alpha;
                 m_run = m_new;
             }
+            // P over the scores just read, 32 keys (16 columns) at a time
             const uint64_t sc2 = f2(sc, sc), nm2 = f2(-m_run, -m_run);
             uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};       // pairs of partial row sums
-            uint32_t pk[4][16];
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
+                uint32_t pk[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     float x0, x1;
@@ -469,8 +445,9 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
                     const float p0 = ex2(x0), p1 = ex2(x1);
                     l2[c & 3] = add2(l2[c & 3], f2(p0, p1));
                     const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                    pk[cb][c] = *reinterpret_cast<const uint32_t*>(&h2);
+                    pk[c] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
+                tc::st16(row + kColS + cb * 16, pk);
             }
             {
                 float a0, a1, b0, b1, c0, c1, d0, d1;
@@ -480,21 +457,11 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
                 f2_split(l2[3], d0, d1);
                 l_run += ((a0 + a1) + (b0 + b1)) + ((c0 + c1) + (d0 + d1));
             }
-            // P.V of tile j-1 must be done with the P columns (and this consumes
-            // the O barrier's phase for tile j-1, keeping its parity unambiguous)
-            if (j >= 1 && !o_seen) {
-                ok = ok && mbar_wait_bounded(bar(kBarO), (j - 1) & 1, p.err);
-                if (tid == 0) mbar_arrive(bar(kBarVEmpty + (j - 1) % kStages));
-            }
-            ok = __all_sync(0xffffffffu, ok);
-            tc::fence_after_sync();
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) tc::st16(row + kColP + cb * 16, pk[cb]);
             tc::wait_st();
             tc::fence_before_sync();
             mbar_arrive(bar(kBarP));
         }
-        if (ok) ok = mbar_wait_bounded(bar(kBarO), (n_tiles - 1) & 1, p.err);
+        if (ok) ok = mbar_wait_bounded(bar(kBarPV), (n_tiles - 1) & 1, p.err);
         ok = __all_sync(0xffffffffu, ok);
         tc::fence_after_sync();
         if (!ok) {
@@ -502,25 +469,25 @@ __global__ void __launch_bounds__(kThreads, 1) paged_prefill_kernel(const Params
         } else {
             const float inv = 1.f / l_run;
             uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)(q0 + (valid ? i : 0)) * p.num_heads + h) * kD);
-            uint32_t ov[4][32];
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) tc::ld32(row + kColO + cb * 32, ov[cb]);
-            tc::wait_ld();
-            if (valid) {
-#pragma unroll
-                for (int cb = 0; cb < 4; ++cb)
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t ov[32];
+                tc::ld32(row + kColO + cb * 32, ov);
+                tc::wait_ld();
+                if (valid) {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         uint32_t w[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const __nv_bfloat162 h2 = __floats2bfloat162_rn(
-                                __uint_as_float(ov[cb][8 * u + 2 * e]) * inv,
-                                __uint_as_float(ov[cb][8 * u + 2 * e + 1]) * inv);
+                                __uint_as_float(ov[8 * u + 2 * e]) * inv,
+                                __uint_as_float(ov[8 * u + 2 * e + 1]) * inv);
                             w[e] = *reinterpret_cast<const uint32_t*>(&h2);
                         }
                         dst[cb * 4 + u] = make_uint4(w[0], w[1], w[2], w[3]);
                     }
+                }
             }
         }
     }
@@ -539,6 +506,17 @@ int launch(const Params& p, dim3 grid, cudaStream_t stream) {
     int occ = 0;
     const int st = kernel_setup(reinterpret_cast<const void*>(kern), kSmem, kThreads, &occ);
     if (st != PKV_OK) return st;
+    // The softmax warpgroup's register increase waits until the other warpgroup
+    // has released enough: the split adds up only for the launch's register
+    // count, so a build that launches with another count is refused here.
+    static int regs_ok = -1;
+    if (regs_ok < 0) {
+        cudaFuncAttributes fa;
+        const cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(kern));
+        if (e != cudaSuccess) return cuda_fail("prefill: kernel attributes", e);
+        regs_ok = fa.numRegs == kLaunchRegs ? 1 : 0;
+    }
+    if (!regs_ok || occ < 1) return PKV_ERR_UNSUPPORTED;
     note_launch();
     kern<<<grid, kThreads, kSmem, stream>>>(p);
     const cudaError_t e = cudaGetLastError();

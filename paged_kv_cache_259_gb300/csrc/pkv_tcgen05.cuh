@@ -101,6 +101,30 @@ __device__ __forceinline__ void mma_ts2(uint32_t d_tmem, uint32_t a_tmem, uint32
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, one instruction (K = 16 for bf16); both
+// descriptors given as their two 32-bit halves.
+__device__ __forceinline__ void mma_ss2(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                        uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\tmov.b64 ad, {%1, %2};\n\t"
+        "mov.b64 bd, {%3, %4};\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Per-warpgroup register budget (all four warps of a warpgroup execute it):
+// release registers down to N, or wait until N are available to this warp.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // 32 lanes x 32 columns of 32 bits: thread i gets lane (base lane + i), columns
 // col .. col+31 in v[0..31]. Valid after wait_ld().
 __device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&v)[32]) {

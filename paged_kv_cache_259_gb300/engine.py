@@ -15,13 +15,16 @@ view) and a host ``BlockManager``. A step is:
 Pools are allocated by torch (device memory is plumbing); all arithmetic runs in
 the library's kernels.
 """
+import ctypes
 from dataclasses import dataclass
 
 import numpy as np
 import torch
 
-from . import (PKV_ERR_POOL_EXHAUSTED, BlockManager, PagedKVError, copy_blocks,
-               paged_attention_decode, paged_attention_decode_grouped, paged_attention_prefill,
+from . import (PKV_ERR_POOL_EXHAUSTED, BlockManager, PagedKVError, bind_copy_blocks,
+               bind_paged_attention_decode, bind_paged_attention_decode_grouped,
+               bind_reshape_and_cache, copy_blocks, paged_attention_decode,
+               paged_attention_decode_grouped, paged_attention_prefill,
                paged_attention_workspace_size, pool_shapes, pool_views, reshape_and_cache,
                swap_blocks)
 
@@ -409,6 +412,46 @@ class PagedKVCache:
         return paged_attention_decode(out, q, self.k_pool, self.v_pool, dev_plan["tables"],
                                       dev_plan["lens"], scale, k_scale, v_scale, workspace, stream)
 
+    def bind_step(self, q, k_new, v_new, dev_plan, out, scale, k_scale=1.0, v_scale=1.0,
+                  workspace=None):
+        """``step`` checked once and bound to these tensors: returns ``run(stream,
+        num_pairs=None, groups=None)`` that launches the step's copies, slot
+        writes and attention. ``num_pairs`` (default: every row of the plan's
+        pairs) counts the filled rows of a pairs buffer sized for the most a step
+        can raise; with a grouped plan, ``groups = (num_groups, max_group_blocks,
+        num_ungrouped)`` counts the filled rows of its group buffers (0 groups:
+        the plain decode)."""
+        pairs = dev_plan["pairs"]
+        cp = bind_copy_blocks(self.k_pool, self.v_pool, pairs) if pairs.shape[0] else None
+        rc = bind_reshape_and_cache(k_new, v_new, self.k_pool, self.v_pool, dev_plan["slots"],
+                                    k_scale, v_scale)
+        plain = bind_paged_attention_decode(out, q, self.k_pool, self.v_pool, dev_plan["tables"],
+                                            dev_plan["lens"], scale, k_scale, v_scale, workspace)
+        grouped = None
+        if "group_members" in dev_plan:
+            grouped = bind_paged_attention_decode_grouped(
+                out, q, self.k_pool, self.v_pool, dev_plan["tables"], dev_plan["lens"], scale,
+                dev_plan["seq_group"], dev_plan["group_members"], dev_plan["group_prefix"],
+                k_scale, v_scale, workspace, dev_plan.get("ungrouped"),
+                dev_plan.get("max_group_blocks", 0))
+        n_all = pairs.shape[0]
+
+        def run(stream, num_pairs=None, groups=None):
+            n = n_all if num_pairs is None else num_pairs
+            if n:
+                cp(stream, num_pairs=n)
+            rc(stream)
+            if grouped is None:
+                plain(stream)
+            elif groups is None:
+                grouped(stream)
+            elif groups[0] == 0:
+                plain(stream)
+            else:
+                ng, mgb, nu = groups
+                grouped(stream, num_groups=ng, max_group_blocks=mgb, num_ungrouped=nu)
+        return run
+
     def step(self, q, k_new, v_new, dev_plan, out, scale, k_scale=1.0, v_scale=1.0,
              workspace=None, stream=None):
         """The device half of a decode step: copies, slot writes, attention."""
@@ -490,6 +533,8 @@ class StepPipeline:
         ev = lambda: [torch.cuda.Event() for _ in range(2)]
         self.uploaded, self.computed, self.downloaded = ev(), ev(), ev()
         self.n = 0
+        self._host_views = [self._views(h) for h in self.host_slabs]
+        self._bound = [None, None]                        # per slab: (key, bound step)
 
     def _views(self, slab):
         return slab_views(slab, self.layout)
@@ -499,7 +544,17 @@ class StepPipeline:
         i = self.n if i is None else i
         if i >= 2:
             self.uploaded[i % 2].synchronize()            # step i-2's slab has been read
-        return self._views(self.host_slabs[i % 2])
+        return self._host_views[i % 2]
+
+    def _bound_step(self, b, scale, k_scale, v_scale, workspace):
+        """Slab b's decode step, bound once to its device views (rebound when the
+        scales or workspace change)."""
+        key = (scale, k_scale, v_scale, None if workspace is None else workspace.data_ptr())
+        if self._bound[b] is None or self._bound[b][0] != key:
+            q, k_new, v_new, plan = self.steps[b]
+            self._bound[b] = (key, self.cache.bind_step(q, k_new, v_new, plan, self.outs[b],
+                                                        scale, k_scale, v_scale, workspace))
+        return self._bound[b][1]
 
     def submit(self, host_out, scale=None, k_scale=1.0, v_scale=1.0, workspace=None):
         """Run the next step from its filled host views; ``host_out`` = pinned
@@ -517,8 +572,7 @@ class StepPipeline:
             self.compute.wait_event(self.downloaded[b])   # step n-2's output was read
         q, k_new, v_new, plan = self.steps[b]
         if self.run is None:
-            self.cache.step(q, k_new, v_new, plan, out, scale, k_scale, v_scale, workspace,
-                            self.compute)
+            self._bound_step(b, scale, k_scale, v_scale, workspace)(self.compute, **self._counts())
         else:
             self.run(q, k_new, v_new, plan, out, self.compute)
         self.computed[b].record(self.compute)
@@ -528,3 +582,92 @@ class StepPipeline:
         self.downloaded[b].record(self.down)
         self.n += 1
         return self.uploaded[b], self.downloaded[b]
+
+    def _counts(self):
+        return {}
+
+
+class LiveDecodePipeline(StepPipeline):
+    """Decode steps planned on the host as they are submitted, fed from pinned
+    memory and overlapped like ``StepPipeline``.
+
+    Every ``submit`` first plans the step -- the native block manager appends a
+    token to each of ``seq_ids`` (slots and copy-on-write pairs), builds dense
+    tables and lengths and finds the prefix groups -- straight into the next
+    pinned slab (no array is allocated on the way), then uploads that slab with
+    the step's q, k_new and v_new (written by the caller into
+    ``host_inputs()``, or left from an earlier step), runs the step's bound
+    launches with that step's counts (pairs, groups) and reads the output back.
+    The slab's plan buffers are sized for the most a step can raise (a pair and
+    a group row per sequence). Planning ahead of the device work is what the
+    pages' lazy allocation asks of the host every step ("Cách phân trang hoạt
+    động" of the "PagedAttention" glossary)."""
+
+    def __init__(self, cache, seq_ids, q, k_new, v_new, out_template, max_blocks, stream=None,
+                 group_prefixes=True):
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        B = len(ids)
+        t = {"q": q, "k_new": k_new, "v_new": v_new,
+             "slots": torch.empty(B, dtype=torch.int64),
+             "pairs": torch.empty(B, 2, dtype=torch.int64),
+             "tables": torch.empty(B, max_blocks, dtype=torch.int32),
+             "lens": torch.empty(B, dtype=torch.int32)}
+        self.max_members = max(1, 8 // (cache.num_heads // cache.num_kv_heads))
+        self.grouped = group_prefixes and cache.k_pool.dtype != torch.float32
+        if self.grouped:
+            t.update(seq_group=torch.empty(B, dtype=torch.int32),
+                     group_members=torch.empty(B, self.max_members, dtype=torch.int32),
+                     group_prefix=torch.empty(B, dtype=torch.int32),
+                     ungrouped=torch.empty(B, dtype=torch.int32))
+        super().__init__(cache, t, out_template, stream)
+        self.ids = ids
+        self.max_blocks = max_blocks
+        self._ids_p = ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+        self._blocks = np.zeros(max(1, B), dtype=np.int32)
+        p64 = lambda x: ctypes.cast(x.data_ptr(), ctypes.POINTER(ctypes.c_int64))
+        p32 = lambda x: ctypes.cast(x.data_ptr(), ctypes.POINTER(ctypes.c_int32))
+        self._ptrs = []
+        for v in self._host_views:
+            g = None
+            if self.grouped:
+                g = (self.max_members, p32(v["group_members"]), p32(v["group_prefix"]),
+                     p32(v["seq_group"]), self._blocks.ctypes.data_as(
+                         ctypes.POINTER(ctypes.c_int32)))
+            self._ptrs.append((p64(v["slots"]), p64(v["pairs"]), p32(v["tables"]),
+                               p32(v["lens"]), g,
+                               v["seq_group"].numpy() if self.grouped else None,
+                               v["ungrouped"].numpy() if self.grouped else None))
+        self._step_counts = {}
+        self.last_lens_sum = 0
+
+    def plan(self):
+        """Plan the next step into its slab (waits until that slab's previous
+        upload has been read). Returns (pairs, groups) of the step."""
+        views = self.host_inputs()
+        slots_p, pairs_p, tables_p, lens_p, g, sg, ung = self._ptrs[self.n % 2]
+        npairs, ng = self.cache.bm.plan_decode_into(self._ids_p, len(self.ids), self.max_blocks,
+                                                    slots_p, pairs_p, tables_p, lens_p, g)
+        counts = {"num_pairs": npairs}
+        if self.grouped:
+            if ng:
+                idx = np.flatnonzero(sg < 0)
+                ung[:len(idx)] = idx
+                counts["groups"] = (ng, int(self._blocks[:ng].max()), len(idx))
+            else:
+                counts["groups"] = (0, 0, 0)
+        self._step_counts = counts
+        self.last_lens_sum = int(views["lens"].numpy().sum(dtype=np.int64))
+        return npairs, ng
+
+    def submit(self, host_out, scale=None, k_scale=1.0, v_scale=1.0, workspace=None):
+        """Plan the next step (``plan``) unless it is planned already, then run
+        it as ``StepPipeline.submit`` does."""
+        if not self._step_counts:
+            self.plan()
+        try:
+            return super().submit(host_out, scale, k_scale, v_scale, workspace)
+        finally:
+            self._step_counts = {}
+
+    def _counts(self):
+        return self._step_counts

@@ -611,3 +611,61 @@ def test_swap_in_takes_evictable_blocks_when_the_free_list_is_short():
     assert nat.free_list() == ora.free == [] and len(ora.evictable) == 3
     assert [tuple(p) for p in nat.swap_in(1)] == [tuple(p) for p in ora.swap_in(1)]
     _same_state(nat, ora, [1, 2])
+
+
+@pytest.mark.parametrize("name", ["shared_prefix_fork_bf16", "beam_search_bf16", "gqa_chat_bf16"])
+def test_plan_into_buffers_matches_the_array_calls(name):
+    """BlockManager.plan_decode_into (the allocation-free host half of a step
+    that engine.LiveDecodePipeline writes into its pinned slab) gives the slots,
+    copy-on-write pairs, tables, lengths and prefix groups of append_slots,
+    build_tables and prefix_groups on an identical manager, step after step;
+    a refused step changes nothing."""
+    w = wl.CONFIGS[name]()
+    a = pkv.BlockManager(w.NB, w.bs, w.free_order)
+    b = pkv.BlockManager(w.NB, w.bs, w.free_order)
+    for bm in (a, b):
+        for op in w.script:
+            if op[0] == "add":
+                bm.add_seq(op[1])
+            elif op[0] == "append":
+                bm.append_n(op[1], op[2])
+            elif op[0] == "fork":
+                bm.fork(op[1], op[2])
+            else:
+                bm.beam_step(op[1], op[2], op[3])
+    ids = np.ascontiguousarray(np.asarray(w.step_seqs, dtype=np.int64))
+    n, mb, mm = len(ids), w.max_blocks_per_seq + 3, max(1, 8 // (w.Hq // w.Hkv))
+    slots = np.zeros(n, np.int64)
+    pairs = np.zeros((n, 2), np.int64)
+    tables = np.zeros((n, mb), np.int32)
+    lens = np.zeros(n, np.int32)
+    members = np.zeros((n, mm), np.int32)
+    prefix = np.zeros(n, np.int32)
+    seq_group = np.zeros(n, np.int32)
+    blocks = np.zeros(n, np.int32)
+    p64 = lambda x: x.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    p32 = lambda x: x.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    for step in range(20):
+        np_, ng = a.plan_decode_into(p64(ids), n, mb, p64(slots), p64(pairs), p32(tables),
+                                     p32(lens), (mm, p32(members), p32(prefix), p32(seq_group),
+                                                 p32(blocks)))
+        s2, pr2 = b.append_slots(ids)
+        t2, l2 = b.build_tables(ids, mb)
+        m2, pf2, sg2, bl2 = b.prefix_groups(ids, mm)
+        assert np.array_equal(slots, s2) and np.array_equal(pairs[:np_], pr2)
+        assert np.array_equal(tables, t2) and np.array_equal(lens, l2)
+        assert ng == len(m2) and np.array_equal(members[:ng], m2)
+        assert np.array_equal(prefix[:ng], pf2) and np.array_equal(seq_group, sg2)
+        assert np.array_equal(blocks[:ng], bl2)
+        if name == "shared_prefix_fork_bf16" and step == 0:
+            assert np_ == 192 and ng > 0
+    # a step the pool cannot hold is refused whole and leaves the manager as it was
+    free = a.free_list()
+    small = pkv.BlockManager(2, w.bs, np.arange(2))
+    small.add_seq(0)
+    small.append_n(0, 2 * w.bs)
+    one = np.array([0], dtype=np.int64)
+    with pytest.raises(pkv.PagedKVError) as e:
+        small.plan_decode_into(p64(one), 1, 4, p64(slots), p64(pairs), p32(tables), p32(lens))
+    assert e.value.status == pkv.PKV_ERR_POOL_EXHAUSTED and small.seq_len(0) == 2 * w.bs
+    assert np.array_equal(a.free_list(), free)

@@ -519,3 +519,58 @@ def test_step_pipeline_matches_serial_steps():
     for a, b in zip(outs["serial"], outs["pipelined"]):
         assert torch.equal(a, b)
     assert not torch.equal(outs["serial"][0], outs["serial"][1])
+
+
+@pytest.mark.parametrize("fork", [True, False], ids=["fork_step", "steady"])
+def test_live_decode_pipeline_matches_planned_serial_steps(fork):
+    """engine.LiveDecodePipeline (each step planned by the native manager
+    straight into the pinned slab, copy-on-write pairs and prefix groups counted
+    per step, uploads and downloads overlapped) gives, step by step, exactly the
+    outputs and pools of plan_step + step run one after another."""
+    from paged_kv_cache_259_gb300.engine import LiveDecodePipeline, PagedKVCache
+    w = wl.shared_prefix(fork_step=fork, groups=3, per_group=4, prompt=150, max_suffix=40,
+                         Hq=16, Hkv=8, seed=11)
+    n, mb = 6, w.max_blocks_per_seq + 2
+    gen = torch.Generator().manual_seed(5)
+    qs = [torch.randn(w.B, w.Hq, w.D, generator=gen).to(torch.bfloat16) for _ in range(n)]
+    ks = [torch.randn(w.B, w.Hkv, w.D, generator=gen).to(torch.bfloat16) for _ in range(n)]
+    vs = [torch.randn(w.B, w.Hkv, w.D, generator=gen).to(torch.bfloat16) for _ in range(n)]
+    k_src, v_src = w.past_pools()
+    outs, pools, counts = {}, {}, []
+    for mode in ("serial", "live"):
+        cache = PagedKVCache(w.NB, w.Hq, w.Hkv, w.D, w.bs, torch.bfloat16, w.free_order, "cuda")
+        cache.load(k_src, v_src)
+        cache.apply_copies(cache.replay(w.script))
+        ws = cache.workspace(w.B, mb)
+        if mode == "serial":
+            res = []
+            for i in range(n):
+                plan = cache.plan_step(w.step_seqs, max_blocks=mb)
+                counts.append((len(plan.pairs), plan.num_groups))
+                o = torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16, device="cuda")
+                cache.step(qs[i].cuda(), ks[i].cuda(), vs[i].cuda(), plan.device_tensors("cuda"),
+                           o, w.scale, workspace=ws)
+                res.append(o.cpu())
+        else:
+            pipe = LiveDecodePipeline(cache, w.step_seqs, qs[0], ks[0], vs[0],
+                                      torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16,
+                                                  device="cuda"), mb)
+            res = [torch.empty(w.B, w.Hq, w.D, dtype=torch.bfloat16).pin_memory()
+                   for _ in range(n)]
+            for i in range(n):
+                views = pipe.host_inputs()
+                views["q"].copy_(qs[i])
+                views["k_new"].copy_(ks[i])
+                views["v_new"].copy_(vs[i])
+                pipe.submit(res[i], w.scale, workspace=ws)
+            torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        outs[mode] = res
+        pools[mode] = (cache.k_pool.cpu(), cache.v_pool.cpu())
+    for a, b in zip(outs["serial"], outs["live"]):
+        assert torch.equal(a, b)
+    assert torch.equal(pools["serial"][0], pools["live"][0])
+    assert torch.equal(pools["serial"][1], pools["live"][1])
+    assert all(g > 0 for _, g in counts)
+    if fork:
+        assert counts[0][0] == 9 and all(p == 0 for p, _ in counts[1:])
