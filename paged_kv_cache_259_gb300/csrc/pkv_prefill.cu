@@ -22,11 +22,10 @@
 //   tile reads its 128 scores, applies the causal mask, keeps the running max /
 //   sum (exp2 domain, scale * log2 e folded in), writes P (bf16) over the
 //   scores it has just read, and finally normalises O;
-// * warp 4 (S issuer): one thread issues S = Q K^T (A = Q, B = the K tile, both
-//   in shared memory, M = N = 128) once the K tile has landed and the previous
-//   tile's P.V has consumed P, and owns the TMEM allocation; warp 7 (P.V
-//   issuer): one thread issues O += P V (A = P from TMEM, B = the V tile, K = 16
-//   keys per instruction) once P is written;
+// * warp 4 (MMA issuer, TMEM owner): one thread issues, in tile order, S = Q K^T
+//   (A = Q, B = the K tile, both in shared memory, M = N = 128) and O += P V
+//   (A = P from TMEM, B = the V tile, K = 16 keys per instruction): P.V of tile
+//   j as soon as P is written, S of tile j+1 right behind it;
 // * warps 5 and 6 (loaders, K and V): copy each tile of 128 keys block by block
 //   (through the block table) with 1-D bulk copies, lane i copying block i of
 //   the tile, into one K and one V buffer: K of the next tile as soon as S is
@@ -38,8 +37,10 @@
 //   rows are written in the same layout. Keys past the sequence in its last,
 //   partly written block get zero V values.
 // Tensor memory per CTA: O in columns 0-127, S in 128-255 with P over its first
-// 64 (P aliases S, so S of the next tile is issued once P.V has read P; by then
-// O holds every earlier tile, so the softmax may rescale it without a wait).
+// 64. P aliases S: S of the next tile is issued after P.V of this one by the
+// same thread, and the tensor cores run one thread's MMAs in issue order; when
+// S of tile j has completed, so has every earlier MMA, so the softmax may
+// rescale O without a wait. Warp 7 only hands its registers over.
 // The running max is only moved (and O rescaled) when a tile's max exceeds it
 // by more than 2^8, so O is rarely touched; the result is the same softmax.
 #include <cmath>
@@ -59,9 +60,8 @@ constexpr int kTileBytes = kKeys * kD * 2;         // one K (or V, or Q) tile, b
 constexpr int kQOff = 0, kKOff = kTileBytes, kVOff = 2 * kTileBytes;
 constexpr int kSmem = 3 * kTileBytes;              // 96 KB: two CTAs per SM
 constexpr int kCtasPerSm = 2;
-constexpr int kMmaWarp = 4;                       // S issuer, TMEM owner
-constexpr int kKLoadWarp = 5, kVLoadWarp = 6;
-constexpr int kPvWarp = 7;                        // P.V issuer
+constexpr int kMmaWarp = 4;                       // MMA issuer, TMEM owner
+constexpr int kKLoadWarp = 5, kVLoadWarp = 6;     // warp 7: no role
 constexpr int kThreads = 8 * 32;
 constexpr int kGroupBytes = (kD / 8) * 128;         // Q, K: 8 rows x 128 dims
 constexpr int kChunkBytes = (kD / 8) * 128;         // V: 128 dims x 8 tokens
@@ -142,8 +142,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 
 // Barriers (in this order in shared memory). One buffer each for K and V, and
 // one phase per KV tile on every barrier.
-enum : int { kBarKFull = 0, kBarVFull, kBarS, kBarP, kBarPV, kBarLand, kBarDrain,
-             kBarDrainPv, kNumBars };
+enum : int { kBarKFull = 0, kBarVFull, kBarS, kBarP, kBarPV, kBarLand, kBarDrain, kNumBars };
 
 template <int BS>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(const Params p) {
@@ -185,7 +184,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
         mbar_init(bar(kBarPV), 1);
         mbar_init(bar(kBarLand), 1);
         mbar_init(bar(kBarDrain), 1);
-        mbar_init(bar(kBarDrainPv), 1);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -319,37 +317,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
             else (void)mbar_wait_bounded(bar(bar_full), (issued - 1) & 1, nullptr);
         }
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ S issuer
+        // ------------------------------------------------------------ MMA issuer
+        // One thread issues both streams in tile order: S(0), then per tile j
+        // O += P(j) V(j) followed at once by S(j+1). The tensor cores execute
+        // one thread's MMAs in issue order, so S(j+1) overwrites P(j) only after
+        // P.V(j) has read it, with no round trip through a barrier in between.
         if (lane == 0) {
             bool ok = true;
-            // A = 128 q rows (8-row groups 2 KB apart, SBO; 8-dim chunks 128 bytes
-            // apart, LBO); B = 128 keys, the same layout; each 16-dim step starts
-            // 256 bytes on for both
+            // S: A = 128 q rows (8-row groups 2 KB apart, SBO; 8-dim chunks 128
+            // bytes apart, LBO); B = 128 keys, the same layout; each 16-dim step
+            // starts 256 bytes on for both
             const uint32_t a_lo = tc::desc_lo(sbase + kQOff, 128);
             const uint32_t b_lo = tc::desc_lo(sbase + kKOff, 128);
-            for (int j = 0; j < n_tiles && ok; ++j) {
+            const uint32_t v_lo = tc::desc_lo(sbase + kVOff, kChunkBytes);
+            auto issue_s = [&](int j) {
                 ok = ok && mbar_wait_bounded(bar(kBarKFull), j & 1, p.err);
-                // S's columns hold P of the previous tile until P.V has read it
-                if (j >= 1) ok = ok && mbar_wait_bounded(bar(kBarPV), (j - 1) & 1, p.err);
-                if (!ok) break;
+                if (!ok) return;
                 tc::fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
                     tc::mma_ss2(tmem + kColS, a_lo + kk * (256 / 16), kKDescHi,
                                 b_lo + kk * (256 / 16), kKDescHi, kIdesc, kk > 0);
                 tc::commit(bar(kBarS));
-            }
-            if (!ok) flag_error(p.err, kErrTimeout);
-            // every MMA issued here is complete before tensor memory is released
-            tc::commit(bar(kBarDrain));
-            mbar_wait_bounded(bar(kBarDrain), 0, nullptr);   // a real wait even after a timeout
-        }
-        __syncwarp();
-    } else if (warp == kPvWarp) {
-        // ------------------------------------------------------------ P.V issuer
-        if (lane == 0) {
-            bool ok = true;
-            const uint32_t lo = tc::desc_lo(sbase + kVOff, kChunkBytes);
+            };
+            issue_s(0);
             for (int j = 0; j < n_tiles && ok; ++j) {
                 ok = ok && mbar_wait_bounded(bar(kBarP), j & 1, p.err);
                 ok = ok && mbar_wait_bounded(bar(kBarVFull), j & 1, p.err);
@@ -363,13 +354,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
                 for (int jj = 0; jj < kKeys / 16; ++jj)
                     if (jj < n16)
                         tc::mma_ts2(tmem + kColO, tmem + kColS + jj * 8,
-                                    lo + jj * (2 * kChunkBytes / 16), kVDescHi, kIdesc,
+                                    v_lo + jj * (2 * kChunkBytes / 16), kVDescHi, kIdesc,
                                     (j > 0 || jj > 0));
                 tc::commit(bar(kBarPV));
+                if (j + 1 < n_tiles) issue_s(j + 1);
             }
             if (!ok) flag_error(p.err, kErrTimeout);
-            tc::commit(bar(kBarDrainPv));
-            mbar_wait_bounded(bar(kBarDrainPv), 0, nullptr);
+            // every MMA issued here is complete before tensor memory is released
+            tc::commit(bar(kBarDrain));
+            mbar_wait_bounded(bar(kBarDrain), 0, nullptr);   // a real wait even after a timeout
         }
         __syncwarp();
     }
@@ -416,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
             if (j == 0) {
                 m_run = mt;
             } else if (__any_sync(0xffffffffu, mt > m_run + kRescaleLog2)) {
-                // move the running max: O holds P.V of every earlier tile (S of
-                // this tile was issued after the previous P.V completed)
+                // move the running max: O holds P.V of every earlier tile (issued
+                // before S of this tile, which has completed)
                 const float m_new = fmaxf(m_run, mt);
                 const float alpha = ex2(m_run - m_new);
 #pragma unroll

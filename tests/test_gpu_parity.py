@@ -18,6 +18,7 @@ import pytest
 import torch
 
 import pkv_workloads as wl
+from oracle import fp8_e4m3 as ofp8
 from _lib import library, pkv
 from _parity import (Inputs, assert_close, check_cache_writes, check_indexing,
                      run_gpu, run_oracle, sample_units)
@@ -215,6 +216,33 @@ def test_bad_block_id_sets_error_word_and_skips(Hq):
     from _parity import assert_close as ac
     ref = oatt.paged_decode(q.cpu()[:1], kc, vc, bt.cpu().numpy()[:1], [100], 0.1, 16)
     ac(out[:1].float().cpu().numpy(), ref, "bf16", "seq 0")
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_paired_stage_with_a_bad_second_block_is_flagged_and_skipped(kv):
+    """A bad id in the second block of a stage (block 3 of sequence 1; the E4M3
+    decode over 16-token blocks stages two blocks at a time) is flagged and its
+    stage skipped; the other sequences, whose last stages hold one block (a
+    40-token sequence) or a second block of one token (17 tokens), match the
+    oracle. The bf16 case runs the one-block stages of the same path."""
+    q, kp, vp, bt, kc, vc = _decode_args(3, 16, 4, 128, 16, 32, 8)
+    if kv == "e4m3":
+        kc8 = torch.from_numpy(ofp8.e4m3_quantize(kc.float().numpy(), 0.05))
+        vc8 = torch.from_numpy(ofp8.e4m3_quantize(vc.float().numpy(), 0.05))
+        kp, vp = to_layout(kc8.cuda(), vc8.cuda())
+    bt[1, 3] = 32          # == num_blocks: outside the pool
+    lens = torch.tensor([40, 100, 17], dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    assert pkv.get_device_error() == 0
+    s = 0.05 if kv == "e4m3" else 1.0
+    pkv.paged_attention_decode(out, q, kp, vp, bt, lens, 0.1, s, s)
+    assert pkv.get_device_error() == -4
+    from oracle import attention as oatt
+    from _parity import assert_close as ac
+    keep = [0, 2]                          # the oracle reads only valid tables
+    tk, tv = (kc8, vc8) if kv == "e4m3" else (kc, vc)
+    ref = oatt.paged_decode(q.cpu()[keep], tk, tv, bt.cpu().numpy()[keep], [40, 17], 0.1, 16, s, s)
+    ac(out[keep].float().cpu().numpy(), ref, kv, "sequences 0 and 2")
 
 
 def test_a_wait_nothing_completes_times_out_and_the_context_stays_usable():
