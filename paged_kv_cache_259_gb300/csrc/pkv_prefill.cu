@@ -15,34 +15,39 @@
 // of one KV head, so each K/V tile feeds every head that shares it) of one
 // sequence; two CTAs share an SM (half its tensor memory, registers and shared
 // memory each), so one CTA's set-up and epilogue overlap the other's tiles and
-// the tensor cores alternate between two independent score pipelines. Warp
-// roles:
+// the tensor cores alternate between two independent score pipelines. Keys go
+// in tiles of 64, so that within its half of the SM a CTA double-buffers the
+// scores (tensor memory) and the K and V tiles (shared memory): the scores of
+// tile j+1 are computed while the softmax works on tile j. Warp roles:
 // * warps 0-3 (softmax, one warpgroup with most of the registers): thread r
 //   owns row r = TMEM lane r. Puts its q row into shared memory, then per KV
-//   tile reads its 128 scores, applies the causal mask, keeps the running max /
+//   tile reads its 64 scores, applies the causal mask, keeps the running max /
 //   sum (exp2 domain, scale * log2 e folded in), writes P (bf16) over the
 //   scores it has just read, and finally normalises O;
 // * warp 4 (MMA issuer, TMEM owner): one thread issues, in tile order, S = Q K^T
-//   (A = Q, B = the K tile, both in shared memory, M = N = 128) and O += P V
-//   (A = P from TMEM, B = the V tile, K = 16 keys per instruction): P.V of tile
-//   j as soon as P is written, S of tile j+1 right behind it;
-// * warps 5 and 6 (loaders, K and V): copy each tile of 128 keys block by block
+//   (A = Q, B = the K tile, both in shared memory, M = 128, N = 64) and O += P V
+//   (A = P from TMEM, B = the V tile, K = 16 keys per instruction): S of tiles
+//   0 and 1 at once, then per tile j, P.V(j) as soon as P is written and S of
+//   tile j+2 right behind it, into the buffer P(j) has just been read from;
+// * warps 5 and 6 (loaders, K and V): copy each tile of 64 keys block by block
 //   (through the block table) with 1-D bulk copies, lane i copying block i of
-//   the tile, into one K and one V buffer: K of the next tile as soon as S is
-//   computed, V of the next tile as soon as P.V is done. The cache stores every
+//   the tile, into two K and two V buffers: K of tile j+2 as soon as S(j) is
+//   computed, V of tile j+2 as soon as P.V(j) is done. The cache stores every
 //   (block, head) tile as 128-byte core matrices, K [bs/8][D/8][8][8] and V
 //   [bs/8][D/8][8][8] (8 dims x 8 tokens), which is the canonical no-swizzle
 //   K-major operand layout, so a tile lands ready for the tensor cores (S with
-//   N = 128 keys over 8 blocks, P.V with K = 16 keys per instruction); the q
+//   N = 64 keys over 64/bs blocks, P.V with K = 16 keys per instruction); the q
 //   rows are written in the same layout. Keys past the sequence in its last,
 //   partly written block get zero V values.
-// Tensor memory per CTA: O in columns 0-127, S in 128-255 with P over its first
-// 64. P aliases S: S of the next tile is issued after P.V of this one by the
-// same thread, and the tensor cores run one thread's MMAs in issue order; when
-// S of tile j has completed, so has every earlier MMA, so the softmax may
-// rescale O without a wait. Warp 7 only hands its registers over.
-// The running max is only moved (and O rescaled) when a tile's max exceeds it
-// by more than 2^8, so O is rarely touched; the result is the same softmax.
+// Tensor memory per CTA: O in columns 0-127, S of even tiles in 128-191, S of
+// odd tiles in 192-255, P of a tile over the first 32 columns of its S. S of
+// tile j+2 reuses the buffer of tile j and is issued after P.V(j) by the same
+// thread; the tensor cores run one thread's MMAs in issue order, so it
+// overwrites P(j) only after P.V(j) has read it. Warp 7 only hands its
+// registers over.
+// The running max is only moved (and O rescaled, after P.V of the previous tile
+// has completed) when a tile's max exceeds it by more than 2^8, so O is rarely
+// touched; the result is the same softmax.
 #include <cmath>
 
 #include <cuda_bf16.h>
@@ -55,10 +60,11 @@ namespace prefill {
 
 constexpr int kD = 128;            // head dim
 constexpr int kRows = 128;         // query rows per CTA (M)
-constexpr int kKeys = 128;         // keys per KV tile (N of S, K of P.V)
-constexpr int kTileBytes = kKeys * kD * 2;         // one K (or V, or Q) tile, bf16
-constexpr int kQOff = 0, kKOff = kTileBytes, kVOff = 2 * kTileBytes;
-constexpr int kSmem = 3 * kTileBytes;              // 96 KB: two CTAs per SM
+constexpr int kKeys = 64;          // keys per KV tile (N of S, K of P.V)
+constexpr int kTileBytes = kKeys * kD * 2;         // one K (or V) tile, bf16: 16 KB
+constexpr int kQBytes = kRows * kD * 2;            // the q rows: 32 KB
+constexpr int kQOff = 0, kKOff = kQBytes, kVOff = kQBytes + 2 * kTileBytes;
+constexpr int kSmem = kQBytes + 4 * kTileBytes;    // 96 KB: two CTAs per SM
 constexpr int kCtasPerSm = 2;
 constexpr int kMmaWarp = 4;                       // MMA issuer, TMEM owner
 constexpr int kKLoadWarp = 5, kVLoadWarp = 6;     // warp 7: no role
@@ -66,9 +72,10 @@ constexpr int kThreads = 8 * 32;
 constexpr int kGroupBytes = (kD / 8) * 128;         // Q, K: 8 rows x 128 dims
 constexpr int kChunkBytes = (kD / 8) * 128;         // V: 128 dims x 8 tokens
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColO = 0, kColS = 128;        // O | S (P over S's first 64 columns)
+constexpr uint32_t kColO = 0, kColS = 128;        // O | S of even tiles | S of odd tiles
 constexpr float kRescaleLog2 = 8.0f;
-constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kRows, 128);      // S and P.V: M = N = 128
+constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kRows, kKeys);   // S: M = 128, N = 64
+constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kRows, kD);      // P.V: M = N = 128
 constexpr uint32_t kKDescHi = tc::desc_hi(kGroupBytes);           // Q, K: SBO = 8-row group
 constexpr uint32_t kVDescHi = tc::desc_hi(128);                   // V: SBO = 8-dim group
 // Registers: the launch gives every thread kLaunchRegs; the softmax warpgroup
@@ -78,6 +85,7 @@ constexpr uint32_t kSoftmaxRegs = 208, kOtherRegs = 48;
 
 static_assert(kCtasPerSm * (kSmem + 1024) <= 228 * 1024, "two CTAs' shared memory per SM");
 static_assert(kCtasPerSm * kTmemCols <= 512, "two CTAs' tensor memory per SM");
+static_assert(kColS + 2 * kKeys == kTmemCols, "two score buffers after O");
 static_assert(128 * kSoftmaxRegs + 128 * kOtherRegs == (uint32_t)(kThreads * kLaunchRegs),
               "the register split must add up to the launch's registers");
 
@@ -140,9 +148,10 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return r;
 }
 
-// Barriers (in this order in shared memory). One buffer each for K and V, and
-// one phase per KV tile on every barrier.
-enum : int { kBarKFull = 0, kBarVFull, kBarS, kBarP, kBarPV, kBarLand, kBarDrain, kNumBars };
+// Barriers (in this order in shared memory). Two of each for the buffers
+// (K, V stages and S buffers: tile j uses buffer j % 2, one phase per use).
+enum : int { kBarKFull = 0, kBarVFull = 2, kBarS = 4, kBarPV = 6, kBarP = 8, kBarLand,
+             kBarDrain, kNumBars };
 
 template <int BS>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(const Params p) {
@@ -177,11 +186,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
     const uint32_t bar0 = smem_addr(bars);
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     if (tid == 0) {
-        mbar_init(bar(kBarKFull), 1);
-        mbar_init(bar(kBarVFull), 1);
-        mbar_init(bar(kBarS), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(kBarKFull + i), 1);
+            mbar_init(bar(kBarVFull + i), 1);
+            mbar_init(bar(kBarS + i), 1);
+            mbar_init(bar(kBarPV + i), 1);
+        }
         mbar_init(bar(kBarP), 128);
-        mbar_init(bar(kBarPV), 1);
         mbar_init(bar(kBarLand), 1);
         mbar_init(bar(kBarDrain), 1);
         fence_mbar_init();
@@ -219,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
     tc::fence_after_sync();
     const uint32_t tmem = tmem_slot;
 
-    // warpgroup 1 (issuers, loaders) hands registers to warpgroup 0 (softmax)
+    // warpgroup 1 (issuer, loaders) hands registers to warpgroup 0 (softmax)
     if (warp >= 4) {
     tc::regs_dec<kOtherRegs>();
     if (warp == kKLoadWarp || warp == kVLoadWarp) {
@@ -230,7 +241,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
         const __nv_bfloat16* pool = is_v ? p.v_pool : p.k_pool;
         const int32_t* bt = p.block_tables + (size_t)b * p.max_blocks;
         const int tail = L % BS;                           // tokens in a partly written last block
-        const uint32_t buf = sbase + (uint32_t)(is_v ? kVOff : kKOff);
         // block ids in a window of 32 blocks, one per lane, with the next window
         // fetched a window ahead, so table reads never wait on the copies
         auto check_id = [&](int blk, int id) {
@@ -262,18 +272,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
             }
             const int my_id = __shfl_sync(0xffffffffu, win_ids, (j * kBlocksPerTile) % 32 +
                                                                     (lane % kBlocksPerTile));
-            // the buffer is free once the previous tile's reader has completed
-            if (j >= 1 && !mbar_wait_bounded(bar(bar_free), (j - 1) & 1, p.err)) {
+            const int sb = j & 1;                          // buffer of this tile
+            // the buffer is free once its previous tile's reader has completed
+            if (j >= 2 && !mbar_wait_bounded(bar(bar_free + sb), ((j - 2) >> 1) & 1, p.err)) {
                 flag_error(p.err, kErrTimeout);
                 break;
             }
+            const uint32_t buf = sbase + (uint32_t)((is_v ? kVOff : kKOff) + sb * kTileBytes);
             const int blk0 = j * kBlocksPerTile;
             const int n_load = min(kBlocksPerTile, blk_last - blk0 + 1);
             // V of the block holding the sequence's last token is zero-filled
             // past it (K there only meets masked scores)
             const bool fix = is_v && tail != 0 && blk_last == (L - 1) / BS &&
                              blk_last < blk0 + kBlocksPerTile;
-            const uint32_t land = fix ? bar(kBarLand) : bar(bar_full);
+            const uint32_t land = fix ? bar(kBarLand) : bar(bar_full + sb);
             if (lane == 0) mbar_arrive_expect_tx(land, (uint32_t)(n_load * kBlockBytes));
             __syncwarp();
             if (lane < n_load) {                           // lane jb copies block jb of the tile
@@ -305,59 +317,60 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
                 }
                 fence_proxy_async_smem();                  // visible to the tensor cores
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(bar_full));
+                if (lane == 0) mbar_arrive(bar(bar_full + sb));
             }
         }
         // Every copy this warp issued lands before the CTA may exit, also after a
         // timeout here or in a consumer: wait, with a bound of its own, on the
-        // last tile issued (a tile is issued only after the previous one landed
-        // and was read, so that phase is unambiguous).
-        if (issued > 0) {
-            if (land_pending) (void)mbar_wait_bounded(bar(kBarLand), 0, nullptr);
-            else (void)mbar_wait_bounded(bar(bar_full), (issued - 1) & 1, nullptr);
+        // last tile issued on each buffer (a buffer takes a tile only after the
+        // previous one there landed and was read, so those phases are
+        // unambiguous).
+        for (int jj = max(0, issued - 2); jj < issued; ++jj) {
+            if (land_pending && jj == issued - 1) continue;   // it lands on kBarLand
+            (void)mbar_wait_bounded(bar(bar_full + (jj & 1)), (jj >> 1) & 1, nullptr);
         }
+        if (land_pending) (void)mbar_wait_bounded(bar(kBarLand), 0, nullptr);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        // One thread issues both streams in tile order: S(0), then per tile j
-        // O += P(j) V(j) followed at once by S(j+1). The tensor cores execute
-        // one thread's MMAs in issue order, so S(j+1) overwrites P(j) only after
-        // P.V(j) has read it, with no round trip through a barrier in between.
         if (lane == 0) {
             bool ok = true;
             // S: A = 128 q rows (8-row groups 2 KB apart, SBO; 8-dim chunks 128
-            // bytes apart, LBO); B = 128 keys, the same layout; each 16-dim step
+            // bytes apart, LBO); B = 64 keys, the same layout; each 16-dim step
             // starts 256 bytes on for both
             const uint32_t a_lo = tc::desc_lo(sbase + kQOff, 128);
-            const uint32_t b_lo = tc::desc_lo(sbase + kKOff, 128);
-            const uint32_t v_lo = tc::desc_lo(sbase + kVOff, kChunkBytes);
             auto issue_s = [&](int j) {
-                ok = ok && mbar_wait_bounded(bar(kBarKFull), j & 1, p.err);
+                const int sb = j & 1;
+                ok = ok && mbar_wait_bounded(bar(kBarKFull + sb), (j >> 1) & 1, p.err);
                 if (!ok) return;
                 tc::fence_after_sync();
+                const uint32_t b_lo = tc::desc_lo(sbase + kKOff + sb * kTileBytes, 128);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
-                    tc::mma_ss2(tmem + kColS, a_lo + kk * (256 / 16), kKDescHi,
-                                b_lo + kk * (256 / 16), kKDescHi, kIdesc, kk > 0);
-                tc::commit(bar(kBarS));
+                    tc::mma_ss2(tmem + kColS + sb * kKeys, a_lo + kk * (256 / 16), kKDescHi,
+                                b_lo + kk * (256 / 16), kKDescHi, kIdescS, kk > 0);
+                tc::commit(bar(kBarS + sb));
             };
             issue_s(0);
+            if (n_tiles > 1) issue_s(1);
             for (int j = 0; j < n_tiles && ok; ++j) {
+                const int sb = j & 1;
                 ok = ok && mbar_wait_bounded(bar(kBarP), j & 1, p.err);
-                ok = ok && mbar_wait_bounded(bar(kBarVFull), j & 1, p.err);
+                ok = ok && mbar_wait_bounded(bar(kBarVFull + sb), (j >> 1) & 1, p.err);
                 if (!ok) break;
                 tc::fence_after_sync();
                 // 16-key steps that hold a key some query sees (P is 0 past them)
                 const int n16 = min(kKeys / 16, (p_max - j * kKeys) / 16 + 1);
                 // B = V of 16 keys: two 8-token chunks 2 KB apart (LBO), 8-dim
                 // core-matrix rows 128 bytes apart (SBO); each step 4 KB on
+                const uint32_t v_lo = tc::desc_lo(sbase + kVOff + sb * kTileBytes, kChunkBytes);
 #pragma unroll
                 for (int jj = 0; jj < kKeys / 16; ++jj)
                     if (jj < n16)
-                        tc::mma_ts2(tmem + kColO, tmem + kColS + jj * 8,
-                                    v_lo + jj * (2 * kChunkBytes / 16), kVDescHi, kIdesc,
+                        tc::mma_ts2(tmem + kColO, tmem + kColS + sb * kKeys + jj * 8,
+                                    v_lo + jj * (2 * kChunkBytes / 16), kVDescHi, kIdescO,
                                     (j > 0 || jj > 0));
-                tc::commit(bar(kBarPV));
-                if (j + 1 < n_tiles) issue_s(j + 1);
+                tc::commit(bar(kBarPV + sb));
+                if (j + 2 < n_tiles) issue_s(j + 2);       // into the buffer P(j) was read from
             }
             if (!ok) flag_error(p.err, kErrTimeout);
             // every MMA issued here is complete before tensor memory is released
@@ -380,17 +393,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
         const float sc = p.scale_log2;
         float m_run = -INFINITY, l_run = 0.f;
         for (int j = 0; j < n_tiles; ++j) {
-            ok = ok && mbar_wait_bounded(bar(kBarS), j & 1, p.err);
+            const int sb = j & 1;
+            const uint32_t scol = kColS + sb * kKeys;
+            ok = ok && mbar_wait_bounded(bar(kBarS + sb), (j >> 1) & 1, p.err);
             ok = __all_sync(0xffffffffu, ok);              // the warp's tcgen05 ops stay converged
             if (!ok) break;
             tc::fence_after_sync();
-            uint32_t sv[4][32];
+            uint32_t sv[2][32];
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) tc::ld32(row + kColS + cb * 32, sv[cb]);
+            for (int cb = 0; cb < 2; ++cb) tc::ld32(row + scol + cb * 32, sv[cb]);
             tc::wait_ld();
             float s[kKeys];
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb)
+            for (int cb = 0; cb < 2; ++cb)
 #pragma unroll
                 for (int c = 0; c < 32; ++c) s[cb * 32 + c] = __uint_as_float(sv[cb][c]);
             if (j >= first_masked) {
@@ -409,8 +424,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
             if (j == 0) {
                 m_run = mt;
             } else if (__any_sync(0xffffffffu, mt > m_run + kRescaleLog2)) {
-                // move the running max: O holds P.V of every earlier tile (issued
-                // before S of this tile, which has completed)
+                // move the running max: O must hold P.V of every earlier tile
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(kBarPV + ((j - 1) & 1)),
+                                                               ((j - 1) >> 1) & 1, p.err));
+                if (!ok) break;
+                tc::fence_after_sync();
                 const float m_new = fmaxf(m_run, mt);
                 const float alpha = ex2(m_run - m_new);
 #pragma unroll
@@ -429,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
             const uint64_t sc2 = f2(sc, sc), nm2 = f2(-m_run, -m_run);
             uint64_t l2[4] = {0ull, 0ull, 0ull, 0ull};       // pairs of partial row sums
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
+            for (int cb = 0; cb < 2; ++cb) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
@@ -440,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
                     const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
                     pk[c] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
-                tc::st16(row + kColS + cb * 16, pk);
+                tc::st16(row + scol + cb * 16, pk);
             }
             {
                 float a0, a1, b0, b1, c0, c1, d0, d1;
@@ -454,7 +472,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
             tc::fence_before_sync();
             mbar_arrive(bar(kBarP));
         }
-        if (ok) ok = mbar_wait_bounded(bar(kBarPV), (n_tiles - 1) & 1, p.err);
+        if (ok) ok = mbar_wait_bounded(bar(kBarPV + ((n_tiles - 1) & 1)), ((n_tiles - 1) >> 1) & 1,
+                                       p.err);
         ok = __all_sync(0xffffffffu, ok);
         tc::fence_after_sync();
         if (!ok) {
