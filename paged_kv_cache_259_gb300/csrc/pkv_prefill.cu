@@ -148,9 +148,11 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return r;
 }
 
-// Barriers (in this order in shared memory). Two of each for the buffers
-// (K, V stages and S buffers: tile j uses buffer j % 2, one phase per use).
-enum : int { kBarKFull = 0, kBarVFull = 2, kBarS = 4, kBarPV = 6, kBarP = 8, kBarLand,
+// Barriers (in this order in shared memory). Two of each for the buffers (K
+// and V stages, S and P buffers: tile j uses buffer j % 2, one phase per use),
+// so that no waiter can fall two phases behind a barrier: the softmax may
+// write P(j+1) before the issuer has waited for P(j), never P(j+2).
+enum : int { kBarKFull = 0, kBarVFull = 2, kBarS = 4, kBarPV = 6, kBarP = 8, kBarLand = 10,
              kBarDrain, kNumBars };
 
 template <int BS>
@@ -193,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
             mbar_init(bar(kBarPV + i), 1);
         }
         mbar_init(bar(kBarP), 128);
+        mbar_init(bar(kBarP + 1), 128);
         mbar_init(bar(kBarLand), 1);
         mbar_init(bar(kBarDrain), 1);
         fence_mbar_init();
@@ -354,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
             if (n_tiles > 1) issue_s(1);
             for (int j = 0; j < n_tiles && ok; ++j) {
                 const int sb = j & 1;
-                ok = ok && mbar_wait_bounded(bar(kBarP), j & 1, p.err);
+                ok = ok && mbar_wait_bounded(bar(kBarP + sb), (j >> 1) & 1, p.err);
                 ok = ok && mbar_wait_bounded(bar(kBarVFull + sb), (j >> 1) & 1, p.err);
                 if (!ok) break;
                 tc::fence_after_sync();
@@ -470,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
             }
             tc::wait_st();
             tc::fence_before_sync();
-            mbar_arrive(bar(kBarP));
+            mbar_arrive(bar(kBarP + sb));
         }
         if (ok) ok = mbar_wait_bounded(bar(kBarPV + ((n_tiles - 1) & 1)), ((n_tiles - 1) >> 1) & 1,
                                        p.err);
