@@ -187,16 +187,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
     const uint32_t sbase = smem_addr(smem);
     const uint32_t bar0 = smem_addr(bars);
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-    if (tid == 0) {
+    if (tid == 0) {                                        // the loaders init their own
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(kBarKFull + i), 1);
-            mbar_init(bar(kBarVFull + i), 1);
             mbar_init(bar(kBarS + i), 1);
             mbar_init(bar(kBarPV + i), 1);
+            mbar_init(bar(kBarP + i), 128);
         }
-        mbar_init(bar(kBarP), 128);
-        mbar_init(bar(kBarP + 1), 128);
-        mbar_init(bar(kBarLand), 1);
         mbar_init(bar(kBarDrain), 1);
         fence_mbar_init();
     }
@@ -204,13 +200,93 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
         tc::alloc(smem_addr(&tmem_slot), kTmemCols);
         tc::relinquish_alloc_permit();
     }
+    // Loader state (warps 5 and 6: K and V). Block ids come in windows of 32
+    // blocks, one per lane, with the next window fetched a window ahead, so table
+    // reads never wait on the copies.
+    const bool is_v = warp == kVLoadWarp;
+    const int bar_full = is_v ? kBarVFull : kBarKFull;
+    const int bar_free = is_v ? kBarPV : kBarS;            // the buffer's last reader is done
+    const __nv_bfloat16* pool = is_v ? p.v_pool : p.k_pool;
+    const int32_t* bt = p.block_tables + (size_t)b * p.max_blocks;
+    const int tail = L % BS;                               // tokens in a partly written last block
+    int win = 0, win_ids = 0, next_ids = 0;
+    int issued = 0;                                        // tiles whose copies went out
+    bool land_pending = false;                             // the zero-fill tile's copies
+    auto check_id = [&](int blk, int id) {
+        if (blk > blk_last) return 0;
+        if (id < 0 || id >= p.num_blocks) {
+            flag_error(p.err, kErrOutOfRange);
+            return 0;                                      // in bounds; the sequence is in error
+        }
+        return id;
+    };
+    auto fetch_id = [&](int blk) { return blk > blk_last ? 0 : check_id(blk, bt[blk]); };
+    // Copies of tile j into buffer j % 2 (false: a wait timed out)
+    auto load_tile = [&](int j) -> bool {
+        if ((j * kBlocksPerTile) / 32 != win) {
+            ++win;
+            win_ids = next_ids;
+            next_ids = fetch_id((win + 1) * 32 + lane);
+        }
+        const int my_id = __shfl_sync(0xffffffffu, win_ids, (j * kBlocksPerTile) % 32 +
+                                                                (lane % kBlocksPerTile));
+        const int sb = j & 1;                              // buffer of this tile
+        // the buffer is free once its previous tile's reader has completed
+        if (j >= 2 && !mbar_wait_bounded(bar(bar_free + sb), ((j - 2) >> 1) & 1, p.err)) {
+            flag_error(p.err, kErrTimeout);
+            return false;
+        }
+        const uint32_t buf = sbase + (uint32_t)((is_v ? kVOff : kKOff) + sb * kTileBytes);
+        const int blk0 = j * kBlocksPerTile;
+        const int n_load = min(kBlocksPerTile, blk_last - blk0 + 1);
+        // V of the block holding the sequence's last token is zero-filled past
+        // it (K there only meets masked scores)
+        const bool fix = is_v && tail != 0 && blk_last == (L - 1) / BS &&
+                         blk_last < blk0 + kBlocksPerTile;
+        const uint32_t land = fix ? bar(kBarLand) : bar(bar_full + sb);
+        if (lane == 0) mbar_arrive_expect_tx(land, (uint32_t)(n_load * kBlockBytes));
+        __syncwarp();
+        if (lane < n_load) {                               // lane jb copies block jb of the tile
+            const size_t off = ((size_t)my_id * p.num_kv_heads + hk) * (size_t)(BS * kD);
+            bulk_load(buf + (uint32_t)(lane * kBlockBytes), pool + off, kBlockBytes, land);
+        }
+        issued = j + 1;
+        land_pending = fix;
+        if (fix) {
+            if (!mbar_wait_bounded(bar(kBarLand), 0, p.err)) {
+                flag_error(p.err, kErrTimeout);
+                return false;
+            }
+            land_pending = false;
+            // V of the last block: [BS/8 chunks][128 dims] rows of 8 tokens
+            const uint32_t vb = buf + (uint32_t)((blk_last - blk0) * kBlockBytes);
+            for (int row = lane; row < (BS / 8) * kD; row += 32) {
+                const int valid = tail - (row / kD) * 8;   // tokens of this row's chunk kept
+                if (valid >= 8) continue;
+                uint4* v = reinterpret_cast<uint4*>(smem + (vb - sbase) + row * 16);
+                uint4 x = *v;
+                uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (2 * e >= valid) w[e] = 0u;
+                    else if (2 * e + 1 >= valid) w[e] &= 0x0000ffffu;
+                }
+                *v = x;
+            }
+            fence_proxy_async_smem();                      // visible to the tensor cores
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bar_full + sb));
+        }
+        return true;
+    };
+
     // The first DRAM reads go out before the set-up barrier: each softmax
     // thread's q row goes straight to shared memory (row r in the K-major core
     // matrix layout: 8-row groups 2 KB apart, 8-dim chunks 128 bytes apart), and
-    // the loaders fetch their first two windows of block ids (a row's first 64
-    // entries are inside the table whatever the length; they are checked where
-    // they are used)
-    int bt_early0 = 0, bt_early1 = 0;
+    // the loaders set up their own barriers and send the copies of the first
+    // two tiles (they wait for no other warp; a row's first 64 table entries are
+    // inside the table whatever the length, checked where they are used)
+    bool load_ok = true;
     if (warp < 4) {
         const int il = tid / G;
         const bool v_ok = i0 + il < C;
@@ -224,9 +300,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
         for (int c = 0; c < kD / 8; ++c) *reinterpret_cast<uint4*>(qrow + c * 128) = qv[c];
         fence_proxy_async_smem();   // visible to the tensor cores after the barrier below
     } else if (warp == kKLoadWarp || warp == kVLoadWarp) {
-        const int32_t* bt = p.block_tables + (size_t)b * p.max_blocks;
-        if (lane < p.max_blocks) bt_early0 = bt[lane];
-        if (32 + lane < p.max_blocks) bt_early1 = bt[32 + lane];
+        if (lane == 0) {
+            mbar_init(bar(bar_full), 1);
+            mbar_init(bar(bar_full + 1), 1);
+            if (is_v) mbar_init(bar(kBarLand), 1);
+            fence_mbar_init();
+        }
+        __syncwarp();
+        win_ids = check_id(lane, lane < p.max_blocks ? bt[lane] : 0);
+        next_ids = check_id(32 + lane, 32 + lane < p.max_blocks ? bt[32 + lane] : 0);
+        for (int j = 0; j < min(2, n_tiles) && load_ok; ++j) load_ok = load_tile(j);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -238,91 +321,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
     tc::regs_dec<kOtherRegs>();
     if (warp == kKLoadWarp || warp == kVLoadWarp) {
         // ------------------------------------------------------------ loaders
-        const bool is_v = warp == kVLoadWarp;
-        const int bar_full = is_v ? kBarVFull : kBarKFull;
-        const int bar_free = is_v ? kBarPV : kBarS;         // the buffer's last reader is done
-        const __nv_bfloat16* pool = is_v ? p.v_pool : p.k_pool;
-        const int32_t* bt = p.block_tables + (size_t)b * p.max_blocks;
-        const int tail = L % BS;                           // tokens in a partly written last block
-        // block ids in a window of 32 blocks, one per lane, with the next window
-        // fetched a window ahead, so table reads never wait on the copies
-        auto check_id = [&](int blk, int id) {
-            if (blk > blk_last) return 0;
-            if (id < 0 || id >= p.num_blocks) {
-                flag_error(p.err, kErrOutOfRange);
-                return 0;                                  // in bounds; the sequence is in error
-            }
-            return id;
-        };
-        auto fetch_id = [&](int blk) {
-            if (blk > blk_last) return 0;
-            const int id = bt[blk];
-            if (id < 0 || id >= p.num_blocks) {
-                flag_error(p.err, kErrOutOfRange);
-                return 0;                                  // in bounds; the sequence is in error
-            }
-            return id;
-        };
-        int win = 0;
-        int win_ids = check_id(lane, bt_early0), next_ids = check_id(32 + lane, bt_early1);
-        int issued = 0;                                    // tiles whose copies went out
-        bool land_pending = false;                         // the zero-fill tile's copies
-        for (int j = 0; j < n_tiles; ++j) {
-            if ((j * kBlocksPerTile) / 32 != win) {
-                ++win;
-                win_ids = next_ids;
-                next_ids = fetch_id((win + 1) * 32 + lane);
-            }
-            const int my_id = __shfl_sync(0xffffffffu, win_ids, (j * kBlocksPerTile) % 32 +
-                                                                    (lane % kBlocksPerTile));
-            const int sb = j & 1;                          // buffer of this tile
-            // the buffer is free once its previous tile's reader has completed
-            if (j >= 2 && !mbar_wait_bounded(bar(bar_free + sb), ((j - 2) >> 1) & 1, p.err)) {
-                flag_error(p.err, kErrTimeout);
-                break;
-            }
-            const uint32_t buf = sbase + (uint32_t)((is_v ? kVOff : kKOff) + sb * kTileBytes);
-            const int blk0 = j * kBlocksPerTile;
-            const int n_load = min(kBlocksPerTile, blk_last - blk0 + 1);
-            // V of the block holding the sequence's last token is zero-filled
-            // past it (K there only meets masked scores)
-            const bool fix = is_v && tail != 0 && blk_last == (L - 1) / BS &&
-                             blk_last < blk0 + kBlocksPerTile;
-            const uint32_t land = fix ? bar(kBarLand) : bar(bar_full + sb);
-            if (lane == 0) mbar_arrive_expect_tx(land, (uint32_t)(n_load * kBlockBytes));
-            __syncwarp();
-            if (lane < n_load) {                           // lane jb copies block jb of the tile
-                const size_t off = ((size_t)my_id * p.num_kv_heads + hk) * (size_t)(BS * kD);
-                bulk_load(buf + (uint32_t)(lane * kBlockBytes), pool + off, kBlockBytes, land);
-            }
-            issued = j + 1;
-            land_pending = fix;
-            if (fix) {
-                if (!mbar_wait_bounded(bar(kBarLand), 0, p.err)) {
-                    flag_error(p.err, kErrTimeout);
-                    break;
-                }
-                land_pending = false;
-                // V of the last block: [BS/8 chunks][128 dims] rows of 8 tokens
-                const uint32_t vb = buf + (uint32_t)((blk_last - blk0) * kBlockBytes);
-                for (int row = lane; row < (BS / 8) * kD; row += 32) {
-                    const int valid = tail - (row / kD) * 8;   // tokens of this row's chunk kept
-                    if (valid >= 8) continue;
-                    uint4* v = reinterpret_cast<uint4*>(smem + (vb - sbase) + row * 16);
-                    uint4 x = *v;
-                    uint32_t* w = reinterpret_cast<uint32_t*>(&x);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (2 * e >= valid) w[e] = 0u;
-                        else if (2 * e + 1 >= valid) w[e] &= 0x0000ffffu;
-                    }
-                    *v = x;
-                }
-                fence_proxy_async_smem();                  // visible to the tensor cores
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(bar_full + sb));
-            }
-        }
+        for (int j = 2; j < n_tiles && load_ok; ++j) load_ok = load_tile(j);
         // Every copy this warp issued lands before the CTA may exit, also after a
         // timeout here or in a consumer: wait, with a bound of its own, on the
         // last tile issued on each buffer (a buffer takes a tile only after the
