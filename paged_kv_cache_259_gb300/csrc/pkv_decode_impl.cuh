@@ -711,20 +711,6 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
         for (int s = 0; s < ST; ++s) mbar_init(smem_addr(&bars[w * ST + s]), 1);
         fence_mbar_init();
     }
-    for (int i = tid; i < G * D; i += NW * 32) {            // query rows of this CTA
-        const int r = i / D;
-        int seq, head;
-        row_target<PREFIX, G>(p, key, hk, r, &seq, &head);
-        float qv = 0.f;
-        if (seq >= 0) qv = to_f(static_cast<const QT*>(p.q)[((size_t)seq * p.num_heads + head) * D + i % D]);
-        qs[i] = Math::kPrescaledQ ? qv * p.qscale : qv;
-    }
-    __syncthreads();
-
-    typename Math::State st;
-    Math::init(st, qs, lane);
-    float* pb = wsm + w * Math::kWarpSmemFloats;
-
     const int nk = nbp > w ? (nbp - w + NW - 1) / NW : 0;  // this warp's blocks
     const uint64_t pol = l2_evict_first();
     const int gh = p.num_heads / p.num_kv_heads;
@@ -823,12 +809,29 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
         }
     };
 
+    // the first stages' copies go out before the q rows are read (each warp
+    // uses only its own barriers and ring)
     const int pro = nk < ST ? nk : ST;
     for (int kk = 0; kk < pro; ++kk) {
         int info, id2;
         const int id = get_id(kk, &info, &id2);
         if (lane == 0) issue(kk, id, id2, info);
     }
+
+    for (int i = tid; i < G * D; i += NW * 32) {            // query rows of this CTA
+        const int r = i / D;
+        int seq, head;
+        row_target<PREFIX, G>(p, key, hk, r, &seq, &head);
+        float qv = 0.f;
+        if (seq >= 0) qv = to_f(static_cast<const QT*>(p.q)[((size_t)seq * p.num_heads + head) * D + i % D]);
+        qs[i] = Math::kPrescaledQ ? qv * p.qscale : qv;
+    }
+    __syncthreads();
+
+    typename Math::State st;
+    Math::init(st, qs, lane);
+    float* pb = wsm + w * Math::kWarpSmemFloats;
+
 
     bool aborted = false;
     int k = 0;

@@ -17,6 +17,7 @@ import numpy as np
 import pytest
 import torch
 
+import bench
 import pkv_workloads as wl
 from oracle import fp8_e4m3 as ofp8
 from _lib import library, pkv
@@ -88,13 +89,19 @@ def test_full_size_workload_sampled(name):
     inp = Inputs(w)
     g = run_gpu(inp, workspace=True)
     assert g["err"] == 0
-    n = 16 if w.kv_dtype == "e4m3" else 48
-    units = sample_units(w, n, seed=1)
-    o = run_oracle(inp, units=units)
+    units = sample_units(w, 128 if w.kv_dtype == "e4m3" else 96, seed=1)
+    o = run_oracle(inp, units=[])                 # the oracle's state: slots, tables, pools
     check_indexing(g, o)
     check_cache_writes(inp, g, o)
+    # the sampled rows through the bench's multi-process oracle runner (one
+    # single-threaded float64 oracle process per host core)
+    per_tok = 2 * w.Hkv * w.D * {"e4m3": 1, "bf16": 2, "f32": 4}[w.kv_dtype]
+    _, _, _, note, rows = bench.oracle_timing(
+        w, (inp.q, o["k_pool"], o["v_pool"], inp.ks, inp.vs), o["tables"], o["lens"], per_tok,
+        0.0, 1, check_units=units)
+    assert sorted(rows) == sorted(units), note
     got = np.stack([g["out"][b, h].numpy() for b, h in units])
-    ref = np.stack([o["out"][u] for u in units])
+    ref = np.stack([rows[u] for u in units])
     assert_close(got, ref, w.kv_dtype, name)
     assert torch.isfinite(g["out"]).all()
     if name == "shared_prefix_fork_bf16":
