@@ -164,8 +164,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
     __shared__ uint32_t tmem_slot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // grid (query tile, kv head, sequence), the query tile fastest: the tiles
+    // of one (sequence, kv head) run side by side and share its K/V through L2
+    // (launching every sequence's last tile first instead measured 0.35 / 0.46
+    // of the bf16 peak against 0.47 / 0.68); within them the longest goes first
     const int b = blockIdx.z, hk = blockIdx.y;
-    const int qtile = gridDim.x - 1 - blockIdx.x;          // longest tiles first
+    const int qtile = gridDim.x - 1 - blockIdx.x;
     const int G = p.G;
     const int tok_per_tile = kRows / G;
     const int L = p.seq_lens[b];
