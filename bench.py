@@ -5,13 +5,17 @@ paged_attention_decode) on a seeded synthetic workload, timed on the GPU.
 
 Prints ONE JSON line (rank 0). ``value`` is achieved algorithmic HBM bytes of the
 whole step per second (GB/s), with every input resident in HBM; ``e2e`` is the
-same metric through the engine (``StepPipeline``), every step's inputs uploaded
-from pinned host memory and its output read back inside the timed region,
-overlapped with the neighbouring steps. ``roofline`` covers the decode
-attention op alone (its kernel plus the split-KV merge), timed with CUDA events
-on its stream. ``cpu_baseline`` times the CPU oracle on a bounded sample of the
-same workload. With ``--impl reference`` the oracle alone is timed (the
-reference arm; a slow CPU program, not a target).
+same metric through the engine (``LiveDecodePipeline``): every step is planned
+on the host by the native block manager straight into a pinned slab, the slab
+is uploaded and the output read back inside the timed region, overlapped with
+the neighbouring steps. ``roofline`` covers the decode attention op alone (its
+kernel plus the split-KV merge), timed with CUDA events on its stream.
+``cpu_baseline`` times the CPU oracle on a bounded sample of the same workload,
+and ``check`` compares the timed steps' output with the oracle rows that run
+computed first. The default workload's line also carries ``others``: every
+other decode workload timed the same way, each with its own check. With
+``--impl reference`` the oracle alone is timed (the reference arm; a slow CPU
+program, not a target).
 
 Other workloads (``--config``): ``prefill_*`` time a chunked-prefill step
 (TFLOP/s of the causal attention, tensor-bound roofline), the prompt workload a
@@ -444,7 +448,7 @@ def e2e_live_planning(cache, w, q, k_new, v_new, out, ks, vs, ws, stream, steps,
     free = w.NB - int(sum(-(-int(L) // w.bs) for L in w.final_lens))
     per_pass = max(1, min(steps, w.bs * max(1, free // w.B)))
     mb = w.max_blocks_per_seq + -(-per_pass // w.bs) + 1
-    plan0 = rewind(cache, w, mb)
+    rewind(cache, w, mb)
     hq, hk, hv = q.pin_memory(), k_new.pin_memory(), v_new.pin_memory()
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     pipe = LiveDecodePipeline(cache, w.step_seqs, hq, hk, hv, out, mb, stream=stream)
@@ -453,7 +457,6 @@ def e2e_live_planning(cache, w, q, k_new, v_new, out, ks, vs, ws, stream, steps,
         v["q"].copy_(hq)
         v["k_new"].copy_(hk)
         v["v_new"].copy_(hv)
-    base_tokens = int(plan0.lens.astype(np.int64).sum())
 
     def one_step(plan_us):
         pipe.host_inputs()                 # wait for the slab outside the planning time
@@ -463,14 +466,14 @@ def e2e_live_planning(cache, w, q, k_new, v_new, out, ks, vs, ws, stream, steps,
         except PagedKVError as e:
             if e.status != PKV_ERR_POOL_EXHAUSTED:
                 raise
-            return None                    # no room for another step in this pass
+            return False                   # no room for another step in this pass
         plan_us.append(1e6 * (time.perf_counter() - t1))
         pipe.submit(hout, w.scale, ks, vs, ws)
-        return pipe.last_lens_sum
+        return True
 
     warm_us = []
     for _ in range(min(warmup, per_pass)):
-        if one_step(warm_us) is None:
+        if not one_step(warm_us):
             break
     torch.cuda.synchronize()
     total_ms, total_bytes, done, plan_us = 0.0, 0.0, 0, []
@@ -484,11 +487,12 @@ def e2e_live_planning(cache, w, q, k_new, v_new, out, ks, vs, ws, stream, steps,
         e0.record(pipe.up)
         k = 0
         for _ in range(n):
-            tokens = one_step(plan_us)
-            if tokens is None:
+            if not one_step(plan_us):
                 break
-            total_bytes += nb["total"] + (tokens - base_tokens) * nb["per_token"]
             k += 1
+            # the pass's k-th step attends over k more tokens per sequence than
+            # the measured step (one appended per sequence per step)
+            total_bytes += nb["total"] + k * w.B * nb["per_token"]
         e1.record(pipe.down)
         torch.cuda.synchronize()
         if k == 0:

@@ -462,6 +462,28 @@ PKV_API int bm_num_free(const pkv_block_manager* bm);
 PKV_API int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
                      int max_members, int32_t* group_members, int32_t* group_prefix,
                      int32_t* seq_group, int32_t* group_blocks, int* num_groups);
+/* The host half of one decode step in one call, written into caller buffers
+ * (e.g. a pinned upload slab) with nothing allocated for the caller: one
+ * append per listed sequence (bm_append_slots: slots int64 [n], copy-on-write
+ * pairs int64 [n][2], their count in *num_cow), dense tables and lengths
+ * (bm_build_tables: int32 [n][max_blocks], int32 [n]) and, when max_members >=
+ * 1, the prefix groups (bm_prefix_groups: members int32 [n][max_members],
+ * prefixes, list blocks int32 [n], seq_group int32 [n], *num_groups) with the
+ * batch indices in no group (ungrouped int32 [n], in batch order,
+ * *num_ungrouped) and the longest group list (*max_group_blocks, 0 without
+ * groups). Pass max_members <= 0 and null group buffers to skip the groups.
+ * All or nothing: a table that would outgrow max_blocks
+ * (PKV_ERR_INVALID_ARG), an unknown id (PKV_ERR_OUT_OF_RANGE) or a pool that
+ * cannot hold the appends (PKV_ERR_POOL_EXHAUSTED) changes nothing. This is
+ * the host work the pages' lazy allocation asks for at every step (glossary
+ * "PagedAttention", "Cách phân trang hoạt động"). */
+PKV_API int bm_plan_decode(pkv_block_manager* bm, const int64_t* seq_ids, int n, int max_blocks,
+                           int64_t* slots, int64_t* cow_pairs, int* num_cow,
+                           int32_t* tables, int32_t* seq_lens, int max_members,
+                           int32_t* group_members, int32_t* group_prefix, int32_t* seq_group,
+                           int32_t* group_blocks, int32_t* ungrouped, int* num_groups,
+                           int* num_ungrouped, int* max_group_blocks);
+
 /* Prefix caching (glossary "Chia sẻ block giữa các chuỗi": requests that begin
  * with the same system prompt reuse one copy of the common prefix, with a count
  * per block; "vLLM PagedAttention: uma revolução...": prefix caching).

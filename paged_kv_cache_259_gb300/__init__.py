@@ -80,6 +80,8 @@ def load_library():
                                                    c_int, c_float, c_float, vp, vp, vp, c_int,
                                                    c_int, c_int, vp, c_int, vp, c_size, vp]),
         "bm_prefix_groups": (c_int, [vp, i64p, c_int, c_int, i32p, i32p, i32p, i32p, ip]),
+        "bm_plan_decode": (c_int, [vp, i64p, c_int, c_int, i64p, i64p, ip, i32p, i32p, c_int, i32p,
+                                   i32p, i32p, i32p, i32p, ip, ip, ip]),
         "paged_attention_decode_noalloc": (c_int, [vp, vp, vp, vp, vp, vp, c_int, c_int, c_int,
                                                    c_int, c_int, c_int, c_int, c_float, c_int,
                                                    c_int, c_float, c_float, vp]),
@@ -681,27 +683,26 @@ class BlockManager:
 
     def plan_decode_into(self, ids_p, n, max_blocks, slots_p, pairs_p, tables_p, lens_p,
                          groups=None):
-        """The host half of a decode step written straight into caller buffers
-        given as ctypes pointers (e.g. views of a pinned upload slab), with no
-        array allocated: one append per listed sequence (``slots_p`` int64 [n],
-        ``pairs_p`` int64 [n, 2]: the copy-on-write pairs), dense ``tables_p``
-        int32 [n, max_blocks] and ``lens_p`` int32 [n], and, with ``groups =
-        (max_members, members_p, prefix_p, seq_group_p, blocks_p)`` (int32 [n,
-        max_members], [n], [n], [n]), the prefix groups. Returns (number of
-        pairs, number of groups). The appends are all or nothing, as in
-        ``append_slots``: PKV_ERR_POOL_EXHAUSTED leaves the manager unchanged."""
-        cnt = ctypes.c_int(0)
-        _check(self._lib.bm_append_slots(self._h, ids_p, n, slots_p, pairs_p, ctypes.byref(cnt)),
-               "bm_append_slots")
-        _check(self._lib.bm_build_tables(self._h, ids_p, n, max_blocks, tables_p, lens_p),
-               "bm_build_tables")
-        ng = ctypes.c_int(0)
-        if groups is not None:
-            mm, members_p, prefix_p, seq_group_p, blocks_p = groups
-            _check(self._lib.bm_prefix_groups(self._h, ids_p, n, mm, members_p, prefix_p,
-                                              seq_group_p, blocks_p, ctypes.byref(ng)),
-                   "bm_prefix_groups")
-        return cnt.value, ng.value
+        """The host half of a decode step in one native call (``bm_plan_decode``),
+        written straight into caller buffers given as ctypes pointers (e.g. views
+        of a pinned upload slab), with no array allocated: one append per listed
+        sequence (``slots_p`` int64 [n], ``pairs_p`` int64 [n, 2]: the
+        copy-on-write pairs), dense ``tables_p`` int32 [n, max_blocks] and
+        ``lens_p`` int32 [n], and, with ``groups = (max_members, members_p,
+        prefix_p, seq_group_p, blocks_p, ungrouped_p)`` (int32 [n, max_members],
+        [n], [n], [n], [n]), the prefix groups and the batch indices in no group.
+        Returns (pairs, groups, ungrouped, longest group list). All or nothing:
+        a refused step leaves the manager unchanged."""
+        cnt, ng, nu, mgb = (ctypes.c_int(0) for _ in range(4))
+        if groups is None:
+            args = (0, None, None, None, None, None)
+        else:
+            args = groups
+        _check(self._lib.bm_plan_decode(self._h, ids_p, n, max_blocks, slots_p, pairs_p,
+                                        ctypes.byref(cnt), tables_p, lens_p, *args,
+                                        ctypes.byref(ng), ctypes.byref(nu), ctypes.byref(mgb)),
+               "bm_plan_decode")
+        return cnt.value, ng.value, nu.value, mgb.value
 
     def fork(self, parent, child):
         _check(self._lib.bm_fork(self._h, parent, child), "bm_fork")

@@ -540,6 +540,44 @@ int bm_prefix_groups(const pkv_block_manager* bm, const int64_t* seq_ids, int n,
     return PKV_OK;
 }
 
+int bm_plan_decode(pkv_block_manager* bm, const int64_t* seq_ids, int n, int max_blocks,
+                   int64_t* slots, int64_t* cow_pairs, int* num_cow, int32_t* tables,
+                   int32_t* seq_lens, int max_members, int32_t* group_members,
+                   int32_t* group_prefix, int32_t* seq_group, int32_t* group_blocks,
+                   int32_t* ungrouped, int* num_groups, int* num_ungrouped,
+                   int* max_group_blocks) {
+    if (!bm || n < 0 || max_blocks < 0 || !num_cow)
+        return PKV_ERR_INVALID_ARG;
+    const bool groups = max_members >= 1;
+    if (groups && (!ungrouped || !group_blocks || !num_groups || !num_ungrouped ||
+                   !max_group_blocks))
+        return PKV_ERR_INVALID_ARG;
+    // every table must still fit max_blocks after its append: checked before any
+    // append, so a refusal changes nothing
+    for (int i = 0; i < n; ++i) {
+        auto it = bm->seqs.find(seq_ids[i]);
+        if (it == bm->seqs.end()) return PKV_ERR_OUT_OF_RANGE;
+        const auto& sq = it->second;
+        const int64_t after = (int64_t)sq.table.size() + (sq.len % bm->block_size == 0 ? 1 : 0);
+        if (after > max_blocks) return PKV_ERR_INVALID_ARG;
+    }
+    int st = bm_append_slots(bm, seq_ids, n, slots, cow_pairs, num_cow);
+    if (st != PKV_OK) return st;
+    st = bm_build_tables(bm, seq_ids, n, max_blocks, tables, seq_lens);
+    if (st != PKV_OK) return st;
+    if (!groups) return PKV_OK;
+    st = bm_prefix_groups(bm, seq_ids, n, max_members, group_members, group_prefix, seq_group,
+                          group_blocks, num_groups);
+    if (st != PKV_OK) return st;
+    int nu = 0, mgb = 0;
+    for (int i = 0; i < n; ++i)
+        if (seq_group[i] < 0) ungrouped[nu++] = i;
+    for (int g = 0; g < *num_groups; ++g) mgb = std::max(mgb, (int)group_blocks[g]);
+    *num_ungrouped = nu;
+    *max_group_blocks = mgb;
+    return PKV_OK;
+}
+
 int bm_enable_prefix_caching(pkv_block_manager* bm) {
     if (!bm || !bm->seqs.empty()) return PKV_ERR_INVALID_ARG;
     if (bm->caching) return PKV_OK;

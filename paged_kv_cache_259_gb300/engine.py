@@ -631,32 +631,25 @@ class LiveDecodePipeline(StepPipeline):
             g = None
             if self.grouped:
                 g = (self.max_members, p32(v["group_members"]), p32(v["group_prefix"]),
-                     p32(v["seq_group"]), self._blocks.ctypes.data_as(
-                         ctypes.POINTER(ctypes.c_int32)))
+                     p32(v["seq_group"]),
+                     self._blocks.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                     p32(v["ungrouped"]))
             self._ptrs.append((p64(v["slots"]), p64(v["pairs"]), p32(v["tables"]),
-                               p32(v["lens"]), g,
-                               v["seq_group"].numpy() if self.grouped else None,
-                               v["ungrouped"].numpy() if self.grouped else None))
+                               p32(v["lens"]), g))
         self._step_counts = {}
-        self.last_lens_sum = 0
 
     def plan(self):
-        """Plan the next step into its slab (waits until that slab's previous
-        upload has been read). Returns (pairs, groups) of the step."""
-        views = self.host_inputs()
-        slots_p, pairs_p, tables_p, lens_p, g, sg, ung = self._ptrs[self.n % 2]
-        npairs, ng = self.cache.bm.plan_decode_into(self._ids_p, len(self.ids), self.max_blocks,
-                                                    slots_p, pairs_p, tables_p, lens_p, g)
-        counts = {"num_pairs": npairs}
+        """Plan the next step into its slab with one native call (waits until
+        that slab's previous upload has been read). Returns (pairs, groups) of
+        the step."""
+        self.host_inputs()
+        slots_p, pairs_p, tables_p, lens_p, g = self._ptrs[self.n % 2]
+        npairs, ng, nu, mgb = self.cache.bm.plan_decode_into(
+            self._ids_p, len(self.ids), self.max_blocks, slots_p, pairs_p, tables_p, lens_p, g)
         if self.grouped:
-            if ng:
-                idx = np.flatnonzero(sg < 0)
-                ung[:len(idx)] = idx
-                counts["groups"] = (ng, int(self._blocks[:ng].max()), len(idx))
-            else:
-                counts["groups"] = (0, 0, 0)
-        self._step_counts = counts
-        self.last_lens_sum = int(views["lens"].numpy().sum(dtype=np.int64))
+            self._step_counts = {"num_pairs": npairs, "groups": (ng, mgb, nu)}
+        else:
+            self._step_counts = {"num_pairs": npairs}
         return npairs, ng
 
     def submit(self, host_out, scale=None, k_scale=1.0, v_scale=1.0, workspace=None):

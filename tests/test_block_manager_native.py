@@ -615,10 +615,11 @@ def test_swap_in_takes_evictable_blocks_when_the_free_list_is_short():
 
 @pytest.mark.parametrize("name", ["shared_prefix_fork_bf16", "beam_search_bf16", "gqa_chat_bf16"])
 def test_plan_into_buffers_matches_the_array_calls(name):
-    """BlockManager.plan_decode_into (the allocation-free host half of a step
-    that engine.LiveDecodePipeline writes into its pinned slab) gives the slots,
-    copy-on-write pairs, tables, lengths and prefix groups of append_slots,
-    build_tables and prefix_groups on an identical manager, step after step;
+    """BlockManager.plan_decode_into (bm_plan_decode: the allocation-free host
+    half of a step that engine.LiveDecodePipeline writes into its pinned slab)
+    gives the slots, copy-on-write pairs, tables, lengths and prefix groups of
+    append_slots, build_tables and prefix_groups on an identical manager, plus
+    the batch indices in no group and the longest group list, step after step;
     a refused step changes nothing."""
     w = wl.CONFIGS[name]()
     a = pkv.BlockManager(w.NB, w.bs, w.free_order)
@@ -643,12 +644,13 @@ def test_plan_into_buffers_matches_the_array_calls(name):
     prefix = np.zeros(n, np.int32)
     seq_group = np.zeros(n, np.int32)
     blocks = np.zeros(n, np.int32)
+    ungrouped = np.zeros(n, np.int32)
     p64 = lambda x: x.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
     p32 = lambda x: x.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    groups = (mm, p32(members), p32(prefix), p32(seq_group), p32(blocks), p32(ungrouped))
     for step in range(20):
-        np_, ng = a.plan_decode_into(p64(ids), n, mb, p64(slots), p64(pairs), p32(tables),
-                                     p32(lens), (mm, p32(members), p32(prefix), p32(seq_group),
-                                                 p32(blocks)))
+        np_, ng, nu, mgb = a.plan_decode_into(p64(ids), n, mb, p64(slots), p64(pairs),
+                                              p32(tables), p32(lens), groups)
         s2, pr2 = b.append_slots(ids)
         t2, l2 = b.build_tables(ids, mb)
         m2, pf2, sg2, bl2 = b.prefix_groups(ids, mm)
@@ -657,10 +659,25 @@ def test_plan_into_buffers_matches_the_array_calls(name):
         assert ng == len(m2) and np.array_equal(members[:ng], m2)
         assert np.array_equal(prefix[:ng], pf2) and np.array_equal(seq_group, sg2)
         assert np.array_equal(blocks[:ng], bl2)
+        assert np.array_equal(ungrouped[:nu], np.flatnonzero(sg2 < 0))
+        assert mgb == (int(bl2.max()) if ng else 0)
         if name == "shared_prefix_fork_bf16" and step == 0:
             assert np_ == 192 and ng > 0
-    # a step the pool cannot hold is refused whole and leaves the manager as it was
+    # without groups: the plain half of the step
+    np_, ng, nu, mgb = a.plan_decode_into(p64(ids), n, mb, p64(slots), p64(pairs), p32(tables),
+                                          p32(lens))
+    b.append_slots(ids)
+    t2, l2 = b.build_tables(ids, mb)
+    assert (ng, nu, mgb) == (0, 0, 0) and np.array_equal(tables, t2) and np.array_equal(lens, l2)
+    # refusals change nothing: tables that would outgrow max_blocks, a pool that
+    # cannot hold the appends
     free = a.free_list()
+    lens_before = [a.seq_len(int(s)) for s in ids]
+    with pytest.raises(pkv.PagedKVError) as e:
+        a.plan_decode_into(p64(ids), n, 1, p64(slots), p64(pairs), p32(tables), p32(lens))
+    assert e.value.status == -1
+    assert np.array_equal(a.free_list(), free)
+    assert [a.seq_len(int(s)) for s in ids] == lens_before
     small = pkv.BlockManager(2, w.bs, np.arange(2))
     small.add_seq(0)
     small.append_n(0, 2 * w.bs)
@@ -668,4 +685,3 @@ def test_plan_into_buffers_matches_the_array_calls(name):
     with pytest.raises(pkv.PagedKVError) as e:
         small.plan_decode_into(p64(one), 1, 4, p64(slots), p64(pairs), p32(tables), p32(lens))
     assert e.value.status == pkv.PKV_ERR_POOL_EXHAUSTED and small.seq_len(0) == 2 * w.bs
-    assert np.array_equal(a.free_list(), free)
