@@ -353,6 +353,34 @@ PKV_API int paged_attention_decode_noalloc(void* out, const void* q,
                                    int block_size, float scale, int q_dtype, int kv_dtype,
                                    float k_scale, float v_scale, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Stream plumbing of a pipelined step (no counterpart in the pages: it is how
+ * a host loop feeds one step after another without spending its time on
+ * runtime calls). Streams and events are cudaStream_t / cudaEvent_t passed as
+ * void*; the caller creates and owns them and the buffers.
+ *
+ * pkv_stage_upload: copy `bytes` of a step's packed inputs from pinned host
+ * memory to the device on `up_stream` and order the step's kernels (on
+ * `compute_stream`) after that copy. When the buffers are being reused, pass
+ * the events of their previous step: the copy then waits for
+ * `reuse_computed_event` (the previous kernels have read the device buffer),
+ * and the compute stream for `reuse_downloaded_event` (the previous output
+ * has been read back); NULL otherwise. Records `uploaded_event` on up_stream.
+ *
+ * pkv_stage_download: record `computed_event` on compute_stream (the step's
+ * kernels are enqueued), then copy `bytes` of output to pinned host memory on
+ * `down_stream` after it and record `downloaded_event` there.
+ *
+ * Both are asynchronous and return PKV_OK, PKV_ERR_INVALID_ARG (null buffer or
+ * event, zero bytes) or PKV_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+PKV_API int pkv_stage_upload(const void* host_src, void* dev_dst, size_t bytes, void* up_stream,
+                             void* compute_stream, void* uploaded_event,
+                             void* reuse_computed_event, void* reuse_downloaded_event);
+PKV_API int pkv_stage_download(const void* dev_src, void* host_dst, size_t bytes,
+                               void* compute_stream, void* down_stream, void* computed_event,
+                               void* downloaded_event);
+
 /* Kernels this library has launched in this process so far (all devices and
  * streams; for tracing and for counting the launches of a step). */
 PKV_API unsigned long long pkv_kernel_launches(void);

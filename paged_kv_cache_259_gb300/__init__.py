@@ -93,6 +93,8 @@ def load_library():
         "copy_blocks": (c_int, [vp, vp, vp, c_int, c_int, c_size, vp]),
         "pkv_get_device_error": (c_int, [ip, vp]),
         "pkv_check_wait_timeout": (c_int, [vp]),
+        "pkv_stage_upload": (c_int, [vp, vp, c_size, vp, vp, vp, vp, vp]),
+        "pkv_stage_download": (c_int, [vp, vp, c_size, vp, vp, vp, vp]),
         "bm_create": (vp, [c_int, c_int, i32p, c_int]),
         "bm_destroy": (None, [vp]),
         "bm_add_seq": (c_int, [vp, ctypes.c_int64]),

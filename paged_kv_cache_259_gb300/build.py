@@ -23,6 +23,7 @@ CUDA_SOURCES = [
     "pkv_decode_e4m3.cu",
     "pkv_decode_noalloc.cu",
     "pkv_prefill.cu",
+    "pkv_pipeline.cu",
 ]
 CXX_SOURCES = ["block_manager.cpp"]
 

@@ -21,12 +21,12 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from . import (PKV_ERR_POOL_EXHAUSTED, BlockManager, PagedKVError, bind_copy_blocks,
+from . import (PKV_ERR_POOL_EXHAUSTED, BlockManager, PagedKVError, _check, bind_copy_blocks,
                bind_paged_attention_decode, bind_paged_attention_decode_grouped,
                bind_reshape_and_cache, copy_blocks, paged_attention_decode,
                paged_attention_decode_grouped, paged_attention_prefill,
-               paged_attention_workspace_size, pool_shapes, pool_views, reshape_and_cache,
-               swap_blocks)
+               load_library, paged_attention_workspace_size, pool_shapes, pool_views,
+               reshape_and_cache, swap_blocks)
 
 
 @dataclass
@@ -532,9 +532,23 @@ class StepPipeline:
             self.steps.append((dev["q"], dev["k_new"], dev["v_new"], plan))
         ev = lambda: [torch.cuda.Event() for _ in range(2)]
         self.uploaded, self.computed, self.downloaded = ev(), ev(), ev()
+        for e in self.uploaded + self.computed + self.downloaded:
+            e.record(self.compute)                        # creates the CUDA event now
         self.n = 0
         self._host_views = [self._views(h) for h in self.host_slabs]
         self._bound = [None, None]                        # per slab: (key, bound step)
+        # raw handles for the library's stream plumbing (pkv_stage_upload/download)
+        self._lib = load_library()
+        vp = ctypes.c_void_p
+        self._h = {"up": vp(self.up.cuda_stream), "down": vp(self.down.cuda_stream),
+                   "compute": vp(self.compute.cuda_stream),
+                   "uploaded": [vp(e.cuda_event) for e in self.uploaded],
+                   "computed": [vp(e.cuda_event) for e in self.computed],
+                   "downloaded": [vp(e.cuda_event) for e in self.downloaded],
+                   "host": [vp(t.data_ptr()) for t in self.host_slabs],
+                   "dev": [vp(t.data_ptr()) for t in self.dev_slabs],
+                   "out": [vp(t.data_ptr()) for t in self.outs]}
+        self._slab_size = ctypes.c_size_t(self.slab_bytes)
 
     def _views(self, slab):
         return slab_views(slab, self.layout)
@@ -558,28 +572,31 @@ class StepPipeline:
 
     def submit(self, host_out, scale=None, k_scale=1.0, v_scale=1.0, workspace=None):
         """Run the next step from its filled host views; ``host_out`` = pinned
-        buffer the output is read back into. Returns the step's (uploaded,
-        downloaded) events."""
+        buffer (contiguous, shaped like the output) the output is read back
+        into. Returns the step's (uploaded, downloaded) events. The copies and
+        the stream ordering are two library calls (pkv_stage_upload /
+        pkv_stage_download); step n-2 used the same buffer set, so its events
+        order the reuse."""
         b = self.n % 2
-        out = self.outs[b]
-        if self.n >= 2:
-            self.up.wait_event(self.computed[b])          # step n-2 is done with this slab
-        with torch.cuda.stream(self.up):
-            self.dev_slabs[b].copy_(self.host_slabs[b], non_blocking=True)
-        self.uploaded[b].record(self.up)
-        self.compute.wait_event(self.uploaded[b])
-        if self.n >= 2:
-            self.compute.wait_event(self.downloaded[b])   # step n-2's output was read
-        q, k_new, v_new, plan = self.steps[b]
+        h = self._h
+        reuse = self.n >= 2
+        _check(self._lib.pkv_stage_upload(
+            h["host"][b], h["dev"][b], self._slab_size, h["up"], h["compute"], h["uploaded"][b],
+            h["computed"][b] if reuse else None, h["downloaded"][b] if reuse else None),
+            "pkv_stage_upload")
         if self.run is None:
             self._bound_step(b, scale, k_scale, v_scale, workspace)(self.compute, **self._counts())
         else:
-            self.run(q, k_new, v_new, plan, out, self.compute)
-        self.computed[b].record(self.compute)
-        self.down.wait_event(self.computed[b])
-        with torch.cuda.stream(self.down):
-            host_out.copy_(out, non_blocking=True)
-        self.downloaded[b].record(self.down)
+            q, k_new, v_new, plan = self.steps[b]
+            self.run(q, k_new, v_new, plan, self.outs[b], self.compute)
+        out = self.outs[b]
+        if not (host_out.is_contiguous() and host_out.numel() == out.numel() and
+                host_out.dtype == out.dtype and not host_out.is_cuda):
+            raise ValueError("host_out must be a contiguous CPU tensor shaped like the output")
+        _check(self._lib.pkv_stage_download(
+            h["out"][b], ctypes.c_void_p(host_out.data_ptr()),
+            ctypes.c_size_t(out.numel() * out.element_size()), h["compute"], h["down"],
+            h["computed"][b], h["downloaded"][b]), "pkv_stage_download")
         self.n += 1
         return self.uploaded[b], self.downloaded[b]
 
