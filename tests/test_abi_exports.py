@@ -174,3 +174,20 @@ def test_noalloc_refuses_a_splittable_batch_beyond_its_scratch():
     assert st == -1
     assert lib.paged_attention_workspace_size(65535, 64, 128, 16, 9) > 0
 
+
+
+def test_stage_calls_refuse_missing_buffers_before_any_cuda_call():
+    """pkv_stage_upload / pkv_stage_download check their arguments on the host:
+    a null buffer or event, or zero bytes, is PKV_ERR_INVALID_ARG and nothing
+    reaches the CUDA runtime (so this runs without a GPU)."""
+    lib = library()
+    vp = ctypes.c_void_p
+    some = vp(0x1000)
+    assert lib.pkv_stage_upload(None, some, 64, None, None, some, None, None) == -1
+    assert lib.pkv_stage_upload(some, None, 64, None, None, some, None, None) == -1
+    assert lib.pkv_stage_upload(some, some, 0, None, None, some, None, None) == -1
+    assert lib.pkv_stage_upload(some, some, 64, None, None, None, None, None) == -1
+    assert lib.pkv_stage_download(None, some, 64, None, None, some, some) == -1
+    assert lib.pkv_stage_download(some, some, 64, None, None, None, some) == -1
+    assert lib.pkv_stage_download(some, some, 64, None, None, some, None) == -1
+    assert lib.pkv_stage_download(some, some, 0, None, None, some, some) == -1
