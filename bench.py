@@ -1360,6 +1360,7 @@ def make_workload(args):
               "long_fp8_bs16": lambda B: wl.long_fp8(16, B=B),
               "long_fp8_bs32": lambda B: wl.long_fp8(32, B=B),
               "shared_prefix_bf16": lambda B: wl.shared_prefix_bf16(groups=max(1, B // 4)),
+              "shared_prefix_fork_bf16": lambda B: wl.shared_prefix_bf16(True, groups=max(1, B // 4)),
               "beam_search_bf16": lambda B: wl.beam_search_bf16(requests=max(1, B // 4))}
     if args.config not in scaled:
         raise SystemExit(f"--batch is not supported for {args.config}")
