@@ -46,6 +46,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <climits>
 #include <cmath>
 #include <type_traits>
 
@@ -632,6 +633,7 @@ template <class Math, typename QT, int D, int BS, int G, int NW, bool PREFIX, in
 __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p) {
     using P = Pipe<Math, D, BS, G, NW>;
     constexpr int TILE = P::kTile, ST = P::kStages;
+    static_assert(ST <= 32, "prologue stages are taken from one warp-wide read");
     constexpr int PBS = BS / PAIR;                          // the cache's block size
     constexpr int PTILE = TILE / PAIR;                      // one cache block's tile
     static_assert(PAIR == 1 || (PAIR == 2 && !PREFIX), "paired stages: regular launch only");
@@ -650,35 +652,53 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
     // reads its prompt once and needs no second launch for the members' tails.
     const int part = blockIdx.x, hk = blockIdx.y;
     const int key = (!PREFIX && p.seq_list) ? p.seq_list[blockIdx.z] : (int)blockIdx.z;
-    __shared__ int grp[4 * kMaxMembers + 4];   // b, L, own start, own count per member; P, T
+    // b, L, own start, own count per member; P, T (one copy per warp)
+    __shared__ int grp_all[NW][4 * kMaxMembers + 4];
+    int* grp = grp_all[threadIdx.x >> 5];
     int L = 0, nblk = 0;                       // regular launch: the sequence
     int total;                                 // blocks (or list entries) of this CTA's key
+    int spec = -1, specP = 0;                  // group launch: see below
     if constexpr (PREFIX) {
-        if (threadIdx.x == 0) {
-            int P = max(p.group_prefix[key], 0), n = 0;
-            for (int m = 0; m < kMaxMembers; ++m) {
-                const int sb = m < p.max_members ? p.group_members[(size_t)key * p.max_members + m] : -1;
-                const bool ok = sb >= 0 && sb < p.num_seqs;
-                const int Lm = ok ? min(max(p.seq_lens[sb], 0), p.max_blocks * BS) : 0;
-                grp[4 * m] = ok ? sb : -1;
-                grp[4 * m + 1] = Lm;
-                if (ok) P = min(P, Lm / BS);                // shared blocks are full for all
-                n += ok;
-            }
-            if (n == 0) P = 0;
-            int T = P;
-            for (int m = 0; m < kMaxMembers; ++m) {
-                const bool ok = m < p.max_members && grp[4 * m] >= 0;
-                const int own = ok ? (grp[4 * m + 1] + BS - 1) / BS - P : 0;
-                grp[4 * m + 2] = T;                          // list index of its first own block
-                grp[4 * m + 3] = own;
-                T += own;
-            }
-            grp[4 * kMaxMembers] = P;
-            grp[4 * kMaxMembers + 1] = T;
+        // Every warp reads the group itself (lane m: member m) and keeps its own
+        // copy, so no warp waits for another before its first copies. In the
+        // round trip of the members' lengths it also reads the table entries of
+        // its first 32 list entries that the group's stated prefix covers (the
+        // first member's row, as the list takes them): the shared blocks' ids
+        // are in when the lengths are, one round trip before the list is known.
+        const int ln = threadIdx.x & 31;
+        int sb = -1;
+        if (ln < kMaxMembers && ln < p.max_members)
+            sb = p.group_members[(size_t)key * p.max_members + ln];
+        const int P0 = max(p.group_prefix[key], 0);
+        const bool ok = sb >= 0 && sb < p.num_seqs;
+        const unsigned okm = __ballot_sync(kFull, ok);
+        const int row0 = okm ? __shfl_sync(kFull, sb, __ffs(okm) - 1) : -1;
+        const int j0 = part * p.part_blocks + (int)(threadIdx.x >> 5) + ln * NW;
+        if (row0 >= 0 && j0 < min(P0, p.max_blocks))
+            spec = p.block_tables[(size_t)row0 * p.max_blocks + j0];
+        const int Lm = ok ? min(max(p.seq_lens[sb], 0), p.max_blocks * BS) : 0;
+        // shared blocks are full for every member
+        const int P = okm ? min(P0, __reduce_min_sync(kFull, ok ? Lm / BS : INT_MAX)) : 0;
+        const int own = ok ? (Lm + BS - 1) / BS - P : 0;
+        int incl = own;                                     // members' own blocks, inclusive scan
+#pragma unroll
+        for (int o = 1; o < kMaxMembers; o <<= 1) {
+            const int t = __shfl_up_sync(kFull, incl, o);
+            if (ln >= o) incl += t;
         }
-        __syncthreads();
-        total = grp[4 * kMaxMembers + 1];
+        if (ln < kMaxMembers) {
+            grp[4 * ln] = ok ? sb : -1;
+            grp[4 * ln + 1] = Lm;
+            grp[4 * ln + 2] = P + incl - own;               // list index of its first own block
+            grp[4 * ln + 3] = own;
+        }
+        total = P + __shfl_sync(kFull, incl, kMaxMembers - 1);
+        if (ln == 0) {
+            grp[4 * kMaxMembers] = P;
+            grp[4 * kMaxMembers + 1] = total;
+        }
+        __syncwarp();
+        specP = P;
     } else {
         if (key < 0 || key >= p.num_seqs) {                 // a bad ungrouped-list entry
             if (part == 0 && hk == 0 && threadIdx.x == 0) flag_error(p.err, kErrOutOfRange);
@@ -705,6 +725,9 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
     const bool single = nparts <= 1;                        // the only contributor: write `out`
 
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+    // A split call's merge launch may start once every CTA of this launch has
+    // started; it reads the partials only after this launch has completed.
+    if (p.slots > 1) launch_dependents();
 
     if (lane == 0) {
 #pragma unroll
@@ -813,8 +836,18 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
     // uses only its own barriers and ring)
     const int pro = nk < ST ? nk : ST;
     for (int kk = 0; kk < pro; ++kk) {
-        int info, id2;
-        const int id = get_id(kk, &info, &id2);
+        int info, id2, id;
+        if (PREFIX && blk0 + w + kk * NW < specP) {          // a shared block: read with the lengths
+            id = __shfl_sync(kFull, spec, kk);
+            if (id < 0 || id >= p.num_blocks) {
+                if (lane == 0) flag_error(p.err, kErrOutOfRange);
+                id = -1;
+            }
+            info = BS | (all_rows << 8);
+            id2 = -1;
+        } else {
+            id = get_id(kk, &info, &id2);
+        }
         if (lane == 0) issue(kk, id, id2, info);
     }
 
@@ -943,6 +976,10 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const Params p, int B
         nparts = ((L + BS - 1) / BS + p.part_blocks - 1) / p.part_blocks;
     }
     if (nparts <= 1) return;                               // written by the decode kernel
+    // Launched as a programmatic dependent of the decode launch (see
+    // launch_merge): everything above was written before that launch began;
+    // the partials below only after it has completed.
+    wait_prerequisites();
     const size_t base = ((size_t)b * p.num_heads + h) * p.slots;
     const float* ml = p.ws_ml + 2 * base;
     const float* wo = p.ws_o + base * D;
@@ -986,6 +1023,29 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const Params p, int B
 }
 
 // ----------------------------------------------------------------- host launch
+// The merge of a split call, launched right behind the decode launch(es) of
+// the same call as a programmatic dependent: its CTAs may be scheduled (and
+// read the lengths and groups) while the decode's last CTAs still run, and
+// wait_prerequisites() holds every read of the partials until the decode
+// launch has completed and its writes are visible.
+template <typename QT, int D>
+int launch_merge(const Params& p, int BS, int max_len, cudaStream_t stream) {
+    note_launch();
+    const unsigned rows = (unsigned)p.num_seqs * p.num_heads;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((rows + 7) / 8);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, split_reduce_kernel<QT, D>, p, BS, max_len);
+    return e == cudaSuccess ? PKV_OK : cuda_fail("decode: split merge launch", e);
+}
+
 struct Args {
     void* out;
     const void* q;
@@ -1097,14 +1157,7 @@ int launch_paired(const Args& a) {
     st = launch_kernel<Math, QT, D, BS, G, false, 2>(p, dim3(parts, a.num_kv_heads, a.num_seqs),
                                                       a.stream);
     if (st != PKV_OK) return st;
-    if (split) {
-        note_launch();
-        const unsigned rows = (unsigned)a.num_seqs * a.num_heads;
-        split_reduce_kernel<QT, D><<<(rows + 7) / 8, 256, 0, a.stream>>>(p, BS,
-                                                                         a.max_blocks * (BS / 2));
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_fail("decode: split merge launch", e);
-    }
+    if (split) return launch_merge<QT, D>(p, BS, a.max_blocks * (BS / 2), a.stream);
     return PKV_OK;
 }
 
@@ -1210,13 +1263,7 @@ int launch_variant(const Args& a) {
         st = launch_kernel<Math, QT, D, BS, G, false>(p, dim3(parts, a.num_kv_heads, n_regular), a.stream);
         if (st != PKV_OK) return st;
     }
-    if (split) {
-        note_launch();
-        const unsigned rows = (unsigned)a.num_seqs * a.num_heads;
-        split_reduce_kernel<QT, D><<<(rows + 7) / 8, 256, 0, a.stream>>>(p, BS, a.max_blocks * BS);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_fail("decode: split merge launch", e);
-    }
+    if (split) return launch_merge<QT, D>(p, BS, a.max_blocks * BS, a.stream);
     return PKV_OK;
 }
 

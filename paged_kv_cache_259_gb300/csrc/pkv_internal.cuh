@@ -62,6 +62,18 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
+// Programmatic dependent launch. launch_dependents: a launch queued behind
+// this one with programmatic stream serialisation may start once every CTA of
+// this launch has executed it (or exited). wait_prerequisites: block until the
+// launches this one depends on have completed and their memory is visible (a
+// no-op for a launch made without that attribute).
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_prerequisites() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }

@@ -172,6 +172,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
     const int qtile = gridDim.x - 1 - blockIdx.x;
     const int G = p.G;
     const int tok_per_tile = kRows / G;
+    // The loaders read the first two 32-entry windows of the table row before
+    // the lengths (the row has max_blocks entries whatever the length), so the
+    // first copies need one round trip less; entries past the sequence are
+    // ignored as before.
+    int pre_ids0 = 0, pre_ids1 = 0;
+    if (warp == kKLoadWarp || warp == kVLoadWarp) {
+        const int32_t* row = p.block_tables + (size_t)b * p.max_blocks;
+        if (lane < p.max_blocks) pre_ids0 = row[lane];
+        if (32 + lane < p.max_blocks) pre_ids1 = row[32 + lane];
+    }
     const int L = p.seq_lens[b];
     const int q0 = p.query_start[b];
     const int C = p.query_start[b + 1] - q0;
@@ -311,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
             fence_mbar_init();
         }
         __syncwarp();
-        win_ids = check_id(lane, lane < p.max_blocks ? bt[lane] : 0);
-        next_ids = check_id(32 + lane, 32 + lane < p.max_blocks ? bt[32 + lane] : 0);
+        win_ids = check_id(lane, pre_ids0);
+        next_ids = check_id(32 + lane, pre_ids1);
         for (int j = 0; j < min(2, n_tiles) && load_ok; ++j) load_ok = load_tile(j);
     }
     tc::fence_before_sync();
