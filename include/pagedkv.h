@@ -135,11 +135,15 @@ PKV_API const char* pkv_last_error_string(void);
  * Supported: head_dim in {64,128}, block_size in {16,32}, G in {1,2,4,8}.
  * A table entry outside [0, num_blocks) is skipped (its tokens get zero
  * weight) and sets the device error word to PKV_ERR_OUT_OF_RANGE.
- * Launches: the decode kernel, then (when it split) the merge, which is
- * launched with programmatic stream serialisation right behind it: its CTAs
- * may start while the decode's last CTAs run, and it reads the partials only
- * after the decode launch has completed. Stream order with respect to the
- * caller's other work is unchanged.
+ * Launches: the decode kernel, then (when it split) the merge. Both, like
+ * the kernels of reshape_and_cache and copy_blocks, are launched with
+ * programmatic stream serialisation: a kernel's CTAs may be scheduled while the
+ * previous launch in the stream finishes, but each waits for that launch (and
+ * so for all earlier work in the stream) to complete before touching memory,
+ * the merge excepted, which reads only the lengths and groups before that
+ * wait. A kernel the caller launches next with programmatic serialisation must
+ * itself wait (griddepcontrol.wait) before reading these outputs; stream order
+ * for every other kind of work is unchanged.
  * ---------------------------------------------------------------------- */
 PKV_API int paged_attention_decode(void* out, const void* q,
                            const void* k_pool, const void* v_pool,

@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const ST* __restrict__ k, const ST* __restrict__ v, CT* __restrict__ k_pool,
     CT* __restrict__ v_pool, const int64_t* __restrict__ slots, int num_tokens, int hkv, int d,
     int bs, int num_blocks, float k_scale, float v_scale, int* err) {
+    pdl_enter();                                           // launched with launch_pdl
     using CC = ChunkConvert<ST, CT>;
     const int planes = d / CC::CV;                         // 16-byte groups per (token, head)
     const long long per_pool = (long long)num_tokens * hkv * planes;
@@ -136,6 +137,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_bf16_windows(
     const uint4* __restrict__ k, const uint4* __restrict__ v, uint4* __restrict__ k_pool,
     uint4* __restrict__ v_pool, const int64_t* __restrict__ slots, int num_tokens, int hkv,
     int d_rt, int bs, int num_blocks, int* err) {
+    pdl_enter();                                           // launched with launch_pdl
     const int d = DT ? DT : d_rt;
     const int planes = d / 8;                              // 16-byte chunks per (token, head)
     const int lane = threadIdx.x & 31;
@@ -220,6 +222,7 @@ constexpr int kCopyCheckPairs = 4096;
 __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
     char* __restrict__ k_pool, char* __restrict__ v_pool, const int64_t* __restrict__ pairs,
     int num_pairs, int num_blocks, size_t block_bytes, int* err) {
+    pdl_enter();                                           // launched with launch_pdl
     const int pair = blockIdx.x >> 1;
     char* pool = (blockIdx.x & 1) ? v_pool : k_pool;
     const int64_t src = pairs[2 * pair], dst = pairs[2 * pair + 1];
@@ -265,10 +268,10 @@ cudaError_t launch_reshape(const void* k, const void* v, void* kp, void* vp, con
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     note_launch();
-    reshape_and_cache_kernel<ST, CT><<<(unsigned)blocks, threads, 0, stream>>>(
-        static_cast<const ST*>(k), static_cast<const ST*>(v), static_cast<CT*>(kp),
-        static_cast<CT*>(vp), slots, num_tokens, hkv, d, bs, num_blocks, ks, vs, err);
-    return cudaGetLastError();
+    return launch_pdl(reshape_and_cache_kernel<ST, CT>, dim3((unsigned)blocks), dim3(threads), 0,
+                      stream, static_cast<const ST*>(k), static_cast<const ST*>(v),
+                      static_cast<CT*>(kp), static_cast<CT*>(vp), slots, num_tokens, hkv, d, bs,
+                      num_blocks, ks, vs, err);
 }
 
 // Block copies between two pools (device or pinned host memory, both reached by
@@ -334,10 +337,10 @@ cudaError_t launch_reshape_groups(const void* k, const void* v, void* kp, void* 
     auto kern = d == 128 ? reshape_and_cache_bf16_windows<128>
                          : d == 64 ? reshape_and_cache_bf16_windows<64>
                                    : reshape_and_cache_bf16_windows<0>;
-    kern<<<(unsigned)blocks, threads, 0, stream>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(kp),
-        static_cast<uint4*>(vp), slots, num_tokens, hkv, d, bs, num_blocks, err);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(threads), 0, stream,
+                      static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+                      static_cast<uint4*>(kp), static_cast<uint4*>(vp), slots, num_tokens, hkv, d,
+                      bs, num_blocks, err);
 }
 
 }  // namespace
@@ -407,10 +410,10 @@ int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs, int nu
     const unsigned chunks = (unsigned)((block_bytes + kCopyChunkBytes - 1) / kCopyChunkBytes);
     dim3 grid(2u * (unsigned)num_pairs, chunks);
     note_launch();
-    copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<char*>(k_pool), static_cast<char*>(v_pool), src_dst_pairs, num_pairs,
-        num_blocks, block_bytes, err);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(copy_blocks_kernel, grid, dim3(kCopyThreads), 0,
+                                     static_cast<cudaStream_t>(stream), static_cast<char*>(k_pool),
+                                     static_cast<char*>(v_pool), src_dst_pairs, num_pairs,
+                                     num_blocks, block_bytes, err);
     return e == cudaSuccess ? PKV_OK : cuda_fail("copy_blocks: kernel launch", e);
 }
 

@@ -638,6 +638,7 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
     constexpr int PTILE = TILE / PAIR;                      // one cache block's tile
     static_assert(PAIR == 1 || (PAIR == 2 && !PREFIX), "paired stages: regular launch only");
 
+    pdl_enter();                                            // launched with launch_pdl
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::kBarOff);
@@ -725,9 +726,6 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
     const bool single = nparts <= 1;                        // the only contributor: write `out`
 
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-    // A split call's merge launch may start once every CTA of this launch has
-    // started; it reads the partials only after this launch has completed.
-    if (p.slots > 1) launch_dependents();
 
     if (lane == 0) {
 #pragma unroll
@@ -980,6 +978,7 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const Params p, int B
     // launch_merge): everything above was written before that launch began;
     // the partials below only after it has completed.
     wait_prerequisites();
+    launch_dependents();
     const size_t base = ((size_t)b * p.num_heads + h) * p.slots;
     const float* ml = p.ws_ml + 2 * base;
     const float* wo = p.ws_o + base * D;
@@ -1114,8 +1113,7 @@ int launch_kernel(const Params& p, dim3 grid, cudaStream_t stream) {
     const int st = kernel_setup(reinterpret_cast<const void*>(kern), P::kSmem, kNumWarps * 32, &occ);
     if (st != PKV_OK) return st;
     note_launch();
-    kern<<<grid, kNumWarps * 32, P::kSmem, stream>>>(p);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(kern, grid, dim3(kNumWarps * 32), P::kSmem, stream, p);
     return e == cudaSuccess ? PKV_OK : cuda_fail("decode: kernel launch", e);
 }
 
