@@ -1,5 +1,6 @@
 """Benchmark: one decode step of paged attention (copy_blocks -> reshape_and_cache ->
-paged_attention_decode) on a seeded synthetic workload, timed on the GPU.
+paged_attention_decode, as one paged_decode_step call) on a seeded synthetic
+workload, timed on the GPU.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
 
@@ -9,7 +10,8 @@ same metric through the engine (``LiveDecodePipeline``): every step is planned
 on the host by the native block manager straight into a pinned slab, the slab
 is uploaded and the output read back inside the timed region, overlapped with
 the neighbouring steps. ``roofline`` covers the decode attention op alone (its
-kernel plus the split-KV merge), timed with CUDA events on its stream.
+kernel plus the split-KV merge), timed with CUDA events on its stream in a
+second pass of the same steps made as separate calls.
 ``cpu_baseline`` times the CPU oracle on a bounded sample of the same workload,
 and ``check`` compares the timed steps' output with the oracle rows that run
 computed first. The default workload's line also carries ``others``: every
@@ -395,16 +397,25 @@ def build_state(w, device):
 
 
 def time_steps(cache, dev, qd, kd, vd, out, w, ks, vs, ws, K, stream, has_copy):
-    """K device-resident steps (copy_blocks when the step has CoW pairs,
-    reshape_and_cache, decode), back to back on ``stream``. Returns the whole
-    time (ms), each step's decode-op time (ms, CUDA events on the stream) and the
-    library's launches."""
+    """K device-resident steps, twice, back to back on ``stream``. First as one
+    ``paged_decode_step`` call each (copy_blocks when the step has CoW pairs,
+    reshape_and_cache and the decode; the decode reads every block but the
+    sequences' last ones while the writes finish): returns that pass's whole time
+    (ms) and the library's launches in it. Then as separate calls with CUDA
+    events around each step's decode op: returns its time per step (ms), the
+    roofline's kernel time."""
     import paged_kv_cache_259_gb300 as pkv
-    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(K)]
+    run = cache.bind_step(qd, kd, vd, dev, out, w.scale, ks, vs, ws)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = pkv.kernel_launches()
     t_start.record(stream)
+    for _ in range(K):
+        run(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = pkv.kernel_launches() - launches0
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
     for i in range(K):
         if has_copy:
             pkv.copy_blocks(cache.k_pool, cache.v_pool, dev["pairs"], stream=stream)
@@ -412,9 +423,7 @@ def time_steps(cache, dev, qd, kd, vd, out, w, ks, vs, ws, K, stream, has_copy):
         ev_dec[i][0].record(stream)
         cache.decode(qd, dev, out, w.scale, ks, vs, ws, stream=stream)
         ev_dec[i][1].record(stream)
-    t_end.record(stream)
     torch.cuda.synchronize()
-    launches = pkv.kernel_launches() - launches0
     return (t_start.elapsed_time(t_end), np.array([a.elapsed_time(b) for a, b in ev_dec]),
             launches)
 
@@ -1521,8 +1530,8 @@ def main():
             "dtype": w.kv_dtype, "data": "synthetic",
             "config": {
                 "workload": workload_desc(w),
-                "step": ("copy_blocks (CoW pairs: %d) + reshape_and_cache + %s; %d kernel "
-                         "launches per step" % (
+                "step": ("paged_decode_step: copy_blocks (CoW pairs: %d) + reshape_and_cache + "
+                         "%s; %d kernel launches per step" % (
                              len(plan.pairs),
                              "paged_attention_decode_grouped (%d prefix groups)" % r["groups"]
                              if r["groups"] else "paged_attention_decode",

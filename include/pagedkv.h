@@ -207,6 +207,40 @@ PKV_API int paged_attention_decode_grouped(void* out, const void* q,
                                    const int32_t* ungrouped_seqs, int num_ungrouped,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * paged_decode_step -- one decode step in one call: the step's copy-on-write
+ * block copies, the slot write of every sequence's new token, then decode
+ * attention (glossary "Cách phân trang hoạt động": a new token's K/V goes into
+ * the sequence's last block, then the kernel reads every block back through the
+ * table; "Chia sẻ block giữa các chuỗi": a write into a shared block copies it
+ * first). The result is that of
+ *     copy_blocks(k_pool, v_pool, src_dst_pairs, num_pairs, num_blocks, block bytes);
+ *     reshape_and_cache(k_new, v_new, k_pool, v_pool, slot_mapping, num_seqs, ...,
+ *                       q_dtype as the source dtype, kv_dtype as the cache dtype);
+ *     paged_attention_decode_grouped(...)   (paged_attention_decode if num_groups == 0)
+ * with the same arguments, k_new / v_new [num_seqs][num_kv_heads][head_dim] of
+ * dtype q_dtype and slot_mapping int64 [num_seqs] (one new token per sequence).
+ * Precondition (bm_append_slots and bm_plan_decode meet it): slot_mapping[b] is
+ * sequence b's newest position, so the slot writes change only the sequences'
+ * last blocks. The decode kernel then starts reading every other block while the
+ * copies and slot writes finish, and waits for them only before it reads a
+ * sequence's last block (the copies are complete by then too). A slot outside
+ * that precondition may be read before it is written.
+ * Errors: those of the three calls; argument errors come before any launch.
+ * ---------------------------------------------------------------------- */
+PKV_API int paged_decode_step(const int64_t* src_dst_pairs, int num_pairs, const void* k_new,
+                              const void* v_new, const int64_t* slot_mapping, void* out,
+                              const void* q, void* k_pool, void* v_pool,
+                              const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                              int max_blocks_per_seq, int num_blocks, int num_heads,
+                              int num_kv_heads, int head_dim, int block_size, float scale,
+                              int q_dtype, int kv_dtype, float k_scale, float v_scale,
+                              const int32_t* seq_group, const int32_t* group_members,
+                              const int32_t* group_prefix_blocks, int num_groups, int max_members,
+                              int max_group_blocks, const int32_t* ungrouped_seqs,
+                              int num_ungrouped, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
 /* Bytes of workspace that lets paged_attention_decode use its finest split for
  * these sizes (an upper bound; any size works, smaller ones split less). A
  * grouped call splits long group lists too when it has max_members times this. */

@@ -27,7 +27,7 @@ __all__ = [
     "paged_attention_prefill", "swap_blocks",
     "reshape_and_cache", "copy_blocks", "get_device_error", "check_wait_timeout",
     "BoundCall", "bind_paged_attention_decode", "bind_paged_attention_decode_grouped",
-    "bind_reshape_and_cache", "bind_copy_blocks",
+    "bind_reshape_and_cache", "bind_copy_blocks", "paged_decode_step", "bind_paged_decode_step",
     "kernel_launches", "BlockManager",
     "library_path", "load_library", "pool_shapes", "pool_views", "pools_from_views", "PKV_F32",
     "PKV_BF16", "PKV_E4M3", "PKV_ERR_POOL_EXHAUSTED",
@@ -79,6 +79,10 @@ def load_library():
                                                    c_int, c_int, c_int, c_int, c_float, c_int,
                                                    c_int, c_float, c_float, vp, vp, vp, c_int,
                                                    c_int, c_int, vp, c_int, vp, c_size, vp]),
+        "paged_decode_step": (c_int, [vp, c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, c_int, c_int,
+                                      c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_int,
+                                      c_float, c_float, vp, vp, vp, c_int, c_int, c_int, vp,
+                                      c_int, vp, c_size, vp]),
         "bm_prefix_groups": (c_int, [vp, i64p, c_int, c_int, i32p, i32p, i32p, i32p, ip]),
         "bm_plan_decode": (c_int, [vp, i64p, c_int, c_int, i64p, i64p, ip, i32p, i32p, c_int, i32p,
                                    i32p, i32p, i32p, i32p, ip, ip, ip]),
@@ -366,6 +370,81 @@ def bind_paged_attention_decode_grouped(out, q, k_pool, v_pool, block_tables, se
         counts["num_ungrouped"] = (25, n_un)
     return BoundCall(lib.paged_attention_decode_grouped, args, "paged_attention_decode_grouped",
                      dev, counts)
+
+
+def paged_decode_step(out, q, k_new, v_new, k_pool, v_pool, block_tables, seq_lens,
+                      slot_mapping, src_dst_pairs, scale, k_scale=1.0, v_scale=1.0,
+                      workspace=None, stream=None, seq_group=None, group_members=None,
+                      group_prefix_blocks=None, ungrouped=None, max_group_blocks=0):
+    """One decode step in one call: the copy-on-write pairs, the slot write of
+    every sequence's new token (k_new / v_new ``[B, Hkv, D]`` like q, slot_mapping
+    int64 ``[B]``: sequence b's newest position) and the attention, grouped when
+    the group tensors are given (as ``paged_attention_decode_grouped`` takes
+    them). The decode reads every block but the sequences' last ones while the
+    copies and slot writes finish."""
+    bind_paged_decode_step(out, q, k_new, v_new, k_pool, v_pool, block_tables, seq_lens,
+                           slot_mapping, src_dst_pairs, scale, k_scale, v_scale, workspace,
+                           seq_group, group_members, group_prefix_blocks, ungrouped,
+                           max_group_blocks)(stream)
+    return out
+
+
+def bind_paged_decode_step(out, q, k_new, v_new, k_pool, v_pool, block_tables, seq_lens,
+                           slot_mapping, src_dst_pairs, scale, k_scale=1.0, v_scale=1.0,
+                           workspace=None, seq_group=None, group_members=None,
+                           group_prefix_blocks=None, ungrouped=None, max_group_blocks=0):
+    """``paged_decode_step`` checked once and bound to these tensors
+    (``BoundCall``). ``src_dst_pairs`` and the group tensors may be sized for the
+    most a step can raise: each call may then pass ``num_pairs``, ``num_groups``,
+    ``max_group_blocks`` and ``num_ungrouped`` for the rows actually filled
+    (``num_groups=0``: the plain decode)."""
+    lib = load_library()
+    B, Hq, D, NB, Hkv, bs = _decode_shapes(out, q, k_pool, v_pool, block_tables, seq_lens)
+    named = [(k_new, "k_new"), (v_new, "v_new"), (slot_mapping, "slot_mapping"),
+             (src_dst_pairs, "src_dst_pairs")]
+    grouped = group_members is not None
+    if grouped:
+        named += [(seq_group, "seq_group"), (group_members, "group_members"),
+                  (group_prefix_blocks, "group_prefix_blocks")]
+        if ungrouped is not None:
+            named.append((ungrouped, "ungrouped"))
+    _tensors(named)
+    if tuple(k_new.shape) != (B, Hkv, D) or v_new.shape != k_new.shape or \
+            k_new.dtype != q.dtype or v_new.dtype != q.dtype:
+        raise ValueError("k_new and v_new must be [B, Hkv, D] in the dtype of q")
+    if slot_mapping.dtype != torch.int64 or tuple(slot_mapping.shape) != (B,):
+        raise ValueError("slot_mapping must be int64 [B]")
+    if src_dst_pairs.dtype != torch.int64 or src_dst_pairs.dim() != 2 or \
+            src_dst_pairs.shape[1] != 2:
+        raise ValueError("src_dst_pairs must be int64 [P, 2]")
+    if grouped:
+        for t, n in named[4:]:
+            if t.dtype != torch.int32:
+                raise TypeError(f"{n} must be int32")
+        if tuple(seq_group.shape) != (B,) or group_members.dim() != 2 or \
+                tuple(group_prefix_blocks.shape) != (group_members.shape[0],) or \
+                (ungrouped is not None and ungrouped.dim() != 1):
+            raise ValueError("inconsistent shapes: seq_group [B], group_members [G, max_members], "
+                             "group_prefix_blocks [G], ungrouped [n]")
+    dev = _on_gpu([(out, "out"), (q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"),
+                   (block_tables, "block_tables"), (seq_lens, "seq_lens")] + named)
+    ws_ptr, ws_bytes = _workspace(workspace, dev)
+    P = src_dst_pairs.shape[0]
+    G = group_members.shape[0] if grouped else 0
+    M = group_members.shape[1] if grouped else 0
+    n_un = -1 if ungrouped is None else ungrouped.numel()
+    args = [_ptr(src_dst_pairs), ctypes.c_int(P), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+            _ptr(out), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(seq_lens)]
+    args += _c_args([B, block_tables.shape[1], NB, Hq, Hkv, D, bs, float(scale), _dt(q, "q"),
+                     _dt(k_pool, "k_pool"), float(k_scale), float(v_scale)])
+    args += [_ptr(seq_group if grouped else None), _ptr(group_members if grouped else None),
+             _ptr(group_prefix_blocks if grouped else None)]
+    args += _c_args([G, M, int(max_group_blocks)])
+    args += [_ptr(ungrouped), ctypes.c_int(n_un), ctypes.c_void_p(ws_ptr), ctypes.c_size_t(ws_bytes)]
+    counts = {"num_pairs": (1, P), "num_groups": (26, G), "max_group_blocks": (28, 2 ** 31 - 1)}
+    if ungrouped is not None:
+        counts["num_ungrouped"] = (30, n_un)
+    return BoundCall(lib.paged_decode_step, args, "paged_decode_step", dev, counts)
 
 
 # scratch bytes of paged_attention_decode_noalloc (PKV_NOALLOC_WORKSPACE_BYTES)

@@ -107,6 +107,10 @@ struct Params {
     int group_part_blocks;         // partition size of the group launch
     int group_parts;               // partitions the group launch has (its grid x)
     int slots;                     // workspace slots per (sequence, head)
+    // Launched right behind this call's own block copies and slot writes, which
+    // change only the sequences' last blocks: wait for them only before the
+    // copy of an entry holding a last block (see paged_decode_step).
+    int defer;
 };
 
 template <typename T> struct Elt;
@@ -638,7 +642,11 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
     constexpr int PTILE = TILE / PAIR;                      // one cache block's tile
     static_assert(PAIR == 1 || (PAIR == 2 && !PREFIX), "paired stages: regular launch only");
 
-    pdl_enter();                                            // launched with launch_pdl
+    // launched with launch_pdl: wait for the previous launch before touching
+    // memory, unless it is this call's own step writes (p.defer: then each warp
+    // waits before copying an entry that holds a sequence's last block)
+    if (p.defer) launch_dependents();
+    else pdl_enter();
     extern __shared__ __align__(128) unsigned char smem[];
     unsigned char* ring = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P::kBarOff);
@@ -733,12 +741,17 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
         fence_mbar_init();
     }
     const int nk = nbp > w ? (nbp - w + NW - 1) / NW : 0;  // this warp's blocks
+    // regular launch: this warp's entry holding the sequence's last block, or -1
+    const int last_rel = nblk - 1 - blk0 - w;
+    const int last_kk = (!PREFIX && last_rel >= 0 && last_rel % NW == 0) ? last_rel / NW : -1;
     const uint64_t pol = l2_evict_first();
     const int gh = p.num_heads / p.num_kv_heads;
     const int all_rows = G >= 32 ? -1 : (1 << G) - 1;
 
-    // block id and (ntok | live rows << 8) of the warp's kk-th entry; with paired
-    // stages also the id of the entry's second block (-1 past the sequence)
+    // block id and (ntok | live rows << 8 | group launch: holds a member's last
+    // block << 30) of the warp's kk-th entry; with paired stages also the id of
+    // the entry's second block (-1 past the sequence)
+    constexpr int kLastBit = 1 << 30;
     auto entry = [&](int kk, int* info, int* id2) -> int {
         const int j = blk0 + w + kk * NW;
         int row, blk, ntok, live;
@@ -757,6 +770,7 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
                 blk = P + (j - grp[4 * m + 2]);
                 ntok = min(BS, grp[4 * m + 1] - blk * BS);
                 live = ((1 << gh) - 1) << (m * gh);
+                if (blk == (grp[4 * m + 1] + BS - 1) / BS - 1) live |= kLastBit >> 8;
             }
         } else {
             row = key;
@@ -811,8 +825,10 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
     auto issue = [&](int kk, int id, int id2, int info) {   // lane 0 only
         const int s = kk % ST;
         const uint32_t bar = smem_addr(&bars[w * ST + s]);
+        // this step's slot writes land in the sequences' last blocks only
+        if (p.defer && (PREFIX ? (info & kLastBit) != 0 : kk == last_kk)) wait_prerequisites();
         stage_id[w * ST + s] = id;
-        if constexpr (PREFIX) stage_info[w * ST + s] = info;
+        if constexpr (PREFIX) stage_info[w * ST + s] = info & ~kLastBit;
         if (id >= 0) {
             const uint32_t dst = smem_addr(ring + (size_t)((w * ST + s) * 2) * TILE);
             const size_t off = ((size_t)id * p.num_kv_heads + hk) * PTILE;
@@ -1066,6 +1082,7 @@ struct Args {
     const int32_t* group_prefix;
     int num_groups, max_members;
     int max_group_blocks;          // longest group list (prefix + own blocks), <= 0: unknown
+    int defer = 0;                 // see Params::defer
 };
 
 constexpr int kNumWarps = PKV_DECODE_WARPS;
@@ -1149,6 +1166,7 @@ int launch_paired(const Args& a) {
     p.qscale = a.scale * a.k_scale * kLog2e;
     p.v_scale = a.v_scale;
     p.slots = parts;
+    p.defer = a.defer;
     const bool split = parts > 1;
     p.ws_o = split ? static_cast<float*>(a.workspace) : nullptr;
     p.ws_ml = split ? p.ws_o + (size_t)a.num_seqs * a.num_heads * parts * D : nullptr;
@@ -1240,6 +1258,7 @@ int launch_variant(const Args& a) {
     p.group_part_blocks = gPB;
     p.group_parts = gparts;
     p.slots = slots;
+    p.defer = a.defer;
     const bool split = slots > 1;
     p.ws_o = split ? static_cast<float*>(a.workspace) : nullptr;
     p.ws_ml = split ? p.ws_o + (size_t)a.num_seqs * a.num_heads * slots * D : nullptr;
@@ -1251,6 +1270,7 @@ int launch_variant(const Args& a) {
             st = launch_kernel<MmaMath<KV, D, BS, kPrefixRows>, QT, D, BS, kPrefixRows, true>(
                 pg, dim3(gparts, a.num_kv_heads, a.num_groups), a.stream);
             if (st != PKV_OK) return st;
+            p.defer = 0;                                     // the next launch waits for this one
         }
     }
     // sequences of no group (all of them, or the caller's list in a grouped call)

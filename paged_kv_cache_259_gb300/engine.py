@@ -21,9 +21,8 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from . import (PKV_ERR_POOL_EXHAUSTED, BlockManager, PagedKVError, _check, bind_copy_blocks,
-               bind_paged_attention_decode, bind_paged_attention_decode_grouped,
-               bind_reshape_and_cache, copy_blocks, paged_attention_decode,
+from . import (PKV_ERR_POOL_EXHAUSTED, BlockManager, PagedKVError, _check,
+               bind_paged_decode_step, copy_blocks, paged_attention_decode,
                paged_attention_decode_grouped, paged_attention_prefill,
                load_library, paged_attention_workspace_size, pool_shapes, pool_views,
                reshape_and_cache, swap_blocks)
@@ -416,51 +415,37 @@ class PagedKVCache:
                   workspace=None):
         """``step`` checked once and bound to these tensors: returns ``run(stream,
         num_pairs=None, groups=None)`` that launches the step's copies, slot
-        writes and attention. ``num_pairs`` (default: every row of the plan's
-        pairs) counts the filled rows of a pairs buffer sized for the most a step
-        can raise; with a grouped plan, ``groups = (num_groups, max_group_blocks,
-        num_ungrouped)`` counts the filled rows of its group buffers (0 groups:
-        the plain decode)."""
-        pairs = dev_plan["pairs"]
-        cp = bind_copy_blocks(self.k_pool, self.v_pool, pairs) if pairs.shape[0] else None
-        rc = bind_reshape_and_cache(k_new, v_new, self.k_pool, self.v_pool, dev_plan["slots"],
-                                    k_scale, v_scale)
-        plain = bind_paged_attention_decode(out, q, self.k_pool, self.v_pool, dev_plan["tables"],
-                                            dev_plan["lens"], scale, k_scale, v_scale, workspace)
-        grouped = None
-        if "group_members" in dev_plan:
-            grouped = bind_paged_attention_decode_grouped(
-                out, q, self.k_pool, self.v_pool, dev_plan["tables"], dev_plan["lens"], scale,
-                dev_plan["seq_group"], dev_plan["group_members"], dev_plan["group_prefix"],
-                k_scale, v_scale, workspace, dev_plan.get("ungrouped"),
-                dev_plan.get("max_group_blocks", 0))
-        n_all = pairs.shape[0]
+        writes and attention (one ``paged_decode_step`` call). ``num_pairs``
+        (default: every row of the plan's pairs) counts the filled rows of a pairs
+        buffer sized for the most a step can raise; with a grouped plan, ``groups
+        = (num_groups, max_group_blocks, num_ungrouped)`` counts the filled rows
+        of its group buffers (0 groups: the plain decode)."""
+        grouped = "group_members" in dev_plan
+        call = bind_paged_decode_step(
+            out, q, k_new, v_new, self.k_pool, self.v_pool, dev_plan["tables"], dev_plan["lens"],
+            dev_plan["slots"], dev_plan["pairs"], scale, k_scale, v_scale, workspace,
+            dev_plan.get("seq_group"), dev_plan.get("group_members"),
+            dev_plan.get("group_prefix"), dev_plan.get("ungrouped") if grouped else None,
+            dev_plan.get("max_group_blocks", 0) if grouped else 0)
 
         def run(stream, num_pairs=None, groups=None):
-            n = n_all if num_pairs is None else num_pairs
-            if n:
-                cp(stream, num_pairs=n)
-            rc(stream)
-            if grouped is None:
-                plain(stream)
-            elif groups is None:
-                grouped(stream)
-            elif groups[0] == 0:
-                plain(stream)
-            else:
+            counts = {}
+            if num_pairs is not None:
+                counts["num_pairs"] = num_pairs
+            if grouped and groups is not None:
                 ng, mgb, nu = groups
-                grouped(stream, num_groups=ng, max_group_blocks=mgb, num_ungrouped=nu)
+                counts.update(num_groups=ng, max_group_blocks=mgb)
+                if dev_plan.get("ungrouped") is not None:
+                    counts["num_ungrouped"] = nu
+            call(stream, **counts)
         return run
 
     def step(self, q, k_new, v_new, dev_plan, out, scale, k_scale=1.0, v_scale=1.0,
              workspace=None, stream=None):
-        """The device half of a decode step: copies, slot writes, attention."""
-        pairs = dev_plan["pairs"]
-        if pairs.shape[0]:
-            copy_blocks(self.k_pool, self.v_pool, pairs, stream=stream)
-        reshape_and_cache(k_new, v_new, self.k_pool, self.v_pool, dev_plan["slots"],
-                          k_scale, v_scale, stream=stream)
-        return self.decode(q, dev_plan, out, scale, k_scale, v_scale, workspace, stream)
+        """The device half of a decode step: copies, slot writes, attention (one
+        ``paged_decode_step`` call)."""
+        self.bind_step(q, k_new, v_new, dev_plan, out, scale, k_scale, v_scale, workspace)(stream)
+        return out
 
 
 def slab_layout(templates, align=256):

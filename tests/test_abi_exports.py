@@ -191,3 +191,30 @@ def test_stage_calls_refuse_missing_buffers_before_any_cuda_call():
     assert lib.pkv_stage_download(some, some, 64, None, None, None, some) == -1
     assert lib.pkv_stage_download(some, some, 64, None, None, some, None) == -1
     assert lib.pkv_stage_download(some, some, 0, None, None, some, some) == -1
+
+
+def test_decode_step_refuses_bad_arguments_before_any_launch():
+    """paged_decode_step checks every argument on the host before it launches
+    anything (so these run without a GPU): negative counts, group arrays
+    missing, an ungrouped list longer than the batch, decode arguments the
+    plain decode refuses (query heads not a multiple of the kv heads), a missing
+    slot mapping; an empty step is a no-op."""
+    lib = library()
+    vp = ctypes.c_void_p
+    some = vp(0x1000)
+
+    def step(pairs=None, num_pairs=0, k=some, v=some, slots=some, B=4, Hq=4, Hkv=4,
+             groups=(None, None, None, 0, 0), ungrouped=(None, -1)):
+        sg, gm, gp, ng, mm = groups
+        return lib.paged_decode_step(pairs, num_pairs, k, v, slots, some, some, some, some, some,
+                                     some, B, 8, 64, Hq, Hkv, 64, 16, 0.1, 1, 1, 1.0, 1.0,
+                                     sg, gm, gp, ng, mm, 0, ungrouped[0], ungrouped[1], None, 0,
+                                     None)
+
+    assert step(num_pairs=-1) == -1
+    assert step(groups=(None, None, None, 1, 4)) == -1          # groups without arrays
+    assert step(ungrouped=(some, 5)) == -1                      # longer than the batch
+    assert step(Hq=6) == -1                                     # Hq % Hkv
+    assert step(slots=None) == -1                               # no slot mapping
+    assert step(num_pairs=2, pairs=None) == -1                  # pairs missing
+    assert step(B=0) == 0                                       # nothing to do
