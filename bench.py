@@ -785,8 +785,15 @@ def run_prefill(args, rank, world, device):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    # the step as one paged_prefill_step call (step time, launches), then as
+    # separate calls with CUDA events around the attention (the roofline's time)
     launches0 = pkv.kernel_launches()
     t0.record(stream)
+    for i in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    launches = pkv.kernel_launches() - launches0
     for i in range(K):
         if dev["pairs"].shape[0]:
             pkv.copy_blocks(cache.k_pool, cache.v_pool, dev["pairs"], stream=stream)
@@ -795,9 +802,7 @@ def run_prefill(args, rank, world, device):
         pkv.paged_attention_prefill(out, qd, cache.k_pool, cache.v_pool, dev["tables"],
                                     dev["lens"], dev["query_start"], w.scale, mql, stream)
         ev[i][1].record(stream)
-    t1.record(stream)
     torch.cuda.synchronize()
-    launches = pkv.kernel_launches() - launches0
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
@@ -943,8 +948,8 @@ def prefill_main(args, rank, world, device):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {
             "workload": prefill_workload_desc(w),
-            "step": ("copy_blocks (CoW pairs: %d) + reshape_and_cache of %d chunk tokens + "
-                     "paged_attention_prefill; %d kernel launches per step"
+            "step": ("paged_prefill_step: copy_blocks (CoW pairs: %d) + reshape_and_cache of %d "
+                     "chunk tokens + paged_attention_prefill; %d kernel launches per step"
                      % (r["pairs"], r["T"], r["launches_per_step"])),
             "l2": "K/V of the step's sequences %.2f GB vs %d MB L2; the chunk's K/V "
                   "(%.0f MB) is rewritten every step" % (

@@ -339,6 +339,34 @@ PKV_API int paged_attention_prefill(void* out, const void* q,
                             float scale, int q_dtype, int kv_dtype, void* stream);
 
 /* ------------------------------------------------------------------------
+ * paged_prefill_step -- one chunked-prefill step in one call: the step's
+ * copy-on-write block copies, the slot write of every chunk token, then the
+ * chunked-prefill attention. The result is that of
+ *     copy_blocks(k_pool, v_pool, src_dst_pairs, num_pairs, num_blocks, block bytes);
+ *     reshape_and_cache(k_new, v_new, k_pool, v_pool, slot_mapping, num_tokens, ...,
+ *                       BF16, BF16, 1, 1);
+ *     paged_attention_prefill(...)
+ * with the same arguments, k_new / v_new [num_tokens][num_kv_heads][head_dim]
+ * bf16 and slot_mapping int64 [num_tokens].
+ * Precondition (the engine's plan_prefill / plan_prompts meet it): the slots
+ * are the chunk positions L - C .. L - 1 of their sequences, so the slot writes
+ * change only those positions. The attention's loaders then read the key tiles
+ * before a sequence's chunk while the copies and slot writes finish, and wait
+ * for them only before the first tile holding a chunk position (the copies are
+ * complete by then too). A slot outside that precondition may be read before
+ * it is written.
+ * Errors: those of the three calls; argument errors come before any launch.
+ * ---------------------------------------------------------------------- */
+PKV_API int paged_prefill_step(const int64_t* src_dst_pairs, int num_pairs, const void* k_new,
+                               const void* v_new, const int64_t* slot_mapping, int num_tokens,
+                               void* out, const void* q, void* k_pool, void* v_pool,
+                               const int32_t* block_tables, const int32_t* seq_lens,
+                               const int32_t* query_start, int num_seqs, int max_query_len,
+                               int max_blocks_per_seq, int num_blocks, int num_heads,
+                               int num_kv_heads, int head_dim, int block_size, float scale,
+                               int q_dtype, int kv_dtype, void* stream);
+
+/* ------------------------------------------------------------------------
  * swap_blocks -- copy whole blocks between two pools, e.g. a device pool and a
  * pinned host pool of the same layout, for preemption by swapping
  * ("KV cache paginado e batching contínuo para LLMs", "Como funciona": when

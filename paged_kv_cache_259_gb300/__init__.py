@@ -27,7 +27,7 @@ __all__ = [
     "paged_attention_prefill", "swap_blocks",
     "reshape_and_cache", "copy_blocks", "get_device_error", "check_wait_timeout",
     "BoundCall", "bind_paged_attention_decode", "bind_paged_attention_decode_grouped",
-    "bind_reshape_and_cache", "bind_copy_blocks", "paged_decode_step", "bind_paged_decode_step",
+    "bind_reshape_and_cache", "bind_copy_blocks", "paged_decode_step", "bind_paged_decode_step", "paged_prefill_step",
     "kernel_launches", "BlockManager",
     "library_path", "load_library", "pool_shapes", "pool_views", "pools_from_views", "PKV_F32",
     "PKV_BF16", "PKV_E4M3", "PKV_ERR_POOL_EXHAUSTED",
@@ -92,6 +92,9 @@ def load_library():
         "paged_attention_prefill": (c_int, [vp, vp, vp, vp, vp, vp, vp, c_int, c_int, c_int,
                                             c_int, c_int, c_int, c_int, c_int, c_float, c_int,
                                             c_int, vp]),
+        "paged_prefill_step": (c_int, [vp, c_int, vp, vp, vp, c_int, vp, vp, vp, vp, vp, vp, vp,
+                                       c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                                       c_float, c_int, c_int, vp]),
         "reshape_and_cache": (c_int, [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
                                       c_int, c_int, c_float, c_float, vp]),
         "copy_blocks": (c_int, [vp, vp, vp, c_int, c_int, c_size, vp]),
@@ -517,6 +520,54 @@ def paged_attention_prefill(out, q, k_pool, v_pool, block_tables, seq_lens, quer
             int(max_query_len), block_tables.shape[1], NB, Hq, Hkv, D, bs, float(scale),
             _dt(q, "q"), _dt(k_pool, "k_pool"), _stream_ptr(stream, dev))
     _check(st, "paged_attention_prefill")
+    return out
+
+
+def paged_prefill_step(out, q, k_new, v_new, k_pool, v_pool, block_tables, seq_lens,
+                       query_start, slot_mapping, src_dst_pairs, scale, max_query_len,
+                       stream=None):
+    """One chunked-prefill step in one call: the copy-on-write pairs (int64
+    ``[P, 2]``), the chunk tokens' K/V (bfloat16 ``[T, Hkv, D]``) into their slots
+    (int64 ``[T]``: the chunk positions of their sequences) and the attention of
+    ``paged_attention_prefill``; the attention reads the key tiles before each
+    chunk while the writes finish."""
+    lib = load_library()
+    named = ((out, "out"), (q, "q"), (k_new, "k_new"), (v_new, "v_new"), (k_pool, "k_pool"),
+             (v_pool, "v_pool"), (block_tables, "block_tables"), (seq_lens, "seq_lens"),
+             (query_start, "query_start"), (slot_mapping, "slot_mapping"),
+             (src_dst_pairs, "src_dst_pairs"))
+    _tensors(named)
+    for t in (block_tables, seq_lens, query_start):
+        if t.dtype != torch.int32:
+            raise TypeError("block_tables, seq_lens and query_start must be int32")
+    if q.dim() != 3 or out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("q and out must be [T, Hq, D] of the same dtype")
+    if seq_lens.dim() != 1:
+        raise ValueError("seq_lens must be [B]")
+    B = seq_lens.shape[0]
+    T, Hq, D = q.shape
+    NB, Hkv, bs, D2 = _pool_dims(k_pool, v_pool)
+    if D2 != D or block_tables.dim() != 2 or block_tables.shape[0] != B or \
+            tuple(query_start.shape) != (B + 1,):
+        raise ValueError("inconsistent shapes: block_tables [B, max_blocks], query_start "
+                         "[B + 1], pools of q's head_dim")
+    if k_new.dim() != 3 or k_new.shape[1:] != (Hkv, D) or v_new.shape != k_new.shape or \
+            k_new.dtype != q.dtype or v_new.dtype != q.dtype:
+        raise ValueError("k_new and v_new must be [T, Hkv, D] in the dtype of q")
+    if slot_mapping.dtype != torch.int64 or tuple(slot_mapping.shape) != (k_new.shape[0],):
+        raise ValueError("slot_mapping must be int64 [T]")
+    if src_dst_pairs.dtype != torch.int64 or src_dst_pairs.dim() != 2 or \
+            src_dst_pairs.shape[1] != 2:
+        raise ValueError("src_dst_pairs must be int64 [P, 2]")
+    dev = _on_gpu(named)
+    with _on_device(dev):
+        st = lib.paged_prefill_step(
+            src_dst_pairs.data_ptr(), src_dst_pairs.shape[0], k_new.data_ptr(), v_new.data_ptr(),
+            slot_mapping.data_ptr(), k_new.shape[0], out.data_ptr(), q.data_ptr(),
+            k_pool.data_ptr(), v_pool.data_ptr(), block_tables.data_ptr(), seq_lens.data_ptr(),
+            query_start.data_ptr(), B, int(max_query_len), block_tables.shape[1], NB, Hq, Hkv, D,
+            bs, float(scale), _dt(q, "q"), _dt(k_pool, "k_pool"), _stream_ptr(stream, dev))
+    _check(st, "paged_prefill_step")
     return out
 
 

@@ -104,6 +104,11 @@ struct Params {
     int G;
     float scale_log2;   // softmax scale * log2(e)
     int* err;
+    // Launched (with programmatic stream serialisation) right behind this call's
+    // own block copies and chunk slot writes, which change only the chunk
+    // positions L - C .. L - 1 of each sequence: the loaders wait for them only
+    // before the first key tile holding one of those positions.
+    int defer;
 };
 
 // 1-D bulk copy global -> shared (TMA engine), completing on `bar`.
@@ -164,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
     __shared__ uint32_t tmem_slot;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (p.defer) launch_dependents();
     // grid (query tile, kv head, sequence), the query tile fastest: the tiles
     // of one (sequence, kv head) run side by side and share its K/V through L2
     // (launching every sequence's last tile first instead measured 0.35 / 0.46
@@ -236,7 +242,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
     };
     auto fetch_id = [&](int blk) { return blk > blk_last ? 0 : check_id(blk, bt[blk]); };
     // Copies of tile j into buffer j % 2 (false: a wait timed out)
+    const int chunk_tile = (L - C) / kKeys;                // first key tile with a chunk position
+    bool waited = !p.defer;
     auto load_tile = [&](int j) -> bool {
+        if (!waited && j >= chunk_tile) {                  // this call's slot writes land there
+            wait_prerequisites();
+            waited = true;
+        }
         if ((j * kBlocksPerTile) / 32 != win) {
             ++win;
             win_ids = next_ids;
@@ -546,21 +558,27 @@ int launch(const Params& p, dim3 grid, cudaStream_t stream) {
     }
     if (!regs_ok || occ < 1) return PKV_ERR_UNSUPPORTED;
     note_launch();
-    kern<<<grid, kThreads, kSmem, stream>>>(p);
-    const cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (p.defer) {
+        e = launch_pdl(kern, grid, dim3(kThreads), kSmem, stream, p);
+    } else {
+        kern<<<grid, kThreads, kSmem, stream>>>(p);
+        e = cudaGetLastError();
+    }
     return e == cudaSuccess ? PKV_OK : cuda_fail("prefill: kernel launch", e);
 }
 
 }  // namespace prefill
 }  // namespace pkv
 
-extern "C" int paged_attention_prefill(void* out, const void* q, const void* k_pool,
-                                       const void* v_pool, const int32_t* block_tables,
-                                       const int32_t* seq_lens, const int32_t* query_start,
-                                       int num_seqs, int max_query_len, int max_blocks_per_seq,
-                                       int num_blocks, int num_heads, int num_kv_heads,
-                                       int head_dim, int block_size, float scale, int q_dtype,
-                                       int kv_dtype, void* stream) {
+namespace {
+
+int prefill_common(void* out, const void* q, const void* k_pool, const void* v_pool,
+                   const int32_t* block_tables, const int32_t* seq_lens,
+                   const int32_t* query_start, int num_seqs, int max_query_len,
+                   int max_blocks_per_seq, int num_blocks, int num_heads, int num_kv_heads,
+                   int head_dim, int block_size, float scale, int q_dtype, int kv_dtype,
+                   void* stream, int defer, bool check_only) {
     using namespace pkv;
     if (num_seqs < 0 || num_seqs > 65535 || max_query_len < 0 || max_blocks_per_seq <= 0 ||
         num_blocks <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_kv_heads > 65535 ||
@@ -576,6 +594,10 @@ extern "C" int paged_attention_prefill(void* out, const void* q, const void* k_p
         return PKV_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool))
         return PKV_ERR_INVALID_ARG;
+    const long long rows = (long long)max_query_len * G;
+    const long long tiles = (rows + prefill::kRows - 1) / prefill::kRows;
+    if (tiles > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
+    if (check_only) return PKV_OK;
     int* err = error_word();
     if (!err) return PKV_ERR_CUDA;
 
@@ -594,10 +616,62 @@ extern "C" int paged_attention_prefill(void* out, const void* q, const void* k_p
     p.G = G;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.err = err;
-    const long long rows = (long long)max_query_len * G;
-    const long long tiles = (rows + prefill::kRows - 1) / prefill::kRows;
-    if (tiles > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
+    p.defer = defer;
     const dim3 grid((unsigned)tiles, (unsigned)num_kv_heads, (unsigned)num_seqs);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return block_size == 16 ? prefill::launch<16>(p, grid, s) : prefill::launch<32>(p, grid, s);
+}
+
+}  // namespace
+
+extern "C" int paged_attention_prefill(void* out, const void* q, const void* k_pool,
+                                       const void* v_pool, const int32_t* block_tables,
+                                       const int32_t* seq_lens, const int32_t* query_start,
+                                       int num_seqs, int max_query_len, int max_blocks_per_seq,
+                                       int num_blocks, int num_heads, int num_kv_heads,
+                                       int head_dim, int block_size, float scale, int q_dtype,
+                                       int kv_dtype, void* stream) {
+    return prefill_common(out, q, k_pool, v_pool, block_tables, seq_lens, query_start, num_seqs,
+                          max_query_len, max_blocks_per_seq, num_blocks, num_heads, num_kv_heads,
+                          head_dim, block_size, scale, q_dtype, kv_dtype, stream, 0, false);
+}
+
+extern "C" int paged_prefill_step(const int64_t* src_dst_pairs, int num_pairs, const void* k_new,
+                                  const void* v_new, const int64_t* slot_mapping, int num_tokens,
+                                  void* out, const void* q, void* k_pool, void* v_pool,
+                                  const int32_t* block_tables, const int32_t* seq_lens,
+                                  const int32_t* query_start, int num_seqs, int max_query_len,
+                                  int max_blocks_per_seq, int num_blocks, int num_heads,
+                                  int num_kv_heads, int head_dim, int block_size, float scale,
+                                  int q_dtype, int kv_dtype, void* stream) {
+    using namespace pkv;
+    if (num_pairs < 0 || num_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (num_pairs == 0 && num_tokens == 0 && (num_seqs == 0 || max_query_len == 0)) return PKV_OK;
+    // every argument error is found before anything is launched
+    int st = prefill_common(out, q, k_pool, v_pool, block_tables, seq_lens, query_start, num_seqs,
+                            max_query_len, max_blocks_per_seq, num_blocks, num_heads,
+                            num_kv_heads, head_dim, block_size, scale, q_dtype, kv_dtype, stream,
+                            1, true);
+    if (st != PKV_OK) return st;
+    if (num_tokens > 0 && (!k_new || !v_new || !slot_mapping || !aligned16(k_new) ||
+                           !aligned16(v_new) || !k_pool || !v_pool))
+        return PKV_ERR_INVALID_ARG;
+    if (num_pairs > 0 && (!src_dst_pairs || !k_pool || !v_pool)) return PKV_ERR_INVALID_ARG;
+    if (num_pairs > (1 << 30)) return PKV_ERR_UNSUPPORTED;
+    const size_t block_bytes = (size_t)num_kv_heads * block_size * head_dim * 2;
+    if (num_pairs > 0) {
+        st = copy_blocks(k_pool, v_pool, src_dst_pairs, num_pairs, num_blocks, block_bytes, stream);
+        if (st != PKV_OK) return st;
+    }
+    if (num_tokens > 0) {
+        st = reshape_and_cache(k_new, v_new, k_pool, v_pool, slot_mapping, num_tokens,
+                               num_kv_heads, head_dim, block_size, num_blocks, q_dtype, kv_dtype,
+                               1.f, 1.f, stream);
+        if (st != PKV_OK) return st;
+    }
+    // deferred waits only behind this call's own launches
+    return prefill_common(out, q, k_pool, v_pool, block_tables, seq_lens, query_start, num_seqs,
+                          max_query_len, max_blocks_per_seq, num_blocks, num_heads, num_kv_heads,
+                          head_dim, block_size, scale, q_dtype, kv_dtype, stream,
+                          (num_pairs > 0 || num_tokens > 0) ? 1 : 0, false);
 }

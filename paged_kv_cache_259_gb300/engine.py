@@ -22,9 +22,8 @@ import numpy as np
 import torch
 
 from . import (PKV_ERR_POOL_EXHAUSTED, BlockManager, PagedKVError, _check,
-               bind_paged_decode_step, copy_blocks, paged_attention_decode,
-               paged_attention_decode_grouped, paged_attention_prefill,
-               load_library, paged_attention_workspace_size, pool_shapes, pool_views,
+               bind_paged_decode_step, copy_blocks, paged_attention_decode, paged_prefill_step,
+               paged_attention_decode_grouped, load_library, paged_attention_workspace_size, pool_shapes, pool_views,
                reshape_and_cache, swap_blocks)
 
 
@@ -383,14 +382,13 @@ class PagedKVCache:
 
     def prefill_step(self, q, k_new, v_new, dev_plan, out, scale, max_query_len, stream=None):
         """Device half of a chunked-prefill step: CoW copies, the chunk's K/V into
-        its slots, then causal attention of every chunk token."""
-        pairs = dev_plan["pairs"]
-        if pairs.shape[0]:
-            copy_blocks(self.k_pool, self.v_pool, pairs, stream=stream)
-        reshape_and_cache(k_new, v_new, self.k_pool, self.v_pool, dev_plan["slots"], stream=stream)
-        return paged_attention_prefill(out, q, self.k_pool, self.v_pool, dev_plan["tables"],
-                                       dev_plan["lens"], dev_plan["query_start"], scale,
-                                       max_query_len, stream)
+        its slots, then causal attention of every chunk token (one
+        ``paged_prefill_step`` call; the attention reads the tiles before each
+        chunk while the writes finish)."""
+        return paged_prefill_step(out, q, k_new, v_new, self.k_pool, self.v_pool,
+                                  dev_plan["tables"], dev_plan["lens"], dev_plan["query_start"],
+                                  dev_plan["slots"], dev_plan["pairs"], scale, max_query_len,
+                                  stream)
 
     def workspace(self, batch, max_blocks):
         """Split-KV scratch, room for split group lists included."""

@@ -218,3 +218,22 @@ def test_decode_step_refuses_bad_arguments_before_any_launch():
     assert step(slots=None) == -1                               # no slot mapping
     assert step(num_pairs=2, pairs=None) == -1                  # pairs missing
     assert step(B=0) == 0                                       # nothing to do
+
+
+def test_prefill_step_refuses_bad_arguments_before_any_launch():
+    """paged_prefill_step checks every argument on the host before it launches
+    anything (so these run without a GPU)."""
+    lib = library()
+    vp = ctypes.c_void_p
+    some = vp(0x1000)
+
+    def step(num_pairs=0, pairs=None, T=8, slots=some, Hq=8, Hkv=8, D=128, bs=16):
+        return lib.paged_prefill_step(pairs, num_pairs, some, some, slots, T, some, some, some,
+                                      some, some, some, some, 2, 8, 8, 64, Hq, Hkv, D, bs, 0.1, 1,
+                                      1, None)
+
+    assert step(num_pairs=-1) == -1
+    assert step(Hq=12) == -1                                    # Hq % Hkv
+    assert step(D=64) == -2                                     # head_dim 128 only
+    assert step(slots=None) == -1                               # no slot mapping
+    assert step(num_pairs=1) == -1                              # pairs missing

@@ -1,10 +1,16 @@
-"""The one-call decode step (paged_decode_step: copy-on-write copies, slot
-writes, attention, with the attention reading every block but the sequences'
-last ones while the writes finish) against the same step as three separate
-calls: outputs and both whole pools bit for bit, on regular, split, grouped
-(fork step with its copies), beam-search and paired-stage E4M3 steps. The
-separate calls are themselves held to the oracle by test_gpu_parity.py; the
-one-call step is also what cache.step runs there."""
+"""The one-call steps against the same steps as separate calls: outputs and
+both whole pools bit for bit.
+
+paged_decode_step (copy-on-write copies, slot writes, attention, with the
+attention reading every block but the sequences' last ones while the writes
+finish) on regular, split, grouped (fork step with its copies), beam-search and
+paired-stage E4M3 steps; paged_prefill_step (the attention reading the key tiles
+before each chunk while the writes finish) on ragged MHA, GQA with 32-token
+blocks, the LLaMA-13B chunk shape and a chunk after a fork (copy-on-write). The
+separate calls are themselves held to the oracle by test_gpu_parity.py and
+test_gpu_prefill.py; the one-call steps are also what cache.step and
+cache.prefill_step run there."""
+import numpy as np
 import pytest
 import torch
 
@@ -87,3 +93,59 @@ def test_one_call_step_repeated_is_idempotent_and_counts_its_launches():
         outs.append(out.cpu())
     assert pkv.get_device_error() == 0
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+def _prefill_workload(name):
+    if name == "fork_cow":
+        # two samples share a 40-token prompt whose last block is partial: the
+        # second one's chunk copies that block first (copy-on-write)
+        w = wl.chunked_prefill("one_call_fork", 77, [0, 0], [1, 1], 8, 2, 128, 16, NB=40)
+        w.script = [("add", 0), ("append", 0, 40), ("fork", 0, 1)]
+        w.chunks = np.array([20, 150])
+        w.final_lens = np.array([60, 190])
+        return w
+    return {
+        "mha_ragged": lambda: wl.chunked_prefill("one_call_mha", 5, [0, 300, 77], [200, 64, 129],
+                                                 8, 8, 128, 16),
+        "gqa_bs32": lambda: wl.chunked_prefill("one_call_gqa", 6, [900, 0, 64], [96, 300, 5],
+                                               32, 8, 128, 32),
+        "llama13b_shape": lambda: wl.prefill_llama13b_bf16(B=2),
+    }[name]()
+
+
+@pytest.mark.parametrize("name", ["mha_ragged", "gqa_bs32", "llama13b_shape", "fork_cow"])
+def test_one_call_prefill_step_equals_separate_calls(name):
+    """paged_prefill_step (the attention reading the tiles before each chunk
+    while the chunk's slot writes and the step's copies finish) against copy_blocks,
+    reshape_and_cache and paged_attention_prefill made one after another: outputs
+    and both whole pools bit for bit."""
+    w = _prefill_workload(name)
+    k_src, v_src = w.past_pools()
+    q, k_new, v_new = w.step_inputs()
+    results = []
+    for fused in (False, True):
+        cache = PagedKVCache(w.NB, w.Hq, w.Hkv, w.D, w.bs, torch.bfloat16, w.free_order, "cuda")
+        cache.load(k_src, v_src)
+        cache.apply_copies(cache.replay(w.script))
+        plan = cache.plan_prefill(w.step_seqs, w.chunks, max_blocks=w.max_blocks_per_seq)
+        dev = plan.device_tensors("cuda")
+        out = torch.full((w.T, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        qd, kd, vd = q.cuda(), k_new.cuda(), v_new.cuda()
+        if fused:
+            cache.prefill_step(qd, kd, vd, dev, out, w.scale, plan.max_query_len)
+        else:
+            if dev["pairs"].shape[0]:
+                pkv.copy_blocks(cache.k_pool, cache.v_pool, dev["pairs"])
+            pkv.reshape_and_cache(kd, vd, cache.k_pool, cache.v_pool, dev["slots"])
+            pkv.paged_attention_prefill(out, qd, cache.k_pool, cache.v_pool, dev["tables"],
+                                        dev["lens"], dev["query_start"], w.scale,
+                                        plan.max_query_len)
+        torch.cuda.synchronize()
+        assert pkv.get_device_error() == 0
+        results.append((out.cpu(), cache.k_pool.cpu(), cache.v_pool.cpu(), plan))
+    (o1, k1, v1, p1), (o2, k2, v2, _) = results
+    if name == "fork_cow":
+        assert len(p1.pairs) > 0
+    assert torch.equal(k1, k2) and torch.equal(v1, v2)
+    assert not torch.isnan(o2.float()).any()
+    assert torch.equal(o1, o2)
