@@ -360,51 +360,54 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
         if (land_pending) (void)mbar_wait_bounded(bar(kBarLand), 0, nullptr);
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            bool ok = true;
-            // S: A = 128 q rows (8-row groups 2 KB apart, SBO; 8-dim chunks 128
-            // bytes apart, LBO); B = 64 keys, the same layout; each 16-dim step
-            // starts 256 bytes on for both
-            const uint32_t a_lo = tc::desc_lo(sbase + kQOff, 128);
-            auto issue_s = [&](int j) {
-                const int sb = j & 1;
-                ok = ok && mbar_wait_bounded(bar(kBarKFull + sb), (j >> 1) & 1, p.err);
-                if (!ok) return;
-                tc::fence_after_sync();
-                const uint32_t b_lo = tc::desc_lo(sbase + kKOff + sb * kTileBytes, 128);
+        // The whole warp runs the issue loop (its descriptors are warp-uniform
+        // values); one elected lane issues each MMA and commit.
+        bool ok = true;
+        auto wait_all = [&](uint32_t b, uint32_t parity) {
+            ok = __all_sync(0xffffffffu, ok && mbar_wait_bounded(b, parity, p.err));
+        };
+        // S: A = 128 q rows (8-row groups 2 KB apart, SBO; 8-dim chunks 128
+        // bytes apart, LBO); B = 64 keys, the same layout; each 16-dim step
+        // starts 256 bytes on for both
+        const uint32_t a_lo = tc::desc_lo(sbase + kQOff, 128);
+        auto issue_s = [&](int j) {
+            const int sb = j & 1;
+            wait_all(bar(kBarKFull + sb), (j >> 1) & 1);
+            if (!ok) return;
+            tc::fence_after_sync();
+            const uint32_t b_lo = tc::desc_lo(sbase + kKOff + sb * kTileBytes, 128);
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk)
-                    tc::mma_ss2(tmem + kColS + sb * kKeys, a_lo + kk * (256 / 16), kKDescHi,
-                                b_lo + kk * (256 / 16), kKDescHi, kIdescS, kk > 0);
-                tc::commit(bar(kBarS + sb));
-            };
-            issue_s(0);
-            if (n_tiles > 1) issue_s(1);
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                const int sb = j & 1;
-                ok = ok && mbar_wait_bounded(bar(kBarP + sb), (j >> 1) & 1, p.err);
-                ok = ok && mbar_wait_bounded(bar(kBarVFull + sb), (j >> 1) & 1, p.err);
-                if (!ok) break;
-                tc::fence_after_sync();
-                // 16-key steps that hold a key some query sees (P is 0 past them)
-                const int n16 = min(kKeys / 16, (p_max - j * kKeys) / 16 + 1);
-                // B = V of 16 keys: two 8-token chunks 2 KB apart (LBO), 8-dim
-                // core-matrix rows 128 bytes apart (SBO); each step 4 KB on
-                const uint32_t v_lo = tc::desc_lo(sbase + kVOff + sb * kTileBytes, kChunkBytes);
+            for (int kk = 0; kk < kD / 16; ++kk)
+                tc::mma_ss2_elect(tmem + kColS + sb * kKeys, a_lo + kk * (256 / 16), kKDescHi,
+                                  b_lo + kk * (256 / 16), kKDescHi, kIdescS, kk > 0);
+            tc::commit_elect(bar(kBarS + sb));
+        };
+        issue_s(0);
+        if (n_tiles > 1) issue_s(1);
+        for (int j = 0; j < n_tiles && ok; ++j) {
+            const int sb = j & 1;
+            wait_all(bar(kBarP + sb), (j >> 1) & 1);
+            wait_all(bar(kBarVFull + sb), (j >> 1) & 1);
+            if (!ok) break;
+            tc::fence_after_sync();
+            // 16-key steps that hold a key some query sees (P is 0 past them)
+            const int n16 = min(kKeys / 16, (p_max - j * kKeys) / 16 + 1);
+            // B = V of 16 keys: two 8-token chunks 2 KB apart (LBO), 8-dim
+            // core-matrix rows 128 bytes apart (SBO); each step 4 KB on
+            const uint32_t v_lo = tc::desc_lo(sbase + kVOff + sb * kTileBytes, kChunkBytes);
 #pragma unroll
-                for (int jj = 0; jj < kKeys / 16; ++jj)
-                    if (jj < n16)
-                        tc::mma_ts2(tmem + kColO, tmem + kColS + sb * kKeys + jj * 8,
-                                    v_lo + jj * (2 * kChunkBytes / 16), kVDescHi, kIdescO,
-                                    (j > 0 || jj > 0));
-                tc::commit(bar(kBarPV + sb));
-                if (j + 2 < n_tiles) issue_s(j + 2);       // into the buffer P(j) was read from
-            }
-            if (!ok) flag_error(p.err, kErrTimeout);
-            // every MMA issued here is complete before tensor memory is released
-            tc::commit(bar(kBarDrain));
-            mbar_wait_bounded(bar(kBarDrain), 0, nullptr);   // a real wait even after a timeout
+            for (int jj = 0; jj < kKeys / 16; ++jj)
+                if (jj < n16)
+                    tc::mma_ts2_elect(tmem + kColO, tmem + kColS + sb * kKeys + jj * 8,
+                                      v_lo + jj * (2 * kChunkBytes / 16), kVDescHi, kIdescO,
+                                      (j > 0 || jj > 0));
+            tc::commit_elect(bar(kBarPV + sb));
+            if (j + 2 < n_tiles) issue_s(j + 2);           // into the buffer P(j) was read from
         }
+        if (!ok && lane == 0) flag_error(p.err, kErrTimeout);
+        // every MMA issued here is complete before tensor memory is released
+        tc::commit_elect(bar(kBarDrain));
+        mbar_wait_bounded(bar(kBarDrain), 0, nullptr);     // a real wait even after a timeout
         __syncwarp();
     }
     } else {
