@@ -43,26 +43,12 @@ __device__ __forceinline__ void fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 operation this thread issued so far
-// has completed.
-__device__ __forceinline__ void commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-// Shared-memory matrix descriptor, no swizzle, K-major (see the file header).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;  // descriptor version of the sm_100 family
-    return d;                // base offset 0, absolute LBO, layout "no swizzle"
-}
-
-// The two 32-bit halves of a no-swizzle descriptor: `lo` holds the start
-// address and LBO, `hi` the SBO and the version bits. Stepping the start
-// address by `bytes` (< 16 KB past it) is `lo + bytes / 16`, one 32-bit add, so
-// an issue loop spends almost nothing per instruction on descriptors.
+// Shared-memory matrix descriptor, no swizzle, K-major (see the file header),
+// as its two 32-bit halves: bits 0-13 start address / 16, 16-29 LBO / 16
+// (`lo`); 32-45 SBO / 16 and bit 46, the descriptor version of the sm_100
+// family (`hi`); base offset 0, absolute LBO, layout "no swizzle". Stepping the
+// start address by `bytes` (< 16 KB past it) is `lo + bytes / 16`, one 32-bit
+// add, so an issue loop spends almost nothing per instruction on descriptors.
 __device__ __forceinline__ uint32_t desc_lo(uint32_t addr, uint32_t lbo) {
     return ((addr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
@@ -80,42 +66,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
            | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, one instruction (K = 16 for bf16).
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// As mma_ts, with the B descriptor given as its two 32-bit halves.
-__device__ __forceinline__ void mma_ts2(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
-                                        uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\tmov.b64 bd, {%2, %3};\n\t"
-        "setp.ne.b32 p, %5, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]^T, one instruction (K = 16 for bf16); both
-// descriptors given as their two 32-bit halves.
-__device__ __forceinline__ void mma_ss2(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
-                                        uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
-                                        uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\tmov.b64 ad, {%1, %2};\n\t"
-        "mov.b64 bd, {%3, %4};\n\tsetp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// The same three, executed by a whole converged warp: one lane (elect.sync)
-// issues the instruction, and the descriptors stay warp-uniform values.
+// MMA and commit instructions, executed by a whole converged warp: one lane
+// (elect.sync) issues each, so the descriptors stay warp-uniform values.
+// Shared-memory descriptors are given as their two 32-bit halves.
+// D[tmem] (+)= A[smem] * B[smem]^T, one instruction (K = 16 for bf16).
 __device__ __forceinline__ void mma_ss2_elect(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
                                               uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
                                               uint32_t accumulate) {
@@ -126,6 +80,7 @@ __device__ __forceinline__ void mma_ss2_elect(uint32_t d_tmem, uint32_t a_lo, ui
         "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T, one instruction (K = 16 for bf16).
 __device__ __forceinline__ void mma_ts2_elect(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                               uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -135,6 +90,8 @@ __device__ __forceinline__ void mma_ts2_elect(uint32_t d_tmem, uint32_t a_tmem, 
         "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Arrive once on `bar` when every tcgen05 operation issued so far (by this
+// warp's elected lane) has completed.
 __device__ __forceinline__ void commit_elect(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
