@@ -822,27 +822,31 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
         return __shfl_sync(kFull, id_cur, kk & 31);
     };
     int32_t* stage_info = reinterpret_cast<int32_t*>(smem + P::kInfoOff);
-    auto issue = [&](int kk, int id, int id2, int info) {   // lane 0 only
+    // the whole converged warp: one elected lane makes the copies and arrivals
+    auto issue = [&](int kk, int id, int id2, int info) {
         const int s = kk % ST;
         const uint32_t bar = smem_addr(&bars[w * ST + s]);
         // this step's slot writes land in the sequences' last blocks only
         if (p.defer && (PREFIX ? (info & kLastBit) != 0 : kk == last_kk)) wait_prerequisites();
-        stage_id[w * ST + s] = id;
-        if constexpr (PREFIX) stage_info[w * ST + s] = info & ~kLastBit;
+        if (lane == 0) {
+            stage_id[w * ST + s] = id;
+            if constexpr (PREFIX) stage_info[w * ST + s] = info & ~kLastBit;
+        }
+        __syncwarp();
         if (id >= 0) {
             const uint32_t dst = smem_addr(ring + (size_t)((w * ST + s) * 2) * TILE);
             const size_t off = ((size_t)id * p.num_kv_heads + hk) * PTILE;
             const bool two = PAIR == 2 && id2 >= 0;
-            mbar_arrive_expect_tx(bar, (two ? 4 : 2) * PTILE);
-            bulk_g2s(dst, p.k_pool + off, PTILE, bar, pol);
-            bulk_g2s(dst + TILE, p.v_pool + off, PTILE, bar, pol);
+            mbar_arrive_expect_tx_elect(bar, (two ? 4 : 2) * PTILE);
+            bulk_g2s_elect(dst, p.k_pool + off, PTILE, bar, pol);
+            bulk_g2s_elect(dst + TILE, p.v_pool + off, PTILE, bar, pol);
             if (two) {                                      // the second block right after
                 const size_t off2 = ((size_t)id2 * p.num_kv_heads + hk) * PTILE;
-                bulk_g2s(dst + PTILE, p.k_pool + off2, PTILE, bar, pol);
-                bulk_g2s(dst + TILE + PTILE, p.v_pool + off2, PTILE, bar, pol);
+                bulk_g2s_elect(dst + PTILE, p.k_pool + off2, PTILE, bar, pol);
+                bulk_g2s_elect(dst + TILE + PTILE, p.v_pool + off2, PTILE, bar, pol);
             }
         } else {
-            mbar_arrive(bar);
+            mbar_arrive_elect(bar);
         }
     };
 
@@ -862,7 +866,7 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
         } else {
             id = get_id(kk, &info, &id2);
         }
-        if (lane == 0) issue(kk, id, id2, info);
+        issue(kk, id, id2, info);
     }
 
     for (int i = tid; i < G * D; i += NW * 32) {            // query rows of this CTA
@@ -903,10 +907,8 @@ __global__ void __launch_bounds__(NW * 32, 3) paged_decode_kernel(const Params p
         if (k + ST < nk) {
             int info, id2;
             const int id = get_id(k + ST, &info, &id2);
-            if (lane == 0) {
-                fence_proxy_async_smem();
-                issue(k + ST, id, id2, info);
-            }
+            fence_proxy_async_smem();
+            issue(k + ST, id, id2, info);
         }
     }
     if (aborted) {
