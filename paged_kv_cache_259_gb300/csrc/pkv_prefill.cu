@@ -120,6 +120,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+__device__ __forceinline__ void st_shared16(uint32_t addr, const uint32_t (&w)[4]) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3])
+                 : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared16(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -160,7 +174,9 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 enum : int { kBarKFull = 0, kBarVFull = 2, kBarS = 4, kBarPV = 6, kBarP = 8, kBarLand = 10,
              kBarDrain, kNumBars };
 
-template <int BS>
+// kStageO (one query head per KV head): the output leaves through shared
+// memory, see the epilogue.
+template <int BS, bool kStageO>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(const Params p) {
     constexpr int kBlocksPerTile = kKeys / BS;
     constexpr int kBlockBytes = BS * kD * 2;       // one (block, head) tile
@@ -511,13 +527,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
             flag_error(p.err, kErrTimeout);
         } else {
             const float inv = 1.f / l_run;
-            uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)(q0 + (valid ? i : 0)) * p.num_heads + h) * kD);
+            if constexpr (kStageO) {
+                // One head per KV head: a warp's 32 rows are 32 tokens, a token's
+                // heads apart in memory. O leaves through shared memory (the K
+                // stages, free once the last S has completed): each thread writes its
+                // bf16 row there (16-byte chunk c at position c ^ (row % 8), so no two
+                // lanes of a quarter-warp share banks), then the warp stores two whole
+                // rows per instruction (256 contiguous bytes each) instead of 32 rows
+                // x 16 bytes.
+                const uint32_t stg = sbase + kKOff + warp * (32 * kD * 2);
+                fence_proxy_async_smem();              // after the tensor cores' reads there
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t ov[32];
-                tc::ld32(row + kColO + cb * 32, ov);
-                tc::wait_ld();
-                if (valid) {
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t ov[32];
+                    tc::ld32(row + kColO + cb * 32, ov);
+                    tc::wait_ld();
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         uint32_t w[4];
@@ -528,7 +552,40 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
                                 __uint_as_float(ov[8 * u + 2 * e + 1]) * inv);
                             w[e] = *reinterpret_cast<const uint32_t*>(&h2);
                         }
-                        dst[cb * 4 + u] = make_uint4(w[0], w[1], w[2], w[3]);
+                        st_shared16(stg + lane * 256 + (((cb * 4 + u) ^ (lane & 7)) << 4), w);
+                    }
+                }
+                __syncwarp();
+                const int half = lane >> 4, ch = lane & 15;
+                uint4* const obase = reinterpret_cast<uint4*>(
+                    p.out + ((size_t)(q0 + i0 + warp * 32) * p.num_heads + hk) * kD) + ch;
+#pragma unroll 4
+                for (int m = 0; m < 16; ++m) {
+                    const int rr = 2 * m + half;                   // token within the warp's rows
+                    const uint4 x = ld_shared16(stg + rr * 256 + ((ch ^ (rr & 7)) << 4));
+                    if (i0 + warp * 32 + rr < C) obase[(size_t)rr * p.num_heads * (kD / 8)] = x;
+                }
+            } else {
+                uint4* dst = reinterpret_cast<uint4*>(
+                    p.out + ((size_t)(q0 + (valid ? i : 0)) * p.num_heads + h) * kD);
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t ov[32];
+                    tc::ld32(row + kColO + cb * 32, ov);
+                    tc::wait_ld();
+                    if (valid) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                                    __uint_as_float(ov[8 * u + 2 * e]) * inv,
+                                    __uint_as_float(ov[8 * u + 2 * e + 1]) * inv);
+                                w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                            }
+                            dst[cb * 4 + u] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
                     }
                 }
             }
@@ -543,9 +600,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
     }
 }
 
-template <int BS>
+template <int BS, bool kStageO>
 int launch(const Params& p, dim3 grid, cudaStream_t stream) {
-    auto kern = paged_prefill_kernel<BS>;
+    auto kern = paged_prefill_kernel<BS, kStageO>;
     int occ = 0;
     const int st = kernel_setup(reinterpret_cast<const void*>(kern), kSmem, kThreads, &occ);
     if (st != PKV_OK) return st;
@@ -622,7 +679,11 @@ int prefill_common(void* out, const void* q, const void* k_pool, const void* v_p
     p.defer = defer;
     const dim3 grid((unsigned)tiles, (unsigned)num_kv_heads, (unsigned)num_seqs);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return block_size == 16 ? prefill::launch<16>(p, grid, s) : prefill::launch<32>(p, grid, s);
+    if (G == 1)
+        return block_size == 16 ? prefill::launch<16, true>(p, grid, s)
+                                : prefill::launch<32, true>(p, grid, s);
+    return block_size == 16 ? prefill::launch<16, false>(p, grid, s)
+                            : prefill::launch<32, false>(p, grid, s);
 }
 
 }  // namespace
