@@ -468,16 +468,15 @@ def e2e_live_planning(cache, w, q, k_new, v_new, out, ks, vs, ws, stream, steps,
         v["v_new"].copy_(hv)
 
     def one_step(plan_us):
-        pipe.host_inputs()                 # wait for the slab outside the planning time
-        t1 = time.perf_counter()
+        # planning, upload, launches and read-back: one library call
+        # (pkv_decode_pipeline_step), which times its planning
         try:
-            pipe.plan()
+            pipe.submit(hout, w.scale, ks, vs, ws)
         except PagedKVError as e:
             if e.status != PKV_ERR_POOL_EXHAUSTED:
                 raise
             return False                   # no room for another step in this pass
-        plan_us.append(1e6 * (time.perf_counter() - t1))
-        pipe.submit(hout, w.scale, ks, vs, ws)
+        plan_us.append(pipe.last_plan_us)
         return True
 
     warm_us = []
@@ -1569,7 +1568,8 @@ def main():
                          "builds the tables and finds the prefix groups straight into a "
                          "pinned slab; the slab (plan, q, k, v) is uploaded, the step runs "
                          "and its output is read back, overlapped with the neighbouring "
-                         "steps; sequences grow by one token per step (bytes counted at each "
+                         "steps, all of it one library call per step "
+                         "(pkv_decode_pipeline_step); sequences grow by one token per step (bytes counted at each "
                          "step's lengths), the manager rewound every %d steps outside the "
                          "timed passes" % e2e["per_pass"])},
             "check": check,

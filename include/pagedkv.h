@@ -583,6 +583,95 @@ PKV_API int bm_plan_decode(pkv_block_manager* bm, const int64_t* seq_ids, int n,
                            int32_t* group_blocks, int32_t* ungrouped, int* num_groups,
                            int* num_ungrouped, int* max_group_blocks);
 
+/* ------------------------------------------------------------------------
+ * pkv_decode_pipeline_step -- one pipelined decode step, host half and device
+ * launches, in one call: bm_plan_decode into the step's pinned host slab
+ * (slots, copy-on-write pairs, tables, lengths and, with max_members >= 1,
+ * the prefix groups), pkv_stage_upload of the whole slab, paged_decode_step on
+ * the slab's device copy with this step's counts (pairs; groups, 0 groups
+ * being the plain decode), and pkv_stage_download of the output into
+ * `host_out`. The same work as those four calls made one after another (the
+ * results are the same, bit for bit), without the host time between them, so
+ * a loop feeding short steps keeps up with the device (glossary
+ * "PagedAttention", "Cách phân trang hoạt động": the host plans every step's
+ * allocation as the sequences grow).
+ *
+ * `a` describes one buffer set of the pipeline and stays valid across calls:
+ * the manager and the step's sequence ids; the host slab views the plan is
+ * written to (h_*, sized for the most a step can raise: a pair and a group
+ * row per sequence; group_blocks host scratch int32 [num_seqs]); the host and
+ * device slabs (slab_bytes each) with the device views of q, k_new, v_new and
+ * of the plan inside the device slab; the step's fixed arguments (those of
+ * paged_decode_step); the output buffer (out_bytes) and the streams and
+ * events of pkv_stage_upload / pkv_stage_download (cudaStream_t, cudaEvent_t).
+ * `reuse` != 0 when this buffer set has run a step before: the upload then
+ * waits for that step's kernels and the kernels for its read-back.
+ * Precondition: the host slab is free, i.e. the caller has waited for the
+ * buffer set's previous upload (its uploaded event) before writing q, k_new
+ * and v_new there and before this call.
+ * Outputs (each may be NULL): counts[4] = copy-on-write pairs, prefix groups,
+ * sequences in no group, longest group list; *plan_us = host microseconds
+ * spent in bm_plan_decode.
+ * Errors: PKV_ERR_INVALID_ARG for a null `a` or `host_out`; otherwise those of
+ * bm_plan_decode (before anything is enqueued; the manager is unchanged) and
+ * of the three enqueueing calls.
+ * ---------------------------------------------------------------------- */
+typedef struct pkv_decode_pipeline_step_args {
+    pkv_block_manager* bm;
+    const int64_t* seq_ids;
+    int num_seqs;
+    int max_blocks;
+    int max_members;
+    int64_t* h_slots;
+    int64_t* h_pairs;
+    int32_t* h_tables;
+    int32_t* h_lens;
+    int32_t* h_group_members;
+    int32_t* h_group_prefix;
+    int32_t* h_seq_group;
+    int32_t* h_ungrouped;
+    int32_t* group_blocks;
+    const void* host_slab;
+    void* dev_slab;
+    size_t slab_bytes;
+    const void* q;
+    const void* k_new;
+    const void* v_new;
+    const int64_t* slots;
+    const int64_t* pairs;
+    const int32_t* tables;
+    const int32_t* lens;
+    const int32_t* seq_group;
+    const int32_t* group_members;
+    const int32_t* group_prefix;
+    const int32_t* ungrouped;
+    void* out;
+    void* k_pool;
+    void* v_pool;
+    int num_blocks;
+    int num_heads;
+    int num_kv_heads;
+    int head_dim;
+    int block_size;
+    float scale;
+    int q_dtype;
+    int kv_dtype;
+    float k_scale;
+    float v_scale;
+    void* workspace;
+    size_t workspace_bytes;
+    size_t out_bytes;
+    void* up_stream;
+    void* compute_stream;
+    void* down_stream;
+    void* uploaded_event;
+    void* computed_event;
+    void* downloaded_event;
+} pkv_decode_pipeline_step_args;
+
+PKV_API int pkv_decode_pipeline_step(const pkv_decode_pipeline_step_args* a, int reuse,
+                                     void* host_out, int* counts, double* plan_us);
+
 /* Prefix caching (glossary "Chia sẻ block giữa các chuỗi": requests that begin
  * with the same system prompt reuse one copy of the common prefix, with a count
  * per block; "vLLM PagedAttention: uma revolução...": prefix caching).

@@ -50,6 +50,31 @@ class PagedKVError(RuntimeError):
         super().__init__(f"{what}: {_STATUS.get(status, 'unknown status')} ({status})")
 
 
+class DecodePipelineStepArgs(ctypes.Structure):
+    """``pkv_decode_pipeline_step_args`` (include/pagedkv.h): one buffer set of a
+    pipelined decode step, field for field."""
+    _vp, _i32p, _i64p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
+    _fields_ = [
+        ("bm", _vp), ("seq_ids", _i64p), ("num_seqs", ctypes.c_int), ("max_blocks", ctypes.c_int),
+        ("max_members", ctypes.c_int),
+        ("h_slots", _i64p), ("h_pairs", _i64p), ("h_tables", _i32p), ("h_lens", _i32p),
+        ("h_group_members", _i32p), ("h_group_prefix", _i32p), ("h_seq_group", _i32p),
+        ("h_ungrouped", _i32p), ("group_blocks", _i32p),
+        ("host_slab", _vp), ("dev_slab", _vp), ("slab_bytes", ctypes.c_size_t),
+        ("q", _vp), ("k_new", _vp), ("v_new", _vp), ("slots", _vp), ("pairs", _vp),
+        ("tables", _vp), ("lens", _vp), ("seq_group", _vp), ("group_members", _vp),
+        ("group_prefix", _vp), ("ungrouped", _vp),
+        ("out", _vp), ("k_pool", _vp), ("v_pool", _vp),
+        ("num_blocks", ctypes.c_int), ("num_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int), ("scale", ctypes.c_float),
+        ("q_dtype", ctypes.c_int), ("kv_dtype", ctypes.c_int), ("k_scale", ctypes.c_float),
+        ("v_scale", ctypes.c_float), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+        ("out_bytes", ctypes.c_size_t),
+        ("up_stream", _vp), ("compute_stream", _vp), ("down_stream", _vp),
+        ("uploaded_event", _vp), ("computed_event", _vp), ("downloaded_event", _vp),
+    ]
+
+
 def library_path():
     return _LIB_PATH
 
@@ -128,6 +153,8 @@ def load_library():
         "bm_append_tokens": (c_int, [vp, ctypes.c_int64, i32p, c_int, i64p, i64p, c_int, ip]),
         "bm_cache_stats": (c_int, [vp, i64p, i64p, ip, ip]),
         "bm_evictable_list": (c_int, [vp, i32p, c_int]),
+        "pkv_decode_pipeline_step": (c_int, [ctypes.POINTER(DecodePipelineStepArgs), c_int, vp, ip,
+                                             ctypes.POINTER(ctypes.c_double)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -4,6 +4,8 @@
 // a download stream once the kernels are done -- each as one call, so a host
 // loop that feeds one step after another spends its time on the steps, not on
 // the runtime calls between them.
+#include <chrono>
+
 #include <cuda_runtime.h>
 
 #include "pkv_internal.cuh"
@@ -42,6 +44,47 @@ int pkv_stage_download(const void* dev_src, void* host_dst, size_t bytes, void* 
     if (e == cudaSuccess) e = cudaMemcpyAsync(host_dst, dev_src, bytes, cudaMemcpyDeviceToHost, down);
     if (e == cudaSuccess) e = cudaEventRecord(static_cast<cudaEvent_t>(downloaded_event), down);
     return e == cudaSuccess ? PKV_OK : cuda_fail("pkv_stage_download", e);
+}
+
+int pkv_decode_pipeline_step(const pkv_decode_pipeline_step_args* a, int reuse, void* host_out,
+                             int* counts, double* plan_us) {
+    using namespace pkv;
+    if (!a || !host_out) return PKV_ERR_INVALID_ARG;
+    const bool grouped = a->max_members >= 1;
+    int pairs = 0, groups = 0, ungrouped = 0, longest = 0;
+    const auto t0 = std::chrono::steady_clock::now();
+    int st = bm_plan_decode(a->bm, a->seq_ids, a->num_seqs, a->max_blocks, a->h_slots, a->h_pairs,
+                            &pairs, a->h_tables, a->h_lens, grouped ? a->max_members : 0,
+                            grouped ? a->h_group_members : nullptr,
+                            grouped ? a->h_group_prefix : nullptr,
+                            grouped ? a->h_seq_group : nullptr, grouped ? a->group_blocks : nullptr,
+                            grouped ? a->h_ungrouped : nullptr, &groups, &ungrouped, &longest);
+    if (plan_us)
+        *plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0)
+                       .count();
+    if (counts) {
+        counts[0] = pairs;
+        counts[1] = groups;
+        counts[2] = ungrouped;
+        counts[3] = longest;
+    }
+    if (st != PKV_OK) return st;
+    st = pkv_stage_upload(a->host_slab, a->dev_slab, a->slab_bytes, a->up_stream, a->compute_stream,
+                          a->uploaded_event, reuse ? a->computed_event : nullptr,
+                          reuse ? a->downloaded_event : nullptr);
+    if (st != PKV_OK) return st;
+    st = paged_decode_step(a->pairs, pairs, a->k_new, a->v_new, a->slots, a->out, a->q, a->k_pool,
+                           a->v_pool, a->tables, a->lens, a->num_seqs, a->max_blocks, a->num_blocks,
+                           a->num_heads, a->num_kv_heads, a->head_dim, a->block_size, a->scale,
+                           a->q_dtype, a->kv_dtype, a->k_scale, a->v_scale,
+                           grouped ? a->seq_group : nullptr, grouped ? a->group_members : nullptr,
+                           grouped ? a->group_prefix : nullptr, grouped ? groups : 0,
+                           grouped ? a->max_members : 0, grouped ? longest : 0,
+                           grouped ? a->ungrouped : nullptr, grouped ? ungrouped : -1,
+                           a->workspace, a->workspace_bytes, a->compute_stream);
+    if (st != PKV_OK) return st;
+    return pkv_stage_download(a->out, host_out, a->out_bytes, a->compute_stream, a->down_stream,
+                              a->computed_event, a->downloaded_event);
 }
 
 }  // extern "C"

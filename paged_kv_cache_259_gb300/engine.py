@@ -21,8 +21,8 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-from . import (PKV_ERR_POOL_EXHAUSTED, BlockManager, PagedKVError, _check,
-               bind_paged_decode_step, copy_blocks, paged_attention_decode, paged_prefill_step,
+from . import (PKV_ERR_POOL_EXHAUSTED, BlockManager, DecodePipelineStepArgs, PagedKVError, _check,
+               _decode_shapes, _dt, _workspace, bind_paged_decode_step, copy_blocks, paged_attention_decode, paged_prefill_step,
                paged_attention_decode_grouped, load_library, paged_attention_workspace_size, pool_shapes, pool_views,
                reshape_and_cache, swap_blocks)
 
@@ -637,6 +637,9 @@ class LiveDecodePipeline(StepPipeline):
             self._ptrs.append((p64(v["slots"]), p64(v["pairs"]), p32(v["tables"]),
                                p32(v["lens"]), g))
         self._step_counts = {}
+        self._native_args = [None, None]                  # per slab: (key, step arguments)
+        self.last_plan_us = 0.0                           # host planning of the last submit
+        self.last_counts = (0, 0, 0, 0)                   # its pairs, groups, ungrouped, longest list
 
     def plan(self):
         """Plan the next step into its slab with one native call (waits until
@@ -652,15 +655,71 @@ class LiveDecodePipeline(StepPipeline):
             self._step_counts = {"num_pairs": npairs}
         return npairs, ng
 
+    def _native(self, b, scale, k_scale, v_scale, workspace):
+        """Slab b's ``pkv_decode_pipeline_step`` arguments, built once per scales
+        and workspace (after the bound step's argument checks)."""
+        key = (scale, k_scale, v_scale, None if workspace is None else workspace.data_ptr())
+        if self._native_args[b] is not None and self._native_args[b][0] == key:
+            return self._native_args[b][1]
+        self._bound_step(b, scale, k_scale, v_scale, workspace)
+        q, k_new, v_new, plan = self.steps[b]
+        out, c, h = self.outs[b], self.cache, self._h
+        B, Hq, D, NB, Hkv, bs = _decode_shapes(out, q, c.k_pool, c.v_pool, plan["tables"],
+                                               plan["lens"])
+        ws_ptr, ws_bytes = _workspace(workspace, out.device)
+        a = DecodePipelineStepArgs()
+        a.seq_ids = self._ids_p
+        a.num_seqs, a.max_blocks = len(self.ids), self.max_blocks
+        slots_p, pairs_p, tables_p, lens_p, g = self._ptrs[b]
+        a.h_slots, a.h_pairs, a.h_tables, a.h_lens = slots_p, pairs_p, tables_p, lens_p
+        if g is not None:
+            (a.max_members, a.h_group_members, a.h_group_prefix, a.h_seq_group, a.group_blocks,
+             a.h_ungrouped) = g
+            a.seq_group, a.group_members, a.group_prefix, a.ungrouped = (
+                plan[k].data_ptr() for k in ("seq_group", "group_members", "group_prefix",
+                                             "ungrouped"))
+        a.host_slab, a.dev_slab, a.slab_bytes = h["host"][b], h["dev"][b], self.slab_bytes
+        a.q, a.k_new, a.v_new = q.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
+        a.slots, a.pairs, a.tables, a.lens = (plan[k].data_ptr()
+                                              for k in ("slots", "pairs", "tables", "lens"))
+        a.out, a.k_pool, a.v_pool = out.data_ptr(), c.k_pool.data_ptr(), c.v_pool.data_ptr()
+        a.num_blocks, a.num_heads, a.num_kv_heads, a.head_dim, a.block_size = NB, Hq, Hkv, D, bs
+        a.scale, a.k_scale, a.v_scale = float(scale), float(k_scale), float(v_scale)
+        a.q_dtype, a.kv_dtype = _dt(q, "q"), _dt(c.k_pool, "k_pool")
+        a.workspace, a.workspace_bytes = ws_ptr, ws_bytes
+        a.out_bytes = out.numel() * out.element_size()
+        a.up_stream, a.compute_stream, a.down_stream = h["up"], h["compute"], h["down"]
+        a.uploaded_event, a.computed_event, a.downloaded_event = (
+            h["uploaded"][b], h["computed"][b], h["downloaded"][b])
+        self._native_args[b] = (key, a)
+        return a
+
     def submit(self, host_out, scale=None, k_scale=1.0, v_scale=1.0, workspace=None):
-        """Plan the next step (``plan``) unless it is planned already, then run
-        it as ``StepPipeline.submit`` does."""
-        if not self._step_counts:
-            self.plan()
-        try:
-            return super().submit(host_out, scale, k_scale, v_scale, workspace)
-        finally:
-            self._step_counts = {}
+        """Plan and run the next step. Unless ``plan`` was called for it, the
+        planning, the upload, the step's launches and the read-back are one
+        library call (``pkv_decode_pipeline_step``; ``last_plan_us`` and
+        ``last_counts`` then report its planning); after ``plan``, the step runs
+        as ``StepPipeline.submit`` does."""
+        if self._step_counts:
+            try:
+                return super().submit(host_out, scale, k_scale, v_scale, workspace)
+            finally:
+                self._step_counts = {}
+        if not (host_out.is_contiguous() and host_out.numel() == self.outs[0].numel() and
+                host_out.dtype == self.outs[0].dtype and not host_out.is_cuda):
+            raise ValueError("host_out must be a contiguous CPU tensor shaped like the output")
+        b = self.n % 2
+        self.host_inputs()                                # the slab's previous upload is done
+        a = self._native(b, scale, k_scale, v_scale, workspace)
+        counts, us = (ctypes.c_int * 4)(), ctypes.c_double(0.0)
+        a.bm = self.cache.bm._h                           # the manager may have been replaced
+        st = self._lib.pkv_decode_pipeline_step(ctypes.byref(a), 1 if self.n >= 2 else 0,
+                                                ctypes.c_void_p(host_out.data_ptr()), counts,
+                                                ctypes.byref(us))
+        self.last_plan_us, self.last_counts = us.value, tuple(counts)
+        _check(st, "pkv_decode_pipeline_step")
+        self.n += 1
+        return self.uploaded[b], self.downloaded[b]
 
     def _counts(self):
         return self._step_counts

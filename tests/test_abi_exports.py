@@ -237,3 +237,64 @@ def test_prefill_step_refuses_bad_arguments_before_any_launch():
     assert step(D=64) == -2                                     # head_dim 128 only
     assert step(slots=None) == -1                               # no slot mapping
     assert step(num_pairs=1) == -1                              # pairs missing
+
+
+def test_decode_pipeline_step_args_match_the_header_layout(tmp_path):
+    """The binding's ctypes mirror of pkv_decode_pipeline_step_args has the C
+    struct's size and every field at the C offset (a C program built from the
+    header prints them)."""
+    import shutil
+    import subprocess
+    import paged_kv_cache_259_gb300 as pkv
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    S = pkv.DecodePipelineStepArgs
+    names = [f[0] for f in S._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stdio.h>\n#include <stddef.h>\n#include <stdint.h>\n"
+                   '#include "pagedkv.h"\nint main(void) {\n'
+                   '    printf("%zu\\n", sizeof(pkv_decode_pipeline_step_args));\n' +
+                   "".join(f'    printf("%zu\\n", offsetof(pkv_decode_pipeline_step_args, {n}));\n'
+                           for n in names) + "    return 0;\n}\n")
+    exe = tmp_path / "layout"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.run([cc, "-I", inc, "-o", str(exe), str(src)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(S)
+    assert got[1:] == [getattr(S, n).offset for n in names]
+
+
+def test_decode_pipeline_step_refuses_before_any_cuda_call():
+    """pkv_decode_pipeline_step: a null argument block or output buffer is
+    PKV_ERR_INVALID_ARG, and a step the block manager refuses (an unknown
+    sequence id) returns its status from the planning, before anything is
+    enqueued (so this runs without a GPU), leaving the manager unchanged."""
+    import paged_kv_cache_259_gb300 as pkv
+    lib = library()
+    S = pkv.DecodePipelineStepArgs
+    some = ctypes.c_void_p(0x1000)
+    assert lib.pkv_decode_pipeline_step(None, 0, some, None, None) == -1
+    bm = pkv.BlockManager(8, 16, np.arange(8))
+    bm.add_seq(0)
+    ids = np.array([7], dtype=np.int64)                   # never added
+    slots = np.zeros(1, dtype=np.int64)
+    pairs = np.zeros(2, dtype=np.int64)
+    tables = np.zeros(4, dtype=np.int32)
+    lens = np.zeros(1, dtype=np.int32)
+    a = S()
+    a.bm = bm._h
+    a.seq_ids = ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    a.num_seqs, a.max_blocks, a.max_members = 1, 4, 0
+    a.h_slots = slots.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    a.h_pairs = pairs.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    a.h_tables = tables.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    a.h_lens = lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    assert lib.pkv_decode_pipeline_step(ctypes.byref(a), 0, None, None, None) == -1
+    counts, us = (ctypes.c_int * 4)(), ctypes.c_double(-1.0)
+    assert lib.pkv_decode_pipeline_step(ctypes.byref(a), 0, some, counts,
+                                        ctypes.byref(us)) == -4
+    assert us.value >= 0.0 and list(counts) == [0, 0, 0, 0]
+    assert bm.seq_len(0) == 0 and bm.num_free() == 8
+

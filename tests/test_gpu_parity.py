@@ -561,7 +561,9 @@ def test_live_decode_pipeline_matches_planned_serial_steps(fork):
     """engine.LiveDecodePipeline (each step planned by the native manager
     straight into the pinned slab, copy-on-write pairs and prefix groups counted
     per step, uploads and downloads overlapped) gives, step by step, exactly the
-    outputs and pools of plan_step + step run one after another."""
+    outputs and pools of plan_step + step run one after another: both as one
+    library call per step (pkv_decode_pipeline_step, whose reported counts
+    match the serial plans) and as plan() followed by the separate calls."""
     from paged_kv_cache_259_gb300.engine import LiveDecodePipeline, PagedKVCache
     w = wl.shared_prefix(fork_step=fork, groups=3, per_group=4, prompt=150, max_suffix=40,
                          Hq=16, Hkv=8, seed=11)
@@ -571,8 +573,8 @@ def test_live_decode_pipeline_matches_planned_serial_steps(fork):
     ks = [torch.randn(w.B, w.Hkv, w.D, generator=gen).to(torch.bfloat16) for _ in range(n)]
     vs = [torch.randn(w.B, w.Hkv, w.D, generator=gen).to(torch.bfloat16) for _ in range(n)]
     k_src, v_src = w.past_pools()
-    outs, pools, counts = {}, {}, []
-    for mode in ("serial", "live"):
+    outs, pools, counts, native_counts = {}, {}, [], []
+    for mode in ("serial", "live", "live_planned"):
         cache = PagedKVCache(w.NB, w.Hq, w.Hkv, w.D, w.bs, torch.bfloat16, w.free_order, "cuda")
         cache.load(k_src, v_src)
         cache.apply_copies(cache.replay(w.script))
@@ -597,15 +599,21 @@ def test_live_decode_pipeline_matches_planned_serial_steps(fork):
                 views["q"].copy_(qs[i])
                 views["k_new"].copy_(ks[i])
                 views["v_new"].copy_(vs[i])
+                if mode == "live_planned":
+                    pipe.plan()
                 pipe.submit(res[i], w.scale, workspace=ws)
+                if mode == "live":
+                    native_counts.append(pipe.last_counts[:2])
             torch.cuda.synchronize()
         assert pkv.get_device_error() == 0
         outs[mode] = res
         pools[mode] = (cache.k_pool.cpu(), cache.v_pool.cpu())
-    for a, b in zip(outs["serial"], outs["live"]):
-        assert torch.equal(a, b)
-    assert torch.equal(pools["serial"][0], pools["live"][0])
-    assert torch.equal(pools["serial"][1], pools["live"][1])
+    for mode in ("live", "live_planned"):
+        for a, b in zip(outs["serial"], outs[mode]):
+            assert torch.equal(a, b)
+        assert torch.equal(pools["serial"][0], pools[mode][0])
+        assert torch.equal(pools["serial"][1], pools[mode][1])
+    assert native_counts == counts
     assert all(g > 0 for _, g in counts)
     if fork:
         assert counts[0][0] == 9 and all(p == 0 for p, _ in counts[1:])
