@@ -596,9 +596,10 @@ class LiveDecodePipeline(StepPipeline):
     tables and lengths and finds the prefix groups -- straight into the next
     pinned slab (no array is allocated on the way), then uploads that slab with
     the step's q, k_new and v_new (written by the caller into
-    ``host_inputs()``, or left from an earlier step), runs the step's bound
-    launches with that step's counts (pairs, groups) and reads the output back.
-    The slab's plan buffers are sized for the most a step can raise (a pair and
+    ``host_inputs()``, or left from an earlier step), runs the step's launches
+    with that step's counts (pairs, groups) and reads the output back -- one
+    library call (``pkv_decode_pipeline_step``) for all of it. The slab's plan
+    buffers are sized for the most a step can raise (a pair and
     a group row per sequence). Planning ahead of the device work is what the
     pages' lazy allocation asks of the host every step ("Cách phân trang hoạt
     động" of the "PagedAttention" glossary)."""
