@@ -103,6 +103,7 @@ struct Params {
     const int32_t* seq_list;       // regular launch over these batch indices (null: all)
     const int32_t* group_members;  // [num_groups][max_members] batch indices, -1 padded
     const int32_t* group_prefix;   // [num_groups] shared full blocks of the group
+    int num_groups;
     int max_members;
     int group_part_blocks;         // partition size of the group launch
     int group_parts;               // partitions the group launch has (its grid x)
@@ -974,6 +975,10 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const Params p, int B
     const int b = row / p.num_heads, h = row % p.num_heads;
     int nparts;
     const int g = p.seq_group ? p.seq_group[b] : -1;
+    if (g >= p.num_groups) {                               // not a group of this call
+        if (h == 0 && lane == 0) flag_error(p.err, kErrOutOfRange);
+        return;
+    }
     if (g >= 0) {                                          // as the group CTA counts its list
         int P = max(p.group_prefix[g], 0), n = 0, sum = 0;
         for (int m = 0; m < p.max_members && m < kMaxMembers; ++m) {
@@ -1235,7 +1240,7 @@ int launch_variant(const Args& a) {
     }
     const int slots = gparts > parts ? gparts : parts;
 
-    Params p;
+    Params p{};
     p.out = a.out;
     p.q = a.q;
     p.k_pool = static_cast<const char*>(a.k_pool);
@@ -1256,6 +1261,7 @@ int launch_variant(const Args& a) {
     p.seq_list = nullptr;
     p.group_members = grouped ? a.group_members : nullptr;
     p.group_prefix = grouped ? a.group_prefix : nullptr;
+    p.num_groups = grouped ? a.num_groups : 0;
     p.max_members = grouped ? a.max_members : 0;
     p.group_part_blocks = gPB;
     p.group_parts = gparts;

@@ -473,6 +473,30 @@ def test_grouped_decode_long_lists_are_split_and_merged():
     assert_close(g["out"].numpy(), o["out"], "bf16", "grouped, split lists")
 
 
+def test_grouped_decode_bad_group_index_is_flagged_not_followed():
+    """A seq_group entry naming no group of the call (>= num_groups) on a call
+    whose group lists are split and merged: the merge's bounds check flags it
+    (PKV_ERR_OUT_OF_RANGE) instead of reading past the group arrays; the context
+    stays usable and the same call with the right groups is clean again."""
+    w = wl.shared_prefix(groups=3, per_group=4, prompt=2000, max_suffix=1500, Hq=8, Hkv=8,
+                         seed=77)
+    inp = Inputs(w)
+    g = run_gpu(inp)
+    assert g["err"] == 0 and g["plan"].num_groups == 3
+    cache, dev = g["cache"], g["plan"].device_tensors("cuda")
+    ws = cache.workspace(w.B, w.max_blocks_per_seq)
+    q = inp.q.cuda()
+    out = torch.empty(w.B, w.Hq, w.D, dtype=w.src_dtype, device="cuda")
+    bad = dev["seq_group"].clone()
+    bad[0] = 1000
+    for sg, want in ((bad, -4), (dev["seq_group"], 0)):
+        pkv.paged_attention_decode_grouped(
+            out, q, cache.k_pool, cache.v_pool, dev["tables"], dev["lens"], w.scale, sg,
+            dev["group_members"], dev["group_prefix"], 1.0, 1.0, ws, None, dev["ungrouped"],
+            dev["max_group_blocks"])
+        assert pkv.get_device_error() == want
+
+
 def test_reshape_and_cache_large_batch_runs_and_ragged_slots():
     """A batch large enough for the grouped slot write (>= 512 tokens): aligned
     runs of 8 consecutive slots (written as whole core matrices), runs that start
