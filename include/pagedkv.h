@@ -326,9 +326,11 @@ PKV_API int copy_blocks(void* k_pool, void* v_pool, const int64_t* src_dst_pairs
  *   stream        cudaStream_t
  * Supported: head_dim 128, block_size in {16,32}, G dividing 128. Runs on the
  * tcgen05 tensor cores (one 128-row query tile per CTA); allocates nothing.
- * A sequence with C > L or L beyond its table, or a table entry outside
- * [0, num_blocks), sets PKV_ERR_OUT_OF_RANGE in the device error word (the
- * sequence's rows are left unwritten, or the block's keys get zero values).
+ * A sequence with C > L or L beyond its table, with rows outside
+ * [0, query_start[num_seqs]) (offsets that are not non-decreasing), or a table
+ * entry outside [0, num_blocks), sets PKV_ERR_OUT_OF_RANGE in the device error
+ * word (the sequence's rows are left unwritten, or the block's keys get zero
+ * values). query_start[num_seqs] itself must be the row count of q and out.
  * ---------------------------------------------------------------------- */
 PKV_API int paged_attention_prefill(void* out, const void* q,
                             const void* k_pool, const void* v_pool,

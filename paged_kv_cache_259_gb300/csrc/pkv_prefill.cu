@@ -206,8 +206,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) paged_prefill_kernel(con
     }
     const int L = p.seq_lens[b];
     const int q0 = p.query_start[b];
-    const int C = p.query_start[b + 1] - q0;
-    if (C < 0 || C > L || L > p.max_blocks * BS) {
+    const int q1 = p.query_start[b + 1];
+    const int T = p.query_start[gridDim.z];                // rows of q and out
+    const int C = q1 - q0;
+    // the chunk's rows must lie inside q and out, and inside the sequence
+    if (C < 0 || C > L || L > p.max_blocks * BS || q0 < 0 || q1 > T) {
         if (tid == 0 && C != 0) flag_error(p.err, kErrOutOfRange);
         return;
     }

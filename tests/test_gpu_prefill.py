@@ -186,6 +186,25 @@ def test_prefill_chunk_longer_than_sequence_is_flagged():
     assert_close(g["out"][5:].numpy(), o["out"][5:], "bf16", "unaffected sequence")
 
 
+def test_prefill_rows_outside_the_output_are_flagged_not_followed():
+    """query_start entries that put a chunk past query_start[num_seqs] (the rows
+    of q and out) or out of order: every affected sequence is flagged
+    (PKV_ERR_OUT_OF_RANGE) and left unwritten -- nothing is read or written past
+    the buffers -- and the same step with the right offsets is clean."""
+    w = wl.chunked_prefill("prefill_bad_rows", 15, [500, 300], [10, 20], 8, 8, 128, 16)
+    c = Case(w)
+
+    def corrupt(dev):
+        dev["query_start"][1] = w.T + 10        # chunk 0 would run past the 30 rows
+    g = run_gpu(c, bad=corrupt)
+    assert g["err"] == -4
+    assert torch.isnan(g["out"]).all()          # sequence 1's offsets are out of order too
+    g = run_gpu(c)
+    assert g["err"] == 0
+    o = run_oracle(c)
+    assert_close(g["out"].numpy(), o["out"], "bf16", "the same step, right offsets")
+
+
 def sample_rows(w, n, seed=0):
     rng = np.random.default_rng(seed)
     qs = w.query_start
